@@ -1,0 +1,173 @@
+"""CPU oracle for the GQA decode step (float64 loops, plain C).
+
+TEST INFRASTRUCTURE. Only the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline / reference leg may import this package. The CUDA
+library shares no code with it and never calls it.
+
+The arithmetic lives in ``gqa_oracle.c`` (see its header for the definition
+and the passages it follows). This module only builds that file with gcc,
+marshals numpy arrays to it and returns float64 outputs.
+
+bfloat16 data is passed as ``numpy.uint16`` arrays holding the raw bits (the
+upper half of an IEEE binary32); float32 data as ``numpy.float32``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gqa_oracle.c")
+_LIB = os.path.join(_HERE, "libgqa_oracle.so")
+
+F32, BF16 = 0, 1
+OK, INVALID_ARGUMENT = 0, 1
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``libgqa_oracle.so`` beside its source."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+             "-Wall", "-Wextra", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            # GQA_ORACLE_LIB lets the mutation tests load a deliberately
+            # broken copy of the oracle to prove the pins catch it.
+            lib = ctypes.CDLL(os.environ.get("GQA_ORACLE_LIB") or build())
+            P, I = ctypes.c_void_p, ctypes.c_int
+            lib.orc_decode_dense.argtypes = [I, P, P, P, P, P, P, P, I, I, I, I, I, I,
+                                             P, I, I, P, I, P]
+            lib.orc_decode_dense.restype = I
+            lib.orc_decode_paged.argtypes = [I, P, P, P, P, P, P, P, I, I, I, I, I, I, I,
+                                             P, I, I, P, I, P]
+            lib.orc_decode_paged.restype = I
+            lib.orc_validate_dense.argtypes = [P, P, I, I, I]
+            lib.orc_validate_dense.restype = I
+            lib.orc_validate_paged.argtypes = [P, P, I, I, I, I]
+            lib.orc_validate_paged.restype = I
+            lib.orc_default_threads.argtypes = []
+            lib.orc_default_threads.restype = I
+            _lib = lib
+    return _lib
+
+
+def default_threads() -> int:
+    return _load().orc_default_threads()
+
+
+def _dtype_code(a: np.ndarray) -> int:
+    if a.dtype == np.float32:
+        return F32
+    if a.dtype == np.uint16:
+        return BF16
+    raise TypeError(f"oracle takes float32 or uint16 (bfloat16 bits), not {a.dtype}")
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def _c(a, dtype=None):
+    if a is None:
+        return None
+    a = np.ascontiguousarray(a if dtype is None else a.astype(dtype, copy=False))
+    return a
+
+
+class OracleResult:
+    def __init__(self, status, out, threads):
+        self.status = status
+        self.out = out
+        self.threads = threads
+
+
+def decode_dense(q, k_new, v_new, k_cache, v_cache, lengths, slot_ids=None, *,
+                 rows=None, append=True, threads=None) -> OracleResult:
+    """One decode step on a dense (R, Hkv, Smax, D) cache, in place.
+
+    ``q`` (B, Hq, D); ``k_new``/``v_new`` (B, Hkv, D); ``lengths`` (B,) int32;
+    ``slot_ids`` (B,) int32 or None. With ``append`` the caches (numpy arrays,
+    modified in place) receive the new key/value at slot ``lengths[b]``.
+    ``rows`` restricts the work to those batch rows (others stay NaN in out).
+    Returns an OracleResult with ``out`` (B, Hq, D) float64.
+    """
+    dt = _dtype_code(q)
+    for a in (k_new, v_new, k_cache, v_cache):
+        if a.dtype != q.dtype:
+            raise TypeError("q, k_new, v_new and the caches share one dtype")
+        if not a.flags.c_contiguous:
+            raise ValueError("arrays must be C-contiguous (the caches are written in place)")
+    B, Hq, D = q.shape
+    R, Hkv, Smax, D2 = k_cache.shape
+    assert D2 == D and v_cache.shape == k_cache.shape and k_new.shape == (B, Hkv, D)
+    q, k_new, v_new = _c(q), _c(k_new), _c(v_new)
+    lengths = _c(lengths, np.int32)
+    slot_ids = _c(slot_ids, np.int32)
+    rows_a = None if rows is None else _c(np.asarray(rows), np.int32)
+    out = np.full((B, Hq, D), np.nan, dtype=np.float64)
+    used = ctypes.c_int(0)
+    nthr = default_threads() if threads is None else int(threads)
+    st = _load().orc_decode_dense(dt, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
+                                  _ptr(v_cache), _ptr(lengths), _ptr(slot_ids),
+                                  B, Hq, Hkv, D, R, Smax, _ptr(rows_a),
+                                  0 if rows_a is None else len(rows_a), int(bool(append)),
+                                  _ptr(out), nthr, ctypes.addressof(used))
+    return OracleResult(st, out, used.value)
+
+
+def decode_paged(q, k_new, v_new, k_blocks, v_blocks, block_table, lengths, *,
+                 rows=None, append=True, threads=None) -> OracleResult:
+    """One decode step on a paged cache (num_blocks, Hkv, block_size, D) with a
+    (B, max_blocks) int32 block table (-1 = unused). Same contract as
+    :func:`decode_dense` otherwise."""
+    dt = _dtype_code(q)
+    for a in (k_new, v_new, k_blocks, v_blocks):
+        if a.dtype != q.dtype:
+            raise TypeError("q, k_new, v_new and the blocks share one dtype")
+        if not a.flags.c_contiguous:
+            raise ValueError("arrays must be C-contiguous (the blocks are written in place)")
+    B, Hq, D = q.shape
+    NB, Hkv, BS, D2 = k_blocks.shape
+    assert D2 == D and v_blocks.shape == k_blocks.shape and k_new.shape == (B, Hkv, D)
+    MB = block_table.shape[1]
+    q, k_new, v_new = _c(q), _c(k_new), _c(v_new)
+    block_table = _c(block_table, np.int32)
+    lengths = _c(lengths, np.int32)
+    rows_a = None if rows is None else _c(np.asarray(rows), np.int32)
+    out = np.full((B, Hq, D), np.nan, dtype=np.float64)
+    used = ctypes.c_int(0)
+    nthr = default_threads() if threads is None else int(threads)
+    st = _load().orc_decode_paged(dt, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_blocks),
+                                  _ptr(v_blocks), _ptr(block_table), _ptr(lengths),
+                                  B, Hq, Hkv, D, NB, BS, MB, _ptr(rows_a),
+                                  0 if rows_a is None else len(rows_a), int(bool(append)),
+                                  _ptr(out), nthr, ctypes.addressof(used))
+    return OracleResult(st, out, used.value)
+
+
+def validate_dense(lengths, slot_ids, R, Smax) -> int:
+    lengths = _c(lengths, np.int32)
+    slot_ids = _c(slot_ids, np.int32)
+    return _load().orc_validate_dense(_ptr(lengths), _ptr(slot_ids), len(lengths), R, Smax)
+
+
+def validate_paged(lengths, block_table, num_blocks, block_size) -> int:
+    lengths = _c(lengths, np.int32)
+    block_table = _c(block_table, np.int32)
+    return _load().orc_validate_paged(_ptr(lengths), _ptr(block_table), len(lengths),
+                                      num_blocks, block_size, block_table.shape[1])

@@ -1,0 +1,347 @@
+/*
+ * GQA decode-step oracle: plain float64 loops on the CPU.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing on the product path may link, load or
+ * call this file; only the tests, the smoke check and the benchmark's CPU
+ * baseline do. It shares no code with the CUDA library.
+ *
+ * What it computes, for every batch row b (all of it written out, no blocking,
+ * fusion or reordering):
+ *
+ *   r   = slot_ids[b] if slot_ids are given, else b           (cache row)
+ *   L   = lengths[b]                                         (append slot)
+ *   cache[r][kvh][L] = k_new[b][kvh], v_new[b][kvh]          (bit copy, in place)
+ *   for each query head h, with G = Hq / Hkv and kvh = floor(h / G):
+ *     s_j = (q[b][h] . K[r][kvh][j]) / sqrt(D)        for j = 0 .. L
+ *     m   = max_j s_j
+ *     w_j = exp(s_j - m) / sum_i exp(s_i - m)
+ *     o   = sum_j w_j V[r][kvh][j]
+ *
+ * Sources (web pages, by title and part):
+ *  - "KV cache decode step" (tensortonic cs336-l10), problem statement: the new
+ *    key and value take position S after the S cached positions, each KV head
+ *    serves a contiguous group of G = Hq/Hkv query heads, and the softmax runs
+ *    over every position including the new token, with the 1/sqrt(D) scale.
+ *  - "Grouped-Query Decode Step" (tensortonic, JAX), statement and formula:
+ *    query head h reads cache head floor(h/G); only the slots below the row's
+ *    length get weight, stale slots get exactly zero; s_j = q.K_j/sqrt(D),
+ *    w_j = e^{s_j} / sum e^{s_m}, o = sum w_j V_j; computed in float32 from
+ *    bfloat16 caches (Requirements), here in float64.
+ *  - "groupQueryAttention" (clika runtime), description: the in-place append,
+ *    slot_ids as a row map on a [max_seqs, Hkv, max_seq, D] cache (entries in
+ *    [0, max_seqs), no two rows sharing one), and the paged block table
+ *    ([B, max_blocks], entries -1 or in [0, num_blocks), no repeats within a
+ *    row, validated whole before any read, INVALID_ARGUMENT otherwise).
+ *
+ * Readings where the pages are silent (each listed in the design notes):
+ *  - lengths[b] is the append slot (the number of tokens already cached), and
+ *    slots 0 .. lengths[b] inclusive are attended: the first page's S per row.
+ *  - dense: 0 <= lengths[b] <= Smax - 1. paged: 0 <= lengths[b] and
+ *    lengths[b] < max_blocks * block_size, and the table entries covering
+ *    slots 0 .. lengths[b] are not -1.
+ *  - subtracting the maximum before exp is the textbook rearrangement of the
+ *    same quotient; it changes no value beyond rounding.
+ *  - bfloat16 values are the upper 16 bits of an IEEE binary32; widening them
+ *    to double is exact.
+ */
+#define _GNU_SOURCE
+#include <math.h>
+#include <sched.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+enum { ORC_F32 = 0, ORC_BF16 = 1 };
+enum { ORC_OK = 0, ORC_INVALID_ARGUMENT = 1 };
+
+/* One element of a float32 or bfloat16 array, widened exactly to double. */
+static double elem(const void *base, size_t i, int dtype)
+{
+    if (dtype == ORC_F32) {
+        return (double)((const float *)base)[i];
+    }
+    uint32_t bits = (uint32_t)((const uint16_t *)base)[i] << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+static size_t esize(int dtype) { return dtype == ORC_F32 ? 4 : 2; }
+
+static void copy_vec(void *dst, size_t dst_i, const void *src, size_t src_i, int D, int dtype)
+{
+    size_t es = esize(dtype);
+    memcpy((char *)dst + dst_i * es, (const char *)src + src_i * es, (size_t)D * es);
+}
+
+/* ---------------------------------------------------------------- checks -- */
+
+/* Dense / slot_ids form: every length in [0, Smax-1]; slot_ids in [0, R) and
+ * pairwise distinct; without slot_ids the cache must hold a row per batch row. */
+int orc_validate_dense(const int32_t *lengths, const int32_t *slot_ids, int B, int R, int Smax)
+{
+    if (B < 0 || R < 0 || Smax < 1)
+        return ORC_INVALID_ARGUMENT;
+    for (int b = 0; b < B; ++b)
+        if (lengths[b] < 0 || lengths[b] > Smax - 1)
+            return ORC_INVALID_ARGUMENT;
+    if (!slot_ids)
+        return B <= R ? ORC_OK : ORC_INVALID_ARGUMENT;
+    for (int b = 0; b < B; ++b) {
+        if (slot_ids[b] < 0 || slot_ids[b] >= R)
+            return ORC_INVALID_ARGUMENT;
+        for (int c = 0; c < b; ++c)
+            if (slot_ids[c] == slot_ids[b])
+                return ORC_INVALID_ARGUMENT;
+    }
+    return ORC_OK;
+}
+
+/* Paged form: every table entry is -1 or in [0, num_blocks); no block repeats
+ * within a row; each length fits the table and the entries that hold slots
+ * 0 .. lengths[b] are real blocks. */
+int orc_validate_paged(const int32_t *lengths, const int32_t *block_table, int B,
+                       int num_blocks, int block_size, int max_blocks)
+{
+    if (B < 0 || num_blocks < 1 || block_size < 1 || max_blocks < 1)
+        return ORC_INVALID_ARGUMENT;
+    for (int b = 0; b < B; ++b) {
+        const int32_t *row = block_table + (size_t)b * max_blocks;
+        for (int i = 0; i < max_blocks; ++i) {
+            if (row[i] == -1)
+                continue;
+            if (row[i] < 0 || row[i] >= num_blocks)
+                return ORC_INVALID_ARGUMENT;
+            for (int k = 0; k < i; ++k)
+                if (row[k] == row[i])
+                    return ORC_INVALID_ARGUMENT;
+        }
+        long long L = lengths[b];
+        if (L < 0 || L >= (long long)max_blocks * block_size)
+            return ORC_INVALID_ARGUMENT;
+        for (long long i = 0; i <= L / block_size; ++i)
+            if (row[i] == -1)
+                return ORC_INVALID_ARGUMENT;
+    }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------ addressing -- */
+
+/* Where slot s of cache head kvh of batch row b lives, as an element index of
+ * the first of its D values. */
+typedef struct {
+    int paged;
+    /* dense */
+    const int32_t *slot_ids;
+    int Hkv, D, Smax;
+    /* paged */
+    const int32_t *block_table;
+    int block_size, max_blocks;
+} layout;
+
+static size_t slot_index(const layout *lay, int b, int kvh, int s)
+{
+    if (!lay->paged) {
+        size_t r = lay->slot_ids ? (size_t)lay->slot_ids[b] : (size_t)b;
+        return ((r * lay->Hkv + kvh) * lay->Smax + s) * lay->D;
+    }
+    size_t blk = (size_t)lay->block_table[(size_t)b * lay->max_blocks + s / lay->block_size];
+    return ((blk * lay->Hkv + kvh) * lay->block_size + (size_t)(s % lay->block_size)) * lay->D;
+}
+
+/* ----------------------------------------------------------------- step -- */
+
+typedef struct {
+    int dtype;
+    const void *q, *k_new, *v_new;
+    void *k_cache, *v_cache;
+    const int32_t *lengths;
+    layout lay;
+    int B, Hq, Hkv, D;
+    int do_append;
+    double *out;       /* (B, Hq, D) */
+    const int32_t *rows; /* batch rows to compute */
+    int nrows;
+    /* work distribution over (row, kvh) pairs */
+    int next;
+    pthread_mutex_t mu;
+} job;
+
+/* One (batch row, cache head) pair: append, then the G query heads. */
+static void one_pair(job *J, int b, int kvh)
+{
+    const int D = J->D, G = J->Hq / J->Hkv;
+    const int L = J->lengths[b];
+    const size_t new_i = ((size_t)b * J->Hkv + kvh) * D;
+
+    if (J->do_append) {
+        size_t dst = slot_index(&J->lay, b, kvh, L);
+        copy_vec(J->k_cache, dst, J->k_new, new_i, D, J->dtype);
+        copy_vec(J->v_cache, dst, J->v_new, new_i, D, J->dtype);
+    }
+
+    double *s = (double *)malloc(sizeof(double) * (size_t)(L + 1));
+    for (int g = 0; g < G; ++g) {
+        const int h = kvh * G + g;           /* floor(h / G) == kvh */
+        const size_t q_i = ((size_t)b * J->Hq + h) * D;
+
+        /* scores over slots 0 .. L; slot L is the new token */
+        for (int j = 0; j <= L; ++j) {
+            double dot = 0.0;
+            for (int d = 0; d < D; ++d) {
+                double kd = (j == L && !J->do_append)
+                                ? elem(J->k_new, new_i + d, J->dtype)
+                                : elem(J->k_cache, slot_index(&J->lay, b, kvh, j) + d, J->dtype);
+                dot += elem(J->q, q_i + d, J->dtype) * kd;
+            }
+            s[j] = dot / sqrt((double)D);
+        }
+
+        /* softmax over the valid slots only */
+        double m = s[0];
+        for (int j = 1; j <= L; ++j)
+            if (s[j] > m)
+                m = s[j];
+        double Z = 0.0;
+        for (int j = 0; j <= L; ++j)
+            Z += exp(s[j] - m);
+
+        /* weighted sum of values */
+        double *o = J->out + q_i;
+        for (int d = 0; d < D; ++d)
+            o[d] = 0.0;
+        for (int j = 0; j <= L; ++j) {
+            double w = exp(s[j] - m) / Z;
+            for (int d = 0; d < D; ++d) {
+                double vd = (j == L && !J->do_append)
+                                ? elem(J->v_new, new_i + d, J->dtype)
+                                : elem(J->v_cache, slot_index(&J->lay, b, kvh, j) + d, J->dtype);
+                o[d] += w * vd;
+            }
+        }
+    }
+    free(s);
+}
+
+static void *worker(void *arg)
+{
+    job *J = (job *)arg;
+    const int total = J->nrows * J->Hkv;
+    for (;;) {
+        pthread_mutex_lock(&J->mu);
+        int t = J->next++;
+        pthread_mutex_unlock(&J->mu);
+        if (t >= total)
+            break;
+        one_pair(J, J->rows[t / J->Hkv], t % J->Hkv);
+    }
+    return NULL;
+}
+
+static int run(job *J, int nthreads)
+{
+    int *all = NULL;
+    if (!J->rows) {
+        all = (int *)malloc(sizeof(int) * (size_t)(J->B > 0 ? J->B : 1));
+        for (int b = 0; b < J->B; ++b)
+            all[b] = b;
+        J->rows = all;
+        J->nrows = J->B;
+    }
+    if (nthreads < 1)
+        nthreads = 1;
+    J->next = 0;
+    pthread_mutex_init(&J->mu, NULL);
+    pthread_t *tid = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    for (int i = 0; i < nthreads; ++i)
+        pthread_create(&tid[i], NULL, worker, J);
+    for (int i = 0; i < nthreads; ++i)
+        pthread_join(tid[i], NULL);
+    free(tid);
+    pthread_mutex_destroy(&J->mu);
+    free(all);
+    return nthreads;
+}
+
+static int usable_shape(int B, int Hq, int Hkv, int D)
+{
+    return B >= 0 && Hq >= 1 && Hkv >= 1 && D >= 1 && Hq % Hkv == 0;
+}
+
+/* Dense or slot_ids cache (R, Hkv, Smax, D). rows/nrows pick the batch rows to
+ * compute (NULL: all); out rows that are not picked are left untouched.
+ * do_append = 0 computes the same output without writing the cache (slot L
+ * then reads k_new / v_new, which is what the append would have put there).
+ * Returns ORC_OK or ORC_INVALID_ARGUMENT; *threads_used gets the thread count. */
+int orc_decode_dense(int dtype, const void *q, const void *k_new, const void *v_new,
+                     void *k_cache, void *v_cache, const int32_t *lengths, const int32_t *slot_ids,
+                     int B, int Hq, int Hkv, int D, int R, int Smax,
+                     const int32_t *rows, int nrows, int do_append, double *out,
+                     int nthreads, int *threads_used)
+{
+    if (!usable_shape(B, Hq, Hkv, D) || (dtype != ORC_F32 && dtype != ORC_BF16))
+        return ORC_INVALID_ARGUMENT;
+    if (orc_validate_dense(lengths, slot_ids, B, R, Smax) != ORC_OK)
+        return ORC_INVALID_ARGUMENT;
+    job J;
+    memset(&J, 0, sizeof J);
+    J.dtype = dtype;
+    J.q = q; J.k_new = k_new; J.v_new = v_new;
+    J.k_cache = k_cache; J.v_cache = v_cache;
+    J.lengths = lengths;
+    J.lay.paged = 0; J.lay.slot_ids = slot_ids;
+    J.lay.Hkv = Hkv; J.lay.D = D; J.lay.Smax = Smax;
+    J.B = B; J.Hq = Hq; J.Hkv = Hkv; J.D = D;
+    J.do_append = do_append;
+    J.out = out;
+    J.rows = (const int32_t *)rows; J.nrows = nrows;
+    int n = run(&J, nthreads);
+    if (threads_used)
+        *threads_used = n;
+    return ORC_OK;
+}
+
+/* Paged cache: blocks (num_blocks, Hkv, block_size, D), block table
+ * (B, max_blocks). Same contract as orc_decode_dense otherwise. */
+int orc_decode_paged(int dtype, const void *q, const void *k_new, const void *v_new,
+                     void *k_blocks, void *v_blocks, const int32_t *block_table,
+                     const int32_t *lengths, int B, int Hq, int Hkv, int D,
+                     int num_blocks, int block_size, int max_blocks,
+                     const int32_t *rows, int nrows, int do_append, double *out,
+                     int nthreads, int *threads_used)
+{
+    if (!usable_shape(B, Hq, Hkv, D) || (dtype != ORC_F32 && dtype != ORC_BF16))
+        return ORC_INVALID_ARGUMENT;
+    if (orc_validate_paged(lengths, block_table, B, num_blocks, block_size, max_blocks) != ORC_OK)
+        return ORC_INVALID_ARGUMENT;
+    job J;
+    memset(&J, 0, sizeof J);
+    J.dtype = dtype;
+    J.q = q; J.k_new = k_new; J.v_new = v_new;
+    J.k_cache = k_blocks; J.v_cache = v_blocks;
+    J.lengths = lengths;
+    J.lay.paged = 1; J.lay.block_table = block_table;
+    J.lay.Hkv = Hkv; J.lay.D = D;
+    J.lay.block_size = block_size; J.lay.max_blocks = max_blocks;
+    J.B = B; J.Hq = Hq; J.Hkv = Hkv; J.D = D;
+    J.do_append = do_append;
+    J.out = out;
+    J.rows = (const int32_t *)rows; J.nrows = nrows;
+    int n = run(&J, nthreads);
+    if (threads_used)
+        *threads_used = n;
+    return ORC_OK;
+}
+
+/* Cores this process may run on (the default thread count). */
+int orc_default_threads(void)
+{
+    cpu_set_t set;
+    if (sched_getaffinity(0, sizeof set, &set) == 0 && CPU_COUNT(&set) > 0)
+        return CPU_COUNT(&set);
+    long n = sysconf(_SC_NPROCESSORS_ONLN);
+    return n > 0 ? (int)n : 1;
+}

@@ -1,0 +1,52 @@
+"""The pins must catch plausible mistakes in the oracle.
+
+Each case copies the oracle's C source, plants one mistake (a dropped term, a
+wrong index or sign, a transposed operand, a skipped step), compiles the copy
+into a temporary directory and runs the pin tests against it in a child
+process. The pins pass on the real oracle and must fail on every mutant.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "gqa_oracle.c")
+
+MUTANTS = {
+    "strided_groups": ("const int h = kvh * G + g;", "const int h = g * J->Hkv + kvh;"),
+    "no_scale": ("s[j] = dot / sqrt((double)D);", "s[j] = dot;"),
+    "scale_by_d": ("s[j] = dot / sqrt((double)D);", "s[j] = dot / (double)D;"),
+    "new_token_dropped": ("        for (int j = 0; j <= L; ++j) {\n            double dot",
+                          "        for (int j = 0; j < L; ++j) {\n            double dot"),
+    "stale_slot_counted": ("        for (int j = 0; j <= L; ++j)\n            Z += exp(s[j] - m);",
+                           "        for (int j = 0; j <= L + 1 && j < 2 * L + 1; ++j)\n            Z += exp(s[j < L + 1 ? j : L] - m);"),
+    "sign_flip": ("Z += exp(s[j] - m);", "Z += exp(m - s[j]);"),
+    "row_head_swapped": ("return ((r * lay->Hkv + kvh) * lay->Smax + s) * lay->D;",
+                         "return ((kvh * lay->Hkv + r % lay->Hkv) * lay->Smax + s) * lay->D;"),
+    "paged_offset": ("(size_t)(s % lay->block_size)) * lay->D;", "(size_t)(s / lay->block_size)) * lay->D;"),
+    "append_skipped": ("    if (J->do_append) {\n        size_t dst", "    if (0) {\n        size_t dst"),
+    "slot_ids_ignored": ("size_t r = lay->slot_ids ? (size_t)lay->slot_ids[b] : (size_t)b;", "size_t r = (size_t)b;"),
+    "duplicates_accepted": ("if (slot_ids[c] == slot_ids[b])", "if (0)"),
+    "paged_repeat_accepted": ("if (row[k] == row[i])", "if (0)"),
+    "bf16_shift": ("[i] << 16;", "[i] << 15;"),
+    "query_head_offset": ("const size_t q_i = ((size_t)b * J->Hq + h) * D;", "const size_t q_i = ((size_t)b * J->Hq + g) * D;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, tmp_path):
+    before, after = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(before) == 1, f"mutation site for {name} not found exactly once"
+    mut = tmp_path / "mutant.c"
+    mut.write_text(src.replace(before, after))
+    lib = tmp_path / "libmutant.so"
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+                           "-o", str(lib), str(mut), "-lm"])
+    env = dict(os.environ, GQA_ORACLE_LIB=str(lib))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"mutant {name} passed every pin:\n{r.stdout[-2000:]}"

@@ -1,0 +1,473 @@
+"""Pins for the CPU oracle: values the pages print, closed forms, invariants,
+library special cases and brute force. None of these re-types the oracle's
+own formula; each checks it against something fixed outside it.
+
+Pages:
+  [P1] tensortonic "KV cache decode step" (cs336-l10): statement, Examples 1-3.
+  [P2] tensortonic "Grouped-Query Decode Step" (JAX): statement, formula,
+       Examples 1-3, Hints 1-3, Requirements, Constraints.
+  [P5] clika runtime "groupQueryAttention": slot_ids and block-table rules.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from helpers import to_np, oracle_inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# --------------------------------------------------------------- page values
+
+@pytest.mark.parametrize("ex", _golden("kv_cache_decode_step_examples.json")["examples"],
+                         ids=lambda e: e["name"])
+def test_p1_examples(ex):
+    """[P1] Examples 1-3: output and both extended caches. The page's cache
+    holds S positions and the new token goes to position S, so our cache has
+    S+1 slots and lengths = S."""
+    f = lambda x: np.asarray(x, dtype=np.float32)
+    q, kn, vn = f(ex["query"]), f(ex["new_key"]), f(ex["new_value"])
+    kc0, vc0 = f(ex["key_cache"]), f(ex["value_cache"])
+    B, Hkv, S, D = kc0.shape
+    assert q.shape[1] == ex["num_query_heads"] and Hkv == ex["num_kv_heads"]
+    kc = np.zeros((B, Hkv, S + 1, D), np.float32)
+    vc = np.zeros_like(kc)
+    kc[:, :, :S], vc[:, :, :S] = kc0, vc0
+    r = oracle.decode_dense(q, kn, vn, kc, vc, np.full(B, S, np.int32))
+    assert r.status == oracle.OK
+    np.testing.assert_allclose(r.out, ex["output"], rtol=0, atol=5e-7)
+    np.testing.assert_allclose(kc, ex["new_key_cache"], rtol=0, atol=5e-7)
+    np.testing.assert_allclose(vc, ex["new_value_cache"], rtol=0, atol=5e-7)
+    # the appended slot holds exactly the new key's bits
+    assert kc[:, :, S].tobytes() == kn.tobytes() and vc[:, :, S].tobytes() == vn.tobytes()
+
+
+@pytest.mark.parametrize("ex", _golden("grouped_query_decode_step_examples.json")["examples"],
+                         ids=lambda e: e["name"])
+def test_p2_examples(ex):
+    """[P2] Examples 1-3. The page's cache is slot-major (B,S,Hkv,D) and its
+    lengths count the new token, which is already stored. Mapped here: the
+    cache is transposed to (B,Hkv,S,D), our append slot is lengths-1 and the
+    new key/value are that slot's contents, so the append rewrites the same
+    bits and the output must be the page's."""
+    q = np.asarray(ex["query"], np.float32)
+    kc = np.ascontiguousarray(np.asarray(ex["key_cache"], np.float32).transpose(0, 2, 1, 3))
+    vc = np.ascontiguousarray(np.asarray(ex["value_cache"], np.float32).transpose(0, 2, 1, 3))
+    lens = np.asarray(ex["lengths"], np.int32)
+    B = q.shape[0]
+    kn = np.stack([kc[b, :, lens[b] - 1] for b in range(B)])
+    vn = np.stack([vc[b, :, lens[b] - 1] for b in range(B)])
+    before_k, before_v = kc.copy(), vc.copy()
+    r = oracle.decode_dense(q, kn, vn, kc, vc, lens - 1)
+    assert r.status == oracle.OK
+    np.testing.assert_allclose(r.out, ex["output"], rtol=0, atol=5e-7)
+    assert kc.tobytes() == before_k.tobytes() and vc.tobytes() == before_v.tobytes()
+
+
+def test_p2_example1_weights():
+    """[P2] Example 1 explanation prints head 0's weights 0.669762/0.330238:
+    with V = identity rows, the output is the weight vector itself."""
+    q = np.array([[[1, 0]]], np.float32)
+    kc = np.array([[[[1, 0], [0, 1], [5, 5]]]], np.float32)
+    vc = np.array([[[[1, 0], [0, 1], [50, 50]]]], np.float32)
+    r = oracle.decode_dense(q, kc[:, :, 1].copy(), vc[:, :, 1].copy(), kc, vc,
+                            np.array([1], np.int32))
+    np.testing.assert_allclose(r.out[0, 0], [0.669762, 0.330238], atol=5e-7)
+
+
+# ---------------------------------------------------------------- bf16 format
+
+def test_bf16_widening_matches_format():
+    """bf16 is the top half of binary32: 0x3F80 = 1, 0xC000 = -2,
+    0x3F81 = 1 + 2^-7, 0x0001 = 2^-133 (subnormal). A one-slot cache returns
+    the new value exactly, so the oracle's widening shows through."""
+    bits = np.array([0x3F80, 0xC000, 0x3F81, 0x0001], np.uint16)
+    want = [1.0, -2.0, 1.0 + 2.0 ** -7, 2.0 ** -133]
+    q = np.zeros((1, 1, 4), np.uint16)
+    k = np.zeros((1, 1, 4), np.uint16)
+    v = bits.reshape(1, 1, 4).copy()
+    kc = np.zeros((1, 1, 1, 4), np.uint16)
+    vc = np.zeros_like(kc)
+    r = oracle.decode_dense(q, k, v, kc, vc, np.array([0], np.int32))
+    assert list(r.out[0, 0]) == want
+
+
+def test_bf16_agrees_with_f32_on_representable_values():
+    """On values exactly representable in bf16, the bf16 and f32 branches of
+    the oracle must give bit-identical float64 outputs."""
+    w = W.small("llama3_8b", B=3, Hq=8, Hkv=2, D=16, Smax=24, len_lo=0, len_hi=23, seed=11)
+    t = W.generate(w)
+    tb = oracle_inputs(t)
+    tf = {k: (to_np(v.float()) if v.dtype == torch.bfloat16 else to_np(v)) for k, v in t.items()}
+    rb = oracle.decode_dense(tb["q"], tb["k_new"], tb["v_new"], tb["k_cache"], tb["v_cache"], tb["lengths"])
+    rf = oracle.decode_dense(tf["q"], tf["k_new"], tf["v_new"], tf["k_cache"], tf["v_cache"], tf["lengths"])
+    assert rb.out.tobytes() == rf.out.tobytes()
+
+
+# --------------------------------------------------------------- brute force
+
+def _brute_force(q, kc, vc, kn, vn, lens, slot_ids=None):
+    """Direct softmax without max subtraction, pure Python, on tiny shapes:
+    w_j = e^{s_j} / sum_m e^{s_m}  ([P2] formula, literally)."""
+    B, Hq, D = q.shape
+    Hkv = kc.shape[1]
+    G = Hq // Hkv
+    out = np.zeros((B, Hq, D))
+    for b in range(B):
+        r = b if slot_ids is None else int(slot_ids[b])
+        L = int(lens[b])
+        for h in range(Hq):
+            g = h // G
+            keys = [[float(x) for x in kc[r, g, j]] for j in range(L)] + [[float(x) for x in kn[b, g]]]
+            vals = [[float(x) for x in vc[r, g, j]] for j in range(L)] + [[float(x) for x in vn[b, g]]]
+            qs = [float(x) for x in q[b, h]]
+            e = [math.exp(sum(a * c for a, c in zip(qs, k)) / math.sqrt(D)) for k in keys]
+            z = sum(e)
+            for d in range(D):
+                out[b, h, d] = sum(e[j] * vals[j][d] for j in range(L + 1)) / z
+    return out
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_brute_force_tiny(seed):
+    """Random tiny cases within the [P2] Constraints (B 1-3, S 3-8, Hq 2-8,
+    D 2-4, Hkv | Hq, lengths in range, stale slots much larger)."""
+    rng = np.random.default_rng(seed)
+    B, S, D = rng.integers(1, 4), rng.integers(3, 9), rng.integers(2, 5)
+    Hq = int(rng.choice([2, 3, 4, 6, 8]))
+    Hkv = int(rng.choice([d for d in range(1, Hq + 1) if Hq % d == 0]))
+    lens = rng.integers(0, S, size=B).astype(np.int32)
+    q = rng.normal(size=(B, Hq, D)).astype(np.float32)
+    kc = (rng.normal(size=(B, Hkv, S, D)) * 50).astype(np.float32)
+    vc = (rng.normal(size=(B, Hkv, S, D)) * 50).astype(np.float32)
+    for b in range(B):
+        kc[b, :, :lens[b]] /= 50
+        vc[b, :, :lens[b]] /= 50
+    kn = rng.normal(size=(B, Hkv, D)).astype(np.float32)
+    vn = rng.normal(size=(B, Hkv, D)).astype(np.float32)
+    want = _brute_force(q, kc, vc, kn, vn, lens)
+    r = oracle.decode_dense(q, kn, vn, kc, vc, lens)
+    np.testing.assert_allclose(r.out, want, rtol=1e-12, atol=1e-12)
+
+
+def test_einsum_mask_formulation():
+    """[P2] Hints 1-3 (reshape by cache head, einsum against a slot-major
+    cache, fixed-shape mask) written in numpy float64, against the oracle."""
+    rng = np.random.default_rng(5)
+    B, S, Hq, Hkv, D = 3, 8, 8, 2, 4
+    G = Hq // Hkv
+    q = rng.normal(size=(B, Hq, D)).astype(np.float32)
+    kc = rng.normal(size=(B, Hkv, S, D)).astype(np.float32)
+    vc = rng.normal(size=(B, Hkv, S, D)).astype(np.float32)
+    lens = np.array([0, 4, 7], np.int32)
+    kn = rng.normal(size=(B, Hkv, D)).astype(np.float32)
+    vn = rng.normal(size=(B, Hkv, D)).astype(np.float32)
+    k_ext, v_ext = kc.astype(np.float64), vc.astype(np.float64)
+    for b in range(B):
+        k_ext[b, :, lens[b]] = kn[b]
+        v_ext[b, :, lens[b]] = vn[b]
+    keys = k_ext.transpose(0, 2, 1, 3)                      # (B,S,Hkv,D)
+    vals = v_ext.transpose(0, 2, 1, 3)
+    qg = q.astype(np.float64).reshape(B, Hkv, G, D)
+    s = np.einsum("bkgd,bskd->bkgs", qg, keys) / np.sqrt(D)
+    mask = np.arange(S)[None, :] < (lens + 1)[:, None]
+    s = np.where(mask[:, None, None, :], s, -np.inf)
+    w = np.exp(s - s.max(-1, keepdims=True))
+    w /= w.sum(-1, keepdims=True)
+    o = np.einsum("bkgs,bskd->bkgd", w, vals).reshape(B, Hq, D)
+    r = oracle.decode_dense(q, kn, vn, kc.copy(), vc.copy(), lens)
+    np.testing.assert_allclose(r.out, o, rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 2), (6, 1)])
+def test_library_sdpa(Hq, Hkv):
+    """torch's scaled_dot_product_attention in float64 on the valid prefix,
+    with each cache head repeated for its G query heads: covers MHA (G=1),
+    GQA and MQA (Hkv=1)."""
+    w = W.small("llama3_8b", dtype="f32", B=3, Hq=Hq, Hkv=Hkv, D=32, Smax=40,
+                len_lo=0, len_hi=39, seed=21)
+    t = W.generate(w)
+    a = oracle_inputs(t)
+    r = oracle.decode_dense(a["q"], a["k_new"], a["v_new"], a["k_cache"], a["v_cache"], a["lengths"])
+    G = Hq // Hkv
+    for b in range(w.B):
+        L = int(t["lengths"][b])
+        k = torch.cat([t["k_cache"][b, :, :L], t["k_new"][b, :, None]], 1).double()
+        v = torch.cat([t["v_cache"][b, :, :L], t["v_new"][b, :, None]], 1).double()
+        k = k.repeat_interleave(G, 0)
+        v = v.repeat_interleave(G, 0)
+        o = torch.nn.functional.scaled_dot_product_attention(
+            t["q"][b][:, None].double(), k, v)[:, 0]
+        np.testing.assert_allclose(r.out[b], o.numpy(), rtol=1e-12, atol=1e-12)
+
+
+# -------------------------------------------------------------- closed forms
+
+def _rand_case(seed, dtype="f32", **kw):
+    base = dict(B=3, Hq=8, Hkv=2, D=16, Smax=32, len_lo=0, len_hi=31, seed=seed)
+    base.update(kw)
+    w = W.small("llama3_8b", dtype=dtype, **base)
+    return w, oracle_inputs(W.generate(w))
+
+
+def test_identical_keys_give_mean_of_values():
+    """[P1] Example 1's explanation, generalised: identical keys -> mean."""
+    w, a = _rand_case(1)
+    a["k_cache"][:] = a["k_cache"][:, :, :1]
+    a["k_new"][:] = a["k_cache"][:, :, 0]
+    r = oracle.decode_dense(a["q"], a["k_new"], a["v_new"], a["k_cache"], a["v_cache"], a["lengths"])
+    for b in range(w.B):
+        L = int(a["lengths"][b])
+        mean = a["v_cache"][b, :, :L + 1].astype(np.float64).mean(1)   # after append
+        np.testing.assert_allclose(r.out[b], np.repeat(mean, w.G, 0), rtol=1e-12, atol=1e-12)
+
+
+def test_zero_query_uniform_weights():
+    """[P1] Example 2 / [P2] Example 3 head 0: equal scores -> uniform."""
+    w, a = _rand_case(2)
+    a["q"][:] = 0
+    r = oracle.decode_dense(a["q"], a["k_new"], a["v_new"], a["k_cache"], a["v_cache"], a["lengths"])
+    for b in range(w.B):
+        L = int(a["lengths"][b])
+        mean = a["v_cache"][b, :, :L + 1].astype(np.float64).mean(1)
+        np.testing.assert_allclose(r.out[b], np.repeat(mean, w.G, 0), rtol=1e-12, atol=1e-12)
+
+
+def test_empty_cache_returns_new_value():
+    """[P2] Example 2 row 1: one valid slot -> output is that value exactly."""
+    w, a = _rand_case(3)
+    a["lengths"][:] = 0
+    r = oracle.decode_dense(a["q"], a["k_new"], a["v_new"], a["k_cache"], a["v_cache"], a["lengths"])
+    want = np.repeat(a["v_new"].astype(np.float64), w.G, 1)
+    assert np.array_equal(r.out, want)
+
+
+def test_weights_sum_to_one():
+    """sum_j w_j = 1: with every value vector all ones the output is 1."""
+    w, a = _rand_case(4)
+    a["v_cache"][:] = 1
+    a["v_new"][:] = 1
+    r = oracle.decode_dense(a["q"], a["k_new"], a["v_new"], a["k_cache"], a["v_cache"], a["lengths"])
+    np.testing.assert_allclose(r.out, 1.0, rtol=0, atol=1e-14)
+
+
+def test_value_shift():
+    """o(V + c) = o(V) + c, because the weights sum to one."""
+    w, a = _rand_case(5)
+    r0 = oracle.decode_dense(a["q"], a["k_new"], a["v_new"], a["k_cache"].copy(), a["v_cache"].copy(), a["lengths"])
+    c = np.float32(2.0)
+    r1 = oracle.decode_dense(a["q"], a["k_new"], a["v_new"] + c, a["k_cache"].copy(), a["v_cache"] + c, a["lengths"])
+    np.testing.assert_allclose(r1.out, r0.out + 2.0, rtol=0, atol=1e-6)
+
+
+def test_key_query_rescale():
+    """Scores use q.K only: K*alpha with q/alpha leaves the output unchanged
+    (alpha a power of two, so the rescaled inputs are exact)."""
+    w, a = _rand_case(6)
+    r0 = oracle.decode_dense(a["q"], a["k_new"], a["v_new"], a["k_cache"].copy(), a["v_cache"].copy(), a["lengths"])
+    r1 = oracle.decode_dense(a["q"] / 4, a["k_new"] * 4, a["v_new"], a["k_cache"] * 4, a["v_cache"].copy(), a["lengths"])
+    assert np.array_equal(r0.out, r1.out)
+
+
+def test_scale_is_inverse_sqrt_d():
+    """s = q.K / sqrt(D): two slots, keys chosen so q.K = sqrt(D)*ln 3 and 0;
+    weights 3/4 and 1/4 exactly (D = 16, sqrt(D) = 4)."""
+    D = 16
+    q = np.zeros((1, 1, D), np.float32); q[0, 0, 0] = 1
+    kc = np.zeros((1, 1, 2, D), np.float32)
+    kc[0, 0, 0, 0] = 4 * math.log(3)
+    vc = np.zeros_like(kc); vc[0, 0, 0, 0] = 1
+    kn = np.zeros((1, 1, D), np.float32)
+    vn = np.zeros((1, 1, D), np.float32); vn[0, 0, 1] = 1
+    r = oracle.decode_dense(q, kn, vn, kc, vc, np.array([1], np.int32))
+    e = math.exp(float(np.float32(4 * math.log(3))) / 4)
+    np.testing.assert_allclose(r.out[0, 0, :2], [e / (e + 1), 1 / (e + 1)], rtol=1e-15)
+    np.testing.assert_allclose(r.out[0, 0, :2], [0.75, 0.25], atol=1e-7)
+
+
+def test_group_mapping_is_contiguous():
+    """Query head h reads cache head floor(h/G) ([P2] statement): give each
+    cache head a distinct constant value and read it back per query head."""
+    B, Hq, Hkv, D, S = 1, 8, 4, 4, 5
+    q = np.random.default_rng(0).normal(size=(B, Hq, D)).astype(np.float32)
+    kc = np.random.default_rng(1).normal(size=(B, Hkv, S, D)).astype(np.float32)
+    vc = np.zeros((B, Hkv, S, D), np.float32)
+    for g in range(Hkv):
+        vc[:, g] = g + 1
+    kn = np.zeros((B, Hkv, D), np.float32)
+    vn = vc[:, :, 0].copy()
+    r = oracle.decode_dense(q, kn, vn, kc, vc, np.array([3], np.int32))
+    for h in range(Hq):
+        np.testing.assert_allclose(r.out[0, h], h // (Hq // Hkv) + 1, atol=1e-14)
+
+
+# ---------------------------------------------------------------- invariants
+
+def test_stale_slots_cannot_matter():
+    """[P2]: slots at or beyond the length get zero weight. Fill them with
+    other numbers, Inf and NaN: the output must not change by a single bit."""
+    w, a = _rand_case(7)
+    r0 = oracle.decode_dense(a["q"], a["k_new"], a["v_new"], a["k_cache"].copy(), a["v_cache"].copy(), a["lengths"])
+    for fill in (1e30, np.inf, np.nan):
+        kc, vc = a["k_cache"].copy(), a["v_cache"].copy()
+        for b in range(w.B):
+            kc[b, :, a["lengths"][b]:] = fill
+            vc[b, :, a["lengths"][b]:] = -fill
+        r1 = oracle.decode_dense(a["q"], a["k_new"], a["v_new"], kc, vc, a["lengths"])
+        assert r1.out.tobytes() == r0.out.tobytes()
+
+
+def test_slot_permutation():
+    """The softmax is a sum over slots: reordering the cached slots changes
+    the output by rounding only."""
+    w, a = _rand_case(8)
+    r0 = oracle.decode_dense(a["q"], a["k_new"], a["v_new"], a["k_cache"].copy(), a["v_cache"].copy(), a["lengths"])
+    kc, vc = a["k_cache"].copy(), a["v_cache"].copy()
+    rng = np.random.default_rng(0)
+    for b in range(w.B):
+        L = int(a["lengths"][b])
+        p = rng.permutation(L)
+        kc[b, :, :L] = kc[b][:, p]
+        vc[b, :, :L] = vc[b][:, p]
+    r1 = oracle.decode_dense(a["q"], a["k_new"], a["v_new"], kc, vc, a["lengths"])
+    np.testing.assert_allclose(r1.out, r0.out, rtol=1e-12, atol=1e-13)
+
+
+def test_append_touches_one_slot_per_row_head():
+    """In-place append ([P5] description): afterwards the cache equals the old
+    cache with exactly slot lengths[b] of each (row, head) replaced by the new
+    key/value bits; every other byte, and every unused row, is unchanged."""
+    w = W.small("ragged_slots", dtype="bf16", B=4, R=7, Hq=8, Hkv=2, D=16, Smax=20,
+                len_lo=1, len_hi=19, seed=9)
+    a = oracle_inputs(W.generate(w))
+    kc, vc = a["k_cache"].copy(), a["v_cache"].copy()
+    oracle.decode_dense(a["q"], a["k_new"], a["v_new"], kc, vc, a["lengths"], a["slot_ids"])
+    want_k, want_v = a["k_cache"].copy(), a["v_cache"].copy()
+    for b in range(w.B):
+        r, L = a["slot_ids"][b], a["lengths"][b]
+        want_k[r, :, L] = a["k_new"][b]
+        want_v[r, :, L] = a["v_new"][b]
+    assert kc.tobytes() == want_k.tobytes() and vc.tobytes() == want_v.tobytes()
+
+
+def test_slot_ids_is_a_row_map():
+    """[P5] slot_ids names the cache row of each batch row: the same data laid
+    out row b -> row slot_ids[b] gives the bit-identical output."""
+    w = W.small("ragged_slots", dtype="f32", B=4, R=9, Hq=8, Hkv=4, D=8, Smax=16,
+                len_lo=0, len_hi=15, seed=10)
+    a = oracle_inputs(W.generate(w))
+    sid = a["slot_ids"]
+    dense_k = np.ascontiguousarray(a["k_cache"][sid])
+    dense_v = np.ascontiguousarray(a["v_cache"][sid])
+    r0 = oracle.decode_dense(a["q"], a["k_new"], a["v_new"], dense_k, dense_v, a["lengths"])
+    r1 = oracle.decode_dense(a["q"], a["k_new"], a["v_new"], a["k_cache"], a["v_cache"], a["lengths"], sid)
+    assert r0.out.tobytes() == r1.out.tobytes()
+    assert np.array_equal(dense_k, a["k_cache"][sid])
+
+
+@pytest.mark.parametrize("block_size", [1, 4, 16])
+def test_paged_equals_dense(block_size):
+    """A paged cache with the same logical content as a dense one gives the
+    bit-identical output, and the append lands in block bt[b][L/bs] at
+    offset L%bs; unused blocks are never read (NaN-filled here)."""
+    max_blocks = 20 // block_size + 1
+    w = W.small("paged", dtype="bf16", B=3, Hq=6, Hkv=2, D=8, num_blocks=3 * max_blocks + 5,
+                block_size=block_size, max_blocks=max_blocks, len_lo=0, len_hi=19, seed=12)
+    a = oracle_inputs(W.generate(w))
+    bt, lens, bs = a["block_table"], a["lengths"], block_size
+    Smax = w.max_blocks * bs
+    dense_k = np.zeros((w.B, w.Hkv, Smax, w.D), np.uint16)
+    dense_v = np.zeros_like(dense_k)
+    for b in range(w.B):
+        for s in range(Smax):
+            blk = bt[b, s // bs]
+            if blk >= 0:
+                dense_k[b, :, s] = a["k_blocks"][blk, :, s % bs]
+                dense_v[b, :, s] = a["v_blocks"][blk, :, s % bs]
+    used = set(bt[bt >= 0].tolist())
+    kb, vb = a["k_blocks"].copy(), a["v_blocks"].copy()
+    for blk in range(w.num_blocks):
+        if blk not in used:
+            kb[blk] = 0x7FC0   # bf16 NaN
+            vb[blk] = 0x7FC0
+    r0 = oracle.decode_dense(a["q"], a["k_new"], a["v_new"], dense_k, dense_v, lens)
+    kb0 = kb.copy()
+    r1 = oracle.decode_paged(a["q"], a["k_new"], a["v_new"], kb, vb, bt, lens)
+    assert r1.status == oracle.OK
+    assert r0.out.tobytes() == r1.out.tobytes()
+    for b in range(w.B):
+        L = lens[b]
+        blk = bt[b, L // bs]
+        assert kb[blk, :, L % bs].tobytes() == a["k_new"][b].tobytes()
+        kb[blk, :, L % bs] = kb0[blk, :, L % bs]
+    assert kb.tobytes() == kb0.tobytes()
+
+
+def test_rows_subset_matches_full():
+    """Computing only some batch rows gives those rows' full-run values."""
+    w, a = _rand_case(13, B=5)
+    r_all = oracle.decode_dense(a["q"], a["k_new"], a["v_new"], a["k_cache"].copy(), a["v_cache"].copy(), a["lengths"])
+    r_sub = oracle.decode_dense(a["q"], a["k_new"], a["v_new"], a["k_cache"].copy(), a["v_cache"].copy(), a["lengths"],
+                                rows=[4, 1], append=False)
+    assert r_sub.out[[1, 4]].tobytes() == r_all.out[[1, 4]].tobytes()
+    assert np.isnan(r_sub.out[[0, 2, 3]]).all()
+
+
+def test_threads_do_not_change_bits():
+    w, a = _rand_case(14, B=4)
+    r1 = oracle.decode_dense(a["q"], a["k_new"], a["v_new"], a["k_cache"].copy(), a["v_cache"].copy(), a["lengths"], threads=1)
+    r8 = oracle.decode_dense(a["q"], a["k_new"], a["v_new"], a["k_cache"].copy(), a["v_cache"].copy(), a["lengths"], threads=8)
+    assert r1.out.tobytes() == r8.out.tobytes()
+
+
+# ----------------------------------------------------------------- validation
+
+def test_validate_dense_rules():
+    """[P5]: slot_ids entries in [0, max_seqs), no two rows sharing one; our
+    reading: 0 <= lengths[b] <= Smax-1, and R >= B without slot_ids."""
+    L = np.array([0, 5, 9], np.int32)
+    assert oracle.validate_dense(L, None, 3, 10) == oracle.OK
+    assert oracle.validate_dense(L, None, 2, 10) == oracle.INVALID_ARGUMENT     # R < B
+    assert oracle.validate_dense(np.array([0, 5, 10], np.int32), None, 3, 10) == oracle.INVALID_ARGUMENT
+    assert oracle.validate_dense(np.array([-1, 5, 9], np.int32), None, 3, 10) == oracle.INVALID_ARGUMENT
+    assert oracle.validate_dense(L, np.array([4, 0, 2], np.int32), 5, 10) == oracle.OK
+    assert oracle.validate_dense(L, np.array([4, 0, 4], np.int32), 5, 10) == oracle.INVALID_ARGUMENT
+    assert oracle.validate_dense(L, np.array([4, 0, 5], np.int32), 5, 10) == oracle.INVALID_ARGUMENT
+    assert oracle.validate_dense(L, np.array([4, -1, 2], np.int32), 5, 10) == oracle.INVALID_ARGUMENT
+
+
+def test_validate_paged_rules():
+    """[P5]: every entry -1 or in [0, num_blocks), no repeats within a row;
+    our reading: the blocks holding slots 0..lengths[b] must be real."""
+    bt = np.array([[3, 1, -1, -1], [0, 2, 5, -1]], np.int32)
+    L = np.array([7, 11], np.int32)          # block size 4: needs 2 and 3 blocks
+    ok = lambda t, l=L: oracle.validate_paged(l, t, 6, 4)
+    assert ok(bt) == oracle.OK
+    bad = bt.copy(); bad[1, 3] = 6
+    assert ok(bad) == oracle.INVALID_ARGUMENT                 # out of range
+    bad = bt.copy(); bad[1, 3] = -2
+    assert ok(bad) == oracle.INVALID_ARGUMENT                 # negative, not -1
+    bad = bt.copy(); bad[1, 2] = 0
+    assert ok(bad) == oracle.INVALID_ARGUMENT                 # repeat in a row
+    rep = bt.copy(); rep[1, 3] = 3
+    assert ok(rep) == oracle.OK                               # a block in two rows is allowed
+    assert ok(bt, np.array([8, 11], np.int32)) == oracle.INVALID_ARGUMENT   # slot 8 needs entry 2 (-1)
+    assert ok(bt, np.array([7, 16], np.int32)) == oracle.INVALID_ARGUMENT   # beyond max_blocks*bs
+    # a failed validation means no append and no output
+    q = np.zeros((2, 2, 4), np.float32)
+    kb = np.zeros((6, 1, 4, 4), np.float32)
+    bad = bt.copy(); bad[0, 1] = 3
+    r = oracle.decode_paged(q, np.ones((2, 1, 4), np.float32), np.ones((2, 1, 4), np.float32),
+                            kb, kb.copy(), bad, L)
+    assert r.status == oracle.INVALID_ARGUMENT and not kb.any()
