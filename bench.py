@@ -1,0 +1,438 @@
+#!/usr/bin/env python
+"""Benchmark of the GQA decode step over a KV cache on one GB300.
+
+A step is one call of the library's decode step (in-place append, split-S
+attention, log-sum-exp combine) over the whole synthetic batch of the chosen
+workload (default: the Llama-3-8B-shaped decode, bf16, B=32, Hq=32, Hkv=8,
+D=128, Smax=4096, lengths ~ U{1024..4095}).
+
+Prints ONE JSON line (rank 0):
+  value     KV-cache bytes the step must read (sum_b lengths[b]*Hkv*D*2*es)
+            divided by the device time of the step, in GB/s, inputs resident
+            in HBM, L2 flushed (256 MB write) between timed steps;
+  e2e       the same metric through the public API with the step's inputs
+            copied from pinned host memory and the output read back, every step;
+  roofline  the decode kernel alone (CUDA events around its launches) against
+            the measured HBM copy bandwidth;
+  cpu_baseline  the float64 CPU oracle on this machine's host cores.
+With --impl reference the oracle itself is timed as the reference arm.
+
+Multi-GPU (torchrun): every rank runs an independent replica with its own
+batch (weak scaling, no data-path collective); times are max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KV-cache HBM GB/s & fraction of ~8 TB/s peak; µs per GQA decode step"
+UNIT = "GB/s"
+NOMINAL_HBM_GBPS = 8000.0
+FALLBACK_HBM_GBPS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama3_8b")
+    ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "tc"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ ranks --
+
+class Ranks:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+
+    def init(self, backend):
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+        dev = "cuda" if self.pg.get_backend() == "nccl" else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def sum(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+        dev = "cuda" if self.pg.get_backend() == "nccl" else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ------------------------------------------------------------- workload ----
+
+def workload(name, rank):
+    import workloads as W
+    w = W.WORKLOADS[name]
+    if rank:
+        from dataclasses import replace
+        w = replace(w, seed=w.seed + 1000 * rank)
+    return w
+
+
+def algorithmic_bytes(w, t) -> dict:
+    """Bytes the step must move (no split partials): the KV read, the append
+    write, the new K/V, q, out and the index reads."""
+    import torch
+    L = t["lengths"].to(torch.int64)
+    es = w.elem_bytes
+    kv = int(L.sum().item()) * w.Hkv * w.D * 2 * es
+    new = w.B * w.Hkv * w.D * es * 2
+    idx = w.B * 4 * (2 if w.slot_ids else 1)
+    if w.paged:
+        idx += int(((L + w.block_size) // w.block_size).sum().item()) * 4
+    return {"kv_read": kv, "append_write": new, "new_kv_read": new,
+            "q_read": w.B * w.Hq * w.D * es, "out_write": w.B * w.Hq * w.D * 4, "index_read": idx,
+            "total": kv + 2 * new + w.B * w.Hq * w.D * es + w.B * w.Hq * w.D * 4 + idx}
+
+
+def step_fn(w, t, kernel, out):
+    import gqa_kv_cache_gb300 as gqa
+    if w.paged:
+        def run(tt=t):
+            gqa.decode_step_paged(tt["q"], tt["k_new"], tt["v_new"], tt["k_blocks"], tt["v_blocks"],
+                                  tt["block_table"], tt["lengths"], out=out, kernel=kernel)
+    else:
+        def run(tt=t):
+            gqa.decode_step(tt["q"], tt["k_new"], tt["v_new"], tt["k_cache"], tt["v_cache"],
+                            tt["lengths"], tt.get("slot_ids"), out=out, kernel=kernel)
+    return run
+
+
+# ---------------------------------------------------------------- clocks ---
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{device_index}.csv")
+
+    def start(self):
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(self.dev).uuid)
+            sel = ["-i", "GPU-" + uuid if not uuid.startswith("GPU-") else uuid]
+        except Exception:
+            sel = []
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50", *sel],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "power_w_max": max(power) if power else None, "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- oracle ---
+
+def oracle_rate(w, t, rows, repeats=3):
+    """CPU oracle over batch rows `rows` (host copies), timed: returns
+    (GB/s of KV processed, seconds per pass, threads)."""
+    import numpy as np
+    import torch
+    import oracle
+    sel = torch.tensor(rows, dtype=torch.long, device=t["q"].device)
+
+    def host(x):
+        x = x.detach().cpu().contiguous()
+        return x.view(torch.int16).numpy().view(np.uint16).copy() if x.dtype == torch.bfloat16 \
+            else x.numpy().copy()
+
+    q, kn, vn, L = host(t["q"][sel]), host(t["k_new"][sel]), host(t["v_new"][sel]), host(t["lengths"][sel])
+    if w.paged:
+        bt = t["block_table"][sel].cpu().numpy()
+        used = sorted(set(int(x) for x in bt[bt >= 0].tolist()))
+        remap = {b: i for i, b in enumerate(used)}
+        idx = torch.tensor(used, dtype=torch.long, device=t["q"].device)
+        kb, vb = host(t["k_blocks"][idx]), host(t["v_blocks"][idx])
+        btr = np.vectorize(lambda x: remap.get(int(x), -1))(bt).astype(np.int32)
+        run = lambda: oracle.decode_paged(q, kn, vn, kb, vb, btr, L, append=False)
+    else:
+        cr = t["slot_ids"][sel].long() if "slot_ids" in t else sel
+        kc, vc = host(t["k_cache"][cr]), host(t["v_cache"][cr])
+        run = lambda: oracle.decode_dense(q, kn, vn, kc, vc, L, append=False)
+    r = run()                                   # warm-up
+    times = []
+    for _ in range(repeats):
+        t0 = time.perf_counter()
+        r = run()
+        times.append(time.perf_counter() - t0)
+    sec = statistics.median(times)
+    kv = int(np.asarray(L, dtype=np.int64).sum()) * w.Hkv * w.D * 2 * w.elem_bytes
+    return kv / sec / 1e9, sec, r.threads
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBPS, "fallback"
+
+
+def traffic_for(kernel_name):
+    """Per-launch DRAM bytes of the kernel from the committed ncu summary,
+    if it was taken on the current source of that kernel; else None."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        d = json.load(open(p))[kernel_name]
+        src = os.path.join(ROOT, "gqa_kv_cache_gb300", "csrc", d["source"])
+        if hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != d["source_sha"]:
+            return None
+        return d["bytes_per_launch"]
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------------ arms ---
+
+def run_reference(args, ranks):
+    """The reference arm: the float64 CPU oracle (plain loops, as it stands),
+    on a bounded sample of the same workload, on this machine's host cores."""
+    if ranks.rank != 0:
+        return
+    import torch
+    w = workload(args.workload, 0)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    import workloads as W
+    t = W.generate(w, dev)
+    n = min(w.B, 4)
+    for i in range(args.warmup):
+        oracle_rate(w, t, [(i * n + k) % w.B for k in range(n)], repeats=1)
+    rates, secs, threads = [], [], 1
+    kv_total, t_total = 0, 0.0
+    for i in range(args.steps):
+        rows = [((i + args.warmup) * n + k) % w.B for k in range(n)]
+        gbs, sec, threads = oracle_rate(w, t, rows, repeats=1)
+        kv_total += gbs * sec * 1e9
+        t_total += sec
+    value = kv_total / t_total / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_total / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv,
+                                        "D": w.D, "sample_rows_per_step": n},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"{n} of {w.B} batch rows per step, rotating, float64 loops"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, ranks):
+    import torch
+    import workloads as W
+    import gqa_kv_cache_gb300 as gqa
+
+    torch.cuda.set_device(ranks.local)
+    dev = torch.device("cuda", ranks.local)
+    w = workload(args.workload, ranks.rank)
+    t = W.generate(w, dev)
+    torch.cuda.synchronize()
+    out = torch.empty(w.B, w.Hq, w.D, dtype=torch.float32, device=dev)
+    step = step_fn(w, t, args.kernel, out)
+    alg = algorithmic_bytes(w, t)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    for i in range(args.warmup):
+        flush.fill_(i & 0xFF)
+        step()
+    torch.cuda.synchronize()
+
+    # ---- timed region: K steps, L2 flushed between them (outside the events)
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    clocks = ClockSampler(ranks.local)
+    clocks.start()
+    ranks.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    ranks.barrier()
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = ranks.max(sum(step_ms))
+    ms_per_step = total_ms / K
+    kv_all = ranks.sum(alg["kv_read"])
+    value = kv_all * K / (total_ms * 1e-3) / 1e9
+
+    # ---- the decode kernel alone (trace: CUDA events around each launch)
+    gqa.trace_enable(True)
+    gqa.trace_collect()
+    Kr = min(K, 500)
+    for i in range(Kr):
+        flush.fill_(i & 0xFF)
+        step()
+    torch.cuda.synchronize()
+    tr = gqa.trace_collect()
+    gqa.trace_enable(False)
+    main = max((k for k in tr if k != "combine_kernel"), key=lambda k: tr[k][0])
+    n_main, ms_main = tr[main]
+    n_comb, ms_comb = tr.get("combine_kernel", (0, 0.0))
+    avg_main_s = ms_main / max(n_main, 1) * 1e-3
+    hbm_peak, peak_kind = peaks()
+    achieved = alg["total"] / avg_main_s / 1e9
+    traffic = traffic_for(main)
+
+    # ---- end to end through the public API, host buffers, copies inside
+    Ke = min(K, 500)
+    inputs = ["q", "k_new", "v_new", "lengths"] + (["slot_ids"] if "slot_ids" in t else []) + \
+        (["block_table"] if "block_table" in t else [])
+    host = {k: t[k].cpu().pin_memory() for k in inputs}
+    dev_in = {k: torch.empty_like(t[k]) for k in inputs}
+    tt = dict(t)
+    tt.update(dev_in)
+    step_e2e = step_fn(w, tt, args.kernel, out)
+    out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h2d = sum(host[k].numel() * host[k].element_size() for k in inputs)
+    d2h = out.numel() * out.element_size()
+    e2e_ms = 0.0
+    for i in range(Ke + 3):
+        flush.fill_(i & 0xFF)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for k in inputs:
+            dev_in[k].copy_(host[k], non_blocking=True)
+        step_e2e()
+        out_host.copy_(out, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        if i >= 3:
+            e2e_ms += a.elapsed_time(b)
+    e2e_ms = ranks.max(e2e_ms)
+    e2e_value = kv_all * Ke / (e2e_ms * 1e-3) / 1e9
+
+    # ---- CPU baseline: the oracle on host cores, rank 0 at N = 1 only
+    cpu = None
+    if ranks.world == 1 and not args.no_cpu_baseline:
+        rows = list(range(w.B))
+        gbs, sec, threads = oracle_rate(w, t, rows, repeats=3)
+        cpu = {"value": gbs, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"all {w.B} batch rows of one step (no append), float64 loops, "
+                         f"median of 3 after 1 warm-up, {sec:.2f} s per pass"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ranks.world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "us_per_step": ms_per_step * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic",
+        "frac_of_8TBps": value / ranks.world / NOMINAL_HBM_GBPS,
+        "frac_of_measured_hbm": value / ranks.world / hbm_peak,
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "G": w.G, "D": w.D,
+                   "Smax": w.Smax, "paged": w.paged, "kernel": main, "kernel_option": args.kernel,
+                   "kv_bytes_per_step_per_gpu": alg["kv_read"],
+                   "l2": "flushed between timed steps (256 MB device write outside the events)",
+                   "parallelism": f"replicas x{ranks.world} (independent batches per GPU)",
+                   "wall_s_timed_region": wall},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": traffic,
+                     "peak_kind": peak_kind + " (STREAM-style copy)",
+                     "kernel": main, "avg_launch_us": avg_main_s * 1e6,
+                     "combine_avg_us": ms_comb / max(n_comb, 1) * 1e3,
+                     "algorithmic_bytes_per_launch": alg["total"]},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "us_per_step": e2e_ms / Ke * 1e3},
+        "gpu_launches": 2 * K,
+        "clocks": clk,
+    }
+    if ranks.rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    ranks = Ranks()
+    if args.impl == "reference":
+        # no GPU collective is needed: rank 0 alone runs the oracle
+        run_reference(args, ranks)
+        return
+    import torch
+    ranks.init("nccl" if torch.cuda.is_available() else "gloo")
+    try:
+        run_ours(args, ranks)
+    finally:
+        ranks.close()
+
+
+if __name__ == "__main__":
+    main()

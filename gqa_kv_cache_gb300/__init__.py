@@ -1,0 +1,185 @@
+"""GQA decode step over a KV cache on GB300 (sm_103a).
+
+Thin Python binding of ``libgqa.so``: it checks tensor shapes and dtypes,
+passes device pointers and the current CUDA stream to the C ABI
+(include/gqa_decode.h) and raises on error codes. Every step of the decode
+runs in the library's CUDA kernels; PyTorch only provides device memory and
+streams. There is no CPU fallback: without the built library or a GPU the
+calls raise.
+
+One decode step, per batch row b: the new key/value are appended in place at
+slot ``lengths[b]`` of the row's cache, and every query head h attends over
+slots ``0..lengths[b]`` of cache head ``h // (Hq // Hkv)`` with a float32
+softmax of ``q.K/sqrt(D)``; the output is float32 (B, Hq, D).
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+
+__all__ = ["decode_step", "decode_step_paged", "workspace_bytes", "validate",
+           "GqaError", "trace_enable", "trace_collect", "KERNELS", "library_path"]
+
+OK, INVALID_ARGUMENT, UNSUPPORTED, CUDA_ERROR, WORKSPACE = 0, 1, 2, 3, 4
+KERNELS = {"auto": 0, "simt": 1, "tc": 2}
+STATUS_BITS = {1: "bad length", 2: "bad slot id", 4: "bad block", 8: "timeout"}
+_DTYPES = {torch.float32: 0, torch.bfloat16: 1}
+
+library_path = _lib.LIB_PATH
+
+
+class GqaError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        msg = _lib.load().gqa_status_string(code).decode()
+        super().__init__(f"{what}: {msg} (status {code})")
+
+
+def _check(code: int, what: str):
+    if code != OK:
+        raise GqaError(code, what)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _opts(kernel, grid_ctas):
+    o = _lib.GqaOptions()
+    o.kernel = KERNELS[kernel] if isinstance(kernel, str) else int(kernel)
+    o.grid_ctas = int(grid_ctas)
+    return o
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+_ws_cache: dict = {}
+
+
+def _workspace(device, nbytes):
+    buf = _ws_cache.get(device)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.empty(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
+        _ws_cache[device] = buf
+    return buf
+
+
+def workspace_bytes(B, Hq, Hkv, D, dtype=torch.bfloat16, kernel="auto", grid_ctas=0) -> int:
+    """Workspace bytes the library needs for one step of these sizes."""
+    o = _opts(kernel, grid_ctas)
+    return int(_lib.load().gqa_workspace_bytes(B, Hq, Hkv, D, _DTYPES[dtype], ctypes.byref(o)))
+
+
+def _common_checks(q, k_new, v_new, caches, lengths, out):
+    if not q.is_cuda:
+        raise ValueError("tensors must be on a CUDA device")
+    dt = q.dtype
+    if dt not in _DTYPES:
+        raise TypeError("q must be float32 or bfloat16")
+    for name, t in (("k_new", k_new), ("v_new", v_new), *caches):
+        if t.dtype != dt:
+            raise TypeError(f"{name} must have q's dtype {dt}")
+        if t.device != q.device:
+            raise ValueError(f"{name} is on {t.device}, q on {q.device}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if not q.is_contiguous():
+        raise ValueError("q must be contiguous")
+    if lengths.dtype != torch.int32 or not lengths.is_contiguous() or lengths.device != q.device:
+        raise TypeError("lengths must be a contiguous int32 tensor on q's device")
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    elif out.shape != (B, Hq, D) or out.dtype != torch.float32 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous float32 (B, Hq, D) tensor")
+    return dt, out
+
+
+def decode_step(q, k_new, v_new, k_cache, v_cache, lengths, slot_ids=None, *, out=None,
+                status=None, kernel="auto", grid_ctas=0, workspace=None, stream=None):
+    """One decode step on a dense (R, Hkv, Smax, D) cache (continuous batch
+    when ``slot_ids`` is given). Appends in place; returns ``out``."""
+    dt, out = _common_checks(q, k_new, v_new, (("k_cache", k_cache), ("v_cache", v_cache)),
+                             lengths, out)
+    B, Hq, D = q.shape
+    R, Hkv, Smax, D2 = k_cache.shape
+    if D2 != D or v_cache.shape != k_cache.shape or k_new.shape != (B, Hkv, D) or v_new.shape != (B, Hkv, D):
+        raise ValueError("shape mismatch between q, k_new, v_new and the caches")
+    if slot_ids is not None and (slot_ids.dtype != torch.int32 or slot_ids.shape != (B,)):
+        raise TypeError("slot_ids must be int32 of shape (B,)")
+    o = _opts(kernel, grid_ctas)
+    lib = _lib.load()
+    need = lib.gqa_workspace_bytes(B, Hq, Hkv, D, _DTYPES[dt], ctypes.byref(o))
+    ws = _workspace(q.device, need) if workspace is None else workspace
+    code = lib.gqa_decode_step_ex(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                  _ptr(lengths), _ptr(slot_ids), _ptr(out), B, Hq, Hkv, D, R, Smax,
+                                  _DTYPES[dt], _ptr(ws), ws.numel() * ws.element_size(),
+                                  _ptr(status), _stream(stream), ctypes.byref(o))
+    _check(code, "gqa_decode_step")
+    return out
+
+
+def decode_step_paged(q, k_new, v_new, k_blocks, v_blocks, block_table, lengths, *, out=None,
+                      status=None, kernel="auto", grid_ctas=0, workspace=None, stream=None):
+    """One decode step on a paged cache (num_blocks, Hkv, block_size, D) with
+    a (B, max_blocks) int32 block table (-1 = unused). Appends in place."""
+    dt, out = _common_checks(q, k_new, v_new, (("k_blocks", k_blocks), ("v_blocks", v_blocks)),
+                             lengths, out)
+    B, Hq, D = q.shape
+    NB, Hkv, BS, D2 = k_blocks.shape
+    if D2 != D or v_blocks.shape != k_blocks.shape or k_new.shape != (B, Hkv, D) or v_new.shape != (B, Hkv, D):
+        raise ValueError("shape mismatch between q, k_new, v_new and the blocks")
+    if block_table.dtype != torch.int32 or block_table.dim() != 2 or block_table.shape[0] != B \
+            or not block_table.is_contiguous():
+        raise TypeError("block_table must be a contiguous int32 (B, max_blocks) tensor")
+    MB = block_table.shape[1]
+    o = _opts(kernel, grid_ctas)
+    lib = _lib.load()
+    need = lib.gqa_workspace_bytes(B, Hq, Hkv, D, _DTYPES[dt], ctypes.byref(o))
+    ws = _workspace(q.device, need) if workspace is None else workspace
+    code = lib.gqa_decode_step_paged_ex(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_blocks),
+                                        _ptr(v_blocks), _ptr(block_table), _ptr(lengths), _ptr(out),
+                                        B, Hq, Hkv, D, NB, BS, MB, _DTYPES[dt], _ptr(ws),
+                                        ws.numel() * ws.element_size(), _ptr(status),
+                                        _stream(stream), ctypes.byref(o))
+    _check(code, "gqa_decode_step_paged")
+    return out
+
+
+def validate(lengths, *, slot_ids=None, R=None, Smax=None, block_table=None, num_blocks=None,
+             block_size=None, stream=None) -> bool:
+    """Full content check on the GPU (synchronous). True when valid."""
+    B = lengths.shape[0]
+    res = torch.empty(1, dtype=torch.int32, device=lengths.device)
+    lib = _lib.load()
+    if block_table is not None:
+        code = lib.gqa_validate(_ptr(lengths), None, _ptr(block_table), B, 0, 0, num_blocks,
+                                block_size, block_table.shape[1], _ptr(res), _stream(stream))
+    else:
+        code = lib.gqa_validate(_ptr(lengths), _ptr(slot_ids), None, B, R, Smax, 0, 0, 0,
+                                _ptr(res), _stream(stream))
+    if code == INVALID_ARGUMENT:
+        return False
+    _check(code, "gqa_validate")
+    return True
+
+
+def trace_enable(on: bool = True) -> bool:
+    return bool(_lib.load().gqa_trace_enable(int(on)))
+
+
+def trace_collect() -> dict:
+    """{kernel name: (launches, total ms)} since the previous collect."""
+    lib = _lib.load()
+    n = 3
+    launches = (ctypes.c_int64 * n)()
+    ms = (ctypes.c_double * n)()
+    _check(lib.gqa_trace_collect(n, launches, ms), "gqa_trace_collect")
+    return {lib.gqa_kernel_name(k).decode(): (launches[k], ms[k]) for k in range(n)}

@@ -1,0 +1,54 @@
+"""ctypes declarations of libgqa.so (the C ABI in include/gqa_decode.h)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libgqa.so")
+
+P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+
+# name -> (restype, argtypes); the exported C functions of include/gqa_decode.h
+SIGNATURES = {
+    "gqa_status_string": (ctypes.c_char_p, [I]),
+    "gqa_workspace_bytes": (Z, [I, I, I, I, I, P]),
+    "gqa_decode_step": (I, [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, Z, P, P]),
+    "gqa_decode_step_paged": (I, [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, P, Z, P, P]),
+    "gqa_decode_step_ex": (I, [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, Z, P, P, P]),
+    "gqa_decode_step_paged_ex": (I, [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, P, Z, P, P, P]),
+    "gqa_validate": (I, [P, P, P, I, I, I, I, I, I, P, P]),
+    "gqa_trace_enable": (I, [I]),
+    "gqa_trace_collect": (I, [I, P, P]),
+    "gqa_kernel_name": (ctypes.c_char_p, [I]),
+    "gqa_version": (I, []),
+}
+
+
+class GqaOptions(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int), ("grid_ctas", ctypes.c_int),
+                ("reserved", ctypes.c_int * 6)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """The loaded library. Raises if it has not been built: there is no
+    fallback implementation."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; "
+                    "g.build()'` (or python gqa_kv_cache_gb300/build.py)")
+            lib = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib

@@ -1,0 +1,450 @@
+// The C ABI (include/gqa_decode.h): host-side argument checks, kernel
+// choice, workspace sizing, TMA descriptor encoding, launches and tracing.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "gqa_decode.h"
+#include "gqa_launch.h"
+
+using namespace gqa;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+int sm_count(int dev)
+{
+    static int cache[kMaxDevices] = {0};
+    if (dev < 0 || dev >= kMaxDevices)
+        return 0;
+    if (!cache[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return 0;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+// Kernel the call will use (GQA_KERNEL_SIMT / GQA_KERNEL_TC) or -1.
+int pick_kernel(const gqa_options *opt, gqa_dtype dt, int D, int G, bool paged, int block_size)
+{
+    const int want = opt ? opt->kernel : GQA_KERNEL_AUTO;
+    const bool bf16 = dt == GQA_DTYPE_BF16;
+    const bool tc_ok = tc_supports(bf16, D, G, paged, block_size);
+    const bool simt_ok = simt_supports(D, G);
+    if (want == GQA_KERNEL_TC)
+        return tc_ok ? GQA_KERNEL_TC : -1;
+    if (want == GQA_KERNEL_SIMT)
+        return simt_ok ? GQA_KERNEL_SIMT : -1;
+    if (want != GQA_KERNEL_AUTO)
+        return -1;
+    if (tc_ok)
+        return GQA_KERNEL_TC;
+    return simt_ok ? GQA_KERNEL_SIMT : -1;
+}
+
+// Persistent grid: every SM holds as many CTAs as fit at once (cached per
+// device and kernel instantiation).
+int grid_for(int kernel, const gqa_options *opt, gqa_dtype dt, int D, int G)
+{
+    if (opt && opt->grid_ctas > 0)
+        return opt->grid_ctas;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return 0;
+    const int sms = sm_count(dev);
+    if (kernel == GQA_KERNEL_TC)
+        return sms * tc_ctas_per_sm();
+    static std::mutex mu;
+    static int cache[kMaxDevices][2][9][9] = {};
+    int dlog = 0;
+    while ((1 << dlog) < D && dlog < 8)
+        ++dlog;
+    const int bf = dt == GQA_DTYPE_BF16 ? 1 : 0;
+    std::lock_guard<std::mutex> g(mu);
+    int &c = cache[dev < kMaxDevices ? dev : 0][bf][dlog][G < 9 ? G : 8];
+    if (!c)
+        c = simt_ctas_per_sm(bf, D, G);
+    return sms * c;
+}
+
+// ------------------------------------------------------------------ trace --
+
+struct TraceRec {
+    int kind;
+    cudaEvent_t start, stop;
+};
+
+struct Trace {
+    std::mutex mu;
+    bool on = false;
+    std::vector<TraceRec> pending;
+    std::vector<cudaEvent_t> pool;
+    cudaEvent_t get()
+    {
+        if (!pool.empty()) {
+            cudaEvent_t e = pool.back();
+            pool.pop_back();
+            return e;
+        }
+        cudaEvent_t e = nullptr;
+        cudaEventCreate(&e);
+        return e;
+    }
+};
+
+Trace &trace()
+{
+    static Trace t;
+    return t;
+}
+
+struct TraceScope {
+    bool on;
+    int kind;
+    cudaStream_t st;
+    cudaEvent_t a = nullptr, b = nullptr;
+    TraceScope(int k, cudaStream_t s) : on(trace().on), kind(k), st(s)
+    {
+        if (on) {
+            std::lock_guard<std::mutex> g(trace().mu);
+            a = trace().get();
+            b = trace().get();
+            cudaEventRecord(a, st);
+        }
+    }
+    ~TraceScope()
+    {
+        if (on) {
+            cudaEventRecord(b, st);
+            std::lock_guard<std::mutex> g(trace().mu);
+            trace().pending.push_back({kind, a, b});
+        }
+    }
+};
+
+// ------------------------------------------------------- tensor maps (TMA) --
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 3-D map over a bf16 cache seen as (D, rows_per_head, heads_total):
+// box (64 elements = 128 bytes, box_rows, 1) with the 128-byte swizzle.
+bool encode_cache_map(CUtensorMap *m, void *base, int D, long long rows_per_head,
+                      long long heads_total, int box_rows)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)rows_per_head, (cuuint64_t)heads_total};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)D * 2 * (cuuint64_t)rows_per_head};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------- the step --
+
+struct Shape {
+    int B, Hq, Hkv, D;
+    gqa_dtype dt;
+    bool paged;
+    int R, Smax;
+    int num_blocks, block_size, max_blocks;
+};
+
+gqa_status check_shape(const Shape &s)
+{
+    if (s.B < 0 || s.Hq < 1 || s.Hkv < 1 || s.D < 1 || s.Hq % s.Hkv != 0)
+        return GQA_ERR_INVALID_ARGUMENT;
+    if (s.dt != GQA_DTYPE_F32 && s.dt != GQA_DTYPE_BF16)
+        return GQA_ERR_INVALID_ARGUMENT;
+    if (s.paged) {
+        if (s.num_blocks < 1 || s.block_size < 1 || s.max_blocks < 1)
+            return GQA_ERR_INVALID_ARGUMENT;
+        if ((long long)s.max_blocks * s.block_size > (1LL << 31) - 1)
+            return GQA_ERR_INVALID_ARGUMENT;
+    } else {
+        if (s.R < 0 || s.Smax < 1)
+            return GQA_ERR_INVALID_ARGUMENT;
+    }
+    return GQA_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+gqa_status run_step(const Shape &s, const void *q, const void *k_new, const void *v_new, void *kc,
+                    void *vc, const int32_t *lengths, const int32_t *slot_ids,
+                    const int32_t *block_table, float *out, void *ws, size_t ws_bytes,
+                    int32_t *d_status, void *stream, const gqa_options *opt)
+{
+    gqa_status st = check_shape(s);
+    if (st != GQA_OK)
+        return st;
+    if (s.B == 0)
+        return GQA_OK;
+    if (!q || !k_new || !v_new || !kc || !vc || !lengths || !out || (s.paged && !block_table))
+        return GQA_ERR_INVALID_ARGUMENT;
+    if (!s.paged && !slot_ids && s.R < s.B)
+        return GQA_ERR_INVALID_ARGUMENT;
+    if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(kc) || !aligned16(vc) ||
+        !aligned16(out))
+        return GQA_ERR_INVALID_ARGUMENT;
+    const int G = s.Hq / s.Hkv;
+    const int kernel = pick_kernel(opt, s.dt, s.D, G, s.paged, s.block_size);
+    if (kernel < 0)
+        return GQA_ERR_UNSUPPORTED;
+    const int grid = grid_for(kernel, opt, s.dt, s.D, G);
+    if (grid <= 0)
+        return GQA_ERR_CUDA;
+    const WorkspaceLayout lay = workspace_layout(s.B, s.Hkv, G, s.D, grid);
+    if (!ws || ws_bytes < lay.bytes || (reinterpret_cast<uintptr_t>(ws) & 255u))
+        return GQA_ERR_WORKSPACE;
+
+    DecodeParams p;
+    std::memset(&p, 0, sizeof p);
+    p.q = q;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.k_cache = kc;
+    p.v_cache = vc;
+    p.lengths = lengths;
+    p.slot_ids = s.paged ? nullptr : slot_ids;
+    p.block_table = s.paged ? block_table : nullptr;
+    p.out = out;
+    p.B = s.B;
+    p.Hq = s.Hq;
+    p.Hkv = s.Hkv;
+    p.G = G;
+    p.D = s.D;
+    p.R = s.R;
+    p.Smax = s.Smax;
+    p.paged = s.paged ? 1 : 0;
+    p.num_blocks = s.num_blocks;
+    p.block_size = s.block_size;
+    p.max_blocks = s.max_blocks;
+    p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)s.D));
+    p.tile = kernel == GQA_KERNEL_TC ? tc_tile() : simt_tile();
+    p.grid = grid;
+    char *w = static_cast<char *>(ws);
+    p.ws_total = reinterpret_cast<long long *>(w + lay.off_total);
+    p.ws_rowpre = reinterpret_cast<long long *>(w + lay.off_rowpre);
+    p.ws_ml = reinterpret_cast<float *>(w + lay.off_ml);
+    p.ws_o = reinterpret_cast<float *>(w + lay.off_o);
+    p.status = d_status;
+
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (kernel == GQA_KERNEL_TC) {
+        TcMaps maps;
+        const int T = p.tile;
+        bool ok;
+        if (s.paged) {
+            const int box = s.block_size < T ? s.block_size : T;
+            ok = encode_cache_map(&maps.k, kc, s.D, s.block_size, (long long)s.num_blocks * s.Hkv, box) &&
+                 encode_cache_map(&maps.v, vc, s.D, s.block_size, (long long)s.num_blocks * s.Hkv, box);
+        } else {
+            ok = encode_cache_map(&maps.k, kc, s.D, s.Smax, (long long)s.R * s.Hkv, T) &&
+                 encode_cache_map(&maps.v, vc, s.D, s.Smax, (long long)s.R * s.Hkv, T);
+        }
+        if (!ok)
+            return GQA_ERR_CUDA;
+        TraceScope ts(1, cs);
+        e = tc_launch(p, maps, cs);
+    } else {
+        TraceScope ts(0, cs);
+        e = simt_launch(p, s.dt == GQA_DTYPE_BF16, cs);
+    }
+    if (e != cudaSuccess)
+        return GQA_ERR_CUDA;
+    {
+        TraceScope ts(2, cs);
+        e = combine_launch(p, cs, !trace().on);
+    }
+    return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *gqa_status_string(gqa_status s)
+{
+    switch (s) {
+    case GQA_OK: return "ok";
+    case GQA_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case GQA_ERR_UNSUPPORTED: return "unsupported sizes (no kernel in this build)";
+    case GQA_ERR_CUDA: return "CUDA runtime error";
+    case GQA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    }
+    return "unknown status";
+}
+
+size_t gqa_workspace_bytes(int B, int Hq, int Hkv, int D, gqa_dtype dt, const gqa_options *opt)
+{
+    if (B < 0 || Hq < 1 || Hkv < 1 || D < 1 || Hq % Hkv)
+        return 0;
+    const int G = Hq / Hkv;
+    // the block size only matters for the paged form; 16 is the common case and
+    // the workspace does not depend on it
+    int kernel = pick_kernel(opt, dt, D, G, false, 16);
+    if (kernel < 0)
+        return 0;
+    int grid = grid_for(kernel, opt, dt, D, G);
+    // AUTO may pick either kernel depending on the block size: size for the larger grid
+    if ((!opt || opt->kernel == GQA_KERNEL_AUTO) && simt_supports(D, G)) {
+        const int g2 = grid_for(GQA_KERNEL_SIMT, opt, dt, D, G);
+        grid = grid > g2 ? grid : g2;
+    }
+    if (grid <= 0)
+        return 0;
+    return workspace_layout(B, Hkv, G, D, grid).bytes;
+}
+
+gqa_status gqa_decode_step_ex(const void *q, const void *k_new, const void *v_new, void *k_cache,
+                              void *v_cache, const int32_t *lengths, const int32_t *slot_ids,
+                              float *out, int B, int Hq, int Hkv, int D, int R, int Smax,
+                              gqa_dtype dt, void *workspace, size_t workspace_bytes,
+                              int32_t *d_status, void *stream, const gqa_options *opt)
+{
+    Shape s = {B, Hq, Hkv, D, dt, false, R, Smax, 0, 0, 0};
+    return run_step(s, q, k_new, v_new, k_cache, v_cache, lengths, slot_ids, nullptr, out,
+                    workspace, workspace_bytes, d_status, stream, opt);
+}
+
+gqa_status gqa_decode_step(const void *q, const void *k_new, const void *v_new, void *k_cache,
+                           void *v_cache, const int32_t *lengths, const int32_t *slot_ids,
+                           float *out, int B, int Hq, int Hkv, int D, int R, int Smax,
+                           gqa_dtype dt, void *workspace, size_t workspace_bytes,
+                           int32_t *d_status, void *stream)
+{
+    return gqa_decode_step_ex(q, k_new, v_new, k_cache, v_cache, lengths, slot_ids, out, B, Hq,
+                              Hkv, D, R, Smax, dt, workspace, workspace_bytes, d_status, stream,
+                              nullptr);
+}
+
+gqa_status gqa_decode_step_paged_ex(const void *q, const void *k_new, const void *v_new,
+                                    void *k_blocks, void *v_blocks, const int32_t *block_table,
+                                    const int32_t *lengths, float *out, int B, int Hq, int Hkv,
+                                    int D, int num_blocks, int block_size, int max_blocks,
+                                    gqa_dtype dt, void *workspace, size_t workspace_bytes,
+                                    int32_t *d_status, void *stream, const gqa_options *opt)
+{
+    Shape s = {B, Hq, Hkv, D, dt, true, 0, 0, num_blocks, block_size, max_blocks};
+    return run_step(s, q, k_new, v_new, k_blocks, v_blocks, lengths, nullptr, block_table, out,
+                    workspace, workspace_bytes, d_status, stream, opt);
+}
+
+gqa_status gqa_decode_step_paged(const void *q, const void *k_new, const void *v_new,
+                                 void *k_blocks, void *v_blocks, const int32_t *block_table,
+                                 const int32_t *lengths, float *out, int B, int Hq, int Hkv, int D,
+                                 int num_blocks, int block_size, int max_blocks, gqa_dtype dt,
+                                 void *workspace, size_t workspace_bytes, int32_t *d_status,
+                                 void *stream)
+{
+    return gqa_decode_step_paged_ex(q, k_new, v_new, k_blocks, v_blocks, block_table, lengths, out,
+                                    B, Hq, Hkv, D, num_blocks, block_size, max_blocks, dt,
+                                    workspace, workspace_bytes, d_status, stream, nullptr);
+}
+
+gqa_status gqa_validate(const int32_t *lengths, const int32_t *slot_ids, const int32_t *block_table,
+                        int B, int R, int Smax, int num_blocks, int block_size, int max_blocks,
+                        int32_t *d_result, void *stream)
+{
+    if (B < 0 || !d_result)
+        return GQA_ERR_INVALID_ARGUMENT;
+    if (block_table) {
+        if (num_blocks < 1 || block_size < 1 || max_blocks < 1)
+            return GQA_ERR_INVALID_ARGUMENT;
+    } else if (R < 0 || Smax < 1 || (!slot_ids && B > R)) {
+        return GQA_ERR_INVALID_ARGUMENT;
+    }
+    if (B == 0)
+        return GQA_OK;
+    if (!lengths)
+        return GQA_ERR_INVALID_ARGUMENT;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(d_result, 0, sizeof(int32_t), cs) != cudaSuccess)
+        return GQA_ERR_CUDA;
+    if (validate_launch(lengths, block_table ? nullptr : slot_ids, block_table, B, R, Smax,
+                        num_blocks, block_size, max_blocks, d_result, cs) != cudaSuccess)
+        return GQA_ERR_CUDA;
+    int32_t h = 0;
+    if (cudaMemcpyAsync(&h, d_result, sizeof h, cudaMemcpyDeviceToHost, cs) != cudaSuccess ||
+        cudaStreamSynchronize(cs) != cudaSuccess)
+        return GQA_ERR_CUDA;
+    return h ? GQA_ERR_INVALID_ARGUMENT : GQA_OK;
+}
+
+int gqa_trace_enable(int on)
+{
+    std::lock_guard<std::mutex> g(trace().mu);
+    int prev = trace().on ? 1 : 0;
+    trace().on = on != 0;
+    return prev;
+}
+
+gqa_status gqa_trace_collect(int n_kinds, int64_t *launches, double *ms)
+{
+    std::vector<TraceRec> recs;
+    {
+        std::lock_guard<std::mutex> g(trace().mu);
+        recs.swap(trace().pending);
+    }
+    for (int k = 0; k < n_kinds; ++k) {
+        if (launches) launches[k] = 0;
+        if (ms) ms[k] = 0.0;
+    }
+    gqa_status st = GQA_OK;
+    for (const TraceRec &r : recs) {
+        float t = 0.f;
+        if (cudaEventSynchronize(r.stop) != cudaSuccess || cudaEventElapsedTime(&t, r.start, r.stop) != cudaSuccess)
+            st = GQA_ERR_CUDA;
+        if (r.kind < n_kinds) {
+            if (launches) launches[r.kind] += 1;
+            if (ms) ms[r.kind] += t;
+        }
+        std::lock_guard<std::mutex> g(trace().mu);
+        trace().pool.push_back(r.start);
+        trace().pool.push_back(r.stop);
+    }
+    return st;
+}
+
+const char *gqa_kernel_name(int kind)
+{
+    switch (kind) {
+    case 0: return "simt_decode_kernel";
+    case 1: return "tc_decode_kernel";
+    case 2: return "combine_kernel";
+    }
+    return "unknown";
+}
+
+int gqa_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,38 @@
+// Host-side entry points of the kernels, used by the C ABI layer.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "gqa_common.cuh"
+
+namespace gqa {
+
+// CUDA-core decode kernel (gqa_simt.cu).
+bool simt_supports(int D, int G);
+int simt_tile();
+int simt_ctas_per_sm(bool bf16, int D, int G);  // occupancy of that instantiation
+cudaError_t simt_launch(const DecodeParams &p, bool bf16, cudaStream_t st);
+
+// TMA-ring + tensor-core decode kernel (gqa_tc.cu).
+struct TcMaps {
+    CUtensorMap k, v;  // tiled maps over the key / value cache, 128-byte swizzle
+};
+bool tc_supports(bool bf16, int D, int G, bool paged, int block_size);
+int tc_tile();
+int tc_ctas_per_sm();
+size_t tc_smem_bytes();
+cudaError_t tc_launch(const DecodeParams &p, const TcMaps &maps, cudaStream_t st);
+
+// Split combine (gqa_combine.cu): merges the partial states of the units cut
+// by CTA boundaries; grid = B * Hkv.
+cudaError_t combine_launch(const DecodeParams &p, cudaStream_t st, bool pdl);
+
+// Content validation (gqa_combine.cu). *d_result must be zero on entry; the
+// kernel sets it to 1 on any violation.
+cudaError_t validate_launch(const int32_t *lengths, const int32_t *slot_ids,
+                            const int32_t *block_table, int B, int R, int Smax,
+                            int num_blocks, int block_size, int max_blocks,
+                            int32_t *d_result, cudaStream_t st);
+
+}  // namespace gqa

@@ -1,0 +1,528 @@
+// Tensor-core decode kernel for bfloat16 caches with D = 128 and G <= 8.
+//
+// Data path (per persistent CTA, one per SM):
+//  * a producer warp walks the CTA's tile list (gqa_common.cuh) and streams
+//    every 64-slot tile of K and V from HBM into a 4-stage shared-memory ring
+//    with TMA tiled copies (cp.async.bulk.tensor, 128-byte swizzle, two
+//    64-element halves per row), signalling an mbarrier per stage; for paged
+//    caches each lane copies one block of the tile;
+//  * four consumer warps each take 16 slots of every tile and compute, on the
+//    tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate):
+//      S  = Q K^T   M = 16 query rows (the G heads; rows >= G are zero),
+//                   N = 8 slots, K = 16 dims, 8 steps over D = 128;
+//      O += P V     M = 16 rows: rows 0..7 carry bf16(p) and rows 8..15 the
+//                   remainder bf16(p - bf16(p)), so p enters the product with
+//                   ~16 significant bits and the sum stays float32-accurate;
+//                   N = 8 dims (16 tiles over D), K = 16 slots.
+//    The S accumulator fragment is reused directly as the A fragment of the
+//    P V product. K fragments come from ldmatrix, V fragments from
+//    ldmatrix.trans; the swizzle makes both conflict-free.
+//  * online softmax in float32 with base-2 scores (scale log2(e)/sqrt(D)
+//    folded in), a lazy rescale (the running max is only raised when a score
+//    exceeds it by more than 8, i.e. p <= 256), masking by selection so stale
+//    slots never enter the arithmetic, and V rows beyond the length zeroed in
+//    shared memory before the product (0 * NaN would not be 0).
+//  * the new token: in the tile that holds slot L the owning warp writes
+//    k_new / v_new into the ring slot of row L (the TMA copy of the stale
+//    cache row is discarded) and stores them into the cache at slot L. The
+//    copy of that tile has landed before the store, and no other CTA loads
+//    slot L, so the append cannot race with a read.
+//  * at the end of each unit segment the four warp states are merged in
+//    shared memory and either the normalised output or a partial state for
+//    the combine kernel is written.
+// Every mbarrier wait is bounded. A wait that gives up sets GQA_STATUS_TIMEOUT
+// and a CTA-wide abort flag: the producer stops issuing and waits (bounded)
+// for its copies in flight; the consumer warps stop waiting and computing but
+// keep walking their tiles and taking part in every barrier, writing NaN.
+#include "gqa_common.cuh"
+#include "gqa_launch.h"
+
+namespace gqa {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kTile = 64;                        // slots per tile
+constexpr int kStages = 4;
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kHalfBytes = kTile * 128;          // one 64-element half of a tile
+constexpr int kStageBytes = 4 * kHalfBytes;      // K lo, K hi, V lo, V hi
+constexpr int kDynSmem = kStages * kStageBytes + 1024;
+constexpr int kGMax = 8;
+constexpr long long kWaitCycles = 4LL << 30;     // ~2 s at 2 GHz
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, int count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(bar), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+
+// Bounded wait; false when it gave up.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
+{
+    if (mbar_try(bar, parity))
+        return true;
+    const long long t0 = clock64();
+    while (!mbar_try(bar, parity)) {
+        if (clock64() - t0 > kWaitCycles)
+            return false;
+    }
+    return true;
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y, int z,
+                                            uint32_t bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4])
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4])
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+                 "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// bf16 pair (lo in the low half) rounded to nearest even.
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Byte offset, within one 64-element half, of 16-byte chunk c8 of row r
+// under the 128-byte swizzle (the half starts on a 1024-byte boundary).
+__device__ __forceinline__ uint32_t swz(int r, int c8) { return (uint32_t)(r * 128 + ((c8 ^ (r & 7)) << 4)); }
+
+struct Shared {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    int stage_bad[kStages];
+    int abort_flag;
+    long long sched[2 * kThreads + 8];
+    float m[kConsumerWarps][kGMax];
+    float l[kConsumerWarps][kGMax];
+    float o[kConsumerWarps][kGMax][kD];
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap mk,
+                     const __grid_constant__ CUtensorMap mv)
+{
+    extern __shared__ uint8_t dyn_smem[];
+    __shared__ Shared sh;
+    uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
+    const uint32_t ring_u32 = smem_u32(ring);
+
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_u32(&sh.full[s]), 1);
+            mbar_init(smem_u32(&sh.empty[s]), kConsumerWarps);
+            sh.stage_bad[s] = 0;
+        }
+        sh.abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    // Let the combine grid get scheduled now; it waits for this grid's end.
+    asm volatile("griddepcontrol.launch_dependents;");
+    const TileCursor start = schedule_start(p, sh.sched);   // contains __syncthreads
+
+    const int G = p.G;
+    const __nv_bfloat16 *knew = static_cast<const __nv_bfloat16 *>(p.k_new);
+    const __nv_bfloat16 *vnew = static_cast<const __nv_bfloat16 *>(p.v_new);
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------ producer --
+        uint64_t policy;
+        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+        TileCursor cur = start;
+        int stage = 0;
+        uint32_t phase = 0;
+        const int bs = p.block_size;
+        const int nblk = p.paged ? (bs < kTile ? kTile / bs : 1) : 1;  // copies per half per tile
+        const int box_rows = p.paged ? (bs < kTile ? bs : kTile) : kTile;
+        int issued = 0;
+        while (cur.g < cur.end) {
+            if (*((volatile int *)&sh.abort_flag))
+                break;
+            if (!mbar_wait(smem_u32(&sh.empty[stage]), phase ^ 1)) {
+                if (lane == 0) {
+                    report(p, kTimeout);
+                    atomicExch(&sh.abort_flag, 1);
+                }
+                break;
+            }
+            const int b = cur.b, kvh = cur.kvh, L = cur.L;
+            const int slot0 = cur.t * kTile;
+            const bool good = row_ok(p, b, L);
+            // which rows of the tile to copy, and from where
+            int z = -1, y = 0;
+            bool bad_entry = false;
+            if (good) {
+                if (!p.paged) {
+                    if (lane == 0) {
+                        const int r = p.slot_ids ? __ldg(p.slot_ids + b) : b;
+                        z = r * p.Hkv + kvh;
+                        y = slot0;
+                    }
+                } else if (lane < nblk) {
+                    const int s = slot0 + lane * box_rows;  // first slot this lane copies
+                    if (s <= L) {
+                        const int e = __ldg(p.block_table + (long long)b * p.max_blocks + s / bs);
+                        if (e >= 0 && e < p.num_blocks) {
+                            z = e * p.Hkv + kvh;
+                            y = s % bs;
+                        } else {
+                            bad_entry = true;
+                        }
+                    }
+                }
+            }
+            const unsigned copying = __ballot_sync(0xffffffffu, z >= 0);
+            const bool any_bad = __any_sync(0xffffffffu, bad_entry);
+            const uint32_t bytes = (uint32_t)__popc(copying) * 4u * (uint32_t)box_rows * 128u;
+            const uint32_t fb = smem_u32(&sh.full[stage]);
+            if (lane == 0) {
+                sh.stage_bad[stage] = any_bad ? 1 : 0;
+                mbar_arrive_tx(fb, bytes);
+            }
+            __syncwarp();
+            if (z >= 0) {
+                const uint32_t dst = ring_u32 + stage * kStageBytes + lane * box_rows * 128;
+                tma_load_3d(dst, &mk, 0, y, z, fb, policy);
+                tma_load_3d(dst + kHalfBytes, &mk, 64, y, z, fb, policy);
+                tma_load_3d(dst + 2 * kHalfBytes, &mv, 0, y, z, fb, policy);
+                tma_load_3d(dst + 3 * kHalfBytes, &mv, 64, y, z, fb, policy);
+            }
+            ++issued;
+            advance(p, cur);
+            if (++stage == kStages) {
+                stage = 0;
+                phase ^= 1;
+            }
+        }
+        // Abort path only: let every copy still in flight land before exit.
+        if (*((volatile int *)&sh.abort_flag)) {
+            int s = stage, ph = phase;
+            for (int k = 0; k < kStages && k < issued; ++k) {
+                if (--s < 0) {
+                    s = kStages - 1;
+                    ph ^= 1;
+                }
+                mbar_wait(smem_u32(&sh.full[s]), ph);
+            }
+        }
+        return;
+    }
+
+    // -------------------------------------------------------- consumers --
+    const int g0 = lane >> 2, q4 = lane & 3;
+    const int row0 = warp * 16;          // this warp's 16 rows of every tile
+    TileCursor cur = start;
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t qa[8][2];                   // Q fragments (rows g0 < G), 8 k-steps
+    float acc_o[16][4];                  // O: 16 n-tiles of 8 dims, rows g0 (hi) and g0+8 (lo)
+    float m_run = -INFINITY, l_run = 0.f;
+    int seg_first_t = 0;
+    bool seg_start = true, row_good = true, aborted = false;
+    int seg_bad = 0;
+
+    while (cur.g < cur.end) {
+        const int b = cur.b, kvh = cur.kvh, L = cur.L;
+        if (seg_start) {
+            seg_first_t = cur.t;
+            row_good = row_ok(p, b, L);
+            if (!row_good && tid == 0 && cur.t == 0 && kvh == 0)
+                report(p, row_error_bits(p, b, L));
+            const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
+                static_cast<const __nv_bfloat16 *>(p.q) + ((long long)b * p.Hq + kvh * G + g0) * kD);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                qa[ks][0] = (g0 < G) ? __ldg(qrow + ks * 8 + q4) : 0u;       // dims 16ks + 2q4, +1
+                qa[ks][1] = (g0 < G) ? __ldg(qrow + ks * 8 + 4 + q4) : 0u;   // dims 16ks + 8 + 2q4, +1
+            }
+#pragma unroll
+            for (int n = 0; n < 16; ++n)
+                acc_o[n][0] = acc_o[n][1] = acc_o[n][2] = acc_o[n][3] = 0.f;
+            m_run = -INFINITY;
+            l_run = 0.f;
+            seg_bad = 0;
+            seg_start = false;
+        }
+
+        // After an abort every warp keeps walking its tiles and taking part in
+        // every barrier, but waits for and computes nothing (outputs NaN).
+        bool have = false;
+        if (!aborted && !*((volatile int *)&sh.abort_flag)) {
+            have = mbar_wait(smem_u32(&sh.full[stage]), phase);
+            if (!have && lane == 0) {
+                report(p, kTimeout);
+                atomicExch(&sh.abort_flag, 1);
+            }
+        }
+        aborted = aborted || !have;
+        seg_bad |= aborted ? 1 : 0;
+
+        const int slot0 = cur.t * kTile;
+        const uint32_t kbase = ring_u32 + stage * kStageBytes;
+        const uint32_t vbase = kbase + 2 * kHalfBytes;
+        uint8_t *vring = ring + stage * kStageBytes + 2 * kHalfBytes;
+        uint8_t *kring = ring + stage * kStageBytes;
+        const int tile_bad = have ? sh.stage_bad[stage] : 1;
+        seg_bad |= tile_bad;
+
+        if (have && row_good && !tile_bad) {
+            const bool last_tile = (cur.t == cur.nt - 1);
+            if (last_tile) {
+                // rows of this warp beyond L: zero V; row L: the new token
+                const int lr = L - slot0;            // 0..63
+                if (lr >= row0 && lr < row0 + 16) {
+                    const long long nidx = ((long long)b * p.Hkv + kvh) * kD;
+                    const int c = lane & 15;          // 16-byte chunk of the row
+                    const int half = c >> 3, c8 = c & 7;
+                    const uint4 *src = reinterpret_cast<const uint4 *>((lane < 16 ? knew : vnew) + nidx) + c;
+                    const uint4 v = __ldg(src);
+                    uint8_t *dst = (lane < 16 ? kring : vring) + half * kHalfBytes + swz(lr, c8);
+                    *reinterpret_cast<uint4 *>(dst) = v;
+                    // the in-place append
+                    const long long off = slot_offset(p, b, kvh, L);
+                    if (off >= 0) {
+                        __nv_bfloat16 *cache = static_cast<__nv_bfloat16 *>(lane < 16 ? p.k_cache : p.v_cache);
+                        reinterpret_cast<uint4 *>(cache + off)[c] = v;
+                    }
+                }
+                for (int r = row0 + (lane >> 4); r < row0 + 16; r += 2) {
+                    if (r > lr) {
+                        const int c = lane & 15;
+                        *reinterpret_cast<uint4 *>(vring + (c >> 3) * kHalfBytes + swz(r, c & 7)) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+                __syncwarp();
+            }
+
+            // ---- S = Q K^T for this warp's 16 slots (two n-tiles of 8)
+            float s_acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            {
+                const int mi = lane >> 3, ri = lane & 7;
+                const int r = row0 + 8 * (mi >> 1) + ri;
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const int c = 2 * ks + (mi & 1);
+                    uint32_t kb[4];
+                    ldsm_x4(kbase + (c >> 3) * kHalfBytes + swz(r, c & 7), kb);
+                    mma_bf16(s_acc[0], qa[ks][0], 0u, qa[ks][1], 0u, kb[0], kb[1]);
+                    mma_bf16(s_acc[1], qa[ks][0], 0u, qa[ks][1], 0u, kb[2], kb[3]);
+                }
+            }
+            // ---- masked online softmax (base 2), rows g0
+            float x[2][2];
+            float mx = -INFINITY;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int j = slot0 + row0 + 8 * nt + 2 * q4 + e;
+                    x[nt][e] = (j <= L) ? s_acc[nt][e] * p.scale_log2 : -INFINITY;
+                    mx = fmaxf(mx, x[nt][e]);
+                }
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            if (mx > m_run + 8.f) {          // raise the running max (also from -inf)
+                const float alpha = (m_run == -INFINITY) ? 0.f : ex2(m_run - mx);
+                l_run *= alpha;
+#pragma unroll
+                for (int n = 0; n < 16; ++n) {
+                    acc_o[n][0] *= alpha;
+                    acc_o[n][1] *= alpha;
+                    acc_o[n][2] *= alpha;
+                    acc_o[n][3] *= alpha;
+                }
+                m_run = mx;
+            }
+            uint32_t pa[4];
+            {
+                float pr[2][2];
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        pr[nt][e] = (x[nt][e] == -INFINITY) ? 0.f : ex2(x[nt][e] - m_run);
+                        l_run += pr[nt][e];
+                    }
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const uint32_t hi = pack_bf16(pr[nt][0], pr[nt][1]);
+                    const float h0 = __uint_as_float(hi << 16), h1 = __uint_as_float(hi & 0xffff0000u);
+                    const uint32_t lo = pack_bf16(pr[nt][0] - h0, pr[nt][1] - h1);
+                    pa[2 * nt] = hi;      // rows g0:   slots 8nt + 2q4, +1
+                    pa[2 * nt + 1] = lo;  // rows g0+8
+                }
+            }
+            // ---- O += P V (16 n-tiles of 8 dims)
+            {
+                const int mi = lane >> 3, ri = lane & 7;
+                const int r = row0 + 8 * (mi & 1) + ri;
+#pragma unroll
+                for (int np = 0; np < 8; ++np) {
+                    const int c = 2 * np + (mi >> 1);
+                    uint32_t vb[4];
+                    ldsm_x4_t(vbase + (c >> 3) * kHalfBytes + swz(r, c & 7), vb);
+                    mma_bf16(acc_o[2 * np], pa[0], pa[1], pa[2], pa[3], vb[0], vb[1]);
+                    mma_bf16(acc_o[2 * np + 1], pa[0], pa[1], pa[2], pa[3], vb[2], vb[3]);
+                }
+            }
+            if (last_tile)
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        }
+        __syncwarp();
+        if (lane == 0 && have)
+            mbar_arrive(smem_u32(&sh.empty[stage]));
+        if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+        }
+
+        const bool unit_done = (cur.t == cur.nt - 1);
+        const bool cta_done = (cur.g + 1 == cur.end);
+        if (unit_done || cta_done) {
+            // ---- merge the four warps' states and emit
+            float l_tot = l_run;
+            l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 1);
+            l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 2);
+            if (g0 < G) {
+                if (q4 == 0) {
+                    sh.m[warp][g0] = m_run;
+                    sh.l[warp][g0] = l_tot;
+                }
+#pragma unroll
+                for (int n = 0; n < 16; ++n) {
+                    sh.o[warp][g0][8 * n + 2 * q4] = acc_o[n][0] + acc_o[n][2];
+                    sh.o[warp][g0][8 * n + 2 * q4 + 1] = acc_o[n][1] + acc_o[n][3];
+                }
+            }
+            asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+            const bool whole = (seg_first_t == 0) && unit_done;
+            const bool bad = !row_good || seg_bad;
+            if (bad && row_good && tid == 0)
+                report(p, kBadBlock);
+            const int u = b * p.Hkv + kvh;
+            const long long P = (long long)u + blockIdx.x;
+            const float qnan = __int_as_float(0x7fc00000);
+            for (int idx = tid; idx < G * kD; idx += kConsumerWarps * 32) {
+                const int g = idx / kD, d = idx % kD;
+                float M = -INFINITY;
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w)
+                    M = fmaxf(M, sh.m[w][g]);
+                float num = 0.f, den = 0.f;
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w) {
+                    const float a = (sh.m[w][g] == -INFINITY) ? 0.f : ex2(sh.m[w][g] - M);
+                    num = fmaf(a, sh.o[w][g][d], num);
+                    den = fmaf(a, sh.l[w][g], den);
+                }
+                if (whole) {
+                    p.out[((long long)b * p.Hq + kvh * G + g) * kD + d] = bad ? qnan : num / den;
+                } else {
+                    p.ws_o[(P * G + g) * kD + d] = bad ? qnan : num;
+                    if (d == 0) {
+                        p.ws_ml[(P * G + g) * 2 + 0] = bad ? qnan : M;
+                        p.ws_ml[(P * G + g) * 2 + 1] = bad ? qnan : den;
+                    }
+                }
+            }
+            asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+            seg_start = true;
+        }
+        advance(p, cur);
+    }
+}
+
+}  // namespace
+
+bool tc_supports(bool bf16, int D, int G, bool paged, int block_size)
+{
+    if (!bf16 || D != kD || G < 1 || G > kGMax)
+        return false;
+    if (paged) {
+        // blocks land on 1024-byte boundaries of the swizzled ring
+        if (block_size < 8 || (block_size & (block_size - 1)))
+            return false;
+    }
+    return true;
+}
+
+int tc_tile() { return kTile; }
+int tc_ctas_per_sm() { return 1; }
+size_t tc_smem_bytes() { return kDynSmem + sizeof(Shared); }
+
+cudaError_t tc_launch(const DecodeParams &p, const TcMaps &maps, cudaStream_t st)
+{
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(tc_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem);
+        if (e != cudaSuccess)
+            return e;
+        attr_set = true;
+    }
+    tc_decode_kernel<<<p.grid, kThreads, kDynSmem, st>>>(p, maps.k, maps.v);
+    return cudaGetLastError();
+}
+
+}  // namespace gqa

@@ -1,0 +1,207 @@
+/*
+ * gqa_decode.h — C ABI of the GB300 grouped-query-attention decode step.
+ *
+ * One decode step, for every batch row b of a batch of B sequences:
+ *
+ *   1. append: the new key and value of cache head kvh, k_new[b][kvh] and
+ *      v_new[b][kvh], are written IN PLACE into slot lengths[b] of the row's
+ *      cache ("groupQueryAttention", clika runtime: binding the present
+ *      outputs to the past buffers appends in place, the decode perf path;
+ *      "KV cache decode step", tensortonic: the new token takes position S
+ *      after the S cached ones);
+ *   2. attend: query head h (G = Hq/Hkv, cache head kvh = floor(h/G), the
+ *      contiguous grouping of "Grouped-Query Decode Step", tensortonic,
+ *      statement) scores slots j = 0..lengths[b] with s_j = q.K_j / sqrt(D),
+ *      takes the softmax over those slots only (stale slots beyond the length
+ *      get exactly zero weight, same page, statement and Requirements) and
+ *      returns o = sum_j w_j V_j in float32.
+ *
+ * Scores, softmax and the weighted sum are computed in float32 from float32
+ * or bfloat16 data ("Grouped-Query Decode Step", Requirements).
+ *
+ * Conventions for every entry point:
+ *  - Pointers marked (device) point to GPU memory of the current device;
+ *    (host) to host memory. The library never allocates, frees or keeps any
+ *    of them; the caller owns every buffer, including the workspace
+ *    (the two-phase size-query-then-execute pattern of "aclnnMlaPrologV3
+ *    WeightNz", CANN, calling sequence).
+ *  - Tensors are dense and row-major in the shapes given; device pointers
+ *    must be 16-byte aligned.
+ *  - `stream` is a cudaStream_t (NULL: the legacy default stream). Calls are
+ *    asynchronous on it unless stated otherwise.
+ *  - Argument errors that the host can see (null pointers, shapes, dtype,
+ *    workspace too small, unsupported sizes) return an error code before
+ *    anything is launched, and nothing is written.
+ *  - Content errors that only the device can see (a length out of range, a
+ *    slot id out of range, a block-table entry out of range or -1 where a
+ *    slot is needed) never fault: the affected batch row gets NaN outputs,
+ *    its append is skipped when the append slot itself cannot be addressed,
+ *    and a bit is OR-ed into *d_status (if d_status is not NULL).
+ *    *d_status is sticky: the library never clears it. gqa_validate checks
+ *    content completely (including duplicates) and synchronously.
+ *  - B = 0 is valid: nothing is launched and GQA_OK is returned (empty
+ *    tensors, "aclnnMlaPrologV3WeightNz", shape restrictions).
+ *  - Results are deterministic: the same inputs and launch configuration give
+ *    the same bits (no floating-point atomics).
+ */
+#ifndef GQA_DECODE_H
+#define GQA_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gqa_status {
+    GQA_OK = 0,
+    GQA_ERR_INVALID_ARGUMENT = 1, /* bad shape/pointer/content (validate)      */
+    GQA_ERR_UNSUPPORTED = 2,      /* a size this build has no kernel for       */
+    GQA_ERR_CUDA = 3,             /* a CUDA runtime call failed                */
+    GQA_ERR_WORKSPACE = 4         /* workspace NULL or smaller than required   */
+} gqa_status;
+
+typedef enum gqa_dtype {
+    GQA_DTYPE_F32 = 0,  /* q, k_new, v_new and the cache in float32  */
+    GQA_DTYPE_BF16 = 1  /* q, k_new, v_new and the cache in bfloat16 */
+} gqa_dtype;
+
+/* Bits OR-ed into *d_status by the kernels. */
+enum {
+    GQA_STATUS_BAD_LENGTH = 1,      /* lengths[b] < 0 or beyond the row's capacity       */
+    GQA_STATUS_BAD_SLOT_ID = 2,     /* slot_ids[b] outside [0, R)                        */
+    GQA_STATUS_BAD_BLOCK = 4,       /* block-table entry outside [0, num_blocks) or -1
+                                       where a slot 0..lengths[b] lives                   */
+    GQA_STATUS_TIMEOUT = 8          /* a bounded on-chip wait gave up (never expected)    */
+};
+
+/* Kernel choice for the *_ex entry points. */
+typedef enum gqa_kernel {
+    GQA_KERNEL_AUTO = 0, /* the fastest kernel that supports the shapes                  */
+    GQA_KERNEL_SIMT = 1, /* CUDA-core FMA kernel: any D in {1,2,4,...,256}, G <= 8,
+                            float32 or bfloat16, any block size                          */
+    GQA_KERNEL_TC = 2    /* TMA ring + tensor-core kernel: bfloat16, D = 128, G <= 8,
+                            block size a power of two >= 8                               */
+} gqa_kernel;
+
+/* Launch options (all zero = defaults). */
+typedef struct gqa_options {
+    int kernel;     /* a gqa_kernel                                                      */
+    int grid_ctas;  /* 0: one persistent wave sized to the device; > 0: exactly this
+                       many CTAs (each takes a contiguous share of the KV tiles; any
+                       value gives the same output up to float32 rounding)             */
+    int reserved[6];
+} gqa_options;
+
+/* Human-readable name of a status code (static storage). */
+const char *gqa_status_string(gqa_status s);
+
+/*
+ * Workspace bytes a decode step needs on the current device for these sizes
+ * (float32 partial softmax states of the split sequences plus a small
+ * schedule table). opt may be NULL. Returns 0 for invalid sizes.
+ */
+size_t gqa_workspace_bytes(int B, int Hq, int Hkv, int D, gqa_dtype dt, const gqa_options *opt);
+
+/*
+ * Dense or continuous-batch decode step.
+ *
+ *  q        (device) (B, Hq, D)          query of the new token
+ *  k_new    (device) (B, Hkv, D)         new key   (appended at lengths[b])
+ *  v_new    (device) (B, Hkv, D)         new value (appended at lengths[b])
+ *  k_cache  (device) (R, Hkv, Smax, D)   key cache, written at one slot per (row, kvh)
+ *  v_cache  (device) (R, Hkv, Smax, D)   value cache, same
+ *  lengths  (device) (B,) int32          append slot = number of cached tokens of
+ *                                        row b; 0 <= lengths[b] <= Smax-1. Not modified:
+ *                                        the caller advances it.
+ *  slot_ids (device) (B,) int32 or NULL  cache row of batch row b on a continuous
+ *                                        [max_seqs = R, Hkv, Smax, D] cache: entries in
+ *                                        [0, R), pairwise distinct ("groupQueryAttention",
+ *                                        slot_ids). NULL: row b uses cache row b (R >= B).
+ *  out      (device) (B, Hq, D) float32  attention output
+ *  workspace(device) >= gqa_workspace_bytes(...) bytes, 256-byte aligned
+ *  d_status (device) int32 or NULL       sticky content-error bits (see above)
+ */
+gqa_status gqa_decode_step(const void *q, const void *k_new, const void *v_new,
+                           void *k_cache, void *v_cache, const int32_t *lengths,
+                           const int32_t *slot_ids, float *out,
+                           int B, int Hq, int Hkv, int D, int R, int Smax, gqa_dtype dt,
+                           void *workspace, size_t workspace_bytes, int32_t *d_status,
+                           void *stream);
+
+/*
+ * Paged decode step. The cache is a pool of blocks; slot s of batch row b
+ * lives in block block_table[b][s / block_size] at offset s % block_size.
+ *
+ *  k_blocks    (device) (num_blocks, Hkv, block_size, D)
+ *  v_blocks    (device) (num_blocks, Hkv, block_size, D)
+ *  block_table (device) (B, max_blocks) int32: each entry -1 (unused tail pad) or
+ *              a block in [0, num_blocks), no block twice in one row
+ *              ("groupQueryAttention", paged block table); the entries holding
+ *              slots 0..lengths[b] must be real blocks. A block named by two rows
+ *              that receives this step's append is undefined (the pages leave it open).
+ *  lengths     (device) (B,) int32, 0 <= lengths[b] < max_blocks * block_size.
+ * Other arguments as in gqa_decode_step (there are no slot_ids: the block
+ * table is the row map).
+ */
+gqa_status gqa_decode_step_paged(const void *q, const void *k_new, const void *v_new,
+                                 void *k_blocks, void *v_blocks, const int32_t *block_table,
+                                 const int32_t *lengths, float *out,
+                                 int B, int Hq, int Hkv, int D,
+                                 int num_blocks, int block_size, int max_blocks, gqa_dtype dt,
+                                 void *workspace, size_t workspace_bytes, int32_t *d_status,
+                                 void *stream);
+
+/* The same two steps with launch options (kernel choice, CTA count). */
+gqa_status gqa_decode_step_ex(const void *q, const void *k_new, const void *v_new,
+                              void *k_cache, void *v_cache, const int32_t *lengths,
+                              const int32_t *slot_ids, float *out,
+                              int B, int Hq, int Hkv, int D, int R, int Smax, gqa_dtype dt,
+                              void *workspace, size_t workspace_bytes, int32_t *d_status,
+                              void *stream, const gqa_options *opt);
+
+gqa_status gqa_decode_step_paged_ex(const void *q, const void *k_new, const void *v_new,
+                                    void *k_blocks, void *v_blocks, const int32_t *block_table,
+                                    const int32_t *lengths, float *out,
+                                    int B, int Hq, int Hkv, int D,
+                                    int num_blocks, int block_size, int max_blocks, gqa_dtype dt,
+                                    void *workspace, size_t workspace_bytes, int32_t *d_status,
+                                    void *stream, const gqa_options *opt);
+
+/*
+ * Content validation, complete and SYNCHRONOUS (it waits for `stream`):
+ * lengths in range; slot_ids in range and distinct; every block-table entry
+ * -1 or in range, no repeats within a row, real blocks for slots
+ * 0..lengths[b] ("groupQueryAttention": the table is validated whole before
+ * any read). Pass block_table = NULL for the dense / slot_ids form (then
+ * num_blocks, block_size and max_blocks are ignored) and slot_ids = NULL for
+ * the plain dense form; with a block table, slot_ids, R and Smax are ignored.
+ * Runs on the GPU; d_result (device) is one int32 of caller memory that the
+ * call overwrites. Returns GQA_OK or GQA_ERR_INVALID_ARGUMENT (or an error of
+ * the call itself).
+ */
+gqa_status gqa_validate(const int32_t *lengths, const int32_t *slot_ids,
+                        const int32_t *block_table, int B, int R, int Smax,
+                        int num_blocks, int block_size, int max_blocks,
+                        int32_t *d_result, void *stream);
+
+/*
+ * Kernel timing trace. When enabled, every decode call records CUDA events
+ * around each kernel it launches; gqa_trace_collect waits for them and
+ * returns, per kernel kind, the launches and total milliseconds since the
+ * previous collect. Kinds: 0 = SIMT decode, 1 = tensor-core decode,
+ * 2 = split combine. Not thread-safe; meant for benchmarks.
+ */
+int gqa_trace_enable(int on);
+gqa_status gqa_trace_collect(int n_kinds, int64_t *launches, double *ms);
+const char *gqa_kernel_name(int kind);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int gqa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_DECODE_H */

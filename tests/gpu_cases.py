@@ -1,0 +1,169 @@
+"""Shared driver for the GPU parity tests: run one decode step through the
+library (C ABI, via the Python binding) and the same step through the CPU
+oracle on identical seeded inputs, then compare.
+
+Bars (the decode step's stated accuracy):
+  * append and addressing: bit-exact, the whole cache compared;
+  * float32 data: max |out - oracle| <= 1e-5;
+  * bfloat16 data: max |out - oracle| <= 2e-2 * max|V| over the attended
+    values, the oracle running on the same bf16 bits.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import workloads as W
+from helpers import to_np
+
+F32_TOL = 1e-5
+BF16_REL_TOL = 2e-2
+
+
+def tolerance(w: W.Workload, vmax: float) -> float:
+    return F32_TOL if w.dtype == "f32" else BF16_REL_TOL * vmax
+
+
+def make_inputs(w: W.Workload, on_gpu_generation: bool = False):
+    """Inputs on cuda:0. Small cases are drawn on the CPU and copied (so the
+    oracle sees the very same values); large ones are drawn on the GPU."""
+    if on_gpu_generation:
+        return W.generate(w, "cuda")
+    t = W.generate(w, "cpu")
+    return {k: v.cuda() for k, v in t.items()}
+
+
+def _sample_rows(w, rows):
+    return list(range(w.B)) if rows is None else sorted(set(int(r) for r in rows))
+
+
+def host_problem(w: W.Workload, t: dict, rows=None):
+    """Host copies of what the oracle needs for batch rows `rows` (all when
+    None), taken BEFORE the GPU step runs. Dense/slot_ids: the rows' cache
+    rows become a compact cache addressed by slot_ids 0..n-1. Paged: the rows'
+    blocks become a compact block pool with a renumbered table. Returns
+    (problem dict, mapping back to the original storage)."""
+    rows = _sample_rows(w, rows)
+    sel = torch.tensor(rows, dtype=torch.long, device=t["q"].device)
+    prob = {"q": to_np(t["q"][sel]), "k_new": to_np(t["k_new"][sel]), "v_new": to_np(t["v_new"][sel]),
+            "lengths": to_np(t["lengths"][sel]), "rows": rows}
+    if w.paged:
+        bt = t["block_table"][sel].cpu().numpy()
+        used = sorted(set(int(x) for x in bt[bt >= 0].tolist()))
+        remap = {blk: i for i, blk in enumerate(used)}
+        idx = torch.tensor(used, dtype=torch.long, device=t["q"].device)
+        prob["k_blocks"] = to_np(t["k_blocks"][idx])
+        prob["v_blocks"] = to_np(t["v_blocks"][idx])
+        prob["block_table"] = np.vectorize(lambda x: remap.get(int(x), -1))(bt).astype(np.int32) \
+            if bt.size else bt.astype(np.int32)
+        prob["blocks"] = used
+        return prob
+    cache_rows = (t["slot_ids"][sel].long() if "slot_ids" in t else sel)
+    prob["k_cache"] = to_np(t["k_cache"][cache_rows])
+    prob["v_cache"] = to_np(t["v_cache"][cache_rows])
+    prob["cache_rows"] = cache_rows.cpu().tolist()
+    return prob
+
+
+def run_oracle(w: W.Workload, prob: dict):
+    """Oracle on the host problem (appends into the host copies)."""
+    if w.paged:
+        r = oracle.decode_paged(prob["q"], prob["k_new"], prob["v_new"], prob["k_blocks"],
+                                prob["v_blocks"], prob["block_table"], prob["lengths"])
+    else:
+        r = oracle.decode_dense(prob["q"], prob["k_new"], prob["v_new"], prob["k_cache"],
+                                prob["v_cache"], prob["lengths"])
+    assert r.status == oracle.OK
+    return r.out
+
+
+def run_gpu(w: W.Workload, t: dict, kernel="auto", grid_ctas=0, status=None):
+    import gqa_kv_cache_gb300 as gqa
+    if w.paged:
+        return gqa.decode_step_paged(t["q"], t["k_new"], t["v_new"], t["k_blocks"], t["v_blocks"],
+                                     t["block_table"], t["lengths"], kernel=kernel,
+                                     grid_ctas=grid_ctas, status=status)
+    return gqa.decode_step(t["q"], t["k_new"], t["v_new"], t["k_cache"], t["v_cache"], t["lengths"],
+                           t.get("slot_ids"), kernel=kernel, grid_ctas=grid_ctas, status=status)
+
+
+def attended_vmax(prob: dict) -> float:
+    """max |V| over the values the step attends (valid slots and the new one)."""
+    vals = [np.abs(_as_float(prob["v_new"])).max()]
+    L = prob["lengths"]
+    if "k_blocks" in prob:
+        vb = _as_float(prob["v_blocks"])
+        bs = vb.shape[2]
+        for i in range(len(L)):
+            for s in range(int(L[i])):
+                vals.append(np.abs(vb[prob["block_table"][i, s // bs], :, s % bs]).max())
+    else:
+        vc = _as_float(prob["v_cache"])
+        for i in range(len(L)):
+            if L[i] > 0:
+                vals.append(np.abs(vc[i, :, :L[i]]).max())
+    return float(max(vals))
+
+
+def _as_float(a):
+    if a.dtype == np.uint16:
+        return (a.astype(np.uint32) << 16).view(np.float32)
+    return a
+
+
+def check_step(w: W.Workload, kernel="auto", grid_ctas=0, rows=None, gpu_gen=False,
+               full_cache_check=True):
+    """Runs one step on the GPU and compares with the oracle. Returns
+    (max abs error, tolerance, gpu out) for the compared rows."""
+    t = make_inputs(w, gpu_gen)
+    if rows == "sample4":   # first, last, longest and one random batch row
+        L = t["lengths"]
+        rows = [0, w.B - 1, int(torch.argmax(L).item()),
+                int(np.random.default_rng(w.seed).integers(0, w.B))]
+    prob = host_problem(w, t, rows)
+    names = ("k_blocks", "v_blocks") if w.paged else ("k_cache", "v_cache")
+    before = {n: t[n].clone() for n in names} if full_cache_check else None
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = run_gpu(w, t, kernel, grid_ctas, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    want = run_oracle(w, prob)
+    sel = prob["rows"]
+    got = out[torch.tensor(sel, device="cuda")].double().cpu().numpy()
+    err = float(np.abs(got - want).max())
+    tol = tolerance(w, attended_vmax(prob))
+    assert np.isfinite(got).all()
+    # append / addressing: the GPU's post-step storage at the sampled rows
+    # equals the oracle's post-step host copies, bit for bit
+    if w.paged:
+        idx = torch.tensor(prob["blocks"], dtype=torch.long, device="cuda")
+        for n in names:
+            assert to_np(t[n][idx]).tobytes() == prob[n].tobytes(), f"{n} differs after the append"
+    else:
+        idx = torch.tensor(prob["cache_rows"], dtype=torch.long, device="cuda")
+        for n in names:
+            assert to_np(t[n][idx]).tobytes() == prob[n].tobytes(), f"{n} differs after the append"
+    if full_cache_check:
+        _check_whole_cache(w, t, before)
+    return err, tol, out
+
+
+def _check_whole_cache(w, t, before):
+    """Everywhere: post-step storage == pre-step storage with exactly the
+    append slots replaced by k_new / v_new (device-side comparison)."""
+    B = w.B
+    L = t["lengths"].long()
+    b = torch.arange(B, device="cuda")
+    for name, new in ((0, "k_new"), (1, "v_new")):
+        n = ("k_blocks", "v_blocks")[name] if w.paged else ("k_cache", "v_cache")[name]
+        exp = before[n]
+        if w.paged:
+            blk = t["block_table"][b, L // w.block_size].long()
+            exp[blk, :, L % w.block_size] = t[new]
+        else:
+            r = t["slot_ids"].long() if "slot_ids" in t else b
+            exp[r, :, L] = t[new]
+        assert torch.equal(exp.view(torch.int16) if exp.dtype == torch.bfloat16 else exp.view(torch.int32),
+                           t[n].view(torch.int16) if exp.dtype == torch.bfloat16 else t[n].view(torch.int32)), \
+            f"{n}: bytes outside the append slots changed, or the append is wrong"
