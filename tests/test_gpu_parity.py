@@ -212,7 +212,7 @@ def test_validate_matches_oracle_rules():
     import gqa_kv_cache_gb300 as gqa
     rng = np.random.default_rng(0)
     for trial in range(60):
-        B, nb, bs, mb = 3, 12, 4, 5
+        B, nb, bs, mb = 3, 16, 4, 5
         bt = rng.integers(-2, nb + 1, size=(B, mb)).astype(np.int32)
         if trial % 3 == 0:
             bt = rng.permutation(nb)[:B * mb].reshape(B, mb).astype(np.int32)
