@@ -23,6 +23,8 @@ SIGNATURES = {
     "gqa_trace_collect": (I, [I, P, P]),
     "gqa_kernel_name": (ctypes.c_char_p, [I]),
     "gqa_version": (I, []),
+    "gqa_noalloc_scratch_bytes": (Z, []),
+    "gqa_decode_step_noalloc": (I, [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P]),
 }
 
 

@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libgqa.so")
 BUILD = os.path.join(HERE, "_build")
-SOURCES = ["gqa_api.cu", "gqa_simt.cu", "gqa_tc.cu", "gqa_combine.cu"]
+SOURCES = ["gqa_api.cu", "gqa_simt.cu", "gqa_tc.cu", "gqa_combine.cu", "gqa_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

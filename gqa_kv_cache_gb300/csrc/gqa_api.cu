@@ -300,6 +300,7 @@ const char *gqa_status_string(gqa_status s)
     case GQA_ERR_UNSUPPORTED: return "unsupported sizes (no kernel in this build)";
     case GQA_ERR_CUDA: return "CUDA runtime error";
     case GQA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case GQA_ERR_TOO_LARGE: return "sizes need more scratch than gqa_decode_step_noalloc holds";
     }
     return "unknown status";
 }

@@ -59,7 +59,9 @@ typedef enum gqa_status {
     GQA_ERR_INVALID_ARGUMENT = 1, /* bad shape/pointer/content (validate)      */
     GQA_ERR_UNSUPPORTED = 2,      /* a size this build has no kernel for       */
     GQA_ERR_CUDA = 3,             /* a CUDA runtime call failed                */
-    GQA_ERR_WORKSPACE = 4         /* workspace NULL or smaller than required   */
+    GQA_ERR_WORKSPACE = 4,        /* workspace NULL or smaller than required   */
+    GQA_ERR_TOO_LARGE = 5         /* sizes need more than the fixed scratch of
+                                     gqa_decode_step_noalloc                   */
 } gqa_status;
 
 typedef enum gqa_dtype {
@@ -196,6 +198,29 @@ gqa_status gqa_validate(const int32_t *lengths, const int32_t *slot_ids,
 int gqa_trace_enable(int on);
 gqa_status gqa_trace_collect(int n_kinds, int64_t *launches, double *ms);
 const char *gqa_kernel_name(int kind);
+
+/*
+ * The dense / continuous-batch decode step without a workspace argument, for
+ * callers that cannot allocate device memory (for example a plugin host that
+ * gives an operator no scratch and forbids allocation while it runs, or a
+ * plain C caller without a device allocator). The pages have no counterpart:
+ * this is a deployment convenience.
+ *
+ * Arguments as in gqa_decode_step. The scratch is a fixed array of
+ * gqa_noalloc_scratch_bytes() (8 MiB) inside the library, held by every GPU
+ * that loads the library until the process exits; sizes whose workspace
+ * (gqa_workspace_bytes) exceeds it return GQA_ERR_TOO_LARGE before any launch.
+ * The call allocates nothing. The first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress) with that device current; make that
+ * first call before any stream capture. All calls share the array: calls whose
+ * kernels overlap on the GPU race and must be serialised by the caller.
+ */
+size_t gqa_noalloc_scratch_bytes(void);
+gqa_status gqa_decode_step_noalloc(const void *q, const void *k_new, const void *v_new,
+                                   void *k_cache, void *v_cache, const int32_t *lengths,
+                                   const int32_t *slot_ids, float *out,
+                                   int B, int Hq, int Hkv, int D, int R, int Smax, gqa_dtype dt,
+                                   int32_t *d_status, void *stream);
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 int gqa_version(void);
