@@ -64,9 +64,11 @@ _ws_cache: dict = {}
 
 
 def _workspace(device, nbytes):
+    """A per-device workspace, zero-filled when allocated; the library leaves
+    it zero-filled after every call, whatever the sizes."""
     buf = _ws_cache.get(device)
     if buf is None or buf.numel() < nbytes:
-        buf = torch.empty(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
+        buf = torch.zeros(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
         _ws_cache[device] = buf
     return buf
 
@@ -105,7 +107,9 @@ def _common_checks(q, k_new, v_new, caches, lengths, out):
 def decode_step(q, k_new, v_new, k_cache, v_cache, lengths, slot_ids=None, *, out=None,
                 status=None, kernel="auto", grid_ctas=0, workspace=None, stream=None):
     """One decode step on a dense (R, Hkv, Smax, D) cache (continuous batch
-    when ``slot_ids`` is given). Appends in place; returns ``out``."""
+    when ``slot_ids`` is given). Appends in place; returns ``out``. A
+    ``workspace`` passed in must be zero-filled before its first use (the
+    library leaves it zero-filled after every call)."""
     dt, out = _common_checks(q, k_new, v_new, (("k_cache", k_cache), ("v_cache", v_cache)),
                              lengths, out)
     B, Hq, D = q.shape
@@ -178,7 +182,7 @@ def trace_enable(on: bool = True) -> bool:
 def trace_collect() -> dict:
     """{kernel name: (launches, total ms)} since the previous collect."""
     lib = _lib.load()
-    n = 3
+    n = 2
     launches = (ctypes.c_int64 * n)()
     ms = (ctypes.c_double * n)()
     _check(lib.gqa_trace_collect(n, launches, ms), "gqa_trace_collect")

@@ -14,6 +14,7 @@ P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
 SIGNATURES = {
     "gqa_status_string": (ctypes.c_char_p, [I]),
     "gqa_workspace_bytes": (Z, [I, I, I, I, I, P]),
+    "gqa_workspace_reset": (I, [P, Z, P]),
     "gqa_decode_step": (I, [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, Z, P, P]),
     "gqa_decode_step_paged": (I, [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, P, Z, P, P]),
     "gqa_decode_step_ex": (I, [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, Z, P, P, P]),

@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libgqa.so")
 BUILD = os.path.join(HERE, "_build")
-SOURCES = ["gqa_api.cu", "gqa_simt.cu", "gqa_tc.cu", "gqa_combine.cu", "gqa_noalloc.cu"]
+SOURCES = ["gqa_api.cu", "gqa_simt.cu", "gqa_tc.cu", "gqa_validate.cu", "gqa_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -29,8 +29,9 @@ def nvcc() -> str:
 
 
 def _flags():
+    extra = os.environ.get("GQA_NVCC_FLAGS", "").split()   # e.g. -DGQA_TC_STAGES=4
     return ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
-                   "-I", INCLUDE, "-I", CSRC, "--expt-relaxed-constexpr"]
+                   "-I", INCLUDE, "-I", CSRC, "--expt-relaxed-constexpr", *extra]
 
 
 def _stale(out, deps):

@@ -28,8 +28,6 @@ int sm_count(int dev)
     return cache[dev];
 }
 
-bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
-
 // Kernel the call will use (GQA_KERNEL_SIMT / GQA_KERNEL_TC) or -1.
 int pick_kernel(const gqa_options *opt, gqa_dtype dt, int D, int G, bool paged, int block_size)
 {
@@ -251,8 +249,7 @@ gqa_status run_step(const Shape &s, const void *q, const void *k_new, const void
     p.tile = kernel == GQA_KERNEL_TC ? tc_tile() : simt_tile();
     p.grid = grid;
     char *w = static_cast<char *>(ws);
-    p.ws_total = reinterpret_cast<long long *>(w + lay.off_total);
-    p.ws_rowpre = reinterpret_cast<long long *>(w + lay.off_rowpre);
+    p.ws_cnt = reinterpret_cast<int *>(w + lay.off_cnt);
     p.ws_ml = reinterpret_cast<float *>(w + lay.off_ml);
     p.ws_o = reinterpret_cast<float *>(w + lay.off_o);
     p.status = d_status;
@@ -278,12 +275,6 @@ gqa_status run_step(const Shape &s, const void *q, const void *k_new, const void
     } else {
         TraceScope ts(0, cs);
         e = simt_launch(p, s.dt == GQA_DTYPE_BF16, cs);
-    }
-    if (e != cudaSuccess)
-        return GQA_ERR_CUDA;
-    {
-        TraceScope ts(2, cs);
-        e = combine_launch(p, cs, !trace().on);
     }
     return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
@@ -441,9 +432,17 @@ const char *gqa_kernel_name(int kind)
     switch (kind) {
     case 0: return "simt_decode_kernel";
     case 1: return "tc_decode_kernel";
-    case 2: return "combine_kernel";
     }
     return "unknown";
+}
+
+gqa_status gqa_workspace_reset(void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (!workspace)
+        return GQA_ERR_INVALID_ARGUMENT;
+    return cudaMemsetAsync(workspace, 0, workspace_bytes, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? GQA_OK
+               : GQA_ERR_CUDA;
 }
 
 int gqa_version(void) { return 100; }

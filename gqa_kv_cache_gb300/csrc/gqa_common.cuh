@@ -1,6 +1,6 @@
-// Device-side pieces shared by the decode kernels and the split combine:
-// launch parameters, the persistent tile schedule, the workspace layout and
-// small numeric helpers.
+// Device-side pieces shared by the decode kernels: launch parameters, the
+// persistent tile schedule, the in-kernel split merge, the workspace layout
+// and small numeric helpers.
 //
 // Work decomposition. A unit is one (batch row b, cache head kvh) pair; unit
 // u = b * Hkv + kvh. Its slots 0..L (L = lengths[b]; slot L is the new token)
@@ -9,10 +9,13 @@
 // a grid takes the contiguous range [floor(i N / C), floor((i+1) N / C)) with
 // C = min(grid size, N), so every working CTA owns at least one tile (CTAs
 // i >= C stay idle). Every CTA therefore streams the same number of KV bytes
-// (to within one tile), whatever the length mix. A unit whose tiles fall inside one CTA is
-// finished there (normalised output written directly); a unit cut by CTA
-// boundaries leaves one partial softmax state per CTA, (m, l, o[D]) per head,
-// and the combine kernel merges them (log-sum-exp merge). The partial of CTA
+// (to within one tile), whatever the length mix. A unit whose tiles fall
+// inside one CTA is finished there (normalised output written directly); a
+// unit cut by CTA boundaries leaves one partial softmax state per CTA,
+// (m, l, o[D]) per head, and the last of those CTAs to finish (an arrival
+// counter per unit in the workspace) merges them with the log-sum-exp rule,
+// then clears the partials and resets the counter: no second kernel is needed
+// and the workspace is zero-filled again after every call. The partial of CTA
 // i for unit u is stored at index u + i: along the (CTA, unit) pairs in
 // order, u + i grows by one or two at every step, so the index is unique and
 // fewer than B * Hkv + C partials exist.
@@ -46,17 +49,19 @@ struct DecodeParams {
     float scale_log2;  // log2(e) / sqrt(D): scores are kept in base-2 units
     int tile;          // T, slots per tile
     int grid;          // C, CTAs of the decode launch
-    // workspace
-    long long *ws_total;   // [1] N, written by CTA 0
-    long long *ws_rowpre;  // [B + 1] tiles before row b (all heads), written by CTA 0
-    float *ws_ml;          // [P][G][2] partial (m, l), base-2 max
-    float *ws_o;           // [P][G][D] partial unnormalised output
-    int32_t *status;       // sticky content-error bits, may be null
+    // workspace (zero-filled between calls)
+    int *ws_cnt;       // [B * Hkv] arrival counters
+    float *ws_ml;      // [P][G][2] partial (m, l), base-2 max
+    float *ws_o;       // [P][G][D] partial unnormalised output
+    int32_t *status;   // sticky content-error bits, may be null
 };
 
 // Workspace layout (bytes from the workspace base), shared by host and device.
+// The workspace is zero-filled before the first call and every call leaves it
+// zero-filled: the last CTA of a cut unit resets the unit's counter and clears
+// the partial states it merged.
 struct WorkspaceLayout {
-    size_t off_total, off_rowpre, off_ml, off_o, bytes;
+    size_t off_cnt, cnt_bytes, off_ml, off_o, bytes;
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -65,9 +70,9 @@ __host__ __device__ inline WorkspaceLayout workspace_layout(int B, int Hkv, int 
 {
     WorkspaceLayout w;
     const size_t P = (size_t)B * Hkv + (size_t)grid;
-    w.off_total = 0;
-    w.off_rowpre = 256;
-    w.off_ml = align_up(w.off_rowpre + sizeof(long long) * ((size_t)B + 1), 256);
+    w.off_cnt = 0;
+    w.cnt_bytes = align_up(sizeof(int) * (size_t)B * Hkv, 256);
+    w.off_ml = w.off_cnt + w.cnt_bytes;
     w.off_o = align_up(w.off_ml + sizeof(float) * P * G * 2, 256);
     w.bytes = align_up(w.off_o + sizeof(float) * P * G * D, 256);
     return w;
@@ -109,80 +114,124 @@ __device__ __forceinline__ void report(const DecodeParams &p, int bits)
 // Position of a CTA in the tile list.
 struct TileCursor {
     long long g;      // global tile index
-    long long end;    // one past this CTA's last tile
+    long long end;    // one past the last tile of the current range
+    long long N, C;   // tiles in the list, CTAs sharing them
     int b, kvh, t;    // current row, head, tile within the unit
     int nt;           // tiles per head of row b
     int L;            // lengths[b]
 };
 
-// Finds this CTA's first tile. Every thread of the block must call it (it
-// uses __syncthreads and `scratch`, >= 2 * blockDim.x + 8 long longs of shared
-// memory). CTA 0 also publishes the row prefix and the total to the workspace
-// for the combine kernel.
-__device__ inline TileCursor schedule_start(const DecodeParams &p, long long *scratch)
+// Cursor at global tile g, which lies in row b whose tiles start at `run`.
+__device__ __forceinline__ TileCursor cursor_at(const DecodeParams &p, int b, long long run, long long g,
+                                               long long end, long long N, long long C)
 {
-    const int nthr = blockDim.x, tid = threadIdx.x;
+    TileCursor c;
+    c.g = g;
+    c.end = end;
+    c.N = N;
+    c.C = C;
+    c.b = b;
+    c.L = __ldg(p.lengths + b);
+    c.nt = row_tiles(p, c.L);
+    const long long within = g - run;
+    c.kvh = (int)(within / c.nt);
+    c.t = (int)(within % c.nt);
+    return c;
+}
+
+// The order in which a CTA walks its tile range [begin, end): first the
+// segment that holds its last tile -- the head of a unit that usually
+// continues in the next CTA -- as range `a` = [split, end), then the rest as
+// range `b` = [begin, split). The units cut by CTA boundaries thus have all
+// their partial states written early in the kernel (the next CTA starts with
+// the same unit's tail), and the end of the kernel finishes whole units only.
+struct TileWalk {
+    TileCursor a, b;
+};
+
+// Every thread of the block must call it (it uses __syncthreads and
+// `scratch`, >= blockDim.x / 32 + 8 long longs of shared memory; blockDim.x a
+// multiple of 32). The row prefix is a block-wide scan of the per-row tile
+// counts, recomputed by every CTA from `lengths` (no host round trip).
+__device__ inline TileWalk schedule_walk(const DecodeParams &p, long long *scratch)
+{
+    const int nthr = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nwarps = nthr >> 5;
     const int chunk = (p.B + nthr - 1) / nthr;
     const int r0 = min(p.B, tid * chunk), r1 = min(p.B, r0 + chunk);
     long long local = 0;
     for (int b = r0; b < r1; ++b)
         local += (long long)p.Hkv * row_tiles(p, __ldg(p.lengths + b));
-    scratch[tid] = local;
-    __syncthreads();
-    // inclusive scan (Hillis-Steele) over the per-thread sums
-    long long *a = scratch, *c = scratch + nthr;
-    for (int off = 1; off < nthr; off <<= 1) {
-        long long v = a[tid] + (tid >= off ? a[tid - off] : 0);
-        __syncthreads();
-        c[tid] = v;
-        __syncthreads();
-        long long *tmp = a; a = c; c = tmp;
+    // inclusive scan: within the warp by shuffles, then over the warp totals
+    long long incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const long long v = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off)
+            incl += v;
     }
-    const long long incl = a[tid];
+    long long *wsum = scratch;              // [nwarps]
+    long long *found = scratch + nwarps;    // row of begin, its run; row of end-1, its run
+    if (lane == 31)
+        wsum[warp] = incl;
+    if (tid == 0)
+        found[0] = found[1] = found[2] = found[3] = 0;
+    __syncthreads();
+    long long before = 0, N = 0;
+    for (int w = 0; w < nwarps; ++w) {
+        const long long v = wsum[w];
+        before += (w < warp) ? v : 0;
+        N += v;
+    }
+    incl += before;
     const long long excl = incl - local;
-    const long long N = a[nthr - 1];
-    long long *found = scratch + 2 * nthr;  // [0] b, [1] tiles before b
     const long long C = working_ctas(N, p.grid);
     const long long begin = blockIdx.x < C ? (long long)blockIdx.x * N / C : N;
     const long long end = blockIdx.x < C ? ((long long)blockIdx.x + 1) * N / C : N;
-    if (tid == 0) {
-        found[0] = p.B;
-        found[1] = N;
-    }
-    __syncthreads();
-    long long run = excl;
-    for (int b = r0; b < r1; ++b) {
-        long long n = (long long)p.Hkv * row_tiles(p, __ldg(p.lengths + b));
-        if (blockIdx.x == 0)
-            p.ws_rowpre[b] = run;
-        if (begin >= run && begin < run + n) {
-            found[0] = b;
-            found[1] = run;
+    const long long last = end - 1;
+    if (begin < end && ((begin >= excl && begin < incl) || (last >= excl && last < incl))) {
+        long long run = excl;
+        for (int b = r0; b < r1; ++b) {
+            const long long n = (long long)p.Hkv * row_tiles(p, __ldg(p.lengths + b));
+            if (begin >= run && begin < run + n) {
+                found[0] = b;
+                found[1] = run;
+            }
+            if (last >= run && last < run + n) {
+                found[2] = b;
+                found[3] = run;
+            }
+            run += n;
         }
-        run += n;
-    }
-    if (blockIdx.x == 0 && tid == 0) {
-        p.ws_rowpre[p.B] = N;
-        p.ws_total[0] = N;
     }
     __syncthreads();
-    TileCursor cur;
-    cur.g = begin;
-    cur.end = end;
-    cur.b = (int)found[0];
-    cur.kvh = 0;
-    cur.t = 0;
-    cur.nt = 1;
-    cur.L = 0;
-    if (begin < end) {
-        cur.L = __ldg(p.lengths + cur.b);
-        cur.nt = row_tiles(p, cur.L);
-        long long within = begin - found[1];
-        cur.kvh = (int)(within / cur.nt);
-        cur.t = (int)(within % cur.nt);
+    TileWalk w;
+    if (begin >= end) {
+        TileCursor none;
+        none.g = none.end = N;
+        none.N = N;
+        none.C = C;
+        none.b = none.kvh = none.t = none.L = 0;
+        none.nt = 1;
+        w.a = w.b = none;
+    } else {
+        const TileCursor first = cursor_at(p, (int)found[0], found[1], begin, end, N, C);
+        const TileCursor tail = cursor_at(p, (int)found[2], found[3], last, end, N, C);
+        const long long unit_start = last - tail.t;
+        if (unit_start <= begin) {        // a single segment: walk it in order
+            w.a = first;
+            w.b = first;
+            w.b.g = w.b.end = end;
+        } else {
+            w.a = tail;
+            w.a.g = unit_start;
+            w.a.t = 0;
+            w.b = first;
+            w.b.end = unit_start;
+        }
     }
     __syncthreads();
-    return cur;
+    return w;
 }
 
 __device__ __forceinline__ void advance(const DecodeParams &p, TileCursor &c)
@@ -199,6 +248,21 @@ __device__ __forceinline__ void advance(const DecodeParams &p, TileCursor &c)
             }
         }
     }
+}
+
+// Next tile of the walk: along the current range, then from range a into
+// range b. False when the CTA has no tile left.
+__device__ __forceinline__ bool walk_next(const DecodeParams &p, TileCursor &c, const TileWalk &w, bool &in_b)
+{
+    advance(p, c);
+    if (c.g < c.end)
+        return true;
+    if (!in_b && w.b.g < w.b.end) {
+        c = w.b;
+        in_b = true;
+        return true;
+    }
+    return false;
 }
 
 // Row-level content check: length in range, slot id in range.
@@ -238,6 +302,163 @@ __device__ __forceinline__ long long slot_offset(const DecodeParams &p, int b, i
     if (blk < 0 || blk >= p.num_blocks)
         return -1;
     return (((long long)blk * p.Hkv + kvh) * p.block_size + s % p.block_size) * (long long)p.D;
+}
+
+__device__ __forceinline__ float fast_ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Shared-memory scratch of the in-kernel merge of a cut unit's partials.
+constexpr int kMergeMax = 32;   // partials merged through shared memory (more: direct loads)
+constexpr int kMergeG = 8;      // heads per unit (G <= 8)
+struct MergeBuf {
+    float w[kMergeMax * kMergeG];   // partial max, then its weight 2^(m_i - M)
+    float l[kMergeMax * kMergeG];
+    float inv_den[kMergeG];
+};
+
+// End of a unit segment. The NW per-warp states of the segment are in shared
+// memory: sm_m[w][g] (base-2 running max, -inf for a warp that saw no slot),
+// sm_l[w][g], sm_o[w][g][d]. All `nthr` calling threads take part; `sync`
+// synchronises exactly them. A whole unit writes its normalised output. A cut
+// unit writes its partial state, then takes an arrival ticket; the last CTA of
+// the unit to arrive merges every partial (log-sum-exp rule), writes the
+// output, zeroes the partials it merged and resets the unit's counter.
+template <int NW, int GP, int DD, class Sync>
+__device__ inline void finish_segment(const DecodeParams &p, const TileCursor &cur, int seg_first_t,
+                                      bool bad, const float (&sm_m)[NW][GP], const float (&sm_l)[NW][GP],
+                                      const float (&sm_o)[NW][GP][DD], int *sm_flag, MergeBuf &mb,
+                                      int tid, int nthr, Sync sync)
+{
+    const int G = p.G, b = cur.b, kvh = cur.kvh;
+    const bool unit_done = (cur.t == cur.nt - 1);
+    const bool whole = (seg_first_t == 0) && unit_done;
+    const int u = b * p.Hkv + kvh;
+    const long long P = (long long)u + blockIdx.x;
+    const float qnan = __int_as_float(0x7fc00000);
+    float *out = p.out + ((long long)b * p.Hq + (long long)kvh * G) * DD;
+    for (int idx = tid; idx < G * DD; idx += nthr) {
+        const int g = idx / DD, d = idx % DD;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NW; ++w)
+            M = fmaxf(M, sm_m[w][g]);
+        float num = 0.f, den = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            const float a = (sm_m[w][g] == -INFINITY) ? 0.f : fast_ex2(sm_m[w][g] - M);
+            num = fmaf(a, sm_o[w][g][d], num);
+            den = fmaf(a, sm_l[w][g], den);
+        }
+        if (whole) {
+            out[idx] = bad ? qnan : num / den;
+        } else {
+            p.ws_o[(P * G + g) * DD + d] = bad ? qnan : num;
+            if (d == 0) {
+                p.ws_ml[(P * G + g) * 2 + 0] = bad ? qnan : M;
+                p.ws_ml[(P * G + g) * 2 + 1] = bad ? qnan : den;
+            }
+        }
+    }
+    if (whole) {
+        sync();
+        return;
+    }
+    // The barrier orders every thread's partial stores before thread 0's
+    // acquire-release ticket at GPU scope (release is cumulative); the last
+    // arriver's acquire plus the barrier order its reads after the stores of
+    // every other CTA of the unit.
+    sync();
+    const long long first_tile = cur.g - cur.t;
+    const int first = cta_of_tile(first_tile, cur.N, cur.C);
+    const int last = cta_of_tile(first_tile + cur.nt - 1, cur.N, cur.C);
+    if (tid == 0) {
+        int old;
+        asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(p.ws_cnt + u) : "memory");
+        *sm_flag = (old == last - first);
+    }
+    sync();
+    if (*sm_flag) {
+        const int K = last - first + 1;
+        const long long P0 = (long long)u + first;
+        if (K <= kMergeMax) {
+            // one parallel load of every partial's (m, l), weights per head,
+            // then independent (vector) loads of the partial outputs
+            for (int k = tid; k < K * G; k += nthr) {
+                mb.w[k] = __ldcg(p.ws_ml + (P0 * G + k) * 2);
+                mb.l[k] = __ldcg(p.ws_ml + (P0 * G + k) * 2 + 1);
+            }
+            sync();
+            if (tid < G) {
+                float M = -INFINITY;
+                for (int i = 0; i < K; ++i)
+                    M = fmaxf(M, mb.w[i * G + tid]);
+                float den = 0.f;
+                for (int i = 0; i < K; ++i) {
+                    const float a = fast_ex2(mb.w[i * G + tid] - M);
+                    mb.w[i * G + tid] = a;
+                    den = fmaf(a, mb.l[i * G + tid], den);
+                }
+                mb.inv_den[tid] = 1.f / den;
+            }
+            sync();
+            constexpr int V = (DD % 4 == 0) ? 4 : 1;
+            for (int idx = tid * V; idx < G * DD; idx += nthr * V) {
+                const int g = idx / DD;
+                float acc[V];
+#pragma unroll
+                for (int e = 0; e < V; ++e)
+                    acc[e] = 0.f;
+#pragma unroll 4
+                for (int i = 0; i < K; ++i) {
+                    const float a = mb.w[i * G + g];
+                    float *po = p.ws_o + (P0 + i) * G * DD + idx;
+                    if constexpr (V == 4) {
+                        const float4 v = __ldcg(reinterpret_cast<const float4 *>(po));
+                        acc[0] = fmaf(a, v.x, acc[0]);
+                        acc[1] = fmaf(a, v.y, acc[1]);
+                        acc[2] = fmaf(a, v.z, acc[2]);
+                        acc[3] = fmaf(a, v.w, acc[3]);
+                        *reinterpret_cast<float4 *>(po) = make_float4(0.f, 0.f, 0.f, 0.f);
+                    } else {
+                        acc[0] = fmaf(a, __ldcg(po), acc[0]);
+                        *po = 0.f;     // consumed: leave the workspace zero-filled
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < V; ++e)
+                    out[idx + e] = acc[e] * mb.inv_den[g];
+            }
+        } else {
+            for (int idx = tid; idx < G * DD; idx += nthr) {
+                const int g = idx / DD, d = idx % DD;
+                float M = -INFINITY;
+                for (int i = 0; i < K; ++i)
+                    M = fmaxf(M, __ldcg(p.ws_ml + ((P0 + i) * G + g) * 2));
+                float num = 0.f, den = 0.f;
+                for (int i = 0; i < K; ++i) {
+                    const long long Q = P0 + i;
+                    const float a = fast_ex2(__ldcg(p.ws_ml + (Q * G + g) * 2) - M);
+                    float *po = p.ws_o + (Q * G + g) * DD + d;
+                    num = fmaf(a, __ldcg(po), num);
+                    den = fmaf(a, __ldcg(p.ws_ml + (Q * G + g) * 2 + 1), den);
+                    *po = 0.f;       // consumed: leave the workspace zero-filled
+                }
+                out[idx] = num / den;
+            }
+        }
+        sync();
+        // the (m, l) pairs of partials u+first .. u+last are contiguous
+        float *ml = p.ws_ml + P0 * G * 2;
+        for (int k = tid; k < K * G * 2; k += nthr)
+            ml[k] = 0.f;
+        if (tid == 0)
+            p.ws_cnt[u] = 0;
+    }
+    sync();
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }

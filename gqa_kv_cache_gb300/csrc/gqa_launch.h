@@ -24,11 +24,7 @@ int tc_ctas_per_sm();
 size_t tc_smem_bytes();
 cudaError_t tc_launch(const DecodeParams &p, const TcMaps &maps, cudaStream_t st);
 
-// Split combine (gqa_combine.cu): merges the partial states of the units cut
-// by CTA boundaries; grid = B * Hkv.
-cudaError_t combine_launch(const DecodeParams &p, cudaStream_t st, bool pdl);
-
-// Content validation (gqa_combine.cu). *d_result must be zero on entry; the
+// Content validation (gqa_validate.cu). *d_result must be zero on entry; the
 // kernel sets it to 1 on any violation.
 cudaError_t validate_launch(const int32_t *lengths, const int32_t *slot_ids,
                             const int32_t *block_table, int B, int R, int Smax,

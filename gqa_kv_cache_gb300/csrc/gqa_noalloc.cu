@@ -15,13 +15,16 @@
 // the first call made on that device; that first call should therefore come
 // before any stream capture. All calls share the one array and it keeps the
 // last call's contents: calls whose kernels overlap on the GPU (two streams,
-// or two threads) race on it and must be serialised by the caller. The decode
-// kernels write every scratch word they read within the same call, so nothing
-// has to be cleared between calls.
+// or two threads) race on it and must be serialised by the caller. Of the
+// scratch only the per-(row, head) arrival counters must start at zero (a
+// completed call leaves all of it zero); each call still clears the counters
+// (an asynchronous memset on its stream, no allocation) before its kernel, so
+// even a call left incomplete cannot affect the next.
 #include <cuda_runtime.h>
 
 #include <mutex>
 
+#include "gqa_common.cuh"
 #include "gqa_decode.h"
 
 namespace {
@@ -73,6 +76,13 @@ gqa_status gqa_decode_step_noalloc(const void *q, const void *k_new, const void 
     if (st != GQA_OK)
         return st;
     // need == 0 means the sizes are invalid: the regular entry point reports why.
+    // The per-(row, head) arrival counters must start at zero: clear them on
+    // this stream before the kernel (a memset, no allocation).
+    if (need != 0 && B > 0 && Hkv > 0) {
+        const size_t cnt = gqa::workspace_layout(B, Hkv, Hq / Hkv, D, 0).cnt_bytes;
+        if (cudaMemsetAsync(ws, 0, cnt, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+            return GQA_ERR_CUDA;
+    }
     return gqa_decode_step(q, k_new, v_new, k_cache, v_cache, lengths, slot_ids, out, B, Hq, Hkv,
                            D, R, Smax, dt, ws, kScratchBytes, d_status, stream);
 }

@@ -10,7 +10,8 @@
 // shuffles, each lane group keeps its own online-softmax state (running
 // base-2 max m, sum l, and its VEC columns of o for every head), and at the
 // end of a unit segment the states of all lane groups and warps are merged
-// with the log-sum-exp rule. The new token (slot L) is read from k_new/v_new
+// with the log-sum-exp rule (finish_segment, which also merges the units cut
+// by CTA boundaries). The new token (slot L) is read from k_new/v_new
 // directly and written into the cache by the lane group that reads it; no
 // thread reads the cache at slot L, so the append cannot race.
 #include "gqa_common.cuh"
@@ -117,7 +118,9 @@ __global__ void __launch_bounds__(kThreads) simt_decode_kernel(const DecodeParam
     using S = SimtShape<T, D>;
     constexpr int VEC = S::VEC, LPS = S::LPS, SPW = S::SPW, STREAMS = S::STREAMS;
 
-    __shared__ long long sched[2 * kThreads + 8];
+    __shared__ long long sched[kThreads / 32 + 8];
+    __shared__ int sm_flag;
+    __shared__ MergeBuf sm_merge;
     __shared__ float sm_m[kWarps][GP], sm_l[kWarps][GP];
     __shared__ float sm_o[kWarps][GP][D];
 
@@ -127,7 +130,9 @@ __global__ void __launch_bounds__(kThreads) simt_decode_kernel(const DecodeParam
     const T *kc = static_cast<const T *>(p.k_cache);
     const T *vc = static_cast<const T *>(p.v_cache);
 
-    TileCursor cur = schedule_start(p, sched);
+    const TileWalk walk = schedule_walk(p, sched);
+    TileCursor cur = walk.a;
+    bool in_b = false;
 
     float q[GP][VEC];
     float m[GP], l[GP], o[GP][VEC];
@@ -136,7 +141,8 @@ __global__ void __launch_bounds__(kThreads) simt_decode_kernel(const DecodeParam
     bool seg_start = true;
     int bad_local = 0;
 
-    while (cur.g < cur.end) {
+    bool more = cur.g < cur.end;
+    while (more) {
         const int b = cur.b, kvh = cur.kvh, L = cur.L;
         if (seg_start) {
             seg_first_t = cur.t;
@@ -260,39 +266,14 @@ __global__ void __launch_bounds__(kThreads) simt_decode_kernel(const DecodeParam
             }
             const bool seg_bad = __syncthreads_or(bad_local) != 0;
             bad_local = 0;
-            const bool whole = (seg_first_t == 0) && unit_done;
             const bool bad = !row_good || seg_bad;
             if (bad && row_good && tid == 0)
                 report(p, kBadBlock);
-            const int u = b * p.Hkv + kvh;
-            const long long P = (long long)u + blockIdx.x;
-            for (int idx = tid; idx < G * D; idx += kThreads) {
-                const int g = idx / D, d = idx % D;
-                float M = -INFINITY;
-#pragma unroll
-                for (int w = 0; w < kWarps; ++w)
-                    M = fmaxf(M, sm_m[w][g]);
-                float num = 0.f, den = 0.f;
-#pragma unroll
-                for (int w = 0; w < kWarps; ++w) {
-                    float a = (sm_m[w][g] == -INFINITY) ? 0.f : ex2(sm_m[w][g] - M);
-                    num = fmaf(a, sm_o[w][g][d], num);
-                    den = fmaf(a, sm_l[w][g], den);
-                }
-                if (whole) {
-                    p.out[((long long)b * p.Hq + kvh * G + g) * D + d] = bad ? __int_as_float(0x7fc00000) : num / den;
-                } else {
-                    p.ws_o[(P * G + g) * D + d] = bad ? __int_as_float(0x7fc00000) : num;
-                    if (d == 0) {
-                        p.ws_ml[(P * G + g) * 2 + 0] = bad ? __int_as_float(0x7fc00000) : M;
-                        p.ws_ml[(P * G + g) * 2 + 1] = bad ? __int_as_float(0x7fc00000) : den;
-                    }
-                }
-            }
-            __syncthreads();
+            finish_segment<kWarps, GP, D>(p, cur, seg_first_t, bad, sm_m, sm_l, sm_o, &sm_flag, sm_merge, tid,
+                                          kThreads, [] { __syncthreads(); });
             seg_start = true;
         }
-        advance(p, cur);
+        more = walk_next(p, cur, walk, in_b);
     }
 }
 

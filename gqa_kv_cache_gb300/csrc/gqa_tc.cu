@@ -1,15 +1,19 @@
 // Tensor-core decode kernel for bfloat16 caches with D = 128 and G <= 8.
 //
-// Data path (per persistent CTA, one per SM):
-//  * a producer warp walks the CTA's tile list (gqa_common.cuh) and streams
-//    every 64-slot tile of K and V from HBM into a 4-stage shared-memory ring
+// Data path (persistent CTAs, kCtasPerSm per SM):
+//  * a producer warp walks the CTA's tiles (gqa_common.cuh) and streams every
+//    64-slot tile of K and V from HBM into a kStages-deep shared-memory ring
 //    with TMA tiled copies (cp.async.bulk.tensor, 128-byte swizzle, two
 //    64-element halves per row), signalling an mbarrier per stage; for paged
-//    caches each lane copies one block of the tile;
+//    caches each lane copies one block of the tile. The first tile of each
+//    unit segment also brings the unit's G query rows (one bulk copy), so no
+//    consumer ever waits on a global load. Table and row lookups for a tile
+//    are issued one tile ahead, before the wait for a free stage.
 //  * four consumer warps each take 16 slots of every tile and compute, on the
 //    tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate):
 //      S  = Q K^T   M = 16 query rows (the G heads; rows >= G are zero),
-//                   N = 8 slots, K = 16 dims, 8 steps over D = 128;
+//                   N = 8 slots, K = 16 dims, 8 steps over D = 128 (two
+//                   accumulator chains per tile, even and odd steps);
 //      O += P V     M = 16 rows: rows 0..7 carry bf16(p) and rows 8..15 the
 //                   remainder bf16(p - bf16(p)), so p enters the product with
 //                   ~16 significant bits and the sum stays float32-accurate;
@@ -28,8 +32,10 @@
 //    copy of that tile has landed before the store, and no other CTA loads
 //    slot L, so the append cannot race with a read.
 //  * at the end of each unit segment the four warp states are merged in
-//    shared memory and either the normalised output or a partial state for
-//    the combine kernel is written.
+//    shared memory (finish_segment): a whole unit writes its output, a cut
+//    unit its partial state, and the last CTA of a cut unit merges them.
+// Two CTAs share each SM, so one CTA's segment epilogue overlaps the other's
+// streaming.
 // Every mbarrier wait is bounded. A wait that gives up sets GQA_STATUS_TIMEOUT
 // and a CTA-wide abort flag: the producer stops issuing and waits (bounded)
 // for its copies in flight; the consumer warps stop waiting and computing but
@@ -40,27 +46,30 @@
 namespace gqa {
 namespace {
 
+#ifndef GQA_TC_STAGES
+#define GQA_TC_STAGES 2
+#endif
+#ifndef GQA_TC_CTAS_PER_SM
+#define GQA_TC_CTAS_PER_SM 2
+#endif
+
 constexpr int kD = 128;
-constexpr int kTile = 64;                        // slots per tile
-constexpr int kStages = 4;
+constexpr int kTile = 64;                             // slots per tile
+constexpr int kStages = GQA_TC_STAGES;                // depth of one CTA's TMA ring
+constexpr int kCtasPerSm = GQA_TC_CTAS_PER_SM;        // resident CTAs per SM
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kHalfBytes = kTile * 128;          // one 64-element half of a tile
-constexpr int kStageBytes = 4 * kHalfBytes;      // K lo, K hi, V lo, V hi
-constexpr int kDynSmem = kStages * kStageBytes + 1024;
 constexpr int kGMax = 8;
-constexpr long long kWaitCycles = 4LL << 30;     // ~2 s at 2 GHz
+constexpr int kHalfBytes = kTile * 128;               // one 64-element half of a tile
+constexpr int kQBytes = kGMax * kD * 2;               // the unit's G query rows
+constexpr int kStageBytes = 4 * kHalfBytes + kQBytes; // K lo, K hi, V lo, V hi, Q
+constexpr int kDynSmem = kStages * kStageBytes + 1024;
+constexpr long long kWaitCycles = 4LL << 30;          // ~2 s at 2 GHz
+static_assert(kStageBytes % 1024 == 0, "stages must stay 1024-byte aligned for the swizzle");
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ float ex2(float x)
-{
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
 }
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, int count)
@@ -113,6 +122,13 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4])
 {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
@@ -152,13 +168,20 @@ struct Shared {
     uint64_t empty[kStages];
     int stage_bad[kStages];
     int abort_flag;
-    long long sched[2 * kThreads + 8];
+    int last_flag;
+    long long sched[kThreads / 32 + 8];
     float m[kConsumerWarps][kGMax];
     float l[kConsumerWarps][kGMax];
     float o[kConsumerWarps][kGMax][kD];
+    MergeBuf merge;
 };
 
-__global__ void __launch_bounds__(kThreads, 1)
+__device__ __forceinline__ void consumer_sync()
+{
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
     tc_decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap mk,
                      const __grid_constant__ CUtensorMap mv)
 {
@@ -177,9 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         sh.abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    // Let the combine grid get scheduled now; it waits for this grid's end.
-    asm volatile("griddepcontrol.launch_dependents;");
-    const TileCursor start = schedule_start(p, sh.sched);   // contains __syncthreads
+    const TileWalk walk = schedule_walk(p, sh.sched);   // contains __syncthreads
 
     const int G = p.G;
     const __nv_bfloat16 *knew = static_cast<const __nv_bfloat16 *>(p.k_new);
@@ -189,14 +210,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------ producer --
         uint64_t policy;
         asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
-        TileCursor cur = start;
+        TileCursor cur = walk.a;
+        bool in_b = false;
+        long long range_start = cur.g;
         int stage = 0;
         uint32_t phase = 0;
         const int bs = p.block_size;
         const int nblk = p.paged ? (bs < kTile ? kTile / bs : 1) : 1;  // copies per half per tile
         const int box_rows = p.paged ? (bs < kTile ? bs : kTile) : kTile;
+        // Where this lane copies tile `c` from: z (cache head row of the
+        // tensor map) and y (first slot in it); z < 0: nothing. Computed one
+        // tile ahead, before the wait for a free stage, so the table reads
+        // overlap the wait.
+        struct Plan {
+            int z, y;
+            bool bad_entry, good;
+        };
+        auto plan = [&](const TileCursor &c) {
+            Plan r{-1, 0, false, row_ok(p, c.b, c.L)};
+            if (!r.good)
+                return r;
+            const int slot0 = c.t * kTile;
+            if (!p.paged) {
+                if (lane == 0) {
+                    const int row = p.slot_ids ? __ldg(p.slot_ids + c.b) : c.b;
+                    r.z = row * p.Hkv + c.kvh;
+                    r.y = slot0;
+                }
+            } else if (lane < nblk) {
+                const int s = slot0 + lane * box_rows;  // first slot this lane copies
+                if (s <= c.L) {
+                    const int e = __ldg(p.block_table + (long long)c.b * p.max_blocks + s / bs);
+                    if (e >= 0 && e < p.num_blocks) {
+                        r.z = e * p.Hkv + c.kvh;
+                        r.y = s % bs;
+                    } else {
+                        r.bad_entry = true;
+                    }
+                }
+            }
+            return r;
+        };
         int issued = 0;
-        while (cur.g < cur.end) {
+        bool more = cur.g < cur.end;
+        Plan pl = more ? plan(cur) : Plan{-1, 0, false, false};
+        while (more) {
             if (*((volatile int *)&sh.abort_flag))
                 break;
             if (!mbar_wait(smem_u32(&sh.empty[stage]), phase ^ 1)) {
@@ -206,50 +264,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 break;
             }
-            const int b = cur.b, kvh = cur.kvh, L = cur.L;
-            const int slot0 = cur.t * kTile;
-            const bool good = row_ok(p, b, L);
-            // which rows of the tile to copy, and from where
-            int z = -1, y = 0;
-            bool bad_entry = false;
-            if (good) {
-                if (!p.paged) {
-                    if (lane == 0) {
-                        const int r = p.slot_ids ? __ldg(p.slot_ids + b) : b;
-                        z = r * p.Hkv + kvh;
-                        y = slot0;
-                    }
-                } else if (lane < nblk) {
-                    const int s = slot0 + lane * box_rows;  // first slot this lane copies
-                    if (s <= L) {
-                        const int e = __ldg(p.block_table + (long long)b * p.max_blocks + s / bs);
-                        if (e >= 0 && e < p.num_blocks) {
-                            z = e * p.Hkv + kvh;
-                            y = s % bs;
-                        } else {
-                            bad_entry = true;
-                        }
-                    }
-                }
-            }
-            const unsigned copying = __ballot_sync(0xffffffffu, z >= 0);
-            const bool any_bad = __any_sync(0xffffffffu, bad_entry);
-            const uint32_t bytes = (uint32_t)__popc(copying) * 4u * (uint32_t)box_rows * 128u;
+            const int b = cur.b, kvh = cur.kvh;
+            const unsigned copying = __ballot_sync(0xffffffffu, pl.z >= 0);
+            const bool any_bad = __any_sync(0xffffffffu, pl.bad_entry);
+            // the first tile of each of this CTA's unit segments also brings
+            // the unit's G query rows (contiguous in q)
+            const bool seg_first = pl.good && (cur.t == 0 || cur.g == range_start);
+            const uint32_t qbytes = seg_first ? (uint32_t)G * kD * 2u : 0u;
+            const uint32_t bytes = (uint32_t)__popc(copying) * 4u * (uint32_t)box_rows * 128u + qbytes;
             const uint32_t fb = smem_u32(&sh.full[stage]);
             if (lane == 0) {
                 sh.stage_bad[stage] = any_bad ? 1 : 0;
                 mbar_arrive_tx(fb, bytes);
+                if (qbytes)
+                    bulk_load(ring_u32 + stage * kStageBytes + 4 * kHalfBytes,
+                              static_cast<const __nv_bfloat16 *>(p.q) + ((long long)b * p.Hq + (long long)kvh * G) * kD,
+                              qbytes, fb);
             }
             __syncwarp();
-            if (z >= 0) {
+            if (pl.z >= 0) {
                 const uint32_t dst = ring_u32 + stage * kStageBytes + lane * box_rows * 128;
-                tma_load_3d(dst, &mk, 0, y, z, fb, policy);
-                tma_load_3d(dst + kHalfBytes, &mk, 64, y, z, fb, policy);
-                tma_load_3d(dst + 2 * kHalfBytes, &mv, 0, y, z, fb, policy);
-                tma_load_3d(dst + 3 * kHalfBytes, &mv, 64, y, z, fb, policy);
+                tma_load_3d(dst, &mk, 0, pl.y, pl.z, fb, policy);
+                tma_load_3d(dst + kHalfBytes, &mk, 64, pl.y, pl.z, fb, policy);
+                tma_load_3d(dst + 2 * kHalfBytes, &mv, 0, pl.y, pl.z, fb, policy);
+                tma_load_3d(dst + 3 * kHalfBytes, &mv, 64, pl.y, pl.z, fb, policy);
             }
             ++issued;
-            advance(p, cur);
+            const bool was_b = in_b;
+            more = walk_next(p, cur, walk, in_b);
+            if (in_b != was_b)
+                range_start = cur.g;
+            if (more)
+                pl = plan(cur);
             if (++stage == kStages) {
                 stage = 0;
                 phase ^= 1;
@@ -272,7 +318,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // -------------------------------------------------------- consumers --
     const int g0 = lane >> 2, q4 = lane & 3;
     const int row0 = warp * 16;          // this warp's 16 rows of every tile
-    TileCursor cur = start;
+    TileCursor cur = walk.a;
+    bool in_b = false;
     int stage = 0;
     uint32_t phase = 0;
     uint32_t qa[8][2];                   // Q fragments (rows g0 < G), 8 k-steps
@@ -282,20 +329,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool seg_start = true, row_good = true, aborted = false;
     int seg_bad = 0;
 
-    while (cur.g < cur.end) {
+    bool more = cur.g < cur.end;
+    while (more) {
         const int b = cur.b, kvh = cur.kvh, L = cur.L;
+        const bool first_of_seg = seg_start;
         if (seg_start) {
             seg_first_t = cur.t;
             row_good = row_ok(p, b, L);
             if (!row_good && tid == 0 && cur.t == 0 && kvh == 0)
                 report(p, row_error_bits(p, b, L));
-            const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
-                static_cast<const __nv_bfloat16 *>(p.q) + ((long long)b * p.Hq + kvh * G + g0) * kD);
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                qa[ks][0] = (g0 < G) ? __ldg(qrow + ks * 8 + q4) : 0u;       // dims 16ks + 2q4, +1
-                qa[ks][1] = (g0 < G) ? __ldg(qrow + ks * 8 + 4 + q4) : 0u;   // dims 16ks + 8 + 2q4, +1
-            }
 #pragma unroll
             for (int n = 0; n < 16; ++n)
                 acc_o[n][0] = acc_o[n][1] = acc_o[n][2] = acc_o[n][3] = 0.f;
@@ -321,10 +363,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int slot0 = cur.t * kTile;
         const uint32_t kbase = ring_u32 + stage * kStageBytes;
         const uint32_t vbase = kbase + 2 * kHalfBytes;
-        uint8_t *vring = ring + stage * kStageBytes + 2 * kHalfBytes;
         uint8_t *kring = ring + stage * kStageBytes;
+        uint8_t *vring = kring + 2 * kHalfBytes;
         const int tile_bad = have ? sh.stage_bad[stage] : 1;
         seg_bad |= tile_bad;
+        if (first_of_seg && have && row_good) {
+            // Q fragments from the ring (rows g0 < G): dims 16ks + 2q4 (+1)
+            // and 16ks + 8 + 2q4 (+1) of head g0
+            const uint8_t *qs = kring + 4 * kHalfBytes + g0 * (kD * 2);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                qa[ks][0] = (g0 < G) ? *reinterpret_cast<const uint32_t *>(qs + (16 * ks + 2 * q4) * 2) : 0u;
+                qa[ks][1] = (g0 < G) ? *reinterpret_cast<const uint32_t *>(qs + (16 * ks + 8 + 2 * q4) * 2) : 0u;
+            }
+        }
 
         if (have && row_good && !tile_bad) {
             const bool last_tile = (cur.t == cur.nt - 1);
@@ -356,9 +408,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
             }
 
-            // ---- S = Q K^T for this warp's 16 slots (two n-tiles of 8)
+            // ---- S = Q K^T for this warp's 16 slots (two n-tiles of 8);
+            // even and odd k-steps accumulate separately (shorter chains)
             float s_acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
             {
+                float s_odd[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
                 const int mi = lane >> 3, ri = lane & 7;
                 const int r = row0 + 8 * (mi >> 1) + ri;
 #pragma unroll
@@ -366,9 +420,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int c = 2 * ks + (mi & 1);
                     uint32_t kb[4];
                     ldsm_x4(kbase + (c >> 3) * kHalfBytes + swz(r, c & 7), kb);
-                    mma_bf16(s_acc[0], qa[ks][0], 0u, qa[ks][1], 0u, kb[0], kb[1]);
-                    mma_bf16(s_acc[1], qa[ks][0], 0u, qa[ks][1], 0u, kb[2], kb[3]);
+                    float(&acc)[2][4] = (ks & 1) ? s_odd : s_acc;
+                    mma_bf16(acc[0], qa[ks][0], 0u, qa[ks][1], 0u, kb[0], kb[1]);
+                    mma_bf16(acc[1], qa[ks][0], 0u, qa[ks][1], 0u, kb[2], kb[3]);
                 }
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        s_acc[nt][e] += s_odd[nt][e];
             }
             // ---- masked online softmax (base 2), rows g0
             float x[2][2];
@@ -384,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
             if (mx > m_run + 8.f) {          // raise the running max (also from -inf)
-                const float alpha = (m_run == -INFINITY) ? 0.f : ex2(m_run - mx);
+                const float alpha = (m_run == -INFINITY) ? 0.f : fast_ex2(m_run - mx);
                 l_run *= alpha;
 #pragma unroll
                 for (int n = 0; n < 16; ++n) {
@@ -402,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
-                        pr[nt][e] = (x[nt][e] == -INFINITY) ? 0.f : ex2(x[nt][e] - m_run);
+                        pr[nt][e] = (x[nt][e] == -INFINITY) ? 0.f : fast_ex2(x[nt][e] - m_run);
                         l_run += pr[nt][e];
                     }
 #pragma unroll
@@ -439,8 +499,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 
         const bool unit_done = (cur.t == cur.nt - 1);
-        const bool cta_done = (cur.g + 1 == cur.end);
-        if (unit_done || cta_done) {
+        const bool range_done = (cur.g + 1 == cur.end);
+        if (unit_done || range_done) {
             // ---- merge the four warps' states and emit
             float l_tot = l_run;
             l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 1);
@@ -456,41 +516,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     sh.o[warp][g0][8 * n + 2 * q4 + 1] = acc_o[n][1] + acc_o[n][3];
                 }
             }
-            asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-            const bool whole = (seg_first_t == 0) && unit_done;
+            consumer_sync();
             const bool bad = !row_good || seg_bad;
             if (bad && row_good && tid == 0)
-                report(p, kBadBlock);
-            const int u = b * p.Hkv + kvh;
-            const long long P = (long long)u + blockIdx.x;
-            const float qnan = __int_as_float(0x7fc00000);
-            for (int idx = tid; idx < G * kD; idx += kConsumerWarps * 32) {
-                const int g = idx / kD, d = idx % kD;
-                float M = -INFINITY;
-#pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w)
-                    M = fmaxf(M, sh.m[w][g]);
-                float num = 0.f, den = 0.f;
-#pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w) {
-                    const float a = (sh.m[w][g] == -INFINITY) ? 0.f : ex2(sh.m[w][g] - M);
-                    num = fmaf(a, sh.o[w][g][d], num);
-                    den = fmaf(a, sh.l[w][g], den);
-                }
-                if (whole) {
-                    p.out[((long long)b * p.Hq + kvh * G + g) * kD + d] = bad ? qnan : num / den;
-                } else {
-                    p.ws_o[(P * G + g) * kD + d] = bad ? qnan : num;
-                    if (d == 0) {
-                        p.ws_ml[(P * G + g) * 2 + 0] = bad ? qnan : M;
-                        p.ws_ml[(P * G + g) * 2 + 1] = bad ? qnan : den;
-                    }
-                }
-            }
-            asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+                report(p, aborted ? kTimeout : kBadBlock);
+            finish_segment<kConsumerWarps, kGMax, kD>(p, cur, seg_first_t, bad, sh.m, sh.l, sh.o,
+                                                      &sh.last_flag, sh.merge, tid, kConsumerWarps * 32,
+                                                      [] { consumer_sync(); });
             seg_start = true;
         }
-        advance(p, cur);
+        more = walk_next(p, cur, walk, in_b);
     }
 }
 
@@ -509,7 +544,7 @@ bool tc_supports(bool bf16, int D, int G, bool paged, int block_size)
 }
 
 int tc_tile() { return kTile; }
-int tc_ctas_per_sm() { return 1; }
+int tc_ctas_per_sm() { return kCtasPerSm; }
 size_t tc_smem_bytes() { return kDynSmem + sizeof(Shared); }
 
 cudaError_t tc_launch(const DecodeParams &p, const TcMaps &maps, cudaStream_t st)

@@ -101,10 +101,20 @@ const char *gqa_status_string(gqa_status s);
 
 /*
  * Workspace bytes a decode step needs on the current device for these sizes
- * (float32 partial softmax states of the split sequences plus a small
- * schedule table). opt may be NULL. Returns 0 for invalid sizes.
+ * (one arrival counter per (row, cache head) and the float32 partial softmax
+ * states of the sequences that several CTAs share). opt may be NULL. Returns
+ * 0 for invalid sizes.
+ *
+ * The workspace must be zero-filled (gqa_workspace_reset or any memset)
+ * before its first use; every call leaves it zero-filled again, whatever the
+ * sizes of the next call. Zero it again after a call that reported
+ * GQA_STATUS_TIMEOUT. One workspace serves one call at a time (calls that may
+ * overlap on the GPU need different workspaces).
  */
 size_t gqa_workspace_bytes(int B, int Hq, int Hkv, int D, gqa_dtype dt, const gqa_options *opt);
+
+/* Zero-fills a workspace asynchronously on `stream` (a cudaMemsetAsync). */
+gqa_status gqa_workspace_reset(void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Dense or continuous-batch decode step.
@@ -122,7 +132,8 @@ size_t gqa_workspace_bytes(int B, int Hq, int Hkv, int D, gqa_dtype dt, const gq
  *                                        [0, R), pairwise distinct ("groupQueryAttention",
  *                                        slot_ids). NULL: row b uses cache row b (R >= B).
  *  out      (device) (B, Hq, D) float32  attention output
- *  workspace(device) >= gqa_workspace_bytes(...) bytes, 256-byte aligned
+ *  workspace(device) >= gqa_workspace_bytes(...) bytes, 256-byte aligned,
+ *                                        zero-filled before its first use
  *  d_status (device) int32 or NULL       sticky content-error bits (see above)
  */
 gqa_status gqa_decode_step(const void *q, const void *k_new, const void *v_new,
@@ -190,10 +201,10 @@ gqa_status gqa_validate(const int32_t *lengths, const int32_t *slot_ids,
 
 /*
  * Kernel timing trace. When enabled, every decode call records CUDA events
- * around each kernel it launches; gqa_trace_collect waits for them and
+ * around the kernel it launches; gqa_trace_collect waits for them and
  * returns, per kernel kind, the launches and total milliseconds since the
- * previous collect. Kinds: 0 = SIMT decode, 1 = tensor-core decode,
- * 2 = split combine. Not thread-safe; meant for benchmarks.
+ * previous collect. Kinds: 0 = SIMT decode, 1 = tensor-core decode (each
+ * decode step is exactly one kernel launch). Meant for benchmarks.
  */
 int gqa_trace_enable(int on);
 gqa_status gqa_trace_collect(int n_kinds, int64_t *launches, double *ms);

@@ -50,7 +50,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings(lib):
-    for code in range(5):
+    for code in range(6):
         assert lib.gqa_status_string(code)
     assert b"workspace" in lib.gqa_status_string(4)
 

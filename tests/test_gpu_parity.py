@@ -257,3 +257,25 @@ def test_full_size_workloads(name):
     small_enough = name == "pr1_fp32"
     err, tol, _ = check_step(w, rows=None if small_enough else "sample4", gpu_gen=not small_enough)
     assert err <= tol, f"{name}: max abs error {err} > {tol}"
+
+
+@pytest.mark.parametrize("kernel", ["simt", "tc"])
+def test_workspace_left_zero_across_sizes(kernel):
+    """One caller-owned workspace, zero-filled once, serves calls of growing
+    and shrinking sizes: each output matches the oracle and after every call
+    the workspace is all zero again (counters reset, merged partials cleared)."""
+    import gqa_kv_cache_gb300 as gqa
+    cases = [W.small("llama3_8b", B=2, Smax=300, len_lo=100, len_hi=299, seed=140),
+             W.small("long_context", B=5, Smax=2000, len_lo=500, len_hi=1999, seed=141),
+             W.small("llama3_8b", B=3, Smax=900, len_lo=0, len_hi=899, seed=142)]
+    need = max(gqa.workspace_bytes(w.B, w.Hq, w.Hkv, w.D, torch.bfloat16, kernel, 37) for w in cases)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    for w in cases:
+        t = make_inputs(w)
+        prob = host_problem(w, t)
+        out = gqa.decode_step(t["q"], t["k_new"], t["v_new"], t["k_cache"], t["v_cache"], t["lengths"],
+                              kernel=kernel, grid_ctas=37, workspace=ws)
+        torch.cuda.synchronize()
+        want = run_oracle(w, prob)
+        assert np.abs(out.double().cpu().numpy() - want).max() <= tolerance(w, attended_vmax(prob))
+        assert int(torch.count_nonzero(ws).item()) == 0

@@ -29,7 +29,7 @@ def _p(t):
 
 def _regular(lib, t, w, out, stream):
     need = lib.gqa_workspace_bytes(w.B, w.Hq, w.Hkv, w.D, DTYPE[t["q"].dtype], None)
-    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")   # zero-filled before first use
     return lib.gqa_decode_step(_p(t["q"]), _p(t["k_new"]), _p(t["v_new"]), _p(t["k_cache"]),
                                _p(t["v_cache"]), _p(t["lengths"]), _p(t.get("slot_ids")), _p(out),
                                w.B, w.Hq, w.Hkv, w.D, w.rows, w.Smax, DTYPE[t["q"].dtype],
