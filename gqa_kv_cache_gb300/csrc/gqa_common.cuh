@@ -311,10 +311,14 @@ __device__ __forceinline__ float fast_ex2(float x)
     return y;
 }
 
-// Shared-memory scratch of the in-kernel merge of a cut unit's partials.
+// Shared-memory scratch of a segment's epilogue and of the in-kernel merge of
+// a cut unit's partials.
 constexpr int kMergeMax = 32;   // partials merged through shared memory (more: direct loads)
 constexpr int kMergeG = 8;      // heads per unit (G <= 8)
+constexpr int kMergeW = 4;      // warps whose states a segment merges
 struct MergeBuf {
+    float a[kMergeW][kMergeG];      // weight 2^(m_w - M) of each warp's state
+    float M[kMergeG], den[kMergeG];
     float w[kMergeMax * kMergeG];   // partial max, then its weight 2^(m_i - M)
     float l[kMergeMax * kMergeG];
     float inv_den[kMergeG];
@@ -322,17 +326,20 @@ struct MergeBuf {
 
 // End of a unit segment. The NW per-warp states of the segment are in shared
 // memory: sm_m[w][g] (base-2 running max, -inf for a warp that saw no slot),
-// sm_l[w][g], sm_o[w][g][d]. All `nthr` calling threads take part; `sync`
-// synchronises exactly them. A whole unit writes its normalised output. A cut
-// unit writes its partial state, then takes an arrival ticket; the last CTA of
-// the unit to arrive merges every partial (log-sum-exp rule), writes the
-// output, zeroes the partials it merged and resets the unit's counter.
-template <int NW, int GP, int DD, class Sync>
+// sm_l[w][g], sm_o[w][g][d] (rows padded to DP >= DD floats). All `nthr`
+// calling threads take part; `sync` synchronises exactly them. The weights
+// of the warp states are formed once per head, then the outputs are merged
+// four at a time. A whole unit writes its normalised output. A cut unit
+// writes its partial state, then takes an arrival ticket; the last CTA of the
+// unit to arrive merges every partial (log-sum-exp rule), writes the output,
+// zeroes the partials it merged and resets the unit's counter.
+template <int NW, int GP, int DD, int DP, class Sync>
 __device__ inline void finish_segment(const DecodeParams &p, const TileCursor &cur, int seg_first_t,
                                       bool bad, const float (&sm_m)[NW][GP], const float (&sm_l)[NW][GP],
-                                      const float (&sm_o)[NW][GP][DD], int *sm_flag, MergeBuf &mb,
+                                      const float (&sm_o)[NW][GP][DP], int *sm_flag, MergeBuf &mb,
                                       int tid, int nthr, Sync sync)
 {
+    static_assert(NW <= kMergeW && GP <= kMergeG && DP >= DD, "merge buffer too small");
     const int G = p.G, b = cur.b, kvh = cur.kvh;
     const bool unit_done = (cur.t == cur.nt - 1);
     const bool whole = (seg_first_t == 0) && unit_done;
@@ -340,26 +347,65 @@ __device__ inline void finish_segment(const DecodeParams &p, const TileCursor &c
     const long long P = (long long)u + blockIdx.x;
     const float qnan = __int_as_float(0x7fc00000);
     float *out = p.out + ((long long)b * p.Hq + (long long)kvh * G) * DD;
-    for (int idx = tid; idx < G * DD; idx += nthr) {
-        const int g = idx / DD, d = idx % DD;
+    if (tid < G) {
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < NW; ++w)
-            M = fmaxf(M, sm_m[w][g]);
-        float num = 0.f, den = 0.f;
+            M = fmaxf(M, sm_m[w][tid]);
+        float den = 0.f;
 #pragma unroll
         for (int w = 0; w < NW; ++w) {
-            const float a = (sm_m[w][g] == -INFINITY) ? 0.f : fast_ex2(sm_m[w][g] - M);
-            num = fmaf(a, sm_o[w][g][d], num);
-            den = fmaf(a, sm_l[w][g], den);
+            const float a = (sm_m[w][tid] == -INFINITY) ? 0.f : fast_ex2(sm_m[w][tid] - M);
+            mb.a[w][tid] = a;
+            den = fmaf(a, sm_l[w][tid], den);
         }
-        if (whole) {
-            out[idx] = bad ? qnan : num / den;
-        } else {
-            p.ws_o[(P * G + g) * DD + d] = bad ? qnan : num;
-            if (d == 0) {
-                p.ws_ml[(P * G + g) * 2 + 0] = bad ? qnan : M;
-                p.ws_ml[(P * G + g) * 2 + 1] = bad ? qnan : den;
+        mb.M[tid] = M;
+        mb.den[tid] = den;
+        if (!whole) {
+            p.ws_ml[(P * G + tid) * 2 + 0] = bad ? qnan : M;
+            p.ws_ml[(P * G + tid) * 2 + 1] = bad ? qnan : den;
+        }
+    }
+    sync();
+    {
+        constexpr int V = (DD % 4 == 0) ? 4 : 1;
+        for (int idx = tid * V; idx < G * DD; idx += nthr * V) {
+            const int g = idx / DD, d = idx % DD;
+            float acc[V];
+#pragma unroll
+            for (int e = 0; e < V; ++e)
+                acc[e] = 0.f;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                const float a = mb.a[w][g];
+                if constexpr (V == 4) {
+                    const float4 o = *reinterpret_cast<const float4 *>(&sm_o[w][g][d]);
+                    acc[0] = fmaf(a, o.x, acc[0]);
+                    acc[1] = fmaf(a, o.y, acc[1]);
+                    acc[2] = fmaf(a, o.z, acc[2]);
+                    acc[3] = fmaf(a, o.w, acc[3]);
+                } else {
+                    acc[0] = fmaf(a, sm_o[w][g][d], acc[0]);
+                }
+            }
+            if (whole) {
+                const float inv = 1.f / mb.den[g];
+#pragma unroll
+                for (int e = 0; e < V; ++e)
+                    acc[e] = bad ? qnan : acc[e] * inv;
+                if constexpr (V == 4)
+                    *reinterpret_cast<float4 *>(out + idx) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                else
+                    out[idx] = acc[0];
+            } else {
+                float *po = p.ws_o + (P * G + g) * DD + d;
+#pragma unroll
+                for (int e = 0; e < V; ++e)
+                    acc[e] = bad ? qnan : acc[e];
+                if constexpr (V == 4)
+                    *reinterpret_cast<float4 *>(po) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                else
+                    *po = acc[0];
             }
         }
     }

@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(kThreads) simt_decode_kernel(const DecodeParam
     __shared__ int sm_flag;
     __shared__ MergeBuf sm_merge;
     __shared__ float sm_m[kWarps][GP], sm_l[kWarps][GP];
-    __shared__ float sm_o[kWarps][GP][D];
+    __shared__ __align__(16) float sm_o[kWarps][GP][D];
 
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int lg = lane / LPS, li = lane % LPS;
@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(kThreads) simt_decode_kernel(const DecodeParam
             const bool bad = !row_good || seg_bad;
             if (bad && row_good && tid == 0)
                 report(p, kBadBlock);
-            finish_segment<kWarps, GP, D>(p, cur, seg_first_t, bad, sm_m, sm_l, sm_o, &sm_flag, sm_merge, tid,
+            finish_segment<kWarps, GP, D, D>(p, cur, seg_first_t, bad, sm_m, sm_l, sm_o, &sm_flag, sm_merge, tid,
                                           kThreads, [] { __syncthreads(); });
             seg_start = true;
         }

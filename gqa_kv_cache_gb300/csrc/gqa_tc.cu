@@ -172,7 +172,7 @@ struct Shared {
     long long sched[kThreads / 32 + 8];
     float m[kConsumerWarps][kGMax];
     float l[kConsumerWarps][kGMax];
-    float o[kConsumerWarps][kGMax][kD];
+    alignas(16) float o[kConsumerWarps][kGMax][kD + 8];   // rows padded: conflict-free 8-byte stores
     MergeBuf merge;
 };
 
@@ -511,16 +511,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     sh.l[warp][g0] = l_tot;
                 }
 #pragma unroll
-                for (int n = 0; n < 16; ++n) {
-                    sh.o[warp][g0][8 * n + 2 * q4] = acc_o[n][0] + acc_o[n][2];
-                    sh.o[warp][g0][8 * n + 2 * q4 + 1] = acc_o[n][1] + acc_o[n][3];
-                }
+                for (int n = 0; n < 16; ++n)
+                    *reinterpret_cast<float2 *>(&sh.o[warp][g0][8 * n + 2 * q4]) =
+                        make_float2(acc_o[n][0] + acc_o[n][2], acc_o[n][1] + acc_o[n][3]);
             }
             consumer_sync();
             const bool bad = !row_good || seg_bad;
             if (bad && row_good && tid == 0)
                 report(p, aborted ? kTimeout : kBadBlock);
-            finish_segment<kConsumerWarps, kGMax, kD>(p, cur, seg_first_t, bad, sh.m, sh.l, sh.o,
+            finish_segment<kConsumerWarps, kGMax, kD, kD + 8>(p, cur, seg_first_t, bad, sh.m, sh.l, sh.o,
                                                       &sh.last_flag, sh.merge, tid, kConsumerWarps * 32,
                                                       [] { consumer_sync(); });
             seg_start = true;
