@@ -130,6 +130,8 @@ __global__ void __launch_bounds__(kThreads) simt_decode_kernel(const DecodeParam
     const T *kc = static_cast<const T *>(p.k_cache);
     const T *vc = static_cast<const T *>(p.v_cache);
 
+    // programmatic dependent of the previous kernel: read no input before it is done
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const TileWalk walk = schedule_walk(p, sched);
     TileCursor cur = walk.a;
     bool in_b = false;
@@ -286,8 +288,16 @@ cudaError_t launch_one(const DecodeParams *p, cudaStream_t st, int *per_sm)
         return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, simt_decode_kernel<T, D, GP>,
                                                              kThreads, 0);
     }
-    simt_decode_kernel<T, D, GP><<<p->grid, kThreads, 0, st>>>(*p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p->grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, simt_decode_kernel<T, D, GP>, *p);
 }
 
 template <typename T, int D>

@@ -200,6 +200,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         sh.abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    if (warp == kConsumerWarps && lane == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mk)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mv)) : "memory");
+    }
+    // Launched as a programmatic dependent of the previous kernel on the
+    // stream: everything above overlaps its tail; no input is read before it
+    // has completed and its memory is visible.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const TileWalk walk = schedule_walk(p, sh.sched);   // contains __syncthreads
 
     const int G = p.G;
@@ -301,6 +309,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 phase ^= 1;
             }
         }
+        // every tile is issued: the next kernel on the stream may start launching
+        asm volatile("griddepcontrol.launch_dependents;");
         // Abort path only: let every copy still in flight land before exit.
         if (*((volatile int *)&sh.abort_flag)) {
             int s = stage, ph = phase;
@@ -555,8 +565,17 @@ cudaError_t tc_launch(const DecodeParams &p, const TcMaps &maps, cudaStream_t st
             return e;
         attr_set = true;
     }
-    tc_decode_kernel<<<p.grid, kThreads, kDynSmem, st>>>(p, maps.k, maps.v);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kDynSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, tc_decode_kernel, p, maps.k, maps.v);
 }
 
 }  // namespace gqa
