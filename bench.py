@@ -9,7 +9,9 @@ D=128, Smax=4096, lengths ~ U{1024..4095}).
 Prints ONE JSON line (rank 0):
   value     KV-cache bytes the step must read (sum_b lengths[b]*Hkv*D*2*es)
             divided by the device time of the step, in GB/s, inputs resident
-            in HBM, L2 flushed (256 MB write) between timed steps;
+            in HBM, L2 flushed between timed steps (a 256 MB write and then a
+            256 MB read, outside the events, so L2 is cold and holds no dirty
+            lines whose write-back would fall inside the next step);
   e2e       the same metric through the public API with the step's inputs
             copied from pinned host memory and the output read back, every step;
   roofline  the decode kernel alone (CUDA events around its launches) against
@@ -49,6 +51,9 @@ def parse():
     ap.add_argument("--workload", default="llama3_8b")
     ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "tc"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--l2-flush", default="write_read", choices=["write_read", "write", "none"],
+                    help="between timed steps: write 256 MB then read another 256 MB (L2 cold "
+                         "and clean), write only (dirty lines left to write back), or nothing")
     return ap.parse_args()
 
 
@@ -304,11 +309,25 @@ def run_ours(args, ranks):
     out = torch.empty(w.B, w.Hq, w.D, dtype=torch.float32, device=dev)
     step = step_fn(w, t, args.kernel, out)
     alg = algorithmic_bytes(w, t)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    flush_sink = torch.empty((), dtype=torch.int64, device=dev)
+
+    def l2_flush(i):
+        """Evict the step's data from L2 outside the timed events. Writing a
+        buffer larger than L2 leaves L2 full of dirty lines whose write-back
+        would land inside the next timed step; reading a second buffer after
+        it pushes those write-backs out here and leaves L2 clean and cold."""
+        if args.l2_flush == "none":
+            return
+        flush_w.fill_(i & 0xFF)
+        if args.l2_flush == "write_read":
+            torch.sum(flush_r, dim=0, dtype=torch.int64, out=flush_sink)
+
     stream = torch.cuda.current_stream()
 
     for i in range(args.warmup):
-        flush.fill_(i & 0xFF)
+        l2_flush(i)
         step()
     torch.cuda.synchronize()
 
@@ -321,7 +340,7 @@ def run_ours(args, ranks):
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
     for i in range(K):
-        flush.fill_(i & 0xFF)
+        l2_flush(i)
         ev[i][0].record(stream)
         step()
         ev[i][1].record(stream)
@@ -340,7 +359,7 @@ def run_ours(args, ranks):
     gqa.trace_collect()
     Kr = min(K, 500)
     for i in range(Kr):
-        flush.fill_(i & 0xFF)
+        l2_flush(i)
         step()
     torch.cuda.synchronize()
     tr = gqa.trace_collect()
@@ -366,7 +385,7 @@ def run_ours(args, ranks):
     d2h = out.numel() * out.element_size()
     e2e_ms = 0.0
     for i in range(Ke + 3):
-        flush.fill_(i & 0xFF)
+        l2_flush(i)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         for k in inputs:
@@ -399,7 +418,10 @@ def run_ours(args, ranks):
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "G": w.G, "D": w.D,
                    "Smax": w.Smax, "paged": w.paged, "kernel": main, "kernel_option": args.kernel,
                    "kv_bytes_per_step_per_gpu": alg["kv_read"],
-                   "l2": "flushed between timed steps (256 MB device write outside the events)",
+                   "l2": {"write_read": "flushed between timed steps (256 MB write, then 256 MB read: "
+                                        "L2 cold and clean; outside the events)",
+                          "write": "flushed between timed steps (256 MB write outside the events)",
+                          "none": "not flushed; inputs larger than L2"}[args.l2_flush],
                    "parallelism": f"replicas x{ranks.world} (independent batches per GPU)",
                    "wall_s_timed_region": wall},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
