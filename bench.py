@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--workload", default="llama3_8b")
     ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "tc"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sched-pad", type=int, default=None,
+                    help="schedule-only tiles per (row, head); default: the library's")
     ap.add_argument("--l2-flush", default="write_read", choices=["write_read", "write", "none"],
                     help="between timed steps: write 256 MB then read another 256 MB (L2 cold "
                          "and clean), write only (dirty lines left to write back), or nothing")
@@ -126,16 +128,18 @@ def algorithmic_bytes(w, t) -> dict:
             "total": kv + 2 * new + w.B * w.Hq * w.D * es + w.B * w.Hq * w.D * 4 + idx}
 
 
-def step_fn(w, t, kernel, out):
+def step_fn(w, t, kernel, out, sched_pad=None):
     import gqa_kv_cache_gb300 as gqa
     if w.paged:
         def run(tt=t):
             gqa.decode_step_paged(tt["q"], tt["k_new"], tt["v_new"], tt["k_blocks"], tt["v_blocks"],
-                                  tt["block_table"], tt["lengths"], out=out, kernel=kernel)
+                                  tt["block_table"], tt["lengths"], out=out, kernel=kernel,
+                                  sched_pad=sched_pad)
     else:
         def run(tt=t):
             gqa.decode_step(tt["q"], tt["k_new"], tt["v_new"], tt["k_cache"], tt["v_cache"],
-                            tt["lengths"], tt.get("slot_ids"), out=out, kernel=kernel)
+                            tt["lengths"], tt.get("slot_ids"), out=out, kernel=kernel,
+                            sched_pad=sched_pad)
     return run
 
 
@@ -307,7 +311,7 @@ def run_ours(args, ranks):
     t = W.generate(w, dev)
     torch.cuda.synchronize()
     out = torch.empty(w.B, w.Hq, w.D, dtype=torch.float32, device=dev)
-    step = step_fn(w, t, args.kernel, out)
+    step = step_fn(w, t, args.kernel, out, args.sched_pad)
     alg = algorithmic_bytes(w, t)
     flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush_r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
@@ -379,7 +383,7 @@ def run_ours(args, ranks):
     dev_in = {k: torch.empty_like(t[k]) for k in inputs}
     tt = dict(t)
     tt.update(dev_in)
-    step_e2e = step_fn(w, tt, args.kernel, out)
+    step_e2e = step_fn(w, tt, args.kernel, out, args.sched_pad)
     out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
     h2d = sum(host[k].numel() * host[k].element_size() for k in inputs)
     d2h = out.numel() * out.element_size()

@@ -47,10 +47,11 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _opts(kernel, grid_ctas):
+def _opts(kernel, grid_ctas, sched_pad=None):
     o = _lib.GqaOptions()
     o.kernel = KERNELS[kernel] if isinstance(kernel, str) else int(kernel)
     o.grid_ctas = int(grid_ctas)
+    o.sched_pad = 0 if sched_pad is None else int(sched_pad) + 1   # 0 = library default
     return o
 
 
@@ -105,7 +106,7 @@ def _common_checks(q, k_new, v_new, caches, lengths, out):
 
 
 def decode_step(q, k_new, v_new, k_cache, v_cache, lengths, slot_ids=None, *, out=None,
-                status=None, kernel="auto", grid_ctas=0, workspace=None, stream=None):
+                status=None, kernel="auto", grid_ctas=0, workspace=None, stream=None, sched_pad=None):
     """One decode step on a dense (R, Hkv, Smax, D) cache (continuous batch
     when ``slot_ids`` is given). Appends in place; returns ``out``. A
     ``workspace`` passed in must be zero-filled before its first use (the
@@ -118,7 +119,7 @@ def decode_step(q, k_new, v_new, k_cache, v_cache, lengths, slot_ids=None, *, ou
         raise ValueError("shape mismatch between q, k_new, v_new and the caches")
     if slot_ids is not None and (slot_ids.dtype != torch.int32 or slot_ids.shape != (B,)):
         raise TypeError("slot_ids must be int32 of shape (B,)")
-    o = _opts(kernel, grid_ctas)
+    o = _opts(kernel, grid_ctas, sched_pad)
     lib = _lib.load()
     need = lib.gqa_workspace_bytes(B, Hq, Hkv, D, _DTYPES[dt], ctypes.byref(o))
     ws = _workspace(q.device, need) if workspace is None else workspace
@@ -131,7 +132,8 @@ def decode_step(q, k_new, v_new, k_cache, v_cache, lengths, slot_ids=None, *, ou
 
 
 def decode_step_paged(q, k_new, v_new, k_blocks, v_blocks, block_table, lengths, *, out=None,
-                      status=None, kernel="auto", grid_ctas=0, workspace=None, stream=None):
+                      status=None, kernel="auto", grid_ctas=0, workspace=None, stream=None,
+                      sched_pad=None):
     """One decode step on a paged cache (num_blocks, Hkv, block_size, D) with
     a (B, max_blocks) int32 block table (-1 = unused). Appends in place."""
     dt, out = _common_checks(q, k_new, v_new, (("k_blocks", k_blocks), ("v_blocks", v_blocks)),
@@ -144,7 +146,7 @@ def decode_step_paged(q, k_new, v_new, k_blocks, v_blocks, block_table, lengths,
             or not block_table.is_contiguous():
         raise TypeError("block_table must be a contiguous int32 (B, max_blocks) tensor")
     MB = block_table.shape[1]
-    o = _opts(kernel, grid_ctas)
+    o = _opts(kernel, grid_ctas, sched_pad)
     lib = _lib.load()
     need = lib.gqa_workspace_bytes(B, Hq, Hkv, D, _DTYPES[dt], ctypes.byref(o))
     ws = _workspace(q.device, need) if workspace is None else workspace

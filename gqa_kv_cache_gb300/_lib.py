@@ -31,7 +31,7 @@ SIGNATURES = {
 
 class GqaOptions(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int), ("grid_ctas", ctypes.c_int),
-                ("reserved", ctypes.c_int * 6)]
+                ("sched_pad", ctypes.c_int), ("reserved", ctypes.c_int * 5)]
 
 
 _lock = threading.Lock()

@@ -13,6 +13,7 @@ using namespace gqa;
 namespace {
 
 constexpr int kMaxDevices = 64;
+constexpr int kDefaultSchedPad = 3;
 
 int sm_count(int dev)
 {
@@ -247,6 +248,8 @@ gqa_status run_step(const Shape &s, const void *q, const void *k_new, const void
     p.max_blocks = s.max_blocks;
     p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)s.D));
     p.tile = kernel == GQA_KERNEL_TC ? tc_tile() : simt_tile();
+    // about the time a CTA spends finishing a sequence, in tiles of streaming
+    p.pad_tiles = (opt && opt->sched_pad > 0) ? opt->sched_pad - 1 : kDefaultSchedPad;
     p.grid = grid;
     char *w = static_cast<char *>(ws);
     p.ws_cnt = reinterpret_cast<int *>(w + lay.off_cnt);

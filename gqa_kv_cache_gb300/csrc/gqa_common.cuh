@@ -48,6 +48,7 @@ struct DecodeParams {
     int paged, num_blocks, block_size, max_blocks;   // paged
     float scale_log2;  // log2(e) / sqrt(D): scores are kept in base-2 units
     int tile;          // T, slots per tile
+    int pad_tiles;     // W, schedule-only tiles appended to every unit (see row_tiles)
     int grid;          // C, CTAs of the decode launch
     // workspace (zero-filled between calls)
     int *ws_cnt;       // [B * Hkv] arrival counters
@@ -84,13 +85,23 @@ __host__ __device__ inline long long row_capacity(const DecodeParams &p)
     return p.paged ? (long long)p.max_blocks * p.block_size : (long long)p.Smax;
 }
 
-// Tiles of batch row b for ONE cache head. Rows with bad content get one tile,
-// which only writes NaN.
-__device__ __forceinline__ int row_tiles(const DecodeParams &p, int L)
+// Tiles of batch row b for ONE cache head that hold data: ceil((L + 1) / T).
+// Rows with bad content get one tile, which only writes NaN.
+__device__ __forceinline__ int real_tiles(const DecodeParams &p, int L)
 {
     if (L < 0 || (long long)L >= row_capacity(p))
         return 1;
-    return (L + p.tile) / p.tile;  // ceil((L + 1) / T)
+    return (L + p.tile) / p.tile;
+}
+
+// Tiles of one unit in the schedule: its real tiles plus W virtual ones that
+// nobody loads or computes. Finishing a unit segment costs a CTA about as much
+// time as streaming a few tiles; counting W extra tiles per unit gives the
+// CTAs whose ranges cross more unit boundaries correspondingly fewer real
+// tiles, so all CTAs finish together.
+__device__ __forceinline__ int row_tiles(const DecodeParams &p, int L)
+{
+    return real_tiles(p, L) + p.pad_tiles;
 }
 
 // CTAs that share the N tiles: min(grid size, N).
@@ -117,7 +128,8 @@ struct TileCursor {
     long long end;    // one past the last tile of the current range
     long long N, C;   // tiles in the list, CTAs sharing them
     int b, kvh, t;    // current row, head, tile within the unit
-    int nt;           // tiles per head of row b
+    int nt;           // tiles per head of row b in the schedule
+    int nr;           // of which real (t < nr holds data; the rest are virtual)
     int L;            // lengths[b]
 };
 
@@ -133,6 +145,7 @@ __device__ __forceinline__ TileCursor cursor_at(const DecodeParams &p, int b, lo
     c.b = b;
     c.L = __ldg(p.lengths + b);
     c.nt = row_tiles(p, c.L);
+    c.nr = real_tiles(p, c.L);
     const long long within = g - run;
     c.kvh = (int)(within / c.nt);
     c.t = (int)(within % c.nt);
@@ -245,22 +258,49 @@ __device__ __forceinline__ void advance(const DecodeParams &p, TileCursor &c)
             if (c.g < c.end) {
                 c.L = __ldg(p.lengths + c.b);
                 c.nt = row_tiles(p, c.L);
+                c.nr = real_tiles(p, c.L);
             }
         }
     }
 }
 
-// Next tile of the walk: along the current range, then from range a into
+// Moves past virtual tiles within the current part of the walk.
+__device__ __forceinline__ void skip_virtual(const DecodeParams &p, TileCursor &c)
+{
+    while (c.g < c.end && c.t >= c.nr)
+        advance(p, c);
+}
+
+// Next real tile of the walk: along the current range, then from range a into
 // range b. False when the CTA has no tile left.
 __device__ __forceinline__ bool walk_next(const DecodeParams &p, TileCursor &c, const TileWalk &w, bool &in_b)
 {
     advance(p, c);
+    skip_virtual(p, c);
     if (c.g < c.end)
         return true;
     if (!in_b && w.b.g < w.b.end) {
         c = w.b;
         in_b = true;
+        skip_virtual(p, c);
+        return c.g < c.end;
+    }
+    return false;
+}
+
+// First real tile of the walk; false when the CTA has none.
+__device__ __forceinline__ bool walk_first(const DecodeParams &p, TileCursor &c, const TileWalk &w, bool &in_b)
+{
+    c = w.a;
+    in_b = false;
+    skip_virtual(p, c);
+    if (c.g < c.end)
         return true;
+    if (w.b.g < w.b.end) {
+        c = w.b;
+        in_b = true;
+        skip_virtual(p, c);
+        return c.g < c.end;
     }
     return false;
 }
@@ -341,7 +381,7 @@ __device__ inline void finish_segment(const DecodeParams &p, const TileCursor &c
 {
     static_assert(NW <= kMergeW && GP <= kMergeG && DP >= DD, "merge buffer too small");
     const int G = p.G, b = cur.b, kvh = cur.kvh;
-    const bool unit_done = (cur.t == cur.nt - 1);
+    const bool unit_done = (cur.t == cur.nr - 1);
     const bool whole = (seg_first_t == 0) && unit_done;
     const int u = b * p.Hkv + kvh;
     const long long P = (long long)u + blockIdx.x;
@@ -420,7 +460,7 @@ __device__ inline void finish_segment(const DecodeParams &p, const TileCursor &c
     sync();
     const long long first_tile = cur.g - cur.t;
     const int first = cta_of_tile(first_tile, cur.N, cur.C);
-    const int last = cta_of_tile(first_tile + cur.nt - 1, cur.N, cur.C);
+    const int last = cta_of_tile(first_tile + cur.nr - 1, cur.N, cur.C);
     if (tid == 0) {
         int old;
         asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(p.ws_cnt + u) : "memory");

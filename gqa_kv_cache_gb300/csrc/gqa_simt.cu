@@ -133,8 +133,9 @@ __global__ void __launch_bounds__(kThreads) simt_decode_kernel(const DecodeParam
     // programmatic dependent of the previous kernel: read no input before it is done
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const TileWalk walk = schedule_walk(p, sched);
-    TileCursor cur = walk.a;
+    TileCursor cur;
     bool in_b = false;
+    bool more = walk_first(p, cur, walk, in_b);
 
     float q[GP][VEC];
     float m[GP], l[GP], o[GP][VEC];
@@ -143,7 +144,6 @@ __global__ void __launch_bounds__(kThreads) simt_decode_kernel(const DecodeParam
     bool seg_start = true;
     int bad_local = 0;
 
-    bool more = cur.g < cur.end;
     while (more) {
         const int b = cur.b, kvh = cur.kvh, L = cur.L;
         if (seg_start) {
@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(kThreads) simt_decode_kernel(const DecodeParam
             }
         }
 
-        const bool unit_done = (cur.t == cur.nt - 1);
+        const bool unit_done = (cur.t == cur.nr - 1);
         const bool cta_done = (cur.g + 1 == cur.end);
         if (unit_done || cta_done) {
             // lane groups of a warp -> one state

@@ -218,8 +218,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         // ------------------------------------------------------ producer --
         uint64_t policy;
         asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
-        TileCursor cur = walk.a;
+        TileCursor cur;
         bool in_b = false;
+        bool more = walk_first(p, cur, walk, in_b);
         long long range_start = cur.g;
         int stage = 0;
         uint32_t phase = 0;
@@ -260,7 +261,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             return r;
         };
         int issued = 0;
-        bool more = cur.g < cur.end;
         Plan pl = more ? plan(cur) : Plan{-1, 0, false, false};
         while (more) {
             if (*((volatile int *)&sh.abort_flag))
@@ -328,8 +328,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // -------------------------------------------------------- consumers --
     const int g0 = lane >> 2, q4 = lane & 3;
     const int row0 = warp * 16;          // this warp's 16 rows of every tile
-    TileCursor cur = walk.a;
+    TileCursor cur;
     bool in_b = false;
+    bool more = walk_first(p, cur, walk, in_b);
     int stage = 0;
     uint32_t phase = 0;
     uint32_t qa[8][2];                   // Q fragments (rows g0 < G), 8 k-steps
@@ -339,7 +340,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     bool seg_start = true, row_good = true, aborted = false;
     int seg_bad = 0;
 
-    bool more = cur.g < cur.end;
     while (more) {
         const int b = cur.b, kvh = cur.kvh, L = cur.L;
         const bool first_of_seg = seg_start;
@@ -389,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         }
 
         if (have && row_good && !tile_bad) {
-            const bool last_tile = (cur.t == cur.nt - 1);
+            const bool last_tile = (cur.t == cur.nr - 1);
             if (last_tile) {
                 // rows of this warp beyond L: zero V; row L: the new token
                 const int lr = L - slot0;            // 0..63
@@ -508,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             phase ^= 1;
         }
 
-        const bool unit_done = (cur.t == cur.nt - 1);
+        const bool unit_done = (cur.t == cur.nr - 1);
         const bool range_done = (cur.g + 1 == cur.end);
         if (unit_done || range_done) {
             // ---- merge the four warps' states and emit

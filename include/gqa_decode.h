@@ -93,7 +93,11 @@ typedef struct gqa_options {
     int grid_ctas;  /* 0: one persistent wave sized to the device; > 0: exactly this
                        many CTAs (each takes a contiguous share of the KV tiles; any
                        value gives the same output up to float32 rounding)             */
-    int reserved[6];
+    int sched_pad;  /* 0: the default; k > 0: count k - 1 extra schedule-only tiles per
+                       (row, cache head) when sharing the tiles among CTAs, which gives
+                       CTAs that finish more sequences fewer tiles (no effect on
+                       results beyond float32 rounding)                                 */
+    int reserved[5];
 } gqa_options;
 
 /* Human-readable name of a status code (static storage). */
