@@ -249,15 +249,23 @@ def peaks():
         return FALLBACK_HBM_GBPS, "fallback"
 
 
-def traffic_for(kernel_name):
-    """Per-launch DRAM bytes of the kernel from the committed ncu summary,
-    if it was taken on the current source of that kernel; else None."""
+def sources_sha(names):
+    """Digest of the kernel sources a profile was taken on."""
     import hashlib
+    h = hashlib.sha256()
+    for n in names:
+        h.update(open(os.path.join(ROOT, "gqa_kv_cache_gb300", "csrc", n), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel_name, workload):
+    """Per-launch DRAM bytes (read + write) of the kernel on this workload from
+    the committed ncu summary, if it was taken on the current sources of that
+    kernel; else None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
-        d = json.load(open(p))[kernel_name]
-        src = os.path.join(ROOT, "gqa_kv_cache_gb300", "csrc", d["source"])
-        if hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != d["source_sha"]:
+        d = json.load(open(p))[kernel_name][workload]
+        if sources_sha(d["sources"]) != d["sources_sha"]:
             return None
         return d["bytes_per_launch"]
     except Exception:
@@ -314,8 +322,8 @@ def run_ours(args, ranks):
     step = step_fn(w, t, args.kernel, out, args.sched_pad)
     alg = algorithmic_bytes(w, t)
     flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    flush_r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
-    flush_sink = torch.empty((), dtype=torch.int64, device=dev)
+    flush_r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_sink = torch.empty((), dtype=torch.float32, device=dev)
 
     def l2_flush(i):
         """Evict the step's data from L2 outside the timed events. Writing a
@@ -326,7 +334,7 @@ def run_ours(args, ranks):
             return
         flush_w.fill_(i & 0xFF)
         if args.l2_flush == "write_read":
-            torch.sum(flush_r, dim=0, dtype=torch.int64, out=flush_sink)
+            torch.sum(flush_r, dim=0, out=flush_sink)
 
     stream = torch.cuda.current_stream()
 
@@ -373,7 +381,7 @@ def run_ours(args, ranks):
     avg_main_s = ms_main / max(n_main, 1) * 1e-3
     hbm_peak, peak_kind = peaks()
     achieved = alg["total"] / avg_main_s / 1e9
-    traffic = traffic_for(main)
+    traffic = traffic_for(main, w.name)
 
     # ---- end to end through the public API, host buffers, copies inside
     Ke = min(K, 500)
