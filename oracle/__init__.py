@@ -1,4 +1,5 @@
-"""CPU oracle for the GQA decode step (float64 loops, plain C).
+"""CPU oracle for the GQA decode step and the read-only attend over a KV
+cache (float64 loops, plain C).
 
 TEST INFRASTRUCTURE. Only the tests, ``__graft_entry__.smoke()`` and the
 benchmark's CPU-baseline / reference leg may import this package. The CUDA
@@ -60,6 +61,16 @@ def _load():
             lib.orc_validate_dense.restype = I
             lib.orc_validate_paged.argtypes = [P, P, I, I, I, I]
             lib.orc_validate_paged.restype = I
+            lib.orc_attend_dense.argtypes = [I, I, P, P, P, P, P, I, I, I, I, I, I,
+                                             P, I, P, I, P]
+            lib.orc_attend_dense.restype = I
+            lib.orc_attend_paged.argtypes = [I, I, P, P, P, P, P, I, I, I, I, I, I, I,
+                                             P, I, P, I, P]
+            lib.orc_attend_paged.restype = I
+            lib.orc_validate_attend_dense.argtypes = [P, P, I, I, I]
+            lib.orc_validate_attend_dense.restype = I
+            lib.orc_validate_attend_paged.argtypes = [P, P, I, I, I, I]
+            lib.orc_validate_attend_paged.restype = I
             lib.orc_default_threads.argtypes = []
             lib.orc_default_threads.restype = I
             _lib = lib
@@ -158,6 +169,71 @@ def decode_paged(q, k_new, v_new, k_blocks, v_blocks, block_table, lengths, *,
                                   0 if rows_a is None else len(rows_a), int(bool(append)),
                                   _ptr(out), nthr, ctypes.addressof(used))
     return OracleResult(st, out, used.value)
+
+
+def attend_dense(q, k_cache, v_cache, lengths, slot_ids=None, *, rows=None,
+                 threads=None) -> OracleResult:
+    """Read-only attend on a dense (R, Hkv, Smax, D) cache: every query head
+    attends slots ``0 .. lengths[b]-1`` of its cache head; nothing is written.
+    ``q`` may be float32 over a bfloat16 cache. Returns ``out`` (B, Hq, D)
+    float64."""
+    qt = _dtype_code(q)
+    kt = _dtype_code(k_cache)
+    if v_cache.dtype != k_cache.dtype:
+        raise TypeError("k_cache and v_cache share one dtype")
+    B, Hq, D = q.shape
+    R, Hkv, Smax, D2 = k_cache.shape
+    assert D2 == D and v_cache.shape == k_cache.shape
+    q, k_cache, v_cache = _c(q), _c(k_cache), _c(v_cache)
+    lengths = _c(lengths, np.int32)
+    slot_ids = _c(slot_ids, np.int32)
+    rows_a = None if rows is None else _c(np.asarray(rows), np.int32)
+    out = np.full((B, Hq, D), np.nan, dtype=np.float64)
+    used = ctypes.c_int(0)
+    nthr = default_threads() if threads is None else int(threads)
+    st = _load().orc_attend_dense(qt, kt, _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(lengths),
+                                  _ptr(slot_ids), B, Hq, Hkv, D, R, Smax, _ptr(rows_a),
+                                  0 if rows_a is None else len(rows_a), _ptr(out), nthr,
+                                  ctypes.addressof(used))
+    return OracleResult(st, out, used.value)
+
+
+def attend_paged(q, k_blocks, v_blocks, block_table, lengths, *, rows=None,
+                 threads=None) -> OracleResult:
+    """Read-only attend on a paged cache; same contract as :func:`attend_dense`."""
+    qt = _dtype_code(q)
+    kt = _dtype_code(k_blocks)
+    if v_blocks.dtype != k_blocks.dtype:
+        raise TypeError("k_blocks and v_blocks share one dtype")
+    B, Hq, D = q.shape
+    NB, Hkv, BS, D2 = k_blocks.shape
+    assert D2 == D and v_blocks.shape == k_blocks.shape
+    MB = block_table.shape[1]
+    q, k_blocks, v_blocks = _c(q), _c(k_blocks), _c(v_blocks)
+    block_table = _c(block_table, np.int32)
+    lengths = _c(lengths, np.int32)
+    rows_a = None if rows is None else _c(np.asarray(rows), np.int32)
+    out = np.full((B, Hq, D), np.nan, dtype=np.float64)
+    used = ctypes.c_int(0)
+    nthr = default_threads() if threads is None else int(threads)
+    st = _load().orc_attend_paged(qt, kt, _ptr(q), _ptr(k_blocks), _ptr(v_blocks),
+                                  _ptr(block_table), _ptr(lengths), B, Hq, Hkv, D, NB, BS, MB,
+                                  _ptr(rows_a), 0 if rows_a is None else len(rows_a), _ptr(out),
+                                  nthr, ctypes.addressof(used))
+    return OracleResult(st, out, used.value)
+
+
+def validate_attend_dense(lengths, slot_ids, R, Smax) -> int:
+    lengths = _c(lengths, np.int32)
+    slot_ids = _c(slot_ids, np.int32)
+    return _load().orc_validate_attend_dense(_ptr(lengths), _ptr(slot_ids), len(lengths), R, Smax)
+
+
+def validate_attend_paged(lengths, block_table, num_blocks, block_size) -> int:
+    lengths = _c(lengths, np.int32)
+    block_table = _c(block_table, np.int32)
+    return _load().orc_validate_attend_paged(_ptr(lengths), _ptr(block_table), len(lengths),
+                                             num_blocks, block_size, block_table.shape[1])
 
 
 def validate_dense(lengths, slot_ids, R, Smax) -> int:

@@ -17,6 +17,10 @@
  *     w_j = exp(s_j - m) / sum_i exp(s_i - m)
  *     o   = sum_j w_j V[r][kvh][j]
  *
+ * The read-only attend (orc_attend_*) is the same computation with no new
+ * token and no write: n = lengths[b] is the number of valid cached slots and
+ * slots 0 .. n-1 are attended; the query may be float32 over a bfloat16 cache.
+ *
  * Sources (web pages, by title and part):
  *  - "KV cache decode step" (tensortonic cs336-l10), problem statement: the new
  *    key and value take position S after the S cached positions, each KV head
@@ -31,7 +35,12 @@
  *    slot_ids as a row map on a [max_seqs, Hkv, max_seq, D] cache (entries in
  *    [0, max_seqs), no two rows sharing one), and the paged block table
  *    ([B, max_blocks], entries -1 or in [0, num_blocks), no repeats within a
- *    row, validated whole before any read, INVALID_ARGUMENT otherwise).
+ *    row, validated whole before any read, INVALID_ARGUMENT otherwise); a
+ *    read-only attend (no key or value given) reads the cache and writes
+ *    nothing ("use attention_over_cache").
+ *  - "Grouped-Query Decode Step", Constraints: the query is float32 while the
+ *    caches are float32 or bfloat16, and every length lies in [1, S]: this is
+ *    the read-only attend's contract.
  *
  * Readings where the pages are silent (each listed in the design notes):
  *  - lengths[b] is the append slot (the number of tokens already cached), and
@@ -39,6 +48,10 @@
  *  - dense: 0 <= lengths[b] <= Smax - 1. paged: 0 <= lengths[b] and
  *    lengths[b] < max_blocks * block_size, and the table entries covering
  *    slots 0 .. lengths[b] are not -1.
+ *  - read-only attend: 1 <= lengths[b] <= Smax (dense) or
+ *    <= max_blocks * block_size (paged, entries covering slots
+ *    0 .. lengths[b]-1 not -1); zero valid slots has no softmax and is
+ *    rejected like any other bad length.
  *  - subtracting the maximum before exp is the textbook rearrangement of the
  *    same quotient; it changes no value beyond rounding.
  *  - bfloat16 values are the upper 16 bits of an IEEE binary32; widening them
@@ -78,14 +91,23 @@ static void copy_vec(void *dst, size_t dst_i, const void *src, size_t src_i, int
 
 /* ---------------------------------------------------------------- checks -- */
 
-/* Dense / slot_ids form: every length in [0, Smax-1]; slot_ids in [0, R) and
- * pairwise distinct; without slot_ids the cache must hold a row per batch row. */
-int orc_validate_dense(const int32_t *lengths, const int32_t *slot_ids, int B, int R, int Smax)
+/* The highest slot a row touches: lengths[b] for the decode step (the append
+ * slot), lengths[b] - 1 for the read-only attend (the last valid slot). */
+static long long last_slot(const int32_t *lengths, int b, int attend)
+{
+    return (long long)lengths[b] - (attend ? 1 : 0);
+}
+
+/* Dense / slot_ids form: every touched slot in [0, Smax-1]; slot_ids in [0, R)
+ * and pairwise distinct; without slot_ids the cache must hold a row per batch
+ * row. */
+static int validate_dense(const int32_t *lengths, const int32_t *slot_ids, int B, int R, int Smax,
+                          int attend)
 {
     if (B < 0 || R < 0 || Smax < 1)
         return ORC_INVALID_ARGUMENT;
     for (int b = 0; b < B; ++b)
-        if (lengths[b] < 0 || lengths[b] > Smax - 1)
+        if (last_slot(lengths, b, attend) < 0 || last_slot(lengths, b, attend) > Smax - 1)
             return ORC_INVALID_ARGUMENT;
     if (!slot_ids)
         return B <= R ? ORC_OK : ORC_INVALID_ARGUMENT;
@@ -99,11 +121,22 @@ int orc_validate_dense(const int32_t *lengths, const int32_t *slot_ids, int B, i
     return ORC_OK;
 }
 
+int orc_validate_dense(const int32_t *lengths, const int32_t *slot_ids, int B, int R, int Smax)
+{
+    return validate_dense(lengths, slot_ids, B, R, Smax, 0);
+}
+
+int orc_validate_attend_dense(const int32_t *lengths, const int32_t *slot_ids, int B, int R,
+                              int Smax)
+{
+    return validate_dense(lengths, slot_ids, B, R, Smax, 1);
+}
+
 /* Paged form: every table entry is -1 or in [0, num_blocks); no block repeats
- * within a row; each length fits the table and the entries that hold slots
- * 0 .. lengths[b] are real blocks. */
-int orc_validate_paged(const int32_t *lengths, const int32_t *block_table, int B,
-                       int num_blocks, int block_size, int max_blocks)
+ * within a row; each touched slot fits the table and the entries that hold
+ * slots 0 .. last touched slot are real blocks. */
+static int validate_paged(const int32_t *lengths, const int32_t *block_table, int B,
+                          int num_blocks, int block_size, int max_blocks, int attend)
 {
     if (B < 0 || num_blocks < 1 || block_size < 1 || max_blocks < 1)
         return ORC_INVALID_ARGUMENT;
@@ -118,14 +151,26 @@ int orc_validate_paged(const int32_t *lengths, const int32_t *block_table, int B
                 if (row[k] == row[i])
                     return ORC_INVALID_ARGUMENT;
         }
-        long long L = lengths[b];
-        if (L < 0 || L >= (long long)max_blocks * block_size)
+        long long last = last_slot(lengths, b, attend);
+        if (last < 0 || last >= (long long)max_blocks * block_size)
             return ORC_INVALID_ARGUMENT;
-        for (long long i = 0; i <= L / block_size; ++i)
+        for (long long i = 0; i <= last / block_size; ++i)
             if (row[i] == -1)
                 return ORC_INVALID_ARGUMENT;
     }
     return ORC_OK;
+}
+
+int orc_validate_paged(const int32_t *lengths, const int32_t *block_table, int B,
+                       int num_blocks, int block_size, int max_blocks)
+{
+    return validate_paged(lengths, block_table, B, num_blocks, block_size, max_blocks, 0);
+}
+
+int orc_validate_attend_paged(const int32_t *lengths, const int32_t *block_table, int B,
+                              int num_blocks, int block_size, int max_blocks)
+{
+    return validate_paged(lengths, block_table, B, num_blocks, block_size, max_blocks, 1);
 }
 
 /* ------------------------------------------------------------ addressing -- */
@@ -155,7 +200,8 @@ static size_t slot_index(const layout *lay, int b, int kvh, int s)
 /* ----------------------------------------------------------------- step -- */
 
 typedef struct {
-    int dtype;
+    int q_dtype, kv_dtype;   /* the decode step has one dtype for all */
+    int attend;              /* 1: read-only attend over slots 0 .. lengths[b]-1 */
     const void *q, *k_new, *v_new;
     void *k_cache, *v_cache;
     const int32_t *lengths;
@@ -170,17 +216,19 @@ typedef struct {
     pthread_mutex_t mu;
 } job;
 
-/* One (batch row, cache head) pair: append, then the G query heads. */
+/* One (batch row, cache head) pair: append (decode step), then the G query
+ * heads over the attended slots 0 .. L. */
 static void one_pair(job *J, int b, int kvh)
 {
     const int D = J->D, G = J->Hq / J->Hkv;
-    const int L = J->lengths[b];
+    const int L = J->attend ? J->lengths[b] - 1 : J->lengths[b];   /* last attended slot */
+    const int from_new = !J->attend && !J->do_append;  /* slot L read from k_new / v_new */
     const size_t new_i = ((size_t)b * J->Hkv + kvh) * D;
 
-    if (J->do_append) {
+    if (!J->attend && J->do_append) {
         size_t dst = slot_index(&J->lay, b, kvh, L);
-        copy_vec(J->k_cache, dst, J->k_new, new_i, D, J->dtype);
-        copy_vec(J->v_cache, dst, J->v_new, new_i, D, J->dtype);
+        copy_vec(J->k_cache, dst, J->k_new, new_i, D, J->kv_dtype);
+        copy_vec(J->v_cache, dst, J->v_new, new_i, D, J->kv_dtype);
     }
 
     double *s = (double *)malloc(sizeof(double) * (size_t)(L + 1));
@@ -188,14 +236,14 @@ static void one_pair(job *J, int b, int kvh)
         const int h = kvh * G + g;           /* floor(h / G) == kvh */
         const size_t q_i = ((size_t)b * J->Hq + h) * D;
 
-        /* scores over slots 0 .. L; slot L is the new token */
+        /* scores over slots 0 .. L; in the decode step slot L is the new token */
         for (int j = 0; j <= L; ++j) {
             double dot = 0.0;
             for (int d = 0; d < D; ++d) {
-                double kd = (j == L && !J->do_append)
-                                ? elem(J->k_new, new_i + d, J->dtype)
-                                : elem(J->k_cache, slot_index(&J->lay, b, kvh, j) + d, J->dtype);
-                dot += elem(J->q, q_i + d, J->dtype) * kd;
+                double kd = (j == L && from_new)
+                                ? elem(J->k_new, new_i + d, J->kv_dtype)
+                                : elem(J->k_cache, slot_index(&J->lay, b, kvh, j) + d, J->kv_dtype);
+                dot += elem(J->q, q_i + d, J->q_dtype) * kd;
             }
             s[j] = dot / sqrt((double)D);
         }
@@ -216,9 +264,9 @@ static void one_pair(job *J, int b, int kvh)
         for (int j = 0; j <= L; ++j) {
             double w = exp(s[j] - m) / Z;
             for (int d = 0; d < D; ++d) {
-                double vd = (j == L && !J->do_append)
-                                ? elem(J->v_new, new_i + d, J->dtype)
-                                : elem(J->v_cache, slot_index(&J->lay, b, kvh, j) + d, J->dtype);
+                double vd = (j == L && from_new)
+                                ? elem(J->v_new, new_i + d, J->kv_dtype)
+                                : elem(J->v_cache, slot_index(&J->lay, b, kvh, j) + d, J->kv_dtype);
                 o[d] += w * vd;
             }
         }
@@ -288,7 +336,7 @@ int orc_decode_dense(int dtype, const void *q, const void *k_new, const void *v_
         return ORC_INVALID_ARGUMENT;
     job J;
     memset(&J, 0, sizeof J);
-    J.dtype = dtype;
+    J.q_dtype = J.kv_dtype = dtype;
     J.q = q; J.k_new = k_new; J.v_new = v_new;
     J.k_cache = k_cache; J.v_cache = v_cache;
     J.lengths = lengths;
@@ -319,7 +367,7 @@ int orc_decode_paged(int dtype, const void *q, const void *k_new, const void *v_
         return ORC_INVALID_ARGUMENT;
     job J;
     memset(&J, 0, sizeof J);
-    J.dtype = dtype;
+    J.q_dtype = J.kv_dtype = dtype;
     J.q = q; J.k_new = k_new; J.v_new = v_new;
     J.k_cache = k_blocks; J.v_cache = v_blocks;
     J.lengths = lengths;
@@ -328,6 +376,70 @@ int orc_decode_paged(int dtype, const void *q, const void *k_new, const void *v_
     J.lay.block_size = block_size; J.lay.max_blocks = max_blocks;
     J.B = B; J.Hq = Hq; J.Hkv = Hkv; J.D = D;
     J.do_append = do_append;
+    J.out = out;
+    J.rows = (const int32_t *)rows; J.nrows = nrows;
+    int n = run(&J, nthreads);
+    if (threads_used)
+        *threads_used = n;
+    return ORC_OK;
+}
+
+static int usable_dtype(int dtype) { return dtype == ORC_F32 || dtype == ORC_BF16; }
+
+/* Read-only attend on a dense or slot_ids cache (R, Hkv, Smax, D): slots
+ * 0 .. lengths[b]-1 of the row, nothing written. q_dtype and kv_dtype are
+ * each ORC_F32 or ORC_BF16. rows/nrows as in orc_decode_dense. */
+int orc_attend_dense(int q_dtype, int kv_dtype, const void *q, const void *k_cache,
+                     const void *v_cache, const int32_t *lengths, const int32_t *slot_ids,
+                     int B, int Hq, int Hkv, int D, int R, int Smax,
+                     const int32_t *rows, int nrows, double *out, int nthreads, int *threads_used)
+{
+    if (!usable_shape(B, Hq, Hkv, D) || !usable_dtype(q_dtype) || !usable_dtype(kv_dtype))
+        return ORC_INVALID_ARGUMENT;
+    if (orc_validate_attend_dense(lengths, slot_ids, B, R, Smax) != ORC_OK)
+        return ORC_INVALID_ARGUMENT;
+    job J;
+    memset(&J, 0, sizeof J);
+    J.q_dtype = q_dtype;
+    J.kv_dtype = kv_dtype;
+    J.attend = 1;
+    J.q = q;
+    J.k_cache = (void *)k_cache; J.v_cache = (void *)v_cache;   /* only read */
+    J.lengths = lengths;
+    J.lay.paged = 0; J.lay.slot_ids = slot_ids;
+    J.lay.Hkv = Hkv; J.lay.D = D; J.lay.Smax = Smax;
+    J.B = B; J.Hq = Hq; J.Hkv = Hkv; J.D = D;
+    J.out = out;
+    J.rows = (const int32_t *)rows; J.nrows = nrows;
+    int n = run(&J, nthreads);
+    if (threads_used)
+        *threads_used = n;
+    return ORC_OK;
+}
+
+/* Read-only attend on a paged cache; same contract as orc_attend_dense. */
+int orc_attend_paged(int q_dtype, int kv_dtype, const void *q, const void *k_blocks,
+                     const void *v_blocks, const int32_t *block_table, const int32_t *lengths,
+                     int B, int Hq, int Hkv, int D, int num_blocks, int block_size, int max_blocks,
+                     const int32_t *rows, int nrows, double *out, int nthreads, int *threads_used)
+{
+    if (!usable_shape(B, Hq, Hkv, D) || !usable_dtype(q_dtype) || !usable_dtype(kv_dtype))
+        return ORC_INVALID_ARGUMENT;
+    if (orc_validate_attend_paged(lengths, block_table, B, num_blocks, block_size, max_blocks)
+        != ORC_OK)
+        return ORC_INVALID_ARGUMENT;
+    job J;
+    memset(&J, 0, sizeof J);
+    J.q_dtype = q_dtype;
+    J.kv_dtype = kv_dtype;
+    J.attend = 1;
+    J.q = q;
+    J.k_cache = (void *)k_blocks; J.v_cache = (void *)v_blocks;
+    J.lengths = lengths;
+    J.lay.paged = 1; J.lay.block_table = block_table;
+    J.lay.Hkv = Hkv; J.lay.D = D;
+    J.lay.block_size = block_size; J.lay.max_blocks = max_blocks;
+    J.B = B; J.Hq = Hq; J.Hkv = Hkv; J.D = D;
     J.out = out;
     J.rows = (const int32_t *)rows; J.nrows = nrows;
     int n = run(&J, nthreads);

@@ -26,11 +26,20 @@ MUTANTS = {
     "row_head_swapped": ("return ((r * lay->Hkv + kvh) * lay->Smax + s) * lay->D;",
                          "return ((kvh * lay->Hkv + r % lay->Hkv) * lay->Smax + s) * lay->D;"),
     "paged_offset": ("(size_t)(s % lay->block_size)) * lay->D;", "(size_t)(s / lay->block_size)) * lay->D;"),
-    "append_skipped": ("    if (J->do_append) {\n        size_t dst", "    if (0) {\n        size_t dst"),
+    "append_skipped": ("    if (!J->attend && J->do_append) {\n        size_t dst", "    if (0) {\n        size_t dst"),
     "slot_ids_ignored": ("size_t r = lay->slot_ids ? (size_t)lay->slot_ids[b] : (size_t)b;", "size_t r = (size_t)b;"),
     "duplicates_accepted": ("if (slot_ids[c] == slot_ids[b])", "if (0)"),
     "paged_repeat_accepted": ("if (row[k] == row[i])", "if (0)"),
     "bf16_shift": ("[i] << 16;", "[i] << 15;"),
+    "attend_stale_slot": ("const int L = J->attend ? J->lengths[b] - 1 : J->lengths[b];",
+                          "const int L = J->lengths[b];"),
+    "attend_query_rounded": ("dot += elem(J->q, q_i + d, J->q_dtype) * kd;",
+                             "{ double x = elem(J->q, q_i + d, J->q_dtype);"
+                             " if (x != 0) x = ldexp(nearbyint(ldexp(x, 7 - ilogb(x))), ilogb(x) - 7);"
+                             " dot += x * kd; }"),
+    "attend_empty_accepted": ("if (last_slot(lengths, b, attend) < 0 ||", "if (last_slot(lengths, b, attend) < -1 ||"),
+    "paged_last_block_unchecked": ("for (long long i = 0; i <= last / block_size; ++i)",
+                                   "for (long long i = 0; i < last / block_size; ++i)"),
     "query_head_offset": ("const size_t q_i = ((size_t)b * J->Hq + h) * D;", "const size_t q_i = ((size_t)b * J->Hq + g) * D;"),
 }
 

@@ -471,3 +471,178 @@ def test_validate_paged_rules():
     r = oracle.decode_paged(q, np.ones((2, 1, 4), np.float32), np.ones((2, 1, 4), np.float32),
                             kb, kb.copy(), bad, L)
     assert r.status == oracle.INVALID_ARGUMENT and not kb.any()
+
+
+# ------------------------------------------------- read-only attend (no append)
+#
+# [P2] is itself the read-only form: its lengths count the valid slots (the
+# new token already stored among them), the query is float32 and the caches
+# float32 or bfloat16. [P5]'s attention_over_cache reads the cache and
+# writes nothing.
+
+def _to_bf16_bits_exact(a):
+    """float32 array -> bf16 bit pattern; asserts every value is representable."""
+    a = np.ascontiguousarray(a, np.float32)
+    bits = (a.view(np.uint32) >> 16).astype(np.uint16)
+    back = (bits.astype(np.uint32) << 16).view(np.float32)
+    assert np.array_equal(back, a), "value not exactly representable in bfloat16"
+    return bits
+
+
+@pytest.mark.parametrize("cache_dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("ex", _golden("grouped_query_decode_step_examples.json")["examples"],
+                         ids=lambda e: e["name"])
+def test_p2_examples_attend(ex, cache_dtype):
+    """[P2] Examples 1-3 in the page's own contract: lengths as printed,
+    float32 query, the cache transposed to (B,Hkv,S,D). Every value printed in
+    the examples is exact in bfloat16, so a bfloat16 cache must give the same
+    outputs; nothing is written."""
+    q = np.asarray(ex["query"], np.float32)
+    kc = np.ascontiguousarray(np.asarray(ex["key_cache"], np.float32).transpose(0, 2, 1, 3))
+    vc = np.ascontiguousarray(np.asarray(ex["value_cache"], np.float32).transpose(0, 2, 1, 3))
+    if cache_dtype == "bf16":
+        kc, vc = _to_bf16_bits_exact(kc), _to_bf16_bits_exact(vc)
+    before = kc.tobytes() + vc.tobytes()
+    r = oracle.attend_dense(q, kc, vc, np.asarray(ex["lengths"], np.int32))
+    assert r.status == oracle.OK
+    np.testing.assert_allclose(r.out, ex["output"], rtol=0, atol=5e-7)
+    assert kc.tobytes() + vc.tobytes() == before
+
+
+def _attend_brute(q, kc, vc, lens):
+    """[P2] formula literally, pure Python: w_j = e^{s_j} / sum_m e^{s_m} over
+    the slots j < lengths[b]."""
+    B, Hq, D = q.shape
+    G = Hq // kc.shape[1]
+    out = np.zeros((B, Hq, D))
+    for b in range(B):
+        n = int(lens[b])
+        for h in range(Hq):
+            qs = [float(x) for x in q[b, h]]
+            e = [math.exp(sum(a * float(c) for a, c in zip(qs, kc[b, h // G, j])) / math.sqrt(D))
+                 for j in range(n)]
+            z = sum(e)
+            for d in range(D):
+                out[b, h, d] = sum(e[j] * float(vc[b, h // G, j, d]) for j in range(n)) / z
+    return out
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_attend_brute_force_tiny(seed):
+    """Random tiny cases within the [P2] Constraints (B 1-3, S 3-8, Hq 2-8,
+    D 2-4, Hkv | Hq, 1 <= lengths <= S, stale slots much larger)."""
+    rng = np.random.default_rng(100 + seed)
+    B, S, D = rng.integers(1, 4), rng.integers(3, 9), rng.integers(2, 5)
+    Hq = int(rng.choice([2, 3, 4, 6, 8]))
+    Hkv = int(rng.choice([d for d in range(1, Hq + 1) if Hq % d == 0]))
+    lens = rng.integers(1, S + 1, size=B).astype(np.int32)
+    q = rng.normal(size=(B, Hq, D)).astype(np.float32)
+    kc = (rng.normal(size=(B, Hkv, S, D)) * 50).astype(np.float32)
+    vc = (rng.normal(size=(B, Hkv, S, D)) * 50).astype(np.float32)
+    for b in range(B):
+        kc[b, :, :lens[b]] /= 50
+        vc[b, :, :lens[b]] /= 50
+    r = oracle.attend_dense(q, kc, vc, lens)
+    np.testing.assert_allclose(r.out, _attend_brute(q, kc, vc, lens), rtol=1e-12, atol=1e-12)
+
+
+def test_attend_float32_query_over_bf16_cache_library_sdpa():
+    """[P2] Requirements: a float32 query over bfloat16 caches widened to
+    float32. torch's scaled_dot_product_attention in float64 on the widened
+    valid prefix must agree; the query carries bits below bfloat16's
+    precision, so an oracle that rounded it would be off by ~1e-3."""
+    w = W.small("llama3_8b", dtype="bf16", B=3, Hq=8, Hkv=2, D=32, Smax=40,
+                len_lo=1, len_hi=39, seed=31)
+    t = W.generate(w)
+    q32 = torch.randn(w.B, w.Hq, w.D, generator=torch.Generator().manual_seed(5)) * (1 + 2 ** -12)
+    lens = t["lengths"] + 1                   # valid-slot counts in [2, 40]
+    a = oracle_inputs(t)
+    r = oracle.attend_dense(to_np(q32), a["k_cache"], a["v_cache"], to_np(lens))
+    assert r.status == oracle.OK
+    G = w.Hq // w.Hkv
+    for b in range(w.B):
+        n = int(lens[b])
+        k = t["k_cache"][b, :, :n].double().repeat_interleave(G, 0)
+        v = t["v_cache"][b, :, :n].double().repeat_interleave(G, 0)
+        o = torch.nn.functional.scaled_dot_product_attention(q32[b][:, None].double(), k, v)[:, 0]
+        np.testing.assert_allclose(r.out[b], o.numpy(), rtol=1e-12, atol=1e-12)
+        qr = q32[b].to(torch.bfloat16).double()
+        o_rounded = torch.nn.functional.scaled_dot_product_attention(qr[:, None], k, v)[:, 0]
+        assert np.abs(r.out[b] - o_rounded.numpy()).max() > 1e-6
+
+
+def test_attend_single_slot_returns_value():
+    """[P2] Example 2 row 1: one valid slot -> every head returns its value."""
+    w, a = _rand_case(32)
+    lens = np.ones(w.B, np.int32)
+    r = oracle.attend_dense(a["q"], a["k_cache"], a["v_cache"], lens)
+    want = np.repeat(a["v_cache"][:, :, 0].astype(np.float64), w.G, 1)
+    assert np.array_equal(r.out, want)
+
+
+def test_attend_stale_slots_cannot_matter():
+    """[P2]: slot lengths[b] and beyond get zero weight, whatever they hold."""
+    w, a = _rand_case(33)
+    lens = a["lengths"] + 1
+    r0 = oracle.attend_dense(a["q"], a["k_cache"], a["v_cache"], lens)
+    for fill in (1e30, np.inf, np.nan):
+        kc, vc = a["k_cache"].copy(), a["v_cache"].copy()
+        for b in range(w.B):
+            kc[b, :, lens[b]:] = fill
+            vc[b, :, lens[b]:] = -fill
+        assert oracle.attend_dense(a["q"], kc, vc, lens).out.tobytes() == r0.out.tobytes()
+
+
+def test_attend_paged_equals_dense_and_slot_ids():
+    """The same logical content through a paged table, through slot_ids and
+    densely gives bit-identical outputs; unused blocks (NaN) are never read."""
+    bs, max_blocks = 4, 6
+    w = W.small("paged", dtype="bf16", B=3, Hq=8, Hkv=2, D=8, num_blocks=24, block_size=bs,
+                max_blocks=max_blocks, len_lo=0, len_hi=22, seed=34)
+    a = oracle_inputs(W.generate(w))
+    bt = a["block_table"]
+    lens = a["lengths"] + 1
+    Smax = max_blocks * bs
+    dense_k = np.zeros((w.B, w.Hkv, Smax, w.D), np.uint16)
+    dense_v = np.zeros_like(dense_k)
+    for b in range(w.B):
+        for s in range(Smax):
+            if bt[b, s // bs] >= 0:
+                dense_k[b, :, s] = a["k_blocks"][bt[b, s // bs], :, s % bs]
+                dense_v[b, :, s] = a["v_blocks"][bt[b, s // bs], :, s % bs]
+    used = set(bt[bt >= 0].tolist())
+    kb, vb = a["k_blocks"].copy(), a["v_blocks"].copy()
+    for blk in range(w.num_blocks):
+        if blk not in used:
+            kb[blk] = vb[blk] = 0x7FC0
+    r0 = oracle.attend_dense(a["q"], dense_k, dense_v, lens)
+    r1 = oracle.attend_paged(a["q"], kb, vb, bt, lens)
+    assert r1.status == oracle.OK and r0.out.tobytes() == r1.out.tobytes()
+    sid = np.array([4, 0, 2], np.int32)
+    rows_k = np.full((5, w.Hkv, Smax, w.D), 0x7FC0, np.uint16)
+    rows_v = rows_k.copy()
+    rows_k[sid], rows_v[sid] = dense_k, dense_v
+    r2 = oracle.attend_dense(a["q"], rows_k, rows_v, lens, sid)
+    assert r2.out.tobytes() == r0.out.tobytes()
+
+
+def test_attend_validate_rules():
+    """Our reading of [P2] Constraints for the read-only attend: 1 <= lengths
+    <= Smax (zero valid slots has no softmax); paged, the entries holding
+    slots 0..lengths[b]-1 must be real; [P5] slot_ids rules unchanged."""
+    ok = oracle.OK
+    bad = oracle.INVALID_ARGUMENT
+    assert oracle.validate_attend_dense(np.array([1, 10], np.int32), None, 2, 10) == ok
+    assert oracle.validate_attend_dense(np.array([0, 10], np.int32), None, 2, 10) == bad
+    assert oracle.validate_attend_dense(np.array([1, 11], np.int32), None, 2, 10) == bad
+    assert oracle.validate_attend_dense(np.array([1, 2], np.int32), np.array([3, 3], np.int32), 4, 10) == bad
+    bt = np.array([[3, -1, -1], [0, 2, -1]], np.int32)
+    assert oracle.validate_attend_paged(np.array([4, 8], np.int32), bt, 6, 4) == ok    # exactly full blocks
+    assert oracle.validate_attend_paged(np.array([5, 8], np.int32), bt, 6, 4) == bad   # slot 4 needs entry 1
+    assert oracle.validate_attend_paged(np.array([4, 0], np.int32), bt, 6, 4) == bad
+    assert oracle.validate_attend_paged(np.array([4, 13], np.int32), bt, 6, 4) == bad  # beyond the table
+    # the decode step's reading of the same numbers differs by one slot
+    assert oracle.validate_paged(np.array([4, 7], np.int32), bt, 6, 4) == bad          # slot 4 for the append
+    r = oracle.attend_dense(np.zeros((1, 1, 2), np.float32), np.zeros((1, 1, 3, 2), np.float32),
+                            np.zeros((1, 1, 3, 2), np.float32), np.array([0], np.int32))
+    assert r.status == bad and np.isnan(r.out).all()
