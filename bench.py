@@ -19,6 +19,9 @@ Prints ONE JSON line (rank 0):
   cpu_baseline  the float64 CPU oracle on this machine's host cores.
 With --impl reference the oracle itself is timed as the reference arm.
 
+--op attend times the read-only attend instead (no append; lengths count the
+valid slots; a float32 query over the workload's cache unless --q-dtype cache).
+
 Multi-GPU (torchrun): every rank runs an independent replica with its own
 batch (weak scaling, no data-path collective); times are max over ranks.
 """
@@ -36,6 +39,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "KV-cache HBM GB/s & fraction of ~8 TB/s peak; µs per GQA decode step"
+METRIC_ATTEND = "KV-cache HBM GB/s & fraction of ~8 TB/s peak; µs per GQA read-only attend"
 UNIT = "GB/s"
 NOMINAL_HBM_GBPS = 8000.0
 FALLBACK_HBM_GBPS = 6800.0
@@ -50,6 +54,10 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama3_8b")
     ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "tc"])
+    ap.add_argument("--op", default="decode", choices=["decode", "attend"],
+                    help="decode step (default) or the read-only attend")
+    ap.add_argument("--q-dtype", default=None, choices=["cache", "f32"],
+                    help="attend only: query dtype (default f32)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sched-pad", type=int, default=None,
                     help="schedule-only tiles per (row, head); default: the library's")
@@ -112,25 +120,37 @@ def workload(name, rank):
     return w
 
 
-def algorithmic_bytes(w, t) -> dict:
+def algorithmic_bytes(w, t, attend=False) -> dict:
     """Bytes the step must move (no split partials): the KV read, the append
-    write, the new K/V, q, out and the index reads."""
+    write, the new K/V, q, out and the index reads. The decode step reads the
+    lengths[b] cached slots (slot lengths[b] comes from k_new / v_new); the
+    read-only attend reads its lengths[b] valid slots and appends nothing."""
     import torch
     L = t["lengths"].to(torch.int64)
     es = w.elem_bytes
     kv = int(L.sum().item()) * w.Hkv * w.D * 2 * es
-    new = w.B * w.Hkv * w.D * es * 2
+    new = 0 if attend else w.B * w.Hkv * w.D * es * 2
     idx = w.B * 4 * (2 if w.slot_ids else 1)
     if w.paged:
-        idx += int(((L + w.block_size) // w.block_size).sum().item()) * 4
+        touched = L if attend else L + 1
+        idx += int(((touched + w.block_size - 1) // w.block_size).sum().item()) * 4
+    q = t["q"].numel() * t["q"].element_size()
     return {"kv_read": kv, "append_write": new, "new_kv_read": new,
-            "q_read": w.B * w.Hq * w.D * es, "out_write": w.B * w.Hq * w.D * 4, "index_read": idx,
-            "total": kv + 2 * new + w.B * w.Hq * w.D * es + w.B * w.Hq * w.D * 4 + idx}
+            "q_read": q, "out_write": w.B * w.Hq * w.D * 4, "index_read": idx,
+            "total": kv + 2 * new + q + w.B * w.Hq * w.D * 4 + idx}
 
 
-def step_fn(w, t, kernel, out, sched_pad=None):
+def step_fn(w, t, kernel, out, sched_pad=None, attend=False):
     import gqa_kv_cache_gb300 as gqa
-    if w.paged:
+    if attend and w.paged:
+        def run(tt=t):
+            gqa.attend_paged(tt["q"], tt["k_blocks"], tt["v_blocks"], tt["block_table"], tt["lengths"],
+                             out=out, kernel=kernel, sched_pad=sched_pad)
+    elif attend:
+        def run(tt=t):
+            gqa.attend(tt["q"], tt["k_cache"], tt["v_cache"], tt["lengths"], tt.get("slot_ids"),
+                       out=out, kernel=kernel, sched_pad=sched_pad)
+    elif w.paged:
         def run(tt=t):
             gqa.decode_step_paged(tt["q"], tt["k_new"], tt["v_new"], tt["k_blocks"], tt["v_blocks"],
                                   tt["block_table"], tt["lengths"], out=out, kernel=kernel,
@@ -216,7 +236,10 @@ def oracle_rate(w, t, rows, repeats=3):
         return x.view(torch.int16).numpy().view(np.uint16).copy() if x.dtype == torch.bfloat16 \
             else x.numpy().copy()
 
-    q, kn, vn, L = host(t["q"][sel]), host(t["k_new"][sel]), host(t["v_new"][sel]), host(t["lengths"][sel])
+    attend = "k_new" not in t
+    q, L = host(t["q"][sel]), host(t["lengths"][sel])
+    if not attend:
+        kn, vn = host(t["k_new"][sel]), host(t["v_new"][sel])
     if w.paged:
         bt = t["block_table"][sel].cpu().numpy()
         used = sorted(set(int(x) for x in bt[bt >= 0].tolist()))
@@ -224,11 +247,13 @@ def oracle_rate(w, t, rows, repeats=3):
         idx = torch.tensor(used, dtype=torch.long, device=t["q"].device)
         kb, vb = host(t["k_blocks"][idx]), host(t["v_blocks"][idx])
         btr = np.vectorize(lambda x: remap.get(int(x), -1))(bt).astype(np.int32)
-        run = lambda: oracle.decode_paged(q, kn, vn, kb, vb, btr, L, append=False)
+        run = (lambda: oracle.attend_paged(q, kb, vb, btr, L)) if attend else \
+            (lambda: oracle.decode_paged(q, kn, vn, kb, vb, btr, L, append=False))
     else:
         cr = t["slot_ids"][sel].long() if "slot_ids" in t else sel
         kc, vc = host(t["k_cache"][cr]), host(t["v_cache"][cr])
-        run = lambda: oracle.decode_dense(q, kn, vn, kc, vc, L, append=False)
+        run = (lambda: oracle.attend_dense(q, kc, vc, L)) if attend else \
+            (lambda: oracle.decode_dense(q, kn, vn, kc, vc, L, append=False))
     r = run()                                   # warm-up
     times = []
     for _ in range(repeats):
@@ -283,7 +308,8 @@ def run_reference(args, ranks):
     w = workload(args.workload, 0)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     import workloads as W
-    t = W.generate(w, dev)
+    attend = args.op == "attend"
+    t = W.generate(w, dev, attend=attend, q_f32=attend and args.q_dtype != "cache")
     n = min(w.B, 4)
     for i in range(args.warmup):
         oracle_rate(w, t, [(i * n + k) % w.B for k in range(n)], repeats=1)
@@ -296,11 +322,11 @@ def run_reference(args, ranks):
         t_total += sec
     value = kv_total / t_total / 1e9
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "impl": "reference", "metric": METRIC_ATTEND if attend else METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_total / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv,
-                                        "D": w.D, "sample_rows_per_step": n},
+        "data": "synthetic", "config": {"workload": w.name, "op": args.op, "B": w.B, "Hq": w.Hq,
+                                        "Hkv": w.Hkv, "D": w.D, "sample_rows_per_step": n},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": f"{n} of {w.B} batch rows per step, rotating, float64 loops"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -316,11 +342,12 @@ def run_ours(args, ranks):
     torch.cuda.set_device(ranks.local)
     dev = torch.device("cuda", ranks.local)
     w = workload(args.workload, ranks.rank)
-    t = W.generate(w, dev)
+    attend = args.op == "attend"
+    t = W.generate(w, dev, attend=attend, q_f32=attend and args.q_dtype != "cache")
     torch.cuda.synchronize()
     out = torch.empty(w.B, w.Hq, w.D, dtype=torch.float32, device=dev)
-    step = step_fn(w, t, args.kernel, out, args.sched_pad)
-    alg = algorithmic_bytes(w, t)
+    step = step_fn(w, t, args.kernel, out, args.sched_pad, attend)
+    alg = algorithmic_bytes(w, t, attend)
     flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush_r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     flush_sink = torch.empty((), dtype=torch.float32, device=dev)
@@ -385,13 +412,14 @@ def run_ours(args, ranks):
 
     # ---- end to end through the public API, host buffers, copies inside
     Ke = min(K, 500)
-    inputs = ["q", "k_new", "v_new", "lengths"] + (["slot_ids"] if "slot_ids" in t else []) + \
+    inputs = ["q", "lengths"] + ([] if attend else ["k_new", "v_new"]) + \
+        (["slot_ids"] if "slot_ids" in t else []) + \
         (["block_table"] if "block_table" in t else [])
     host = {k: t[k].cpu().pin_memory() for k in inputs}
     dev_in = {k: torch.empty_like(t[k]) for k in inputs}
     tt = dict(t)
     tt.update(dev_in)
-    step_e2e = step_fn(w, tt, args.kernel, out, args.sched_pad)
+    step_e2e = step_fn(w, tt, args.kernel, out, args.sched_pad, attend)
     out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
     h2d = sum(host[k].numel() * host[k].element_size() for k in inputs)
     d2h = out.numel() * out.element_size()
@@ -421,13 +449,15 @@ def run_ours(args, ranks):
                          f"median of 3 after 1 warm-up, {sec:.2f} s per pass"}
 
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ranks.world, "steps": K,
+        "metric": METRIC_ATTEND if attend else METRIC, "value": value, "unit": UNIT,
+        "n_gpus": ranks.world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "us_per_step": ms_per_step * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic",
         "frac_of_8TBps": value / ranks.world / NOMINAL_HBM_GBPS,
         "frac_of_measured_hbm": value / ranks.world / hbm_peak,
-        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "G": w.G, "D": w.D,
+        "config": {"workload": w.name, "op": args.op, "q_dtype": str(t["q"].dtype).replace("torch.", ""),
+                   "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "G": w.G, "D": w.D,
                    "Smax": w.Smax, "paged": w.paged, "kernel": main, "kernel_option": args.kernel,
                    "kv_bytes_per_step_per_gpu": alg["kv_read"],
                    "l2": {"write_read": "flushed between timed steps (256 MB write, then 256 MB read: "

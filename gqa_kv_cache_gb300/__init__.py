@@ -11,6 +11,10 @@ One decode step, per batch row b: the new key/value are appended in place at
 slot ``lengths[b]`` of the row's cache, and every query head h attends over
 slots ``0..lengths[b]`` of cache head ``h // (Hq // Hkv)`` with a float32
 softmax of ``q.K/sqrt(D)``; the output is float32 (B, Hq, D).
+
+The read-only attend (``attend``, ``attend_paged``) attends slots
+``0..lengths[b]-1`` (lengths counts the valid slots) and writes nothing but
+its output; its query may be float32 over a bfloat16 cache.
 """
 from __future__ import annotations
 
@@ -20,7 +24,8 @@ import torch
 
 from . import _lib
 
-__all__ = ["decode_step", "decode_step_paged", "workspace_bytes", "validate",
+__all__ = ["decode_step", "decode_step_paged", "attend", "attend_paged", "workspace_bytes",
+           "validate", "validate_attend",
            "GqaError", "trace_enable", "trace_collect", "KERNELS", "library_path"]
 
 OK, INVALID_ARGUMENT, UNSUPPORTED, CUDA_ERROR, WORKSPACE = 0, 1, 2, 3, 4
@@ -80,15 +85,19 @@ def workspace_bytes(B, Hq, Hkv, D, dtype=torch.bfloat16, kernel="auto", grid_cta
     return int(_lib.load().gqa_workspace_bytes(B, Hq, Hkv, D, _DTYPES[dtype], ctypes.byref(o)))
 
 
-def _common_checks(q, k_new, v_new, caches, lengths, out):
+def _common_checks(q, k_new, v_new, caches, lengths, out, q_any_dtype=False):
+    """Checks shared by the entry points; returns (cache dtype, out)."""
     if not q.is_cuda:
         raise ValueError("tensors must be on a CUDA device")
-    dt = q.dtype
-    if dt not in _DTYPES:
+    if q.dtype not in _DTYPES:
         raise TypeError("q must be float32 or bfloat16")
-    for name, t in (("k_new", k_new), ("v_new", v_new), *caches):
+    dt = caches[0][1].dtype if q_any_dtype else q.dtype
+    if dt not in _DTYPES:
+        raise TypeError("the cache must be float32 or bfloat16")
+    news = () if k_new is None else (("k_new", k_new), ("v_new", v_new))
+    for name, t in (*news, *caches):
         if t.dtype != dt:
-            raise TypeError(f"{name} must have q's dtype {dt}")
+            raise TypeError(f"{name} must have dtype {dt}")
         if t.device != q.device:
             raise ValueError(f"{name} is on {t.device}, q on {q.device}")
         if not t.is_contiguous():
@@ -159,22 +168,84 @@ def decode_step_paged(q, k_new, v_new, k_blocks, v_blocks, block_table, lengths,
     return out
 
 
-def validate(lengths, *, slot_ids=None, R=None, Smax=None, block_table=None, num_blocks=None,
-             block_size=None, stream=None) -> bool:
-    """Full content check on the GPU (synchronous). True when valid."""
+def attend(q, k_cache, v_cache, lengths, slot_ids=None, *, out=None, status=None, kernel="auto",
+           grid_ctas=0, workspace=None, stream=None, sched_pad=None):
+    """Read-only attend on a dense (R, Hkv, Smax, D) cache: slots
+    ``0..lengths[b]-1`` (1 <= lengths[b] <= Smax), nothing written but ``out``.
+    ``q`` (B, Hq, D) is float32 or bfloat16 whatever the cache dtype."""
+    dt, out = _common_checks(q, None, None, (("k_cache", k_cache), ("v_cache", v_cache)),
+                             lengths, out, q_any_dtype=True)
+    B, Hq, D = q.shape
+    R, Hkv, Smax, D2 = k_cache.shape
+    if D2 != D or v_cache.shape != k_cache.shape or Hq % Hkv:
+        raise ValueError("shape mismatch between q and the caches")
+    if slot_ids is not None and (slot_ids.dtype != torch.int32 or slot_ids.shape != (B,)):
+        raise TypeError("slot_ids must be int32 of shape (B,)")
+    o = _opts(kernel, grid_ctas, sched_pad)
+    lib = _lib.load()
+    need = lib.gqa_workspace_bytes(B, Hq, Hkv, D, _DTYPES[dt], ctypes.byref(o))
+    ws = _workspace(q.device, need) if workspace is None else workspace
+    code = lib.gqa_attend(_ptr(q), _DTYPES[q.dtype], _ptr(k_cache), _ptr(v_cache), _ptr(lengths),
+                          _ptr(slot_ids), _ptr(out), B, Hq, Hkv, D, R, Smax, _DTYPES[dt], _ptr(ws),
+                          ws.numel() * ws.element_size(), _ptr(status), _stream(stream),
+                          ctypes.byref(o))
+    _check(code, "gqa_attend")
+    return out
+
+
+def attend_paged(q, k_blocks, v_blocks, block_table, lengths, *, out=None, status=None,
+                 kernel="auto", grid_ctas=0, workspace=None, stream=None, sched_pad=None):
+    """Read-only attend on a paged cache (num_blocks, Hkv, block_size, D)."""
+    dt, out = _common_checks(q, None, None, (("k_blocks", k_blocks), ("v_blocks", v_blocks)),
+                             lengths, out, q_any_dtype=True)
+    B, Hq, D = q.shape
+    NB, Hkv, BS, D2 = k_blocks.shape
+    if D2 != D or v_blocks.shape != k_blocks.shape or Hq % Hkv:
+        raise ValueError("shape mismatch between q and the blocks")
+    if block_table.dtype != torch.int32 or block_table.dim() != 2 or block_table.shape[0] != B \
+            or not block_table.is_contiguous():
+        raise TypeError("block_table must be a contiguous int32 (B, max_blocks) tensor")
+    o = _opts(kernel, grid_ctas, sched_pad)
+    lib = _lib.load()
+    need = lib.gqa_workspace_bytes(B, Hq, Hkv, D, _DTYPES[dt], ctypes.byref(o))
+    ws = _workspace(q.device, need) if workspace is None else workspace
+    code = lib.gqa_attend_paged(_ptr(q), _DTYPES[q.dtype], _ptr(k_blocks), _ptr(v_blocks),
+                                _ptr(block_table), _ptr(lengths), _ptr(out), B, Hq, Hkv, D, NB, BS,
+                                block_table.shape[1], _DTYPES[dt], _ptr(ws),
+                                ws.numel() * ws.element_size(), _ptr(status), _stream(stream),
+                                ctypes.byref(o))
+    _check(code, "gqa_attend_paged")
+    return out
+
+
+def _validate(fn, what, lengths, slot_ids, R, Smax, block_table, num_blocks, block_size, stream):
     B = lengths.shape[0]
     res = torch.empty(1, dtype=torch.int32, device=lengths.device)
-    lib = _lib.load()
     if block_table is not None:
-        code = lib.gqa_validate(_ptr(lengths), None, _ptr(block_table), B, 0, 0, num_blocks,
-                                block_size, block_table.shape[1], _ptr(res), _stream(stream))
+        code = fn(_ptr(lengths), None, _ptr(block_table), B, 0, 0, num_blocks, block_size,
+                  block_table.shape[1], _ptr(res), _stream(stream))
     else:
-        code = lib.gqa_validate(_ptr(lengths), _ptr(slot_ids), None, B, R, Smax, 0, 0, 0,
-                                _ptr(res), _stream(stream))
+        code = fn(_ptr(lengths), _ptr(slot_ids), None, B, R, Smax, 0, 0, 0, _ptr(res),
+                  _stream(stream))
     if code == INVALID_ARGUMENT:
         return False
-    _check(code, "gqa_validate")
+    _check(code, what)
     return True
+
+
+def validate(lengths, *, slot_ids=None, R=None, Smax=None, block_table=None, num_blocks=None,
+             block_size=None, stream=None) -> bool:
+    """Full content check on the GPU for the decode step (synchronous). True
+    when valid."""
+    return _validate(_lib.load().gqa_validate, "gqa_validate", lengths, slot_ids, R, Smax,
+                     block_table, num_blocks, block_size, stream)
+
+
+def validate_attend(lengths, *, slot_ids=None, R=None, Smax=None, block_table=None,
+                    num_blocks=None, block_size=None, stream=None) -> bool:
+    """Full content check on the GPU for the read-only attend (synchronous)."""
+    return _validate(_lib.load().gqa_validate_attend, "gqa_validate_attend", lengths, slot_ids, R,
+                     Smax, block_table, num_blocks, block_size, stream)
 
 
 def trace_enable(on: bool = True) -> bool:

@@ -20,6 +20,9 @@ SIGNATURES = {
     "gqa_decode_step_ex": (I, [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, Z, P, P, P]),
     "gqa_decode_step_paged_ex": (I, [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, P, Z, P, P, P]),
     "gqa_validate": (I, [P, P, P, I, I, I, I, I, I, P, P]),
+    "gqa_validate_attend": (I, [P, P, P, I, I, I, I, I, I, P, P]),
+    "gqa_attend": (I, [P, I, P, P, P, P, P, I, I, I, I, I, I, I, P, Z, P, P, P]),
+    "gqa_attend_paged": (I, [P, I, P, P, P, P, P, I, I, I, I, I, I, I, I, P, Z, P, P, P]),
     "gqa_trace_enable": (I, [I]),
     "gqa_trace_collect": (I, [I, P, P]),
     "gqa_kernel_name": (ctypes.c_char_p, [I]),

@@ -170,17 +170,21 @@ bool encode_cache_map(CUtensorMap *m, void *base, int D, long long rows_per_head
 
 struct Shape {
     int B, Hq, Hkv, D;
-    gqa_dtype dt;
+    gqa_dtype dt;  // the cache (and k_new / v_new)
     bool paged;
     int R, Smax;
     int num_blocks, block_size, max_blocks;
+    bool attend = false;          // read-only attend: no new token, nothing written but out
+    gqa_dtype q_dt = GQA_DTYPE_F32;
 };
+
+bool valid_dtype(gqa_dtype d) { return d == GQA_DTYPE_F32 || d == GQA_DTYPE_BF16; }
 
 gqa_status check_shape(const Shape &s)
 {
     if (s.B < 0 || s.Hq < 1 || s.Hkv < 1 || s.D < 1 || s.Hq % s.Hkv != 0)
         return GQA_ERR_INVALID_ARGUMENT;
-    if (s.dt != GQA_DTYPE_F32 && s.dt != GQA_DTYPE_BF16)
+    if (!valid_dtype(s.dt) || !valid_dtype(s.q_dt))
         return GQA_ERR_INVALID_ARGUMENT;
     if (s.paged) {
         if (s.num_blocks < 1 || s.block_size < 1 || s.max_blocks < 1)
@@ -206,12 +210,15 @@ gqa_status run_step(const Shape &s, const void *q, const void *k_new, const void
         return st;
     if (s.B == 0)
         return GQA_OK;
-    if (!q || !k_new || !v_new || !kc || !vc || !lengths || !out || (s.paged && !block_table))
+    if (!q || !kc || !vc || !lengths || !out || (s.paged && !block_table))
+        return GQA_ERR_INVALID_ARGUMENT;
+    if (!s.attend && (!k_new || !v_new))
         return GQA_ERR_INVALID_ARGUMENT;
     if (!s.paged && !slot_ids && s.R < s.B)
         return GQA_ERR_INVALID_ARGUMENT;
-    if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(kc) || !aligned16(vc) ||
-        !aligned16(out))
+    if (!aligned16(q) || !aligned16(kc) || !aligned16(vc) || !aligned16(out))
+        return GQA_ERR_INVALID_ARGUMENT;
+    if (!s.attend && (!aligned16(k_new) || !aligned16(v_new)))
         return GQA_ERR_INVALID_ARGUMENT;
     const int G = s.Hq / s.Hkv;
     const int kernel = pick_kernel(opt, s.dt, s.D, G, s.paged, s.block_size);
@@ -227,8 +234,10 @@ gqa_status run_step(const Shape &s, const void *q, const void *k_new, const void
     DecodeParams p;
     std::memset(&p, 0, sizeof p);
     p.q = q;
-    p.k_new = k_new;
-    p.v_new = v_new;
+    p.attend = s.attend ? 1 : 0;
+    p.q_bf16 = s.q_dt == GQA_DTYPE_BF16 ? 1 : 0;
+    p.k_new = s.attend ? nullptr : k_new;
+    p.v_new = s.attend ? nullptr : v_new;
     p.k_cache = kc;
     p.v_cache = vc;
     p.lengths = lengths;
@@ -326,7 +335,7 @@ gqa_status gqa_decode_step_ex(const void *q, const void *k_new, const void *v_ne
                               gqa_dtype dt, void *workspace, size_t workspace_bytes,
                               int32_t *d_status, void *stream, const gqa_options *opt)
 {
-    Shape s = {B, Hq, Hkv, D, dt, false, R, Smax, 0, 0, 0};
+    Shape s = {B, Hq, Hkv, D, dt, false, R, Smax, 0, 0, 0, false, dt};
     return run_step(s, q, k_new, v_new, k_cache, v_cache, lengths, slot_ids, nullptr, out,
                     workspace, workspace_bytes, d_status, stream, opt);
 }
@@ -349,7 +358,7 @@ gqa_status gqa_decode_step_paged_ex(const void *q, const void *k_new, const void
                                     gqa_dtype dt, void *workspace, size_t workspace_bytes,
                                     int32_t *d_status, void *stream, const gqa_options *opt)
 {
-    Shape s = {B, Hq, Hkv, D, dt, true, 0, 0, num_blocks, block_size, max_blocks};
+    Shape s = {B, Hq, Hkv, D, dt, true, 0, 0, num_blocks, block_size, max_blocks, false, dt};
     return run_step(s, q, k_new, v_new, k_blocks, v_blocks, lengths, nullptr, block_table, out,
                     workspace, workspace_bytes, d_status, stream, opt);
 }
@@ -366,9 +375,13 @@ gqa_status gqa_decode_step_paged(const void *q, const void *k_new, const void *v
                                     workspace, workspace_bytes, d_status, stream, nullptr);
 }
 
-gqa_status gqa_validate(const int32_t *lengths, const int32_t *slot_ids, const int32_t *block_table,
-                        int B, int R, int Smax, int num_blocks, int block_size, int max_blocks,
-                        int32_t *d_result, void *stream)
+}  // extern "C"
+
+namespace {
+
+gqa_status validate_common(const int32_t *lengths, const int32_t *slot_ids, const int32_t *block_table,
+                           int B, int R, int Smax, int num_blocks, int block_size, int max_blocks,
+                           int attend, int32_t *d_result, void *stream)
 {
     if (B < 0 || !d_result)
         return GQA_ERR_INVALID_ARGUMENT;
@@ -386,13 +399,58 @@ gqa_status gqa_validate(const int32_t *lengths, const int32_t *slot_ids, const i
     if (cudaMemsetAsync(d_result, 0, sizeof(int32_t), cs) != cudaSuccess)
         return GQA_ERR_CUDA;
     if (validate_launch(lengths, block_table ? nullptr : slot_ids, block_table, B, R, Smax,
-                        num_blocks, block_size, max_blocks, d_result, cs) != cudaSuccess)
+                        num_blocks, block_size, max_blocks, attend, d_result, cs) != cudaSuccess)
         return GQA_ERR_CUDA;
     int32_t h = 0;
     if (cudaMemcpyAsync(&h, d_result, sizeof h, cudaMemcpyDeviceToHost, cs) != cudaSuccess ||
         cudaStreamSynchronize(cs) != cudaSuccess)
         return GQA_ERR_CUDA;
     return h ? GQA_ERR_INVALID_ARGUMENT : GQA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gqa_status gqa_validate(const int32_t *lengths, const int32_t *slot_ids, const int32_t *block_table,
+                        int B, int R, int Smax, int num_blocks, int block_size, int max_blocks,
+                        int32_t *d_result, void *stream)
+{
+    return validate_common(lengths, slot_ids, block_table, B, R, Smax, num_blocks, block_size,
+                           max_blocks, 0, d_result, stream);
+}
+
+gqa_status gqa_validate_attend(const int32_t *lengths, const int32_t *slot_ids,
+                               const int32_t *block_table, int B, int R, int Smax, int num_blocks,
+                               int block_size, int max_blocks, int32_t *d_result, void *stream)
+{
+    return validate_common(lengths, slot_ids, block_table, B, R, Smax, num_blocks, block_size,
+                           max_blocks, 1, d_result, stream);
+}
+
+gqa_status gqa_attend(const void *q, gqa_dtype q_dtype, const void *k_cache, const void *v_cache,
+                      const int32_t *lengths, const int32_t *slot_ids, float *out, int B, int Hq,
+                      int Hkv, int D, int R, int Smax, gqa_dtype kv_dtype, void *workspace,
+                      size_t workspace_bytes, int32_t *d_status, void *stream,
+                      const gqa_options *opt)
+{
+    Shape s = {B, Hq, Hkv, D, kv_dtype, false, R, Smax, 0, 0, 0, true, q_dtype};
+    // the kernels never write the cache in this mode
+    return run_step(s, q, nullptr, nullptr, const_cast<void *>(k_cache), const_cast<void *>(v_cache),
+                    lengths, slot_ids, nullptr, out, workspace, workspace_bytes, d_status, stream, opt);
+}
+
+gqa_status gqa_attend_paged(const void *q, gqa_dtype q_dtype, const void *k_blocks,
+                            const void *v_blocks, const int32_t *block_table,
+                            const int32_t *lengths, float *out, int B, int Hq, int Hkv, int D,
+                            int num_blocks, int block_size, int max_blocks, gqa_dtype kv_dtype,
+                            void *workspace, size_t workspace_bytes, int32_t *d_status,
+                            void *stream, const gqa_options *opt)
+{
+    Shape s = {B, Hq, Hkv, D, kv_dtype, true, 0, 0, num_blocks, block_size, max_blocks, true, q_dtype};
+    return run_step(s, q, nullptr, nullptr, const_cast<void *>(k_blocks), const_cast<void *>(v_blocks),
+                    lengths, nullptr, block_table, out, workspace, workspace_bytes, d_status, stream,
+                    opt);
 }
 
 int gqa_trace_enable(int on)

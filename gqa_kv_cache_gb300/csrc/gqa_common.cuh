@@ -3,8 +3,9 @@
 // and small numeric helpers.
 //
 // Work decomposition. A unit is one (batch row b, cache head kvh) pair; unit
-// u = b * Hkv + kvh. Its slots 0..L (L = lengths[b]; slot L is the new token)
-// are cut into tiles of T slots, n_tiles(b) = ceil((L + 1) / T). The tiles of
+// u = b * Hkv + kvh. Its slots 0..L are attended: in the decode step
+// L = lengths[b] and slot L is the new token; in the read-only attend
+// L = lengths[b] - 1 (lengths counts the valid slots). They are cut into tiles of T slots, n_tiles(b) = ceil((L + 1) / T). The tiles of
 // all units, in (b, kvh, tile) order, form one list of N tiles, and CTA i of
 // a grid takes the contiguous range [floor(i N / C), floor((i+1) N / C)) with
 // C = min(grid size, N), so every working CTA owns at least one tile (CTAs
@@ -43,6 +44,8 @@ struct DecodeParams {
     const int32_t *slot_ids;     // dense only, may be null
     const int32_t *block_table;  // paged only
     float *out;                  // (B, Hq, D)
+    int attend;        // 1: read-only attend (no new token, nothing written but out)
+    int q_bf16;        // query dtype: 1 bfloat16, 0 float32 (the cache has its own)
     int B, Hq, Hkv, G, D;
     int R, Smax;                                     // dense
     int paged, num_blocks, block_size, max_blocks;   // paged
@@ -79,7 +82,16 @@ __host__ __device__ inline WorkspaceLayout workspace_layout(int B, int Hkv, int 
     return w;
 }
 
-// Capacity of one row in slots: lengths[b] must be below it.
+// Last attended slot of row b: lengths[b] in the decode step (the append
+// slot), lengths[b] - 1 in the read-only attend; -1 (a bad row) when the
+// attend has no valid slot.
+__device__ __forceinline__ int last_slot(const DecodeParams &p, int b)
+{
+    const int n = __ldg(p.lengths + b);
+    return p.attend ? (n > 0 ? n - 1 : -1) : n;
+}
+
+// Capacity of one row in slots: the last attended slot must be below it.
 __host__ __device__ inline long long row_capacity(const DecodeParams &p)
 {
     return p.paged ? (long long)p.max_blocks * p.block_size : (long long)p.Smax;
@@ -130,7 +142,7 @@ struct TileCursor {
     int b, kvh, t;    // current row, head, tile within the unit
     int nt;           // tiles per head of row b in the schedule
     int nr;           // of which real (t < nr holds data; the rest are virtual)
-    int L;            // lengths[b]
+    int L;            // last attended slot of row b (last_slot)
 };
 
 // Cursor at global tile g, which lies in row b whose tiles start at `run`.
@@ -143,7 +155,7 @@ __device__ __forceinline__ TileCursor cursor_at(const DecodeParams &p, int b, lo
     c.N = N;
     c.C = C;
     c.b = b;
-    c.L = __ldg(p.lengths + b);
+    c.L = last_slot(p, b);
     c.nt = row_tiles(p, c.L);
     c.nr = real_tiles(p, c.L);
     const long long within = g - run;
@@ -174,7 +186,7 @@ __device__ inline TileWalk schedule_walk(const DecodeParams &p, long long *scrat
     const int r0 = min(p.B, tid * chunk), r1 = min(p.B, r0 + chunk);
     long long local = 0;
     for (int b = r0; b < r1; ++b)
-        local += (long long)p.Hkv * row_tiles(p, __ldg(p.lengths + b));
+        local += (long long)p.Hkv * row_tiles(p, last_slot(p, b));
     // inclusive scan: within the warp by shuffles, then over the warp totals
     long long incl = local;
 #pragma unroll
@@ -205,7 +217,7 @@ __device__ inline TileWalk schedule_walk(const DecodeParams &p, long long *scrat
     if (begin < end && ((begin >= excl && begin < incl) || (last >= excl && last < incl))) {
         long long run = excl;
         for (int b = r0; b < r1; ++b) {
-            const long long n = (long long)p.Hkv * row_tiles(p, __ldg(p.lengths + b));
+            const long long n = (long long)p.Hkv * row_tiles(p, last_slot(p, b));
             if (begin >= run && begin < run + n) {
                 found[0] = b;
                 found[1] = run;
@@ -256,7 +268,7 @@ __device__ __forceinline__ void advance(const DecodeParams &p, TileCursor &c)
             c.kvh = 0;
             ++c.b;
             if (c.g < c.end) {
-                c.L = __ldg(p.lengths + c.b);
+                c.L = last_slot(p, c.b);
                 c.nt = row_tiles(p, c.L);
                 c.nr = real_tiles(p, c.L);
             }

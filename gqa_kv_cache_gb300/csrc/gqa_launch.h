@@ -18,17 +18,18 @@ cudaError_t simt_launch(const DecodeParams &p, bool bf16, cudaStream_t st);
 struct TcMaps {
     CUtensorMap k, v;  // tiled maps over the key / value cache, 128-byte swizzle
 };
-bool tc_supports(bool bf16, int D, int G, bool paged, int block_size);
+bool tc_supports(bool bf16, int D, int G, bool paged, int block_size);  // bf16: the cache
 int tc_tile();
 int tc_ctas_per_sm();
-size_t tc_smem_bytes();
+size_t tc_smem_bytes(bool q_bf16);
 cudaError_t tc_launch(const DecodeParams &p, const TcMaps &maps, cudaStream_t st);
 
 // Content validation (gqa_validate.cu). *d_result must be zero on entry; the
-// kernel sets it to 1 on any violation.
+// kernel sets it to 1 on any violation. attend = 1 checks the read-only
+// attend's reading of lengths (the number of valid slots).
 cudaError_t validate_launch(const int32_t *lengths, const int32_t *slot_ids,
                             const int32_t *block_table, int B, int R, int Smax,
-                            int num_blocks, int block_size, int max_blocks,
+                            int num_blocks, int block_size, int max_blocks, int attend,
                             int32_t *d_result, cudaStream_t st);
 
 }  // namespace gqa

@@ -1,6 +1,7 @@
-// CUDA-core (FMA) decode kernel: the general path (float32 or bfloat16, any
-// power-of-two head width up to 256, group size up to 8, dense / slot_ids /
-// paged addressing with any block size).
+// CUDA-core (FMA) decode kernel: the general path (float32 or bfloat16 cache,
+// float32 or bfloat16 query, any power-of-two head width up to 256, group
+// size up to 8, dense / slot_ids / paged addressing with any block size; the
+// decode step and the read-only attend).
 //
 // One persistent CTA of 4 warps walks its contiguous share of the tile list
 // (see gqa_common.cuh). Inside a tile, a group of LPS = D / VEC lanes owns
@@ -11,9 +12,10 @@
 // base-2 max m, sum l, and its VEC columns of o for every head), and at the
 // end of a unit segment the states of all lane groups and warps are merged
 // with the log-sum-exp rule (finish_segment, which also merges the units cut
-// by CTA boundaries). The new token (slot L) is read from k_new/v_new
-// directly and written into the cache by the lane group that reads it; no
-// thread reads the cache at slot L, so the append cannot race.
+// by CTA boundaries). In the decode step the new token (slot L) is read from
+// k_new/v_new directly and written into the cache by the lane group that
+// reads it; no thread reads the cache at slot L, so the append cannot race.
+// The read-only attend reads slot L from the cache and writes nothing but out.
 #include "gqa_common.cuh"
 #include "gqa_launch.h"
 
@@ -72,6 +74,16 @@ __device__ __forceinline__ void load_vec(const T *p, float (&v)[VEC])
         for (int e = 0; e < VEC; ++e)
             v[e] = (e & 1) ? bf16_hi(w[e / 2]) : bf16_lo(w[e / 2]);
     }
+}
+
+// VEC query elements at element index i, in the query's own dtype.
+template <int VEC>
+__device__ __forceinline__ void load_q(const DecodeParams &p, long long i, float (&v)[VEC])
+{
+    if (p.q_bf16)
+        load_vec<__nv_bfloat16, VEC>(static_cast<const __nv_bfloat16 *>(p.q) + i, v);
+    else
+        load_vec<float, VEC>(static_cast<const float *>(p.q) + i, v);
 }
 
 // Raw copy of VEC elements (the append is a bit copy).
@@ -160,8 +172,7 @@ __global__ void __launch_bounds__(kThreads) simt_decode_kernel(const DecodeParam
                     o[g][e] = 0.f;
                 if (g < G) {
                     float tmp[VEC];
-                    load_vec<T, VEC>(static_cast<const T *>(p.q) +
-                                         ((long long)b * p.Hq + kvh * G + g) * D + li * VEC, tmp);
+                    load_q<VEC>(p, ((long long)b * p.Hq + kvh * G + g) * D + li * VEC, tmp);
 #pragma unroll
                     for (int e = 0; e < VEC; ++e)
                         q[g][e] = tmp[e] * p.scale_log2;
@@ -186,7 +197,7 @@ __global__ void __launch_bounds__(kThreads) simt_decode_kernel(const DecodeParam
                 for (int e = 0; e < VEC; ++e)
                     kv[e] = vv[e] = 0.f;
                 bool use = false;
-                if (j < L) {
+                if (j < L || (p.attend && j == L)) {
                     long long off = slot_offset(p, b, kvh, j);
                     if (off < 0) {
                         bad_local = 1;

@@ -1,4 +1,5 @@
-// Tensor-core decode kernel for bfloat16 caches with D = 128 and G <= 8.
+// Tensor-core decode kernel for bfloat16 caches with D = 128 and G <= 8; the
+// query is bfloat16 or float32.
 //
 // Data path (persistent CTAs, kCtasPerSm per SM):
 //  * a producer warp walks the CTA's tiles (gqa_common.cuh) and streams every
@@ -11,9 +12,13 @@
 //    are issued one tile ahead, before the wait for a free stage.
 //  * four consumer warps each take 16 slots of every tile and compute, on the
 //    tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate):
-//      S  = Q K^T   M = 16 query rows (the G heads; rows >= G are zero),
-//                   N = 8 slots, K = 16 dims, 8 steps over D = 128 (two
-//                   accumulator chains per tile, even and odd steps);
+//      S  = Q K^T   M = 16 query rows: rows 0..7 hold the G heads (rows >= G
+//                   are zero); a float32 query is split into bf16(q) in rows
+//                   0..7 and the remainder bf16(q - bf16(q)) in rows 8..15,
+//                   and the two halves of S are added (so q enters with ~16
+//                   significant bits at no extra MMA: rows 8..15 would be
+//                   padding); N = 8 slots, K = 16 dims, 8 steps over D = 128
+//                   (two accumulator chains per tile, even and odd steps);
 //      O += P V     M = 16 rows: rows 0..7 carry bf16(p) and rows 8..15 the
 //                   remainder bf16(p - bf16(p)), so p enters the product with
 //                   ~16 significant bits and the sum stays float32-accurate;
@@ -26,7 +31,8 @@
 //    exceeds it by more than 8, i.e. p <= 256), masking by selection so stale
 //    slots never enter the arithmetic, and V rows beyond the length zeroed in
 //    shared memory before the product (0 * NaN would not be 0).
-//  * the new token: in the tile that holds slot L the owning warp writes
+//  * the new token (decode step only; the read-only attend reads slot L from
+//    the cache like any other): in the tile that holds slot L the owning warp writes
 //    k_new / v_new into the ring slot of row L (the TMA copy of the stale
 //    cache row is discarded) and stores them into the cache at slot L. The
 //    copy of that tile has landed before the store, and no other CTA loads
@@ -61,11 +67,17 @@ constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kGMax = 8;
 constexpr int kHalfBytes = kTile * 128;               // one 64-element half of a tile
-constexpr int kQBytes = kGMax * kD * 2;               // the unit's G query rows
-constexpr int kStageBytes = 4 * kHalfBytes + kQBytes; // K lo, K hi, V lo, V hi, Q
-constexpr int kDynSmem = kStages * kStageBytes + 1024;
 constexpr long long kWaitCycles = 4LL << 30;          // ~2 s at 2 GHz
-static_assert(kStageBytes % 1024 == 0, "stages must stay 1024-byte aligned for the swizzle");
+
+// Ring geometry for a bfloat16 (QF32 = false) or float32 query.
+template <bool QF32>
+struct Ring {
+    static constexpr int kQElem = QF32 ? 4 : 2;
+    static constexpr int kQBytes = kGMax * kD * kQElem;              // the unit's G query rows
+    static constexpr int kStageBytes = 4 * kHalfBytes + kQBytes;     // K lo, K hi, V lo, V hi, Q
+    static constexpr int kDynSmem = kStages * kStageBytes + 1024;
+    static_assert(kStageBytes % 1024 == 0, "stages must stay 1024-byte aligned for the swizzle");
+};
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {
@@ -159,6 +171,13 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// A float32 pair as bf16 hi parts and bf16 remainders: v = hi + lo to ~16 bits.
+__device__ __forceinline__ void split_bf16(float2 v, uint32_t &hi, uint32_t &lo)
+{
+    hi = pack_bf16(v.x, v.y);
+    lo = pack_bf16(v.x - __uint_as_float(hi << 16), v.y - __uint_as_float(hi & 0xffff0000u));
+}
+
 // Byte offset, within one 64-element half, of 16-byte chunk c8 of row r
 // under the 128-byte swizzle (the half starts on a 1024-byte boundary).
 __device__ __forceinline__ uint32_t swz(int r, int c8) { return (uint32_t)(r * 128 + ((c8 ^ (r & 7)) << 4)); }
@@ -181,10 +200,12 @@ __device__ __forceinline__ void consumer_sync()
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
 }
 
+template <bool QF32>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     tc_decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap mk,
                      const __grid_constant__ CUtensorMap mv)
 {
+    constexpr int kStageBytes = Ring<QF32>::kStageBytes;
     extern __shared__ uint8_t dyn_smem[];
     __shared__ Shared sh;
     uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
@@ -278,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             // the first tile of each of this CTA's unit segments also brings
             // the unit's G query rows (contiguous in q)
             const bool seg_first = pl.good && (cur.t == 0 || cur.g == range_start);
-            const uint32_t qbytes = seg_first ? (uint32_t)G * kD * 2u : 0u;
+            const uint32_t qbytes = seg_first ? (uint32_t)(G * kD * Ring<QF32>::kQElem) : 0u;
             const uint32_t bytes = (uint32_t)__popc(copying) * 4u * (uint32_t)box_rows * 128u + qbytes;
             const uint32_t fb = smem_u32(&sh.full[stage]);
             if (lane == 0) {
@@ -286,7 +307,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 mbar_arrive_tx(fb, bytes);
                 if (qbytes)
                     bulk_load(ring_u32 + stage * kStageBytes + 4 * kHalfBytes,
-                              static_cast<const __nv_bfloat16 *>(p.q) + ((long long)b * p.Hq + (long long)kvh * G) * kD,
+                              static_cast<const uint8_t *>(p.q) +
+                                  ((long long)b * p.Hq + (long long)kvh * G) * kD * Ring<QF32>::kQElem,
                               qbytes, fb);
             }
             __syncwarp();
@@ -334,6 +356,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     int stage = 0;
     uint32_t phase = 0;
     uint32_t qa[8][2];                   // Q fragments (rows g0 < G), 8 k-steps
+    uint32_t ql[8][2];                   // float32 query: the remainders (rows g0 + 8)
     float acc_o[16][4];                  // O: 16 n-tiles of 8 dims, rows g0 (hi) and g0+8 (lo)
     float m_run = -INFINITY, l_run = 0.f;
     int seg_first_t = 0;
@@ -380,11 +403,24 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         if (first_of_seg && have && row_good) {
             // Q fragments from the ring (rows g0 < G): dims 16ks + 2q4 (+1)
             // and 16ks + 8 + 2q4 (+1) of head g0
-            const uint8_t *qs = kring + 4 * kHalfBytes + g0 * (kD * 2);
+            if constexpr (QF32) {
+                const float *qs = reinterpret_cast<const float *>(kring + 4 * kHalfBytes) + g0 * kD;
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                qa[ks][0] = (g0 < G) ? *reinterpret_cast<const uint32_t *>(qs + (16 * ks + 2 * q4) * 2) : 0u;
-                qa[ks][1] = (g0 < G) ? *reinterpret_cast<const uint32_t *>(qs + (16 * ks + 8 + 2 * q4) * 2) : 0u;
+                for (int ks = 0; ks < 8; ++ks) {
+                    qa[ks][0] = qa[ks][1] = ql[ks][0] = ql[ks][1] = 0u;
+                    if (g0 < G) {
+                        split_bf16(*reinterpret_cast<const float2 *>(qs + 16 * ks + 2 * q4), qa[ks][0], ql[ks][0]);
+                        split_bf16(*reinterpret_cast<const float2 *>(qs + 16 * ks + 8 + 2 * q4), qa[ks][1],
+                                   ql[ks][1]);
+                    }
+                }
+            } else {
+                const uint8_t *qs = kring + 4 * kHalfBytes + g0 * (kD * 2);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    qa[ks][0] = (g0 < G) ? *reinterpret_cast<const uint32_t *>(qs + (16 * ks + 2 * q4) * 2) : 0u;
+                    qa[ks][1] = (g0 < G) ? *reinterpret_cast<const uint32_t *>(qs + (16 * ks + 8 + 2 * q4) * 2) : 0u;
+                }
             }
         }
 
@@ -393,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             if (last_tile) {
                 // rows of this warp beyond L: zero V; row L: the new token
                 const int lr = L - slot0;            // 0..63
-                if (lr >= row0 && lr < row0 + 16) {
+                if (!p.attend && lr >= row0 && lr < row0 + 16) {
                     const long long nidx = ((long long)b * p.Hkv + kvh) * kD;
                     const int c = lane & 15;          // 16-byte chunk of the row
                     const int half = c >> 3, c8 = c & 7;
@@ -431,8 +467,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     uint32_t kb[4];
                     ldsm_x4(kbase + (c >> 3) * kHalfBytes + swz(r, c & 7), kb);
                     float(&acc)[2][4] = (ks & 1) ? s_odd : s_acc;
-                    mma_bf16(acc[0], qa[ks][0], 0u, qa[ks][1], 0u, kb[0], kb[1]);
-                    mma_bf16(acc[1], qa[ks][0], 0u, qa[ks][1], 0u, kb[2], kb[3]);
+                    if constexpr (QF32) {
+                        mma_bf16(acc[0], qa[ks][0], ql[ks][0], qa[ks][1], ql[ks][1], kb[0], kb[1]);
+                        mma_bf16(acc[1], qa[ks][0], ql[ks][0], qa[ks][1], ql[ks][1], kb[2], kb[3]);
+                    } else {
+                        mma_bf16(acc[0], qa[ks][0], 0u, qa[ks][1], 0u, kb[0], kb[1]);
+                        mma_bf16(acc[1], qa[ks][0], 0u, qa[ks][1], 0u, kb[2], kb[3]);
+                    }
                 }
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt)
@@ -448,7 +489,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int j = slot0 + row0 + 8 * nt + 2 * q4 + e;
-                    x[nt][e] = (j <= L) ? s_acc[nt][e] * p.scale_log2 : -INFINITY;
+                    float sc = s_acc[nt][e];
+                    if constexpr (QF32)
+                        sc += s_acc[nt][e + 2];   // row g0 + 8: the query remainder
+                    x[nt][e] = (j <= L) ? sc * p.scale_log2 : -INFINITY;
                     mx = fmaxf(mx, x[nt][e]);
                 }
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
@@ -554,13 +598,20 @@ bool tc_supports(bool bf16, int D, int G, bool paged, int block_size)
 
 int tc_tile() { return kTile; }
 int tc_ctas_per_sm() { return kCtasPerSm; }
-size_t tc_smem_bytes() { return kDynSmem + sizeof(Shared); }
-
-cudaError_t tc_launch(const DecodeParams &p, const TcMaps &maps, cudaStream_t st)
+size_t tc_smem_bytes(bool q_bf16)
 {
+    return (q_bf16 ? Ring<false>::kDynSmem : Ring<true>::kDynSmem) + sizeof(Shared);
+}
+
+namespace {
+template <bool QF32>
+cudaError_t launch_q(const DecodeParams &p, const TcMaps &maps, cudaStream_t st)
+{
+    constexpr int kDynSmem = Ring<QF32>::kDynSmem;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(tc_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem);
+        cudaError_t e = cudaFuncSetAttribute(tc_decode_kernel<QF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kDynSmem);
         if (e != cudaSuccess)
             return e;
         attr_set = true;
@@ -575,7 +626,13 @@ cudaError_t tc_launch(const DecodeParams &p, const TcMaps &maps, cudaStream_t st
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tc_decode_kernel, p, maps.k, maps.v);
+    return cudaLaunchKernelEx(&cfg, tc_decode_kernel<QF32>, p, maps.k, maps.v);
+}
+}  // namespace
+
+cudaError_t tc_launch(const DecodeParams &p, const TcMaps &maps, cudaStream_t st)
+{
+    return p.q_bf16 ? launch_q<false>(p, maps, st) : launch_q<true>(p, maps, st);
 }
 
 }  // namespace gqa

@@ -1,4 +1,5 @@
-// Content validation: every rule of gqa_validate, one CTA per batch row.
+// Content validation: every rule of gqa_validate / gqa_validate_attend, one
+// CTA per batch row.
 #include "gqa_common.cuh"
 #include "gqa_launch.h"
 
@@ -6,13 +7,15 @@ namespace gqa {
 namespace {
 
 // One CTA per batch row: every rule of the public header's gqa_validate.
+// L is the last slot the call touches: lengths[b] for the decode step (the
+// append slot), lengths[b] - 1 for the read-only attend.
 __global__ void __launch_bounds__(256) validate_kernel(const int32_t *lengths, const int32_t *slot_ids,
                                                        const int32_t *block_table, int B, int R, int Smax,
                                                        int num_blocks, int block_size, int max_blocks,
-                                                       int32_t *result)
+                                                       int attend, int32_t *result)
 {
     const int b = blockIdx.x;
-    const long long L = lengths[b];
+    const long long L = (long long)lengths[b] - attend;
     bool bad = false;
     if (!block_table) {
         if (threadIdx.x == 0) {
@@ -56,11 +59,11 @@ __global__ void __launch_bounds__(256) validate_kernel(const int32_t *lengths, c
 
 cudaError_t validate_launch(const int32_t *lengths, const int32_t *slot_ids,
                             const int32_t *block_table, int B, int R, int Smax,
-                            int num_blocks, int block_size, int max_blocks,
+                            int num_blocks, int block_size, int max_blocks, int attend,
                             int32_t *d_result, cudaStream_t st)
 {
     validate_kernel<<<B, 256, 0, st>>>(lengths, slot_ids, block_table, B, R, Smax, num_blocks,
-                                       block_size, max_blocks, d_result);
+                                       block_size, max_blocks, attend, d_result);
     return cudaGetLastError();
 }
 

@@ -19,6 +19,11 @@
  * Scores, softmax and the weighted sum are computed in float32 from float32
  * or bfloat16 data ("Grouped-Query Decode Step", Requirements).
  *
+ * The read-only attend (gqa_attend, gqa_attend_paged) is step 2 alone over
+ * slots 0..lengths[b]-1, with lengths[b] counting the valid cached slots and
+ * a query dtype of its own (a float32 query over a bfloat16 cache is that
+ * page's contract); it writes nothing but its output.
+ *
  * Conventions for every entry point:
  *  - Pointers marked (device) point to GPU memory of the current device;
  *    (host) to host memory. The library never allocates, frees or keeps any
@@ -65,13 +70,14 @@ typedef enum gqa_status {
 } gqa_status;
 
 typedef enum gqa_dtype {
-    GQA_DTYPE_F32 = 0,  /* q, k_new, v_new and the cache in float32  */
-    GQA_DTYPE_BF16 = 1  /* q, k_new, v_new and the cache in bfloat16 */
+    GQA_DTYPE_F32 = 0,  /* float32  (decode step: q, k_new, v_new and the cache) */
+    GQA_DTYPE_BF16 = 1  /* bfloat16 (decode step: q, k_new, v_new and the cache) */
 } gqa_dtype;
 
 /* Bits OR-ed into *d_status by the kernels. */
 enum {
-    GQA_STATUS_BAD_LENGTH = 1,      /* lengths[b] < 0 or beyond the row's capacity       */
+    GQA_STATUS_BAD_LENGTH = 1,      /* lengths[b] < 0 (attend: < 1) or beyond the row's
+                                       capacity                                           */
     GQA_STATUS_BAD_SLOT_ID = 2,     /* slot_ids[b] outside [0, R)                        */
     GQA_STATUS_BAD_BLOCK = 4,       /* block-table entry outside [0, num_blocks) or -1
                                        where a slot 0..lengths[b] lives                   */
@@ -202,6 +208,58 @@ gqa_status gqa_validate(const int32_t *lengths, const int32_t *slot_ids,
                         const int32_t *block_table, int B, int R, int Smax,
                         int num_blocks, int block_size, int max_blocks,
                         int32_t *d_result, void *stream);
+
+/*
+ * Read-only attend over a dense or continuous-batch cache: every query head h
+ * attends slots 0..lengths[b]-1 of cache head floor(h/G) of its row, with the
+ * same scores, softmax and float32 output as the decode step, and nothing is
+ * appended or written besides `out` ("groupQueryAttention": a read-only attend
+ * passes no key or value and takes no present outputs, attention_over_cache;
+ * "Grouped-Query Decode Step", statement and Constraints: lengths counts the
+ * valid slots, the new token already among them, 1 <= lengths[b] <= S; the
+ * query is float32 and the caches float32 or bfloat16).
+ *
+ *  q        (device) (B, Hq, D) of q_dtype (float32 or bfloat16)
+ *  k_cache  (device) (R, Hkv, Smax, D) of kv_dtype, only read
+ *  v_cache  (device) (R, Hkv, Smax, D) of kv_dtype, only read
+ *  lengths  (device) (B,) int32, 1 <= lengths[b] <= Smax: valid slots of row b
+ *  slot_ids (device) (B,) int32 or NULL, as in gqa_decode_step
+ *  out      (device) (B, Hq, D) float32
+ *  workspace, d_status, stream: as in gqa_decode_step (the same
+ *           gqa_workspace_bytes, computed with kv_dtype); opt may be NULL.
+ * A bad length (< 1 or > Smax) or slot id gives that row NaN outputs and sets
+ * its status bit. The tensor-core kernel takes a bfloat16 cache with D = 128
+ * and G <= 8 and either query dtype; everything else runs on the CUDA-core
+ * kernel.
+ */
+gqa_status gqa_attend(const void *q, gqa_dtype q_dtype, const void *k_cache, const void *v_cache,
+                      const int32_t *lengths, const int32_t *slot_ids, float *out,
+                      int B, int Hq, int Hkv, int D, int R, int Smax, gqa_dtype kv_dtype,
+                      void *workspace, size_t workspace_bytes, int32_t *d_status, void *stream,
+                      const gqa_options *opt);
+
+/*
+ * Read-only attend over a paged cache (blocks and table as in
+ * gqa_decode_step_paged); 1 <= lengths[b] <= max_blocks * block_size and the
+ * entries holding slots 0..lengths[b]-1 must be real blocks.
+ */
+gqa_status gqa_attend_paged(const void *q, gqa_dtype q_dtype, const void *k_blocks,
+                            const void *v_blocks, const int32_t *block_table,
+                            const int32_t *lengths, float *out,
+                            int B, int Hq, int Hkv, int D,
+                            int num_blocks, int block_size, int max_blocks, gqa_dtype kv_dtype,
+                            void *workspace, size_t workspace_bytes, int32_t *d_status,
+                            void *stream, const gqa_options *opt);
+
+/*
+ * gqa_validate for the read-only attend's reading of lengths: the same rules
+ * with 1 <= lengths[b] <= capacity and real blocks for slots
+ * 0..lengths[b]-1. Synchronous; same arguments and results.
+ */
+gqa_status gqa_validate_attend(const int32_t *lengths, const int32_t *slot_ids,
+                               const int32_t *block_table, int B, int R, int Smax,
+                               int num_blocks, int block_size, int max_blocks,
+                               int32_t *d_result, void *stream);
 
 /*
  * Kernel timing trace. When enabled, every decode call records CUDA events

@@ -46,8 +46,8 @@ def host_problem(w: W.Workload, t: dict, rows=None):
     (problem dict, mapping back to the original storage)."""
     rows = _sample_rows(w, rows)
     sel = torch.tensor(rows, dtype=torch.long, device=t["q"].device)
-    prob = {"q": to_np(t["q"][sel]), "k_new": to_np(t["k_new"][sel]), "v_new": to_np(t["v_new"][sel]),
-            "lengths": to_np(t["lengths"][sel]), "rows": rows}
+    prob = {k: to_np(t[k][sel]) for k in ("q", "k_new", "v_new", "lengths") if k in t}
+    prob["rows"] = rows
     if w.paged:
         bt = t["block_table"][sel].cpu().numpy()
         used = sorted(set(int(x) for x in bt[bt >= 0].tolist()))
@@ -89,8 +89,9 @@ def run_gpu(w: W.Workload, t: dict, kernel="auto", grid_ctas=0, status=None):
 
 
 def attended_vmax(prob: dict) -> float:
-    """max |V| over the values the step attends (valid slots and the new one)."""
-    vals = [np.abs(_as_float(prob["v_new"])).max()]
+    """max |V| over the values the call attends: the valid slots below
+    lengths[b] and, in the decode step, the new value."""
+    vals = [np.abs(_as_float(prob["v_new"])).max()] if "v_new" in prob else [0.0]
     L = prob["lengths"]
     if "k_blocks" in prob:
         vb = _as_float(prob["v_blocks"])

@@ -24,6 +24,12 @@ library is measured on):
                  65536 blocks reshaped to (64,1024), entries at index
                  >= ceil((lengths[b]+1)/16) set to -1; lengths ~ U{512..16383}.
 
+The read-only attend uses the same draws (``generate(w, attend=True)``):
+lengths then count the valid slots (the decode draw + 1, so the slot the
+decode step would append to is valid data), the stale region starts after
+them, and there is no k_new / v_new; ``q_f32=True`` keeps the query in
+float32 instead of casting it to the cache dtype.
+
 Random draws come from a ``torch.Generator`` on the target device seeded
 with the workload's seed, in a fixed order, in chunks of ``_CHUNK`` elements
 (so an 8 GB cache never needs a 17 GB float32 staging copy).
@@ -138,19 +144,26 @@ def _lengths(w, gen, device):
     return torch.floor(x).clamp(w.len_lo, w.len_hi).to(torch.int32)
 
 
-def generate(w: Workload, device="cpu") -> dict:
+def generate(w: Workload, device="cpu", attend: bool = False, q_f32: bool = False) -> dict:
     """All inputs of one decode step of workload ``w`` on ``device``.
 
     Returns a dict with q (B,Hq,D), k_new/v_new (B,Hkv,D), lengths (B,) int32,
     and either k_cache/v_cache (R,Hkv,Smax,D) [+ slot_ids (B,) int32] or
     k_blocks/v_blocks (num_blocks,Hkv,block_size,D) + block_table (B,max_blocks).
+    With ``attend`` the inputs of the read-only attend instead (see the module
+    docstring): lengths count valid slots and there is no k_new / v_new.
     """
     device = torch.device(device)
     gen = torch.Generator(device=device)
     gen.manual_seed(w.seed)
     t = {}
     t["lengths"] = _lengths(w, gen, device)
-    t["q"] = _normal_cast((w.B, w.Hq, w.D), gen, device, w)
+    if attend:
+        t["lengths"] = t["lengths"] + 1
+    if q_f32:
+        t["q"] = _normal((w.B, w.Hq, w.D), gen, device)
+    else:
+        t["q"] = _normal_cast((w.B, w.Hq, w.D), gen, device, w)
     t["k_new"] = _normal_cast((w.B, w.Hkv, w.D), gen, device, w, w.key_scale)
     t["v_new"] = _normal_cast((w.B, w.Hkv, w.D), gen, device, w)
     if w.paged:
@@ -162,10 +175,12 @@ def generate(w: Workload, device="cpu") -> dict:
             raise ValueError("the block-table recipe needs num_blocks >= B * max_blocks")
         perm = torch.randperm(w.num_blocks, generator=gen, device=device)[:need]
         bt = perm.view(w.B, w.max_blocks).to(torch.int32)
-        used = (t["lengths"].to(torch.int64) + 1 + w.block_size - 1) // w.block_size
+        # blocks holding the slots the call touches: 0..lengths[b] (decode), 0..lengths[b]-1 (attend)
+        touched = t["lengths"].to(torch.int64) + (0 if attend else 1)
+        used = (touched + w.block_size - 1) // w.block_size
         idx = torch.arange(w.max_blocks, device=device)[None, :]
         t["block_table"] = torch.where(idx < used[:, None], bt, torch.full_like(bt, -1))
-        return t
+        return _drop_new(t, attend)
     shape = (w.rows, w.Hkv, w.Smax, w.D)
     if w.stale_std == 1.0:
         t["k_cache"] = _normal_cast(shape, gen, device, w, w.key_scale)
@@ -185,6 +200,12 @@ def generate(w: Workload, device="cpu") -> dict:
         valid = (torch.arange(w.Smax, device=device)[None, :] < row_len[:, None])[:, None, :, None]
         t["k_cache"] = _cast(torch.where(valid, valid_k, stale_k), w)
         t["v_cache"] = _cast(torch.where(valid, valid_v, stale_v), w)
+    return _drop_new(t, attend)
+
+
+def _drop_new(t: dict, attend: bool) -> dict:
+    if attend:
+        del t["k_new"], t["v_new"]
     return t
 
 
