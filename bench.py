@@ -408,7 +408,7 @@ def run_ours(args, ranks):
     avg_main_s = ms_main / max(n_main, 1) * 1e-3
     hbm_peak, peak_kind = peaks()
     achieved = alg["total"] / avg_main_s / 1e9
-    traffic = traffic_for(main, w.name)
+    traffic = traffic_for(main, w.name + ("/attend" if attend else ""))
 
     # ---- end to end through the public API, host buffers, copies inside
     Ke = min(K, 500)
