@@ -32,6 +32,31 @@ _lock = threading.Lock()
 _lib = None
 
 
+class _Mods(ctypes.Structure):
+    _fields_ = [("head_sink", ctypes.c_void_p), ("window", ctypes.c_int),
+                ("kept_prefix", ctypes.c_int), ("kept_prefix_rows", ctypes.c_void_p)]
+
+
+def _mods(sink, window, kept_prefix, keep):
+    """The orc_mods argument (None when no modifier is given). Arrays that
+    back it are appended to ``keep`` so they outlive the call."""
+    if sink is None and not window and (kept_prefix is None or np.isscalar(kept_prefix) and kept_prefix == 0):
+        return None
+    m = _Mods()
+    if sink is not None:
+        a = np.ascontiguousarray(sink, dtype=np.float32)
+        keep.append(a)
+        m.head_sink = a.ctypes.data
+    m.window = int(window or 0)
+    if kept_prefix is None or np.isscalar(kept_prefix):
+        m.kept_prefix = int(kept_prefix or 0)
+    else:
+        a = np.ascontiguousarray(kept_prefix, dtype=np.int32)
+        keep.append(a)
+        m.kept_prefix_rows = a.ctypes.data
+    return ctypes.byref(m), m
+
+
 def build(force: bool = False) -> str:
     """Compile the oracle into ``libgqa_oracle.so`` beside its source."""
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
@@ -52,20 +77,20 @@ def _load():
             lib = ctypes.CDLL(os.environ.get("GQA_ORACLE_LIB") or build())
             P, I = ctypes.c_void_p, ctypes.c_int
             lib.orc_decode_dense.argtypes = [I, P, P, P, P, P, P, P, I, I, I, I, I, I,
-                                             P, I, I, P, I, P]
+                                             P, I, I, P, P, I, P]
             lib.orc_decode_dense.restype = I
             lib.orc_decode_paged.argtypes = [I, P, P, P, P, P, P, P, I, I, I, I, I, I, I,
-                                             P, I, I, P, I, P]
+                                             P, I, I, P, P, I, P]
             lib.orc_decode_paged.restype = I
             lib.orc_validate_dense.argtypes = [P, P, I, I, I]
             lib.orc_validate_dense.restype = I
             lib.orc_validate_paged.argtypes = [P, P, I, I, I, I]
             lib.orc_validate_paged.restype = I
             lib.orc_attend_dense.argtypes = [I, I, P, P, P, P, P, I, I, I, I, I, I,
-                                             P, I, P, I, P]
+                                             P, I, P, P, I, P]
             lib.orc_attend_dense.restype = I
             lib.orc_attend_paged.argtypes = [I, I, P, P, P, P, P, I, I, I, I, I, I, I,
-                                             P, I, P, I, P]
+                                             P, I, P, P, I, P]
             lib.orc_attend_paged.restype = I
             lib.orc_validate_attend_dense.argtypes = [P, P, I, I, I]
             lib.orc_validate_attend_dense.restype = I
@@ -108,13 +133,16 @@ class OracleResult:
 
 
 def decode_dense(q, k_new, v_new, k_cache, v_cache, lengths, slot_ids=None, *,
-                 rows=None, append=True, threads=None) -> OracleResult:
+                 rows=None, append=True, threads=None, sink=None, window=0,
+                 kept_prefix=0) -> OracleResult:
     """One decode step on a dense (R, Hkv, Smax, D) cache, in place.
 
     ``q`` (B, Hq, D); ``k_new``/``v_new`` (B, Hkv, D); ``lengths`` (B,) int32;
     ``slot_ids`` (B,) int32 or None. With ``append`` the caches (numpy arrays,
     modified in place) receive the new key/value at slot ``lengths[b]``.
     ``rows`` restricts the work to those batch rows (others stay NaN in out).
+    Softmax modifiers: ``sink`` (Hq,) float32 logits, ``window`` W (0: none),
+    ``kept_prefix`` an int or a (B,) int32 array.
     Returns an OracleResult with ``out`` (B, Hq, D) float64.
     """
     dt = _dtype_code(q)
@@ -133,16 +161,19 @@ def decode_dense(q, k_new, v_new, k_cache, v_cache, lengths, slot_ids=None, *,
     out = np.full((B, Hq, D), np.nan, dtype=np.float64)
     used = ctypes.c_int(0)
     nthr = default_threads() if threads is None else int(threads)
+    keep = []
+    mods = _mods(sink, window, kept_prefix, keep)
     st = _load().orc_decode_dense(dt, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
                                   _ptr(v_cache), _ptr(lengths), _ptr(slot_ids),
                                   B, Hq, Hkv, D, R, Smax, _ptr(rows_a),
                                   0 if rows_a is None else len(rows_a), int(bool(append)),
-                                  _ptr(out), nthr, ctypes.addressof(used))
+                                  _ptr(out), mods and mods[0], nthr, ctypes.addressof(used))
     return OracleResult(st, out, used.value)
 
 
 def decode_paged(q, k_new, v_new, k_blocks, v_blocks, block_table, lengths, *,
-                 rows=None, append=True, threads=None) -> OracleResult:
+                 rows=None, append=True, threads=None, sink=None, window=0,
+                 kept_prefix=0) -> OracleResult:
     """One decode step on a paged cache (num_blocks, Hkv, block_size, D) with a
     (B, max_blocks) int32 block table (-1 = unused). Same contract as
     :func:`decode_dense` otherwise."""
@@ -163,16 +194,18 @@ def decode_paged(q, k_new, v_new, k_blocks, v_blocks, block_table, lengths, *,
     out = np.full((B, Hq, D), np.nan, dtype=np.float64)
     used = ctypes.c_int(0)
     nthr = default_threads() if threads is None else int(threads)
+    keep = []
+    mods = _mods(sink, window, kept_prefix, keep)
     st = _load().orc_decode_paged(dt, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_blocks),
                                   _ptr(v_blocks), _ptr(block_table), _ptr(lengths),
                                   B, Hq, Hkv, D, NB, BS, MB, _ptr(rows_a),
                                   0 if rows_a is None else len(rows_a), int(bool(append)),
-                                  _ptr(out), nthr, ctypes.addressof(used))
+                                  _ptr(out), mods and mods[0], nthr, ctypes.addressof(used))
     return OracleResult(st, out, used.value)
 
 
 def attend_dense(q, k_cache, v_cache, lengths, slot_ids=None, *, rows=None,
-                 threads=None) -> OracleResult:
+                 threads=None, sink=None, window=0, kept_prefix=0) -> OracleResult:
     """Read-only attend on a dense (R, Hkv, Smax, D) cache: every query head
     attends slots ``0 .. lengths[b]-1`` of its cache head; nothing is written.
     ``q`` may be float32 over a bfloat16 cache. Returns ``out`` (B, Hq, D)
@@ -191,15 +224,17 @@ def attend_dense(q, k_cache, v_cache, lengths, slot_ids=None, *, rows=None,
     out = np.full((B, Hq, D), np.nan, dtype=np.float64)
     used = ctypes.c_int(0)
     nthr = default_threads() if threads is None else int(threads)
+    keep = []
+    mods = _mods(sink, window, kept_prefix, keep)
     st = _load().orc_attend_dense(qt, kt, _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(lengths),
                                   _ptr(slot_ids), B, Hq, Hkv, D, R, Smax, _ptr(rows_a),
-                                  0 if rows_a is None else len(rows_a), _ptr(out), nthr,
-                                  ctypes.addressof(used))
+                                  0 if rows_a is None else len(rows_a), _ptr(out),
+                                  mods and mods[0], nthr, ctypes.addressof(used))
     return OracleResult(st, out, used.value)
 
 
 def attend_paged(q, k_blocks, v_blocks, block_table, lengths, *, rows=None,
-                 threads=None) -> OracleResult:
+                 threads=None, sink=None, window=0, kept_prefix=0) -> OracleResult:
     """Read-only attend on a paged cache; same contract as :func:`attend_dense`."""
     qt = _dtype_code(q)
     kt = _dtype_code(k_blocks)
@@ -216,10 +251,12 @@ def attend_paged(q, k_blocks, v_blocks, block_table, lengths, *, rows=None,
     out = np.full((B, Hq, D), np.nan, dtype=np.float64)
     used = ctypes.c_int(0)
     nthr = default_threads() if threads is None else int(threads)
+    keep = []
+    mods = _mods(sink, window, kept_prefix, keep)
     st = _load().orc_attend_paged(qt, kt, _ptr(q), _ptr(k_blocks), _ptr(v_blocks),
                                   _ptr(block_table), _ptr(lengths), B, Hq, Hkv, D, NB, BS, MB,
                                   _ptr(rows_a), 0 if rows_a is None else len(rows_a), _ptr(out),
-                                  nthr, ctypes.addressof(used))
+                                  mods and mods[0], nthr, ctypes.addressof(used))
     return OracleResult(st, out, used.value)
 
 

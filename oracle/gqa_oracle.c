@@ -21,6 +21,14 @@
  * token and no write: n = lengths[b] is the number of valid cached slots and
  * slots 0 .. n-1 are attended; the query may be float32 over a bfloat16 cache.
  *
+ * Optional softmax modifiers (orc_mods, any entry point), with the query at
+ * position L (the new token, or the last valid slot of the attend):
+ *   window W > 0   slot j is attended only if L - W < j (the W positions up
+ *                  to and including the query's own) ...
+ *   kept prefix P  ... or if j < P (the sequence's first P keys);
+ *   sink           one more logit per query head in the denominator:
+ *                  w_j = exp(s_j) / (exp(sink_h) + sum_{i attended} exp(s_i)).
+ *
  * Sources (web pages, by title and part):
  *  - "KV cache decode step" (tensortonic cs336-l10), problem statement: the new
  *    key and value take position S after the S cached positions, each KV head
@@ -41,6 +49,11 @@
  *  - "Grouped-Query Decode Step", Constraints: the query is float32 while the
  *    caches are float32 or bfloat16, and every length lies in [1, S]: this is
  *    the read-only attend's contract.
+ *  - "groupQueryAttention", description: head_sink is a per-head virtual
+ *    logit folded into the softmax denominator; kept_prefix keeps each
+ *    sequence's first P keys attended beside the sliding window, a key is
+ *    attended when it is inside the first P keys or inside the window (the
+ *    window alone without P), and a negative P is refused.
  *
  * Readings where the pages are silent (each listed in the design notes):
  *  - lengths[b] is the append slot (the number of tokens already cached), and
@@ -48,6 +61,10 @@
  *  - dense: 0 <= lengths[b] <= Smax - 1. paged: 0 <= lengths[b] and
  *    lengths[b] < max_blocks * block_size, and the table entries covering
  *    slots 0 .. lengths[b] are not -1.
+ *  - the window holds the W positions ending at the query's own (so W = 1
+ *    attends the query's own key only); the sink is a logit in the same units
+ *    as s_j (already scaled, not multiplied by 1/sqrt(D)); a kept prefix has
+ *    no effect without a window; window < 0 is refused like a negative P.
  *  - read-only attend: 1 <= lengths[b] <= Smax (dense) or
  *    <= max_blocks * block_size (paged, entries covering slots
  *    0 .. lengths[b]-1 not -1); zero valid slots has no softmax and is
@@ -68,6 +85,14 @@
 
 enum { ORC_F32 = 0, ORC_BF16 = 1 };
 enum { ORC_OK = 0, ORC_INVALID_ARGUMENT = 1 };
+
+/* Softmax modifiers; a NULL orc_mods pointer means none. */
+typedef struct {
+    const float *head_sink;         /* (Hq,) logits, or NULL: no sink          */
+    int window;                     /* 0: no window; > 0: W                    */
+    int kept_prefix;                /* P for every row (rows NULL), >= 0       */
+    const int32_t *kept_prefix_rows;/* (B,) P per batch row, or NULL           */
+} orc_mods;
 
 /* One element of a float32 or bfloat16 array, widened exactly to double. */
 static double elem(const void *base, size_t i, int dtype)
@@ -209,12 +234,40 @@ typedef struct {
     int B, Hq, Hkv, D;
     int do_append;
     double *out;       /* (B, Hq, D) */
+    const orc_mods *mods;  /* NULL: plain softmax */
     const int32_t *rows; /* batch rows to compute */
     int nrows;
     /* work distribution over (row, kvh) pairs */
     int next;
     pthread_mutex_t mu;
 } job;
+
+/* Whether slot j (0 <= j <= L, the query at position L) of batch row b takes
+ * part in the softmax: always without a window; with one, inside the window
+ * or the kept prefix. */
+static int attended(const job *J, int b, int L, int j)
+{
+    const orc_mods *M = J->mods;
+    if (!M || M->window <= 0)
+        return 1;
+    if (j > L - M->window)
+        return 1;
+    const int P = M->kept_prefix_rows ? M->kept_prefix_rows[b] : M->kept_prefix;
+    return j < P;
+}
+
+static int mods_ok(const orc_mods *M, int B)
+{
+    if (!M)
+        return 1;
+    if (M->window < 0 || (!M->kept_prefix_rows && M->kept_prefix < 0))
+        return 0;
+    if (M->kept_prefix_rows)
+        for (int b = 0; b < B; ++b)
+            if (M->kept_prefix_rows[b] < 0)
+                return 0;
+    return 1;
+}
 
 /* One (batch row, cache head) pair: append (decode step), then the G query
  * heads over the attended slots 0 .. L. */
@@ -248,20 +301,27 @@ static void one_pair(job *J, int b, int kvh)
             s[j] = dot / sqrt((double)D);
         }
 
-        /* softmax over the valid slots only */
-        double m = s[0];
-        for (int j = 1; j <= L; ++j)
-            if (s[j] > m)
-                m = s[j];
-        double Z = 0.0;
+        /* softmax over the attended slots (the valid ones, cut to the window
+         * and the kept prefix when given), the sink as one more logit */
+        const float *sink = J->mods ? J->mods->head_sink : NULL;
+        double m = -INFINITY;
         for (int j = 0; j <= L; ++j)
-            Z += exp(s[j] - m);
+            if (attended(J, b, L, j) && s[j] > m)
+                m = s[j];
+        if (sink && (double)sink[h] > m)
+            m = (double)sink[h];
+        double Z = sink ? exp((double)sink[h] - m) : 0.0;
+        for (int j = 0; j <= L; ++j)
+            if (attended(J, b, L, j))
+                Z += exp(s[j] - m);
 
         /* weighted sum of values */
         double *o = J->out + q_i;
         for (int d = 0; d < D; ++d)
             o[d] = 0.0;
         for (int j = 0; j <= L; ++j) {
+            if (!attended(J, b, L, j))
+                continue;
             double w = exp(s[j] - m) / Z;
             for (int d = 0; d < D; ++d) {
                 double vd = (j == L && from_new)
@@ -328,9 +388,9 @@ int orc_decode_dense(int dtype, const void *q, const void *k_new, const void *v_
                      void *k_cache, void *v_cache, const int32_t *lengths, const int32_t *slot_ids,
                      int B, int Hq, int Hkv, int D, int R, int Smax,
                      const int32_t *rows, int nrows, int do_append, double *out,
-                     int nthreads, int *threads_used)
+                     const orc_mods *mods, int nthreads, int *threads_used)
 {
-    if (!usable_shape(B, Hq, Hkv, D) || (dtype != ORC_F32 && dtype != ORC_BF16))
+    if (!usable_shape(B, Hq, Hkv, D) || (dtype != ORC_F32 && dtype != ORC_BF16) || !mods_ok(mods, B))
         return ORC_INVALID_ARGUMENT;
     if (orc_validate_dense(lengths, slot_ids, B, R, Smax) != ORC_OK)
         return ORC_INVALID_ARGUMENT;
@@ -345,6 +405,7 @@ int orc_decode_dense(int dtype, const void *q, const void *k_new, const void *v_
     J.B = B; J.Hq = Hq; J.Hkv = Hkv; J.D = D;
     J.do_append = do_append;
     J.out = out;
+    J.mods = mods;
     J.rows = (const int32_t *)rows; J.nrows = nrows;
     int n = run(&J, nthreads);
     if (threads_used)
@@ -359,9 +420,9 @@ int orc_decode_paged(int dtype, const void *q, const void *k_new, const void *v_
                      const int32_t *lengths, int B, int Hq, int Hkv, int D,
                      int num_blocks, int block_size, int max_blocks,
                      const int32_t *rows, int nrows, int do_append, double *out,
-                     int nthreads, int *threads_used)
+                     const orc_mods *mods, int nthreads, int *threads_used)
 {
-    if (!usable_shape(B, Hq, Hkv, D) || (dtype != ORC_F32 && dtype != ORC_BF16))
+    if (!usable_shape(B, Hq, Hkv, D) || (dtype != ORC_F32 && dtype != ORC_BF16) || !mods_ok(mods, B))
         return ORC_INVALID_ARGUMENT;
     if (orc_validate_paged(lengths, block_table, B, num_blocks, block_size, max_blocks) != ORC_OK)
         return ORC_INVALID_ARGUMENT;
@@ -377,6 +438,7 @@ int orc_decode_paged(int dtype, const void *q, const void *k_new, const void *v_
     J.B = B; J.Hq = Hq; J.Hkv = Hkv; J.D = D;
     J.do_append = do_append;
     J.out = out;
+    J.mods = mods;
     J.rows = (const int32_t *)rows; J.nrows = nrows;
     int n = run(&J, nthreads);
     if (threads_used)
@@ -392,9 +454,11 @@ static int usable_dtype(int dtype) { return dtype == ORC_F32 || dtype == ORC_BF1
 int orc_attend_dense(int q_dtype, int kv_dtype, const void *q, const void *k_cache,
                      const void *v_cache, const int32_t *lengths, const int32_t *slot_ids,
                      int B, int Hq, int Hkv, int D, int R, int Smax,
-                     const int32_t *rows, int nrows, double *out, int nthreads, int *threads_used)
+                     const int32_t *rows, int nrows, double *out, const orc_mods *mods,
+                     int nthreads, int *threads_used)
 {
-    if (!usable_shape(B, Hq, Hkv, D) || !usable_dtype(q_dtype) || !usable_dtype(kv_dtype))
+    if (!usable_shape(B, Hq, Hkv, D) || !usable_dtype(q_dtype) || !usable_dtype(kv_dtype) ||
+        !mods_ok(mods, B))
         return ORC_INVALID_ARGUMENT;
     if (orc_validate_attend_dense(lengths, slot_ids, B, R, Smax) != ORC_OK)
         return ORC_INVALID_ARGUMENT;
@@ -410,6 +474,7 @@ int orc_attend_dense(int q_dtype, int kv_dtype, const void *q, const void *k_cac
     J.lay.Hkv = Hkv; J.lay.D = D; J.lay.Smax = Smax;
     J.B = B; J.Hq = Hq; J.Hkv = Hkv; J.D = D;
     J.out = out;
+    J.mods = mods;
     J.rows = (const int32_t *)rows; J.nrows = nrows;
     int n = run(&J, nthreads);
     if (threads_used)
@@ -421,9 +486,11 @@ int orc_attend_dense(int q_dtype, int kv_dtype, const void *q, const void *k_cac
 int orc_attend_paged(int q_dtype, int kv_dtype, const void *q, const void *k_blocks,
                      const void *v_blocks, const int32_t *block_table, const int32_t *lengths,
                      int B, int Hq, int Hkv, int D, int num_blocks, int block_size, int max_blocks,
-                     const int32_t *rows, int nrows, double *out, int nthreads, int *threads_used)
+                     const int32_t *rows, int nrows, double *out, const orc_mods *mods,
+                     int nthreads, int *threads_used)
 {
-    if (!usable_shape(B, Hq, Hkv, D) || !usable_dtype(q_dtype) || !usable_dtype(kv_dtype))
+    if (!usable_shape(B, Hq, Hkv, D) || !usable_dtype(q_dtype) || !usable_dtype(kv_dtype) ||
+        !mods_ok(mods, B))
         return ORC_INVALID_ARGUMENT;
     if (orc_validate_attend_paged(lengths, block_table, B, num_blocks, block_size, max_blocks)
         != ORC_OK)
@@ -441,6 +508,7 @@ int orc_attend_paged(int q_dtype, int kv_dtype, const void *q, const void *k_blo
     J.lay.block_size = block_size; J.lay.max_blocks = max_blocks;
     J.B = B; J.Hq = Hq; J.Hkv = Hkv; J.D = D;
     J.out = out;
+    J.mods = mods;
     J.rows = (const int32_t *)rows; J.nrows = nrows;
     int n = run(&J, nthreads);
     if (threads_used)

@@ -20,9 +20,17 @@ MUTANTS = {
     "scale_by_d": ("s[j] = dot / sqrt((double)D);", "s[j] = dot / (double)D;"),
     "new_token_dropped": ("        for (int j = 0; j <= L; ++j) {\n            double dot",
                           "        for (int j = 0; j < L; ++j) {\n            double dot"),
-    "stale_slot_counted": ("        for (int j = 0; j <= L; ++j)\n            Z += exp(s[j] - m);",
-                           "        for (int j = 0; j <= L + 1 && j < 2 * L + 1; ++j)\n            Z += exp(s[j < L + 1 ? j : L] - m);"),
-    "sign_flip": ("Z += exp(s[j] - m);", "Z += exp(m - s[j]);"),
+    "stale_slot_counted": ("        for (int j = 0; j <= L; ++j)\n            if (attended(J, b, L, j))\n                Z += exp(s[j] - m);",
+                           "        for (int j = 0; j <= L + 1 && j < 2 * L + 1; ++j)\n            if (attended(J, b, L, j < L + 1 ? j : L))\n                Z += exp(s[j < L + 1 ? j : L] - m);"),
+    "window_off_by_one": ("if (j > L - M->window)", "if (j >= L - M->window)"),
+    "prefix_inclusive": ("    return j < P;\n}", "    return j <= P;\n}"),
+    "sink_scaled": ("double Z = sink ? exp((double)sink[h] - m) : 0.0;",
+                    "double Z = sink ? exp((double)sink[h] / sqrt((double)D) - m) : 0.0;"),
+    "sink_dropped": ("double Z = sink ? exp((double)sink[h] - m) : 0.0;", "double Z = 0.0;"),
+    "prefix_rows_ignored": ("const int P = M->kept_prefix_rows ? M->kept_prefix_rows[b] : M->kept_prefix;",
+                            "const int P = M->kept_prefix;"),
+    "masked_slot_weighted": ("            if (!attended(J, b, L, j))\n                continue;\n", ""),
+    "sign_flip": ("                Z += exp(s[j] - m);", "                Z += exp(m - s[j]);"),
     "row_head_swapped": ("return ((r * lay->Hkv + kvh) * lay->Smax + s) * lay->D;",
                          "return ((kvh * lay->Hkv + r % lay->Hkv) * lay->Smax + s) * lay->D;"),
     "paged_offset": ("(size_t)(s % lay->block_size)) * lay->D;", "(size_t)(s / lay->block_size)) * lay->D;"),

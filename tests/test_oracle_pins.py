@@ -646,3 +646,162 @@ def test_attend_validate_rules():
     r = oracle.attend_dense(np.zeros((1, 1, 2), np.float32), np.zeros((1, 1, 3, 2), np.float32),
                             np.zeros((1, 1, 3, 2), np.float32), np.array([0], np.int32))
     assert r.status == bad and np.isnan(r.out).all()
+
+
+# ------------------------------------------- softmax modifiers (sink, window)
+#
+# [P5] groupQueryAttention: head_sink is a per-head virtual logit folded into
+# the softmax denominator; kept_prefix keeps the first P keys attended beside
+# the sliding window (a key is attended when it is inside the first P keys or
+# inside the window; the window alone without P); a negative P is refused.
+# Readings: the window holds the W positions ending at the query's own; the
+# sink is in the units of the scaled scores.
+
+def _mods_case(seed, **kw):
+    base = dict(B=3, Hq=8, Hkv=2, D=16, Smax=40, len_lo=5, len_hi=39, seed=seed)
+    base.update(kw)
+    w = W.small("llama3_8b", dtype="f32", **base)
+    return w, oracle_inputs(W.generate(w))
+
+
+def _mods_brute(q, kc, vc, kn, vn, lens, sink, window, prefix):
+    """[P5] rules and the softmax, literally, in pure Python on tiny shapes:
+    w_j = e^{s_j} / (e^{sink_h} + sum over attended slots e^{s_i})."""
+    B, Hq, D = q.shape
+    G = Hq // kc.shape[1]
+    out = np.zeros((B, Hq, D))
+    for b in range(B):
+        L = int(lens[b])
+        P = int(prefix[b]) if np.ndim(prefix) else int(prefix)
+        keep = [j for j in range(L + 1) if window == 0 or j > L - window or j < P]
+        for h in range(Hq):
+            g = h // G
+            qs = [float(x) for x in q[b, h]]
+            key = lambda j: kn[b, g] if j == L else kc[b, g, j]
+            val = lambda j: vn[b, g] if j == L else vc[b, g, j]
+            e = {j: math.exp(sum(a * float(c) for a, c in zip(qs, key(j))) / math.sqrt(D)) for j in keep}
+            z = sum(e.values()) + (math.exp(float(sink[h])) if sink is not None else 0.0)
+            for d in range(D):
+                out[b, h, d] = sum(e[j] * float(val(j)[d]) for j in keep) / z
+    return out
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_mods_brute_force_tiny(seed):
+    rng = np.random.default_rng(300 + seed)
+    B, S, D, Hq, Hkv = 3, 12, 4, 4, 2
+    lens = rng.integers(0, S, size=B).astype(np.int32)
+    q = rng.normal(size=(B, Hq, D)).astype(np.float32)
+    kc = rng.normal(size=(B, Hkv, S, D)).astype(np.float32)
+    vc = rng.normal(size=(B, Hkv, S, D)).astype(np.float32)
+    kn = rng.normal(size=(B, Hkv, D)).astype(np.float32)
+    vn = rng.normal(size=(B, Hkv, D)).astype(np.float32)
+    sink = rng.normal(size=Hq).astype(np.float32) * 2 if seed % 2 == 0 else None
+    window = int(rng.integers(1, 6))
+    prefix = rng.integers(0, 4, size=B).astype(np.int32) if seed % 3 else int(rng.integers(0, 3))
+    r = oracle.decode_dense(q, kn, vn, kc.copy(), vc.copy(), lens, sink=sink, window=window,
+                            kept_prefix=prefix)
+    assert r.status == oracle.OK
+    want = _mods_brute(q, kc, vc, kn, vn, lens, sink, window, prefix)
+    np.testing.assert_allclose(r.out, want, rtol=1e-12, atol=1e-12)
+
+
+def test_sink_as_virtual_key_library_sdpa():
+    """A sink logit equals one more key per query head whose score is the sink
+    and whose value is zero: torch SDPA in float64 on the valid slots plus that
+    virtual key must agree with the oracle's sink."""
+    w, a = _mods_case(41)
+    sink = np.linspace(-2, 3, w.Hq).astype(np.float32)
+    r = oracle.decode_dense(a["q"], a["k_new"], a["v_new"], a["k_cache"].copy(), a["v_cache"].copy(),
+                            a["lengths"], sink=sink)
+    G = w.G
+    for b in range(w.B):
+        L = int(a["lengths"][b])
+        k = torch.cat([torch.from_numpy(a["k_cache"][b, :, :L]), torch.from_numpy(a["k_new"][b])[:, None]], 1)
+        v = torch.cat([torch.from_numpy(a["v_cache"][b, :, :L]), torch.from_numpy(a["v_new"][b])[:, None]], 1)
+        k = k.double().repeat_interleave(G, 0)
+        v = v.double().repeat_interleave(G, 0)
+        qb = torch.from_numpy(a["q"][b]).double()
+        ks = qb * (torch.from_numpy(sink).double() * math.sqrt(w.D) / (qb * qb).sum(-1))[:, None]
+        k = torch.cat([k, ks[:, None]], 1)
+        v = torch.cat([v, torch.zeros(w.Hq, 1, w.D, dtype=torch.float64)], 1)
+        o = torch.nn.functional.scaled_dot_product_attention(qb[:, None], k, v)[:, 0]
+        np.testing.assert_allclose(r.out[b], o.numpy(), rtol=1e-11, atol=1e-12)
+
+
+def test_window_equals_compacted_cache():
+    """Window and kept prefix select slots: the same output comes from a
+    cache that holds only the selected slots, in order (bit for bit, the sums
+    run over the same terms in the same order)."""
+    w, a = _mods_case(42, Smax=64, len_lo=20, len_hi=60)
+    W_, P = 9, 4
+    r = oracle.decode_dense(a["q"], a["k_new"], a["v_new"], a["k_cache"].copy(), a["v_cache"].copy(),
+                            a["lengths"], window=W_, kept_prefix=P)
+    for b in range(w.B):
+        L = int(a["lengths"][b])
+        keep = [j for j in range(L) if j > L - W_ or j < P]
+        kc = np.ascontiguousarray(a["k_cache"][b:b + 1][:, :, keep + [0]])
+        vc = np.ascontiguousarray(a["v_cache"][b:b + 1][:, :, keep + [0]])
+        rb = oracle.decode_dense(a["q"][b:b + 1], a["k_new"][b:b + 1], a["v_new"][b:b + 1], kc, vc,
+                                 np.array([len(keep)], np.int32))
+        assert rb.out.tobytes() == r.out[b:b + 1].tobytes()
+
+
+def test_window_one_returns_new_value_and_wide_window_is_plain():
+    w, a = _mods_case(43)
+    r1 = oracle.decode_dense(a["q"], a["k_new"], a["v_new"], a["k_cache"].copy(), a["v_cache"].copy(),
+                             a["lengths"], window=1)
+    assert np.array_equal(r1.out, np.repeat(a["v_new"].astype(np.float64), w.G, 1))
+    r0 = oracle.decode_dense(a["q"], a["k_new"], a["v_new"], a["k_cache"].copy(), a["v_cache"].copy(),
+                             a["lengths"])
+    big = oracle.decode_dense(a["q"], a["k_new"], a["v_new"], a["k_cache"].copy(), a["v_cache"].copy(),
+                              a["lengths"], window=w.Smax + 1)
+    prefix_only = oracle.decode_dense(a["q"], a["k_new"], a["v_new"], a["k_cache"].copy(),
+                                      a["v_cache"].copy(), a["lengths"], kept_prefix=7)
+    minus_inf = oracle.decode_dense(a["q"], a["k_new"], a["v_new"], a["k_cache"].copy(),
+                                    a["v_cache"].copy(), a["lengths"],
+                                    sink=np.full(w.Hq, -np.inf, np.float32))
+    for r in (big, prefix_only, minus_inf):
+        assert r.out.tobytes() == r0.out.tobytes()
+
+
+def test_kept_prefix_per_row_matches_scalar():
+    w, a = _mods_case(44)
+    per = np.array([0, 3, 11], np.int32)
+    r = oracle.decode_dense(a["q"], a["k_new"], a["v_new"], a["k_cache"].copy(), a["v_cache"].copy(),
+                            a["lengths"], window=5, kept_prefix=per)
+    for b in range(w.B):
+        rb = oracle.decode_dense(a["q"], a["k_new"], a["v_new"], a["k_cache"].copy(), a["v_cache"].copy(),
+                                 a["lengths"], window=5, kept_prefix=int(per[b]), rows=[b])
+        assert rb.out[b].tobytes() == r.out[b].tobytes()
+
+
+def test_mods_attend_and_paged_agree_with_dense_decode():
+    """The modifiers act on the query position L in every form: the attend
+    of lengths L + 1 over a cache holding the new token equals the decode
+    step's output; paged equals dense."""
+    w, a = _mods_case(45)
+    sink = np.linspace(-1, 1, w.Hq).astype(np.float32)
+    kc, vc = a["k_cache"].copy(), a["v_cache"].copy()
+    r_dec = oracle.decode_dense(a["q"], a["k_new"], a["v_new"], kc, vc, a["lengths"], sink=sink,
+                                window=6, kept_prefix=2)
+    r_att = oracle.attend_dense(a["q"], kc, vc, a["lengths"] + 1, sink=sink, window=6, kept_prefix=2)
+    assert r_att.out.tobytes() == r_dec.out.tobytes()
+    bs = 4
+    nb = w.Smax // bs
+    kb = np.ascontiguousarray(kc.reshape(w.B, w.Hkv, nb, bs, w.D).transpose(0, 2, 1, 3, 4)
+                              .reshape(w.B * nb, w.Hkv, bs, w.D))
+    vb = np.ascontiguousarray(vc.reshape(w.B, w.Hkv, nb, bs, w.D).transpose(0, 2, 1, 3, 4)
+                              .reshape(w.B * nb, w.Hkv, bs, w.D))
+    bt = np.arange(w.B * nb, dtype=np.int32).reshape(w.B, nb)
+    r_pg = oracle.attend_paged(a["q"], kb, vb, bt, a["lengths"] + 1, sink=sink, window=6, kept_prefix=2)
+    assert r_pg.out.tobytes() == r_dec.out.tobytes()
+
+
+def test_mods_refused():
+    w, a = _mods_case(46)
+    for kw in (dict(window=-1), dict(window=4, kept_prefix=-1),
+               dict(window=4, kept_prefix=np.array([0, -2, 1], np.int32))):
+        r = oracle.decode_dense(a["q"], a["k_new"], a["v_new"], a["k_cache"].copy(), a["v_cache"].copy(),
+                                a["lengths"], **kw)
+        assert r.status == oracle.INVALID_ARGUMENT
