@@ -21,6 +21,8 @@ With --impl reference the oracle itself is timed as the reference arm.
 
 --op attend times the read-only attend instead (no append; lengths count the
 valid slots; a float32 query over the workload's cache unless --q-dtype cache).
+--window W / --kept-prefix P / --sink add the softmax modifiers; the KV bytes
+then count only the slots inside the window or the prefix.
 
 Multi-GPU (torchrun): every rank runs an independent replica with its own
 batch (weak scaling, no data-path collective); times are max over ranks.
@@ -58,6 +60,9 @@ def parse():
                     help="decode step (default) or the read-only attend")
     ap.add_argument("--q-dtype", default=None, choices=["cache", "f32"],
                     help="attend only: query dtype (default f32)")
+    ap.add_argument("--window", type=int, default=0, help="sliding window W (0: none)")
+    ap.add_argument("--kept-prefix", type=int, default=0, help="kept prefix P (with a window)")
+    ap.add_argument("--sink", action="store_true", help="a per-head sink logit (seeded N(0,1))")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sched-pad", type=int, default=None,
                     help="schedule-only tiles per (row, head); default: the library's")
@@ -120,15 +125,30 @@ def workload(name, rank):
     return w
 
 
-def algorithmic_bytes(w, t, attend=False) -> dict:
+def cached_slots_read(L, attend, window=0, kept_prefix=0):
+    """Cached slots each row's step must read: the decode step reads slots
+    0..L-1 (slot L = lengths[b] comes from k_new / v_new), the attend slots
+    0..L-1 with L = lengths[b]; with a window W only those above L' - W (L' the
+    query position) and those below the kept prefix P."""
+    import torch
+    L = L.to(torch.int64)
+    if not window:
+        return L
+    last = L - 1 if attend else L                      # query position
+    lo = torch.clamp(last - window + 1, min=0)
+    return (L - lo) + torch.clamp(lo, max=kept_prefix)
+
+
+def algorithmic_bytes(w, t, attend=False, window=0, kept_prefix=0) -> dict:
     """Bytes the step must move (no split partials): the KV read, the append
     write, the new K/V, q, out and the index reads. The decode step reads the
     lengths[b] cached slots (slot lengths[b] comes from k_new / v_new); the
-    read-only attend reads its lengths[b] valid slots and appends nothing."""
+    read-only attend reads its lengths[b] valid slots and appends nothing; a
+    window and kept prefix cut both to the attended slots."""
     import torch
     L = t["lengths"].to(torch.int64)
     es = w.elem_bytes
-    kv = int(L.sum().item()) * w.Hkv * w.D * 2 * es
+    kv = int(cached_slots_read(L, attend, window, kept_prefix).sum().item()) * w.Hkv * w.D * 2 * es
     new = 0 if attend else w.B * w.Hkv * w.D * es * 2
     idx = w.B * 4 * (2 if w.slot_ids else 1)
     if w.paged:
@@ -140,26 +160,23 @@ def algorithmic_bytes(w, t, attend=False) -> dict:
             "total": kv + 2 * new + q + w.B * w.Hq * w.D * 4 + idx}
 
 
-def step_fn(w, t, kernel, out, sched_pad=None, attend=False):
+def step_fn(w, t, kernel, out, sched_pad=None, attend=False, mods=None):
     import gqa_kv_cache_gb300 as gqa
+    kw = dict(out=out, kernel=kernel, sched_pad=sched_pad, **(mods or {}))
     if attend and w.paged:
         def run(tt=t):
-            gqa.attend_paged(tt["q"], tt["k_blocks"], tt["v_blocks"], tt["block_table"], tt["lengths"],
-                             out=out, kernel=kernel, sched_pad=sched_pad)
+            gqa.attend_paged(tt["q"], tt["k_blocks"], tt["v_blocks"], tt["block_table"], tt["lengths"], **kw)
     elif attend:
         def run(tt=t):
-            gqa.attend(tt["q"], tt["k_cache"], tt["v_cache"], tt["lengths"], tt.get("slot_ids"),
-                       out=out, kernel=kernel, sched_pad=sched_pad)
+            gqa.attend(tt["q"], tt["k_cache"], tt["v_cache"], tt["lengths"], tt.get("slot_ids"), **kw)
     elif w.paged:
         def run(tt=t):
             gqa.decode_step_paged(tt["q"], tt["k_new"], tt["v_new"], tt["k_blocks"], tt["v_blocks"],
-                                  tt["block_table"], tt["lengths"], out=out, kernel=kernel,
-                                  sched_pad=sched_pad)
+                                  tt["block_table"], tt["lengths"], **kw)
     else:
         def run(tt=t):
             gqa.decode_step(tt["q"], tt["k_new"], tt["v_new"], tt["k_cache"], tt["v_cache"],
-                            tt["lengths"], tt.get("slot_ids"), out=out, kernel=kernel,
-                            sched_pad=sched_pad)
+                            tt["lengths"], tt.get("slot_ids"), **kw)
     return run
 
 
@@ -223,7 +240,7 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- oracle ---
 
-def oracle_rate(w, t, rows, repeats=3):
+def oracle_rate(w, t, rows, repeats=3, mods=None):
     """CPU oracle over batch rows `rows` (host copies), timed: returns
     (GB/s of KV processed, seconds per pass, threads)."""
     import numpy as np
@@ -237,6 +254,11 @@ def oracle_rate(w, t, rows, repeats=3):
             else x.numpy().copy()
 
     attend = "k_new" not in t
+    om = {}
+    if mods:
+        om = {"window": mods.get("window", 0), "kept_prefix": mods.get("kept_prefix", 0)}
+        if mods.get("sink") is not None:
+            om["sink"] = mods["sink"].cpu().numpy()
     q, L = host(t["q"][sel]), host(t["lengths"][sel])
     if not attend:
         kn, vn = host(t["k_new"][sel]), host(t["v_new"][sel])
@@ -247,13 +269,13 @@ def oracle_rate(w, t, rows, repeats=3):
         idx = torch.tensor(used, dtype=torch.long, device=t["q"].device)
         kb, vb = host(t["k_blocks"][idx]), host(t["v_blocks"][idx])
         btr = np.vectorize(lambda x: remap.get(int(x), -1))(bt).astype(np.int32)
-        run = (lambda: oracle.attend_paged(q, kb, vb, btr, L)) if attend else \
-            (lambda: oracle.decode_paged(q, kn, vn, kb, vb, btr, L, append=False))
+        run = (lambda: oracle.attend_paged(q, kb, vb, btr, L, **om)) if attend else \
+            (lambda: oracle.decode_paged(q, kn, vn, kb, vb, btr, L, append=False, **om))
     else:
         cr = t["slot_ids"][sel].long() if "slot_ids" in t else sel
         kc, vc = host(t["k_cache"][cr]), host(t["v_cache"][cr])
-        run = (lambda: oracle.attend_dense(q, kc, vc, L)) if attend else \
-            (lambda: oracle.decode_dense(q, kn, vn, kc, vc, L, append=False))
+        run = (lambda: oracle.attend_dense(q, kc, vc, L, **om)) if attend else \
+            (lambda: oracle.decode_dense(q, kn, vn, kc, vc, L, append=False, **om))
     r = run()                                   # warm-up
     times = []
     for _ in range(repeats):
@@ -261,8 +283,26 @@ def oracle_rate(w, t, rows, repeats=3):
         r = run()
         times.append(time.perf_counter() - t0)
     sec = statistics.median(times)
-    kv = int(np.asarray(L, dtype=np.int64).sum()) * w.Hkv * w.D * 2 * w.elem_bytes
+    win, kp = (mods or {}).get("window", 0), (mods or {}).get("kept_prefix", 0)
+    n = cached_slots_read(torch.from_numpy(np.asarray(L, dtype=np.int64)), attend, win, kp)
+    kv = int(n.sum().item()) * w.Hkv * w.D * 2 * w.elem_bytes
     return kv / sec / 1e9, sec, r.threads
+
+
+def make_mods(args, w, dev):
+    """The softmax modifiers asked for on the command line (None: none)."""
+    import torch
+    if not args.window and not args.kept_prefix and not args.sink:
+        return None
+    m = {"window": args.window, "kept_prefix": args.kept_prefix}
+    if args.sink:
+        g = torch.Generator().manual_seed(1234)
+        m["sink"] = torch.randn(w.Hq, generator=g).to(dev)
+    return m
+
+
+def mods_config(args):
+    return {"window": args.window, "kept_prefix": args.kept_prefix, "sink": bool(args.sink)}
 
 
 def peaks():
@@ -310,14 +350,15 @@ def run_reference(args, ranks):
     import workloads as W
     attend = args.op == "attend"
     t = W.generate(w, dev, attend=attend, q_f32=attend and args.q_dtype != "cache")
+    mods = make_mods(args, w, dev)
     n = min(w.B, 4)
     for i in range(args.warmup):
-        oracle_rate(w, t, [(i * n + k) % w.B for k in range(n)], repeats=1)
+        oracle_rate(w, t, [(i * n + k) % w.B for k in range(n)], repeats=1, mods=mods)
     rates, secs, threads = [], [], 1
     kv_total, t_total = 0, 0.0
     for i in range(args.steps):
         rows = [((i + args.warmup) * n + k) % w.B for k in range(n)]
-        gbs, sec, threads = oracle_rate(w, t, rows, repeats=1)
+        gbs, sec, threads = oracle_rate(w, t, rows, repeats=1, mods=mods)
         kv_total += gbs * sec * 1e9
         t_total += sec
     value = kv_total / t_total / 1e9
@@ -326,7 +367,8 @@ def run_reference(args, ranks):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_total / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": w.name, "op": args.op, "B": w.B, "Hq": w.Hq,
-                                        "Hkv": w.Hkv, "D": w.D, "sample_rows_per_step": n},
+                                        "Hkv": w.Hkv, "D": w.D, "sample_rows_per_step": n,
+                                        **mods_config(args)},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": f"{n} of {w.B} batch rows per step, rotating, float64 loops"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -346,8 +388,9 @@ def run_ours(args, ranks):
     t = W.generate(w, dev, attend=attend, q_f32=attend and args.q_dtype != "cache")
     torch.cuda.synchronize()
     out = torch.empty(w.B, w.Hq, w.D, dtype=torch.float32, device=dev)
-    step = step_fn(w, t, args.kernel, out, args.sched_pad, attend)
-    alg = algorithmic_bytes(w, t, attend)
+    mods = make_mods(args, w, dev)
+    step = step_fn(w, t, args.kernel, out, args.sched_pad, attend, mods)
+    alg = algorithmic_bytes(w, t, attend, args.window, args.kept_prefix)
     flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush_r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     flush_sink = torch.empty((), dtype=torch.float32, device=dev)
@@ -408,7 +451,7 @@ def run_ours(args, ranks):
     avg_main_s = ms_main / max(n_main, 1) * 1e-3
     hbm_peak, peak_kind = peaks()
     achieved = alg["total"] / avg_main_s / 1e9
-    traffic = traffic_for(main, w.name + ("/attend" if attend else ""))
+    traffic = None if mods else traffic_for(main, w.name + ("/attend" if attend else ""))
 
     # ---- end to end through the public API, host buffers, copies inside
     Ke = min(K, 500)
@@ -419,7 +462,7 @@ def run_ours(args, ranks):
     dev_in = {k: torch.empty_like(t[k]) for k in inputs}
     tt = dict(t)
     tt.update(dev_in)
-    step_e2e = step_fn(w, tt, args.kernel, out, args.sched_pad, attend)
+    step_e2e = step_fn(w, tt, args.kernel, out, args.sched_pad, attend, mods)
     out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
     h2d = sum(host[k].numel() * host[k].element_size() for k in inputs)
     d2h = out.numel() * out.element_size()
@@ -443,7 +486,7 @@ def run_ours(args, ranks):
     cpu = None
     if ranks.world == 1 and not args.no_cpu_baseline:
         rows = list(range(w.B))
-        gbs, sec, threads = oracle_rate(w, t, rows, repeats=3)
+        gbs, sec, threads = oracle_rate(w, t, rows, repeats=3, mods=mods)
         cpu = {"value": gbs, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": f"all {w.B} batch rows of one step (no append), float64 loops, "
                          f"median of 3 after 1 warm-up, {sec:.2f} s per pass"}
@@ -465,6 +508,7 @@ def run_ours(args, ranks):
                           "write": "flushed between timed steps (256 MB write outside the events)",
                           "none": "not flushed; inputs larger than L2"}[args.l2_flush],
                    "parallelism": f"replicas x{ranks.world} (independent batches per GPU)",
+                   **mods_config(args),
                    "wall_s_timed_region": wall},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": traffic,

@@ -30,7 +30,7 @@ __all__ = ["decode_step", "decode_step_paged", "attend", "attend_paged", "worksp
 
 OK, INVALID_ARGUMENT, UNSUPPORTED, CUDA_ERROR, WORKSPACE = 0, 1, 2, 3, 4
 KERNELS = {"auto": 0, "simt": 1, "tc": 2}
-STATUS_BITS = {1: "bad length", 2: "bad slot id", 4: "bad block", 8: "timeout"}
+STATUS_BITS = {1: "bad length", 2: "bad slot id", 4: "bad block", 8: "timeout", 16: "bad kept prefix"}
 _DTYPES = {torch.float32: 0, torch.bfloat16: 1}
 
 library_path = _lib.LIB_PATH
@@ -52,11 +52,28 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _opts(kernel, grid_ctas, sched_pad=None):
+def _opts(kernel, grid_ctas, sched_pad=None, sink=None, window=0, kept_prefix=0, device=None, B=None,
+          Hq=None):
+    """The gqa_options struct. Softmax modifiers: ``sink`` a float32 (Hq,)
+    device tensor, ``window`` an int >= 0, ``kept_prefix`` an int >= 0 or an
+    int32 (B,) device tensor."""
     o = _lib.GqaOptions()
     o.kernel = KERNELS[kernel] if isinstance(kernel, str) else int(kernel)
     o.grid_ctas = int(grid_ctas)
     o.sched_pad = 0 if sched_pad is None else int(sched_pad) + 1   # 0 = library default
+    o.window = int(window or 0)
+    if sink is not None:
+        if sink.dtype != torch.float32 or sink.shape != (Hq,) or not sink.is_contiguous() \
+                or sink.device != device:
+            raise TypeError("sink must be a contiguous float32 (Hq,) tensor on q's device")
+        o.head_sink = sink.data_ptr()
+    if isinstance(kept_prefix, torch.Tensor):
+        if kept_prefix.dtype != torch.int32 or kept_prefix.shape != (B,) \
+                or not kept_prefix.is_contiguous() or kept_prefix.device != device:
+            raise TypeError("kept_prefix must be an int or a contiguous int32 (B,) tensor on q's device")
+        o.kept_prefix_rows = kept_prefix.data_ptr()
+    else:
+        o.kept_prefix = int(kept_prefix or 0)
     return o
 
 
@@ -115,11 +132,13 @@ def _common_checks(q, k_new, v_new, caches, lengths, out, q_any_dtype=False):
 
 
 def decode_step(q, k_new, v_new, k_cache, v_cache, lengths, slot_ids=None, *, out=None,
-                status=None, kernel="auto", grid_ctas=0, workspace=None, stream=None, sched_pad=None):
+                status=None, kernel="auto", grid_ctas=0, workspace=None, stream=None, sched_pad=None,
+                sink=None, window=0, kept_prefix=0):
     """One decode step on a dense (R, Hkv, Smax, D) cache (continuous batch
     when ``slot_ids`` is given). Appends in place; returns ``out``. A
     ``workspace`` passed in must be zero-filled before its first use (the
-    library leaves it zero-filled after every call)."""
+    library leaves it zero-filled after every call). ``sink``, ``window`` and
+    ``kept_prefix`` are the softmax modifiers of the C header's gqa_options."""
     dt, out = _common_checks(q, k_new, v_new, (("k_cache", k_cache), ("v_cache", v_cache)),
                              lengths, out)
     B, Hq, D = q.shape
@@ -128,7 +147,7 @@ def decode_step(q, k_new, v_new, k_cache, v_cache, lengths, slot_ids=None, *, ou
         raise ValueError("shape mismatch between q, k_new, v_new and the caches")
     if slot_ids is not None and (slot_ids.dtype != torch.int32 or slot_ids.shape != (B,)):
         raise TypeError("slot_ids must be int32 of shape (B,)")
-    o = _opts(kernel, grid_ctas, sched_pad)
+    o = _opts(kernel, grid_ctas, sched_pad, sink, window, kept_prefix, q.device, B, Hq)
     lib = _lib.load()
     need = lib.gqa_workspace_bytes(B, Hq, Hkv, D, _DTYPES[dt], ctypes.byref(o))
     ws = _workspace(q.device, need) if workspace is None else workspace
@@ -142,7 +161,7 @@ def decode_step(q, k_new, v_new, k_cache, v_cache, lengths, slot_ids=None, *, ou
 
 def decode_step_paged(q, k_new, v_new, k_blocks, v_blocks, block_table, lengths, *, out=None,
                       status=None, kernel="auto", grid_ctas=0, workspace=None, stream=None,
-                      sched_pad=None):
+                      sched_pad=None, sink=None, window=0, kept_prefix=0):
     """One decode step on a paged cache (num_blocks, Hkv, block_size, D) with
     a (B, max_blocks) int32 block table (-1 = unused). Appends in place."""
     dt, out = _common_checks(q, k_new, v_new, (("k_blocks", k_blocks), ("v_blocks", v_blocks)),
@@ -155,7 +174,7 @@ def decode_step_paged(q, k_new, v_new, k_blocks, v_blocks, block_table, lengths,
             or not block_table.is_contiguous():
         raise TypeError("block_table must be a contiguous int32 (B, max_blocks) tensor")
     MB = block_table.shape[1]
-    o = _opts(kernel, grid_ctas, sched_pad)
+    o = _opts(kernel, grid_ctas, sched_pad, sink, window, kept_prefix, q.device, B, Hq)
     lib = _lib.load()
     need = lib.gqa_workspace_bytes(B, Hq, Hkv, D, _DTYPES[dt], ctypes.byref(o))
     ws = _workspace(q.device, need) if workspace is None else workspace
@@ -169,7 +188,8 @@ def decode_step_paged(q, k_new, v_new, k_blocks, v_blocks, block_table, lengths,
 
 
 def attend(q, k_cache, v_cache, lengths, slot_ids=None, *, out=None, status=None, kernel="auto",
-           grid_ctas=0, workspace=None, stream=None, sched_pad=None):
+           grid_ctas=0, workspace=None, stream=None, sched_pad=None, sink=None, window=0,
+           kept_prefix=0):
     """Read-only attend on a dense (R, Hkv, Smax, D) cache: slots
     ``0..lengths[b]-1`` (1 <= lengths[b] <= Smax), nothing written but ``out``.
     ``q`` (B, Hq, D) is float32 or bfloat16 whatever the cache dtype."""
@@ -181,7 +201,7 @@ def attend(q, k_cache, v_cache, lengths, slot_ids=None, *, out=None, status=None
         raise ValueError("shape mismatch between q and the caches")
     if slot_ids is not None and (slot_ids.dtype != torch.int32 or slot_ids.shape != (B,)):
         raise TypeError("slot_ids must be int32 of shape (B,)")
-    o = _opts(kernel, grid_ctas, sched_pad)
+    o = _opts(kernel, grid_ctas, sched_pad, sink, window, kept_prefix, q.device, B, Hq)
     lib = _lib.load()
     need = lib.gqa_workspace_bytes(B, Hq, Hkv, D, _DTYPES[dt], ctypes.byref(o))
     ws = _workspace(q.device, need) if workspace is None else workspace
@@ -194,7 +214,8 @@ def attend(q, k_cache, v_cache, lengths, slot_ids=None, *, out=None, status=None
 
 
 def attend_paged(q, k_blocks, v_blocks, block_table, lengths, *, out=None, status=None,
-                 kernel="auto", grid_ctas=0, workspace=None, stream=None, sched_pad=None):
+                 kernel="auto", grid_ctas=0, workspace=None, stream=None, sched_pad=None,
+                 sink=None, window=0, kept_prefix=0):
     """Read-only attend on a paged cache (num_blocks, Hkv, block_size, D)."""
     dt, out = _common_checks(q, None, None, (("k_blocks", k_blocks), ("v_blocks", v_blocks)),
                              lengths, out, q_any_dtype=True)
@@ -205,7 +226,7 @@ def attend_paged(q, k_blocks, v_blocks, block_table, lengths, *, out=None, statu
     if block_table.dtype != torch.int32 or block_table.dim() != 2 or block_table.shape[0] != B \
             or not block_table.is_contiguous():
         raise TypeError("block_table must be a contiguous int32 (B, max_blocks) tensor")
-    o = _opts(kernel, grid_ctas, sched_pad)
+    o = _opts(kernel, grid_ctas, sched_pad, sink, window, kept_prefix, q.device, B, Hq)
     lib = _lib.load()
     need = lib.gqa_workspace_bytes(B, Hq, Hkv, D, _DTYPES[dt], ctypes.byref(o))
     ws = _workspace(q.device, need) if workspace is None else workspace

@@ -218,6 +218,10 @@ gqa_status run_step(const Shape &s, const void *q, const void *k_new, const void
         return GQA_ERR_INVALID_ARGUMENT;
     if (!aligned16(q) || !aligned16(kc) || !aligned16(vc) || !aligned16(out))
         return GQA_ERR_INVALID_ARGUMENT;
+    if (opt && (opt->window < 0 || opt->kept_prefix < 0 ||
+                (reinterpret_cast<uintptr_t>(opt->head_sink) & 3u) ||
+                (reinterpret_cast<uintptr_t>(opt->kept_prefix_rows) & 3u)))
+        return GQA_ERR_INVALID_ARGUMENT;
     if (!s.attend && (!aligned16(k_new) || !aligned16(v_new)))
         return GQA_ERR_INVALID_ARGUMENT;
     const int G = s.Hq / s.Hkv;
@@ -256,6 +260,12 @@ gqa_status run_step(const Shape &s, const void *q, const void *k_new, const void
     p.block_size = s.block_size;
     p.max_blocks = s.max_blocks;
     p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)s.D));
+    if (opt) {
+        p.sink = opt->head_sink;
+        p.window = opt->window;
+        p.kept_prefix = opt->kept_prefix;
+        p.kept_prefix_rows = opt->kept_prefix_rows;
+    }
     p.tile = kernel == GQA_KERNEL_TC ? tc_tile() : simt_tile();
     // about the time a CTA spends finishing a sequence, in tiles of streaming
     p.pad_tiles = (opt && opt->sched_pad > 0) ? opt->sched_pad - 1 : kDefaultSchedPad;

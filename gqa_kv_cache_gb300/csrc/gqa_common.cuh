@@ -5,7 +5,10 @@
 // Work decomposition. A unit is one (batch row b, cache head kvh) pair; unit
 // u = b * Hkv + kvh. Its slots 0..L are attended: in the decode step
 // L = lengths[b] and slot L is the new token; in the read-only attend
-// L = lengths[b] - 1 (lengths counts the valid slots). They are cut into tiles of T slots, n_tiles(b) = ceil((L + 1) / T). The tiles of
+// L = lengths[b] - 1 (lengths counts the valid slots). With a sliding window
+// W and a kept prefix P only the slots j <= L with j > L - W or j < P are
+// attended, and only the tiles that hold such a slot are listed (the prefix
+// tiles, then the window tiles: the tiles in between are skipped). They are cut into tiles of T slots, n_tiles(b) = ceil((L + 1) / T). The tiles of
 // all units, in (b, kvh, tile) order, form one list of N tiles, and CTA i of
 // a grid takes the contiguous range [floor(i N / C), floor((i+1) N / C)) with
 // C = min(grid size, N), so every working CTA owns at least one tile (CTAs
@@ -33,6 +36,7 @@ constexpr int kBadLength = 1;
 constexpr int kBadSlotId = 2;
 constexpr int kBadBlock = 4;
 constexpr int kTimeout = 8;
+constexpr int kBadPrefix = 16;
 
 struct DecodeParams {
     const void *q;      // (B, Hq, D)
@@ -50,6 +54,11 @@ struct DecodeParams {
     int R, Smax;                                     // dense
     int paged, num_blocks, block_size, max_blocks;   // paged
     float scale_log2;  // log2(e) / sqrt(D): scores are kept in base-2 units
+    // softmax modifiers
+    const float *sink;               // (Hq) logits folded into the denominator, or null
+    int window;                      // W > 0: only the last W positions (and the prefix); 0: all
+    int kept_prefix;                 // P for every row when kept_prefix_rows is null
+    const int32_t *kept_prefix_rows; // (B) P per row, or null
     int tile;          // T, slots per tile
     int pad_tiles;     // W, schedule-only tiles appended to every unit (see row_tiles)
     int grid;          // C, CTAs of the decode launch
@@ -97,13 +106,60 @@ __host__ __device__ inline long long row_capacity(const DecodeParams &p)
     return p.paged ? (long long)p.max_blocks * p.block_size : (long long)p.Smax;
 }
 
-// Tiles of batch row b for ONE cache head that hold data: ceil((L + 1) / T).
-// Rows with bad content get one tile, which only writes NaN.
-__device__ __forceinline__ int real_tiles(const DecodeParams &p, int L)
+// The kept prefix of row b (negative: a bad row).
+__device__ __forceinline__ int kept_prefix(const DecodeParams &p, int b)
 {
-    if (L < 0 || (long long)L >= row_capacity(p))
-        return 1;
-    return (L + p.tile) / p.tile;
+    return p.kept_prefix_rows ? __ldg(p.kept_prefix_rows + b) : p.kept_prefix;
+}
+
+// Geometry of batch row b's tiles (the same for every cache head). Slot j is
+// attended when j <= L and (j >= lo or j < P). The real tiles are the tiles at
+// positions 0 .. tp-1 (those holding prefix slots below lo) and then
+// tp + gap .. L / T (those holding window slots); without a window lo = 0,
+// gap = 0 and all ceil((L + 1) / T) tiles are real. Rows with bad content get
+// one tile, which only writes NaN.
+struct RowGeom {
+    int L;    // last attended slot
+    int lo;   // first slot of the window (0 without one)
+    int P;    // kept prefix
+    int nr;   // real tiles
+    int tp;   // tiles holding prefix slots below lo
+    int gap;  // tiles skipped between them and the window's first tile
+};
+
+__device__ __forceinline__ bool geom_ok(const DecodeParams &p, int L, int P)
+{
+    return L >= 0 && (long long)L < row_capacity(p) && P >= 0;
+}
+
+__device__ __forceinline__ RowGeom row_geom(const DecodeParams &p, int b)
+{
+    RowGeom r;
+    r.L = last_slot(p, b);
+    r.P = kept_prefix(p, b);
+    r.lo = 0;
+    r.tp = 0;
+    r.gap = 0;
+    if (!geom_ok(p, r.L, r.P)) {
+        r.nr = 1;
+        return r;
+    }
+    const int T = p.tile;
+    const int last_tile = r.L / T;
+    if (p.window > 0) {
+        r.lo = (int)max(0LL, (long long)r.L - p.window + 1);
+        const int pe = min(r.P, r.lo);                 // prefix slots below the window
+        r.tp = (pe + T - 1) / T;
+        r.gap = max(0, r.lo / T - r.tp);
+    }
+    r.nr = last_tile + 1 - r.gap;
+    return r;
+}
+
+// Whether slot j of a row with this geometry takes part in the softmax.
+__device__ __forceinline__ bool attended(int L, int lo, int P, int j)
+{
+    return j <= L && (j >= lo || j < P);
 }
 
 // Tiles of one unit in the schedule: its real tiles plus W virtual ones that
@@ -111,9 +167,9 @@ __device__ __forceinline__ int real_tiles(const DecodeParams &p, int L)
 // time as streaming a few tiles; counting W extra tiles per unit gives the
 // CTAs whose ranges cross more unit boundaries correspondingly fewer real
 // tiles, so all CTAs finish together.
-__device__ __forceinline__ int row_tiles(const DecodeParams &p, int L)
+__device__ __forceinline__ int row_tiles(const DecodeParams &p, int b)
 {
-    return real_tiles(p, L) + p.pad_tiles;
+    return row_geom(p, b).nr + p.pad_tiles;
 }
 
 // CTAs that share the N tiles: min(grid size, N).
@@ -135,32 +191,49 @@ __device__ __forceinline__ void report(const DecodeParams &p, int bits)
 }
 
 // Position of a CTA in the tile list.
+// (Kept small: it lives in registers through the whole streaming loop. The
+// schedule's constants N and C live in the shared TileWalk.)
 struct TileCursor {
     long long g;      // global tile index
     long long end;    // one past the last tile of the current range
-    long long N, C;   // tiles in the list, CTAs sharing them
     int b, kvh, t;    // current row, head, tile within the unit
-    int nt;           // tiles per head of row b in the schedule
-    int nr;           // of which real (t < nr holds data; the rest are virtual)
+    int nr;           // real tiles of the unit (t < nr holds data; the next
+                      // pad_tiles schedule positions are virtual)
     int L;            // last attended slot of row b (last_slot)
+    int lo, P;        // window start and kept prefix of row b (see RowGeom)
+    int tp, gap;      // real tile t sits at tile position t (t < tp) or t + gap
 };
+
+__device__ __forceinline__ void set_row(const DecodeParams &p, TileCursor &c)
+{
+    const RowGeom r = row_geom(p, c.b);
+    c.L = r.L;
+    c.lo = r.lo;
+    c.P = r.P;
+    c.nr = r.nr;
+    c.tp = r.tp;
+    c.gap = r.gap;
+}
+
+// First slot of the cursor's (real) tile.
+__device__ __forceinline__ int tile_slot0(const TileCursor &c, int T)
+{
+    return (c.t < c.tp ? c.t : c.t + c.gap) * T;
+}
 
 // Cursor at global tile g, which lies in row b whose tiles start at `run`.
 __device__ __forceinline__ TileCursor cursor_at(const DecodeParams &p, int b, long long run, long long g,
-                                               long long end, long long N, long long C)
+                                               long long end)
 {
     TileCursor c;
     c.g = g;
     c.end = end;
-    c.N = N;
-    c.C = C;
     c.b = b;
-    c.L = last_slot(p, b);
-    c.nt = row_tiles(p, c.L);
-    c.nr = real_tiles(p, c.L);
+    set_row(p, c);
+    const int nt = c.nr + p.pad_tiles;
     const long long within = g - run;
-    c.kvh = (int)(within / c.nt);
-    c.t = (int)(within % c.nt);
+    c.kvh = (int)(within / nt);
+    c.t = (int)(within % nt);
     return c;
 }
 
@@ -170,15 +243,18 @@ __device__ __forceinline__ TileCursor cursor_at(const DecodeParams &p, int b, lo
 // range `b` = [begin, split). The units cut by CTA boundaries thus have all
 // their partial states written early in the kernel (the next CTA starts with
 // the same unit's tail), and the end of the kernel finishes whole units only.
+// Held in shared memory (one copy per CTA).
 struct TileWalk {
     TileCursor a, b;
+    long long N, C;   // tiles in the list, CTAs sharing them
 };
 
 // Every thread of the block must call it (it uses __syncthreads and
 // `scratch`, >= blockDim.x / 32 + 8 long longs of shared memory; blockDim.x a
 // multiple of 32). The row prefix is a block-wide scan of the per-row tile
-// counts, recomputed by every CTA from `lengths` (no host round trip).
-__device__ inline TileWalk schedule_walk(const DecodeParams &p, long long *scratch)
+// counts, recomputed by every CTA from `lengths` (no host round trip). The
+// walk is written to `out` (shared memory), visible to all threads on return.
+__device__ inline void schedule_walk(const DecodeParams &p, long long *scratch, TileWalk *out)
 {
     const int nthr = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nwarps = nthr >> 5;
@@ -186,7 +262,7 @@ __device__ inline TileWalk schedule_walk(const DecodeParams &p, long long *scrat
     const int r0 = min(p.B, tid * chunk), r1 = min(p.B, r0 + chunk);
     long long local = 0;
     for (int b = r0; b < r1; ++b)
-        local += (long long)p.Hkv * row_tiles(p, last_slot(p, b));
+        local += (long long)p.Hkv * row_tiles(p, b);
     // inclusive scan: within the warp by shuffles, then over the warp totals
     long long incl = local;
 #pragma unroll
@@ -217,7 +293,7 @@ __device__ inline TileWalk schedule_walk(const DecodeParams &p, long long *scrat
     if (begin < end && ((begin >= excl && begin < incl) || (last >= excl && last < incl))) {
         long long run = excl;
         for (int b = r0; b < r1; ++b) {
-            const long long n = (long long)p.Hkv * row_tiles(p, last_slot(p, b));
+            const long long n = (long long)p.Hkv * row_tiles(p, b);
             if (begin >= run && begin < run + n) {
                 found[0] = b;
                 found[1] = run;
@@ -230,48 +306,47 @@ __device__ inline TileWalk schedule_walk(const DecodeParams &p, long long *scrat
         }
     }
     __syncthreads();
-    TileWalk w;
-    if (begin >= end) {
-        TileCursor none;
-        none.g = none.end = N;
-        none.N = N;
-        none.C = C;
-        none.b = none.kvh = none.t = none.L = 0;
-        none.nt = 1;
-        w.a = w.b = none;
-    } else {
-        const TileCursor first = cursor_at(p, (int)found[0], found[1], begin, end, N, C);
-        const TileCursor tail = cursor_at(p, (int)found[2], found[3], last, end, N, C);
-        const long long unit_start = last - tail.t;
-        if (unit_start <= begin) {        // a single segment: walk it in order
-            w.a = first;
-            w.b = first;
-            w.b.g = w.b.end = end;
+    if (tid == 0) {
+        TileWalk &w = *out;
+        w.N = N;
+        w.C = C;
+        if (begin >= end) {
+            TileCursor none;
+            none.g = none.end = N;
+            none.b = none.kvh = none.t = none.L = 0;
+            none.lo = none.P = none.tp = none.gap = 0;
+            none.nr = 1;
+            w.a = w.b = none;
         } else {
-            w.a = tail;
-            w.a.g = unit_start;
-            w.a.t = 0;
-            w.b = first;
-            w.b.end = unit_start;
+            const TileCursor first = cursor_at(p, (int)found[0], found[1], begin, end);
+            const TileCursor tail = cursor_at(p, (int)found[2], found[3], last, end);
+            const long long unit_start = last - tail.t;
+            if (unit_start <= begin) {        // a single segment: walk it in order
+                w.a = first;
+                w.b = first;
+                w.b.g = w.b.end = end;
+            } else {
+                w.a = tail;
+                w.a.g = unit_start;
+                w.a.t = 0;
+                w.b = first;
+                w.b.end = unit_start;
+            }
         }
     }
     __syncthreads();
-    return w;
 }
 
 __device__ __forceinline__ void advance(const DecodeParams &p, TileCursor &c)
 {
     ++c.g;
-    if (++c.t == c.nt) {
+    if (++c.t == c.nr + p.pad_tiles) {
         c.t = 0;
         if (++c.kvh == p.Hkv) {
             c.kvh = 0;
             ++c.b;
-            if (c.g < c.end) {
-                c.L = last_slot(p, c.b);
-                c.nt = row_tiles(p, c.L);
-                c.nr = real_tiles(p, c.L);
-            }
+            if (c.g < c.end)
+                set_row(p, c);
         }
     }
 }
@@ -320,7 +395,7 @@ __device__ __forceinline__ bool walk_first(const DecodeParams &p, TileCursor &c,
 // Row-level content check: length in range, slot id in range.
 __device__ __forceinline__ bool row_ok(const DecodeParams &p, int b, int L)
 {
-    if (L < 0 || (long long)L >= row_capacity(p))
+    if (L < 0 || (long long)L >= row_capacity(p) || kept_prefix(p, b) < 0)
         return false;
     if (!p.paged && p.slot_ids) {
         int r = __ldg(p.slot_ids + b);
@@ -334,6 +409,8 @@ __device__ __forceinline__ int row_error_bits(const DecodeParams &p, int b, int 
 {
     if (L < 0 || (long long)L >= row_capacity(p))
         return kBadLength;
+    if (kept_prefix(p, b) < 0)
+        return kBadPrefix;
     if (!p.paged && p.slot_ids) {
         int r = __ldg(p.slot_ids + b);
         if (r < 0 || r >= p.R)
@@ -384,9 +461,19 @@ struct MergeBuf {
 // four at a time. A whole unit writes its normalised output. A cut unit
 // writes its partial state, then takes an arrival ticket; the last CTA of the
 // unit to arrive merges every partial (log-sum-exp rule), writes the output,
-// zeroes the partials it merged and resets the unit's counter.
+// zeroes the partials it merged and resets the unit's counter. A sink logit,
+// when given, joins the final normalisation only (whole units here, cut units
+// in the merge): it raises the maximum if larger and adds 2^(sink - M) to the
+// denominator.
+// Sink logit of query head h in base-2 units (the scores' units).
+__device__ __forceinline__ float sink_log2(const DecodeParams &p, int h)
+{
+    return __ldg(p.sink + h) * 1.4426950408889634f;
+}
+
 template <int NW, int GP, int DD, int DP, class Sync>
-__device__ inline void finish_segment(const DecodeParams &p, const TileCursor &cur, int seg_first_t,
+__device__ inline void finish_segment(const DecodeParams &p, const TileCursor &cur, const TileWalk &walk,
+                                      int seg_first_t,
                                       bool bad, const float (&sm_m)[NW][GP], const float (&sm_l)[NW][GP],
                                       const float (&sm_o)[NW][GP][DP], int *sm_flag, MergeBuf &mb,
                                       int tid, int nthr, Sync sync)
@@ -404,7 +491,9 @@ __device__ inline void finish_segment(const DecodeParams &p, const TileCursor &c
 #pragma unroll
         for (int w = 0; w < NW; ++w)
             M = fmaxf(M, sm_m[w][tid]);
-        float den = 0.f;
+        const float sk = (whole && p.sink) ? sink_log2(p, kvh * G + tid) : -INFINITY;
+        M = fmaxf(M, sk);
+        float den = (sk == -INFINITY) ? 0.f : fast_ex2(sk - M);
 #pragma unroll
         for (int w = 0; w < NW; ++w) {
             const float a = (sm_m[w][tid] == -INFINITY) ? 0.f : fast_ex2(sm_m[w][tid] - M);
@@ -471,8 +560,8 @@ __device__ inline void finish_segment(const DecodeParams &p, const TileCursor &c
     // every other CTA of the unit.
     sync();
     const long long first_tile = cur.g - cur.t;
-    const int first = cta_of_tile(first_tile, cur.N, cur.C);
-    const int last = cta_of_tile(first_tile + cur.nr - 1, cur.N, cur.C);
+    const int first = cta_of_tile(first_tile, walk.N, walk.C);
+    const int last = cta_of_tile(first_tile + cur.nr - 1, walk.N, walk.C);
     if (tid == 0) {
         int old;
         asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(p.ws_cnt + u) : "memory");
@@ -494,7 +583,9 @@ __device__ inline void finish_segment(const DecodeParams &p, const TileCursor &c
                 float M = -INFINITY;
                 for (int i = 0; i < K; ++i)
                     M = fmaxf(M, mb.w[i * G + tid]);
-                float den = 0.f;
+                const float sk = p.sink ? sink_log2(p, kvh * G + tid) : -INFINITY;
+                M = fmaxf(M, sk);
+                float den = (sk == -INFINITY) ? 0.f : fast_ex2(sk - M);
                 for (int i = 0; i < K; ++i) {
                     const float a = fast_ex2(mb.w[i * G + tid] - M);
                     mb.w[i * G + tid] = a;
@@ -536,7 +627,9 @@ __device__ inline void finish_segment(const DecodeParams &p, const TileCursor &c
                 float M = -INFINITY;
                 for (int i = 0; i < K; ++i)
                     M = fmaxf(M, __ldcg(p.ws_ml + ((P0 + i) * G + g) * 2));
-                float num = 0.f, den = 0.f;
+                const float sk = p.sink ? sink_log2(p, kvh * G + g) : -INFINITY;
+                M = fmaxf(M, sk);
+                float num = 0.f, den = (sk == -INFINITY) ? 0.f : fast_ex2(sk - M);
                 for (int i = 0; i < K; ++i) {
                     const long long Q = P0 + i;
                     const float a = fast_ex2(__ldcg(p.ws_ml + (Q * G + g) * 2) - M);

@@ -131,6 +131,7 @@ __global__ void __launch_bounds__(kThreads) simt_decode_kernel(const DecodeParam
     constexpr int VEC = S::VEC, LPS = S::LPS, SPW = S::SPW, STREAMS = S::STREAMS;
 
     __shared__ long long sched[kThreads / 32 + 8];
+    __shared__ TileWalk walk;
     __shared__ int sm_flag;
     __shared__ MergeBuf sm_merge;
     __shared__ float sm_m[kWarps][GP], sm_l[kWarps][GP];
@@ -144,7 +145,7 @@ __global__ void __launch_bounds__(kThreads) simt_decode_kernel(const DecodeParam
 
     // programmatic dependent of the previous kernel: read no input before it is done
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const TileWalk walk = schedule_walk(p, sched);
+    schedule_walk(p, sched, &walk);
     TileCursor cur;
     bool in_b = false;
     bool more = walk_first(p, cur, walk, in_b);
@@ -186,7 +187,7 @@ __global__ void __launch_bounds__(kThreads) simt_decode_kernel(const DecodeParam
         }
 
         if (row_good) {
-            const int s0 = cur.t * p.tile;
+            const int s0 = tile_slot0(cur, p.tile);
             const int s1 = min(s0 + p.tile, L + 1);
             const long long new_off = ((long long)b * p.Hkv + kvh) * D + li * VEC;
             // warp-uniform trip count: every lane takes part in the shuffles
@@ -197,7 +198,7 @@ __global__ void __launch_bounds__(kThreads) simt_decode_kernel(const DecodeParam
                 for (int e = 0; e < VEC; ++e)
                     kv[e] = vv[e] = 0.f;
                 bool use = false;
-                if (j < L || (p.attend && j == L)) {
+                if ((j < L || (p.attend && j == L)) && attended(L, cur.lo, cur.P, j)) {
                     long long off = slot_offset(p, b, kvh, j);
                     if (off < 0) {
                         bad_local = 1;
@@ -282,7 +283,7 @@ __global__ void __launch_bounds__(kThreads) simt_decode_kernel(const DecodeParam
             const bool bad = !row_good || seg_bad;
             if (bad && row_good && tid == 0)
                 report(p, kBadBlock);
-            finish_segment<kWarps, GP, D, D>(p, cur, seg_first_t, bad, sm_m, sm_l, sm_o, &sm_flag, sm_merge, tid,
+            finish_segment<kWarps, GP, D, D>(p, cur, walk, seg_first_t, bad, sm_m, sm_l, sm_o, &sm_flag, sm_merge, tid,
                                           kThreads, [] { __syncthreads(); });
             seg_start = true;
         }

@@ -29,8 +29,11 @@
 //  * online softmax in float32 with base-2 scores (scale log2(e)/sqrt(D)
 //    folded in), a lazy rescale (the running max is only raised when a score
 //    exceeds it by more than 8, i.e. p <= 256), masking by selection so stale
-//    slots never enter the arithmetic, and V rows beyond the length zeroed in
-//    shared memory before the product (0 * NaN would not be 0).
+//    slots (and slots outside a sliding window and kept prefix) never enter
+//    the arithmetic, and the V rows of such slots zeroed in shared memory
+//    before the product (0 * NaN would not be 0). A window skips whole tiles
+//    (the schedule lists only tiles holding attended slots) and, for paged
+//    caches, whole blocks.
 //  * the new token (decode step only; the read-only attend reads slot L from
 //    the cache like any other): in the tile that holds slot L the owning warp writes
 //    k_new / v_new into the ring slot of row L (the TMA copy of the stale
@@ -189,6 +192,7 @@ struct Shared {
     int abort_flag;
     int last_flag;
     long long sched[kThreads / 32 + 8];
+    TileWalk walk;
     float m[kConsumerWarps][kGMax];
     float l[kConsumerWarps][kGMax];
     alignas(16) float o[kConsumerWarps][kGMax][kD + 8];   // rows padded: conflict-free 8-byte stores
@@ -229,7 +233,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // stream: everything above overlaps its tail; no input is read before it
     // has completed and its memory is visible.
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const TileWalk walk = schedule_walk(p, sh.sched);   // contains __syncthreads
+    schedule_walk(p, sh.sched, &sh.walk);   // contains __syncthreads
+    const TileWalk &walk = sh.walk;
 
     const int G = p.G;
     const __nv_bfloat16 *knew = static_cast<const __nv_bfloat16 *>(p.k_new);
@@ -260,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             Plan r{-1, 0, false, row_ok(p, c.b, c.L)};
             if (!r.good)
                 return r;
-            const int slot0 = c.t * kTile;
+            const int slot0 = tile_slot0(c, kTile);
             if (!p.paged) {
                 if (lane == 0) {
                     const int row = p.slot_ids ? __ldg(p.slot_ids + c.b) : c.b;
@@ -269,7 +274,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 }
             } else if (lane < nblk) {
                 const int s = slot0 + lane * box_rows;  // first slot this lane copies
-                if (s <= c.L) {
+                // a block is copied when it holds an attended slot
+                if (s <= c.L && (s + box_rows - 1 >= c.lo || s < c.P)) {
                     const int e = __ldg(p.block_table + (long long)c.b * p.max_blocks + s / bs);
                     if (e >= 0 && e < p.num_blocks) {
                         r.z = e * p.Hkv + c.kvh;
@@ -393,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         aborted = aborted || !have;
         seg_bad |= aborted ? 1 : 0;
 
-        const int slot0 = cur.t * kTile;
+        const int slot0 = tile_slot0(cur, kTile);
         const uint32_t kbase = ring_u32 + stage * kStageBytes;
         const uint32_t vbase = kbase + 2 * kHalfBytes;
         uint8_t *kring = ring + stage * kStageBytes;
@@ -426,10 +432,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
         if (have && row_good && !tile_bad) {
             const bool last_tile = (cur.t == cur.nr - 1);
-            if (last_tile) {
-                // rows of this warp beyond L: zero V; row L: the new token
-                const int lr = L - slot0;            // 0..63
-                if (!p.attend && lr >= row0 && lr < row0 + 16) {
+            // tiles that hold slots outside the softmax: the last one (beyond
+            // L) and, with a window, those below its start
+            const bool partial = last_tile || slot0 < cur.lo;
+            if (partial) {
+                // row L of the last tile: the new token; rows not attended: zero V
+                const int lr = L - slot0;            // 0..63 in the last tile
+                if (last_tile && !p.attend && lr >= row0 && lr < row0 + 16) {
                     const long long nidx = ((long long)b * p.Hkv + kvh) * kD;
                     const int c = lane & 15;          // 16-byte chunk of the row
                     const int half = c >> 3, c8 = c & 7;
@@ -445,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     }
                 }
                 for (int r = row0 + (lane >> 4); r < row0 + 16; r += 2) {
-                    if (r > lr) {
+                    if (!attended(L, cur.lo, cur.P, slot0 + r)) {
                         const int c = lane & 15;
                         *reinterpret_cast<uint4 *>(vring + (c >> 3) * kHalfBytes + swz(r, c & 7)) =
                             make_uint4(0u, 0u, 0u, 0u);
@@ -492,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     float sc = s_acc[nt][e];
                     if constexpr (QF32)
                         sc += s_acc[nt][e + 2];   // row g0 + 8: the query remainder
-                    x[nt][e] = (j <= L) ? sc * p.scale_log2 : -INFINITY;
+                    x[nt][e] = attended(L, cur.lo, cur.P, j) ? sc * p.scale_log2 : -INFINITY;
                     mx = fmaxf(mx, x[nt][e]);
                 }
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
@@ -541,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     mma_bf16(acc_o[2 * np + 1], pa[0], pa[1], pa[2], pa[3], vb[2], vb[3]);
                 }
             }
-            if (last_tile)
+            if (partial)
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         }
         __syncwarp();
@@ -573,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             const bool bad = !row_good || seg_bad;
             if (bad && row_good && tid == 0)
                 report(p, aborted ? kTimeout : kBadBlock);
-            finish_segment<kConsumerWarps, kGMax, kD, kD + 8>(p, cur, seg_first_t, bad, sh.m, sh.l, sh.o,
+            finish_segment<kConsumerWarps, kGMax, kD, kD + 8>(p, cur, walk, seg_first_t, bad, sh.m, sh.l, sh.o,
                                                       &sh.last_flag, sh.merge, tid, kConsumerWarps * 32,
                                                       [] { consumer_sync(); });
             seg_start = true;

@@ -81,7 +81,8 @@ enum {
     GQA_STATUS_BAD_SLOT_ID = 2,     /* slot_ids[b] outside [0, R)                        */
     GQA_STATUS_BAD_BLOCK = 4,       /* block-table entry outside [0, num_blocks) or -1
                                        where a slot 0..lengths[b] lives                   */
-    GQA_STATUS_TIMEOUT = 8          /* a bounded on-chip wait gave up (never expected)    */
+    GQA_STATUS_TIMEOUT = 8,         /* a bounded on-chip wait gave up (never expected)    */
+    GQA_STATUS_BAD_PREFIX = 16      /* kept_prefix_rows[b] < 0                            */
 };
 
 /* Kernel choice for the *_ex entry points. */
@@ -103,7 +104,23 @@ typedef struct gqa_options {
                        (row, cache head) when sharing the tiles among CTAs, which gives
                        CTAs that finish more sequences fewer tiles (no effect on
                        results beyond float32 rounding)                                 */
-    int reserved[5];
+    /* Softmax modifiers ("groupQueryAttention": slidingWindow, kept_prefix,
+     * head_sink). With the query at position L (the appended slot of the decode
+     * step, the last valid slot of the attend), slot j <= L is attended when
+     * window == 0, or j > L - window (the window positions up to and including
+     * the query's own), or j < P (the row's kept prefix, used only with a
+     * window). Only tiles (and paged blocks) holding attended slots are read;
+     * the other slots' contents do not matter, and paged entries that hold no
+     * attended slot (nor the appended one) may be -1. The sink of query head h
+     * is one more logit in the softmax denominator, in the units of the scaled
+     * scores: w_j = e^{s_j} / (e^{sink_h} + sum_{i attended} e^{s_i}).        */
+    int window;       /* >= 0 (0: no window); < 0 is GQA_ERR_INVALID_ARGUMENT          */
+    int kept_prefix;  /* P >= 0 for every row, used when kept_prefix_rows is NULL       */
+    int reserved[3];
+    const float *head_sink;          /* (device) (Hq,) float32 logits, or NULL          */
+    const int32_t *kept_prefix_rows; /* (device) (B,) int32 P per batch row, or NULL;
+                                        a negative entry makes that row bad
+                                        (NaN, GQA_STATUS_BAD_PREFIX)                    */
 } gqa_options;
 
 /* Human-readable name of a status code (static storage). */
