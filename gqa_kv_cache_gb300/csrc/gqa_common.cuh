@@ -132,7 +132,10 @@ __device__ __forceinline__ bool geom_ok(const DecodeParams &p, int L, int P)
     return L >= 0 && (long long)L < row_capacity(p) && P >= 0;
 }
 
-__device__ __forceinline__ RowGeom row_geom(const DecodeParams &p, int b)
+// Not inlined: it is reached from half a dozen places (schedule scan, cursor
+// set-up, row changes) and inlining its window arithmetic into each of them
+// measurably slowed the streaming loop (instruction fetch).
+static __device__ __noinline__ RowGeom row_geom(const DecodeParams &p, int b)
 {
     RowGeom r;
     r.L = last_slot(p, b);

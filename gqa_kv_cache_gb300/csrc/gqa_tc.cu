@@ -204,7 +204,9 @@ __device__ __forceinline__ void consumer_sync()
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
 }
 
-template <bool QF32>
+// WIN: a sliding window is in force. Without one the window fields of the
+// cursor are never read, so they take no registers and no code.
+template <bool QF32, bool WIN>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     tc_decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap mk,
                      const __grid_constant__ CUtensorMap mv)
@@ -265,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             Plan r{-1, 0, false, row_ok(p, c.b, c.L)};
             if (!r.good)
                 return r;
-            const int slot0 = tile_slot0(c, kTile);
+            const int slot0 = WIN ? tile_slot0(c, kTile) : c.t * kTile;
             if (!p.paged) {
                 if (lane == 0) {
                     const int row = p.slot_ids ? __ldg(p.slot_ids + c.b) : c.b;
@@ -275,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             } else if (lane < nblk) {
                 const int s = slot0 + lane * box_rows;  // first slot this lane copies
                 // a block is copied when it holds an attended slot
-                if (s <= c.L && (s + box_rows - 1 >= c.lo || s < c.P)) {
+                if (s <= c.L && (!WIN || s + box_rows - 1 >= c.lo || s < c.P)) {
                     const int e = __ldg(p.block_table + (long long)c.b * p.max_blocks + s / bs);
                     if (e >= 0 && e < p.num_blocks) {
                         r.z = e * p.Hkv + c.kvh;
@@ -399,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         aborted = aborted || !have;
         seg_bad |= aborted ? 1 : 0;
 
-        const int slot0 = tile_slot0(cur, kTile);
+        const int slot0 = WIN ? tile_slot0(cur, kTile) : cur.t * kTile;
         const uint32_t kbase = ring_u32 + stage * kStageBytes;
         const uint32_t vbase = kbase + 2 * kHalfBytes;
         uint8_t *kring = ring + stage * kStageBytes;
@@ -434,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             const bool last_tile = (cur.t == cur.nr - 1);
             // tiles that hold slots outside the softmax: the last one (beyond
             // L) and, with a window, those below its start
-            const bool partial = last_tile || slot0 < cur.lo;
+            const bool partial = last_tile || (WIN && slot0 < cur.lo);
             if (partial) {
                 // row L of the last tile: the new token; rows not attended: zero V
                 const int lr = L - slot0;            // 0..63 in the last tile
@@ -454,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     }
                 }
                 for (int r = row0 + (lane >> 4); r < row0 + 16; r += 2) {
-                    if (!attended(L, cur.lo, cur.P, slot0 + r)) {
+                    if (WIN ? !attended(L, cur.lo, cur.P, slot0 + r) : slot0 + r > L) {
                         const int c = lane & 15;
                         *reinterpret_cast<uint4 *>(vring + (c >> 3) * kHalfBytes + swz(r, c & 7)) =
                             make_uint4(0u, 0u, 0u, 0u);
@@ -490,7 +492,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     for (int e = 0; e < 4; ++e)
                         s_acc[nt][e] += s_odd[nt][e];
             }
-            // ---- masked online softmax (base 2), rows g0
+            // ---- masked online softmax (base 2), rows g0; only the partial
+            // tiles (the last one, those below a window's start) test slots
             float x[2][2];
             float mx = -INFINITY;
 #pragma unroll
@@ -501,7 +504,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     float sc = s_acc[nt][e];
                     if constexpr (QF32)
                         sc += s_acc[nt][e + 2];   // row g0 + 8: the query remainder
-                    x[nt][e] = attended(L, cur.lo, cur.P, j) ? sc * p.scale_log2 : -INFINITY;
+                    const bool on = WIN ? attended(L, cur.lo, cur.P, j) : j <= L;
+                    x[nt][e] = (!partial || on) ? sc * p.scale_log2 : -INFINITY;
                     mx = fmaxf(mx, x[nt][e]);
                 }
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
@@ -613,14 +617,14 @@ size_t tc_smem_bytes(bool q_bf16)
 }
 
 namespace {
-template <bool QF32>
+template <bool QF32, bool WIN>
 cudaError_t launch_q(const DecodeParams &p, const TcMaps &maps, cudaStream_t st)
 {
     constexpr int kDynSmem = Ring<QF32>::kDynSmem;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(tc_decode_kernel<QF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kDynSmem);
+        cudaError_t e = cudaFuncSetAttribute(tc_decode_kernel<QF32, WIN>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem);
         if (e != cudaSuccess)
             return e;
         attr_set = true;
@@ -635,13 +639,16 @@ cudaError_t launch_q(const DecodeParams &p, const TcMaps &maps, cudaStream_t st)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tc_decode_kernel<QF32>, p, maps.k, maps.v);
+    return cudaLaunchKernelEx(&cfg, tc_decode_kernel<QF32, WIN>, p, maps.k, maps.v);
 }
 }  // namespace
 
 cudaError_t tc_launch(const DecodeParams &p, const TcMaps &maps, cudaStream_t st)
 {
-    return p.q_bf16 ? launch_q<false>(p, maps, st) : launch_q<true>(p, maps, st);
+    const bool win = p.window > 0;
+    if (p.q_bf16)
+        return win ? launch_q<false, true>(p, maps, st) : launch_q<false, false>(p, maps, st);
+    return win ? launch_q<true, true>(p, maps, st) : launch_q<true, false>(p, maps, st);
 }
 
 }  // namespace gqa
