@@ -96,6 +96,16 @@ def _load():
             lib.orc_validate_attend_dense.restype = I
             lib.orc_validate_attend_paged.argtypes = [P, P, I, I, I, I]
             lib.orc_validate_attend_paged.restype = I
+            lib.orc_decode_multi_dense.argtypes = [I, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I,
+                                                   I, P, P, I, P]
+            lib.orc_decode_multi_dense.restype = I
+            lib.orc_decode_multi_paged.argtypes = [I, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I,
+                                                   I, P, P, I, P]
+            lib.orc_decode_multi_paged.restype = I
+            lib.orc_validate_multi_dense.argtypes = [P, P, P, I, I, I, I]
+            lib.orc_validate_multi_dense.restype = I
+            lib.orc_validate_multi_paged.argtypes = [P, P, P, I, I, I, I, I]
+            lib.orc_validate_multi_paged.restype = I
             lib.orc_default_threads.argtypes = []
             lib.orc_default_threads.restype = I
             _lib = lib
@@ -258,6 +268,78 @@ def attend_paged(q, k_blocks, v_blocks, block_table, lengths, *, rows=None,
                                   _ptr(rows_a), 0 if rows_a is None else len(rows_a), _ptr(out),
                                   mods and mods[0], nthr, ctypes.addressof(used))
     return OracleResult(st, out, used.value)
+
+
+def decode_multi_dense(q, k_new, v_new, k_cache, v_cache, lengths, cu_q, slot_ids=None, *,
+                       append=True, threads=None, sink=None, window=0, kept_prefix=0) -> OracleResult:
+    """Multi-token step on a dense (R, Hkv, Smax, D) cache: the q_len[b] =
+    cu_q[b+1] - cu_q[b] new tokens of row b (rows cu_q[b].. of the packed
+    q (T, Hq, D), k_new / v_new (T, Hkv, D)) are appended in place at slots
+    lengths[b] + i, and token i attends slots 0 .. lengths[b] + i. Returns
+    ``out`` (T, Hq, D) float64."""
+    dt = _dtype_code(q)
+    for a in (k_new, v_new, k_cache, v_cache):
+        if a.dtype != q.dtype:
+            raise TypeError("q, k_new, v_new and the caches share one dtype")
+        if not a.flags.c_contiguous:
+            raise ValueError("arrays must be C-contiguous (the caches are written in place)")
+    T, Hq, D = q.shape
+    R, Hkv, Smax, D2 = k_cache.shape
+    assert D2 == D and v_cache.shape == k_cache.shape and k_new.shape == (T, Hkv, D)
+    q, k_new, v_new = _c(q), _c(k_new), _c(v_new)
+    lengths, cu_q, slot_ids = _c(lengths, np.int32), _c(cu_q, np.int32), _c(slot_ids, np.int32)
+    B = len(lengths)
+    out = np.full((T, Hq, D), np.nan, dtype=np.float64)
+    used = ctypes.c_int(0)
+    nthr = default_threads() if threads is None else int(threads)
+    keep = []
+    mods = _mods(sink, window, kept_prefix, keep)
+    st = _load().orc_decode_multi_dense(dt, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
+                                        _ptr(v_cache), _ptr(lengths), _ptr(cu_q), _ptr(slot_ids), B, T,
+                                        Hq, Hkv, D, R, Smax, int(bool(append)), _ptr(out),
+                                        mods and mods[0], nthr, ctypes.addressof(used))
+    return OracleResult(st, out, used.value)
+
+
+def decode_multi_paged(q, k_new, v_new, k_blocks, v_blocks, block_table, lengths, cu_q, *,
+                       append=True, threads=None, sink=None, window=0, kept_prefix=0) -> OracleResult:
+    """Multi-token step on a paged cache; same contract as
+    :func:`decode_multi_dense`."""
+    dt = _dtype_code(q)
+    for a in (k_new, v_new, k_blocks, v_blocks):
+        if a.dtype != q.dtype:
+            raise TypeError("q, k_new, v_new and the blocks share one dtype")
+        if not a.flags.c_contiguous:
+            raise ValueError("arrays must be C-contiguous (the blocks are written in place)")
+    T, Hq, D = q.shape
+    NB, Hkv, BS, D2 = k_blocks.shape
+    assert D2 == D and v_blocks.shape == k_blocks.shape and k_new.shape == (T, Hkv, D)
+    MB = block_table.shape[1]
+    q, k_new, v_new = _c(q), _c(k_new), _c(v_new)
+    block_table, lengths, cu_q = _c(block_table, np.int32), _c(lengths, np.int32), _c(cu_q, np.int32)
+    B = len(lengths)
+    out = np.full((T, Hq, D), np.nan, dtype=np.float64)
+    used = ctypes.c_int(0)
+    nthr = default_threads() if threads is None else int(threads)
+    keep = []
+    mods = _mods(sink, window, kept_prefix, keep)
+    st = _load().orc_decode_multi_paged(dt, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_blocks),
+                                        _ptr(v_blocks), _ptr(block_table), _ptr(lengths), _ptr(cu_q), B,
+                                        T, Hq, Hkv, D, NB, BS, MB, int(bool(append)), _ptr(out),
+                                        mods and mods[0], nthr, ctypes.addressof(used))
+    return OracleResult(st, out, used.value)
+
+
+def validate_multi_dense(lengths, cu_q, slot_ids, T, R, Smax) -> int:
+    lengths, cu_q, slot_ids = _c(lengths, np.int32), _c(cu_q, np.int32), _c(slot_ids, np.int32)
+    return _load().orc_validate_multi_dense(_ptr(lengths), _ptr(cu_q), _ptr(slot_ids), len(lengths), T,
+                                            R, Smax)
+
+
+def validate_multi_paged(lengths, cu_q, block_table, T, num_blocks, block_size) -> int:
+    lengths, cu_q, bt = _c(lengths, np.int32), _c(cu_q, np.int32), _c(block_table, np.int32)
+    return _load().orc_validate_multi_paged(_ptr(lengths), _ptr(cu_q), _ptr(bt), len(lengths), T,
+                                            num_blocks, block_size, bt.shape[1])
 
 
 def validate_attend_dense(lengths, slot_ids, R, Smax) -> int:

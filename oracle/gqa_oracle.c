@@ -21,6 +21,12 @@
  * token and no write: n = lengths[b] is the number of valid cached slots and
  * slots 0 .. n-1 are attended; the query may be float32 over a bfloat16 cache.
  *
+ * The multi-token step (orc_decode_multi_*) appends the q_len[b] =
+ * cu_q[b+1] - cu_q[b] new tokens of row b (packed rows cu_q[b] .. cu_q[b+1]-1
+ * of q, k_new, v_new and out) at slots lengths[b] + i, and query token i
+ * attends slots 0 .. lengths[b] + i (the causal bound); q_len = 1 everywhere
+ * is the decode step.
+ *
  * Optional softmax modifiers (orc_mods, any entry point), with the query at
  * position L (the new token, or the last valid slot of the attend):
  *   window W > 0   slot j is attended only if L - W < j (the W positions up
@@ -53,7 +59,9 @@
  *    logit folded into the softmax denominator; kept_prefix keeps each
  *    sequence's first P keys attended beside the sliding window, a key is
  *    attended when it is inside the first P keys or inside the window (the
- *    window alone without P), and a negative P is refused.
+ *    window alone without P), and a negative P is refused. The packed
+ *    (hidden-folded, [sum S, heads * head_dim]) q/k/v and the write offset of
+ *    each row, cu_seqlens_k[b] - q_len[b], give the multi-token form.
  *
  * Readings where the pages are silent (each listed in the design notes):
  *  - lengths[b] is the append slot (the number of tokens already cached), and
@@ -65,6 +73,10 @@
  *    attends the query's own key only); the sink is a logit in the same units
  *    as s_j (already scaled, not multiplied by 1/sqrt(D)); a kept prefix has
  *    no effect without a window; window < 0 is refused like a negative P.
+ *  - multi-token: lengths[b] is the write offset (tokens already cached), so
+ *    cu_seqlens_k[b] = lengths[b] + q_len[b]; cu_q[0] = 0, cu_q nondecreasing,
+ *    cu_q[B] = T; 0 <= lengths[b] and lengths[b] + q_len[b] <= capacity; a
+ *    row with q_len = 0 has nothing to do.
  *  - read-only attend: 1 <= lengths[b] <= Smax (dense) or
  *    <= max_blocks * block_size (paged, entries covering slots
  *    0 .. lengths[b]-1 not -1); zero valid slots has no softmax and is
@@ -75,6 +87,7 @@
  *    to double is exact.
  */
 #define _GNU_SOURCE
+#include <limits.h>
 #include <math.h>
 #include <sched.h>
 #include <pthread.h>
@@ -233,8 +246,9 @@ typedef struct {
     layout lay;
     int B, Hq, Hkv, D;
     int do_append;
-    double *out;       /* (B, Hq, D) */
+    double *out;       /* (B, Hq, D); multi-token: (T, Hq, D) */
     const orc_mods *mods;  /* NULL: plain softmax */
+    const int32_t *cu_q;   /* multi-token: (B + 1) token offsets, else NULL */
     const int32_t *rows; /* batch rows to compute */
     int nrows;
     /* work distribution over (row, kvh) pairs */
@@ -269,32 +283,30 @@ static int mods_ok(const orc_mods *M, int B)
     return 1;
 }
 
-/* One (batch row, cache head) pair: append (decode step), then the G query
- * heads over the attended slots 0 .. L. */
-static void one_pair(job *J, int b, int kvh)
+/* Element index of the new key / value of token `tok`, cache head kvh. */
+static size_t new_index(const job *J, int tok, int kvh)
+{
+    return ((size_t)tok * J->Hkv + kvh) * J->D;
+}
+
+/* The G query heads of token `tok` (its rows of q and out) over the attended
+ * slots 0 .. L of (batch row b, cache head kvh). Slots at or beyond first_new
+ * are read from the new keys / values of tokens new_tok0, new_tok0 + 1, ...
+ * (the tokens a step without append did not write into the cache). */
+static void attend_heads(job *J, int b, int kvh, int L, int tok, int first_new, int new_tok0)
 {
     const int D = J->D, G = J->Hq / J->Hkv;
-    const int L = J->attend ? J->lengths[b] - 1 : J->lengths[b];   /* last attended slot */
-    const int from_new = !J->attend && !J->do_append;  /* slot L read from k_new / v_new */
-    const size_t new_i = ((size_t)b * J->Hkv + kvh) * D;
-
-    if (!J->attend && J->do_append) {
-        size_t dst = slot_index(&J->lay, b, kvh, L);
-        copy_vec(J->k_cache, dst, J->k_new, new_i, D, J->kv_dtype);
-        copy_vec(J->v_cache, dst, J->v_new, new_i, D, J->kv_dtype);
-    }
-
     double *s = (double *)malloc(sizeof(double) * (size_t)(L + 1));
     for (int g = 0; g < G; ++g) {
         const int h = kvh * G + g;           /* floor(h / G) == kvh */
-        const size_t q_i = ((size_t)b * J->Hq + h) * D;
+        const size_t q_i = ((size_t)tok * J->Hq + h) * D;
 
-        /* scores over slots 0 .. L; in the decode step slot L is the new token */
+        /* scores over slots 0 .. L */
         for (int j = 0; j <= L; ++j) {
             double dot = 0.0;
             for (int d = 0; d < D; ++d) {
-                double kd = (j == L && from_new)
-                                ? elem(J->k_new, new_i + d, J->kv_dtype)
+                double kd = (j >= first_new)
+                                ? elem(J->k_new, new_index(J, new_tok0 + j - first_new, kvh) + d, J->kv_dtype)
                                 : elem(J->k_cache, slot_index(&J->lay, b, kvh, j) + d, J->kv_dtype);
                 dot += elem(J->q, q_i + d, J->q_dtype) * kd;
             }
@@ -324,14 +336,44 @@ static void one_pair(job *J, int b, int kvh)
                 continue;
             double w = exp(s[j] - m) / Z;
             for (int d = 0; d < D; ++d) {
-                double vd = (j == L && from_new)
-                                ? elem(J->v_new, new_i + d, J->kv_dtype)
+                double vd = (j >= first_new)
+                                ? elem(J->v_new, new_index(J, new_tok0 + j - first_new, kvh) + d, J->kv_dtype)
                                 : elem(J->v_cache, slot_index(&J->lay, b, kvh, j) + d, J->kv_dtype);
                 o[d] += w * vd;
             }
         }
     }
     free(s);
+}
+
+/* One (batch row, cache head) pair: append (decode step), then the G query
+ * heads over the attended slots 0 .. L. */
+static void one_pair(job *J, int b, int kvh)
+{
+    const int D = J->D;
+    if (J->cu_q) {
+        /* multi-token: tokens t0 .. t0 + nq - 1 take slots Lb .. Lb + nq - 1,
+         * and token i attends slots 0 .. Lb + i */
+        const int t0 = J->cu_q[b], nq = J->cu_q[b + 1] - t0, Lb = J->lengths[b];
+        if (J->do_append)
+            for (int i = 0; i < nq; ++i) {
+                size_t dst = slot_index(&J->lay, b, kvh, Lb + i);
+                copy_vec(J->k_cache, dst, J->k_new, new_index(J, t0 + i, kvh), D, J->kv_dtype);
+                copy_vec(J->v_cache, dst, J->v_new, new_index(J, t0 + i, kvh), D, J->kv_dtype);
+            }
+        for (int i = 0; i < nq; ++i)
+            attend_heads(J, b, kvh, Lb + i, t0 + i, J->do_append ? INT_MAX : Lb, t0);
+        return;
+    }
+    const int L = J->attend ? J->lengths[b] - 1 : J->lengths[b];   /* last attended slot */
+    const int from_new = !J->attend && !J->do_append;  /* slot L read from k_new / v_new */
+
+    if (!J->attend && J->do_append) {
+        size_t dst = slot_index(&J->lay, b, kvh, L);
+        copy_vec(J->k_cache, dst, J->k_new, new_index(J, b, kvh), D, J->kv_dtype);
+        copy_vec(J->v_cache, dst, J->v_new, new_index(J, b, kvh), D, J->kv_dtype);
+    }
+    attend_heads(J, b, kvh, L, b, from_new ? L : INT_MAX, b);
 }
 
 static void *worker(void *arg)
@@ -510,6 +552,114 @@ int orc_attend_paged(int q_dtype, int kv_dtype, const void *q, const void *k_blo
     J.out = out;
     J.mods = mods;
     J.rows = (const int32_t *)rows; J.nrows = nrows;
+    int n = run(&J, nthreads);
+    if (threads_used)
+        *threads_used = n;
+    return ORC_OK;
+}
+
+/* Multi-token checks: cu_q[0] = 0, nondecreasing, cu_q[B] = T; every row
+ * 0 <= lengths[b] and lengths[b] + q_len[b] <= capacity. */
+static int validate_cu_q(const int32_t *cu_q, int B, int T)
+{
+    if (B < 0 || T < 0 || cu_q[0] != 0 || cu_q[B] != T)
+        return ORC_INVALID_ARGUMENT;
+    for (int b = 0; b < B; ++b)
+        if (cu_q[b + 1] < cu_q[b])
+            return ORC_INVALID_ARGUMENT;
+    return ORC_OK;
+}
+
+int orc_validate_multi_dense(const int32_t *lengths, const int32_t *cu_q, const int32_t *slot_ids,
+                             int B, int T, int R, int Smax)
+{
+    if (validate_cu_q(cu_q, B, T) != ORC_OK)
+        return ORC_INVALID_ARGUMENT;
+    for (int b = 0; b < B; ++b)
+        if (lengths[b] < 0 || (long long)lengths[b] + (cu_q[b + 1] - cu_q[b]) > Smax)
+            return ORC_INVALID_ARGUMENT;
+    /* the slot_ids / row rules of the decode step, with the lengths checked above */
+    int32_t *zero = (int32_t *)calloc((size_t)(B > 0 ? B : 1), sizeof(int32_t));
+    int st = orc_validate_dense(zero, slot_ids, B, R, Smax);
+    free(zero);
+    return st;
+}
+
+int orc_validate_multi_paged(const int32_t *lengths, const int32_t *cu_q, const int32_t *block_table,
+                             int B, int T, int num_blocks, int block_size, int max_blocks)
+{
+    if (validate_cu_q(cu_q, B, T) != ORC_OK)
+        return ORC_INVALID_ARGUMENT;
+    /* the table rules of the decode step, with the last touched slot
+     * lengths[b] + q_len[b] - 1 (rows without tokens touch none) */
+    int32_t *last = (int32_t *)malloc(sizeof(int32_t) * (size_t)(B > 0 ? B : 1));
+    for (int b = 0; b < B; ++b) {
+        const long long l = (long long)lengths[b] + (cu_q[b + 1] - cu_q[b]) - 1;
+        last[b] = lengths[b] < 0 ? -1 : (l < 0 ? 0 : (l > INT_MAX ? INT_MAX : (int32_t)l));
+    }
+    int st = orc_validate_paged(last, block_table, B, num_blocks, block_size, max_blocks);
+    free(last);
+    return st;
+}
+
+/* Multi-token step on a dense or slot_ids cache. q (T, Hq, D), k_new / v_new
+ * (T, Hkv, D), out (T, Hq, D); cu_q (B + 1). do_append = 0 computes the same
+ * outputs without writing the cache. */
+int orc_decode_multi_dense(int dtype, const void *q, const void *k_new, const void *v_new,
+                           void *k_cache, void *v_cache, const int32_t *lengths, const int32_t *cu_q,
+                           const int32_t *slot_ids, int B, int T, int Hq, int Hkv, int D, int R,
+                           int Smax, int do_append, double *out, const orc_mods *mods, int nthreads,
+                           int *threads_used)
+{
+    if (!usable_shape(B, Hq, Hkv, D) || !usable_dtype(dtype) || !mods_ok(mods, B))
+        return ORC_INVALID_ARGUMENT;
+    if (orc_validate_multi_dense(lengths, cu_q, slot_ids, B, T, R, Smax) != ORC_OK)
+        return ORC_INVALID_ARGUMENT;
+    job J;
+    memset(&J, 0, sizeof J);
+    J.q_dtype = J.kv_dtype = dtype;
+    J.q = q; J.k_new = k_new; J.v_new = v_new;
+    J.k_cache = k_cache; J.v_cache = v_cache;
+    J.lengths = lengths;
+    J.cu_q = cu_q;
+    J.lay.paged = 0; J.lay.slot_ids = slot_ids;
+    J.lay.Hkv = Hkv; J.lay.D = D; J.lay.Smax = Smax;
+    J.B = B; J.Hq = Hq; J.Hkv = Hkv; J.D = D;
+    J.do_append = do_append;
+    J.out = out;
+    J.mods = mods;
+    int n = run(&J, nthreads);
+    if (threads_used)
+        *threads_used = n;
+    return ORC_OK;
+}
+
+/* Multi-token step on a paged cache; same contract otherwise. */
+int orc_decode_multi_paged(int dtype, const void *q, const void *k_new, const void *v_new,
+                           void *k_blocks, void *v_blocks, const int32_t *block_table,
+                           const int32_t *lengths, const int32_t *cu_q, int B, int T, int Hq, int Hkv,
+                           int D, int num_blocks, int block_size, int max_blocks, int do_append,
+                           double *out, const orc_mods *mods, int nthreads, int *threads_used)
+{
+    if (!usable_shape(B, Hq, Hkv, D) || !usable_dtype(dtype) || !mods_ok(mods, B))
+        return ORC_INVALID_ARGUMENT;
+    if (orc_validate_multi_paged(lengths, cu_q, block_table, B, T, num_blocks, block_size, max_blocks) !=
+        ORC_OK)
+        return ORC_INVALID_ARGUMENT;
+    job J;
+    memset(&J, 0, sizeof J);
+    J.q_dtype = J.kv_dtype = dtype;
+    J.q = q; J.k_new = k_new; J.v_new = v_new;
+    J.k_cache = k_blocks; J.v_cache = v_blocks;
+    J.lengths = lengths;
+    J.cu_q = cu_q;
+    J.lay.paged = 1; J.lay.block_table = block_table;
+    J.lay.Hkv = Hkv; J.lay.D = D;
+    J.lay.block_size = block_size; J.lay.max_blocks = max_blocks;
+    J.B = B; J.Hq = Hq; J.Hkv = Hkv; J.D = D;
+    J.do_append = do_append;
+    J.out = out;
+    J.mods = mods;
     int n = run(&J, nthreads);
     if (threads_used)
         *threads_used = n;

@@ -48,7 +48,14 @@ MUTANTS = {
     "attend_empty_accepted": ("if (last_slot(lengths, b, attend) < 0 ||", "if (last_slot(lengths, b, attend) < -1 ||"),
     "paged_last_block_unchecked": ("for (long long i = 0; i <= last / block_size; ++i)",
                                    "for (long long i = 0; i < last / block_size; ++i)"),
-    "query_head_offset": ("const size_t q_i = ((size_t)b * J->Hq + h) * D;", "const size_t q_i = ((size_t)b * J->Hq + g) * D;"),
+    "multi_not_causal": ("attend_heads(J, b, kvh, Lb + i, t0 + i, J->do_append ? INT_MAX : Lb, t0);",
+                         "attend_heads(J, b, kvh, Lb + nq - 1, t0 + i, J->do_append ? INT_MAX : Lb, t0);"),
+    "multi_append_offset": ("size_t dst = slot_index(&J->lay, b, kvh, Lb + i);",
+                            "size_t dst = slot_index(&J->lay, b, kvh, Lb + i + (i > 0));"),
+    "multi_same_token_appended": ("copy_vec(J->k_cache, dst, J->k_new, new_index(J, t0 + i, kvh), D, J->kv_dtype);",
+                                  "copy_vec(J->k_cache, dst, J->k_new, new_index(J, t0, kvh), D, J->kv_dtype);"),
+    "multi_cu_q_unchecked": ("        if (cu_q[b + 1] < cu_q[b])\n            return ORC_INVALID_ARGUMENT;\n", ""),
+    "query_head_offset": ("const size_t q_i = ((size_t)tok * J->Hq + h) * D;", "const size_t q_i = ((size_t)tok * J->Hq + g) * D;"),
 }
 
 

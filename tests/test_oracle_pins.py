@@ -805,3 +805,157 @@ def test_mods_refused():
         r = oracle.decode_dense(a["q"], a["k_new"], a["v_new"], a["k_cache"].copy(), a["v_cache"].copy(),
                                 a["lengths"], **kw)
         assert r.status == oracle.INVALID_ARGUMENT
+
+
+# ------------------------------------------------ multi-token append (q_len > 1)
+#
+# [P5] groupQueryAttention: q/k/v are packed over the tokens of all sequences
+# ([sum S, heads * head_dim]); each row's write offset is cu_seqlens_k[b] -
+# q_len[b] (our lengths[b]); the new keys and values are appended in place;
+# "under the causal bound" token i sees the keys up to its own position.
+
+def _multi_case(seed, q_lens, Smax=24, dtype="f32", Hq=4, Hkv=2, D=8):
+    rng = np.random.default_rng(seed)
+    B = len(q_lens)
+    cu = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    T = int(cu[-1])
+    lens = np.array([rng.integers(0, Smax - n + 1) for n in q_lens], np.int32)
+    f = lambda *sh: rng.normal(size=sh).astype(np.float32)
+    q, kn, vn = f(T, Hq, D), f(T, Hkv, D), f(T, Hkv, D)
+    kc, vc = f(B, Hkv, Smax, D), f(B, Hkv, Smax, D)
+    if dtype == "bf16":
+        q, kn, vn, kc, vc = (to_np(torch.from_numpy(a).to(torch.bfloat16)) for a in (q, kn, vn, kc, vc))
+    return dict(q=q, k_new=kn, v_new=vn, k_cache=kc, v_cache=vc, lengths=lens, cu_q=cu, T=T)
+
+
+def test_multi_q_len_one_is_the_decode_step():
+    c = _multi_case(50, [1, 1, 1, 1], dtype="bf16")
+    kc1, vc1 = c["k_cache"].copy(), c["v_cache"].copy()
+    r1 = oracle.decode_multi_dense(c["q"], c["k_new"], c["v_new"], kc1, vc1, c["lengths"], c["cu_q"])
+    kc2, vc2 = c["k_cache"].copy(), c["v_cache"].copy()
+    r2 = oracle.decode_dense(c["q"], c["k_new"], c["v_new"], kc2, vc2, c["lengths"])
+    assert r1.status == oracle.OK
+    assert r1.out.tobytes() == r2.out.tobytes()
+    assert kc1.tobytes() == kc2.tobytes() and vc1.tobytes() == vc2.tobytes()
+
+
+@pytest.mark.parametrize("mods", [{}, dict(window=5, kept_prefix=2, sink=np.linspace(-1, 1, 4).astype(np.float32))])
+def test_multi_equals_successive_decode_steps(mods):
+    """Appending n tokens at once with the causal bound is the same as n
+    decode steps, each appending one token and attending up to it (bit for
+    bit: the same terms in the same order)."""
+    q_lens = [3, 1, 5, 2]
+    c = _multi_case(51, q_lens)
+    kcm, vcm = c["k_cache"].copy(), c["v_cache"].copy()
+    rm = oracle.decode_multi_dense(c["q"], c["k_new"], c["v_new"], kcm, vcm, c["lengths"], c["cu_q"], **mods)
+    assert rm.status == oracle.OK
+    kcs, vcs = c["k_cache"].copy(), c["v_cache"].copy()
+    for b, n in enumerate(q_lens):
+        for i in range(n):
+            t = int(c["cu_q"][b]) + i
+            kb, vb = np.ascontiguousarray(kcs[b:b + 1]), np.ascontiguousarray(vcs[b:b + 1])
+            m = dict(mods)
+            r = oracle.decode_dense(c["q"][t:t + 1], c["k_new"][t:t + 1], c["v_new"][t:t + 1], kb, vb,
+                                    np.array([c["lengths"][b] + i], np.int32), **m)
+            kcs[b:b + 1], vcs[b:b + 1] = kb, vb
+            assert r.out.tobytes() == rm.out[t:t + 1].tobytes(), (b, i)
+    assert kcs.tobytes() == kcm.tobytes() and vcs.tobytes() == vcm.tobytes()
+
+
+def test_multi_causal_library_sdpa():
+    """torch SDPA in float64 with an explicit causal mask: row b's n queries
+    over its lengths[b] + n keys, query i masked beyond key lengths[b] + i."""
+    q_lens = [4, 2, 6]
+    c = _multi_case(52, q_lens, Smax=30, Hq=6, Hkv=2, D=16)
+    kc, vc = c["k_cache"].copy(), c["v_cache"].copy()
+    r = oracle.decode_multi_dense(c["q"], c["k_new"], c["v_new"], kc, vc, c["lengths"], c["cu_q"])
+    G = 3
+    for b, n in enumerate(q_lens):
+        Lb = int(c["lengths"][b])
+        t0 = int(c["cu_q"][b])
+        k = torch.from_numpy(kc[b, :, :Lb + n]).double().repeat_interleave(G, 0)   # (Hq, S, D)
+        v = torch.from_numpy(vc[b, :, :Lb + n]).double().repeat_interleave(G, 0)
+        qb = torch.from_numpy(c["q"][t0:t0 + n]).double().permute(1, 0, 2)          # (Hq, n, D)
+        mask = torch.arange(Lb + n)[None, :] <= (Lb + torch.arange(n))[:, None]
+        o = torch.nn.functional.scaled_dot_product_attention(qb, k, v, attn_mask=mask)
+        np.testing.assert_allclose(r.out[t0:t0 + n], o.permute(1, 0, 2).numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_multi_brute_force_tiny():
+    q_lens = [2, 0, 3]
+    c = _multi_case(53, q_lens, Smax=9, Hq=4, Hkv=1, D=3)
+    kc, vc = c["k_cache"].copy(), c["v_cache"].copy()
+    r = oracle.decode_multi_dense(c["q"], c["k_new"], c["v_new"], kc, vc, c["lengths"], c["cu_q"])
+    want = np.full_like(r.out, np.nan)
+    for b, n in enumerate(q_lens):
+        Lb, t0 = int(c["lengths"][b]), int(c["cu_q"][b])
+        keys = [c["k_cache"][b, 0, j] for j in range(Lb)] + [c["k_new"][t0 + i, 0] for i in range(n)]
+        vals = [c["v_cache"][b, 0, j] for j in range(Lb)] + [c["v_new"][t0 + i, 0] for i in range(n)]
+        for i in range(n):
+            for h in range(4):
+                qs = [float(x) for x in c["q"][t0 + i, h]]
+                e = [math.exp(sum(a * float(k) for a, k in zip(qs, keys[j])) / math.sqrt(3))
+                     for j in range(Lb + i + 1)]
+                z = sum(e)
+                for d in range(3):
+                    want[t0 + i, h, d] = sum(e[j] * float(vals[j][d]) for j in range(Lb + i + 1)) / z
+    np.testing.assert_allclose(r.out, want, rtol=1e-12, atol=1e-12)
+
+
+def test_multi_append_and_no_append():
+    """The n new tokens' bits land at slots lengths[b] .. lengths[b]+n-1 and
+    nothing else changes; without the append the outputs are the same and
+    the cache untouched."""
+    q_lens = [3, 1, 0, 4]
+    c = _multi_case(54, q_lens, dtype="bf16")
+    kc, vc = c["k_cache"].copy(), c["v_cache"].copy()
+    r = oracle.decode_multi_dense(c["q"], c["k_new"], c["v_new"], kc, vc, c["lengths"], c["cu_q"])
+    want_k, want_v = c["k_cache"].copy(), c["v_cache"].copy()
+    for b, n in enumerate(q_lens):
+        for i in range(n):
+            want_k[b, :, c["lengths"][b] + i] = c["k_new"][c["cu_q"][b] + i]
+            want_v[b, :, c["lengths"][b] + i] = c["v_new"][c["cu_q"][b] + i]
+    assert kc.tobytes() == want_k.tobytes() and vc.tobytes() == want_v.tobytes()
+    kc2, vc2 = c["k_cache"].copy(), c["v_cache"].copy()
+    r2 = oracle.decode_multi_dense(c["q"], c["k_new"], c["v_new"], kc2, vc2, c["lengths"], c["cu_q"],
+                                   append=False)
+    assert r2.out.tobytes() == r.out.tobytes()
+    assert kc2.tobytes() == c["k_cache"].tobytes()
+
+
+def test_multi_paged_equals_dense():
+    q_lens = [3, 2, 4]
+    c = _multi_case(55, q_lens, Smax=24, dtype="bf16")
+    bs, nb = 4, 6
+    B = len(q_lens)
+    kb = np.ascontiguousarray(c["k_cache"].reshape(B, 2, nb, bs, 8).transpose(0, 2, 1, 3, 4).reshape(B * nb, 2, bs, 8))
+    vb = np.ascontiguousarray(c["v_cache"].reshape(B, 2, nb, bs, 8).transpose(0, 2, 1, 3, 4).reshape(B * nb, 2, bs, 8))
+    perm = np.random.default_rng(5).permutation(B * nb)
+    kb2, vb2 = np.empty_like(kb), np.empty_like(vb)
+    kb2[perm], vb2[perm] = kb, vb
+    bt = perm.reshape(B, nb).astype(np.int32)
+    kc, vc = c["k_cache"].copy(), c["v_cache"].copy()
+    rd = oracle.decode_multi_dense(c["q"], c["k_new"], c["v_new"], kc, vc, c["lengths"], c["cu_q"])
+    rp = oracle.decode_multi_paged(c["q"], c["k_new"], c["v_new"], kb2, vb2, bt, c["lengths"], c["cu_q"])
+    assert rp.status == oracle.OK and rp.out.tobytes() == rd.out.tobytes()
+    back = kb2[perm].reshape(B, nb, 2, bs, 8).transpose(0, 2, 1, 3, 4).reshape(B, 2, nb * bs, 8)
+    assert back.tobytes() == kc.tobytes()
+
+
+def test_multi_validate_rules():
+    ok, bad = oracle.OK, oracle.INVALID_ARGUMENT
+    L = np.array([3, 0, 5], np.int32)
+    assert oracle.validate_multi_dense(L, np.array([0, 2, 2, 5], np.int32), None, 5, 3, 10) == ok
+    assert oracle.validate_multi_dense(L, np.array([1, 2, 2, 5], np.int32), None, 5, 3, 10) == bad   # cu_q[0] != 0
+    assert oracle.validate_multi_dense(L, np.array([0, 3, 2, 5], np.int32), None, 5, 3, 10) == bad   # decreasing
+    assert oracle.validate_multi_dense(L, np.array([0, 2, 2, 4], np.int32), None, 5, 3, 10) == bad   # cu_q[B] != T
+    assert oracle.validate_multi_dense(L, np.array([0, 2, 2, 5], np.int32), None, 5, 3, 7) == bad    # 5 + 3 > 7
+    assert oracle.validate_multi_dense(L, np.array([0, 2, 2, 5], np.int32), None, 5, 3, 8) == ok     # exactly full
+    assert oracle.validate_multi_dense(np.array([3, -1, 5], np.int32), np.array([0, 2, 2, 5], np.int32),
+                                       None, 5, 3, 10) == bad
+    assert oracle.validate_multi_dense(L, np.array([0, 2, 2, 5], np.int32), np.array([1, 1, 0], np.int32),
+                                       5, 3, 10) == bad
+    bt = np.array([[0, 1, -1], [2, -1, -1], [3, 4, -1]], np.int32)
+    Lp = np.array([3, 1, 4], np.int32)
+    assert oracle.validate_multi_paged(Lp, np.array([0, 2, 3, 5], np.int32), bt, 5, 6, 4) == ok       # 4 + 1 slots / 8
+    assert oracle.validate_multi_paged(Lp, np.array([0, 2, 3, 8], np.int32), bt, 8, 6, 4) == bad      # 4 + 5 > 8
