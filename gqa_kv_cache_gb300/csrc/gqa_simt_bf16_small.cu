@@ -1,0 +1,19 @@
+// CUDA-core decode kernel instantiations: __nv_bfloat16, D in {1, 2, 4, 8, 16}
+// (the kernel is in gqa_simt_kernel.cuh).
+#include "gqa_simt_kernel.cuh"
+
+namespace gqa {
+
+cudaError_t simt_launch_bf16_small(int D, int G, const DecodeParams *p, cudaStream_t st, int *per_sm)
+{
+    switch (D) {
+    case 1: return launch_g<__nv_bfloat16, 1>(G, p, st, per_sm);
+    case 2: return launch_g<__nv_bfloat16, 2>(G, p, st, per_sm);
+    case 4: return launch_g<__nv_bfloat16, 4>(G, p, st, per_sm);
+    case 8: return launch_g<__nv_bfloat16, 8>(G, p, st, per_sm);
+    case 16: return launch_g<__nv_bfloat16, 16>(G, p, st, per_sm);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace gqa
