@@ -23,6 +23,9 @@ With --impl reference the oracle itself is timed as the reference arm.
 valid slots; a float32 query over the workload's cache unless --q-dtype cache).
 --window W / --kept-prefix P / --sink add the softmax modifiers; the KV bytes
 then count only the slots inside the window or the prefix.
+--q-len N times the multi-token step (N new tokens per row, causal); its KV
+bytes count the cached slots once (a row whose tokens span several chunks of
+8 / G tokens streams them once per chunk, which shows in the roofline).
 
 Multi-GPU (torchrun): every rank runs an independent replica with its own
 batch (weak scaling, no data-path collective); times are max over ranks.
@@ -42,6 +45,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "KV-cache HBM GB/s & fraction of ~8 TB/s peak; µs per GQA decode step"
 METRIC_ATTEND = "KV-cache HBM GB/s & fraction of ~8 TB/s peak; µs per GQA read-only attend"
+METRIC_MULTI = "KV-cache HBM GB/s & fraction of ~8 TB/s peak; µs per GQA multi-token decode step"
 UNIT = "GB/s"
 NOMINAL_HBM_GBPS = 8000.0
 FALLBACK_HBM_GBPS = 6800.0
@@ -63,6 +67,7 @@ def parse():
     ap.add_argument("--window", type=int, default=0, help="sliding window W (0: none)")
     ap.add_argument("--kept-prefix", type=int, default=0, help="kept prefix P (with a window)")
     ap.add_argument("--sink", action="store_true", help="a per-head sink logit (seeded N(0,1))")
+    ap.add_argument("--q-len", type=int, default=0, help="multi-token step with this many new tokens per row")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sched-pad", type=int, default=None,
                     help="schedule-only tiles per (row, head); default: the library's")
@@ -139,6 +144,25 @@ def cached_slots_read(L, attend, window=0, kept_prefix=0):
     return (L - lo) + torch.clamp(lo, max=kept_prefix)
 
 
+def algorithmic_bytes_multi(w, t) -> dict:
+    """Multi-token step: every cached slot read once, the new tokens' K/V
+    read and appended, q read, out written, index reads."""
+    import torch
+    L = t["lengths"].to(torch.int64)
+    es = w.elem_bytes
+    T = t["q"].shape[0]
+    kv = int(L.sum().item()) * w.Hkv * w.D * 2 * es
+    new = T * w.Hkv * w.D * es * 2
+    q = t["q"].numel() * t["q"].element_size()
+    out = T * w.Hq * w.D * 4
+    idx = w.B * 4 * (3 if w.slot_ids else 2)
+    if w.paged:
+        ql = (t["cu_q"][1:] - t["cu_q"][:-1]).to(torch.int64)
+        idx += int(((L + ql + w.block_size - 1) // w.block_size).sum().item()) * 4
+    return {"kv_read": kv, "append_write": new, "new_kv_read": new, "q_read": q, "out_write": out,
+            "index_read": idx, "total": kv + 2 * new + q + out + idx}
+
+
 def algorithmic_bytes(w, t, attend=False, window=0, kept_prefix=0) -> dict:
     """Bytes the step must move (no split partials): the KV read, the append
     write, the new K/V, q, out and the index reads. The decode step reads the
@@ -160,10 +184,18 @@ def algorithmic_bytes(w, t, attend=False, window=0, kept_prefix=0) -> dict:
             "total": kv + 2 * new + q + w.B * w.Hq * w.D * 4 + idx}
 
 
-def step_fn(w, t, kernel, out, sched_pad=None, attend=False, mods=None):
+def step_fn(w, t, kernel, out, sched_pad=None, attend=False, mods=None, max_q=0):
     import gqa_kv_cache_gb300 as gqa
     kw = dict(out=out, kernel=kernel, sched_pad=sched_pad, **(mods or {}))
-    if attend and w.paged:
+    if max_q and w.paged:
+        def run(tt=t):
+            gqa.decode_multi_paged(tt["q"], tt["k_new"], tt["v_new"], tt["k_blocks"], tt["v_blocks"],
+                                   tt["block_table"], tt["lengths"], tt["cu_q"], max_q_len=max_q, **kw)
+    elif max_q:
+        def run(tt=t):
+            gqa.decode_multi(tt["q"], tt["k_new"], tt["v_new"], tt["k_cache"], tt["v_cache"], tt["lengths"],
+                             tt["cu_q"], tt.get("slot_ids"), max_q_len=max_q, **kw)
+    elif attend and w.paged:
         def run(tt=t):
             gqa.attend_paged(tt["q"], tt["k_blocks"], tt["v_blocks"], tt["block_table"], tt["lengths"], **kw)
     elif attend:
@@ -302,7 +334,8 @@ def make_mods(args, w, dev):
 
 
 def mods_config(args):
-    return {"window": args.window, "kept_prefix": args.kept_prefix, "sink": bool(args.sink)}
+    return {"window": args.window, "kept_prefix": args.kept_prefix, "sink": bool(args.sink),
+            "q_len": args.q_len or 1}
 
 
 def peaks():
@@ -385,12 +418,17 @@ def run_ours(args, ranks):
     dev = torch.device("cuda", ranks.local)
     w = workload(args.workload, ranks.rank)
     attend = args.op == "attend"
-    t = W.generate(w, dev, attend=attend, q_f32=attend and args.q_dtype != "cache")
+    multi = args.q_len > 0
+    if multi and (attend or args.window or args.kept_prefix):
+        raise SystemExit("--q-len times the plain multi-token step (no --op attend / window)")
+    t = W.generate(w, dev, attend=attend, q_f32=attend and args.q_dtype != "cache",
+                   q_lens=[args.q_len] * w.B if multi else None)
     torch.cuda.synchronize()
-    out = torch.empty(w.B, w.Hq, w.D, dtype=torch.float32, device=dev)
+    out = torch.empty(t["q"].shape[0], w.Hq, w.D, dtype=torch.float32, device=dev)
     mods = make_mods(args, w, dev)
-    step = step_fn(w, t, args.kernel, out, args.sched_pad, attend, mods)
-    alg = algorithmic_bytes(w, t, attend, args.window, args.kept_prefix)
+    step = step_fn(w, t, args.kernel, out, args.sched_pad, attend, mods, args.q_len)
+    alg = algorithmic_bytes_multi(w, t) if multi else algorithmic_bytes(w, t, attend, args.window,
+                                                                         args.kept_prefix)
     flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush_r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     flush_sink = torch.empty((), dtype=torch.float32, device=dev)
@@ -451,18 +489,18 @@ def run_ours(args, ranks):
     avg_main_s = ms_main / max(n_main, 1) * 1e-3
     hbm_peak, peak_kind = peaks()
     achieved = alg["total"] / avg_main_s / 1e9
-    traffic = None if mods else traffic_for(main, w.name + ("/attend" if attend else ""))
+    traffic = None if (mods or multi) else traffic_for(main, w.name + ("/attend" if attend else ""))
 
     # ---- end to end through the public API, host buffers, copies inside
     Ke = min(K, 500)
-    inputs = ["q", "lengths"] + ([] if attend else ["k_new", "v_new"]) + \
+    inputs = ["q", "lengths"] + ([] if attend else ["k_new", "v_new"]) + (["cu_q"] if multi else []) + \
         (["slot_ids"] if "slot_ids" in t else []) + \
         (["block_table"] if "block_table" in t else [])
     host = {k: t[k].cpu().pin_memory() for k in inputs}
     dev_in = {k: torch.empty_like(t[k]) for k in inputs}
     tt = dict(t)
     tt.update(dev_in)
-    step_e2e = step_fn(w, tt, args.kernel, out, args.sched_pad, attend, mods)
+    step_e2e = step_fn(w, tt, args.kernel, out, args.sched_pad, attend, mods, args.q_len)
     out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
     h2d = sum(host[k].numel() * host[k].element_size() for k in inputs)
     d2h = out.numel() * out.element_size()
@@ -484,7 +522,7 @@ def run_ours(args, ranks):
 
     # ---- CPU baseline: the oracle on host cores, rank 0 at N = 1 only
     cpu = None
-    if ranks.world == 1 and not args.no_cpu_baseline:
+    if ranks.world == 1 and not args.no_cpu_baseline and not multi:
         rows = list(range(w.B))
         gbs, sec, threads = oracle_rate(w, t, rows, repeats=3, mods=mods)
         cpu = {"value": gbs, "unit": UNIT, "cores": threads, "kind": "oracle",
@@ -492,7 +530,8 @@ def run_ours(args, ranks):
                          f"median of 3 after 1 warm-up, {sec:.2f} s per pass"}
 
     line = {
-        "metric": METRIC_ATTEND if attend else METRIC, "value": value, "unit": UNIT,
+        "metric": METRIC_MULTI if multi else (METRIC_ATTEND if attend else METRIC), "value": value,
+        "unit": UNIT,
         "n_gpus": ranks.world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "us_per_step": ms_per_step * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,

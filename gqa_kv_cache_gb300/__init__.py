@@ -24,13 +24,14 @@ import torch
 
 from . import _lib
 
-__all__ = ["decode_step", "decode_step_paged", "attend", "attend_paged", "workspace_bytes",
-           "validate", "validate_attend",
+__all__ = ["decode_step", "decode_step_paged", "attend", "attend_paged", "decode_multi",
+           "decode_multi_paged", "workspace_bytes", "validate", "validate_attend", "validate_multi",
            "GqaError", "trace_enable", "trace_collect", "KERNELS", "library_path"]
 
 OK, INVALID_ARGUMENT, UNSUPPORTED, CUDA_ERROR, WORKSPACE = 0, 1, 2, 3, 4
 KERNELS = {"auto": 0, "simt": 1, "tc": 2}
-STATUS_BITS = {1: "bad length", 2: "bad slot id", 4: "bad block", 8: "timeout", 16: "bad kept prefix"}
+STATUS_BITS = {1: "bad length", 2: "bad slot id", 4: "bad block", 8: "timeout", 16: "bad kept prefix",
+               32: "bad token offsets"}
 _DTYPES = {torch.float32: 0, torch.bfloat16: 1}
 
 library_path = _lib.LIB_PATH
@@ -237,6 +238,88 @@ def attend_paged(q, k_blocks, v_blocks, block_table, lengths, *, out=None, statu
                                 ctypes.byref(o))
     _check(code, "gqa_attend_paged")
     return out
+
+
+def _multi_checks(q, k_new, v_new, caches, lengths, cu_q, out):
+    dt, out = _common_checks(q, k_new, v_new, caches, lengths, out)
+    if cu_q.dtype != torch.int32 or cu_q.dim() != 1 or cu_q.shape[0] != lengths.shape[0] + 1 \
+            or not cu_q.is_contiguous() or cu_q.device != q.device:
+        raise TypeError("cu_q must be a contiguous int32 (B + 1,) tensor on q's device")
+    return dt, out
+
+
+def decode_multi(q, k_new, v_new, k_cache, v_cache, lengths, cu_q, slot_ids=None, *, max_q_len,
+                 out=None, status=None, kernel="auto", grid_ctas=0, workspace=None, stream=None,
+                 sched_pad=None, sink=None, window=0, kept_prefix=0):
+    """Multi-token step on a dense (R, Hkv, Smax, D) cache: the packed tokens
+    cu_q[b] .. cu_q[b+1]-1 of row b (q (T, Hq, D), k_new / v_new (T, Hkv, D))
+    are appended at slots lengths[b] + i and token i attends slots
+    0 .. lengths[b] + i. ``max_q_len`` bounds every q_len. Returns out
+    (T, Hq, D)."""
+    dt, out = _multi_checks(q, k_new, v_new, (("k_cache", k_cache), ("v_cache", v_cache)), lengths,
+                            cu_q, out)
+    T, Hq, D = q.shape
+    B = lengths.shape[0]
+    R, Hkv, Smax, D2 = k_cache.shape
+    if D2 != D or v_cache.shape != k_cache.shape or k_new.shape != (T, Hkv, D) or v_new.shape != (T, Hkv, D):
+        raise ValueError("shape mismatch between q, k_new, v_new and the caches")
+    if slot_ids is not None and (slot_ids.dtype != torch.int32 or slot_ids.shape != (B,)):
+        raise TypeError("slot_ids must be int32 of shape (B,)")
+    o = _opts(kernel, grid_ctas, sched_pad, sink, window, kept_prefix, q.device, B, Hq)
+    lib = _lib.load()
+    need = lib.gqa_workspace_bytes_multi(B, Hq, Hkv, D, _DTYPES[dt], int(max_q_len), ctypes.byref(o))
+    ws = _workspace(q.device, need) if workspace is None else workspace
+    code = lib.gqa_decode_multi(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                _ptr(lengths), _ptr(cu_q), _ptr(slot_ids), _ptr(out), B, T, int(max_q_len),
+                                Hq, Hkv, D, R, Smax, _DTYPES[dt], _ptr(ws), ws.numel() * ws.element_size(),
+                                _ptr(status), _stream(stream), ctypes.byref(o))
+    _check(code, "gqa_decode_multi")
+    return out
+
+
+def decode_multi_paged(q, k_new, v_new, k_blocks, v_blocks, block_table, lengths, cu_q, *, max_q_len,
+                       out=None, status=None, kernel="auto", grid_ctas=0, workspace=None, stream=None,
+                       sched_pad=None, sink=None, window=0, kept_prefix=0):
+    """Multi-token step on a paged cache (num_blocks, Hkv, block_size, D)."""
+    dt, out = _multi_checks(q, k_new, v_new, (("k_blocks", k_blocks), ("v_blocks", v_blocks)), lengths,
+                            cu_q, out)
+    T, Hq, D = q.shape
+    B = lengths.shape[0]
+    NB, Hkv, BS, D2 = k_blocks.shape
+    if D2 != D or v_blocks.shape != k_blocks.shape or k_new.shape != (T, Hkv, D) or v_new.shape != (T, Hkv, D):
+        raise ValueError("shape mismatch between q, k_new, v_new and the blocks")
+    if block_table.dtype != torch.int32 or block_table.dim() != 2 or block_table.shape[0] != B \
+            or not block_table.is_contiguous():
+        raise TypeError("block_table must be a contiguous int32 (B, max_blocks) tensor")
+    o = _opts(kernel, grid_ctas, sched_pad, sink, window, kept_prefix, q.device, B, Hq)
+    lib = _lib.load()
+    need = lib.gqa_workspace_bytes_multi(B, Hq, Hkv, D, _DTYPES[dt], int(max_q_len), ctypes.byref(o))
+    ws = _workspace(q.device, need) if workspace is None else workspace
+    code = lib.gqa_decode_multi_paged(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_blocks), _ptr(v_blocks),
+                                      _ptr(block_table), _ptr(lengths), _ptr(cu_q), _ptr(out), B, T,
+                                      int(max_q_len), Hq, Hkv, D, NB, BS, block_table.shape[1], _DTYPES[dt],
+                                      _ptr(ws), ws.numel() * ws.element_size(), _ptr(status),
+                                      _stream(stream), ctypes.byref(o))
+    _check(code, "gqa_decode_multi_paged")
+    return out
+
+
+def validate_multi(lengths, cu_q, T, *, slot_ids=None, R=None, Smax=None, block_table=None,
+                   num_blocks=None, block_size=None, stream=None) -> bool:
+    """Full content check on the GPU for a multi-token step (synchronous)."""
+    B = lengths.shape[0]
+    res = torch.empty(1, dtype=torch.int32, device=lengths.device)
+    lib = _lib.load()
+    if block_table is not None:
+        code = lib.gqa_validate_multi(_ptr(lengths), _ptr(cu_q), None, _ptr(block_table), B, T, 0, 0,
+                                      num_blocks, block_size, block_table.shape[1], _ptr(res), _stream(stream))
+    else:
+        code = lib.gqa_validate_multi(_ptr(lengths), _ptr(cu_q), _ptr(slot_ids), None, B, T, R, Smax, 0, 0, 0,
+                                      _ptr(res), _stream(stream))
+    if code == INVALID_ARGUMENT:
+        return False
+    _check(code, "gqa_validate_multi")
+    return True
 
 
 def _validate(fn, what, lengths, slot_ids, R, Smax, block_table, num_blocks, block_size, stream):

@@ -22,6 +22,11 @@ SIGNATURES = {
     "gqa_validate": (I, [P, P, P, I, I, I, I, I, I, P, P]),
     "gqa_validate_attend": (I, [P, P, P, I, I, I, I, I, I, P, P]),
     "gqa_attend": (I, [P, I, P, P, P, P, P, I, I, I, I, I, I, I, P, Z, P, P, P]),
+    "gqa_workspace_bytes_multi": (Z, [I, I, I, I, I, I, P]),
+    "gqa_decode_multi": (I, [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, P, Z, P, P, P]),
+    "gqa_decode_multi_paged": (I, [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, P, Z, P, P,
+                                   P]),
+    "gqa_validate_multi": (I, [P, P, P, P, I, I, I, I, I, I, I, P, P]),
     "gqa_attend_paged": (I, [P, I, P, P, P, P, P, I, I, I, I, I, I, I, I, P, Z, P, P, P]),
     "gqa_trace_enable": (I, [I]),
     "gqa_trace_collect": (I, [I, P, P]),

@@ -176,7 +176,28 @@ struct Shape {
     int num_blocks, block_size, max_blocks;
     bool attend = false;          // read-only attend: no new token, nothing written but out
     gqa_dtype q_dt = GQA_DTYPE_F32;
+    bool multi = false;           // multi-token step: T packed tokens, q_len <= max_q
+    int T = 0, max_q = 1;
 };
+
+// How a multi-token step is cut into virtual rows: tokens per chunk (so that
+// chunk rows G * tpc fit the 8 query rows of the tensor-core tile) and chunks
+// per batch row.
+struct MultiCut {
+    int tpc, chunks;
+};
+
+MultiCut multi_cut(int G, int max_q)
+{
+    MultiCut c;
+    c.tpc = G >= 8 ? 1 : 8 / G;
+    if (c.tpc > max_q)
+        c.tpc = max_q > 0 ? max_q : 1;
+    c.chunks = (max_q + c.tpc - 1) / c.tpc;
+    if (c.chunks < 1)
+        c.chunks = 1;
+    return c;
+}
 
 bool valid_dtype(gqa_dtype d) { return d == GQA_DTYPE_F32 || d == GQA_DTYPE_BF16; }
 
@@ -203,12 +224,15 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 gqa_status run_step(const Shape &s, const void *q, const void *k_new, const void *v_new, void *kc,
                     void *vc, const int32_t *lengths, const int32_t *slot_ids,
                     const int32_t *block_table, float *out, void *ws, size_t ws_bytes,
-                    int32_t *d_status, void *stream, const gqa_options *opt)
+                    int32_t *d_status, void *stream, const gqa_options *opt,
+                    const int32_t *cu_q = nullptr)
 {
     gqa_status st = check_shape(s);
     if (st != GQA_OK)
         return st;
-    if (s.B == 0)
+    if (s.multi && (s.T < 0 || s.max_q < 0 || !cu_q))
+        return GQA_ERR_INVALID_ARGUMENT;
+    if (s.B == 0 || (s.multi && (s.T == 0 || s.max_q == 0)))
         return GQA_OK;
     if (!q || !kc || !vc || !lengths || !out || (s.paged && !block_table))
         return GQA_ERR_INVALID_ARGUMENT;
@@ -224,14 +248,19 @@ gqa_status run_step(const Shape &s, const void *q, const void *k_new, const void
         return GQA_ERR_INVALID_ARGUMENT;
     if (!s.attend && (!aligned16(k_new) || !aligned16(v_new)))
         return GQA_ERR_INVALID_ARGUMENT;
-    const int G = s.Hq / s.Hkv;
+    const int Gh = s.Hq / s.Hkv;
+    if (s.multi && Gh > 8)
+        return GQA_ERR_UNSUPPORTED;
+    const MultiCut cut = s.multi ? multi_cut(Gh, s.max_q) : MultiCut{1, 1};
+    const int G = Gh * cut.tpc;             // query rows of a unit
+    const int Bv = s.B * cut.chunks;        // (virtual) rows of the schedule
     const int kernel = pick_kernel(opt, s.dt, s.D, G, s.paged, s.block_size);
     if (kernel < 0)
         return GQA_ERR_UNSUPPORTED;
     const int grid = grid_for(kernel, opt, s.dt, s.D, G);
     if (grid <= 0)
         return GQA_ERR_CUDA;
-    const WorkspaceLayout lay = workspace_layout(s.B, s.Hkv, G, s.D, grid);
+    const WorkspaceLayout lay = workspace_layout(Bv, s.Hkv, G, s.D, grid);
     if (!ws || ws_bytes < lay.bytes || (reinterpret_cast<uintptr_t>(ws) & 255u))
         return GQA_ERR_WORKSPACE;
 
@@ -248,10 +277,16 @@ gqa_status run_step(const Shape &s, const void *q, const void *k_new, const void
     p.slot_ids = s.paged ? nullptr : slot_ids;
     p.block_table = s.paged ? block_table : nullptr;
     p.out = out;
-    p.B = s.B;
+    p.B = Bv;
     p.Hq = s.Hq;
     p.Hkv = s.Hkv;
     p.G = G;
+    p.Gh = Gh;
+    p.tpc = cut.tpc;
+    p.max_chunks = cut.chunks;
+    p.cu_q = s.multi ? cu_q : nullptr;
+    p.T = s.T;
+    p.max_q = s.max_q;
     p.D = s.D;
     p.R = s.R;
     p.Smax = s.Smax;
@@ -391,7 +426,8 @@ namespace {
 
 gqa_status validate_common(const int32_t *lengths, const int32_t *slot_ids, const int32_t *block_table,
                            int B, int R, int Smax, int num_blocks, int block_size, int max_blocks,
-                           int attend, int32_t *d_result, void *stream)
+                           int attend, int32_t *d_result, void *stream, const int32_t *cu_q = nullptr,
+                           int T = 0)
 {
     if (B < 0 || !d_result)
         return GQA_ERR_INVALID_ARGUMENT;
@@ -409,7 +445,7 @@ gqa_status validate_common(const int32_t *lengths, const int32_t *slot_ids, cons
     if (cudaMemsetAsync(d_result, 0, sizeof(int32_t), cs) != cudaSuccess)
         return GQA_ERR_CUDA;
     if (validate_launch(lengths, block_table ? nullptr : slot_ids, block_table, B, R, Smax,
-                        num_blocks, block_size, max_blocks, attend, d_result, cs) != cudaSuccess)
+                        num_blocks, block_size, max_blocks, attend, cu_q, T, d_result, cs) != cudaSuccess)
         return GQA_ERR_CUDA;
     int32_t h = 0;
     if (cudaMemcpyAsync(&h, d_result, sizeof h, cudaMemcpyDeviceToHost, cs) != cudaSuccess ||
@@ -436,6 +472,62 @@ gqa_status gqa_validate_attend(const int32_t *lengths, const int32_t *slot_ids,
 {
     return validate_common(lengths, slot_ids, block_table, B, R, Smax, num_blocks, block_size,
                            max_blocks, 1, d_result, stream);
+}
+
+gqa_status gqa_validate_multi(const int32_t *lengths, const int32_t *cu_q, const int32_t *slot_ids,
+                              const int32_t *block_table, int B, int T, int R, int Smax, int num_blocks,
+                              int block_size, int max_blocks, int32_t *d_result, void *stream)
+{
+    if (!cu_q || T < 0)
+        return GQA_ERR_INVALID_ARGUMENT;
+    return validate_common(lengths, slot_ids, block_table, B, R, Smax, num_blocks, block_size,
+                           max_blocks, 0, d_result, stream, cu_q, T);
+}
+
+size_t gqa_workspace_bytes_multi(int B, int Hq, int Hkv, int D, gqa_dtype dt, int max_q_len,
+                                 const gqa_options *opt)
+{
+    if (B < 0 || Hq < 1 || Hkv < 1 || D < 1 || Hq % Hkv || max_q_len < 0 || Hq / Hkv > 8)
+        return 0;
+    const MultiCut cut = multi_cut(Hq / Hkv, max_q_len);
+    const int G = (Hq / Hkv) * cut.tpc;
+    int kernel = pick_kernel(opt, dt, D, G, false, 16);
+    if (kernel < 0)
+        return 0;
+    int grid = grid_for(kernel, opt, dt, D, G);
+    if ((!opt || opt->kernel == GQA_KERNEL_AUTO) && simt_supports(D, G)) {
+        const int g2 = grid_for(GQA_KERNEL_SIMT, opt, dt, D, G);
+        grid = grid > g2 ? grid : g2;
+    }
+    if (grid <= 0)
+        return 0;
+    return workspace_layout(B * cut.chunks, Hkv, G, D, grid).bytes;
+}
+
+gqa_status gqa_decode_multi(const void *q, const void *k_new, const void *v_new, void *k_cache,
+                            void *v_cache, const int32_t *lengths, const int32_t *cu_q,
+                            const int32_t *slot_ids, float *out, int B, int T, int max_q_len, int Hq,
+                            int Hkv, int D, int R, int Smax, gqa_dtype dt, void *workspace,
+                            size_t workspace_bytes, int32_t *d_status, void *stream,
+                            const gqa_options *opt)
+{
+    Shape s = {B, Hq, Hkv, D, dt, false, R, Smax, 0, 0, 0, false, dt, true, T, max_q_len};
+    return run_step(s, q, k_new, v_new, k_cache, v_cache, lengths, slot_ids, nullptr, out, workspace,
+                    workspace_bytes, d_status, stream, opt, cu_q);
+}
+
+gqa_status gqa_decode_multi_paged(const void *q, const void *k_new, const void *v_new,
+                                  void *k_blocks, void *v_blocks, const int32_t *block_table,
+                                  const int32_t *lengths, const int32_t *cu_q, float *out, int B,
+                                  int T, int max_q_len, int Hq, int Hkv, int D, int num_blocks,
+                                  int block_size, int max_blocks, gqa_dtype dt, void *workspace,
+                                  size_t workspace_bytes, int32_t *d_status, void *stream,
+                                  const gqa_options *opt)
+{
+    Shape s = {B, Hq, Hkv, D, dt, true, 0, 0, num_blocks, block_size, max_blocks, false, dt, true, T,
+               max_q_len};
+    return run_step(s, q, k_new, v_new, k_blocks, v_blocks, lengths, nullptr, block_table, out,
+                    workspace, workspace_bytes, d_status, stream, opt, cu_q);
 }
 
 gqa_status gqa_attend(const void *q, gqa_dtype q_dtype, const void *k_cache, const void *v_cache,

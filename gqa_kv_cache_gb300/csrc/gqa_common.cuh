@@ -23,8 +23,19 @@
 // i for unit u is stored at index u + i: along the (CTA, unit) pairs in
 // order, u + i grows by one or two at every step, so the index is unique and
 // fewer than B * Hkv + C partials exist.
+//
+// Multi-token step. A batch row with q_len new tokens is cut into chunks of
+// up to tpc tokens (tpc * Gh <= 8 query rows); each (row, chunk) is a
+// virtual batch row, so B above counts B_real * max_chunks virtual rows and G
+// counts the query rows of a unit, (token, head) pairs in token-major order.
+// Chunk c of row b attends slots 0 .. L with L the position of its last
+// token; row r (token i of the chunk) is masked beyond L - (nq - 1 - i).
+// Every slot at or beyond the row's write offset Lb holds a new token: it is
+// taken from k_new / v_new, never from the cache, and the chunk owning the
+// token writes it into the cache (the append).
 #pragma once
 
+#include <climits>
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -37,6 +48,7 @@ constexpr int kBadSlotId = 2;
 constexpr int kBadBlock = 4;
 constexpr int kTimeout = 8;
 constexpr int kBadPrefix = 16;
+constexpr int kBadQLen = 32;
 
 struct DecodeParams {
     const void *q;      // (B, Hq, D)
@@ -59,6 +71,13 @@ struct DecodeParams {
     int window;                      // W > 0: only the last W positions (and the prefix); 0: all
     int kept_prefix;                 // P for every row when kept_prefix_rows is null
     const int32_t *kept_prefix_rows; // (B) P per row, or null
+    // multi-token step (cu_q non-null; see above)
+    const int32_t *cu_q;  // (B_real + 1) packed token offsets
+    int T;                // packed tokens
+    int Gh;               // query heads per cache head (G = Gh * tpc query rows)
+    int tpc;              // tokens per chunk
+    int max_chunks;       // chunks (virtual rows) per batch row
+    int max_q;            // largest accepted q_len (tpc * max_chunks)
     int tile;          // T, slots per tile
     int pad_tiles;     // W, schedule-only tiles appended to every unit (see row_tiles)
     int grid;          // C, CTAs of the decode launch
@@ -93,11 +112,40 @@ __host__ __device__ inline WorkspaceLayout workspace_layout(int B, int Hkv, int 
 
 // Last attended slot of row b: lengths[b] in the decode step (the append
 // slot), lengths[b] - 1 in the read-only attend; -1 (a bad row) when the
-// attend has no valid slot.
+// attend has no valid slot. (Single-token forms; see row_geom for chunks.)
 __device__ __forceinline__ int last_slot(const DecodeParams &p, int b)
 {
     const int n = __ldg(p.lengths + b);
     return p.attend ? (n > 0 ? n - 1 : -1) : n;
+}
+
+// Batch row of virtual row vb.
+__device__ __forceinline__ int real_row(const DecodeParams &p, int vb)
+{
+    return p.cu_q ? vb / p.max_chunks : vb;
+}
+
+// The tokens of virtual row vb of a multi-token step: nq tokens (0: an empty
+// chunk; -1: the row's token offsets are bad), i0 tokens of the row before
+// them, tok0 the packed index of the row's first token, Lb its write offset.
+struct ChunkInfo {
+    int nq, i0, tok0, Lb;
+};
+
+__device__ __forceinline__ ChunkInfo chunk_info(const DecodeParams &p, int vb)
+{
+    const int b = vb / p.max_chunks, c = vb % p.max_chunks;
+    const int t0 = __ldg(p.cu_q + b), t1 = __ldg(p.cu_q + b + 1);
+    ChunkInfo ci;
+    ci.i0 = c * p.tpc;
+    ci.tok0 = t0;
+    ci.Lb = __ldg(p.lengths + b);
+    const int qlen = t1 - t0;
+    if (t0 < 0 || t1 > p.T || qlen < 0 || qlen > p.max_q)
+        ci.nq = (c == 0) ? -1 : 0;
+    else
+        ci.nq = max(0, min(p.tpc, qlen - ci.i0));
+    return ci;
 }
 
 // Capacity of one row in slots: the last attended slot must be below it.
@@ -106,10 +154,10 @@ __host__ __device__ inline long long row_capacity(const DecodeParams &p)
     return p.paged ? (long long)p.max_blocks * p.block_size : (long long)p.Smax;
 }
 
-// The kept prefix of row b (negative: a bad row).
-__device__ __forceinline__ int kept_prefix(const DecodeParams &p, int b)
+// The kept prefix of virtual row vb (negative: a bad row).
+__device__ __forceinline__ int kept_prefix(const DecodeParams &p, int vb)
 {
-    return p.kept_prefix_rows ? __ldg(p.kept_prefix_rows + b) : p.kept_prefix;
+    return p.kept_prefix_rows ? __ldg(p.kept_prefix_rows + real_row(p, vb)) : p.kept_prefix;
 }
 
 // Geometry of batch row b's tiles (the same for every cache head). Slot j is
@@ -122,9 +170,12 @@ struct RowGeom {
     int L;    // last attended slot
     int lo;   // first slot of the window (0 without one)
     int P;    // kept prefix
-    int nr;   // real tiles
+    int nr;   // real tiles (0: an empty chunk of a multi-token step)
     int tp;   // tiles holding prefix slots below lo
     int gap;  // tiles skipped between them and the window's first tile
+    int nq;   // tokens (query rows / Gh) of the unit: 1 for a single-token form
+    int tokL; // packed index of the token at slot L (single-token forms: b)
+    int Lb;   // first slot holding a new token (single-token decode: L)
 };
 
 __device__ __forceinline__ bool geom_ok(const DecodeParams &p, int L, int P)
@@ -138,19 +189,35 @@ __device__ __forceinline__ bool geom_ok(const DecodeParams &p, int L, int P)
 static __device__ __noinline__ RowGeom row_geom(const DecodeParams &p, int b)
 {
     RowGeom r;
-    r.L = last_slot(p, b);
     r.P = kept_prefix(p, b);
     r.lo = 0;
     r.tp = 0;
     r.gap = 0;
-    if (!geom_ok(p, r.L, r.P)) {
+    if (p.cu_q) {
+        const ChunkInfo ci = chunk_info(p, b);
+        if (ci.nq == 0) {            // an empty chunk: no tiles at all
+            r.L = r.Lb = r.tokL = r.nq = r.nr = 0;
+            return r;
+        }
+        r.nq = max(ci.nq, 0);        // bad token offsets: one tile, no output rows
+        r.L = ci.nq < 0 ? -1 : ci.Lb + ci.i0 + ci.nq - 1;
+        r.tokL = ci.tok0 + ci.i0 + ci.nq - 1;
+        r.Lb = ci.Lb;
+    } else {
+        r.L = last_slot(p, b);
+        r.nq = 1;
+        r.tokL = b;
+        r.Lb = r.L;
+    }
+    if (!geom_ok(p, r.L, r.P) || (p.cu_q && r.Lb < 0)) {
         r.nr = 1;
         return r;
     }
     const int T = p.tile;
     const int last_tile = r.L / T;
     if (p.window > 0) {
-        r.lo = (int)max(0LL, (long long)r.L - p.window + 1);
+        // the window of the unit's first token (the lowest of its rows)
+        r.lo = (int)max(0LL, (long long)r.L - (r.nq - 1) - p.window + 1);
         const int pe = min(r.P, r.lo);                 // prefix slots below the window
         r.tp = (pe + T - 1) / T;
         r.gap = max(0, r.lo / T - r.tp);
@@ -172,7 +239,8 @@ __device__ __forceinline__ bool attended(int L, int lo, int P, int j)
 // tiles, so all CTAs finish together.
 __device__ __forceinline__ int row_tiles(const DecodeParams &p, int b)
 {
-    return row_geom(p, b).nr + p.pad_tiles;
+    const int nr = row_geom(p, b).nr;
+    return nr ? nr + p.pad_tiles : 0;
 }
 
 // CTAs that share the N tiles: min(grid size, N).
@@ -205,6 +273,7 @@ struct TileCursor {
     int L;            // last attended slot of row b (last_slot)
     int lo, P;        // window start and kept prefix of row b (see RowGeom)
     int tp, gap;      // real tile t sits at tile position t (t < tp) or t + gap
+    int nq, tokL, Lb; // multi-token unit: tokens, token at slot L, first new slot
 };
 
 __device__ __forceinline__ void set_row(const DecodeParams &p, TileCursor &c)
@@ -216,6 +285,9 @@ __device__ __forceinline__ void set_row(const DecodeParams &p, TileCursor &c)
     c.nr = r.nr;
     c.tp = r.tp;
     c.gap = r.gap;
+    c.nq = r.nq;
+    c.tokL = r.tokL;
+    c.Lb = r.Lb;
 }
 
 // First slot of the cursor's (real) tile.
@@ -233,7 +305,7 @@ __device__ __forceinline__ TileCursor cursor_at(const DecodeParams &p, int b, lo
     c.end = end;
     c.b = b;
     set_row(p, c);
-    const int nt = c.nr + p.pad_tiles;
+    const int nt = c.nr + p.pad_tiles;   // cursor_at is only used on rows with tiles
     const long long within = g - run;
     c.kvh = (int)(within / nt);
     c.t = (int)(within % nt);
@@ -318,6 +390,7 @@ __device__ inline void schedule_walk(const DecodeParams &p, long long *scratch, 
             none.g = none.end = N;
             none.b = none.kvh = none.t = none.L = 0;
             none.lo = none.P = none.tp = none.gap = 0;
+        none.nq = none.tokL = none.Lb = 0;
             none.nr = 1;
             w.a = w.b = none;
         } else {
@@ -348,8 +421,13 @@ __device__ __forceinline__ void advance(const DecodeParams &p, TileCursor &c)
         if (++c.kvh == p.Hkv) {
             c.kvh = 0;
             ++c.b;
-            if (c.g < c.end)
+            if (c.g < c.end) {
                 set_row(p, c);
+                while (c.nr == 0) {   // empty chunks of a multi-token step hold no tiles
+                    ++c.b;
+                    set_row(p, c);
+                }
+            }
         }
     }
 }
@@ -396,36 +474,39 @@ __device__ __forceinline__ bool walk_first(const DecodeParams &p, TileCursor &c,
 }
 
 // Row-level content check: length in range, slot id in range.
-__device__ __forceinline__ bool row_ok(const DecodeParams &p, int b, int L)
-{
-    if (L < 0 || (long long)L >= row_capacity(p) || kept_prefix(p, b) < 0)
-        return false;
-    if (!p.paged && p.slot_ids) {
-        int r = __ldg(p.slot_ids + b);
-        if (r < 0 || r >= p.R)
-            return false;
-    }
-    return true;
-}
-
+// Content error bits of virtual row b whose last attended slot is L (0: a
+// good row).
 __device__ __forceinline__ int row_error_bits(const DecodeParams &p, int b, int L)
 {
+    if (p.cu_q) {
+        const ChunkInfo ci = chunk_info(p, b);
+        if (ci.nq < 0)
+            return kBadQLen;
+        if (ci.Lb < 0)
+            return kBadLength;
+    }
     if (L < 0 || (long long)L >= row_capacity(p))
         return kBadLength;
     if (kept_prefix(p, b) < 0)
         return kBadPrefix;
     if (!p.paged && p.slot_ids) {
-        int r = __ldg(p.slot_ids + b);
+        int r = __ldg(p.slot_ids + real_row(p, b));
         if (r < 0 || r >= p.R)
             return kBadSlotId;
     }
     return 0;
 }
 
+__device__ __forceinline__ bool row_ok(const DecodeParams &p, int b, int L)
+{
+    return row_error_bits(p, b, L) == 0;
+}
+
 // Element offset of slot s of (b, kvh) in the dense cache, or -1 when the
 // paged table entry that holds it is unusable.
-__device__ __forceinline__ long long slot_offset(const DecodeParams &p, int b, int kvh, int s)
+__device__ __forceinline__ long long slot_offset(const DecodeParams &p, int vb, int kvh, int s)
 {
+    const int b = real_row(p, vb);
     if (!p.paged) {
         long long r = p.slot_ids ? __ldg(p.slot_ids + b) : b;
         return ((r * p.Hkv + kvh) * p.Smax + s) * (long long)p.D;
@@ -474,6 +555,14 @@ __device__ __forceinline__ float sink_log2(const DecodeParams &p, int h)
     return __ldg(p.sink + h) * 1.4426950408889634f;
 }
 
+// Output row of query row g of the cursor's unit: token tokL - (nq - 1 -
+// g / Gh), head kvh * Gh + g % Gh (single-token forms: row b, head kvh*G + g).
+__device__ __forceinline__ float *out_row(const DecodeParams &p, const TileCursor &c, int g, int DD)
+{
+    const long long tok = c.tokL - (c.nq - 1 - g / p.Gh);
+    return p.out + (tok * p.Hq + (long long)c.kvh * p.Gh + g % p.Gh) * DD;
+}
+
 template <int NW, int GP, int DD, int DP, class Sync>
 __device__ inline void finish_segment(const DecodeParams &p, const TileCursor &cur, const TileWalk &walk,
                                       int seg_first_t,
@@ -488,13 +577,13 @@ __device__ inline void finish_segment(const DecodeParams &p, const TileCursor &c
     const int u = b * p.Hkv + kvh;
     const long long P = (long long)u + blockIdx.x;
     const float qnan = __int_as_float(0x7fc00000);
-    float *out = p.out + ((long long)b * p.Hq + (long long)kvh * G) * DD;
+    const int nrow = p.Gh * cur.nq;   // query rows with an output (multi-token: its tokens)
     if (tid < G) {
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < NW; ++w)
             M = fmaxf(M, sm_m[w][tid]);
-        const float sk = (whole && p.sink) ? sink_log2(p, kvh * G + tid) : -INFINITY;
+        const float sk = (whole && p.sink) ? sink_log2(p, kvh * p.Gh + tid % p.Gh) : -INFINITY;
         M = fmaxf(M, sk);
         float den = (sk == -INFINITY) ? 0.f : fast_ex2(sk - M);
 #pragma unroll
@@ -537,10 +626,13 @@ __device__ inline void finish_segment(const DecodeParams &p, const TileCursor &c
 #pragma unroll
                 for (int e = 0; e < V; ++e)
                     acc[e] = bad ? qnan : acc[e] * inv;
-                if constexpr (V == 4)
-                    *reinterpret_cast<float4 *>(out + idx) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-                else
-                    out[idx] = acc[0];
+                if (g < nrow) {
+                    float *o = out_row(p, cur, g, DD) + d;
+                    if constexpr (V == 4)
+                        *reinterpret_cast<float4 *>(o) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                    else
+                        *o = acc[0];
+                }
             } else {
                 float *po = p.ws_o + (P * G + g) * DD + d;
 #pragma unroll
@@ -586,7 +678,7 @@ __device__ inline void finish_segment(const DecodeParams &p, const TileCursor &c
                 float M = -INFINITY;
                 for (int i = 0; i < K; ++i)
                     M = fmaxf(M, mb.w[i * G + tid]);
-                const float sk = p.sink ? sink_log2(p, kvh * G + tid) : -INFINITY;
+                const float sk = p.sink ? sink_log2(p, kvh * p.Gh + tid % p.Gh) : -INFINITY;
                 M = fmaxf(M, sk);
                 float den = (sk == -INFINITY) ? 0.f : fast_ex2(sk - M);
                 for (int i = 0; i < K; ++i) {
@@ -620,9 +712,12 @@ __device__ inline void finish_segment(const DecodeParams &p, const TileCursor &c
                         *po = 0.f;     // consumed: leave the workspace zero-filled
                     }
                 }
+                if (g < nrow) {
+                    float *o = out_row(p, cur, g, DD) + (idx - g * DD);
 #pragma unroll
-                for (int e = 0; e < V; ++e)
-                    out[idx + e] = acc[e] * mb.inv_den[g];
+                    for (int e = 0; e < V; ++e)
+                        o[e] = acc[e] * mb.inv_den[g];
+                }
             }
         } else {
             for (int idx = tid; idx < G * DD; idx += nthr) {
@@ -630,7 +725,7 @@ __device__ inline void finish_segment(const DecodeParams &p, const TileCursor &c
                 float M = -INFINITY;
                 for (int i = 0; i < K; ++i)
                     M = fmaxf(M, __ldcg(p.ws_ml + ((P0 + i) * G + g) * 2));
-                const float sk = p.sink ? sink_log2(p, kvh * G + g) : -INFINITY;
+                const float sk = p.sink ? sink_log2(p, kvh * p.Gh + g % p.Gh) : -INFINITY;
                 M = fmaxf(M, sk);
                 float num = 0.f, den = (sk == -INFINITY) ? 0.f : fast_ex2(sk - M);
                 for (int i = 0; i < K; ++i) {
@@ -641,7 +736,8 @@ __device__ inline void finish_segment(const DecodeParams &p, const TileCursor &c
                     den = fmaf(a, __ldcg(p.ws_ml + (Q * G + g) * 2 + 1), den);
                     *po = 0.f;       // consumed: leave the workspace zero-filled
                 }
-                out[idx] = num / den;
+                if (g < nrow)
+                    out_row(p, cur, g, DD)[d] = num / den;
             }
         }
         sync();

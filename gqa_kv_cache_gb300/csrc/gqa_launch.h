@@ -30,6 +30,6 @@ cudaError_t tc_launch(const DecodeParams &p, const TcMaps &maps, cudaStream_t st
 cudaError_t validate_launch(const int32_t *lengths, const int32_t *slot_ids,
                             const int32_t *block_table, int B, int R, int Smax,
                             int num_blocks, int block_size, int max_blocks, int attend,
-                            int32_t *d_result, cudaStream_t st);
+                            const int32_t *cu_q, int T, int32_t *d_result, cudaStream_t st);
 
 }  // namespace gqa

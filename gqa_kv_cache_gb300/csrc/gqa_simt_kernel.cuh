@@ -16,6 +16,9 @@
 // k_new/v_new directly and written into the cache by the lane group that
 // reads it; no thread reads the cache at slot L, so the append cannot race.
 // The read-only attend reads slot L from the cache and writes nothing but out.
+// In a multi-token step every slot from the row's write offset on is a new
+// token, read from k_new / v_new (and appended by the chunk that owns it), and
+// each query row (token, head) is masked beyond its own token's position.
 #pragma once
 
 #include "gqa_common.cuh"
@@ -154,6 +157,7 @@ __global__ void __launch_bounds__(kThreads) simt_decode_kernel(const DecodeParam
 
     float q[GP][VEC];
     float m[GP], l[GP], o[GP][VEC];
+    int lim[GP];                  // each query row's last attended slot
     int seg_first_t = 0;
     bool row_good = true;
     bool seg_start = true;
@@ -166,16 +170,20 @@ __global__ void __launch_bounds__(kThreads) simt_decode_kernel(const DecodeParam
             row_good = row_ok(p, b, L);
             if (!row_good && tid == 0 && cur.t == 0 && kvh == 0)
                 report(p, row_error_bits(p, b, L));
+            const int qrows = p.cu_q ? p.Gh * cur.nq : G;   // query rows with data
 #pragma unroll
             for (int g = 0; g < GP; ++g) {
                 m[g] = -INFINITY;
                 l[g] = 0.f;
+                lim[g] = p.cu_q ? L - (cur.nq - 1 - g / p.Gh) : L;
 #pragma unroll
                 for (int e = 0; e < VEC; ++e)
                     o[g][e] = 0.f;
-                if (g < G) {
+                if (g < qrows) {
                     float tmp[VEC];
-                    load_q<VEC>(p, ((long long)b * p.Hq + kvh * G + g) * D + li * VEC, tmp);
+                    // row g: token tok, head kvh * Gh + g % Gh
+                    const long long tok = p.cu_q ? cur.tokL - (cur.nq - 1 - g / p.Gh) : b;
+                    load_q<VEC>(p, (tok * p.Hq + (long long)kvh * p.Gh + g % p.Gh) * D + li * VEC, tmp);
 #pragma unroll
                     for (int e = 0; e < VEC; ++e)
                         q[g][e] = tmp[e] * p.scale_log2;
@@ -191,7 +199,8 @@ __global__ void __launch_bounds__(kThreads) simt_decode_kernel(const DecodeParam
         if (row_good) {
             const int s0 = tile_slot0(cur, p.tile);
             const int s1 = min(s0 + p.tile, L + 1);
-            const long long new_off = ((long long)b * p.Hkv + kvh) * D + li * VEC;
+            // slots from here on are new tokens (none in the read-only attend)
+            const int first_new = p.attend ? INT_MAX : (p.cu_q ? cur.Lb : L);
             // warp-uniform trip count: every lane takes part in the shuffles
             for (int jb = s0 + warp * SPW; jb < s1; jb += STREAMS) {
                 const int j = jb + lg;
@@ -200,26 +209,31 @@ __global__ void __launch_bounds__(kThreads) simt_decode_kernel(const DecodeParam
                 for (int e = 0; e < VEC; ++e)
                     kv[e] = vv[e] = 0.f;
                 bool use = false;
-                if ((j < L || (p.attend && j == L)) && attended(L, cur.lo, cur.P, j)) {
-                    long long off = slot_offset(p, b, kvh, j);
-                    if (off < 0) {
-                        bad_local = 1;
-                    } else {
-                        load_vec<T, VEC>(kc + off + li * VEC, kv);
-                        load_vec<T, VEC>(vc + off + li * VEC, vv);
-                        use = true;
+                if (j < first_new) {
+                    if (attended(L, cur.lo, cur.P, j)) {
+                        long long off = slot_offset(p, b, kvh, j);
+                        if (off < 0) {
+                            bad_local = 1;
+                        } else {
+                            load_vec<T, VEC>(kc + off + li * VEC, kv);
+                            load_vec<T, VEC>(vc + off + li * VEC, vv);
+                            use = true;
+                        }
                     }
-                } else if (j == L) {  // the new token, and its in-place append
+                } else if (j <= L) {  // a new token, and its in-place append
+                    const long long tok = p.cu_q ? cur.tokL - (L - j) : b;
+                    const long long new_off = (tok * p.Hkv + kvh) * D + li * VEC;
                     load_vec<T, VEC>(static_cast<const T *>(p.k_new) + new_off, kv);
                     load_vec<T, VEC>(static_cast<const T *>(p.v_new) + new_off, vv);
                     use = true;
-                    long long off = slot_offset(p, b, kvh, L);
+                    // appended by the unit that owns the token
+                    long long off = (!p.cu_q || j > L - cur.nq) ? slot_offset(p, b, kvh, j) : -2;
                     if (off >= 0) {
                         copy_vec<T, VEC>(static_cast<T *>(p.k_cache) + off + li * VEC,
                                          static_cast<const T *>(p.k_new) + new_off);
                         copy_vec<T, VEC>(static_cast<T *>(p.v_cache) + off + li * VEC,
                                          static_cast<const T *>(p.v_new) + new_off);
-                    } else {
+                    } else if (off == -1) {
                         bad_local = 1;
                     }
                 }
@@ -238,6 +252,9 @@ __global__ void __launch_bounds__(kThreads) simt_decode_kernel(const DecodeParam
                 if (use) {
 #pragma unroll
                     for (int g = 0; g < GP; ++g) {
+                        // row g's own causal bound and window
+                        if (j > lim[g] || (p.window > 0 && j <= lim[g] - p.window && j >= cur.P))
+                            continue;
                         float mn = fmaxf(m[g], s[g]);
                         float alpha = ex2(m[g] - mn);  // m = -inf gives 0
                         float pj = ex2(s[g] - mn);

@@ -34,6 +34,11 @@
 //    before the product (0 * NaN would not be 0). A window skips whole tiles
 //    (the schedule lists only tiles holding attended slots) and, for paged
 //    caches, whole blocks.
+//  * multi-token steps (MULTI): a unit is a chunk of up to 8 / G tokens of a
+//    row; its query rows are (token, head) pairs gathered by one bulk copy per
+//    token, each row is masked beyond its own token's position, every slot
+//    holding a new token is substituted from k_new / v_new as below, and the
+//    chunk appends its own tokens.
 //  * the new token (decode step only; the read-only attend reads slot L from
 //    the cache like any other): in the tile that holds slot L the owning warp writes
 //    k_new / v_new into the ring slot of row L (the TMA copy of the stale
@@ -205,8 +210,9 @@ __device__ __forceinline__ void consumer_sync()
 }
 
 // WIN: a sliding window is in force. Without one the window fields of the
-// cursor are never read, so they take no registers and no code.
-template <bool QF32, bool WIN>
+// cursor are never read, so they take no registers and no code. MULTI: a
+// multi-token step (the chunk fields of the cursor are read only then).
+template <bool QF32, bool WIN, bool MULTI>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     tc_decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap mk,
                      const __grid_constant__ CUtensorMap mv)
@@ -268,9 +274,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             if (!r.good)
                 return r;
             const int slot0 = WIN ? tile_slot0(c, kTile) : c.t * kTile;
+            const int rb = MULTI ? real_row(p, c.b) : c.b;   // the batch row
             if (!p.paged) {
                 if (lane == 0) {
-                    const int row = p.slot_ids ? __ldg(p.slot_ids + c.b) : c.b;
+                    const int row = p.slot_ids ? __ldg(p.slot_ids + rb) : rb;
                     r.z = row * p.Hkv + c.kvh;
                     r.y = slot0;
                 }
@@ -278,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 const int s = slot0 + lane * box_rows;  // first slot this lane copies
                 // a block is copied when it holds an attended slot
                 if (s <= c.L && (!WIN || s + box_rows - 1 >= c.lo || s < c.P)) {
-                    const int e = __ldg(p.block_table + (long long)c.b * p.max_blocks + s / bs);
+                    const int e = __ldg(p.block_table + (long long)rb * p.max_blocks + s / bs);
                     if (e >= 0 && e < p.num_blocks) {
                         r.z = e * p.Hkv + c.kvh;
                         r.y = s % bs;
@@ -307,17 +314,32 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             // the first tile of each of this CTA's unit segments also brings
             // the unit's G query rows (contiguous in q)
             const bool seg_first = pl.good && (cur.t == 0 || cur.g == range_start);
-            const uint32_t qbytes = seg_first ? (uint32_t)(G * kD * Ring<QF32>::kQElem) : 0u;
+            const int qrows = MULTI ? p.Gh * cur.nq : G;   // query rows with data
+            const uint32_t qbytes = seg_first ? (uint32_t)(qrows * kD * Ring<QF32>::kQElem) : 0u;
             const uint32_t bytes = (uint32_t)__popc(copying) * 4u * (uint32_t)box_rows * 128u + qbytes;
             const uint32_t fb = smem_u32(&sh.full[stage]);
             if (lane == 0) {
                 sh.stage_bad[stage] = any_bad ? 1 : 0;
                 mbar_arrive_tx(fb, bytes);
-                if (qbytes)
-                    bulk_load(ring_u32 + stage * kStageBytes + 4 * kHalfBytes,
-                              static_cast<const uint8_t *>(p.q) +
-                                  ((long long)b * p.Hq + (long long)kvh * G) * kD * Ring<QF32>::kQElem,
-                              qbytes, fb);
+                if (qbytes) {
+                    const uint32_t qdst = ring_u32 + stage * kStageBytes + 4 * kHalfBytes;
+                    if constexpr (MULTI) {
+                        // one copy per token: its Gh heads are contiguous in q
+                        const uint32_t tb = (uint32_t)(p.Gh * kD * Ring<QF32>::kQElem);
+                        for (int i = 0; i < cur.nq; ++i) {
+                            const long long tok = cur.tokL - (cur.nq - 1 - i);
+                            bulk_load(qdst + i * tb,
+                                      static_cast<const uint8_t *>(p.q) +
+                                          (tok * p.Hq + (long long)kvh * p.Gh) * kD * Ring<QF32>::kQElem,
+                                      tb, fb);
+                        }
+                    } else {
+                        bulk_load(qdst,
+                                  static_cast<const uint8_t *>(p.q) +
+                                      ((long long)b * p.Hq + (long long)kvh * G) * kD * Ring<QF32>::kQElem,
+                                  qbytes, fb);
+                    }
+                }
             }
             __syncwarp();
             if (pl.z >= 0) {
@@ -370,6 +392,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     int seg_first_t = 0;
     bool seg_start = true, row_good = true, aborted = false;
     int seg_bad = 0;
+    int lim = 0, lo_r = 0, qrows = G;    // this lane's row g0: last slot, window start; rows with data
 
     while (more) {
         const int b = cur.b, kvh = cur.kvh, L = cur.L;
@@ -386,6 +409,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             l_run = 0.f;
             seg_bad = 0;
             seg_start = false;
+            lim = L;
+            if constexpr (MULTI) {
+                lim = L - (cur.nq - 1 - g0 / p.Gh);   // row g0 is token g0 / Gh of the chunk
+                qrows = p.Gh * cur.nq;
+            }
+            if constexpr (WIN)
+                lo_r = max(0, lim - p.window + 1);
         }
 
         // After an abort every warp keeps walking its tiles and taking part in
@@ -416,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     qa[ks][0] = qa[ks][1] = ql[ks][0] = ql[ks][1] = 0u;
-                    if (g0 < G) {
+                    if (g0 < qrows) {
                         split_bf16(*reinterpret_cast<const float2 *>(qs + 16 * ks + 2 * q4), qa[ks][0], ql[ks][0]);
                         split_bf16(*reinterpret_cast<const float2 *>(qs + 16 * ks + 8 + 2 * q4), qa[ks][1],
                                    ql[ks][1]);
@@ -426,33 +456,47 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 const uint8_t *qs = kring + 4 * kHalfBytes + g0 * (kD * 2);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
-                    qa[ks][0] = (g0 < G) ? *reinterpret_cast<const uint32_t *>(qs + (16 * ks + 2 * q4) * 2) : 0u;
-                    qa[ks][1] = (g0 < G) ? *reinterpret_cast<const uint32_t *>(qs + (16 * ks + 8 + 2 * q4) * 2) : 0u;
+                    qa[ks][0] = (g0 < qrows) ? *reinterpret_cast<const uint32_t *>(qs + (16 * ks + 2 * q4) * 2) : 0u;
+                    qa[ks][1] = (g0 < qrows) ? *reinterpret_cast<const uint32_t *>(qs + (16 * ks + 8 + 2 * q4) * 2) : 0u;
                 }
             }
         }
 
         if (have && row_good && !tile_bad) {
             const bool last_tile = (cur.t == cur.nr - 1);
-            // tiles that hold slots outside the softmax: the last one (beyond
-            // L) and, with a window, those below its start
-            const bool partial = last_tile || (WIN && slot0 < cur.lo);
+            // tiles holding new tokens: the last one; in a multi-token step
+            // every tile reaching the row's write offset
+            const bool newt = MULTI ? (slot0 + kTile - 1 >= cur.Lb) : last_tile;
+            // tiles that hold slots outside some row's softmax: those, and,
+            // with a window, those below the last row's window start
+            const bool partial = newt || (WIN && slot0 < max(0, L - p.window + 1));
             if (partial) {
-                // row L of the last tile: the new token; rows not attended: zero V
-                const int lr = L - slot0;            // 0..63 in the last tile
-                if (last_tile && !p.attend && lr >= row0 && lr < row0 + 16) {
-                    const long long nidx = ((long long)b * p.Hkv + kvh) * kD;
-                    const int c = lane & 15;          // 16-byte chunk of the row
-                    const int half = c >> 3, c8 = c & 7;
-                    const uint4 *src = reinterpret_cast<const uint4 *>((lane < 16 ? knew : vnew) + nidx) + c;
-                    const uint4 v = __ldg(src);
-                    uint8_t *dst = (lane < 16 ? kring : vring) + half * kHalfBytes + swz(lr, c8);
-                    *reinterpret_cast<uint4 *>(dst) = v;
-                    // the in-place append
-                    const long long off = slot_offset(p, b, kvh, L);
-                    if (off >= 0) {
-                        __nv_bfloat16 *cache = static_cast<__nv_bfloat16 *>(lane < 16 ? p.k_cache : p.v_cache);
-                        reinterpret_cast<uint4 *>(cache + off)[c] = v;
+                // new-token rows: substituted from k_new / v_new (and appended
+                // by the unit owning the token); rows no query row attends:
+                // zero V
+                if (newt && !p.attend) {
+                    // this warp's rows holding new tokens (slot L only, for a
+                    // single-token step)
+                    const int first_new = MULTI ? max(cur.Lb, slot0 + row0) : max(L, slot0 + row0);
+                    const int last_new = min(L, slot0 + row0 + 15);
+                    for (int sn = first_new; sn <= last_new; ++sn) {
+                        const int lr = sn - slot0;
+                        const long long tok = MULTI ? cur.tokL - (L - sn) : b;
+                        const long long nidx = (tok * p.Hkv + kvh) * kD;
+                        const int c = lane & 15;          // 16-byte chunk of the row
+                        const int half = c >> 3, c8 = c & 7;
+                        const uint4 *src = reinterpret_cast<const uint4 *>((lane < 16 ? knew : vnew) + nidx) + c;
+                        const uint4 v = __ldg(src);
+                        uint8_t *dst = (lane < 16 ? kring : vring) + half * kHalfBytes + swz(lr, c8);
+                        *reinterpret_cast<uint4 *>(dst) = v;
+                        // the in-place append, by the unit that owns the token
+                        if (!MULTI || sn > L - cur.nq) {
+                            const long long off = slot_offset(p, b, kvh, sn);
+                            if (off >= 0) {
+                                __nv_bfloat16 *cache = static_cast<__nv_bfloat16 *>(lane < 16 ? p.k_cache : p.v_cache);
+                                reinterpret_cast<uint4 *>(cache + off)[c] = v;
+                            }
+                        }
                     }
                 }
                 for (int r = row0 + (lane >> 4); r < row0 + 16; r += 2) {
@@ -504,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     float sc = s_acc[nt][e];
                     if constexpr (QF32)
                         sc += s_acc[nt][e + 2];   // row g0 + 8: the query remainder
-                    const bool on = WIN ? attended(L, cur.lo, cur.P, j) : j <= L;
+                    const bool on = WIN ? attended(lim, lo_r, cur.P, j) : j <= lim;
                     x[nt][e] = (!partial || on) ? sc * p.scale_log2 : -INFINITY;
                     mx = fmaxf(mx, x[nt][e]);
                 }
@@ -617,13 +661,13 @@ size_t tc_smem_bytes(bool q_bf16)
 }
 
 namespace {
-template <bool QF32, bool WIN>
+template <bool QF32, bool WIN, bool MULTI>
 cudaError_t launch_q(const DecodeParams &p, const TcMaps &maps, cudaStream_t st)
 {
     constexpr int kDynSmem = Ring<QF32>::kDynSmem;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(tc_decode_kernel<QF32, WIN>,
+        cudaError_t e = cudaFuncSetAttribute(tc_decode_kernel<QF32, WIN, MULTI>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem);
         if (e != cudaSuccess)
             return e;
@@ -639,16 +683,21 @@ cudaError_t launch_q(const DecodeParams &p, const TcMaps &maps, cudaStream_t st)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tc_decode_kernel<QF32, WIN>, p, maps.k, maps.v);
+    return cudaLaunchKernelEx(&cfg, tc_decode_kernel<QF32, WIN, MULTI>, p, maps.k, maps.v);
 }
 }  // namespace
 
 cudaError_t tc_launch(const DecodeParams &p, const TcMaps &maps, cudaStream_t st)
 {
     const bool win = p.window > 0;
+    if (p.cu_q) {   // multi-token steps have a bfloat16 query
+        if (!p.q_bf16)
+            return cudaErrorInvalidValue;
+        return win ? launch_q<false, true, true>(p, maps, st) : launch_q<false, false, true>(p, maps, st);
+    }
     if (p.q_bf16)
-        return win ? launch_q<false, true>(p, maps, st) : launch_q<false, false>(p, maps, st);
-    return win ? launch_q<true, true>(p, maps, st) : launch_q<true, false>(p, maps, st);
+        return win ? launch_q<false, true, false>(p, maps, st) : launch_q<false, false, false>(p, maps, st);
+    return win ? launch_q<true, true, false>(p, maps, st) : launch_q<true, false, false>(p, maps, st);
 }
 
 }  // namespace gqa

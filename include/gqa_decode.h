@@ -82,7 +82,9 @@ enum {
     GQA_STATUS_BAD_BLOCK = 4,       /* block-table entry outside [0, num_blocks) or -1
                                        where a slot 0..lengths[b] lives                   */
     GQA_STATUS_TIMEOUT = 8,         /* a bounded on-chip wait gave up (never expected)    */
-    GQA_STATUS_BAD_PREFIX = 16      /* kept_prefix_rows[b] < 0                            */
+    GQA_STATUS_BAD_PREFIX = 16,     /* kept_prefix_rows[b] < 0                            */
+    GQA_STATUS_BAD_QLEN = 32        /* multi-token: cu_q[b] / cu_q[b+1] outside [0, T],
+                                       decreasing, or q_len above max_q_len             */
 };
 
 /* Kernel choice for the *_ex entry points. */
@@ -277,6 +279,65 @@ gqa_status gqa_validate_attend(const int32_t *lengths, const int32_t *slot_ids,
                                const int32_t *block_table, int B, int R, int Smax,
                                int num_blocks, int block_size, int max_blocks,
                                int32_t *d_result, void *stream);
+
+/*
+ * Multi-token step (speculative or chunked decode): batch row b brings
+ * q_len[b] = cu_q[b+1] - cu_q[b] new tokens, the packed rows cu_q[b] ..
+ * cu_q[b+1]-1 of q, k_new, v_new and out. They are appended in place at slots
+ * lengths[b] .. lengths[b] + q_len[b] - 1, and the query heads of token i
+ * attend slots 0 .. lengths[b] + i of their cache head, the new tokens up to
+ * their own included ("groupQueryAttention": q/k/v are packed [sum S,
+ * heads * head_dim]; each row's write offset is cu_seqlens_k[b] - q_len[b],
+ * i.e. lengths[b]; the append is in place; keys beyond the query's own
+ * position are outside the causal bound). q_len = 1 everywhere is exactly
+ * gqa_decode_step.
+ *
+ *  q        (device) (T, Hq, D)          queries of the new tokens
+ *  k_new    (device) (T, Hkv, D)         their keys   (appended)
+ *  v_new    (device) (T, Hkv, D)         their values (appended)
+ *  lengths  (device) (B,) int32          write offset of row b (tokens already cached);
+ *                                        0 <= lengths[b], lengths[b] + q_len[b] <= capacity
+ *  cu_q     (device) (B + 1,) int32      cu_q[0] = 0, nondecreasing, cu_q[B] = T
+ *  max_q_len (host)  bound on every q_len[b] (sizes the schedule and workspace;
+ *                    a larger q_len makes the row bad: GQA_STATUS_BAD_QLEN and
+ *                    its outputs are not written)
+ *  out      (device) (T, Hq, D) float32
+ *  Other arguments as in gqa_decode_step / gqa_decode_step_paged (the same
+ *  softmax modifiers apply, each token with its own position). The workspace
+ *  is gqa_workspace_bytes_multi(...). A bad row (length, slot id, block) gets
+ *  NaN outputs for its tokens and its appends are skipped where their slots
+ *  cannot be addressed. Rows with q_len = 0 are left alone.
+ * Kernels: up to 8 / G tokens of a row (G = Hq / Hkv <= 8) share one pass over
+ * the cache; longer runs are cut into chunks, each streaming the cache
+ * again.
+ */
+size_t gqa_workspace_bytes_multi(int B, int Hq, int Hkv, int D, gqa_dtype dt, int max_q_len,
+                                 const gqa_options *opt);
+
+gqa_status gqa_decode_multi(const void *q, const void *k_new, const void *v_new,
+                            void *k_cache, void *v_cache, const int32_t *lengths,
+                            const int32_t *cu_q, const int32_t *slot_ids, float *out,
+                            int B, int T, int max_q_len, int Hq, int Hkv, int D, int R, int Smax,
+                            gqa_dtype dt, void *workspace, size_t workspace_bytes,
+                            int32_t *d_status, void *stream, const gqa_options *opt);
+
+gqa_status gqa_decode_multi_paged(const void *q, const void *k_new, const void *v_new,
+                                  void *k_blocks, void *v_blocks, const int32_t *block_table,
+                                  const int32_t *lengths, const int32_t *cu_q, float *out,
+                                  int B, int T, int max_q_len, int Hq, int Hkv, int D,
+                                  int num_blocks, int block_size, int max_blocks, gqa_dtype dt,
+                                  void *workspace, size_t workspace_bytes, int32_t *d_status,
+                                  void *stream, const gqa_options *opt);
+
+/*
+ * gqa_validate for a multi-token step: the cu_q rules above, 0 <= lengths[b],
+ * lengths[b] + q_len[b] <= Smax (dense) and, paged, the table rules with real
+ * blocks for slots 0 .. lengths[b] + q_len[b] - 1. Synchronous.
+ */
+gqa_status gqa_validate_multi(const int32_t *lengths, const int32_t *cu_q, const int32_t *slot_ids,
+                              const int32_t *block_table, int B, int T, int R, int Smax,
+                              int num_blocks, int block_size, int max_blocks, int32_t *d_result,
+                              void *stream);
 
 /*
  * Kernel timing trace. When enabled, every decode call records CUDA events

@@ -1,0 +1,202 @@
+"""GPU parity of the multi-token step (speculative / chunked decode): the
+packed tokens cu_q[b] .. cu_q[b+1]-1 of row b are appended in place at slots
+lengths[b] + i and token i attends slots 0 .. lengths[b] + i
+("groupQueryAttention": packed q/k/v, write offset cu_seqlens_k[b] - q_len[b],
+the causal bound). Against the CPU oracle on the same seeded inputs, both
+kernels, dense / slot_ids / paged, group sizes 1..8 (tokens per chunk 8..1),
+rows with q_len 0, chunks crossing tiles, the softmax modifiers; the whole
+cache is compared with the oracle's appended host copy bit for bit. Bars:
+float32 1e-5; bfloat16 2e-2 max|V|."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from gpu_cases import BF16_REL_TOL, F32_TOL
+from helpers import to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def _tc_ok(w):
+    return w.dtype == "bf16" and w.D == 128 and (
+        not w.paged or (w.block_size >= 8 and (w.block_size & (w.block_size - 1)) == 0))
+
+
+def _run_gpu(w, t, max_q, kernel="auto", grid=0, status=None, **mods):
+    import gqa_kv_cache_gb300 as gqa
+    kw = dict(max_q_len=max_q, kernel=kernel, grid_ctas=grid, status=status, **mods)
+    if w.paged:
+        return gqa.decode_multi_paged(t["q"], t["k_new"], t["v_new"], t["k_blocks"], t["v_blocks"],
+                                      t["block_table"], t["lengths"], t["cu_q"], **kw)
+    return gqa.decode_multi(t["q"], t["k_new"], t["v_new"], t["k_cache"], t["v_cache"], t["lengths"],
+                            t["cu_q"], t.get("slot_ids"), **kw)
+
+
+def _run_oracle(w, a, **mods):
+    om = {}
+    if mods.get("sink") is not None:
+        om["sink"] = mods["sink"].cpu().numpy()
+    om["window"] = mods.get("window", 0)
+    om["kept_prefix"] = mods.get("kept_prefix", 0)
+    if w.paged:
+        r = oracle.decode_multi_paged(a["q"], a["k_new"], a["v_new"], a["k_blocks"], a["v_blocks"],
+                                      a["block_table"], a["lengths"], a["cu_q"], **om)
+    else:
+        r = oracle.decode_multi_dense(a["q"], a["k_new"], a["v_new"], a["k_cache"], a["v_cache"],
+                                      a["lengths"], a["cu_q"], a.get("slot_ids"), **om)
+    assert r.status == oracle.OK
+    return r.out
+
+
+def _vmax(a):
+    v = a["v_blocks"] if "v_blocks" in a else a["v_cache"]
+    f = lambda x: (x.astype(np.uint32) << 16).view(np.float32) if x.dtype == np.uint16 else x
+    return float(max(np.abs(f(v)).max(), np.abs(f(a["v_new"])).max()))
+
+
+def check_multi(w, q_lens, kernel="auto", grid=0, **mods):
+    t = {k: v.cuda() for k, v in W.generate(w, q_lens=q_lens).items()}
+    a = {k: to_np(v) for k, v in t.items()}
+    max_q = max(max(q_lens), 1)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = _run_gpu(w, t, max_q, kernel, grid, st, **mods)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, f"device status {int(st.item())}"
+    want = _run_oracle(w, a, **mods)          # appends into the host copies
+    got = out.double().cpu().numpy()
+    assert np.isfinite(got).all()
+    tol = F32_TOL if w.dtype == "f32" else BF16_REL_TOL * _vmax(a)
+    err = float(np.abs(got - want).max()) if got.size else 0.0
+    assert err <= tol, f"max abs error {err} > {tol}"
+    for n in (("k_blocks", "v_blocks") if w.paged else ("k_cache", "v_cache")):
+        assert to_np(t[n]).tobytes() == a[n].tobytes(), f"{n} differs from the oracle's appended copy"
+    return err
+
+
+CASES = [
+    # name, workload family, sizes, q_lens (chunks of 8 / G tokens)
+    ("g4", "llama3_8b", dict(B=6, Smax=300, len_lo=0, len_hi=290, seed=401), [1, 2, 3, 0, 5, 8]),
+    ("g8", "long_context", dict(B=4, Smax=400, len_lo=50, len_hi=390, seed=402), [3, 1, 6, 2]),
+    ("g2", "llama3_8b", dict(Hq=4, Hkv=2, B=4, Smax=260, len_lo=0, len_hi=250, seed=403), [4, 7, 1, 9]),
+    ("g1", "llama3_8b", dict(Hq=2, Hkv=2, B=3, Smax=200, len_lo=0, len_hi=190, seed=404), [8, 13, 2]),
+    ("g6_paged16", "paged", dict(B=4, num_blocks=4 * 30, max_blocks=30, len_lo=0, len_hi=470, seed=405), [2, 4, 1, 3]),
+    ("g3", "llama3_8b", dict(Hq=6, Hkv=2, B=3, Smax=300, len_lo=0, len_hi=290, seed=406), [5, 2, 4]),
+    ("g8_slots", "ragged_slots", dict(B=5, R=9, Smax=300, len_lo=1, len_hi=290, seed=407), [2, 3, 1, 4, 2]),
+    ("g4_paged8", "paged", dict(Hq=8, Hkv=2, B=3, block_size=8, num_blocks=3 * 40, max_blocks=40,
+                                len_lo=0, len_hi=310, seed=408), [3, 6, 2]),
+    ("f32_d64", "pr1_fp32", dict(B=3, Smax=256, len_lo=0, len_hi=250, seed=409), [3, 1, 4]),
+]
+
+
+@pytest.mark.parametrize("kernel", ["simt", "tc"])
+@pytest.mark.parametrize("name,base,kw,q_lens", CASES, ids=[c[0] for c in CASES])
+@pytest.mark.parametrize("grid", [0, 7])
+def test_multi_small_cases(name, base, kw, q_lens, kernel, grid):
+    w = W.small(base, **kw)
+    if kernel == "tc" and not _tc_ok(w):
+        pytest.skip("kernel does not take these sizes")
+    check_multi(w, q_lens, kernel, grid)
+
+
+@pytest.mark.parametrize("kernel", ["simt", "tc"])
+def test_multi_with_window_and_sink(kernel):
+    w = W.small("llama3_8b", B=4, Smax=500, len_lo=100, len_hi=490, seed=410)
+    g = torch.Generator().manual_seed(3)
+    check_multi(w, [3, 4, 1, 2], kernel, 0, window=70, kept_prefix=9,
+                sink=(torch.randn(w.Hq, generator=g)).cuda())
+
+
+@pytest.mark.parametrize("kernel", ["simt", "tc"])
+def test_multi_q_len_one_matches_decode_step(kernel):
+    """q_len = 1 everywhere is the decode step: the same bits."""
+    import gqa_kv_cache_gb300 as gqa
+    w = W.small("llama3_8b", B=5, Smax=600, len_lo=0, len_hi=590, seed=411)
+    t = {k: v.cuda() for k, v in W.generate(w, q_lens=[1] * w.B).items()}
+    t2 = {k: v.clone() for k, v in t.items()}
+    a = _run_gpu(w, t, 1, kernel).clone()
+    b = gqa.decode_step(t2["q"], t2["k_new"], t2["v_new"], t2["k_cache"], t2["v_cache"], t2["lengths"],
+                        kernel=kernel)
+    assert torch.equal(a, b)
+    assert torch.equal(t["k_cache"], t2["k_cache"]) and torch.equal(t["v_cache"], t2["v_cache"])
+
+
+@pytest.mark.parametrize("kernel", ["simt", "tc"])
+def test_multi_bad_rows(kernel):
+    """A q_len above max_q_len and a write offset that does not leave room
+    for the tokens: status bits, NaN (or nothing) for those rows only."""
+    w = W.small("llama3_8b", B=3, Smax=128, len_lo=10, len_hi=100, seed=412)
+    t = {k: v.cuda() for k, v in W.generate(w, q_lens=[2, 5, 2]).items()}
+    t["lengths"][2] = 127                     # 127 + 2 > 128
+    out = torch.full((int(t["cu_q"][-1]), w.Hq, w.D), 7.0, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    import gqa_kv_cache_gb300 as gqa
+    gqa.decode_multi(t["q"], t["k_new"], t["v_new"], t["k_cache"], t["v_cache"], t["lengths"], t["cu_q"],
+                     max_q_len=4, out=out, status=st, kernel=kernel)
+    torch.cuda.synchronize()
+    s = int(st.item())
+    assert s & 32 and s & 1
+    assert torch.isfinite(out[0:2]).all()               # row 0
+    assert (out[2:7] == 7.0).all()                      # row 1: q_len 5 > 4, not written
+    assert torch.isnan(out[7:9]).all()                  # row 2: bad length
+    assert not gqa.validate_multi(t["lengths"], t["cu_q"], 9, R=w.B, Smax=w.Smax)
+
+
+def test_validate_multi_matches_oracle_rules():
+    import gqa_kv_cache_gb300 as gqa
+    rng = np.random.default_rng(2)
+    for trial in range(60):
+        B, T = 3, 7
+        cu = np.sort(rng.integers(0, T + 1, size=B + 1)).astype(np.int32)
+        if trial % 2:
+            cu[0], cu[-1] = 0, T
+        if trial % 5 == 0:
+            cu[1], cu[2] = cu[2], cu[1]
+        L = rng.integers(-1, 15, size=B).astype(np.int32)
+        want = oracle.validate_multi_dense(L, cu, None, T, 3, 16) == oracle.OK
+        got = gqa.validate_multi(torch.from_numpy(L).cuda(), torch.from_numpy(cu).cuda(), T, R=3, Smax=16)
+        assert got == want, (trial, cu, L)
+        bt = rng.integers(-2, 17, size=(B, 5)).astype(np.int32)
+        if trial % 3 == 0:
+            bt = rng.permutation(16)[:B * 5].reshape(B, 5).astype(np.int32)
+        want = oracle.validate_multi_paged(L, cu, bt, T, 16, 4) == oracle.OK
+        got = gqa.validate_multi(torch.from_numpy(L).cuda(), torch.from_numpy(cu).cuda(), T,
+                                 block_table=torch.from_numpy(bt).cuda(), num_blocks=16, block_size=4)
+        assert got == want, (trial, cu, L, bt)
+
+
+@pytest.mark.parametrize("name,q_len", [("llama3_8b", 2), ("llama3_8b", 4), ("paged", 3)])
+def test_multi_full_size(name, q_len):
+    """Full-size caches with q_len new tokens per row: the tokens of 3
+    sampled rows against the oracle (the sampled rows' caches copied to the
+    host), the appended slots bit for bit."""
+    import gqa_kv_cache_gb300 as gqa
+    w = W.WORKLOADS[name]
+    t = W.generate(w, "cuda", q_lens=[q_len] * w.B)
+    rows = [0, w.B // 2, w.B - 1]
+    sel = torch.tensor(rows, device="cuda")
+    tok = torch.cat([torch.arange(int(t["cu_q"][b]), int(t["cu_q"][b + 1]), device="cuda") for b in rows])
+    a = {"q": to_np(t["q"][tok]), "k_new": to_np(t["k_new"][tok]), "v_new": to_np(t["v_new"][tok]),
+         "lengths": to_np(t["lengths"][sel]),
+         "cu_q": np.arange(0, q_len * (len(rows) + 1), q_len, dtype=np.int32)}
+    if w.paged:
+        bt = t["block_table"][sel].cpu().numpy()
+        used = sorted(set(int(x) for x in bt[bt >= 0].tolist()))
+        remap = {b: i for i, b in enumerate(used)}
+        idx = torch.tensor(used, device="cuda")
+        a["k_blocks"], a["v_blocks"] = to_np(t["k_blocks"][idx]), to_np(t["v_blocks"][idx])
+        a["block_table"] = np.vectorize(lambda x: remap.get(int(x), -1))(bt).astype(np.int32)
+    else:
+        a["k_cache"], a["v_cache"] = to_np(t["k_cache"][sel]), to_np(t["v_cache"][sel])
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = _run_gpu(w, t, q_len, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    want = _run_oracle(w, a)
+    got = out[tok].double().cpu().numpy()
+    assert np.abs(got - want).max() <= BF16_REL_TOL * _vmax(a)
+    if w.paged:
+        assert to_np(t["k_blocks"][idx]).tobytes() == a["k_blocks"].tobytes()
+    else:
+        assert to_np(t["k_cache"][sel]).tobytes() == a["k_cache"].tobytes()

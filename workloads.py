@@ -30,6 +30,12 @@ decode step would append to is valid data), the stale region starts after
 them, and there is no k_new / v_new; ``q_f32=True`` keeps the query in
 float32 instead of casting it to the cache dtype.
 
+The multi-token step uses ``generate(w, q_lens=...)``: row b brings
+q_lens[b] new tokens, lengths are the decode draw clamped so the tokens fit
+(lengths[b] + q_lens[b] <= capacity), q / k_new / v_new are packed over the
+T = sum(q_lens) tokens, cu_q holds the offsets and a paged table covers
+every touched slot.
+
 Random draws come from a ``torch.Generator`` on the target device seeded
 with the workload's seed, in a fixed order, in chunks of ``_CHUNK`` elements
 (so an 8 GB cache never needs a 17 GB float32 staging copy).
@@ -144,7 +150,8 @@ def _lengths(w, gen, device):
     return torch.floor(x).clamp(w.len_lo, w.len_hi).to(torch.int32)
 
 
-def generate(w: Workload, device="cpu", attend: bool = False, q_f32: bool = False) -> dict:
+def generate(w: Workload, device="cpu", attend: bool = False, q_f32: bool = False,
+             q_lens=None) -> dict:
     """All inputs of one decode step of workload ``w`` on ``device``.
 
     Returns a dict with q (B,Hq,D), k_new/v_new (B,Hkv,D), lengths (B,) int32,
@@ -160,12 +167,19 @@ def generate(w: Workload, device="cpu", attend: bool = False, q_f32: bool = Fals
     t["lengths"] = _lengths(w, gen, device)
     if attend:
         t["lengths"] = t["lengths"] + 1
+    ntok = w.B
+    if q_lens is not None:
+        ql = torch.as_tensor(q_lens, dtype=torch.int64).to(device)
+        cap = w.max_blocks * w.block_size if w.paged else w.Smax
+        t["lengths"] = torch.minimum(t["lengths"].to(torch.int64), cap - ql).clamp(min=0).to(torch.int32)
+        t["cu_q"] = torch.cat([torch.zeros(1, dtype=torch.int64, device=device), torch.cumsum(ql, 0)]).to(torch.int32)
+        ntok = int(ql.sum().item())
     if q_f32:
-        t["q"] = _normal((w.B, w.Hq, w.D), gen, device)
+        t["q"] = _normal((ntok, w.Hq, w.D), gen, device)
     else:
-        t["q"] = _normal_cast((w.B, w.Hq, w.D), gen, device, w)
-    t["k_new"] = _normal_cast((w.B, w.Hkv, w.D), gen, device, w, w.key_scale)
-    t["v_new"] = _normal_cast((w.B, w.Hkv, w.D), gen, device, w)
+        t["q"] = _normal_cast((ntok, w.Hq, w.D), gen, device, w)
+    t["k_new"] = _normal_cast((ntok, w.Hkv, w.D), gen, device, w, w.key_scale)
+    t["v_new"] = _normal_cast((ntok, w.Hkv, w.D), gen, device, w)
     if w.paged:
         shape = (w.num_blocks, w.Hkv, w.block_size, w.D)
         t["k_blocks"] = _normal_cast(shape, gen, device, w, w.key_scale)
@@ -176,7 +190,10 @@ def generate(w: Workload, device="cpu", attend: bool = False, q_f32: bool = Fals
         perm = torch.randperm(w.num_blocks, generator=gen, device=device)[:need]
         bt = perm.view(w.B, w.max_blocks).to(torch.int32)
         # blocks holding the slots the call touches: 0..lengths[b] (decode), 0..lengths[b]-1 (attend)
-        touched = t["lengths"].to(torch.int64) + (0 if attend else 1)
+        if q_lens is not None:
+            touched = t["lengths"].to(torch.int64) + torch.as_tensor(q_lens, dtype=torch.int64).to(device)
+        else:
+            touched = t["lengths"].to(torch.int64) + (0 if attend else 1)
         used = (touched + w.block_size - 1) // w.block_size
         idx = torch.arange(w.max_blocks, device=device)[None, :]
         t["block_table"] = torch.where(idx < used[:, None], bt, torch.full_like(bt, -1))
