@@ -35,6 +35,14 @@
 // token writes it into the cache (the append).
 #pragma once
 
+// GQA_MULTI_TOKEN 0 compiles the multi-token branches of the schedule out (a
+// translation unit that instantiates single-token kernels only: their
+// streaming loops then carry none of that code). The types shared with the
+// host are the same either way.
+#ifndef GQA_MULTI_TOKEN
+#define GQA_MULTI_TOKEN 1
+#endif
+
 #include <climits>
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -122,7 +130,11 @@ __device__ __forceinline__ int last_slot(const DecodeParams &p, int b)
 // Batch row of virtual row vb.
 __device__ __forceinline__ int real_row(const DecodeParams &p, int vb)
 {
+#if GQA_MULTI_TOKEN
     return p.cu_q ? vb / p.max_chunks : vb;
+#else
+    return vb;
+#endif
 }
 
 // The tokens of virtual row vb of a multi-token step: nq tokens (0: an empty
@@ -132,6 +144,7 @@ struct ChunkInfo {
     int nq, i0, tok0, Lb;
 };
 
+#if GQA_MULTI_TOKEN
 __device__ __forceinline__ ChunkInfo chunk_info(const DecodeParams &p, int vb)
 {
     const int b = vb / p.max_chunks, c = vb % p.max_chunks;
@@ -147,6 +160,7 @@ __device__ __forceinline__ ChunkInfo chunk_info(const DecodeParams &p, int vb)
         ci.nq = max(0, min(p.tpc, qlen - ci.i0));
     return ci;
 }
+#endif
 
 // Capacity of one row in slots: the last attended slot must be below it.
 __host__ __device__ inline long long row_capacity(const DecodeParams &p)
@@ -166,8 +180,11 @@ __device__ __forceinline__ int kept_prefix(const DecodeParams &p, int vb)
 // tp + gap .. L / T (those holding window slots); without a window lo = 0,
 // gap = 0 and all ceil((L + 1) / T) tiles are real. Rows with bad content get
 // one tile, which only writes NaN.
+// L of a multi-token row whose token offsets are bad (GQA_STATUS_BAD_QLEN).
+constexpr int kBadQLenSlot = INT_MIN;
+
 struct RowGeom {
-    int L;    // last attended slot
+    int L;    // last attended slot (< 0: a bad row; kBadQLenSlot: bad token offsets)
     int lo;   // first slot of the window (0 without one)
     int P;    // kept prefix
     int nr;   // real tiles (0: an empty chunk of a multi-token step)
@@ -193,6 +210,7 @@ static __device__ __noinline__ RowGeom row_geom(const DecodeParams &p, int b)
     r.lo = 0;
     r.tp = 0;
     r.gap = 0;
+#if GQA_MULTI_TOKEN
     if (p.cu_q) {
         const ChunkInfo ci = chunk_info(p, b);
         if (ci.nq == 0) {            // an empty chunk: no tiles at all
@@ -200,16 +218,18 @@ static __device__ __noinline__ RowGeom row_geom(const DecodeParams &p, int b)
             return r;
         }
         r.nq = max(ci.nq, 0);        // bad token offsets: one tile, no output rows
-        r.L = ci.nq < 0 ? -1 : ci.Lb + ci.i0 + ci.nq - 1;
+        r.L = ci.nq < 0 ? kBadQLenSlot : (ci.Lb < 0 ? -1 : ci.Lb + ci.i0 + ci.nq - 1);
         r.tokL = ci.tok0 + ci.i0 + ci.nq - 1;
         r.Lb = ci.Lb;
-    } else {
+    } else
+#endif
+    {
         r.L = last_slot(p, b);
         r.nq = 1;
         r.tokL = b;
         r.Lb = r.L;
     }
-    if (!geom_ok(p, r.L, r.P) || (p.cu_q && r.Lb < 0)) {
+    if (!geom_ok(p, r.L, r.P)) {
         r.nr = 1;
         return r;
     }
@@ -240,7 +260,11 @@ __device__ __forceinline__ bool attended(int L, int lo, int P, int j)
 __device__ __forceinline__ int row_tiles(const DecodeParams &p, int b)
 {
     const int nr = row_geom(p, b).nr;
+#if GQA_MULTI_TOKEN
     return nr ? nr + p.pad_tiles : 0;
+#else
+    return nr + p.pad_tiles;
+#endif
 }
 
 // CTAs that share the N tiles: min(grid size, N).
@@ -285,9 +309,11 @@ __device__ __forceinline__ void set_row(const DecodeParams &p, TileCursor &c)
     c.nr = r.nr;
     c.tp = r.tp;
     c.gap = r.gap;
+#if GQA_MULTI_TOKEN
     c.nq = r.nq;
     c.tokL = r.tokL;
     c.Lb = r.Lb;
+#endif
 }
 
 // First slot of the cursor's (real) tile.
@@ -413,6 +439,19 @@ __device__ inline void schedule_walk(const DecodeParams &p, long long *scratch, 
     __syncthreads();
 }
 
+// The cursor's next row with tiles (empty chunks of a multi-token step hold
+// none). Out of line: it runs once per row, and keeping its code out of the
+// streaming loops keeps them short.
+#if GQA_MULTI_TOKEN
+static __device__ __noinline__ void next_row(const DecodeParams &p, TileCursor &c)
+{
+    do {
+        ++c.b;
+        set_row(p, c);
+    } while (c.nr == 0);
+}
+#endif
+
 __device__ __forceinline__ void advance(const DecodeParams &p, TileCursor &c)
 {
     ++c.g;
@@ -420,14 +459,16 @@ __device__ __forceinline__ void advance(const DecodeParams &p, TileCursor &c)
         c.t = 0;
         if (++c.kvh == p.Hkv) {
             c.kvh = 0;
+#if GQA_MULTI_TOKEN
+            if (c.g < c.end)
+                next_row(p, c);
+            else
+                ++c.b;
+#else
             ++c.b;
-            if (c.g < c.end) {
+            if (c.g < c.end)
                 set_row(p, c);
-                while (c.nr == 0) {   // empty chunks of a multi-token step hold no tiles
-                    ++c.b;
-                    set_row(p, c);
-                }
-            }
+#endif
         }
     }
 }
@@ -478,13 +519,10 @@ __device__ __forceinline__ bool walk_first(const DecodeParams &p, TileCursor &c,
 // good row).
 __device__ __forceinline__ int row_error_bits(const DecodeParams &p, int b, int L)
 {
-    if (p.cu_q) {
-        const ChunkInfo ci = chunk_info(p, b);
-        if (ci.nq < 0)
-            return kBadQLen;
-        if (ci.Lb < 0)
-            return kBadLength;
-    }
+#if GQA_MULTI_TOKEN
+    if (L == kBadQLenSlot)
+        return kBadQLen;
+#endif
     if (L < 0 || (long long)L >= row_capacity(p))
         return kBadLength;
     if (kept_prefix(p, b) < 0)
@@ -556,14 +594,22 @@ __device__ __forceinline__ float sink_log2(const DecodeParams &p, int h)
 }
 
 // Output row of query row g of the cursor's unit: token tokL - (nq - 1 -
-// g / Gh), head kvh * Gh + g % Gh (single-token forms: row b, head kvh*G + g).
+// g / Gh), head kvh * Gh + g % Gh; single-token forms (MULTI false): row b,
+// head kvh * G + g, without touching the cursor's chunk fields (which then
+// take no registers in the streaming loop).
+template <bool MULTI>
 __device__ __forceinline__ float *out_row(const DecodeParams &p, const TileCursor &c, int g, int DD)
 {
-    const long long tok = c.tokL - (c.nq - 1 - g / p.Gh);
-    return p.out + (tok * p.Hq + (long long)c.kvh * p.Gh + g % p.Gh) * DD;
+    if constexpr (MULTI) {
+        const long long tok = c.tokL - (c.nq - 1 - g / p.Gh);
+        return p.out + (tok * p.Hq + (long long)c.kvh * p.Gh + g % p.Gh) * DD;
+    } else {
+        return p.out + ((long long)c.b * p.Hq + (long long)c.kvh * p.G + g) * DD;
+    }
 }
 
-template <int NW, int GP, int DD, int DP, class Sync>
+// MULTI: the unit may be a chunk of a multi-token step (any form then works).
+template <int NW, int GP, int DD, int DP, bool MULTI, class Sync>
 __device__ inline void finish_segment(const DecodeParams &p, const TileCursor &cur, const TileWalk &walk,
                                       int seg_first_t,
                                       bool bad, const float (&sm_m)[NW][GP], const float (&sm_l)[NW][GP],
@@ -577,7 +623,7 @@ __device__ inline void finish_segment(const DecodeParams &p, const TileCursor &c
     const int u = b * p.Hkv + kvh;
     const long long P = (long long)u + blockIdx.x;
     const float qnan = __int_as_float(0x7fc00000);
-    const int nrow = p.Gh * cur.nq;   // query rows with an output (multi-token: its tokens)
+    const int nrow = MULTI ? p.Gh * cur.nq : G;   // query rows with an output
     if (tid < G) {
         float M = -INFINITY;
 #pragma unroll
@@ -627,7 +673,7 @@ __device__ inline void finish_segment(const DecodeParams &p, const TileCursor &c
                 for (int e = 0; e < V; ++e)
                     acc[e] = bad ? qnan : acc[e] * inv;
                 if (g < nrow) {
-                    float *o = out_row(p, cur, g, DD) + d;
+                    float *o = out_row<MULTI>(p, cur, g, DD) + d;
                     if constexpr (V == 4)
                         *reinterpret_cast<float4 *>(o) = make_float4(acc[0], acc[1], acc[2], acc[3]);
                     else
@@ -713,7 +759,7 @@ __device__ inline void finish_segment(const DecodeParams &p, const TileCursor &c
                     }
                 }
                 if (g < nrow) {
-                    float *o = out_row(p, cur, g, DD) + (idx - g * DD);
+                    float *o = out_row<MULTI>(p, cur, g, DD) + (idx - g * DD);
 #pragma unroll
                     for (int e = 0; e < V; ++e)
                         o[e] = acc[e] * mb.inv_den[g];
@@ -737,7 +783,7 @@ __device__ inline void finish_segment(const DecodeParams &p, const TileCursor &c
                     *po = 0.f;       // consumed: leave the workspace zero-filled
                 }
                 if (g < nrow)
-                    out_row(p, cur, g, DD)[d] = num / den;
+                    out_row<MULTI>(p, cur, g, DD)[d] = num / den;
             }
         }
         sync();

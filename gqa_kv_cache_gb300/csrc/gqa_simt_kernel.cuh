@@ -302,7 +302,7 @@ __global__ void __launch_bounds__(kThreads) simt_decode_kernel(const DecodeParam
             const bool bad = !row_good || seg_bad;
             if (bad && row_good && tid == 0)
                 report(p, kBadBlock);
-            finish_segment<kWarps, GP, D, D>(p, cur, walk, seg_first_t, bad, sm_m, sm_l, sm_o, &sm_flag, sm_merge, tid,
+            finish_segment<kWarps, GP, D, D, true>(p, cur, walk, seg_first_t, bad, sm_m, sm_l, sm_o, &sm_flag, sm_merge, tid,
                                           kThreads, [] { __syncthreads(); });
             seg_start = true;
         }

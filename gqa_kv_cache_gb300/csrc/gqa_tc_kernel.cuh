@@ -1,0 +1,696 @@
+// Tensor-core decode kernel for bfloat16 caches with D = 128 and G <= 8; the
+// query is bfloat16 or float32.
+//
+// Data path (persistent CTAs, kCtasPerSm per SM):
+//  * a producer warp walks the CTA's tiles (gqa_common.cuh) and streams every
+//    64-slot tile of K and V from HBM into a kStages-deep shared-memory ring
+//    with TMA tiled copies (cp.async.bulk.tensor, 128-byte swizzle, two
+//    64-element halves per row), signalling an mbarrier per stage; for paged
+//    caches each lane copies one block of the tile. The first tile of each
+//    unit segment also brings the unit's G query rows (one bulk copy), so no
+//    consumer ever waits on a global load. Table and row lookups for a tile
+//    are issued one tile ahead, before the wait for a free stage.
+//  * four consumer warps each take 16 slots of every tile and compute, on the
+//    tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate):
+//      S  = Q K^T   M = 16 query rows: rows 0..7 hold the G heads (rows >= G
+//                   are zero); a float32 query is split into bf16(q) in rows
+//                   0..7 and the remainder bf16(q - bf16(q)) in rows 8..15,
+//                   and the two halves of S are added (so q enters with ~16
+//                   significant bits at no extra MMA: rows 8..15 would be
+//                   padding); N = 8 slots, K = 16 dims, 8 steps over D = 128
+//                   (two accumulator chains per tile, even and odd steps);
+//      O += P V     M = 16 rows: rows 0..7 carry bf16(p) and rows 8..15 the
+//                   remainder bf16(p - bf16(p)), so p enters the product with
+//                   ~16 significant bits and the sum stays float32-accurate;
+//                   N = 8 dims (16 tiles over D), K = 16 slots.
+//    The S accumulator fragment is reused directly as the A fragment of the
+//    P V product. K fragments come from ldmatrix, V fragments from
+//    ldmatrix.trans; the swizzle makes both conflict-free.
+//  * online softmax in float32 with base-2 scores (scale log2(e)/sqrt(D)
+//    folded in), a lazy rescale (the running max is only raised when a score
+//    exceeds it by more than 8, i.e. p <= 256), masking by selection so stale
+//    slots (and slots outside a sliding window and kept prefix) never enter
+//    the arithmetic, and the V rows of such slots zeroed in shared memory
+//    before the product (0 * NaN would not be 0). A window skips whole tiles
+//    (the schedule lists only tiles holding attended slots) and, for paged
+//    caches, whole blocks.
+//  * multi-token steps (MULTI): a unit is a chunk of up to 8 / G tokens of a
+//    row; its query rows are (token, head) pairs gathered by one bulk copy per
+//    token, each row is masked beyond its own token's position, every slot
+//    holding a new token is substituted from k_new / v_new as below, and the
+//    chunk appends its own tokens.
+//  * the new token (decode step only; the read-only attend reads slot L from
+//    the cache like any other): in the tile that holds slot L the owning warp writes
+//    k_new / v_new into the ring slot of row L (the TMA copy of the stale
+//    cache row is discarded) and stores them into the cache at slot L. The
+//    copy of that tile has landed before the store, and no other CTA loads
+//    slot L, so the append cannot race with a read.
+//  * at the end of each unit segment the four warp states are merged in
+//    shared memory (finish_segment): a whole unit writes its output, a cut
+//    unit its partial state, and the last CTA of a cut unit merges them.
+// Two CTAs share each SM, so one CTA's segment epilogue overlaps the other's
+// streaming.
+// Every mbarrier wait is bounded. A wait that gives up sets GQA_STATUS_TIMEOUT
+// and a CTA-wide abort flag: the producer stops issuing and waits (bounded)
+// for its copies in flight; the consumer warps stop waiting and computing but
+// keep walking their tiles and taking part in every barrier, writing NaN.
+#pragma once
+
+#include "gqa_common.cuh"
+#include "gqa_launch.h"
+
+namespace gqa {
+namespace {
+
+#ifndef GQA_TC_STAGES
+#define GQA_TC_STAGES 2
+#endif
+#ifndef GQA_TC_CTAS_PER_SM
+#define GQA_TC_CTAS_PER_SM 2
+#endif
+
+constexpr int kD = 128;
+constexpr int kTile = 64;                             // slots per tile
+constexpr int kStages = GQA_TC_STAGES;                // depth of one CTA's TMA ring
+constexpr int kCtasPerSm = GQA_TC_CTAS_PER_SM;        // resident CTAs per SM
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kGMax = 8;
+constexpr int kHalfBytes = kTile * 128;               // one 64-element half of a tile
+constexpr long long kWaitCycles = 4LL << 30;          // ~2 s at 2 GHz
+
+// Ring geometry for a bfloat16 (QF32 = false) or float32 query.
+template <bool QF32>
+struct Ring {
+    static constexpr int kQElem = QF32 ? 4 : 2;
+    static constexpr int kQBytes = kGMax * kD * kQElem;              // the unit's G query rows
+    static constexpr int kStageBytes = 4 * kHalfBytes + kQBytes;     // K lo, K hi, V lo, V hi, Q
+    static constexpr int kDynSmem = kStages * kStageBytes + 1024;
+    static_assert(kStageBytes % 1024 == 0, "stages must stay 1024-byte aligned for the swizzle");
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, int count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(bar), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+
+// Bounded wait; false when it gave up.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
+{
+    if (mbar_try(bar, parity))
+        return true;
+    const long long t0 = clock64();
+    while (!mbar_try(bar, parity)) {
+        if (clock64() - t0 > kWaitCycles)
+            return false;
+    }
+    return true;
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y, int z,
+                                            uint32_t bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4])
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4])
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+                 "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// bf16 pair (lo in the low half) rounded to nearest even.
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// A float32 pair as bf16 hi parts and bf16 remainders: v = hi + lo to ~16 bits.
+__device__ __forceinline__ void split_bf16(float2 v, uint32_t &hi, uint32_t &lo)
+{
+    hi = pack_bf16(v.x, v.y);
+    lo = pack_bf16(v.x - __uint_as_float(hi << 16), v.y - __uint_as_float(hi & 0xffff0000u));
+}
+
+// Byte offset, within one 64-element half, of 16-byte chunk c8 of row r
+// under the 128-byte swizzle (the half starts on a 1024-byte boundary).
+__device__ __forceinline__ uint32_t swz(int r, int c8) { return (uint32_t)(r * 128 + ((c8 ^ (r & 7)) << 4)); }
+
+struct Shared {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    int stage_bad[kStages];
+    int abort_flag;
+    int last_flag;
+    long long sched[kThreads / 32 + 8];
+    TileWalk walk;
+    float m[kConsumerWarps][kGMax];
+    float l[kConsumerWarps][kGMax];
+    alignas(16) float o[kConsumerWarps][kGMax][kD + 8];   // rows padded: conflict-free 8-byte stores
+    MergeBuf merge;
+};
+
+__device__ __forceinline__ void consumer_sync()
+{
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+}
+
+// WIN: a sliding window is in force. Without one the window fields of the
+// cursor are never read, so they take no registers and no code. MULTI: a
+// multi-token step (the chunk fields of the cursor are read only then).
+template <bool QF32, bool WIN, bool MULTI>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+    tc_decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap mk,
+                     const __grid_constant__ CUtensorMap mv)
+{
+    constexpr int kStageBytes = Ring<QF32>::kStageBytes;
+    extern __shared__ uint8_t dyn_smem[];
+    __shared__ Shared sh;
+    uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
+    const uint32_t ring_u32 = smem_u32(ring);
+
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_u32(&sh.full[s]), 1);
+            mbar_init(smem_u32(&sh.empty[s]), kConsumerWarps);
+            sh.stage_bad[s] = 0;
+        }
+        sh.abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == kConsumerWarps && lane == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mk)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mv)) : "memory");
+    }
+    // Launched as a programmatic dependent of the previous kernel on the
+    // stream: everything above overlaps its tail; no input is read before it
+    // has completed and its memory is visible.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    schedule_walk(p, sh.sched, &sh.walk);   // contains __syncthreads
+    const TileWalk &walk = sh.walk;
+
+    const int G = p.G;
+    const __nv_bfloat16 *knew = static_cast<const __nv_bfloat16 *>(p.k_new);
+    const __nv_bfloat16 *vnew = static_cast<const __nv_bfloat16 *>(p.v_new);
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------ producer --
+        uint64_t policy;
+        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+        TileCursor cur;
+        bool in_b = false;
+        bool more = walk_first(p, cur, walk, in_b);
+        long long range_start = cur.g;
+        int stage = 0;
+        uint32_t phase = 0;
+        const int bs = p.block_size;
+        const int nblk = p.paged ? (bs < kTile ? kTile / bs : 1) : 1;  // copies per half per tile
+        const int box_rows = p.paged ? (bs < kTile ? bs : kTile) : kTile;
+        // Where this lane copies tile `c` from: z (cache head row of the
+        // tensor map) and y (first slot in it); z < 0: nothing. Computed one
+        // tile ahead, before the wait for a free stage, so the table reads
+        // overlap the wait.
+        struct Plan {
+            int z, y;
+            bool bad_entry, good;
+        };
+        auto plan = [&](const TileCursor &c) {
+            Plan r{-1, 0, false, row_ok(p, c.b, c.L)};
+            if (!r.good)
+                return r;
+            const int slot0 = WIN ? tile_slot0(c, kTile) : c.t * kTile;
+            const int rb = MULTI ? real_row(p, c.b) : c.b;   // the batch row
+            if (!p.paged) {
+                if (lane == 0) {
+                    const int row = p.slot_ids ? __ldg(p.slot_ids + rb) : rb;
+                    r.z = row * p.Hkv + c.kvh;
+                    r.y = slot0;
+                }
+            } else if (lane < nblk) {
+                const int s = slot0 + lane * box_rows;  // first slot this lane copies
+                // a block is copied when it holds an attended slot
+                if (s <= c.L && (!WIN || s + box_rows - 1 >= c.lo || s < c.P)) {
+                    const int e = __ldg(p.block_table + (long long)rb * p.max_blocks + s / bs);
+                    if (e >= 0 && e < p.num_blocks) {
+                        r.z = e * p.Hkv + c.kvh;
+                        r.y = s % bs;
+                    } else {
+                        r.bad_entry = true;
+                    }
+                }
+            }
+            return r;
+        };
+        int issued = 0;
+        Plan pl = more ? plan(cur) : Plan{-1, 0, false, false};
+        while (more) {
+            if (*((volatile int *)&sh.abort_flag))
+                break;
+            if (!mbar_wait(smem_u32(&sh.empty[stage]), phase ^ 1)) {
+                if (lane == 0) {
+                    report(p, kTimeout);
+                    atomicExch(&sh.abort_flag, 1);
+                }
+                break;
+            }
+            const int b = cur.b, kvh = cur.kvh;
+            const unsigned copying = __ballot_sync(0xffffffffu, pl.z >= 0);
+            const bool any_bad = __any_sync(0xffffffffu, pl.bad_entry);
+            // the first tile of each of this CTA's unit segments also brings
+            // the unit's G query rows (contiguous in q)
+            const bool seg_first = pl.good && (cur.t == 0 || cur.g == range_start);
+            const int qrows = MULTI ? p.Gh * cur.nq : G;   // query rows with data
+            const uint32_t qbytes = seg_first ? (uint32_t)(qrows * kD * Ring<QF32>::kQElem) : 0u;
+            const uint32_t bytes = (uint32_t)__popc(copying) * 4u * (uint32_t)box_rows * 128u + qbytes;
+            const uint32_t fb = smem_u32(&sh.full[stage]);
+            if (lane == 0) {
+                sh.stage_bad[stage] = any_bad ? 1 : 0;
+                mbar_arrive_tx(fb, bytes);
+                if (qbytes) {
+                    const uint32_t qdst = ring_u32 + stage * kStageBytes + 4 * kHalfBytes;
+                    if constexpr (MULTI) {
+                        // one copy per token: its Gh heads are contiguous in q
+                        const uint32_t tb = (uint32_t)(p.Gh * kD * Ring<QF32>::kQElem);
+                        for (int i = 0; i < cur.nq; ++i) {
+                            const long long tok = cur.tokL - (cur.nq - 1 - i);
+                            bulk_load(qdst + i * tb,
+                                      static_cast<const uint8_t *>(p.q) +
+                                          (tok * p.Hq + (long long)kvh * p.Gh) * kD * Ring<QF32>::kQElem,
+                                      tb, fb);
+                        }
+                    } else {
+                        bulk_load(qdst,
+                                  static_cast<const uint8_t *>(p.q) +
+                                      ((long long)b * p.Hq + (long long)kvh * G) * kD * Ring<QF32>::kQElem,
+                                  qbytes, fb);
+                    }
+                }
+            }
+            __syncwarp();
+            if (pl.z >= 0) {
+                const uint32_t dst = ring_u32 + stage * kStageBytes + lane * box_rows * 128;
+                tma_load_3d(dst, &mk, 0, pl.y, pl.z, fb, policy);
+                tma_load_3d(dst + kHalfBytes, &mk, 64, pl.y, pl.z, fb, policy);
+                tma_load_3d(dst + 2 * kHalfBytes, &mv, 0, pl.y, pl.z, fb, policy);
+                tma_load_3d(dst + 3 * kHalfBytes, &mv, 64, pl.y, pl.z, fb, policy);
+            }
+            ++issued;
+            const bool was_b = in_b;
+            more = walk_next(p, cur, walk, in_b);
+            if (in_b != was_b)
+                range_start = cur.g;
+            if (more)
+                pl = plan(cur);
+            if (++stage == kStages) {
+                stage = 0;
+                phase ^= 1;
+            }
+        }
+        // every tile is issued: the next kernel on the stream may start launching
+        asm volatile("griddepcontrol.launch_dependents;");
+        // Abort path only: let every copy still in flight land before exit.
+        if (*((volatile int *)&sh.abort_flag)) {
+            int s = stage, ph = phase;
+            for (int k = 0; k < kStages && k < issued; ++k) {
+                if (--s < 0) {
+                    s = kStages - 1;
+                    ph ^= 1;
+                }
+                mbar_wait(smem_u32(&sh.full[s]), ph);
+            }
+        }
+        return;
+    }
+
+    // -------------------------------------------------------- consumers --
+    const int g0 = lane >> 2, q4 = lane & 3;
+    const int row0 = warp * 16;          // this warp's 16 rows of every tile
+    TileCursor cur;
+    bool in_b = false;
+    bool more = walk_first(p, cur, walk, in_b);
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t qa[8][2];                   // Q fragments (rows g0 < G), 8 k-steps
+    uint32_t ql[8][2];                   // float32 query: the remainders (rows g0 + 8)
+    float acc_o[16][4];                  // O: 16 n-tiles of 8 dims, rows g0 (hi) and g0+8 (lo)
+    float m_run = -INFINITY, l_run = 0.f;
+    int seg_first_t = 0;
+    bool seg_start = true, row_good = true, aborted = false;
+    int seg_bad = 0;
+    // multi-token units only: this lane's row g0 (last slot, window start), rows with data
+    int lim = 0, lo_r = 0, qrows = G;
+
+    while (more) {
+        const int b = cur.b, kvh = cur.kvh, L = cur.L;
+        const bool first_of_seg = seg_start;
+        if (seg_start) {
+            seg_first_t = cur.t;
+            row_good = row_ok(p, b, L);
+            if (!row_good && tid == 0 && cur.t == 0 && kvh == 0)
+                report(p, row_error_bits(p, b, L));
+#pragma unroll
+            for (int n = 0; n < 16; ++n)
+                acc_o[n][0] = acc_o[n][1] = acc_o[n][2] = acc_o[n][3] = 0.f;
+            m_run = -INFINITY;
+            l_run = 0.f;
+            seg_bad = 0;
+            seg_start = false;
+            if constexpr (MULTI) {
+                lim = L - (cur.nq - 1 - g0 / p.Gh);   // row g0 is token g0 / Gh of the chunk
+                qrows = p.Gh * cur.nq;
+                if constexpr (WIN)
+                    lo_r = max(0, lim - p.window + 1);
+            }
+        }
+
+        // After an abort every warp keeps walking its tiles and taking part in
+        // every barrier, but waits for and computes nothing (outputs NaN).
+        bool have = false;
+        if (!aborted && !*((volatile int *)&sh.abort_flag)) {
+            have = mbar_wait(smem_u32(&sh.full[stage]), phase);
+            if (!have && lane == 0) {
+                report(p, kTimeout);
+                atomicExch(&sh.abort_flag, 1);
+            }
+        }
+        aborted = aborted || !have;
+        seg_bad |= aborted ? 1 : 0;
+
+        const int slot0 = WIN ? tile_slot0(cur, kTile) : cur.t * kTile;
+        const uint32_t kbase = ring_u32 + stage * kStageBytes;
+        const uint32_t vbase = kbase + 2 * kHalfBytes;
+        uint8_t *kring = ring + stage * kStageBytes;
+        uint8_t *vring = kring + 2 * kHalfBytes;
+        const int tile_bad = have ? sh.stage_bad[stage] : 1;
+        seg_bad |= tile_bad;
+        if (first_of_seg && have && row_good) {
+            // Q fragments from the ring (rows g0 < G): dims 16ks + 2q4 (+1)
+            // and 16ks + 8 + 2q4 (+1) of head g0
+            if constexpr (QF32) {
+                const float *qs = reinterpret_cast<const float *>(kring + 4 * kHalfBytes) + g0 * kD;
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    qa[ks][0] = qa[ks][1] = ql[ks][0] = ql[ks][1] = 0u;
+                    if (g0 < (MULTI ? qrows : G)) {
+                        split_bf16(*reinterpret_cast<const float2 *>(qs + 16 * ks + 2 * q4), qa[ks][0], ql[ks][0]);
+                        split_bf16(*reinterpret_cast<const float2 *>(qs + 16 * ks + 8 + 2 * q4), qa[ks][1],
+                                   ql[ks][1]);
+                    }
+                }
+            } else {
+                const uint8_t *qs = kring + 4 * kHalfBytes + g0 * (kD * 2);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const bool on = g0 < (MULTI ? qrows : G);
+                    qa[ks][0] = on ? *reinterpret_cast<const uint32_t *>(qs + (16 * ks + 2 * q4) * 2) : 0u;
+                    qa[ks][1] = on ? *reinterpret_cast<const uint32_t *>(qs + (16 * ks + 8 + 2 * q4) * 2) : 0u;
+                }
+            }
+        }
+
+        if (have && row_good && !tile_bad) {
+            const bool last_tile = (cur.t == cur.nr - 1);
+            // tiles holding new tokens: the last one; in a multi-token step
+            // every tile reaching the row's write offset
+            const bool newt = MULTI ? (slot0 + kTile - 1 >= cur.Lb) : last_tile;
+            // tiles that hold slots outside some row's softmax: those, and,
+            // with a window, those below the last row's window start
+            const bool partial = newt || (WIN && slot0 < (MULTI ? max(0, L - p.window + 1) : cur.lo));
+            if (partial) {
+                // new-token rows: substituted from k_new / v_new (and appended
+                // by the unit owning the token); rows no query row attends:
+                // zero V
+                if constexpr (MULTI) {
+                    // this warp's rows holding new tokens
+                    const int first_new = max(cur.Lb, slot0 + row0);
+                    const int last_new = min(L, slot0 + row0 + 15);
+                    for (int sn = first_new; sn <= last_new; ++sn) {
+                        const int lr = sn - slot0;
+                        const long long tok = cur.tokL - (L - sn);
+                        const long long nidx = (tok * p.Hkv + kvh) * kD;
+                        const int c = lane & 15;          // 16-byte chunk of the row
+                        const int half = c >> 3, c8 = c & 7;
+                        const uint4 *src = reinterpret_cast<const uint4 *>((lane < 16 ? knew : vnew) + nidx) + c;
+                        const uint4 v = __ldg(src);
+                        uint8_t *dst = (lane < 16 ? kring : vring) + half * kHalfBytes + swz(lr, c8);
+                        *reinterpret_cast<uint4 *>(dst) = v;
+                        // the in-place append, by the unit that owns the token
+                        if (sn > L - cur.nq) {
+                            const long long off = slot_offset(p, b, kvh, sn);
+                            if (off >= 0) {
+                                __nv_bfloat16 *cache = static_cast<__nv_bfloat16 *>(lane < 16 ? p.k_cache : p.v_cache);
+                                reinterpret_cast<uint4 *>(cache + off)[c] = v;
+                            }
+                        }
+                    }
+                } else {
+                    // row L of the last tile: the new token
+                    const int lr = L - slot0;            // 0..63 in the last tile
+                    if (last_tile && !p.attend && lr >= row0 && lr < row0 + 16) {
+                        const long long nidx = ((long long)b * p.Hkv + kvh) * kD;
+                        const int c = lane & 15;          // 16-byte chunk of the row
+                        const int half = c >> 3, c8 = c & 7;
+                        const uint4 *src = reinterpret_cast<const uint4 *>((lane < 16 ? knew : vnew) + nidx) + c;
+                        const uint4 v = __ldg(src);
+                        uint8_t *dst = (lane < 16 ? kring : vring) + half * kHalfBytes + swz(lr, c8);
+                        *reinterpret_cast<uint4 *>(dst) = v;
+                        // the in-place append
+                        const long long off = slot_offset(p, b, kvh, L);
+                        if (off >= 0) {
+                            __nv_bfloat16 *cache = static_cast<__nv_bfloat16 *>(lane < 16 ? p.k_cache : p.v_cache);
+                            reinterpret_cast<uint4 *>(cache + off)[c] = v;
+                        }
+                    }
+                }
+                for (int r = row0 + (lane >> 4); r < row0 + 16; r += 2) {
+                    if (WIN ? !attended(L, cur.lo, cur.P, slot0 + r) : slot0 + r > L) {
+                        const int c = lane & 15;
+                        *reinterpret_cast<uint4 *>(vring + (c >> 3) * kHalfBytes + swz(r, c & 7)) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+                __syncwarp();
+            }
+
+            // ---- S = Q K^T for this warp's 16 slots (two n-tiles of 8);
+            // even and odd k-steps accumulate separately (shorter chains)
+            float s_acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            {
+                float s_odd[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                const int mi = lane >> 3, ri = lane & 7;
+                const int r = row0 + 8 * (mi >> 1) + ri;
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const int c = 2 * ks + (mi & 1);
+                    uint32_t kb[4];
+                    ldsm_x4(kbase + (c >> 3) * kHalfBytes + swz(r, c & 7), kb);
+                    float(&acc)[2][4] = (ks & 1) ? s_odd : s_acc;
+                    if constexpr (QF32) {
+                        mma_bf16(acc[0], qa[ks][0], ql[ks][0], qa[ks][1], ql[ks][1], kb[0], kb[1]);
+                        mma_bf16(acc[1], qa[ks][0], ql[ks][0], qa[ks][1], ql[ks][1], kb[2], kb[3]);
+                    } else {
+                        mma_bf16(acc[0], qa[ks][0], 0u, qa[ks][1], 0u, kb[0], kb[1]);
+                        mma_bf16(acc[1], qa[ks][0], 0u, qa[ks][1], 0u, kb[2], kb[3]);
+                    }
+                }
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        s_acc[nt][e] += s_odd[nt][e];
+            }
+            // ---- masked online softmax (base 2), rows g0; only the partial
+            // tiles (the last one, those below a window's start) test slots
+            float x[2][2];
+            float mx = -INFINITY;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int j = slot0 + row0 + 8 * nt + 2 * q4 + e;
+                    float sc = s_acc[nt][e];
+                    if constexpr (QF32)
+                        sc += s_acc[nt][e + 2];   // row g0 + 8: the query remainder
+                    const bool on = MULTI ? (WIN ? attended(lim, lo_r, cur.P, j) : j <= lim)
+                                          : (WIN ? attended(L, cur.lo, cur.P, j) : j <= L);
+                    x[nt][e] = (!partial || on) ? sc * p.scale_log2 : -INFINITY;
+                    mx = fmaxf(mx, x[nt][e]);
+                }
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            if (mx > m_run + 8.f) {          // raise the running max (also from -inf)
+                const float alpha = (m_run == -INFINITY) ? 0.f : fast_ex2(m_run - mx);
+                l_run *= alpha;
+#pragma unroll
+                for (int n = 0; n < 16; ++n) {
+                    acc_o[n][0] *= alpha;
+                    acc_o[n][1] *= alpha;
+                    acc_o[n][2] *= alpha;
+                    acc_o[n][3] *= alpha;
+                }
+                m_run = mx;
+            }
+            uint32_t pa[4];
+            {
+                float pr[2][2];
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        pr[nt][e] = (x[nt][e] == -INFINITY) ? 0.f : fast_ex2(x[nt][e] - m_run);
+                        l_run += pr[nt][e];
+                    }
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const uint32_t hi = pack_bf16(pr[nt][0], pr[nt][1]);
+                    const float h0 = __uint_as_float(hi << 16), h1 = __uint_as_float(hi & 0xffff0000u);
+                    const uint32_t lo = pack_bf16(pr[nt][0] - h0, pr[nt][1] - h1);
+                    pa[2 * nt] = hi;      // rows g0:   slots 8nt + 2q4, +1
+                    pa[2 * nt + 1] = lo;  // rows g0+8
+                }
+            }
+            // ---- O += P V (16 n-tiles of 8 dims)
+            {
+                const int mi = lane >> 3, ri = lane & 7;
+                const int r = row0 + 8 * (mi & 1) + ri;
+#pragma unroll
+                for (int np = 0; np < 8; ++np) {
+                    const int c = 2 * np + (mi >> 1);
+                    uint32_t vb[4];
+                    ldsm_x4_t(vbase + (c >> 3) * kHalfBytes + swz(r, c & 7), vb);
+                    mma_bf16(acc_o[2 * np], pa[0], pa[1], pa[2], pa[3], vb[0], vb[1]);
+                    mma_bf16(acc_o[2 * np + 1], pa[0], pa[1], pa[2], pa[3], vb[2], vb[3]);
+                }
+            }
+            if (partial)
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        }
+        __syncwarp();
+        if (lane == 0 && have)
+            mbar_arrive(smem_u32(&sh.empty[stage]));
+        if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+        }
+
+        const bool unit_done = (cur.t == cur.nr - 1);
+        const bool range_done = (cur.g + 1 == cur.end);
+        if (unit_done || range_done) {
+            // ---- merge the four warps' states and emit
+            float l_tot = l_run;
+            l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 1);
+            l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 2);
+            if (g0 < G) {
+                if (q4 == 0) {
+                    sh.m[warp][g0] = m_run;
+                    sh.l[warp][g0] = l_tot;
+                }
+#pragma unroll
+                for (int n = 0; n < 16; ++n)
+                    *reinterpret_cast<float2 *>(&sh.o[warp][g0][8 * n + 2 * q4]) =
+                        make_float2(acc_o[n][0] + acc_o[n][2], acc_o[n][1] + acc_o[n][3]);
+            }
+            consumer_sync();
+            const bool bad = !row_good || seg_bad;
+            if (bad && row_good && tid == 0)
+                report(p, aborted ? kTimeout : kBadBlock);
+            finish_segment<kConsumerWarps, kGMax, kD, kD + 8, MULTI>(p, cur, walk, seg_first_t, bad, sh.m, sh.l, sh.o,
+                                                      &sh.last_flag, sh.merge, tid, kConsumerWarps * 32,
+                                                      [] { consumer_sync(); });
+            seg_start = true;
+        }
+        more = walk_next(p, cur, walk, in_b);
+    }
+}
+
+
+template <bool QF32, bool WIN, bool MULTI>
+cudaError_t launch_q(const DecodeParams &p, const TcMaps &maps, cudaStream_t st)
+{
+    constexpr int kDynSmem = Ring<QF32>::kDynSmem;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(tc_decode_kernel<QF32, WIN, MULTI>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem);
+        if (e != cudaSuccess)
+            return e;
+        attr_set = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kDynSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, tc_decode_kernel<QF32, WIN, MULTI>, p, maps.k, maps.v);
+}
+
+}  // namespace
+
+// The instantiations live in two translation units: the single-token kernels
+// (gqa_tc.cu, compiled without the multi-token schedule code) and the
+// multi-token kernels (gqa_tc_multi.cu).
+cudaError_t tc_launch_multi(const DecodeParams &p, const TcMaps &maps, cudaStream_t st);
+
+}  // namespace gqa
