@@ -10,7 +10,9 @@ and the passages it follows). This module only builds that file with gcc,
 marshals numpy arrays to it and returns float64 outputs.
 
 bfloat16 data is passed as ``numpy.uint16`` arrays holding the raw bits (the
-upper half of an IEEE binary32); float32 data as ``numpy.float32``.
+upper half of an IEEE binary32); float32 data as ``numpy.float32``; an E4M3
+(OCP FP8) cache as ``numpy.uint8`` bytes with ``k_scale`` / ``v_scale``
+float32 arrays of one scale per cache head.
 """
 from __future__ import annotations
 
@@ -25,7 +27,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gqa_oracle.c")
 _LIB = os.path.join(_HERE, "libgqa_oracle.so")
 
-F32, BF16 = 0, 1
+F32, BF16, E4M3 = 0, 1, 2
 OK, INVALID_ARGUMENT = 0, 1
 
 _lock = threading.Lock()
@@ -34,15 +36,23 @@ _lib = None
 
 class _Mods(ctypes.Structure):
     _fields_ = [("head_sink", ctypes.c_void_p), ("window", ctypes.c_int),
-                ("kept_prefix", ctypes.c_int), ("kept_prefix_rows", ctypes.c_void_p)]
+                ("kept_prefix", ctypes.c_int), ("kept_prefix_rows", ctypes.c_void_p),
+                ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p), ("new_dtype", ctypes.c_int)]
 
 
-def _mods(sink, window, kept_prefix, keep):
+def _mods(sink, window, kept_prefix, keep, scales=None):
     """The orc_mods argument (None when no modifier is given). Arrays that
-    back it are appended to ``keep`` so they outlive the call."""
-    if sink is None and not window and (kept_prefix is None or np.isscalar(kept_prefix) and kept_prefix == 0):
+    back it are appended to ``keep`` so they outlive the call. ``scales`` =
+    (k_scale, v_scale, new_dtype) for an E4M3 cache."""
+    if sink is None and not window and scales is None and \
+            (kept_prefix is None or np.isscalar(kept_prefix) and kept_prefix == 0):
         return None
     m = _Mods()
+    if scales is not None:
+        ks = np.ascontiguousarray(scales[0], dtype=np.float32)
+        vs = np.ascontiguousarray(scales[1], dtype=np.float32)
+        keep += [ks, vs]
+        m.k_scale, m.v_scale, m.new_dtype = ks.ctypes.data, vs.ctypes.data, int(scales[2])
     if sink is not None:
         a = np.ascontiguousarray(sink, dtype=np.float32)
         keep.append(a)
@@ -106,6 +116,10 @@ def _load():
             lib.orc_validate_multi_dense.restype = I
             lib.orc_validate_multi_paged.argtypes = [P, P, P, I, I, I, I, I]
             lib.orc_validate_multi_paged.restype = I
+            lib.orc_e4m3_encode.argtypes = [ctypes.c_float]
+            lib.orc_e4m3_encode.restype = ctypes.c_uint8
+            lib.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
+            lib.orc_e4m3_decode.restype = ctypes.c_double
             lib.orc_default_threads.argtypes = []
             lib.orc_default_threads.restype = I
             _lib = lib
@@ -121,7 +135,39 @@ def _dtype_code(a: np.ndarray) -> int:
         return F32
     if a.dtype == np.uint16:
         return BF16
-    raise TypeError(f"oracle takes float32 or uint16 (bfloat16 bits), not {a.dtype}")
+    if a.dtype == np.uint8:
+        return E4M3
+    raise TypeError(f"oracle takes float32, uint16 (bfloat16 bits) or uint8 (E4M3 bytes), not {a.dtype}")
+
+
+def e4m3_encode(x: float) -> int:
+    """E4M3 code of float32 x (round to nearest even, saturating)."""
+    return int(_load().orc_e4m3_encode(float(np.float32(x))))
+
+
+def e4m3_decode(c: int) -> float:
+    return float(_load().orc_e4m3_decode(int(c)))
+
+
+def _cache_dtypes(q, news, caches, k_scale, v_scale):
+    """(dtype code passed to the oracle, scales tuple or None): q and the new
+    keys / values share one dtype; the caches that one too, or E4M3 bytes with
+    per-head scales."""
+    for a in news:
+        if a is not None and a.dtype != q.dtype:
+            raise TypeError("q, k_new and v_new share one dtype")
+    for a in caches:
+        if not a.flags.c_contiguous:
+            raise ValueError("arrays must be C-contiguous (the caches are written in place)")
+        if a.dtype != caches[0].dtype:
+            raise TypeError("the two caches share one dtype")
+    if caches[0].dtype == np.uint8:
+        if k_scale is None or v_scale is None:
+            raise ValueError("an E4M3 cache needs k_scale and v_scale")
+        return E4M3, (k_scale, v_scale, _dtype_code(q))
+    if caches[0].dtype != q.dtype:
+        raise TypeError("q, k_new, v_new and the caches share one dtype")
+    return _dtype_code(q), None
 
 
 def _ptr(a):
@@ -144,7 +190,7 @@ class OracleResult:
 
 def decode_dense(q, k_new, v_new, k_cache, v_cache, lengths, slot_ids=None, *,
                  rows=None, append=True, threads=None, sink=None, window=0,
-                 kept_prefix=0) -> OracleResult:
+                 kept_prefix=0, k_scale=None, v_scale=None) -> OracleResult:
     """One decode step on a dense (R, Hkv, Smax, D) cache, in place.
 
     ``q`` (B, Hq, D); ``k_new``/``v_new`` (B, Hkv, D); ``lengths`` (B,) int32;
@@ -155,12 +201,7 @@ def decode_dense(q, k_new, v_new, k_cache, v_cache, lengths, slot_ids=None, *,
     ``kept_prefix`` an int or a (B,) int32 array.
     Returns an OracleResult with ``out`` (B, Hq, D) float64.
     """
-    dt = _dtype_code(q)
-    for a in (k_new, v_new, k_cache, v_cache):
-        if a.dtype != q.dtype:
-            raise TypeError("q, k_new, v_new and the caches share one dtype")
-        if not a.flags.c_contiguous:
-            raise ValueError("arrays must be C-contiguous (the caches are written in place)")
+    dt, scales = _cache_dtypes(q, (k_new, v_new), (k_cache, v_cache), k_scale, v_scale)
     B, Hq, D = q.shape
     R, Hkv, Smax, D2 = k_cache.shape
     assert D2 == D and v_cache.shape == k_cache.shape and k_new.shape == (B, Hkv, D)
@@ -172,7 +213,7 @@ def decode_dense(q, k_new, v_new, k_cache, v_cache, lengths, slot_ids=None, *,
     used = ctypes.c_int(0)
     nthr = default_threads() if threads is None else int(threads)
     keep = []
-    mods = _mods(sink, window, kept_prefix, keep)
+    mods = _mods(sink, window, kept_prefix, keep, scales)
     st = _load().orc_decode_dense(dt, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
                                   _ptr(v_cache), _ptr(lengths), _ptr(slot_ids),
                                   B, Hq, Hkv, D, R, Smax, _ptr(rows_a),
@@ -183,16 +224,11 @@ def decode_dense(q, k_new, v_new, k_cache, v_cache, lengths, slot_ids=None, *,
 
 def decode_paged(q, k_new, v_new, k_blocks, v_blocks, block_table, lengths, *,
                  rows=None, append=True, threads=None, sink=None, window=0,
-                 kept_prefix=0) -> OracleResult:
+                 kept_prefix=0, k_scale=None, v_scale=None) -> OracleResult:
     """One decode step on a paged cache (num_blocks, Hkv, block_size, D) with a
     (B, max_blocks) int32 block table (-1 = unused). Same contract as
     :func:`decode_dense` otherwise."""
-    dt = _dtype_code(q)
-    for a in (k_new, v_new, k_blocks, v_blocks):
-        if a.dtype != q.dtype:
-            raise TypeError("q, k_new, v_new and the blocks share one dtype")
-        if not a.flags.c_contiguous:
-            raise ValueError("arrays must be C-contiguous (the blocks are written in place)")
+    dt, scales = _cache_dtypes(q, (k_new, v_new), (k_blocks, v_blocks), k_scale, v_scale)
     B, Hq, D = q.shape
     NB, Hkv, BS, D2 = k_blocks.shape
     assert D2 == D and v_blocks.shape == k_blocks.shape and k_new.shape == (B, Hkv, D)
@@ -205,7 +241,7 @@ def decode_paged(q, k_new, v_new, k_blocks, v_blocks, block_table, lengths, *,
     used = ctypes.c_int(0)
     nthr = default_threads() if threads is None else int(threads)
     keep = []
-    mods = _mods(sink, window, kept_prefix, keep)
+    mods = _mods(sink, window, kept_prefix, keep, scales)
     st = _load().orc_decode_paged(dt, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_blocks),
                                   _ptr(v_blocks), _ptr(block_table), _ptr(lengths),
                                   B, Hq, Hkv, D, NB, BS, MB, _ptr(rows_a),
@@ -215,7 +251,8 @@ def decode_paged(q, k_new, v_new, k_blocks, v_blocks, block_table, lengths, *,
 
 
 def attend_dense(q, k_cache, v_cache, lengths, slot_ids=None, *, rows=None,
-                 threads=None, sink=None, window=0, kept_prefix=0) -> OracleResult:
+                 threads=None, sink=None, window=0, kept_prefix=0, k_scale=None,
+                 v_scale=None) -> OracleResult:
     """Read-only attend on a dense (R, Hkv, Smax, D) cache: every query head
     attends slots ``0 .. lengths[b]-1`` of its cache head; nothing is written.
     ``q`` may be float32 over a bfloat16 cache. Returns ``out`` (B, Hq, D)
@@ -235,7 +272,8 @@ def attend_dense(q, k_cache, v_cache, lengths, slot_ids=None, *, rows=None,
     used = ctypes.c_int(0)
     nthr = default_threads() if threads is None else int(threads)
     keep = []
-    mods = _mods(sink, window, kept_prefix, keep)
+    mods = _mods(sink, window, kept_prefix, keep,
+                 (k_scale, v_scale, qt) if kt == E4M3 else None)
     st = _load().orc_attend_dense(qt, kt, _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(lengths),
                                   _ptr(slot_ids), B, Hq, Hkv, D, R, Smax, _ptr(rows_a),
                                   0 if rows_a is None else len(rows_a), _ptr(out),
@@ -244,7 +282,8 @@ def attend_dense(q, k_cache, v_cache, lengths, slot_ids=None, *, rows=None,
 
 
 def attend_paged(q, k_blocks, v_blocks, block_table, lengths, *, rows=None,
-                 threads=None, sink=None, window=0, kept_prefix=0) -> OracleResult:
+                 threads=None, sink=None, window=0, kept_prefix=0, k_scale=None,
+                 v_scale=None) -> OracleResult:
     """Read-only attend on a paged cache; same contract as :func:`attend_dense`."""
     qt = _dtype_code(q)
     kt = _dtype_code(k_blocks)
@@ -262,7 +301,8 @@ def attend_paged(q, k_blocks, v_blocks, block_table, lengths, *, rows=None,
     used = ctypes.c_int(0)
     nthr = default_threads() if threads is None else int(threads)
     keep = []
-    mods = _mods(sink, window, kept_prefix, keep)
+    mods = _mods(sink, window, kept_prefix, keep,
+                 (k_scale, v_scale, qt) if kt == E4M3 else None)
     st = _load().orc_attend_paged(qt, kt, _ptr(q), _ptr(k_blocks), _ptr(v_blocks),
                                   _ptr(block_table), _ptr(lengths), B, Hq, Hkv, D, NB, BS, MB,
                                   _ptr(rows_a), 0 if rows_a is None else len(rows_a), _ptr(out),
@@ -271,18 +311,14 @@ def attend_paged(q, k_blocks, v_blocks, block_table, lengths, *, rows=None,
 
 
 def decode_multi_dense(q, k_new, v_new, k_cache, v_cache, lengths, cu_q, slot_ids=None, *,
-                       append=True, threads=None, sink=None, window=0, kept_prefix=0) -> OracleResult:
+                       append=True, threads=None, sink=None, window=0, kept_prefix=0,
+                       k_scale=None, v_scale=None) -> OracleResult:
     """Multi-token step on a dense (R, Hkv, Smax, D) cache: the q_len[b] =
     cu_q[b+1] - cu_q[b] new tokens of row b (rows cu_q[b].. of the packed
     q (T, Hq, D), k_new / v_new (T, Hkv, D)) are appended in place at slots
     lengths[b] + i, and token i attends slots 0 .. lengths[b] + i. Returns
     ``out`` (T, Hq, D) float64."""
-    dt = _dtype_code(q)
-    for a in (k_new, v_new, k_cache, v_cache):
-        if a.dtype != q.dtype:
-            raise TypeError("q, k_new, v_new and the caches share one dtype")
-        if not a.flags.c_contiguous:
-            raise ValueError("arrays must be C-contiguous (the caches are written in place)")
+    dt, scales = _cache_dtypes(q, (k_new, v_new), (k_cache, v_cache), k_scale, v_scale)
     T, Hq, D = q.shape
     R, Hkv, Smax, D2 = k_cache.shape
     assert D2 == D and v_cache.shape == k_cache.shape and k_new.shape == (T, Hkv, D)
@@ -293,7 +329,7 @@ def decode_multi_dense(q, k_new, v_new, k_cache, v_cache, lengths, cu_q, slot_id
     used = ctypes.c_int(0)
     nthr = default_threads() if threads is None else int(threads)
     keep = []
-    mods = _mods(sink, window, kept_prefix, keep)
+    mods = _mods(sink, window, kept_prefix, keep, scales)
     st = _load().orc_decode_multi_dense(dt, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
                                         _ptr(v_cache), _ptr(lengths), _ptr(cu_q), _ptr(slot_ids), B, T,
                                         Hq, Hkv, D, R, Smax, int(bool(append)), _ptr(out),
@@ -302,15 +338,11 @@ def decode_multi_dense(q, k_new, v_new, k_cache, v_cache, lengths, cu_q, slot_id
 
 
 def decode_multi_paged(q, k_new, v_new, k_blocks, v_blocks, block_table, lengths, cu_q, *,
-                       append=True, threads=None, sink=None, window=0, kept_prefix=0) -> OracleResult:
+                       append=True, threads=None, sink=None, window=0, kept_prefix=0,
+                       k_scale=None, v_scale=None) -> OracleResult:
     """Multi-token step on a paged cache; same contract as
     :func:`decode_multi_dense`."""
-    dt = _dtype_code(q)
-    for a in (k_new, v_new, k_blocks, v_blocks):
-        if a.dtype != q.dtype:
-            raise TypeError("q, k_new, v_new and the blocks share one dtype")
-        if not a.flags.c_contiguous:
-            raise ValueError("arrays must be C-contiguous (the blocks are written in place)")
+    dt, scales = _cache_dtypes(q, (k_new, v_new), (k_blocks, v_blocks), k_scale, v_scale)
     T, Hq, D = q.shape
     NB, Hkv, BS, D2 = k_blocks.shape
     assert D2 == D and v_blocks.shape == k_blocks.shape and k_new.shape == (T, Hkv, D)
@@ -322,7 +354,7 @@ def decode_multi_paged(q, k_new, v_new, k_blocks, v_blocks, block_table, lengths
     used = ctypes.c_int(0)
     nthr = default_threads() if threads is None else int(threads)
     keep = []
-    mods = _mods(sink, window, kept_prefix, keep)
+    mods = _mods(sink, window, kept_prefix, keep, scales)
     st = _load().orc_decode_multi_paged(dt, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_blocks),
                                         _ptr(v_blocks), _ptr(block_table), _ptr(lengths), _ptr(cu_q), B,
                                         T, Hq, Hkv, D, NB, BS, MB, int(bool(append)), _ptr(out),

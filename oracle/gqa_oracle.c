@@ -27,6 +27,12 @@
  * attends slots 0 .. lengths[b] + i (the causal bound); q_len = 1 everywhere
  * is the decode step.
  *
+ * A quantised cache (kv dtype ORC_E4M3) holds OCP FP8 E4M3 bytes with one
+ * float32 scale per cache head for K and one for V: K = k_scale[kvh] * K8,
+ * V = v_scale[kvh] * V8. The query and the new keys / values keep their own
+ * dtype (new_dtype); the append stores E4M3(float32(k_new) / k_scale), rounded
+ * to nearest even and saturated to the largest finite value.
+ *
  * Optional softmax modifiers (orc_mods, any entry point), with the query at
  * position L (the new token, or the last valid slot of the attend):
  *   window W > 0   slot j is attended only if L - W < j (the W positions up
@@ -73,6 +79,11 @@
  *    attends the query's own key only); the sink is a logit in the same units
  *    as s_j (already scaled, not multiplied by 1/sqrt(D)); a kept prefix has
  *    no effect without a window; window < 0 is refused like a negative P.
+ *  - quantised cache ("groupQueryAttention" names kScale / vScale and says
+ *    nothing more): per-cache-head float32 scales, E4M3 bytes, dequantised
+ *    value = scale * decoded byte; the new key / value is divided by the
+ *    scale in float32 (round to nearest) and encoded round-to-nearest-even
+ *    with saturation to +-448; NaN encodes to 0x7F.
  *  - multi-token: lengths[b] is the write offset (tokens already cached), so
  *    cu_seqlens_k[b] = lengths[b] + q_len[b]; cu_q[0] = 0, cu_q nondecreasing,
  *    cu_q[B] = T; 0 <= lengths[b] and lengths[b] + q_len[b] <= capacity; a
@@ -96,16 +107,55 @@
 #include <string.h>
 #include <unistd.h>
 
-enum { ORC_F32 = 0, ORC_BF16 = 1 };
+enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_E4M3 = 2 };
 enum { ORC_OK = 0, ORC_INVALID_ARGUMENT = 1 };
 
-/* Softmax modifiers; a NULL orc_mods pointer means none. */
+/* Softmax modifiers and the scales of a quantised cache; a NULL orc_mods
+ * pointer means none of them. */
 typedef struct {
     const float *head_sink;         /* (Hq,) logits, or NULL: no sink          */
     int window;                     /* 0: no window; > 0: W                    */
     int kept_prefix;                /* P for every row (rows NULL), >= 0       */
     const int32_t *kept_prefix_rows;/* (B,) P per batch row, or NULL           */
+    const float *k_scale, *v_scale; /* (Hkv,) E4M3 cache scales                */
+    int new_dtype;                  /* E4M3 cache: dtype of q, k_new, v_new    */
 } orc_mods;
+
+/* ------------------------------------------------------------- E4M3 ----
+ * OCP 8-bit floating point, E4M3: sign bit, 4 exponent bits (bias 7), 3
+ * mantissa bits; no infinities; S.1111.111 is NaN; exponent field 0 holds
+ * the subnormals m/8 * 2^-6; the largest finite magnitude is 1.75 * 2^8 = 448. */
+double orc_e4m3_decode(uint8_t c)
+{
+    const int e = (c >> 3) & 15, m = c & 7;
+    if (e == 15 && m == 7)
+        return NAN;
+    const double v = e == 0 ? ldexp(m / 8.0, -6) : ldexp(1.0 + m / 8.0, e - 7);
+    return (c & 0x80) ? -v : v;
+}
+
+/* Nearest E4M3 code to x, ties to the even code (mantissa bit 0 clear),
+ * magnitudes at or above 448 saturated to 448, NaN to 0x7F. The finite
+ * non-negative codes 0x00 .. 0x7E are increasing in value, so the nearest
+ * one is found by a scan. */
+uint8_t orc_e4m3_encode(float x)
+{
+    if (isnan(x))
+        return 0x7F;
+    const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    const double a = fabs((double)x);
+    if (a >= 448.0)
+        return sign | 0x7E;
+    int lo = 0;
+    while (lo < 0x7E && orc_e4m3_decode((uint8_t)(lo + 1)) <= a)
+        ++lo;                              /* largest code with value <= a */
+    if (orc_e4m3_decode((uint8_t)lo) == a)
+        return sign | (uint8_t)lo;
+    const int hi = lo + 1;
+    const double dl = a - orc_e4m3_decode((uint8_t)lo), dh = orc_e4m3_decode((uint8_t)hi) - a;
+    const int pick = dl < dh ? lo : (dh < dl ? hi : ((lo & 1) ? hi : lo));
+    return sign | (uint8_t)pick;
+}
 
 /* One element of a float32 or bfloat16 array, widened exactly to double. */
 static double elem(const void *base, size_t i, int dtype)
@@ -119,7 +169,9 @@ static double elem(const void *base, size_t i, int dtype)
     return (double)f;
 }
 
-static size_t esize(int dtype) { return dtype == ORC_F32 ? 4 : 2; }
+static int usable_dtype(int dtype) { return dtype == ORC_F32 || dtype == ORC_BF16; }
+
+static size_t esize(int dtype) { return dtype == ORC_F32 ? 4 : (dtype == ORC_E4M3 ? 1 : 2); }
 
 static void copy_vec(void *dst, size_t dst_i, const void *src, size_t src_i, int D, int dtype)
 {
@@ -239,6 +291,7 @@ static size_t slot_index(const layout *lay, int b, int kvh, int s)
 
 typedef struct {
     int q_dtype, kv_dtype;   /* the decode step has one dtype for all */
+    int new_dtype;           /* k_new / v_new (differs from kv_dtype for an E4M3 cache) */
     int attend;              /* 1: read-only attend over slots 0 .. lengths[b]-1 */
     const void *q, *k_new, *v_new;
     void *k_cache, *v_cache;
@@ -274,6 +327,8 @@ static int mods_ok(const orc_mods *M, int B)
 {
     if (!M)
         return 1;
+    if ((M->k_scale == NULL) != (M->v_scale == NULL))
+        return 0;
     if (M->window < 0 || (!M->kept_prefix_rows && M->kept_prefix < 0))
         return 0;
     if (M->kept_prefix_rows)
@@ -281,6 +336,57 @@ static int mods_ok(const orc_mods *M, int B)
             if (M->kept_prefix_rows[b] < 0)
                 return 0;
     return 1;
+}
+
+/* The job's dtypes: q_dtype for the query; the cache's kv_dtype; the new
+ * keys / values share the cache dtype, except over an E4M3 cache, which takes
+ * their dtype and its scales from mods. 0 when the combination is invalid. */
+static int setup_dtypes(job *J, int q_dtype, int kv_dtype, const orc_mods *mods)
+{
+    J->q_dtype = q_dtype;
+    J->kv_dtype = kv_dtype;
+    J->new_dtype = kv_dtype;
+    if (kv_dtype == ORC_E4M3) {
+        if (!mods || !mods->k_scale || !usable_dtype(mods->new_dtype))
+            return 0;
+        J->new_dtype = mods->new_dtype;
+    } else if (!usable_dtype(kv_dtype)) {
+        return 0;
+    }
+    return usable_dtype(q_dtype);
+}
+
+/* Element d of slot j of a cache (the dequantised value for E4M3). */
+static double cache_elem(const job *J, const void *cache, const float *scale, size_t i, int kvh)
+{
+    if (J->kv_dtype == ORC_E4M3)
+        return (double)scale[kvh] * orc_e4m3_decode(((const uint8_t *)cache)[i]);
+    return elem(cache, i, J->kv_dtype);
+}
+
+/* The value an append stores for new element x of cache head kvh, as the
+ * cache then reads it back. */
+static double stored_new(const job *J, const void *news, const float *scale, size_t i, int kvh)
+{
+    const double x = elem(news, i, J->new_dtype);
+    if (J->kv_dtype != ORC_E4M3)
+        return x;
+    const float y = (float)x / scale[kvh];     /* float32 division, round to nearest */
+    return (double)scale[kvh] * orc_e4m3_decode(orc_e4m3_encode(y));
+}
+
+/* Append of D new elements into a cache slot. */
+static void append_vec(const job *J, void *cache, size_t dst, const void *news, size_t src,
+                       const float *scale, int kvh)
+{
+    if (J->kv_dtype != ORC_E4M3) {
+        copy_vec(cache, dst, news, src, J->D, J->kv_dtype);
+        return;
+    }
+    for (int d = 0; d < J->D; ++d) {
+        const float y = (float)elem(news, src + d, J->new_dtype) / scale[kvh];
+        ((uint8_t *)cache)[dst + d] = orc_e4m3_encode(y);
+    }
 }
 
 /* Element index of the new key / value of token `tok`, cache head kvh. */
@@ -296,6 +402,7 @@ static size_t new_index(const job *J, int tok, int kvh)
 static void attend_heads(job *J, int b, int kvh, int L, int tok, int first_new, int new_tok0)
 {
     const int D = J->D, G = J->Hq / J->Hkv;
+    const float *KS = J->mods ? J->mods->k_scale : NULL, *VS = J->mods ? J->mods->v_scale : NULL;
     double *s = (double *)malloc(sizeof(double) * (size_t)(L + 1));
     for (int g = 0; g < G; ++g) {
         const int h = kvh * G + g;           /* floor(h / G) == kvh */
@@ -306,8 +413,8 @@ static void attend_heads(job *J, int b, int kvh, int L, int tok, int first_new, 
             double dot = 0.0;
             for (int d = 0; d < D; ++d) {
                 double kd = (j >= first_new)
-                                ? elem(J->k_new, new_index(J, new_tok0 + j - first_new, kvh) + d, J->kv_dtype)
-                                : elem(J->k_cache, slot_index(&J->lay, b, kvh, j) + d, J->kv_dtype);
+                                ? stored_new(J, J->k_new, KS, new_index(J, new_tok0 + j - first_new, kvh) + d, kvh)
+                                : cache_elem(J, J->k_cache, KS, slot_index(&J->lay, b, kvh, j) + d, kvh);
                 dot += elem(J->q, q_i + d, J->q_dtype) * kd;
             }
             s[j] = dot / sqrt((double)D);
@@ -337,8 +444,8 @@ static void attend_heads(job *J, int b, int kvh, int L, int tok, int first_new, 
             double w = exp(s[j] - m) / Z;
             for (int d = 0; d < D; ++d) {
                 double vd = (j >= first_new)
-                                ? elem(J->v_new, new_index(J, new_tok0 + j - first_new, kvh) + d, J->kv_dtype)
-                                : elem(J->v_cache, slot_index(&J->lay, b, kvh, j) + d, J->kv_dtype);
+                                ? stored_new(J, J->v_new, VS, new_index(J, new_tok0 + j - first_new, kvh) + d, kvh)
+                                : cache_elem(J, J->v_cache, VS, slot_index(&J->lay, b, kvh, j) + d, kvh);
                 o[d] += w * vd;
             }
         }
@@ -350,7 +457,7 @@ static void attend_heads(job *J, int b, int kvh, int L, int tok, int first_new, 
  * heads over the attended slots 0 .. L. */
 static void one_pair(job *J, int b, int kvh)
 {
-    const int D = J->D;
+    const float *KS = J->mods ? J->mods->k_scale : NULL, *VS = J->mods ? J->mods->v_scale : NULL;
     if (J->cu_q) {
         /* multi-token: tokens t0 .. t0 + nq - 1 take slots Lb .. Lb + nq - 1,
          * and token i attends slots 0 .. Lb + i */
@@ -358,8 +465,8 @@ static void one_pair(job *J, int b, int kvh)
         if (J->do_append)
             for (int i = 0; i < nq; ++i) {
                 size_t dst = slot_index(&J->lay, b, kvh, Lb + i);
-                copy_vec(J->k_cache, dst, J->k_new, new_index(J, t0 + i, kvh), D, J->kv_dtype);
-                copy_vec(J->v_cache, dst, J->v_new, new_index(J, t0 + i, kvh), D, J->kv_dtype);
+                append_vec(J, J->k_cache, dst, J->k_new, new_index(J, t0 + i, kvh), KS, kvh);
+                append_vec(J, J->v_cache, dst, J->v_new, new_index(J, t0 + i, kvh), VS, kvh);
             }
         for (int i = 0; i < nq; ++i)
             attend_heads(J, b, kvh, Lb + i, t0 + i, J->do_append ? INT_MAX : Lb, t0);
@@ -370,8 +477,8 @@ static void one_pair(job *J, int b, int kvh)
 
     if (!J->attend && J->do_append) {
         size_t dst = slot_index(&J->lay, b, kvh, L);
-        copy_vec(J->k_cache, dst, J->k_new, new_index(J, b, kvh), D, J->kv_dtype);
-        copy_vec(J->v_cache, dst, J->v_new, new_index(J, b, kvh), D, J->kv_dtype);
+        append_vec(J, J->k_cache, dst, J->k_new, new_index(J, b, kvh), KS, kvh);
+        append_vec(J, J->v_cache, dst, J->v_new, new_index(J, b, kvh), VS, kvh);
     }
     attend_heads(J, b, kvh, L, b, from_new ? L : INT_MAX, b);
 }
@@ -432,13 +539,14 @@ int orc_decode_dense(int dtype, const void *q, const void *k_new, const void *v_
                      const int32_t *rows, int nrows, int do_append, double *out,
                      const orc_mods *mods, int nthreads, int *threads_used)
 {
-    if (!usable_shape(B, Hq, Hkv, D) || (dtype != ORC_F32 && dtype != ORC_BF16) || !mods_ok(mods, B))
+    if (!usable_shape(B, Hq, Hkv, D) || !mods_ok(mods, B))
         return ORC_INVALID_ARGUMENT;
     if (orc_validate_dense(lengths, slot_ids, B, R, Smax) != ORC_OK)
         return ORC_INVALID_ARGUMENT;
     job J;
     memset(&J, 0, sizeof J);
-    J.q_dtype = J.kv_dtype = dtype;
+    if (!setup_dtypes(&J, dtype == ORC_E4M3 && mods ? mods->new_dtype : dtype, dtype, mods))
+        return ORC_INVALID_ARGUMENT;
     J.q = q; J.k_new = k_new; J.v_new = v_new;
     J.k_cache = k_cache; J.v_cache = v_cache;
     J.lengths = lengths;
@@ -464,13 +572,14 @@ int orc_decode_paged(int dtype, const void *q, const void *k_new, const void *v_
                      const int32_t *rows, int nrows, int do_append, double *out,
                      const orc_mods *mods, int nthreads, int *threads_used)
 {
-    if (!usable_shape(B, Hq, Hkv, D) || (dtype != ORC_F32 && dtype != ORC_BF16) || !mods_ok(mods, B))
+    if (!usable_shape(B, Hq, Hkv, D) || !mods_ok(mods, B))
         return ORC_INVALID_ARGUMENT;
     if (orc_validate_paged(lengths, block_table, B, num_blocks, block_size, max_blocks) != ORC_OK)
         return ORC_INVALID_ARGUMENT;
     job J;
     memset(&J, 0, sizeof J);
-    J.q_dtype = J.kv_dtype = dtype;
+    if (!setup_dtypes(&J, dtype == ORC_E4M3 && mods ? mods->new_dtype : dtype, dtype, mods))
+        return ORC_INVALID_ARGUMENT;
     J.q = q; J.k_new = k_new; J.v_new = v_new;
     J.k_cache = k_blocks; J.v_cache = v_blocks;
     J.lengths = lengths;
@@ -488,7 +597,6 @@ int orc_decode_paged(int dtype, const void *q, const void *k_new, const void *v_
     return ORC_OK;
 }
 
-static int usable_dtype(int dtype) { return dtype == ORC_F32 || dtype == ORC_BF16; }
 
 /* Read-only attend on a dense or slot_ids cache (R, Hkv, Smax, D): slots
  * 0 .. lengths[b]-1 of the row, nothing written. q_dtype and kv_dtype are
@@ -499,15 +607,14 @@ int orc_attend_dense(int q_dtype, int kv_dtype, const void *q, const void *k_cac
                      const int32_t *rows, int nrows, double *out, const orc_mods *mods,
                      int nthreads, int *threads_used)
 {
-    if (!usable_shape(B, Hq, Hkv, D) || !usable_dtype(q_dtype) || !usable_dtype(kv_dtype) ||
-        !mods_ok(mods, B))
+    if (!usable_shape(B, Hq, Hkv, D) || !mods_ok(mods, B))
         return ORC_INVALID_ARGUMENT;
     if (orc_validate_attend_dense(lengths, slot_ids, B, R, Smax) != ORC_OK)
         return ORC_INVALID_ARGUMENT;
     job J;
     memset(&J, 0, sizeof J);
-    J.q_dtype = q_dtype;
-    J.kv_dtype = kv_dtype;
+    if (!setup_dtypes(&J, q_dtype, kv_dtype, mods))
+        return ORC_INVALID_ARGUMENT;
     J.attend = 1;
     J.q = q;
     J.k_cache = (void *)k_cache; J.v_cache = (void *)v_cache;   /* only read */
@@ -531,16 +638,15 @@ int orc_attend_paged(int q_dtype, int kv_dtype, const void *q, const void *k_blo
                      const int32_t *rows, int nrows, double *out, const orc_mods *mods,
                      int nthreads, int *threads_used)
 {
-    if (!usable_shape(B, Hq, Hkv, D) || !usable_dtype(q_dtype) || !usable_dtype(kv_dtype) ||
-        !mods_ok(mods, B))
+    if (!usable_shape(B, Hq, Hkv, D) || !mods_ok(mods, B))
         return ORC_INVALID_ARGUMENT;
     if (orc_validate_attend_paged(lengths, block_table, B, num_blocks, block_size, max_blocks)
         != ORC_OK)
         return ORC_INVALID_ARGUMENT;
     job J;
     memset(&J, 0, sizeof J);
-    J.q_dtype = q_dtype;
-    J.kv_dtype = kv_dtype;
+    if (!setup_dtypes(&J, q_dtype, kv_dtype, mods))
+        return ORC_INVALID_ARGUMENT;
     J.attend = 1;
     J.q = q;
     J.k_cache = (void *)k_blocks; J.v_cache = (void *)v_blocks;
@@ -611,13 +717,14 @@ int orc_decode_multi_dense(int dtype, const void *q, const void *k_new, const vo
                            int Smax, int do_append, double *out, const orc_mods *mods, int nthreads,
                            int *threads_used)
 {
-    if (!usable_shape(B, Hq, Hkv, D) || !usable_dtype(dtype) || !mods_ok(mods, B))
+    if (!usable_shape(B, Hq, Hkv, D) || !mods_ok(mods, B))
         return ORC_INVALID_ARGUMENT;
     if (orc_validate_multi_dense(lengths, cu_q, slot_ids, B, T, R, Smax) != ORC_OK)
         return ORC_INVALID_ARGUMENT;
     job J;
     memset(&J, 0, sizeof J);
-    J.q_dtype = J.kv_dtype = dtype;
+    if (!setup_dtypes(&J, dtype == ORC_E4M3 && mods ? mods->new_dtype : dtype, dtype, mods))
+        return ORC_INVALID_ARGUMENT;
     J.q = q; J.k_new = k_new; J.v_new = v_new;
     J.k_cache = k_cache; J.v_cache = v_cache;
     J.lengths = lengths;
@@ -641,14 +748,15 @@ int orc_decode_multi_paged(int dtype, const void *q, const void *k_new, const vo
                            int D, int num_blocks, int block_size, int max_blocks, int do_append,
                            double *out, const orc_mods *mods, int nthreads, int *threads_used)
 {
-    if (!usable_shape(B, Hq, Hkv, D) || !usable_dtype(dtype) || !mods_ok(mods, B))
+    if (!usable_shape(B, Hq, Hkv, D) || !mods_ok(mods, B))
         return ORC_INVALID_ARGUMENT;
     if (orc_validate_multi_paged(lengths, cu_q, block_table, B, T, num_blocks, block_size, max_blocks) !=
         ORC_OK)
         return ORC_INVALID_ARGUMENT;
     job J;
     memset(&J, 0, sizeof J);
-    J.q_dtype = J.kv_dtype = dtype;
+    if (!setup_dtypes(&J, dtype == ORC_E4M3 && mods ? mods->new_dtype : dtype, dtype, mods))
+        return ORC_INVALID_ARGUMENT;
     J.q = q; J.k_new = k_new; J.v_new = v_new;
     J.k_cache = k_blocks; J.v_cache = v_blocks;
     J.lengths = lengths;

@@ -52,9 +52,15 @@ MUTANTS = {
                          "attend_heads(J, b, kvh, Lb + nq - 1, t0 + i, J->do_append ? INT_MAX : Lb, t0);"),
     "multi_append_offset": ("size_t dst = slot_index(&J->lay, b, kvh, Lb + i);",
                             "size_t dst = slot_index(&J->lay, b, kvh, Lb + i + (i > 0));"),
-    "multi_same_token_appended": ("copy_vec(J->k_cache, dst, J->k_new, new_index(J, t0 + i, kvh), D, J->kv_dtype);",
-                                  "copy_vec(J->k_cache, dst, J->k_new, new_index(J, t0, kvh), D, J->kv_dtype);"),
+    "multi_same_token_appended": ("append_vec(J, J->k_cache, dst, J->k_new, new_index(J, t0 + i, kvh), KS, kvh);",
+                                  "append_vec(J, J->k_cache, dst, J->k_new, new_index(J, t0, kvh), KS, kvh);"),
     "multi_cu_q_unchecked": ("        if (cu_q[b + 1] < cu_q[b])\n            return ORC_INVALID_ARGUMENT;\n", ""),
+    "e4m3_exponent_bias": ("ldexp(1.0 + m / 8.0, e - 7)", "ldexp(1.0 + m / 8.0, e - 8)"),
+    "e4m3_ties_away": ("(lo & 1) ? hi : lo", "hi"),
+    "e4m3_scale_not_applied": ("return (double)scale[kvh] * orc_e4m3_decode(((const uint8_t *)cache)[i]);",
+                               "return orc_e4m3_decode(((const uint8_t *)cache)[i]);"),
+    "e4m3_append_not_divided": ("const float y = (float)elem(news, src + d, J->new_dtype) / scale[kvh];",
+                                "const float y = (float)elem(news, src + d, J->new_dtype);"),
     "query_head_offset": ("const size_t q_i = ((size_t)tok * J->Hq + h) * D;", "const size_t q_i = ((size_t)tok * J->Hq + g) * D;"),
 }
 

@@ -959,3 +959,137 @@ def test_multi_validate_rules():
     Lp = np.array([3, 1, 4], np.int32)
     assert oracle.validate_multi_paged(Lp, np.array([0, 2, 3, 5], np.int32), bt, 5, 6, 4) == ok       # 4 + 1 slots / 8
     assert oracle.validate_multi_paged(Lp, np.array([0, 2, 3, 8], np.int32), bt, 8, 6, 4) == bad      # 4 + 5 > 8
+
+
+# ------------------------------------------------------ E4M3 (FP8) KV cache
+#
+# [P5] names kScale / vScale and says no more. Reading: OCP FP8 E4M3 bytes
+# with one float32 scale per cache head, K = k_scale * K8; the append stores
+# E4M3(float32(k_new) / k_scale), round to nearest even, saturating at 448.
+
+def _e4m3_lib(x):
+    """torch's float8_e4m3fn (a library routine) for in-range float32 values."""
+    return torch.from_numpy(np.asarray(x, np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def test_e4m3_decode_matches_library_and_closed_forms():
+    codes = np.arange(256, dtype=np.uint8)
+    lib = torch.from_numpy(codes).view(torch.float8_e4m3fn).float().numpy()
+    ours = np.array([oracle.e4m3_decode(int(c)) for c in codes])
+    assert np.array_equal(np.isnan(ours), np.isnan(lib))
+    ok = ~np.isnan(ours)
+    assert np.array_equal(ours[ok], lib[ok].astype(np.float64))
+    assert oracle.e4m3_decode(0x7E) == 448.0 and oracle.e4m3_decode(0x38) == 1.0
+    assert oracle.e4m3_decode(0x08) == 2.0 ** -6 and oracle.e4m3_decode(0x01) == 2.0 ** -9
+    assert math.copysign(1.0, oracle.e4m3_decode(0x80)) == -1.0 and np.isnan(oracle.e4m3_decode(0x7F))
+
+
+def test_e4m3_encode_round_trip_and_saturation():
+    for c in list(range(0x7F)) + list(range(0x80, 0xFF)):
+        assert oracle.e4m3_encode(oracle.e4m3_decode(c)) == c, hex(c)
+    assert oracle.e4m3_encode(1000.0) == 0x7E and oracle.e4m3_encode(-1e9) == 0xFE
+    assert oracle.e4m3_encode(float("inf")) == 0x7E and oracle.e4m3_encode(float("-inf")) == 0xFE
+    assert oracle.e4m3_encode(float("nan")) == 0x7F
+
+
+def test_e4m3_encode_matches_library_rounding():
+    """Random in-range floats and every midpoint between neighbouring codes
+    (ties go to the even code) against torch's cast."""
+    rng = np.random.default_rng(60)
+    xs = np.concatenate([rng.uniform(-440, 440, 2000), rng.normal(0, 1, 2000), rng.normal(0, 0.01, 2000)])
+    mids = []
+    for c in range(0x7E):
+        mids.append((oracle.e4m3_decode(c) + oracle.e4m3_decode(c + 1)) / 2)
+    xs = np.concatenate([xs, mids, -np.asarray(mids)]).astype(np.float32)
+    ours = np.array([oracle.e4m3_encode(float(x)) for x in xs], np.uint8)
+    assert np.array_equal(ours, _e4m3_lib(xs))
+
+
+def _e4m3_case(seed, Hkv=2, B=3, S=20, D=8):
+    rng = np.random.default_rng(seed)
+    finite = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8)
+    kc = rng.choice(finite, size=(B, Hkv, S, D)).astype(np.uint8)
+    vc = rng.choice(finite, size=(B, Hkv, S, D)).astype(np.uint8)
+    lens = rng.integers(0, S, size=B).astype(np.int32)
+    dec = np.vectorize(oracle.e4m3_decode)
+    kn_codes = rng.choice(finite, size=(B, Hkv, D)).astype(np.uint8)
+    vn_codes = rng.choice(finite, size=(B, Hkv, D)).astype(np.uint8)
+    return kc, vc, lens, dec, kn_codes, vn_codes
+
+
+def test_e4m3_unit_scales_equal_the_bf16_step():
+    """E4M3 values are exact in bf16: with scales 1 the quantised step equals
+    the bf16 step on the decoded values bit for bit, and the append stores
+    the new values' own codes."""
+    kc, vc, lens, dec, knc, vnc = _e4m3_case(61)
+    B, Hkv, S, D = kc.shape
+    to_bf16 = lambda a: to_np(torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16))
+    q = to_bf16(np.random.default_rng(1).normal(size=(B, 4, D)))
+    kn, vn = to_bf16(dec(knc)), to_bf16(dec(vnc))
+    one = np.ones(Hkv, np.float32)
+    k8, v8 = kc.copy(), vc.copy()
+    r8 = oracle.decode_dense(q, kn, vn, k8, v8, lens, k_scale=one, v_scale=one)
+    kb, vb = to_bf16(dec(kc)), to_bf16(dec(vc))
+    rb = oracle.decode_dense(q, kn, vn, kb, vb, lens)
+    assert r8.status == oracle.OK and r8.out.tobytes() == rb.out.tobytes()
+    for b in range(B):
+        assert k8[b, :, lens[b]].tobytes() == knc[b].tobytes() and v8[b, :, lens[b]].tobytes() == vnc[b].tobytes()
+
+
+def test_e4m3_scales_multiply_per_cache_head():
+    """Power-of-two scales are exact multipliers: the E4M3 step with
+    k_scale = 2^a, v_scale = 2^c per head equals the bf16 step on
+    scale * decoded values bit for bit."""
+    kc, vc, lens, dec, knc, vnc = _e4m3_case(62)
+    B, Hkv, S, D = kc.shape
+    ks = np.array([0.25, 4.0], np.float32)
+    vs = np.array([2.0, 0.5], np.float32)
+    to_bf16 = lambda a: to_np(torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16))
+    q = to_bf16(np.random.default_rng(2).normal(size=(B, 4, D)))
+    kn = to_bf16(dec(knc) * ks[None, :, None])
+    vn = to_bf16(dec(vnc) * vs[None, :, None])
+    r8 = oracle.decode_dense(q, kn, vn, kc.copy(), vc.copy(), lens, k_scale=ks, v_scale=vs)
+    rb = oracle.decode_dense(q, kn, vn, to_bf16(dec(kc) * ks[None, :, None, None]),
+                             to_bf16(dec(vc) * vs[None, :, None, None]), lens)
+    assert r8.out.tobytes() == rb.out.tobytes()
+
+
+def test_e4m3_append_quantises_after_division():
+    """The stored byte is the library's E4M3 cast of float32(k_new) / k_scale."""
+    kc, vc, lens, dec, _, _ = _e4m3_case(63)
+    B, Hkv, S, D = kc.shape
+    rng = np.random.default_rng(3)
+    # in range for the library cast (torch's cast does not saturate)
+    kn = np.clip(rng.normal(size=(B, Hkv, D)), -4, 4).astype(np.float32) * 3
+    vn = np.clip(rng.normal(size=(B, Hkv, D)), -4, 4).astype(np.float32)
+    ks = np.array([0.03, 0.11], np.float32)
+    vs = np.array([0.02, 0.05], np.float32)
+    q = rng.normal(size=(B, 4, D)).astype(np.float32)
+    k8, v8 = kc.copy(), vc.copy()
+    r = oracle.decode_dense(q, kn, vn, k8, v8, lens, k_scale=ks, v_scale=vs)
+    assert r.status == oracle.OK
+    for b in range(B):
+        assert np.abs(kn[b] / ks[:, None]).max() < 448
+        assert np.array_equal(k8[b, :, lens[b]], _e4m3_lib(kn[b] / ks[:, None]))
+        assert np.array_equal(v8[b, :, lens[b]], _e4m3_lib(vn[b] / vs[:, None]))
+
+
+def test_e4m3_library_sdpa_on_dequantised_cache():
+    """torch SDPA in float64 over scale * decoded slots (the stored new token
+    included), per cache head, repeated for the G query heads."""
+    kc, vc, lens, dec, _, _ = _e4m3_case(64, Hkv=2, B=3, S=24, D=16)
+    B, Hkv, S, D = kc.shape
+    rng = np.random.default_rng(4)
+    q = rng.normal(size=(B, 6, D)).astype(np.float32)
+    kn = rng.normal(size=(B, Hkv, D)).astype(np.float32)
+    vn = rng.normal(size=(B, Hkv, D)).astype(np.float32)
+    ks = np.array([0.05, 0.02], np.float32)
+    vs = np.array([0.01, 0.03], np.float32)
+    k8, v8 = kc.copy(), vc.copy()
+    r = oracle.decode_dense(q, kn, vn, k8, v8, lens, k_scale=ks, v_scale=vs)
+    for b in range(B):
+        L = int(lens[b])
+        k = torch.from_numpy(dec(k8[b, :, :L + 1]) * ks[:, None, None].astype(np.float64)).repeat_interleave(3, 0)
+        v = torch.from_numpy(dec(v8[b, :, :L + 1]) * vs[:, None, None].astype(np.float64)).repeat_interleave(3, 0)
+        o = torch.nn.functional.scaled_dot_product_attention(torch.from_numpy(q[b]).double()[:, None], k, v)[:, 0]
+        np.testing.assert_allclose(r.out[b], o.numpy(), rtol=1e-12, atol=1e-12)
