@@ -23,6 +23,8 @@ With --impl reference the oracle itself is timed as the reference arm.
 valid slots; a float32 query over the workload's cache unless --q-dtype cache).
 --window W / --kept-prefix P / --sink add the softmax modifiers; the KV bytes
 then count only the slots inside the window or the prefix.
+--kv e4m3 stores the cache as E4M3 (FP8) bytes with per-head scales (the KV
+bytes are then one per element; q, k_new, v_new stay bfloat16).
 --q-len N times the multi-token step (N new tokens per row, causal); its KV
 bytes count the cached slots once (a row whose tokens span several chunks of
 8 / G tokens streams them once per chunk, which shows in the roofline).
@@ -68,6 +70,8 @@ def parse():
     ap.add_argument("--kept-prefix", type=int, default=0, help="kept prefix P (with a window)")
     ap.add_argument("--sink", action="store_true", help="a per-head sink logit (seeded N(0,1))")
     ap.add_argument("--q-len", type=int, default=0, help="multi-token step with this many new tokens per row")
+    ap.add_argument("--kv", default="native", choices=["native", "e4m3"],
+                    help="cache element type: the workload's own or E4M3 bytes with per-head scales")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sched-pad", type=int, default=None,
                     help="schedule-only tiles per (row, head); default: the library's")
@@ -163,7 +167,7 @@ def algorithmic_bytes_multi(w, t) -> dict:
             "index_read": idx, "total": kv + 2 * new + q + out + idx}
 
 
-def algorithmic_bytes(w, t, attend=False, window=0, kept_prefix=0) -> dict:
+def algorithmic_bytes(w, t, attend=False, window=0, kept_prefix=0, kv_es=None) -> dict:
     """Bytes the step must move (no split partials): the KV read, the append
     write, the new K/V, q, out and the index reads. The decode step reads the
     lengths[b] cached slots (slot lengths[b] comes from k_new / v_new); the
@@ -172,16 +176,20 @@ def algorithmic_bytes(w, t, attend=False, window=0, kept_prefix=0) -> dict:
     import torch
     L = t["lengths"].to(torch.int64)
     es = w.elem_bytes
-    kv = int(cached_slots_read(L, attend, window, kept_prefix).sum().item()) * w.Hkv * w.D * 2 * es
-    new = 0 if attend else w.B * w.Hkv * w.D * es * 2
+    kes = es if kv_es is None else kv_es      # cache element bytes (1 for E4M3)
+    kv = int(cached_slots_read(L, attend, window, kept_prefix).sum().item()) * w.Hkv * w.D * 2 * kes
+    # the new token's K and V: read (their own dtype) and appended (cache element bytes)
+    new_read = 0 if attend else 2 * w.B * w.Hkv * w.D * es
+    new_write = 0 if attend else 2 * w.B * w.Hkv * w.D * kes
+    new = new_read + new_write
     idx = w.B * 4 * (2 if w.slot_ids else 1)
     if w.paged:
         touched = L if attend else L + 1
         idx += int(((touched + w.block_size - 1) // w.block_size).sum().item()) * 4
     q = t["q"].numel() * t["q"].element_size()
-    return {"kv_read": kv, "append_write": new, "new_kv_read": new,
+    return {"kv_read": kv, "append_write": new_write, "new_kv_read": new_read,
             "q_read": q, "out_write": w.B * w.Hq * w.D * 4, "index_read": idx,
-            "total": kv + 2 * new + q + w.B * w.Hq * w.D * 4 + idx}
+            "total": kv + new + q + w.B * w.Hq * w.D * 4 + idx}
 
 
 def step_fn(w, t, kernel, out, sched_pad=None, attend=False, mods=None, max_q=0):
@@ -335,7 +343,7 @@ def make_mods(args, w, dev):
 
 def mods_config(args):
     return {"window": args.window, "kept_prefix": args.kept_prefix, "sink": bool(args.sink),
-            "q_len": args.q_len or 1}
+            "q_len": args.q_len or 1, "kv": args.kv}
 
 
 def peaks():
@@ -421,14 +429,19 @@ def run_ours(args, ranks):
     multi = args.q_len > 0
     if multi and (attend or args.window or args.kept_prefix):
         raise SystemExit("--q-len times the plain multi-token step (no --op attend / window)")
+    fp8 = args.kv == "e4m3"
+    if fp8 and multi:
+        raise SystemExit("--kv e4m3 takes single-token steps")
     t = W.generate(w, dev, attend=attend, q_f32=attend and args.q_dtype != "cache",
-                   q_lens=[args.q_len] * w.B if multi else None)
+                   q_lens=[args.q_len] * w.B if multi else None, kv_e4m3=fp8)
     torch.cuda.synchronize()
     out = torch.empty(t["q"].shape[0], w.Hq, w.D, dtype=torch.float32, device=dev)
     mods = make_mods(args, w, dev)
+    if fp8:
+        mods = dict(mods or {}, k_scale=t["k_scale"], v_scale=t["v_scale"])
     step = step_fn(w, t, args.kernel, out, args.sched_pad, attend, mods, args.q_len)
     alg = algorithmic_bytes_multi(w, t) if multi else algorithmic_bytes(w, t, attend, args.window,
-                                                                         args.kept_prefix)
+                                                                         args.kept_prefix, 1 if fp8 else None)
     flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush_r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     flush_sink = torch.empty((), dtype=torch.float32, device=dev)
@@ -489,7 +502,7 @@ def run_ours(args, ranks):
     avg_main_s = ms_main / max(n_main, 1) * 1e-3
     hbm_peak, peak_kind = peaks()
     achieved = alg["total"] / avg_main_s / 1e9
-    traffic = None if (mods or multi) else traffic_for(main, w.name + ("/attend" if attend else ""))
+    traffic = None if (mods or multi or fp8) else traffic_for(main, w.name + ("/attend" if attend else ""))
 
     # ---- end to end through the public API, host buffers, copies inside
     Ke = min(K, 500)
@@ -522,7 +535,7 @@ def run_ours(args, ranks):
 
     # ---- CPU baseline: the oracle on host cores, rank 0 at N = 1 only
     cpu = None
-    if ranks.world == 1 and not args.no_cpu_baseline and not multi:
+    if ranks.world == 1 and not args.no_cpu_baseline and not multi and not fp8:
         rows = list(range(w.B))
         gbs, sec, threads = oracle_rate(w, t, rows, repeats=3, mods=mods)
         cpu = {"value": gbs, "unit": UNIT, "cores": threads, "kind": "oracle",

@@ -15,6 +15,11 @@ softmax of ``q.K/sqrt(D)``; the output is float32 (B, Hq, D).
 The read-only attend (``attend``, ``attend_paged``) attends slots
 ``0..lengths[b]-1`` (lengths counts the valid slots) and writes nothing but
 its output; its query may be float32 over a bfloat16 cache.
+
+A cache of E4M3 (FP8) bytes (``torch.uint8`` or ``torch.float8_e4m3fn``
+tensors) takes ``k_scale`` / ``v_scale`` float32 (Hkv,) tensors: K =
+k_scale[kvh] * K8; the decode step then takes bfloat16 q, k_new and v_new and
+quantises the appended token.
 """
 from __future__ import annotations
 
@@ -33,6 +38,17 @@ KERNELS = {"auto": 0, "simt": 1, "tc": 2}
 STATUS_BITS = {1: "bad length", 2: "bad slot id", 4: "bad block", 8: "timeout", 16: "bad kept prefix",
                32: "bad token offsets"}
 _DTYPES = {torch.float32: 0, torch.bfloat16: 1}
+E4M3 = 2
+_BYTE_DTYPES = (torch.uint8,) + ((torch.float8_e4m3fn,) if hasattr(torch, "float8_e4m3fn") else ())
+
+
+def _cache_code(t) -> int:
+    """gqa_dtype of a cache tensor."""
+    if t.dtype in _BYTE_DTYPES:
+        return E4M3
+    if t.dtype not in _DTYPES:
+        raise TypeError("a cache must be float32, bfloat16 or E4M3 bytes")
+    return _DTYPES[t.dtype]
 
 library_path = _lib.LIB_PATH
 
@@ -54,7 +70,7 @@ def _ptr(t):
 
 
 def _opts(kernel, grid_ctas, sched_pad=None, sink=None, window=0, kept_prefix=0, device=None, B=None,
-          Hq=None):
+          Hq=None, k_scale=None, v_scale=None, Hkv=None):
     """The gqa_options struct. Softmax modifiers: ``sink`` a float32 (Hq,)
     device tensor, ``window`` an int >= 0, ``kept_prefix`` an int >= 0 or an
     int32 (B,) device tensor."""
@@ -75,6 +91,12 @@ def _opts(kernel, grid_ctas, sched_pad=None, sink=None, window=0, kept_prefix=0,
         o.kept_prefix_rows = kept_prefix.data_ptr()
     else:
         o.kept_prefix = int(kept_prefix or 0)
+    for name, t in (("k_scale", k_scale), ("v_scale", v_scale)):
+        if t is None:
+            continue
+        if t.dtype != torch.float32 or t.shape != (Hkv,) or not t.is_contiguous() or t.device != device:
+            raise TypeError(f"{name} must be a contiguous float32 (Hkv,) tensor on q's device")
+        setattr(o, name, t.data_ptr())
     return o
 
 
@@ -100,22 +122,36 @@ def _workspace(device, nbytes):
 def workspace_bytes(B, Hq, Hkv, D, dtype=torch.bfloat16, kernel="auto", grid_ctas=0) -> int:
     """Workspace bytes the library needs for one step of these sizes."""
     o = _opts(kernel, grid_ctas)
-    return int(_lib.load().gqa_workspace_bytes(B, Hq, Hkv, D, _DTYPES[dtype], ctypes.byref(o)))
+    code = E4M3 if dtype in _BYTE_DTYPES else _DTYPES[dtype]
+    return int(_lib.load().gqa_workspace_bytes(B, Hq, Hkv, D, code, ctypes.byref(o)))
 
 
 def _common_checks(q, k_new, v_new, caches, lengths, out, q_any_dtype=False):
-    """Checks shared by the entry points; returns (cache dtype, out)."""
+    """Checks shared by the entry points; returns (cache gqa_dtype, out). The
+    query and the new keys / values share the cache dtype, except over an E4M3
+    cache (bfloat16 then; the attend's query is free)."""
     if not q.is_cuda:
         raise ValueError("tensors must be on a CUDA device")
     if q.dtype not in _DTYPES:
         raise TypeError("q must be float32 or bfloat16")
-    dt = caches[0][1].dtype if q_any_dtype else q.dtype
-    if dt not in _DTYPES:
-        raise TypeError("the cache must be float32 or bfloat16")
+    code = _cache_code(caches[0][1])
+    if code == E4M3:
+        if not q_any_dtype and q.dtype != torch.bfloat16:
+            raise TypeError("over an E4M3 cache q, k_new and v_new are bfloat16")
+        new_dt = torch.bfloat16
+    else:
+        dt = caches[0][1].dtype if q_any_dtype else q.dtype
+        if dt not in _DTYPES:
+            raise TypeError("the cache must be float32 or bfloat16")
+        new_dt = dt
     news = () if k_new is None else (("k_new", k_new), ("v_new", v_new))
+    for name, t in news:
+        if t.dtype != new_dt:
+            raise TypeError(f"{name} must have dtype {new_dt}")
+    for name, t in caches:
+        if t.dtype != caches[0][1].dtype:
+            raise TypeError(f"{name} must have dtype {caches[0][1].dtype}")
     for name, t in (*news, *caches):
-        if t.dtype != dt:
-            raise TypeError(f"{name} must have dtype {dt}")
         if t.device != q.device:
             raise ValueError(f"{name} is on {t.device}, q on {q.device}")
         if not t.is_contiguous():
@@ -129,12 +165,12 @@ def _common_checks(q, k_new, v_new, caches, lengths, out, q_any_dtype=False):
         out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
     elif out.shape != (B, Hq, D) or out.dtype != torch.float32 or not out.is_contiguous():
         raise ValueError("out must be a contiguous float32 (B, Hq, D) tensor")
-    return dt, out
+    return code, out
 
 
 def decode_step(q, k_new, v_new, k_cache, v_cache, lengths, slot_ids=None, *, out=None,
                 status=None, kernel="auto", grid_ctas=0, workspace=None, stream=None, sched_pad=None,
-                sink=None, window=0, kept_prefix=0):
+                sink=None, window=0, kept_prefix=0, k_scale=None, v_scale=None):
     """One decode step on a dense (R, Hkv, Smax, D) cache (continuous batch
     when ``slot_ids`` is given). Appends in place; returns ``out``. A
     ``workspace`` passed in must be zero-filled before its first use (the
@@ -148,13 +184,13 @@ def decode_step(q, k_new, v_new, k_cache, v_cache, lengths, slot_ids=None, *, ou
         raise ValueError("shape mismatch between q, k_new, v_new and the caches")
     if slot_ids is not None and (slot_ids.dtype != torch.int32 or slot_ids.shape != (B,)):
         raise TypeError("slot_ids must be int32 of shape (B,)")
-    o = _opts(kernel, grid_ctas, sched_pad, sink, window, kept_prefix, q.device, B, Hq)
+    o = _opts(kernel, grid_ctas, sched_pad, sink, window, kept_prefix, q.device, B, Hq, k_scale, v_scale, Hkv)
     lib = _lib.load()
-    need = lib.gqa_workspace_bytes(B, Hq, Hkv, D, _DTYPES[dt], ctypes.byref(o))
+    need = lib.gqa_workspace_bytes(B, Hq, Hkv, D, dt, ctypes.byref(o))
     ws = _workspace(q.device, need) if workspace is None else workspace
     code = lib.gqa_decode_step_ex(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
                                   _ptr(lengths), _ptr(slot_ids), _ptr(out), B, Hq, Hkv, D, R, Smax,
-                                  _DTYPES[dt], _ptr(ws), ws.numel() * ws.element_size(),
+                                  dt, _ptr(ws), ws.numel() * ws.element_size(),
                                   _ptr(status), _stream(stream), ctypes.byref(o))
     _check(code, "gqa_decode_step")
     return out
@@ -162,7 +198,7 @@ def decode_step(q, k_new, v_new, k_cache, v_cache, lengths, slot_ids=None, *, ou
 
 def decode_step_paged(q, k_new, v_new, k_blocks, v_blocks, block_table, lengths, *, out=None,
                       status=None, kernel="auto", grid_ctas=0, workspace=None, stream=None,
-                      sched_pad=None, sink=None, window=0, kept_prefix=0):
+                      sched_pad=None, sink=None, window=0, kept_prefix=0, k_scale=None, v_scale=None):
     """One decode step on a paged cache (num_blocks, Hkv, block_size, D) with
     a (B, max_blocks) int32 block table (-1 = unused). Appends in place."""
     dt, out = _common_checks(q, k_new, v_new, (("k_blocks", k_blocks), ("v_blocks", v_blocks)),
@@ -175,13 +211,13 @@ def decode_step_paged(q, k_new, v_new, k_blocks, v_blocks, block_table, lengths,
             or not block_table.is_contiguous():
         raise TypeError("block_table must be a contiguous int32 (B, max_blocks) tensor")
     MB = block_table.shape[1]
-    o = _opts(kernel, grid_ctas, sched_pad, sink, window, kept_prefix, q.device, B, Hq)
+    o = _opts(kernel, grid_ctas, sched_pad, sink, window, kept_prefix, q.device, B, Hq, k_scale, v_scale, Hkv)
     lib = _lib.load()
-    need = lib.gqa_workspace_bytes(B, Hq, Hkv, D, _DTYPES[dt], ctypes.byref(o))
+    need = lib.gqa_workspace_bytes(B, Hq, Hkv, D, dt, ctypes.byref(o))
     ws = _workspace(q.device, need) if workspace is None else workspace
     code = lib.gqa_decode_step_paged_ex(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_blocks),
                                         _ptr(v_blocks), _ptr(block_table), _ptr(lengths), _ptr(out),
-                                        B, Hq, Hkv, D, NB, BS, MB, _DTYPES[dt], _ptr(ws),
+                                        B, Hq, Hkv, D, NB, BS, MB, dt, _ptr(ws),
                                         ws.numel() * ws.element_size(), _ptr(status),
                                         _stream(stream), ctypes.byref(o))
     _check(code, "gqa_decode_step_paged")
@@ -190,7 +226,7 @@ def decode_step_paged(q, k_new, v_new, k_blocks, v_blocks, block_table, lengths,
 
 def attend(q, k_cache, v_cache, lengths, slot_ids=None, *, out=None, status=None, kernel="auto",
            grid_ctas=0, workspace=None, stream=None, sched_pad=None, sink=None, window=0,
-           kept_prefix=0):
+           kept_prefix=0, k_scale=None, v_scale=None):
     """Read-only attend on a dense (R, Hkv, Smax, D) cache: slots
     ``0..lengths[b]-1`` (1 <= lengths[b] <= Smax), nothing written but ``out``.
     ``q`` (B, Hq, D) is float32 or bfloat16 whatever the cache dtype."""
@@ -202,12 +238,12 @@ def attend(q, k_cache, v_cache, lengths, slot_ids=None, *, out=None, status=None
         raise ValueError("shape mismatch between q and the caches")
     if slot_ids is not None and (slot_ids.dtype != torch.int32 or slot_ids.shape != (B,)):
         raise TypeError("slot_ids must be int32 of shape (B,)")
-    o = _opts(kernel, grid_ctas, sched_pad, sink, window, kept_prefix, q.device, B, Hq)
+    o = _opts(kernel, grid_ctas, sched_pad, sink, window, kept_prefix, q.device, B, Hq, k_scale, v_scale, Hkv)
     lib = _lib.load()
-    need = lib.gqa_workspace_bytes(B, Hq, Hkv, D, _DTYPES[dt], ctypes.byref(o))
+    need = lib.gqa_workspace_bytes(B, Hq, Hkv, D, dt, ctypes.byref(o))
     ws = _workspace(q.device, need) if workspace is None else workspace
     code = lib.gqa_attend(_ptr(q), _DTYPES[q.dtype], _ptr(k_cache), _ptr(v_cache), _ptr(lengths),
-                          _ptr(slot_ids), _ptr(out), B, Hq, Hkv, D, R, Smax, _DTYPES[dt], _ptr(ws),
+                          _ptr(slot_ids), _ptr(out), B, Hq, Hkv, D, R, Smax, dt, _ptr(ws),
                           ws.numel() * ws.element_size(), _ptr(status), _stream(stream),
                           ctypes.byref(o))
     _check(code, "gqa_attend")
@@ -216,7 +252,7 @@ def attend(q, k_cache, v_cache, lengths, slot_ids=None, *, out=None, status=None
 
 def attend_paged(q, k_blocks, v_blocks, block_table, lengths, *, out=None, status=None,
                  kernel="auto", grid_ctas=0, workspace=None, stream=None, sched_pad=None,
-                 sink=None, window=0, kept_prefix=0):
+                 sink=None, window=0, kept_prefix=0, k_scale=None, v_scale=None):
     """Read-only attend on a paged cache (num_blocks, Hkv, block_size, D)."""
     dt, out = _common_checks(q, None, None, (("k_blocks", k_blocks), ("v_blocks", v_blocks)),
                              lengths, out, q_any_dtype=True)
@@ -227,13 +263,13 @@ def attend_paged(q, k_blocks, v_blocks, block_table, lengths, *, out=None, statu
     if block_table.dtype != torch.int32 or block_table.dim() != 2 or block_table.shape[0] != B \
             or not block_table.is_contiguous():
         raise TypeError("block_table must be a contiguous int32 (B, max_blocks) tensor")
-    o = _opts(kernel, grid_ctas, sched_pad, sink, window, kept_prefix, q.device, B, Hq)
+    o = _opts(kernel, grid_ctas, sched_pad, sink, window, kept_prefix, q.device, B, Hq, k_scale, v_scale, Hkv)
     lib = _lib.load()
-    need = lib.gqa_workspace_bytes(B, Hq, Hkv, D, _DTYPES[dt], ctypes.byref(o))
+    need = lib.gqa_workspace_bytes(B, Hq, Hkv, D, dt, ctypes.byref(o))
     ws = _workspace(q.device, need) if workspace is None else workspace
     code = lib.gqa_attend_paged(_ptr(q), _DTYPES[q.dtype], _ptr(k_blocks), _ptr(v_blocks),
                                 _ptr(block_table), _ptr(lengths), _ptr(out), B, Hq, Hkv, D, NB, BS,
-                                block_table.shape[1], _DTYPES[dt], _ptr(ws),
+                                block_table.shape[1], dt, _ptr(ws),
                                 ws.numel() * ws.element_size(), _ptr(status), _stream(stream),
                                 ctypes.byref(o))
     _check(code, "gqa_attend_paged")
@@ -267,11 +303,11 @@ def decode_multi(q, k_new, v_new, k_cache, v_cache, lengths, cu_q, slot_ids=None
         raise TypeError("slot_ids must be int32 of shape (B,)")
     o = _opts(kernel, grid_ctas, sched_pad, sink, window, kept_prefix, q.device, B, Hq)
     lib = _lib.load()
-    need = lib.gqa_workspace_bytes_multi(B, Hq, Hkv, D, _DTYPES[dt], int(max_q_len), ctypes.byref(o))
+    need = lib.gqa_workspace_bytes_multi(B, Hq, Hkv, D, dt, int(max_q_len), ctypes.byref(o))
     ws = _workspace(q.device, need) if workspace is None else workspace
     code = lib.gqa_decode_multi(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
                                 _ptr(lengths), _ptr(cu_q), _ptr(slot_ids), _ptr(out), B, T, int(max_q_len),
-                                Hq, Hkv, D, R, Smax, _DTYPES[dt], _ptr(ws), ws.numel() * ws.element_size(),
+                                Hq, Hkv, D, R, Smax, dt, _ptr(ws), ws.numel() * ws.element_size(),
                                 _ptr(status), _stream(stream), ctypes.byref(o))
     _check(code, "gqa_decode_multi")
     return out
@@ -293,11 +329,11 @@ def decode_multi_paged(q, k_new, v_new, k_blocks, v_blocks, block_table, lengths
         raise TypeError("block_table must be a contiguous int32 (B, max_blocks) tensor")
     o = _opts(kernel, grid_ctas, sched_pad, sink, window, kept_prefix, q.device, B, Hq)
     lib = _lib.load()
-    need = lib.gqa_workspace_bytes_multi(B, Hq, Hkv, D, _DTYPES[dt], int(max_q_len), ctypes.byref(o))
+    need = lib.gqa_workspace_bytes_multi(B, Hq, Hkv, D, dt, int(max_q_len), ctypes.byref(o))
     ws = _workspace(q.device, need) if workspace is None else workspace
     code = lib.gqa_decode_multi_paged(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_blocks), _ptr(v_blocks),
                                       _ptr(block_table), _ptr(lengths), _ptr(cu_q), _ptr(out), B, T,
-                                      int(max_q_len), Hq, Hkv, D, NB, BS, block_table.shape[1], _DTYPES[dt],
+                                      int(max_q_len), Hq, Hkv, D, NB, BS, block_table.shape[1], dt,
                                       _ptr(ws), ws.numel() * ws.element_size(), _ptr(status),
                                       _stream(stream), ctypes.byref(o))
     _check(code, "gqa_decode_multi_paged")

@@ -41,7 +41,8 @@ class GqaOptions(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int), ("grid_ctas", ctypes.c_int),
                 ("sched_pad", ctypes.c_int), ("window", ctypes.c_int),
                 ("kept_prefix", ctypes.c_int), ("reserved", ctypes.c_int * 3),
-                ("head_sink", ctypes.c_void_p), ("kept_prefix_rows", ctypes.c_void_p)]
+                ("head_sink", ctypes.c_void_p), ("kept_prefix_rows", ctypes.c_void_p),
+                ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p)]
 
 
 _lock = threading.Lock()

@@ -33,9 +33,9 @@ int sm_count(int dev)
 int pick_kernel(const gqa_options *opt, gqa_dtype dt, int D, int G, bool paged, int block_size)
 {
     const int want = opt ? opt->kernel : GQA_KERNEL_AUTO;
-    const bool bf16 = dt == GQA_DTYPE_BF16;
+    const bool bf16 = dt == GQA_DTYPE_BF16 || dt == GQA_DTYPE_E4M3;   // the tensor-core kernel's caches
     const bool tc_ok = tc_supports(bf16, D, G, paged, block_size);
-    const bool simt_ok = simt_supports(D, G);
+    const bool simt_ok = dt != GQA_DTYPE_E4M3 && simt_supports(D, G);
     if (want == GQA_KERNEL_TC)
         return tc_ok ? GQA_KERNEL_TC : -1;
     if (want == GQA_KERNEL_SIMT)
@@ -149,19 +149,21 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-// 3-D map over a bf16 cache seen as (D, rows_per_head, heads_total):
-// box (64 elements = 128 bytes, box_rows, 1) with the 128-byte swizzle.
+// 3-D map over a bf16 (es = 2) or E4M3 (es = 1) cache seen as (D,
+// rows_per_head, heads_total): box (128 bytes of elements, box_rows, 1) with
+// the 128-byte swizzle.
 bool encode_cache_map(CUtensorMap *m, void *base, int D, long long rows_per_head,
-                      long long heads_total, int box_rows)
+                      long long heads_total, int box_rows, int es = 2)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn)
         return false;
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)rows_per_head, (cuuint64_t)heads_total};
-    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)D * 2 * (cuuint64_t)rows_per_head};
-    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+    cuuint64_t strides[2] = {(cuuint64_t)D * es, (cuuint64_t)D * es * (cuuint64_t)rows_per_head};
+    cuuint32_t box[3] = {(cuuint32_t)(128 / es), (cuuint32_t)box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+    return fn(m, es == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims,
+              strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -205,7 +207,7 @@ gqa_status check_shape(const Shape &s)
 {
     if (s.B < 0 || s.Hq < 1 || s.Hkv < 1 || s.D < 1 || s.Hq % s.Hkv != 0)
         return GQA_ERR_INVALID_ARGUMENT;
-    if (!valid_dtype(s.dt) || !valid_dtype(s.q_dt))
+    if ((!valid_dtype(s.dt) && s.dt != GQA_DTYPE_E4M3) || !valid_dtype(s.q_dt))
         return GQA_ERR_INVALID_ARGUMENT;
     if (s.paged) {
         if (s.num_blocks < 1 || s.block_size < 1 || s.max_blocks < 1)
@@ -232,6 +234,12 @@ gqa_status run_step(const Shape &s, const void *q, const void *k_new, const void
         return st;
     if (s.multi && (s.T < 0 || s.max_q < 0 || !cu_q))
         return GQA_ERR_INVALID_ARGUMENT;
+    const bool kv8 = s.dt == GQA_DTYPE_E4M3;
+    if (kv8 && (!opt || !opt->k_scale || !opt->v_scale || (reinterpret_cast<uintptr_t>(opt->k_scale) & 3u) ||
+                (reinterpret_cast<uintptr_t>(opt->v_scale) & 3u)))
+        return GQA_ERR_INVALID_ARGUMENT;
+    if (kv8 && s.multi)
+        return GQA_ERR_UNSUPPORTED;
     if (s.B == 0 || (s.multi && (s.T == 0 || s.max_q == 0)))
         return GQA_OK;
     if (!q || !kc || !vc || !lengths || !out || (s.paged && !block_table))
@@ -267,6 +275,11 @@ gqa_status run_step(const Shape &s, const void *q, const void *k_new, const void
     DecodeParams p;
     std::memset(&p, 0, sizeof p);
     p.q = q;
+    p.kv8 = kv8 ? 1 : 0;
+    if (kv8) {
+        p.k_scale = opt->k_scale;
+        p.v_scale = opt->v_scale;
+    }
     p.attend = s.attend ? 1 : 0;
     p.q_bf16 = s.q_dt == GQA_DTYPE_BF16 ? 1 : 0;
     p.k_new = s.attend ? nullptr : k_new;
@@ -317,13 +330,14 @@ gqa_status run_step(const Shape &s, const void *q, const void *k_new, const void
         TcMaps maps;
         const int T = p.tile;
         bool ok;
+        const int es = kv8 ? 1 : 2;
         if (s.paged) {
             const int box = s.block_size < T ? s.block_size : T;
-            ok = encode_cache_map(&maps.k, kc, s.D, s.block_size, (long long)s.num_blocks * s.Hkv, box) &&
-                 encode_cache_map(&maps.v, vc, s.D, s.block_size, (long long)s.num_blocks * s.Hkv, box);
+            ok = encode_cache_map(&maps.k, kc, s.D, s.block_size, (long long)s.num_blocks * s.Hkv, box, es) &&
+                 encode_cache_map(&maps.v, vc, s.D, s.block_size, (long long)s.num_blocks * s.Hkv, box, es);
         } else {
-            ok = encode_cache_map(&maps.k, kc, s.D, s.Smax, (long long)s.R * s.Hkv, T) &&
-                 encode_cache_map(&maps.v, vc, s.D, s.Smax, (long long)s.R * s.Hkv, T);
+            ok = encode_cache_map(&maps.k, kc, s.D, s.Smax, (long long)s.R * s.Hkv, T, es) &&
+                 encode_cache_map(&maps.v, vc, s.D, s.Smax, (long long)s.R * s.Hkv, T, es);
         }
         if (!ok)
             return GQA_ERR_CUDA;
@@ -380,7 +394,9 @@ gqa_status gqa_decode_step_ex(const void *q, const void *k_new, const void *v_ne
                               gqa_dtype dt, void *workspace, size_t workspace_bytes,
                               int32_t *d_status, void *stream, const gqa_options *opt)
 {
-    Shape s = {B, Hq, Hkv, D, dt, false, R, Smax, 0, 0, 0, false, dt};
+    // over an E4M3 cache the query and the new key / value are bfloat16
+    const gqa_dtype qdt = dt == GQA_DTYPE_E4M3 ? GQA_DTYPE_BF16 : dt;
+    Shape s = {B, Hq, Hkv, D, dt, false, R, Smax, 0, 0, 0, false, qdt};
     return run_step(s, q, k_new, v_new, k_cache, v_cache, lengths, slot_ids, nullptr, out,
                     workspace, workspace_bytes, d_status, stream, opt);
 }
@@ -403,7 +419,8 @@ gqa_status gqa_decode_step_paged_ex(const void *q, const void *k_new, const void
                                     gqa_dtype dt, void *workspace, size_t workspace_bytes,
                                     int32_t *d_status, void *stream, const gqa_options *opt)
 {
-    Shape s = {B, Hq, Hkv, D, dt, true, 0, 0, num_blocks, block_size, max_blocks, false, dt};
+    const gqa_dtype qdt = dt == GQA_DTYPE_E4M3 ? GQA_DTYPE_BF16 : dt;
+    Shape s = {B, Hq, Hkv, D, dt, true, 0, 0, num_blocks, block_size, max_blocks, false, qdt};
     return run_step(s, q, k_new, v_new, k_blocks, v_blocks, lengths, nullptr, block_table, out,
                     workspace, workspace_bytes, d_status, stream, opt);
 }

@@ -70,6 +70,8 @@ struct DecodeParams {
     float *out;                  // (B, Hq, D)
     int attend;        // 1: read-only attend (no new token, nothing written but out)
     int q_bf16;        // query dtype: 1 bfloat16, 0 float32 (the cache has its own)
+    int kv8;           // 1: E4M3 cache bytes (k_new / v_new then bfloat16)
+    const float *k_scale, *v_scale;  // E4M3 cache: (Hkv) dequantisation scales
     int B, Hq, Hkv, G, D;
     int R, Smax;                                     // dense
     int paged, num_blocks, block_size, max_blocks;   // paged

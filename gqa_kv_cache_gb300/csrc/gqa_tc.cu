@@ -8,6 +8,7 @@ namespace gqa {
 
 bool tc_supports(bool bf16, int D, int G, bool paged, int block_size)
 {
+    // bf16: a bfloat16 or E4M3 cache (the kernel's two forms)
     if (!bf16 || D != kD || G < 1 || G > kGMax)
         return false;
     if (paged) {
@@ -22,7 +23,7 @@ int tc_tile() { return kTile; }
 int tc_ctas_per_sm() { return kCtasPerSm; }
 size_t tc_smem_bytes(bool q_bf16)
 {
-    return (q_bf16 ? Ring<false>::kDynSmem : Ring<true>::kDynSmem) + sizeof(Shared);
+    return (q_bf16 ? Ring<false>::kDynSmem : Ring<true>::kDynSmem) + sizeof(Shared<kStages>);
 }
 
 cudaError_t tc_launch(const DecodeParams &p, const TcMaps &maps, cudaStream_t st)
@@ -30,6 +31,12 @@ cudaError_t tc_launch(const DecodeParams &p, const TcMaps &maps, cudaStream_t st
     const bool win = p.window > 0;
     if (p.cu_q)     // multi-token steps (bfloat16 query)
         return tc_launch_multi(p, maps, st);
+    if (p.kv8) {    // E4M3 cache
+        if (p.q_bf16)
+            return win ? launch_q<false, true, false, true>(p, maps, st)
+                       : launch_q<false, false, false, true>(p, maps, st);
+        return win ? launch_q<true, true, false, true>(p, maps, st) : launch_q<true, false, false, true>(p, maps, st);
+    }
     if (p.q_bf16)
         return win ? launch_q<false, true, false>(p, maps, st) : launch_q<false, false, false>(p, maps, st);
     return win ? launch_q<true, true, false>(p, maps, st) : launch_q<true, false, false>(p, maps, st);

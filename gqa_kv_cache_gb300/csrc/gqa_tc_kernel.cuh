@@ -1,5 +1,5 @@
-// Tensor-core decode kernel for bfloat16 caches with D = 128 and G <= 8; the
-// query is bfloat16 or float32.
+// Tensor-core decode kernel for bfloat16 or E4M3 (FP8) caches with D = 128 and
+// G <= 8; the query is bfloat16 or float32.
 //
 // Data path (persistent CTAs, kCtasPerSm per SM):
 //  * a producer warp walks the CTA's tiles (gqa_common.cuh) and streams every
@@ -34,6 +34,14 @@
 //    before the product (0 * NaN would not be 0). A window skips whole tiles
 //    (the schedule lists only tiles holding attended slots) and, for paged
 //    caches, whole blocks.
+//  * E4M3 caches (KV8): tiles arrive as bytes (half the traffic), a 3-stage
+//    ring (2 with a float32 query); each consumer warp converts its 16 rows of
+//    K and V to f16 in a private scratch (exact: every E4M3 value is an f16),
+//    releases the stage at once and runs the products in f16 (the query and P
+//    in f16, P split into hi + remainder as below); the K scale joins the score
+//    scale, the V scale multiplies the accumulator before the epilogue, and the
+//    appended token is quantised (float32 division by the scale, round to
+//    nearest even, saturating).
 //  * multi-token steps (MULTI): a unit is a chunk of up to 8 / G tokens of a
 //    row; its query rows are (token, head) pairs gathered by one bulk copy per
 //    token, each row is masked beyond its own token's position, every slot
@@ -56,6 +64,8 @@
 // keep walking their tiles and taking part in every barrier, writing NaN.
 #pragma once
 
+#include <cuda_fp16.h>
+
 #include "gqa_common.cuh"
 #include "gqa_launch.h"
 
@@ -71,7 +81,7 @@ namespace {
 
 constexpr int kD = 128;
 constexpr int kTile = 64;                             // slots per tile
-constexpr int kStages = GQA_TC_STAGES;                // depth of one CTA's TMA ring
+constexpr int kStages = GQA_TC_STAGES;                // depth of one CTA's TMA ring (bf16)
 constexpr int kCtasPerSm = GQA_TC_CTAS_PER_SM;        // resident CTAs per SM
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
@@ -79,13 +89,20 @@ constexpr int kGMax = 8;
 constexpr int kHalfBytes = kTile * 128;               // one 64-element half of a tile
 constexpr long long kWaitCycles = 4LL << 30;          // ~2 s at 2 GHz
 
-// Ring geometry for a bfloat16 (QF32 = false) or float32 query.
-template <bool QF32>
+// Ring geometry for a bfloat16 (QF32 = false) or float32 query over a
+// bfloat16 or E4M3 (KV8) cache.
+template <bool QF32, bool KV8 = false>
 struct Ring {
     static constexpr int kQElem = QF32 ? 4 : 2;
     static constexpr int kQBytes = kGMax * kD * kQElem;              // the unit's G query rows
-    static constexpr int kStageBytes = 4 * kHalfBytes + kQBytes;     // K lo, K hi, V lo, V hi, Q
-    static constexpr int kDynSmem = kStages * kStageBytes + 1024;
+    static constexpr int kKVBytes = KV8 ? kTile * kD : 2 * kHalfBytes; // K (or V) of one tile
+    static constexpr int kStageBytes = 2 * kKVBytes + kQBytes;       // K (lo, hi), V (lo, hi), Q
+    static constexpr int kNumStages = KV8 ? (QF32 ? 2 : 3) : kStages;
+    // E4M3: per consumer warp, its 16 rows of K and of V in f16 (two
+    // 64-element halves each, 128-byte swizzle)
+    static constexpr int kWarpScratch = 2 * 16 * kD * 2;
+    static constexpr int kScratch = KV8 ? kConsumerWarps * kWarpScratch : 0;
+    static constexpr int kDynSmem = kNumStages * kStageBytes + kScratch + 1024;
     static_assert(kStageBytes % 1024 == 0, "stages must stay 1024-byte aligned for the swizzle");
 };
 
@@ -181,6 +198,58 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+                 "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// f16 pair (lo in the low half) rounded to nearest even.
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ float f16_lo(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)(v & 0xffffu))); }
+__device__ __forceinline__ float f16_hi(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)(v >> 16))); }
+
+// A float32 pair as f16 hi parts and f16 remainders: v = hi + lo to ~22 bits.
+__device__ __forceinline__ void split_f16(float2 v, uint32_t &hi, uint32_t &lo)
+{
+    hi = pack_f16(v.x, v.y);
+    lo = pack_f16(v.x - f16_lo(hi), v.y - f16_hi(hi));
+}
+
+// Four E4M3 bytes (the first in the low byte) as two f16 pairs; exact.
+__device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t &lo, uint32_t &hi)
+{
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(lo) : "h"((unsigned short)(w & 0xffffu)));
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hi) : "h"((unsigned short)(w >> 16)));
+}
+
+// Sixteen consecutive bf16 values (two 16-byte words, the first value in the
+// low half of a.x) divided by `scale` in float32 (round to nearest) and
+// encoded as E4M3 (round to nearest even, saturating): sixteen bytes.
+__device__ __forceinline__ uint4 quant_e4m3x16(uint4 a, uint4 b, float scale)
+{
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t o[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float x0 = __fdiv_rn(__uint_as_float(w[i] << 16), scale);
+        const float x1 = __fdiv_rn(__uint_as_float(w[i] & 0xffff0000u), scale);
+        unsigned short q;
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(q) : "f"(x1), "f"(x0));
+        o[i >> 1] |= (uint32_t)q << (16 * (i & 1));
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // A float32 pair as bf16 hi parts and bf16 remainders: v = hi + lo to ~16 bits.
 __device__ __forceinline__ void split_bf16(float2 v, uint32_t &hi, uint32_t &lo)
 {
@@ -192,10 +261,11 @@ __device__ __forceinline__ void split_bf16(float2 v, uint32_t &hi, uint32_t &lo)
 // under the 128-byte swizzle (the half starts on a 1024-byte boundary).
 __device__ __forceinline__ uint32_t swz(int r, int c8) { return (uint32_t)(r * 128 + ((c8 ^ (r & 7)) << 4)); }
 
+template <int NS>
 struct Shared {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
-    int stage_bad[kStages];
+    uint64_t full[NS];
+    uint64_t empty[NS];
+    int stage_bad[NS];
     int abort_flag;
     int last_flag;
     long long sched[kThreads / 32 + 8];
@@ -213,21 +283,26 @@ __device__ __forceinline__ void consumer_sync()
 
 // WIN: a sliding window is in force. Without one the window fields of the
 // cursor are never read, so they take no registers and no code. MULTI: a
-// multi-token step (the chunk fields of the cursor are read only then).
-template <bool QF32, bool WIN, bool MULTI>
+// multi-token step (the chunk fields of the cursor are read only then). KV8:
+// an E4M3 cache (single-token forms).
+template <bool QF32, bool WIN, bool MULTI, bool KV8>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     tc_decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap mk,
                      const __grid_constant__ CUtensorMap mv)
 {
-    constexpr int kStageBytes = Ring<QF32>::kStageBytes;
+    static_assert(!(KV8 && MULTI), "E4M3 caches take single-token steps");
+    using RG = Ring<QF32, KV8>;
+    constexpr int kStageBytes = RG::kStageBytes;
+    constexpr int kNS = RG::kNumStages;   // ring depth
+    constexpr int kKVB = RG::kKVBytes;    // K (or V) bytes of one tile
     extern __shared__ uint8_t dyn_smem[];
-    __shared__ Shared sh;
+    __shared__ Shared<kNS> sh;
     uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
     const uint32_t ring_u32 = smem_u32(ring);
 
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kNS; ++s) {
             mbar_init(smem_u32(&sh.full[s]), 1);
             mbar_init(smem_u32(&sh.empty[s]), kConsumerWarps);
             sh.stage_bad[s] = 0;
@@ -317,28 +392,28 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             // the unit's G query rows (contiguous in q)
             const bool seg_first = pl.good && (cur.t == 0 || cur.g == range_start);
             const int qrows = MULTI ? p.Gh * cur.nq : G;   // query rows with data
-            const uint32_t qbytes = seg_first ? (uint32_t)(qrows * kD * Ring<QF32>::kQElem) : 0u;
-            const uint32_t bytes = (uint32_t)__popc(copying) * 4u * (uint32_t)box_rows * 128u + qbytes;
+            const uint32_t qbytes = seg_first ? (uint32_t)(qrows * kD * RG::kQElem) : 0u;
+            const uint32_t bytes = (uint32_t)__popc(copying) * (KV8 ? 2u : 4u) * (uint32_t)box_rows * 128u + qbytes;
             const uint32_t fb = smem_u32(&sh.full[stage]);
             if (lane == 0) {
                 sh.stage_bad[stage] = any_bad ? 1 : 0;
                 mbar_arrive_tx(fb, bytes);
                 if (qbytes) {
-                    const uint32_t qdst = ring_u32 + stage * kStageBytes + 4 * kHalfBytes;
+                    const uint32_t qdst = ring_u32 + stage * kStageBytes + 2 * kKVB;
                     if constexpr (MULTI) {
                         // one copy per token: its Gh heads are contiguous in q
-                        const uint32_t tb = (uint32_t)(p.Gh * kD * Ring<QF32>::kQElem);
+                        const uint32_t tb = (uint32_t)(p.Gh * kD * RG::kQElem);
                         for (int i = 0; i < cur.nq; ++i) {
                             const long long tok = cur.tokL - (cur.nq - 1 - i);
                             bulk_load(qdst + i * tb,
                                       static_cast<const uint8_t *>(p.q) +
-                                          (tok * p.Hq + (long long)kvh * p.Gh) * kD * Ring<QF32>::kQElem,
+                                          (tok * p.Hq + (long long)kvh * p.Gh) * kD * RG::kQElem,
                                       tb, fb);
                         }
                     } else {
                         bulk_load(qdst,
                                   static_cast<const uint8_t *>(p.q) +
-                                      ((long long)b * p.Hq + (long long)kvh * G) * kD * Ring<QF32>::kQElem,
+                                      ((long long)b * p.Hq + (long long)kvh * G) * kD * RG::kQElem,
                                   qbytes, fb);
                     }
                 }
@@ -346,10 +421,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             __syncwarp();
             if (pl.z >= 0) {
                 const uint32_t dst = ring_u32 + stage * kStageBytes + lane * box_rows * 128;
-                tma_load_3d(dst, &mk, 0, pl.y, pl.z, fb, policy);
-                tma_load_3d(dst + kHalfBytes, &mk, 64, pl.y, pl.z, fb, policy);
-                tma_load_3d(dst + 2 * kHalfBytes, &mv, 0, pl.y, pl.z, fb, policy);
-                tma_load_3d(dst + 3 * kHalfBytes, &mv, 64, pl.y, pl.z, fb, policy);
+                if constexpr (KV8) {   // rows of 128 one-byte elements: one box each
+                    tma_load_3d(dst, &mk, 0, pl.y, pl.z, fb, policy);
+                    tma_load_3d(dst + kKVB, &mv, 0, pl.y, pl.z, fb, policy);
+                } else {
+                    tma_load_3d(dst, &mk, 0, pl.y, pl.z, fb, policy);
+                    tma_load_3d(dst + kHalfBytes, &mk, 64, pl.y, pl.z, fb, policy);
+                    tma_load_3d(dst + 2 * kHalfBytes, &mv, 0, pl.y, pl.z, fb, policy);
+                    tma_load_3d(dst + 3 * kHalfBytes, &mv, 64, pl.y, pl.z, fb, policy);
+                }
             }
             ++issued;
             const bool was_b = in_b;
@@ -358,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 range_start = cur.g;
             if (more)
                 pl = plan(cur);
-            if (++stage == kStages) {
+            if (++stage == kNS) {
                 stage = 0;
                 phase ^= 1;
             }
@@ -368,9 +448,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         // Abort path only: let every copy still in flight land before exit.
         if (*((volatile int *)&sh.abort_flag)) {
             int s = stage, ph = phase;
-            for (int k = 0; k < kStages && k < issued; ++k) {
+            for (int k = 0; k < kNS && k < issued; ++k) {
                 if (--s < 0) {
-                    s = kStages - 1;
+                    s = kNS - 1;
                     ph ^= 1;
                 }
                 mbar_wait(smem_u32(&sh.full[s]), ph);
@@ -396,6 +476,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     int seg_bad = 0;
     // multi-token units only: this lane's row g0 (last slot, window start), rows with data
     int lim = 0, lo_r = 0, qrows = G;
+    // E4M3 cache: the unit's score scale (with k_scale) and v_scale; this
+    // warp's f16 scratch (16 rows of K, then of V)
+    float ssc = p.scale_log2, vsc = 1.f;
+    const uint32_t scr_k = ring_u32 + kNS * kStageBytes + warp * RG::kWarpScratch;
+    const uint32_t scr_v = scr_k + RG::kWarpScratch / 2;
 
     while (more) {
         const int b = cur.b, kvh = cur.kvh, L = cur.L;
@@ -418,6 +503,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 if constexpr (WIN)
                     lo_r = max(0, lim - p.window + 1);
             }
+            if constexpr (KV8) {
+                ssc = p.scale_log2 * __ldg(p.k_scale + kvh);
+                vsc = __ldg(p.v_scale + kvh);
+            }
         }
 
         // After an abort every warp keeps walking its tiles and taking part in
@@ -435,27 +524,47 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
         const int slot0 = WIN ? tile_slot0(cur, kTile) : cur.t * kTile;
         const uint32_t kbase = ring_u32 + stage * kStageBytes;
-        const uint32_t vbase = kbase + 2 * kHalfBytes;
+        const uint32_t vbase = kbase + kKVB;
         uint8_t *kring = ring + stage * kStageBytes;
-        uint8_t *vring = kring + 2 * kHalfBytes;
+        uint8_t *vring = kring + kKVB;
+        bool released = false;
         const int tile_bad = have ? sh.stage_bad[stage] : 1;
         seg_bad |= tile_bad;
         if (first_of_seg && have && row_good) {
             // Q fragments from the ring (rows g0 < G): dims 16ks + 2q4 (+1)
             // and 16ks + 8 + 2q4 (+1) of head g0
             if constexpr (QF32) {
-                const float *qs = reinterpret_cast<const float *>(kring + 4 * kHalfBytes) + g0 * kD;
+                const float *qs = reinterpret_cast<const float *>(kring + 2 * kKVB) + g0 * kD;
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     qa[ks][0] = qa[ks][1] = ql[ks][0] = ql[ks][1] = 0u;
                     if (g0 < (MULTI ? qrows : G)) {
-                        split_bf16(*reinterpret_cast<const float2 *>(qs + 16 * ks + 2 * q4), qa[ks][0], ql[ks][0]);
-                        split_bf16(*reinterpret_cast<const float2 *>(qs + 16 * ks + 8 + 2 * q4), qa[ks][1],
-                                   ql[ks][1]);
+                        const float2 v0 = *reinterpret_cast<const float2 *>(qs + 16 * ks + 2 * q4);
+                        const float2 v1 = *reinterpret_cast<const float2 *>(qs + 16 * ks + 8 + 2 * q4);
+                        if constexpr (KV8) {   // f16 products over an E4M3 cache
+                            split_f16(v0, qa[ks][0], ql[ks][0]);
+                            split_f16(v1, qa[ks][1], ql[ks][1]);
+                        } else {
+                            split_bf16(v0, qa[ks][0], ql[ks][0]);
+                            split_bf16(v1, qa[ks][1], ql[ks][1]);
+                        }
+                    }
+                }
+            } else if constexpr (KV8) {
+                // bf16 query as f16 (exact in the normal range)
+                const uint8_t *qs = kring + 2 * kKVB + g0 * (kD * 2);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    qa[ks][0] = qa[ks][1] = 0u;
+                    if (g0 < G) {
+                        const uint32_t w0 = *reinterpret_cast<const uint32_t *>(qs + (16 * ks + 2 * q4) * 2);
+                        const uint32_t w1 = *reinterpret_cast<const uint32_t *>(qs + (16 * ks + 8 + 2 * q4) * 2);
+                        qa[ks][0] = pack_f16(bf16_lo(w0), bf16_hi(w0));
+                        qa[ks][1] = pack_f16(bf16_lo(w1), bf16_hi(w1));
                     }
                 }
             } else {
-                const uint8_t *qs = kring + 4 * kHalfBytes + g0 * (kD * 2);
+                const uint8_t *qs = kring + 2 * kKVB + g0 * (kD * 2);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     const bool on = g0 < (MULTI ? qrows : G);
@@ -477,7 +586,24 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 // new-token rows: substituted from k_new / v_new (and appended
                 // by the unit owning the token); rows no query row attends:
                 // zero V
-                if constexpr (MULTI) {
+                if constexpr (KV8) {
+                    // row L of the last tile: the new token, quantised into the
+                    // ring and appended to the cache (lanes 0-7: K, 8-15: V,
+                    // sixteen elements each)
+                    const int lr = L - slot0;
+                    if (last_tile && !p.attend && lr >= row0 && lr < row0 + 16 && lane < 16) {
+                        const long long nidx = ((long long)b * p.Hkv + kvh) * kD;
+                        const int c16 = lane & 7;
+                        const bool is_k = lane < 8;
+                        const uint4 *src = reinterpret_cast<const uint4 *>((is_k ? knew : vnew) + nidx) + 2 * c16;
+                        const uint4 q8 = quant_e4m3x16(__ldg(src), __ldg(src + 1),
+                                                       __ldg((is_k ? p.k_scale : p.v_scale) + kvh));
+                        *reinterpret_cast<uint4 *>((is_k ? kring : vring) + swz(lr, c16)) = q8;
+                        const long long off = slot_offset(p, b, kvh, L);
+                        if (off >= 0)
+                            reinterpret_cast<uint4 *>(static_cast<uint8_t *>(is_k ? p.k_cache : p.v_cache) + off)[c16] = q8;
+                    }
+                } else if constexpr (MULTI) {
                     // this warp's rows holding new tokens
                     const int first_new = max(cur.Lb, slot0 + row0);
                     const int last_new = min(L, slot0 + row0 + 15);
@@ -519,14 +645,54 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                         }
                     }
                 }
-                for (int r = row0 + (lane >> 4); r < row0 + 16; r += 2) {
-                    if (WIN ? !attended(L, cur.lo, cur.P, slot0 + r) : slot0 + r > L) {
-                        const int c = lane & 15;
-                        *reinterpret_cast<uint4 *>(vring + (c >> 3) * kHalfBytes + swz(r, c & 7)) =
-                            make_uint4(0u, 0u, 0u, 0u);
+                if constexpr (KV8) {
+                    for (int r = row0 + (lane >> 3); r < row0 + 16; r += 4) {
+                        if (WIN ? !attended(L, cur.lo, cur.P, slot0 + r) : slot0 + r > L)
+                            *reinterpret_cast<uint4 *>(vring + swz(r, lane & 7)) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                } else {
+                    for (int r = row0 + (lane >> 4); r < row0 + 16; r += 2) {
+                        if (WIN ? !attended(L, cur.lo, cur.P, slot0 + r) : slot0 + r > L) {
+                            const int c = lane & 15;
+                            *reinterpret_cast<uint4 *>(vring + (c >> 3) * kHalfBytes + swz(r, c & 7)) =
+                                make_uint4(0u, 0u, 0u, 0u);
+                        }
                     }
                 }
                 __syncwarp();
+            }
+            if constexpr (KV8) {
+                // this warp's 16 rows of K and V: E4M3 bytes -> f16 scratch
+                // (row r of the ring, 16-byte chunk c16 = elements 16 c16 ..
+                // +15 -> f16 chunks 2 c16, 2 c16 + 1 of half c16 / 4)
+#pragma unroll
+                for (int it = 0; it < 4; ++it) {
+                    const int idx = it * 32 + lane;
+                    const int rl = idx >> 3, c16 = idx & 7;
+                    const int r = row0 + rl;
+#pragma unroll
+                    for (int kv = 0; kv < 2; ++kv) {
+                        const uint4 w = *reinterpret_cast<const uint4 *>((kv ? vring : kring) + swz(r, c16));
+                        uint4 lo, hi;
+                        e4m3x4_to_f16(w.x, lo.x, lo.y);
+                        e4m3x4_to_f16(w.y, lo.z, lo.w);
+                        e4m3x4_to_f16(w.z, hi.x, hi.y);
+                        e4m3x4_to_f16(w.w, hi.z, hi.w);
+                        const uint32_t base = (kv ? scr_v : scr_k) + (c16 >> 2) * (16 * 128);
+                        const int c8 = 2 * (c16 & 3);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(base + swz(rl, c8)),
+                                     "r"(lo.x), "r"(lo.y), "r"(lo.z), "r"(lo.w) : "memory");
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(base + swz(rl, c8 + 1)),
+                                     "r"(hi.x), "r"(hi.y), "r"(hi.z), "r"(hi.w) : "memory");
+                    }
+                }
+                // the stage goes back to the producer now
+                if (partial)
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(smem_u32(&sh.empty[stage]));
+                released = true;
             }
 
             // ---- S = Q K^T for this warp's 16 slots (two n-tiles of 8);
@@ -540,8 +706,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 for (int ks = 0; ks < 8; ++ks) {
                     const int c = 2 * ks + (mi & 1);
                     uint32_t kb[4];
-                    ldsm_x4(kbase + (c >> 3) * kHalfBytes + swz(r, c & 7), kb);
                     float(&acc)[2][4] = (ks & 1) ? s_odd : s_acc;
+                    if constexpr (KV8) {
+                        ldsm_x4(scr_k + (c >> 3) * (16 * 128) + swz(r - row0, c & 7), kb);
+                        mma_f16(acc[0], qa[ks][0], QF32 ? ql[ks][0] : 0u, qa[ks][1], QF32 ? ql[ks][1] : 0u, kb[0], kb[1]);
+                        mma_f16(acc[1], qa[ks][0], QF32 ? ql[ks][0] : 0u, qa[ks][1], QF32 ? ql[ks][1] : 0u, kb[2], kb[3]);
+                        continue;
+                    }
+                    ldsm_x4(kbase + (c >> 3) * kHalfBytes + swz(r, c & 7), kb);
                     if constexpr (QF32) {
                         mma_bf16(acc[0], qa[ks][0], ql[ks][0], qa[ks][1], ql[ks][1], kb[0], kb[1]);
                         mma_bf16(acc[1], qa[ks][0], ql[ks][0], qa[ks][1], ql[ks][1], kb[2], kb[3]);
@@ -570,7 +742,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                         sc += s_acc[nt][e + 2];   // row g0 + 8: the query remainder
                     const bool on = MULTI ? (WIN ? attended(lim, lo_r, cur.P, j) : j <= lim)
                                           : (WIN ? attended(L, cur.lo, cur.P, j) : j <= L);
-                    x[nt][e] = (!partial || on) ? sc * p.scale_log2 : -INFINITY;
+                    x[nt][e] = (!partial || on) ? sc * (KV8 ? ssc : p.scale_log2) : -INFINITY;
                     mx = fmaxf(mx, x[nt][e]);
                 }
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
@@ -599,6 +771,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     }
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt) {
+                    if constexpr (KV8) {
+                        uint32_t hi, lo;
+                        split_f16(make_float2(pr[nt][0], pr[nt][1]), hi, lo);
+                        pa[2 * nt] = hi;
+                        pa[2 * nt + 1] = lo;
+                        continue;
+                    }
                     const uint32_t hi = pack_bf16(pr[nt][0], pr[nt][1]);
                     const float h0 = __uint_as_float(hi << 16), h1 = __uint_as_float(hi & 0xffff0000u);
                     const uint32_t lo = pack_bf16(pr[nt][0] - h0, pr[nt][1] - h1);
@@ -614,18 +793,24 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 for (int np = 0; np < 8; ++np) {
                     const int c = 2 * np + (mi >> 1);
                     uint32_t vb[4];
+                    if constexpr (KV8) {
+                        ldsm_x4_t(scr_v + (c >> 3) * (16 * 128) + swz(r - row0, c & 7), vb);
+                        mma_f16(acc_o[2 * np], pa[0], pa[1], pa[2], pa[3], vb[0], vb[1]);
+                        mma_f16(acc_o[2 * np + 1], pa[0], pa[1], pa[2], pa[3], vb[2], vb[3]);
+                        continue;
+                    }
                     ldsm_x4_t(vbase + (c >> 3) * kHalfBytes + swz(r, c & 7), vb);
                     mma_bf16(acc_o[2 * np], pa[0], pa[1], pa[2], pa[3], vb[0], vb[1]);
                     mma_bf16(acc_o[2 * np + 1], pa[0], pa[1], pa[2], pa[3], vb[2], vb[3]);
                 }
             }
-            if (partial)
+            if (!KV8 && partial)
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         }
         __syncwarp();
-        if (lane == 0 && have)
+        if (lane == 0 && have && !released)
             mbar_arrive(smem_u32(&sh.empty[stage]));
-        if (++stage == kStages) {
+        if (++stage == kNS) {
             stage = 0;
             phase ^= 1;
         }
@@ -643,9 +828,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     sh.l[warp][g0] = l_tot;
                 }
 #pragma unroll
-                for (int n = 0; n < 16; ++n)
-                    *reinterpret_cast<float2 *>(&sh.o[warp][g0][8 * n + 2 * q4]) =
-                        make_float2(acc_o[n][0] + acc_o[n][2], acc_o[n][1] + acc_o[n][3]);
+                for (int n = 0; n < 16; ++n) {
+                    float2 o = make_float2(acc_o[n][0] + acc_o[n][2], acc_o[n][1] + acc_o[n][3]);
+                    if constexpr (KV8) {   // the V scale of an E4M3 cache
+                        o.x *= vsc;
+                        o.y *= vsc;
+                    }
+                    *reinterpret_cast<float2 *>(&sh.o[warp][g0][8 * n + 2 * q4]) = o;
+                }
             }
             consumer_sync();
             const bool bad = !row_good || seg_bad;
@@ -661,13 +851,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 }
 
 
-template <bool QF32, bool WIN, bool MULTI>
+template <bool QF32, bool WIN, bool MULTI, bool KV8 = false>
 cudaError_t launch_q(const DecodeParams &p, const TcMaps &maps, cudaStream_t st)
 {
-    constexpr int kDynSmem = Ring<QF32>::kDynSmem;
+    constexpr int kDynSmem = Ring<QF32, KV8>::kDynSmem;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(tc_decode_kernel<QF32, WIN, MULTI>,
+        cudaError_t e = cudaFuncSetAttribute(tc_decode_kernel<QF32, WIN, MULTI, KV8>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem);
         if (e != cudaSuccess)
             return e;
@@ -683,7 +873,7 @@ cudaError_t launch_q(const DecodeParams &p, const TcMaps &maps, cudaStream_t st)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tc_decode_kernel<QF32, WIN, MULTI>, p, maps.k, maps.v);
+    return cudaLaunchKernelEx(&cfg, tc_decode_kernel<QF32, WIN, MULTI, KV8>, p, maps.k, maps.v);
 }
 
 }  // namespace

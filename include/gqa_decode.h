@@ -71,7 +71,16 @@ typedef enum gqa_status {
 
 typedef enum gqa_dtype {
     GQA_DTYPE_F32 = 0,  /* float32  (decode step: q, k_new, v_new and the cache) */
-    GQA_DTYPE_BF16 = 1  /* bfloat16 (decode step: q, k_new, v_new and the cache) */
+    GQA_DTYPE_BF16 = 1, /* bfloat16 (decode step: q, k_new, v_new and the cache) */
+    GQA_DTYPE_E4M3 = 2  /* a cache of OCP FP8 E4M3 bytes with per-cache-head float32
+                           scales (gqa_options.k_scale / v_scale): K = k_scale[kvh] *
+                           K8, V = v_scale[kvh] * V8 ("groupQueryAttention": kScale,
+                           vScale). The decode step then takes bfloat16 q, k_new and
+                           v_new and appends E4M3(float32(k_new) / k_scale[kvh]),
+                           rounded to nearest even and saturated to +-448; the
+                           read-only attend takes a float32 or bfloat16 query. Only
+                           the tensor-core kernel takes it (D = 128, G <= 8; paged
+                           block sizes a power of two >= 8); single-token steps. */
 } gqa_dtype;
 
 /* Bits OR-ed into *d_status by the kernels. */
@@ -123,6 +132,9 @@ typedef struct gqa_options {
     const int32_t *kept_prefix_rows; /* (device) (B,) int32 P per batch row, or NULL;
                                         a negative entry makes that row bad
                                         (NaN, GQA_STATUS_BAD_PREFIX)                    */
+    const float *k_scale;            /* (device) (Hkv,) float32: required with an
+                                        E4M3 cache (GQA_DTYPE_E4M3), else ignored       */
+    const float *v_scale;            /* (device) (Hkv,) float32, likewise               */
 } gqa_options;
 
 /* Human-readable name of a status code (static storage). */

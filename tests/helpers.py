@@ -5,7 +5,8 @@ import torch
 
 
 def to_np(t: torch.Tensor) -> np.ndarray:
-    """float32 -> float32 array; bfloat16 -> uint16 array of the raw bits."""
+    """float32 -> float32 array; bfloat16 -> uint16 array of the raw bits;
+    E4M3 bytes -> uint8 array."""
     t = t.detach().cpu().contiguous()
     if t.dtype == torch.bfloat16:
         return t.view(torch.int16).numpy().view(np.uint16).copy()
@@ -13,6 +14,8 @@ def to_np(t: torch.Tensor) -> np.ndarray:
         return t.numpy().copy()
     if t.dtype in (torch.int32, torch.int64):
         return t.numpy().astype(np.int32)
+    if t.dtype == torch.uint8 or t.dtype == getattr(torch, "float8_e4m3fn", None):
+        return t.view(torch.uint8).numpy().copy()
     raise TypeError(t.dtype)
 
 

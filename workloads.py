@@ -36,6 +36,12 @@ q_lens[b] new tokens, lengths are the decode draw clamped so the tokens fit
 T = sum(q_lens) tokens, cu_q holds the offsets and a paged table covers
 every touched slot.
 
+``generate(w, kv_e4m3=True)`` stores the cache as E4M3 (OCP FP8) bytes:
+the same draws, divided per cache head by a scale 4 * key_scale / 448 (so
+N(0,1) data up to 4 sigma uses the whole E4M3 range), clamped to +-448 and
+cast with torch's float8_e4m3fn; k_scale / v_scale hold the scales; q,
+k_new and v_new stay bfloat16.
+
 Random draws come from a ``torch.Generator`` on the target device seeded
 with the workload's seed, in a fixed order, in chunks of ``_CHUNK`` elements
 (so an 8 GB cache never needs a 17 GB float32 staging copy).
@@ -151,7 +157,7 @@ def _lengths(w, gen, device):
 
 
 def generate(w: Workload, device="cpu", attend: bool = False, q_f32: bool = False,
-             q_lens=None) -> dict:
+             q_lens=None, kv_e4m3: bool = False) -> dict:
     """All inputs of one decode step of workload ``w`` on ``device``.
 
     Returns a dict with q (B,Hq,D), k_new/v_new (B,Hkv,D), lengths (B,) int32,
@@ -197,7 +203,7 @@ def generate(w: Workload, device="cpu", attend: bool = False, q_f32: bool = Fals
         used = (touched + w.block_size - 1) // w.block_size
         idx = torch.arange(w.max_blocks, device=device)[None, :]
         t["block_table"] = torch.where(idx < used[:, None], bt, torch.full_like(bt, -1))
-        return _drop_new(t, attend)
+        return quantise_cache(w, _drop_new(t, attend)) if kv_e4m3 else _drop_new(t, attend)
     shape = (w.rows, w.Hkv, w.Smax, w.D)
     if w.stale_std == 1.0:
         t["k_cache"] = _normal_cast(shape, gen, device, w, w.key_scale)
@@ -217,12 +223,36 @@ def generate(w: Workload, device="cpu", attend: bool = False, q_f32: bool = Fals
         valid = (torch.arange(w.Smax, device=device)[None, :] < row_len[:, None])[:, None, :, None]
         t["k_cache"] = _cast(torch.where(valid, valid_k, stale_k), w)
         t["v_cache"] = _cast(torch.where(valid, valid_v, stale_v), w)
-    return _drop_new(t, attend)
+    return quantise_cache(w, _drop_new(t, attend)) if kv_e4m3 else _drop_new(t, attend)
 
 
 def _drop_new(t: dict, attend: bool) -> dict:
     if attend:
         del t["k_new"], t["v_new"]
+    return t
+
+
+def _to_e4m3(x, scale):
+    """(N, Hkv, S, D) values as E4M3 bytes of x / scale[kvh] (chunked over N)."""
+    out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    s = scale.view(1, -1, 1, 1)
+    step = max(1, _CHUNK // max(1, x[0].numel()))
+    for i in range(0, x.shape[0], step):
+        y = (x[i:i + step].float() / s).clamp_(-448.0, 448.0)
+        out[i:i + step] = y.to(torch.float8_e4m3fn).view(torch.uint8)
+    return out
+
+
+def quantise_cache(w: Workload, t: dict) -> dict:
+    """The cache of ``t`` as E4M3 bytes with per-head scales (see the module
+    docstring); the other inputs unchanged."""
+    dev = t["q"].device
+    ks = torch.full((w.Hkv,), 4.0 * w.key_scale / 448.0, dtype=torch.float32, device=dev)
+    vs = torch.full((w.Hkv,), 4.0 / 448.0, dtype=torch.float32, device=dev)
+    names = ("k_blocks", "v_blocks") if w.paged else ("k_cache", "v_cache")
+    t[names[0]] = _to_e4m3(t[names[0]], ks)
+    t[names[1]] = _to_e4m3(t[names[1]], vs)
+    t["k_scale"], t["v_scale"] = ks, vs
     return t
 
 
