@@ -34,14 +34,20 @@
 //    before the product (0 * NaN would not be 0). A window skips whole tiles
 //    (the schedule lists only tiles holding attended slots) and, for paged
 //    caches, whole blocks.
-//  * E4M3 caches (KV8): tiles arrive as bytes (half the traffic), a 3-stage
-//    ring (2 with a float32 query); each consumer warp converts its 16 rows of
-//    K and V to f16 in a private scratch (exact: every E4M3 value is an f16),
-//    releases the stage at once and runs the products in f16 (the query and P
-//    in f16, P split into hi + remainder as below); the K scale joins the score
-//    scale, the V scale multiplies the accumulator before the epilogue, and the
-//    appended token is quantised (float32 division by the scale, round to
-//    nearest even, saturating).
+//  * E4M3 caches (KV8): tiles arrive as bytes (half the traffic) through a
+//    4-stage ring, and the products run in f16 (every E4M3 value is an f16):
+//    K fragments come from a b16 ldmatrix over the byte rows -- each lane gets
+//    four consecutive E4M3 values, two conversions make its B fragment, and
+//    the query fragments are gathered in the same permuted order of the 16
+//    dims of a k-step (a dot product does not depend on the order); V
+//    fragments come from ldmatrix.trans, whose byte pairs one byte permute
+//    splits into (slot, slot + 1) pairs of an even and of an odd dim, so each
+//    transposed matrix feeds two products and the accumulator columns are
+//    interleaved (undone in the epilogue). The query and P are f16 (a float32
+//    query and P split into hi + remainder as below); the K scale joins the
+//    score scale, the V scale multiplies the accumulator before the epilogue,
+//    and the appended token is quantised (float32 division by the scale,
+//    round to nearest even, saturating).
 //  * multi-token steps (MULTI): a unit is a chunk of up to 8 / G tokens of a
 //    row; its query rows are (token, head) pairs gathered by one bulk copy per
 //    token, each row is masked beyond its own token's position, every slot
@@ -97,12 +103,8 @@ struct Ring {
     static constexpr int kQBytes = kGMax * kD * kQElem;              // the unit's G query rows
     static constexpr int kKVBytes = KV8 ? kTile * kD : 2 * kHalfBytes; // K (or V) of one tile
     static constexpr int kStageBytes = 2 * kKVBytes + kQBytes;       // K (lo, hi), V (lo, hi), Q
-    static constexpr int kNumStages = KV8 ? (QF32 ? 2 : 3) : kStages;
-    // E4M3: per consumer warp, its 16 rows of K and of V in f16 (two
-    // 64-element halves each, 128-byte swizzle)
-    static constexpr int kWarpScratch = 2 * 16 * kD * 2;
-    static constexpr int kScratch = KV8 ? kConsumerWarps * kWarpScratch : 0;
-    static constexpr int kDynSmem = kNumStages * kStageBytes + kScratch + 1024;
+    static constexpr int kNumStages = KV8 ? 4 : kStages;
+    static constexpr int kDynSmem = kNumStages * kStageBytes + 1024;
     static_assert(kStageBytes % 1024 == 0, "stages must stay 1024-byte aligned for the swizzle");
 };
 
@@ -476,11 +478,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     int seg_bad = 0;
     // multi-token units only: this lane's row g0 (last slot, window start), rows with data
     int lim = 0, lo_r = 0, qrows = G;
-    // E4M3 cache: the unit's score scale (with k_scale) and v_scale; this
-    // warp's f16 scratch (16 rows of K, then of V)
+    // E4M3 cache: the unit's score scale (with k_scale) and v_scale
     float ssc = p.scale_log2, vsc = 1.f;
-    const uint32_t scr_k = ring_u32 + kNS * kStageBytes + warp * RG::kWarpScratch;
-    const uint32_t scr_v = scr_k + RG::kWarpScratch / 2;
 
     while (more) {
         const int b = cur.b, kvh = cur.kvh, L = cur.L;
@@ -527,7 +526,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const uint32_t vbase = kbase + kKVB;
         uint8_t *kring = ring + stage * kStageBytes;
         uint8_t *vring = kring + kKVB;
-        bool released = false;
         const int tile_bad = have ? sh.stage_bad[stage] : 1;
         seg_bad |= tile_bad;
         if (first_of_seg && have && row_good) {
@@ -539,8 +537,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 for (int ks = 0; ks < 8; ++ks) {
                     qa[ks][0] = qa[ks][1] = ql[ks][0] = ql[ks][1] = 0u;
                     if (g0 < (MULTI ? qrows : G)) {
-                        const float2 v0 = *reinterpret_cast<const float2 *>(qs + 16 * ks + 2 * q4);
-                        const float2 v1 = *reinterpret_cast<const float2 *>(qs + 16 * ks + 8 + 2 * q4);
+                        // over an E4M3 cache the k-step's dims are taken in the
+                        // order the byte fragments of K deliver them (4 q4 .. +3)
+                        const int d0 = KV8 ? 16 * ks + 4 * q4 : 16 * ks + 2 * q4;
+                        const int d1 = KV8 ? 16 * ks + 4 * q4 + 2 : 16 * ks + 8 + 2 * q4;
+                        const float2 v0 = *reinterpret_cast<const float2 *>(qs + d0);
+                        const float2 v1 = *reinterpret_cast<const float2 *>(qs + d1);
                         if constexpr (KV8) {   // f16 products over an E4M3 cache
                             split_f16(v0, qa[ks][0], ql[ks][0]);
                             split_f16(v1, qa[ks][1], ql[ks][1]);
@@ -557,8 +559,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 for (int ks = 0; ks < 8; ++ks) {
                     qa[ks][0] = qa[ks][1] = 0u;
                     if (g0 < G) {
-                        const uint32_t w0 = *reinterpret_cast<const uint32_t *>(qs + (16 * ks + 2 * q4) * 2);
-                        const uint32_t w1 = *reinterpret_cast<const uint32_t *>(qs + (16 * ks + 8 + 2 * q4) * 2);
+                        const uint32_t w0 = *reinterpret_cast<const uint32_t *>(qs + (16 * ks + 4 * q4) * 2);
+                        const uint32_t w1 = *reinterpret_cast<const uint32_t *>(qs + (16 * ks + 4 * q4 + 2) * 2);
                         qa[ks][0] = pack_f16(bf16_lo(w0), bf16_hi(w0));
                         qa[ks][1] = pack_f16(bf16_lo(w1), bf16_hi(w1));
                     }
@@ -661,39 +663,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 }
                 __syncwarp();
             }
-            if constexpr (KV8) {
-                // this warp's 16 rows of K and V: E4M3 bytes -> f16 scratch
-                // (row r of the ring, 16-byte chunk c16 = elements 16 c16 ..
-                // +15 -> f16 chunks 2 c16, 2 c16 + 1 of half c16 / 4)
-#pragma unroll
-                for (int it = 0; it < 4; ++it) {
-                    const int idx = it * 32 + lane;
-                    const int rl = idx >> 3, c16 = idx & 7;
-                    const int r = row0 + rl;
-#pragma unroll
-                    for (int kv = 0; kv < 2; ++kv) {
-                        const uint4 w = *reinterpret_cast<const uint4 *>((kv ? vring : kring) + swz(r, c16));
-                        uint4 lo, hi;
-                        e4m3x4_to_f16(w.x, lo.x, lo.y);
-                        e4m3x4_to_f16(w.y, lo.z, lo.w);
-                        e4m3x4_to_f16(w.z, hi.x, hi.y);
-                        e4m3x4_to_f16(w.w, hi.z, hi.w);
-                        const uint32_t base = (kv ? scr_v : scr_k) + (c16 >> 2) * (16 * 128);
-                        const int c8 = 2 * (c16 & 3);
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(base + swz(rl, c8)),
-                                     "r"(lo.x), "r"(lo.y), "r"(lo.z), "r"(lo.w) : "memory");
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(base + swz(rl, c8 + 1)),
-                                     "r"(hi.x), "r"(hi.y), "r"(hi.z), "r"(hi.w) : "memory");
-                    }
-                }
-                // the stage goes back to the producer now
-                if (partial)
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(smem_u32(&sh.empty[stage]));
-                released = true;
-            }
+
 
             // ---- S = Q K^T for this warp's 16 slots (two n-tiles of 8);
             // even and odd k-steps accumulate separately (shorter chains)
@@ -702,17 +672,30 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 float s_odd[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
                 const int mi = lane >> 3, ri = lane & 7;
                 const int r = row0 + 8 * (mi >> 1) + ri;
+                if constexpr (KV8) {
+                    // matrix mi: slots 8 (mi >> 1) .. +7 of the warp, k-step
+                    // 2 kp + (mi & 1) (16 bytes of each row)
+                    const int rk = row0 + 8 * (mi >> 1) + ri;
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
+                    for (int kp = 0; kp < 4; ++kp) {
+                        uint32_t kb[4];
+                        ldsm_x4(kbase + swz(rk, 2 * kp + (mi & 1)), kb);
+#pragma unroll
+                        for (int mm = 0; mm < 4; ++mm) {
+                            const int ks = 2 * kp + (mm & 1), nt = mm >> 1;
+                            uint32_t b0, b1;
+                            e4m3x4_to_f16(kb[mm], b0, b1);
+                            float(&acc)[2][4] = (ks & 1) ? s_odd : s_acc;
+                            mma_f16(acc[nt], qa[ks][0], QF32 ? ql[ks][0] : 0u, qa[ks][1], QF32 ? ql[ks][1] : 0u,
+                                    b0, b1);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int ks = 0; ks < (KV8 ? 0 : 8); ++ks) {
                     const int c = 2 * ks + (mi & 1);
                     uint32_t kb[4];
                     float(&acc)[2][4] = (ks & 1) ? s_odd : s_acc;
-                    if constexpr (KV8) {
-                        ldsm_x4(scr_k + (c >> 3) * (16 * 128) + swz(r - row0, c & 7), kb);
-                        mma_f16(acc[0], qa[ks][0], QF32 ? ql[ks][0] : 0u, qa[ks][1], QF32 ? ql[ks][1] : 0u, kb[0], kb[1]);
-                        mma_f16(acc[1], qa[ks][0], QF32 ? ql[ks][0] : 0u, qa[ks][1], QF32 ? ql[ks][1] : 0u, kb[2], kb[3]);
-                        continue;
-                    }
                     ldsm_x4(kbase + (c >> 3) * kHalfBytes + swz(r, c & 7), kb);
                     if constexpr (QF32) {
                         mma_bf16(acc[0], qa[ks][0], ql[ks][0], qa[ks][1], ql[ks][1], kb[0], kb[1]);
@@ -789,26 +772,41 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             {
                 const int mi = lane >> 3, ri = lane & 7;
                 const int r = row0 + 8 * (mi & 1) + ri;
+                if constexpr (KV8) {
+                    // matrix mi: slots 8 (mi & 1) .. +7, 16-dim block
+                    // 2 bp + (mi >> 1); each lane gets bytes (s, d), (s, d+1),
+                    // (s+1, d), (s+1, d+1) and splits them into the (s, s+1)
+                    // pairs of dim d (even) and d + 1 (odd)
 #pragma unroll
-                for (int np = 0; np < 8; ++np) {
+                    for (int bp = 0; bp < 4; ++bp) {
+                        uint32_t vb[4];
+                        ldsm_x4_t(vbase + swz(r, 2 * bp + (mi >> 1)), vb);
+                        uint32_t ev[4], od[4];
+#pragma unroll
+                        for (int mm = 0; mm < 4; ++mm)
+                            e4m3x4_to_f16(__byte_perm(vb[mm], 0u, 0x3120u), ev[mm], od[mm]);
+#pragma unroll
+                        for (int hb = 0; hb < 2; ++hb) {   // block 2 bp + hb: matrices 2 hb (slots 0-7), 2 hb + 1
+                            const int blk = 2 * bp + hb;
+                            mma_f16(acc_o[2 * blk], pa[0], pa[1], pa[2], pa[3], ev[2 * hb], ev[2 * hb + 1]);
+                            mma_f16(acc_o[2 * blk + 1], pa[0], pa[1], pa[2], pa[3], od[2 * hb], od[2 * hb + 1]);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int np = 0; np < (KV8 ? 0 : 8); ++np) {
                     const int c = 2 * np + (mi >> 1);
                     uint32_t vb[4];
-                    if constexpr (KV8) {
-                        ldsm_x4_t(scr_v + (c >> 3) * (16 * 128) + swz(r - row0, c & 7), vb);
-                        mma_f16(acc_o[2 * np], pa[0], pa[1], pa[2], pa[3], vb[0], vb[1]);
-                        mma_f16(acc_o[2 * np + 1], pa[0], pa[1], pa[2], pa[3], vb[2], vb[3]);
-                        continue;
-                    }
                     ldsm_x4_t(vbase + (c >> 3) * kHalfBytes + swz(r, c & 7), vb);
                     mma_bf16(acc_o[2 * np], pa[0], pa[1], pa[2], pa[3], vb[0], vb[1]);
                     mma_bf16(acc_o[2 * np + 1], pa[0], pa[1], pa[2], pa[3], vb[2], vb[3]);
                 }
             }
-            if (!KV8 && partial)
+            if (partial)
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         }
         __syncwarp();
-        if (lane == 0 && have && !released)
+        if (lane == 0 && have)
             mbar_arrive(smem_u32(&sh.empty[stage]));
         if (++stage == kNS) {
             stage = 0;
@@ -829,12 +827,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 }
 #pragma unroll
                 for (int n = 0; n < 16; ++n) {
-                    float2 o = make_float2(acc_o[n][0] + acc_o[n][2], acc_o[n][1] + acc_o[n][3]);
-                    if constexpr (KV8) {   // the V scale of an E4M3 cache
-                        o.x *= vsc;
-                        o.y *= vsc;
+                    const float2 o = make_float2(acc_o[n][0] + acc_o[n][2], acc_o[n][1] + acc_o[n][3]);
+                    if constexpr (KV8) {
+                        // n-tile n = 2 blk + parity holds dims 16 blk + 2 c +
+                        // parity for its columns c; times the V scale
+                        const int d = 16 * (n >> 1) + 4 * q4 + (n & 1);
+                        sh.o[warp][g0][d] = o.x * vsc;
+                        sh.o[warp][g0][d + 2] = o.y * vsc;
+                    } else {
+                        *reinterpret_cast<float2 *>(&sh.o[warp][g0][8 * n + 2 * q4]) = o;
                     }
-                    *reinterpret_cast<float2 *>(&sh.o[warp][g0][8 * n + 2 * q4]) = o;
                 }
             }
             consumer_sync();
