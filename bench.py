@@ -502,7 +502,8 @@ def run_ours(args, ranks):
     avg_main_s = ms_main / max(n_main, 1) * 1e-3
     hbm_peak, peak_kind = peaks()
     achieved = alg["total"] / avg_main_s / 1e9
-    traffic = None if (mods or multi or fp8) else traffic_for(main, w.name + ("/attend" if attend else ""))
+    traffic = None if (mods or multi) else traffic_for(
+        main, w.name + ("/attend" if attend else "") + ("/e4m3" if fp8 else ""))
 
     # ---- end to end through the public API, host buffers, copies inside
     Ke = min(K, 500)
