@@ -183,16 +183,16 @@ struct Shape {
 };
 
 // How a multi-token step is cut into virtual rows: tokens per chunk (so that
-// chunk rows G * tpc fit the 8 query rows of the tensor-core tile) and chunks
-// per batch row.
+// chunk rows G * tpc fit the query rows of a unit: 16 for the tensor-core
+// kernel, 8 for the CUDA-core one) and chunks per batch row.
 struct MultiCut {
     int tpc, chunks;
 };
 
-MultiCut multi_cut(int G, int max_q)
+MultiCut multi_cut(int G, int max_q, int rows)
 {
     MultiCut c;
-    c.tpc = G >= 8 ? 1 : 8 / G;
+    c.tpc = G >= rows ? 1 : rows / G;
     if (c.tpc > max_q)
         c.tpc = max_q > 0 ? max_q : 1;
     c.chunks = (max_q + c.tpc - 1) / c.tpc;
@@ -259,12 +259,12 @@ gqa_status run_step(const Shape &s, const void *q, const void *k_new, const void
     const int Gh = s.Hq / s.Hkv;
     if (s.multi && Gh > 8)
         return GQA_ERR_UNSUPPORTED;
-    const MultiCut cut = s.multi ? multi_cut(Gh, s.max_q) : MultiCut{1, 1};
-    const int G = Gh * cut.tpc;             // query rows of a unit
-    const int Bv = s.B * cut.chunks;        // (virtual) rows of the schedule
-    const int kernel = pick_kernel(opt, s.dt, s.D, G, s.paged, s.block_size);
+    const int kernel = pick_kernel(opt, s.dt, s.D, Gh, s.paged, s.block_size);
     if (kernel < 0)
         return GQA_ERR_UNSUPPORTED;
+    const MultiCut cut = s.multi ? multi_cut(Gh, s.max_q, kernel == GQA_KERNEL_TC ? 16 : 8) : MultiCut{1, 1};
+    const int G = Gh * cut.tpc;             // query rows of a unit
+    const int Bv = s.B * cut.chunks;        // (virtual) rows of the schedule
     const int grid = grid_for(kernel, opt, s.dt, s.D, G);
     if (grid <= 0)
         return GQA_ERR_CUDA;
@@ -506,19 +506,27 @@ size_t gqa_workspace_bytes_multi(int B, int Hq, int Hkv, int D, gqa_dtype dt, in
 {
     if (B < 0 || Hq < 1 || Hkv < 1 || D < 1 || Hq % Hkv || max_q_len < 0 || Hq / Hkv > 8)
         return 0;
-    const MultiCut cut = multi_cut(Hq / Hkv, max_q_len);
-    const int G = (Hq / Hkv) * cut.tpc;
-    int kernel = pick_kernel(opt, dt, D, G, false, 16);
-    if (kernel < 0)
-        return 0;
-    int grid = grid_for(kernel, opt, dt, D, G);
-    if ((!opt || opt->kernel == GQA_KERNEL_AUTO) && simt_supports(D, G)) {
-        const int g2 = grid_for(GQA_KERNEL_SIMT, opt, dt, D, G);
-        grid = grid > g2 ? grid : g2;
+    const int Gh = Hq / Hkv;
+    // enough for whichever kernel the call will pick (AUTO may depend on the
+    // paged block size): the larger of the two cuts' workspaces
+    size_t bytes = 0;
+    for (int k = GQA_KERNEL_SIMT; k <= GQA_KERNEL_TC; ++k) {
+        const int want = opt ? opt->kernel : GQA_KERNEL_AUTO;
+        if (want != GQA_KERNEL_AUTO && want != k)
+            continue;
+        gqa_options o = opt ? *opt : gqa_options{};
+        o.kernel = k;
+        if (pick_kernel(&o, dt, D, Gh, false, 16) != k)
+            continue;
+        const MultiCut cut = multi_cut(Gh, max_q_len, k == GQA_KERNEL_TC ? 16 : 8);
+        const int G = Gh * cut.tpc;
+        const int grid = grid_for(k, &o, dt, D, G);
+        if (grid <= 0)
+            continue;
+        const size_t b = workspace_layout(B * cut.chunks, Hkv, G, D, grid).bytes;
+        bytes = b > bytes ? b : bytes;
     }
-    if (grid <= 0)
-        return 0;
-    return workspace_layout(B * cut.chunks, Hkv, G, D, grid).bytes;
+    return bytes;
 }
 
 gqa_status gqa_decode_multi(const void *q, const void *k_new, const void *v_new, void *k_cache,

@@ -567,15 +567,18 @@ __device__ __forceinline__ float fast_ex2(float x)
 // Shared-memory scratch of a segment's epilogue and of the in-kernel merge of
 // a cut unit's partials.
 constexpr int kMergeMax = 32;   // partials merged through shared memory (more: direct loads)
-constexpr int kMergeG = 8;      // heads per unit (G <= 8)
+constexpr int kMergeG = 8;      // query rows per unit (G <= 8)
 constexpr int kMergeW = 4;      // warps whose states a segment merges
-struct MergeBuf {
-    float a[kMergeW][kMergeG];      // weight 2^(m_w - M) of each warp's state
-    float M[kMergeG], den[kMergeG];
-    float w[kMergeMax * kMergeG];   // partial max, then its weight 2^(m_i - M)
-    float l[kMergeMax * kMergeG];
-    float inv_den[kMergeG];
+// For GR query rows per unit, up to KM partials merged through shared memory.
+template <int GR, int KM>
+struct MergeBufT {
+    float a[kMergeW][GR];      // weight 2^(m_w - M) of each warp's state
+    float M[GR], den[GR];
+    float w[KM * GR];          // partial max, then its weight 2^(m_i - M)
+    float l[KM * GR];
+    float inv_den[GR];
 };
+using MergeBuf = MergeBufT<kMergeG, kMergeMax>;
 
 // End of a unit segment. The NW per-warp states of the segment are in shared
 // memory: sm_m[w][g] (base-2 running max, -inf for a warp that saw no slot),
@@ -611,14 +614,14 @@ __device__ __forceinline__ float *out_row(const DecodeParams &p, const TileCurso
 }
 
 // MULTI: the unit may be a chunk of a multi-token step (any form then works).
-template <int NW, int GP, int DD, int DP, bool MULTI, class Sync>
+template <int NW, int GP, int DD, int DP, bool MULTI, class Sync, int GR, int KM>
 __device__ inline void finish_segment(const DecodeParams &p, const TileCursor &cur, const TileWalk &walk,
                                       int seg_first_t,
                                       bool bad, const float (&sm_m)[NW][GP], const float (&sm_l)[NW][GP],
-                                      const float (&sm_o)[NW][GP][DP], int *sm_flag, MergeBuf &mb,
+                                      const float (&sm_o)[NW][GP][DP], int *sm_flag, MergeBufT<GR, KM> &mb,
                                       int tid, int nthr, Sync sync)
 {
-    static_assert(NW <= kMergeW && GP <= kMergeG && DP >= DD, "merge buffer too small");
+    static_assert(NW <= kMergeW && GP <= GR && DP >= DD, "merge buffer too small");
     const int G = p.G, b = cur.b, kvh = cur.kvh;
     const bool unit_done = (cur.t == cur.nr - 1);
     const bool whole = (seg_first_t == 0) && unit_done;
@@ -714,7 +717,7 @@ __device__ inline void finish_segment(const DecodeParams &p, const TileCursor &c
     if (*sm_flag) {
         const int K = last - first + 1;
         const long long P0 = (long long)u + first;
-        if (K <= kMergeMax) {
+        if (K <= KM) {
             // one parallel load of every partial's (m, l), weights per head,
             // then independent (vector) loads of the partial outputs
             for (int k = tid; k < K * G; k += nthr) {

@@ -48,11 +48,13 @@
 //    score scale, the V scale multiplies the accumulator before the epilogue,
 //    and the appended token is quantised (float32 division by the scale,
 //    round to nearest even, saturating).
-//  * multi-token steps (MULTI): a unit is a chunk of up to 8 / G tokens of a
-//    row; its query rows are (token, head) pairs gathered by one bulk copy per
-//    token, each row is masked beyond its own token's position, every slot
-//    holding a new token is substituted from k_new / v_new as below, and the
-//    chunk appends its own tokens.
+//  * multi-token steps (MULTI): a unit is a chunk of up to 16 / G tokens of a
+//    row; its query rows are (token, head) pairs, up to 16 distinct rows in
+//    the 16 MMA rows (so P enters in plain bf16, no remainder rows), gathered
+//    by one bulk copy per token; each row is masked beyond its own token's
+//    position and keeps its own softmax state, every slot holding a new token
+//    is substituted from k_new / v_new as below, and the chunk appends its own
+//    tokens.
 //  * the new token (decode step only; the read-only attend reads slot L from
 //    the cache like any other): in the tile that holds slot L the owning warp writes
 //    k_new / v_new into the ring slot of row L (the TMA copy of the stale
@@ -97,10 +99,11 @@ constexpr long long kWaitCycles = 4LL << 30;          // ~2 s at 2 GHz
 
 // Ring geometry for a bfloat16 (QF32 = false) or float32 query over a
 // bfloat16 or E4M3 (KV8) cache.
-template <bool QF32, bool KV8 = false>
+template <bool QF32, bool KV8 = false, bool MULTI = false>
 struct Ring {
     static constexpr int kQElem = QF32 ? 4 : 2;
-    static constexpr int kQBytes = kGMax * kD * kQElem;              // the unit's G query rows
+    static constexpr int kQRows = MULTI ? 2 * kGMax : kGMax;         // query rows of a unit
+    static constexpr int kQBytes = kQRows * kD * kQElem;             // the unit's query rows
     static constexpr int kKVBytes = KV8 ? kTile * kD : 2 * kHalfBytes; // K (or V) of one tile
     static constexpr int kStageBytes = 2 * kKVBytes + kQBytes;       // K (lo, hi), V (lo, hi), Q
     static constexpr int kNumStages = KV8 ? 4 : kStages;
@@ -263,8 +266,11 @@ __device__ __forceinline__ void split_bf16(float2 v, uint32_t &hi, uint32_t &lo)
 // under the 128-byte swizzle (the half starts on a 1024-byte boundary).
 __device__ __forceinline__ uint32_t swz(int r, int c8) { return (uint32_t)(r * 128 + ((c8 ^ (r & 7)) << 4)); }
 
-template <int NS>
+// NS ring stages; RW query rows per unit (8, or 16 for multi-token units,
+// whose o rows take less padding to fit two CTAs per SM).
+template <int NS, int RW = kGMax>
 struct Shared {
+    static constexpr int kOPad = RW == kGMax ? 8 : 4;
     uint64_t full[NS];
     uint64_t empty[NS];
     int stage_bad[NS];
@@ -272,10 +278,10 @@ struct Shared {
     int last_flag;
     long long sched[kThreads / 32 + 8];
     TileWalk walk;
-    float m[kConsumerWarps][kGMax];
-    float l[kConsumerWarps][kGMax];
-    alignas(16) float o[kConsumerWarps][kGMax][kD + 8];   // rows padded: conflict-free 8-byte stores
-    MergeBuf merge;
+    float m[kConsumerWarps][RW];
+    float l[kConsumerWarps][RW];
+    alignas(16) float o[kConsumerWarps][RW][kD + kOPad];  // rows padded: (near) conflict-free 8-byte stores
+    MergeBufT<RW, RW == kGMax ? kMergeMax : 16> merge;
 };
 
 __device__ __forceinline__ void consumer_sync()
@@ -293,12 +299,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                      const __grid_constant__ CUtensorMap mv)
 {
     static_assert(!(KV8 && MULTI), "E4M3 caches take single-token steps");
-    using RG = Ring<QF32, KV8>;
+    using RG = Ring<QF32, KV8, MULTI>;
+    static_assert(!(MULTI && QF32), "multi-token steps take a bfloat16 query");
+    constexpr int kRW = MULTI ? 2 * kGMax : kGMax;   // query rows of a unit
     constexpr int kStageBytes = RG::kStageBytes;
     constexpr int kNS = RG::kNumStages;   // ring depth
     constexpr int kKVB = RG::kKVBytes;    // K (or V) bytes of one tile
     extern __shared__ uint8_t dyn_smem[];
-    __shared__ Shared<kNS> sh;
+    __shared__ Shared<kNS, kRW> sh;
     uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
     const uint32_t ring_u32 = smem_u32(ring);
 
@@ -476,8 +484,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     int seg_first_t = 0;
     bool seg_start = true, row_good = true, aborted = false;
     int seg_bad = 0;
-    // multi-token units only: this lane's row g0 (last slot, window start), rows with data
-    int lim = 0, lo_r = 0, qrows = G;
+    // multi-token units only: this lane's rows g0 and g0 + 8 (last slot,
+    // window start, softmax state of the second), rows with data
+    int lim = 0, lo_r = 0, lim1 = 0, lo_r1 = 0, qrows = G;
+    float m_run1 = -INFINITY, l_run1 = 0.f;
     // E4M3 cache: the unit's score scale (with k_scale) and v_scale
     float ssc = p.scale_log2, vsc = 1.f;
 
@@ -497,10 +507,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             seg_bad = 0;
             seg_start = false;
             if constexpr (MULTI) {
-                lim = L - (cur.nq - 1 - g0 / p.Gh);   // row g0 is token g0 / Gh of the chunk
+                lim = L - (cur.nq - 1 - g0 / p.Gh);          // row g0 is token g0 / Gh of the chunk
+                lim1 = L - (cur.nq - 1 - (g0 + 8) / p.Gh);   // row g0 + 8
                 qrows = p.Gh * cur.nq;
-                if constexpr (WIN)
+                m_run1 = -INFINITY;
+                l_run1 = 0.f;
+                if constexpr (WIN) {
                     lo_r = max(0, lim - p.window + 1);
+                    lo_r1 = max(0, lim1 - p.window + 1);
+                }
             }
             if constexpr (KV8) {
                 ssc = p.scale_log2 * __ldg(p.k_scale + kvh);
@@ -572,6 +587,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     const bool on = g0 < (MULTI ? qrows : G);
                     qa[ks][0] = on ? *reinterpret_cast<const uint32_t *>(qs + (16 * ks + 2 * q4) * 2) : 0u;
                     qa[ks][1] = on ? *reinterpret_cast<const uint32_t *>(qs + (16 * ks + 8 + 2 * q4) * 2) : 0u;
+                    if constexpr (MULTI) {   // row g0 + 8: a query row of its own
+                        const bool on1 = g0 + 8 < qrows;
+                        const uint8_t *qs1 = qs + 8 * (kD * 2);
+                        ql[ks][0] = on1 ? *reinterpret_cast<const uint32_t *>(qs1 + (16 * ks + 2 * q4) * 2) : 0u;
+                        ql[ks][1] = on1 ? *reinterpret_cast<const uint32_t *>(qs1 + (16 * ks + 8 + 2 * q4) * 2) : 0u;
+                    }
                 }
             }
         }
@@ -697,7 +718,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     uint32_t kb[4];
                     float(&acc)[2][4] = (ks & 1) ? s_odd : s_acc;
                     ldsm_x4(kbase + (c >> 3) * kHalfBytes + swz(r, c & 7), kb);
-                    if constexpr (QF32) {
+                    if constexpr (QF32 || MULTI) {   // rows g0 + 8: the remainder / a second query row
                         mma_bf16(acc[0], qa[ks][0], ql[ks][0], qa[ks][1], ql[ks][1], kb[0], kb[1]);
                         mma_bf16(acc[1], qa[ks][0], ql[ks][0], qa[ks][1], ql[ks][1], kb[2], kb[3]);
                     } else {
@@ -711,61 +732,117 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     for (int e = 0; e < 4; ++e)
                         s_acc[nt][e] += s_odd[nt][e];
             }
-            // ---- masked online softmax (base 2), rows g0; only the partial
-            // tiles (the last one, those below a window's start) test slots
-            float x[2][2];
-            float mx = -INFINITY;
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int j = slot0 + row0 + 8 * nt + 2 * q4 + e;
-                    float sc = s_acc[nt][e];
-                    if constexpr (QF32)
-                        sc += s_acc[nt][e + 2];   // row g0 + 8: the query remainder
-                    const bool on = MULTI ? (WIN ? attended(lim, lo_r, cur.P, j) : j <= lim)
-                                          : (WIN ? attended(L, cur.lo, cur.P, j) : j <= L);
-                    x[nt][e] = (!partial || on) ? sc * (KV8 ? ssc : p.scale_log2) : -INFINITY;
-                    mx = fmaxf(mx, x[nt][e]);
-                }
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            if (mx > m_run + 8.f) {          // raise the running max (also from -inf)
-                const float alpha = (m_run == -INFINITY) ? 0.f : fast_ex2(m_run - mx);
-                l_run *= alpha;
-#pragma unroll
-                for (int n = 0; n < 16; ++n) {
-                    acc_o[n][0] *= alpha;
-                    acc_o[n][1] *= alpha;
-                    acc_o[n][2] *= alpha;
-                    acc_o[n][3] *= alpha;
-                }
-                m_run = mx;
-            }
             uint32_t pa[4];
-            {
-                float pr[2][2];
+            if constexpr (MULTI) {
+                // two query rows per lane, g0 (c0, c1) and g0 + 8 (c2, c3), each
+                // with its own causal bound, window and softmax state; P in bf16
+                float x0[2][2], x1[2][2];
+                float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
-                        pr[nt][e] = (x[nt][e] == -INFINITY) ? 0.f : fast_ex2(x[nt][e] - m_run);
-                        l_run += pr[nt][e];
+                        const int j = slot0 + row0 + 8 * nt + 2 * q4 + e;
+                        const bool on0 = WIN ? attended(lim, lo_r, cur.P, j) : j <= lim;
+                        const bool on1 = WIN ? attended(lim1, lo_r1, cur.P, j) : j <= lim1;
+                        x0[nt][e] = (!partial || on0) ? s_acc[nt][e] * p.scale_log2 : -INFINITY;
+                        x1[nt][e] = (!partial || on1) ? s_acc[nt][e + 2] * p.scale_log2 : -INFINITY;
+                        mx0 = fmaxf(mx0, x0[nt][e]);
+                        mx1 = fmaxf(mx1, x1[nt][e]);
                     }
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+                if (mx0 > m_run + 8.f) {
+                    const float alpha = (m_run == -INFINITY) ? 0.f : fast_ex2(m_run - mx0);
+                    l_run *= alpha;
+#pragma unroll
+                    for (int n = 0; n < 16; ++n) {
+                        acc_o[n][0] *= alpha;
+                        acc_o[n][1] *= alpha;
+                    }
+                    m_run = mx0;
+                }
+                if (mx1 > m_run1 + 8.f) {
+                    const float alpha = (m_run1 == -INFINITY) ? 0.f : fast_ex2(m_run1 - mx1);
+                    l_run1 *= alpha;
+#pragma unroll
+                    for (int n = 0; n < 16; ++n) {
+                        acc_o[n][2] *= alpha;
+                        acc_o[n][3] *= alpha;
+                    }
+                    m_run1 = mx1;
+                }
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt) {
-                    if constexpr (KV8) {
-                        uint32_t hi, lo;
-                        split_f16(make_float2(pr[nt][0], pr[nt][1]), hi, lo);
-                        pa[2 * nt] = hi;
-                        pa[2 * nt + 1] = lo;
-                        continue;
+                    float p0[2], p1[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        p0[e] = (x0[nt][e] == -INFINITY) ? 0.f : fast_ex2(x0[nt][e] - m_run);
+                        p1[e] = (x1[nt][e] == -INFINITY) ? 0.f : fast_ex2(x1[nt][e] - m_run1);
+                        l_run += p0[e];
+                        l_run1 += p1[e];
                     }
-                    const uint32_t hi = pack_bf16(pr[nt][0], pr[nt][1]);
-                    const float h0 = __uint_as_float(hi << 16), h1 = __uint_as_float(hi & 0xffff0000u);
-                    const uint32_t lo = pack_bf16(pr[nt][0] - h0, pr[nt][1] - h1);
-                    pa[2 * nt] = hi;      // rows g0:   slots 8nt + 2q4, +1
-                    pa[2 * nt + 1] = lo;  // rows g0+8
+                    pa[2 * nt] = pack_bf16(p0[0], p0[1]);       // row g0:     slots 8nt + 2q4, +1
+                    pa[2 * nt + 1] = pack_bf16(p1[0], p1[1]);   // row g0 + 8
+                }
+            } else {
+                // ---- masked online softmax (base 2), rows g0; only the partial
+                // tiles (the last one, those below a window's start) test slots
+                float x[2][2];
+                float mx = -INFINITY;
+    #pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+    #pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int j = slot0 + row0 + 8 * nt + 2 * q4 + e;
+                        float sc = s_acc[nt][e];
+                        if constexpr (QF32)
+                            sc += s_acc[nt][e + 2];   // row g0 + 8: the query remainder
+                        const bool on = MULTI ? (WIN ? attended(lim, lo_r, cur.P, j) : j <= lim)
+                                              : (WIN ? attended(L, cur.lo, cur.P, j) : j <= L);
+                        x[nt][e] = (!partial || on) ? sc * (KV8 ? ssc : p.scale_log2) : -INFINITY;
+                        mx = fmaxf(mx, x[nt][e]);
+                    }
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                if (mx > m_run + 8.f) {          // raise the running max (also from -inf)
+                    const float alpha = (m_run == -INFINITY) ? 0.f : fast_ex2(m_run - mx);
+                    l_run *= alpha;
+    #pragma unroll
+                    for (int n = 0; n < 16; ++n) {
+                        acc_o[n][0] *= alpha;
+                        acc_o[n][1] *= alpha;
+                        acc_o[n][2] *= alpha;
+                        acc_o[n][3] *= alpha;
+                    }
+                    m_run = mx;
+                }
+                {
+                    float pr[2][2];
+    #pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+    #pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            pr[nt][e] = (x[nt][e] == -INFINITY) ? 0.f : fast_ex2(x[nt][e] - m_run);
+                            l_run += pr[nt][e];
+                        }
+    #pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        if constexpr (KV8) {
+                            uint32_t hi, lo;
+                            split_f16(make_float2(pr[nt][0], pr[nt][1]), hi, lo);
+                            pa[2 * nt] = hi;
+                            pa[2 * nt + 1] = lo;
+                            continue;
+                        }
+                        const uint32_t hi = pack_bf16(pr[nt][0], pr[nt][1]);
+                        const float h0 = __uint_as_float(hi << 16), h1 = __uint_as_float(hi & 0xffff0000u);
+                        const uint32_t lo = pack_bf16(pr[nt][0] - h0, pr[nt][1] - h1);
+                        pa[2 * nt] = hi;      // rows g0:   slots 8nt + 2q4, +1
+                        pa[2 * nt + 1] = lo;  // rows g0+8
+                    }
                 }
             }
             // ---- O += P V (16 n-tiles of 8 dims)
@@ -820,7 +897,23 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             float l_tot = l_run;
             l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 1);
             l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 2);
-            if (g0 < G) {
+            float l_tot1 = l_run1;
+            l_tot1 += __shfl_xor_sync(0xffffffffu, l_tot1, 1);
+            l_tot1 += __shfl_xor_sync(0xffffffffu, l_tot1, 2);
+            if constexpr (MULTI) {   // rows g0 and g0 + 8, each its own query row
+                if (q4 == 0) {
+                    sh.m[warp][g0] = m_run;
+                    sh.l[warp][g0] = l_tot;
+                    sh.m[warp][g0 + 8] = m_run1;
+                    sh.l[warp][g0 + 8] = l_tot1;
+                }
+#pragma unroll
+                for (int n = 0; n < 16; ++n) {
+                    *reinterpret_cast<float2 *>(&sh.o[warp][g0][8 * n + 2 * q4]) = make_float2(acc_o[n][0], acc_o[n][1]);
+                    *reinterpret_cast<float2 *>(&sh.o[warp][g0 + 8][8 * n + 2 * q4]) =
+                        make_float2(acc_o[n][2], acc_o[n][3]);
+                }
+            } else if (g0 < G) {
                 if (q4 == 0) {
                     sh.m[warp][g0] = m_run;
                     sh.l[warp][g0] = l_tot;
@@ -843,7 +936,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             const bool bad = !row_good || seg_bad;
             if (bad && row_good && tid == 0)
                 report(p, aborted ? kTimeout : kBadBlock);
-            finish_segment<kConsumerWarps, kGMax, kD, kD + 8, MULTI>(p, cur, walk, seg_first_t, bad, sh.m, sh.l, sh.o,
+            finish_segment<kConsumerWarps, kRW, kD, kD + Shared<kNS, kRW>::kOPad, MULTI>(p, cur, walk, seg_first_t,
+                                                                                   bad, sh.m, sh.l, sh.o,
                                                       &sh.last_flag, sh.merge, tid, kConsumerWarps * 32,
                                                       [] { consumer_sync(); });
             seg_start = true;
@@ -856,7 +950,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 template <bool QF32, bool WIN, bool MULTI, bool KV8 = false>
 cudaError_t launch_q(const DecodeParams &p, const TcMaps &maps, cudaStream_t st)
 {
-    constexpr int kDynSmem = Ring<QF32, KV8>::kDynSmem;
+    constexpr int kDynSmem = Ring<QF32, KV8, MULTI>::kDynSmem;
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(tc_decode_kernel<QF32, WIN, MULTI, KV8>,

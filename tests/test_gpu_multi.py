@@ -3,7 +3,8 @@ packed tokens cu_q[b] .. cu_q[b+1]-1 of row b are appended in place at slots
 lengths[b] + i and token i attends slots 0 .. lengths[b] + i
 ("groupQueryAttention": packed q/k/v, write offset cu_seqlens_k[b] - q_len[b],
 the causal bound). Against the CPU oracle on the same seeded inputs, both
-kernels, dense / slot_ids / paged, group sizes 1..8 (tokens per chunk 8..1),
+kernels, dense / slot_ids / paged, group sizes 1..8 (tokens per chunk: 16 / G
+on the tensor cores, 8 / G on the CUDA cores),
 rows with q_len 0, chunks crossing tiles, the softmax modifiers; the whole
 cache is compared with the oracle's appended host copy bit for bit. Bars:
 float32 1e-5; bfloat16 2e-2 max|V|."""
@@ -87,6 +88,10 @@ CASES = [
     ("g4_paged8", "paged", dict(Hq=8, Hkv=2, B=3, block_size=8, num_blocks=3 * 40, max_blocks=40,
                                 len_lo=0, len_hi=310, seed=408), [3, 6, 2]),
     ("f32_d64", "pr1_fp32", dict(B=3, Smax=256, len_lo=0, len_hi=250, seed=409), [3, 1, 4]),
+    # full 16-row units on the tensor cores (and two 8-row chunks on the CUDA cores)
+    ("g4_rows16", "llama3_8b", dict(B=3, Smax=400, len_lo=0, len_hi=390, seed=413), [4, 8, 3]),
+    ("g2_rows16", "llama3_8b", dict(Hq=4, Hkv=2, B=2, Smax=300, len_lo=0, len_hi=290, seed=414), [8, 16]),
+    ("g1_rows16", "llama3_8b", dict(Hq=2, Hkv=2, B=2, Smax=300, len_lo=0, len_hi=280, seed=415), [16, 5]),
 ]
 
 
@@ -110,7 +115,9 @@ def test_multi_with_window_and_sink(kernel):
 
 @pytest.mark.parametrize("kernel", ["simt", "tc"])
 def test_multi_q_len_one_matches_decode_step(kernel):
-    """q_len = 1 everywhere is the decode step: the same bits."""
+    """q_len = 1 everywhere is the decode step: the same appended bytes and
+    outputs within the bf16 bar (a multi-token tensor-core unit takes P in
+    plain bf16, the decode step splits it into bf16 + remainder)."""
     import gqa_kv_cache_gb300 as gqa
     w = W.small("llama3_8b", B=5, Smax=600, len_lo=0, len_hi=590, seed=411)
     t = {k: v.cuda() for k, v in W.generate(w, q_lens=[1] * w.B).items()}
@@ -118,7 +125,8 @@ def test_multi_q_len_one_matches_decode_step(kernel):
     a = _run_gpu(w, t, 1, kernel).clone()
     b = gqa.decode_step(t2["q"], t2["k_new"], t2["v_new"], t2["k_cache"], t2["v_cache"], t2["lengths"],
                         kernel=kernel)
-    assert torch.equal(a, b)
+    vmax = max(t["v_cache"].float().abs().max().item(), t["v_new"].float().abs().max().item())
+    assert (a - b).abs().max().item() <= BF16_REL_TOL * vmax
     assert torch.equal(t["k_cache"], t2["k_cache"]) and torch.equal(t["v_cache"], t2["v_cache"])
 
 
