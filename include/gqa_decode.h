@@ -319,9 +319,10 @@ gqa_status gqa_validate_attend(const int32_t *lengths, const int32_t *slot_ids,
  *  is gqa_workspace_bytes_multi(...). A bad row (length, slot id, block) gets
  *  NaN outputs for its tokens and its appends are skipped where their slots
  *  cannot be addressed. Rows with q_len = 0 are left alone.
- * Kernels: up to 8 / G tokens of a row (G = Hq / Hkv <= 8) share one pass over
- * the cache; longer runs are cut into chunks, each streaming the cache
- * again.
+ * Kernels: up to 16 / G tokens of a row (G = Hq / Hkv <= 8; 8 / G on the
+ * CUDA-core kernel) share one pass over the cache; longer runs are cut into
+ * chunks, each streaming the cache again. An E4M3 cache takes single-token
+ * steps only (GQA_ERR_UNSUPPORTED here).
  */
 size_t gqa_workspace_bytes_multi(int B, int Hq, int Hkv, int D, gqa_dtype dt, int max_q_len,
                                  const gqa_options *opt);
