@@ -149,23 +149,26 @@ def cached_slots_read(L, attend, window=0, kept_prefix=0):
     return (L - lo) + torch.clamp(lo, max=kept_prefix)
 
 
-def algorithmic_bytes_multi(w, t) -> dict:
+def algorithmic_bytes_multi(w, t, kv_es=None) -> dict:
     """Multi-token step: every cached slot read once, the new tokens' K/V
-    read and appended, q read, out written, index reads."""
+    read (their own dtype) and appended (cache element bytes), q read, out
+    written, index reads."""
     import torch
     L = t["lengths"].to(torch.int64)
     es = w.elem_bytes
+    kes = es if kv_es is None else kv_es      # cache element bytes (1 for E4M3)
     T = t["q"].shape[0]
-    kv = int(L.sum().item()) * w.Hkv * w.D * 2 * es
-    new = T * w.Hkv * w.D * es * 2
+    kv = int(L.sum().item()) * w.Hkv * w.D * 2 * kes
+    new_read = T * w.Hkv * w.D * es * 2
+    new_write = T * w.Hkv * w.D * kes * 2
     q = t["q"].numel() * t["q"].element_size()
     out = T * w.Hq * w.D * 4
     idx = w.B * 4 * (3 if w.slot_ids else 2)
     if w.paged:
         ql = (t["cu_q"][1:] - t["cu_q"][:-1]).to(torch.int64)
         idx += int(((L + ql + w.block_size - 1) // w.block_size).sum().item()) * 4
-    return {"kv_read": kv, "append_write": new, "new_kv_read": new, "q_read": q, "out_write": out,
-            "index_read": idx, "total": kv + 2 * new + q + out + idx}
+    return {"kv_read": kv, "append_write": new_write, "new_kv_read": new_read, "q_read": q, "out_write": out,
+            "index_read": idx, "total": kv + new_read + new_write + q + out + idx}
 
 
 def algorithmic_bytes(w, t, attend=False, window=0, kept_prefix=0, kv_es=None) -> dict:
@@ -431,8 +434,6 @@ def run_ours(args, ranks):
     if multi and (attend or args.window or args.kept_prefix):
         raise SystemExit("--q-len times the plain multi-token step (no --op attend / window)")
     fp8 = args.kv == "e4m3"
-    if fp8 and multi:
-        raise SystemExit("--kv e4m3 takes single-token steps")
     t = W.generate(w, dev, attend=attend, q_f32=attend and args.q_dtype != "cache",
                    q_lens=[args.q_len] * w.B if multi else None, kv_e4m3=fp8)
     torch.cuda.synchronize()
@@ -441,7 +442,7 @@ def run_ours(args, ranks):
     if fp8:
         mods = dict(mods or {}, k_scale=t["k_scale"], v_scale=t["v_scale"])
     step = step_fn(w, t, args.kernel, out, args.sched_pad, attend, mods, args.q_len)
-    alg = algorithmic_bytes_multi(w, t) if multi else algorithmic_bytes(w, t, attend, args.window,
+    alg = algorithmic_bytes_multi(w, t, 1 if fp8 else None) if multi else algorithmic_bytes(w, t, attend, args.window,
                                                                          args.kept_prefix, 1 if fp8 else None)
     flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush_r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)

@@ -286,12 +286,14 @@ def _multi_checks(q, k_new, v_new, caches, lengths, cu_q, out):
 
 def decode_multi(q, k_new, v_new, k_cache, v_cache, lengths, cu_q, slot_ids=None, *, max_q_len,
                  out=None, status=None, kernel="auto", grid_ctas=0, workspace=None, stream=None,
-                 sched_pad=None, sink=None, window=0, kept_prefix=0):
+                 sched_pad=None, sink=None, window=0, kept_prefix=0, k_scale=None,
+                 v_scale=None):
     """Multi-token step on a dense (R, Hkv, Smax, D) cache: the packed tokens
     cu_q[b] .. cu_q[b+1]-1 of row b (q (T, Hq, D), k_new / v_new (T, Hkv, D))
     are appended at slots lengths[b] + i and token i attends slots
-    0 .. lengths[b] + i. ``max_q_len`` bounds every q_len. Returns out
-    (T, Hq, D)."""
+    0 .. lengths[b] + i. ``max_q_len`` bounds every q_len. Over an E4M3
+    cache q, k_new and v_new are bfloat16 and ``k_scale`` / ``v_scale`` are
+    required, as in :func:`decode_step`. Returns out (T, Hq, D)."""
     dt, out = _multi_checks(q, k_new, v_new, (("k_cache", k_cache), ("v_cache", v_cache)), lengths,
                             cu_q, out)
     T, Hq, D = q.shape
@@ -301,7 +303,7 @@ def decode_multi(q, k_new, v_new, k_cache, v_cache, lengths, cu_q, slot_ids=None
         raise ValueError("shape mismatch between q, k_new, v_new and the caches")
     if slot_ids is not None and (slot_ids.dtype != torch.int32 or slot_ids.shape != (B,)):
         raise TypeError("slot_ids must be int32 of shape (B,)")
-    o = _opts(kernel, grid_ctas, sched_pad, sink, window, kept_prefix, q.device, B, Hq)
+    o = _opts(kernel, grid_ctas, sched_pad, sink, window, kept_prefix, q.device, B, Hq, k_scale, v_scale, Hkv)
     lib = _lib.load()
     need = lib.gqa_workspace_bytes_multi(B, Hq, Hkv, D, dt, int(max_q_len), ctypes.byref(o))
     ws = _workspace(q.device, need) if workspace is None else workspace
@@ -315,7 +317,8 @@ def decode_multi(q, k_new, v_new, k_cache, v_cache, lengths, cu_q, slot_ids=None
 
 def decode_multi_paged(q, k_new, v_new, k_blocks, v_blocks, block_table, lengths, cu_q, *, max_q_len,
                        out=None, status=None, kernel="auto", grid_ctas=0, workspace=None, stream=None,
-                       sched_pad=None, sink=None, window=0, kept_prefix=0):
+                       sched_pad=None, sink=None, window=0, kept_prefix=0, k_scale=None,
+                       v_scale=None):
     """Multi-token step on a paged cache (num_blocks, Hkv, block_size, D)."""
     dt, out = _multi_checks(q, k_new, v_new, (("k_blocks", k_blocks), ("v_blocks", v_blocks)), lengths,
                             cu_q, out)
@@ -327,7 +330,7 @@ def decode_multi_paged(q, k_new, v_new, k_blocks, v_blocks, block_table, lengths
     if block_table.dtype != torch.int32 or block_table.dim() != 2 or block_table.shape[0] != B \
             or not block_table.is_contiguous():
         raise TypeError("block_table must be a contiguous int32 (B, max_blocks) tensor")
-    o = _opts(kernel, grid_ctas, sched_pad, sink, window, kept_prefix, q.device, B, Hq)
+    o = _opts(kernel, grid_ctas, sched_pad, sink, window, kept_prefix, q.device, B, Hq, k_scale, v_scale, Hkv)
     lib = _lib.load()
     need = lib.gqa_workspace_bytes_multi(B, Hq, Hkv, D, dt, int(max_q_len), ctypes.byref(o))
     ws = _workspace(q.device, need) if workspace is None else workspace

@@ -238,8 +238,6 @@ gqa_status run_step(const Shape &s, const void *q, const void *k_new, const void
     if (kv8 && (!opt || !opt->k_scale || !opt->v_scale || (reinterpret_cast<uintptr_t>(opt->k_scale) & 3u) ||
                 (reinterpret_cast<uintptr_t>(opt->v_scale) & 3u)))
         return GQA_ERR_INVALID_ARGUMENT;
-    if (kv8 && s.multi)
-        return GQA_ERR_UNSUPPORTED;
     if (s.B == 0 || (s.multi && (s.T == 0 || s.max_q == 0)))
         return GQA_OK;
     if (!q || !kc || !vc || !lengths || !out || (s.paged && !block_table))
@@ -536,7 +534,8 @@ gqa_status gqa_decode_multi(const void *q, const void *k_new, const void *v_new,
                             size_t workspace_bytes, int32_t *d_status, void *stream,
                             const gqa_options *opt)
 {
-    Shape s = {B, Hq, Hkv, D, dt, false, R, Smax, 0, 0, 0, false, dt, true, T, max_q_len};
+    const gqa_dtype qdt = dt == GQA_DTYPE_E4M3 ? GQA_DTYPE_BF16 : dt;   // query and new tokens
+    Shape s = {B, Hq, Hkv, D, dt, false, R, Smax, 0, 0, 0, false, qdt, true, T, max_q_len};
     return run_step(s, q, k_new, v_new, k_cache, v_cache, lengths, slot_ids, nullptr, out, workspace,
                     workspace_bytes, d_status, stream, opt, cu_q);
 }
@@ -549,7 +548,8 @@ gqa_status gqa_decode_multi_paged(const void *q, const void *k_new, const void *
                                   size_t workspace_bytes, int32_t *d_status, void *stream,
                                   const gqa_options *opt)
 {
-    Shape s = {B, Hq, Hkv, D, dt, true, 0, 0, num_blocks, block_size, max_blocks, false, dt, true, T,
+    const gqa_dtype qdt = dt == GQA_DTYPE_E4M3 ? GQA_DTYPE_BF16 : dt;
+    Shape s = {B, Hq, Hkv, D, dt, true, 0, 0, num_blocks, block_size, max_blocks, false, qdt, true, T,
                max_q_len};
     return run_step(s, q, k_new, v_new, k_blocks, v_blocks, lengths, nullptr, block_table, out,
                     workspace, workspace_bytes, d_status, stream, opt, cu_q);

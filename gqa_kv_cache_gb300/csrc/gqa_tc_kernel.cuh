@@ -50,11 +50,12 @@
 //    round to nearest even, saturating).
 //  * multi-token steps (MULTI): a unit is a chunk of up to 16 / G tokens of a
 //    row; its query rows are (token, head) pairs, up to 16 distinct rows in
-//    the 16 MMA rows (so P enters in plain bf16, no remainder rows), gathered
-//    by one bulk copy per token; each row is masked beyond its own token's
-//    position and keeps its own softmax state, every slot holding a new token
-//    is substituted from k_new / v_new as below, and the chunk appends its own
-//    tokens.
+//    the 16 MMA rows (so P enters in plain bf16, f16 over an E4M3 cache; no
+//    remainder rows), gathered by one bulk copy per token; each row is masked
+//    beyond its own token's position and keeps its own softmax state, every
+//    slot holding a new token is substituted from k_new / v_new as below
+//    (quantised over an E4M3 cache), and the chunk appends its own tokens.
+//    With 16 query rows the E4M3 ring takes 3 stages (two CTAs per SM).
 //  * the new token (decode step only; the read-only attend reads slot L from
 //    the cache like any other): in the tile that holds slot L the owning warp writes
 //    k_new / v_new into the ring slot of row L (the TMA copy of the stale
@@ -106,7 +107,9 @@ struct Ring {
     static constexpr int kQBytes = kQRows * kD * kQElem;             // the unit's query rows
     static constexpr int kKVBytes = KV8 ? kTile * kD : 2 * kHalfBytes; // K (or V) of one tile
     static constexpr int kStageBytes = 2 * kKVBytes + kQBytes;       // K (lo, hi), V (lo, hi), Q
-    static constexpr int kNumStages = KV8 ? 4 : kStages;
+    // E4M3: 4 stages; 3 with the 16 query rows of a multi-token unit, so two
+    // CTAs still share an SM
+    static constexpr int kNumStages = KV8 ? (MULTI ? 3 : 4) : kStages;
     static constexpr int kDynSmem = kNumStages * kStageBytes + 1024;
     static_assert(kStageBytes % 1024 == 0, "stages must stay 1024-byte aligned for the swizzle");
 };
@@ -292,13 +295,12 @@ __device__ __forceinline__ void consumer_sync()
 // WIN: a sliding window is in force. Without one the window fields of the
 // cursor are never read, so they take no registers and no code. MULTI: a
 // multi-token step (the chunk fields of the cursor are read only then). KV8:
-// an E4M3 cache (single-token forms).
+// an E4M3 cache.
 template <bool QF32, bool WIN, bool MULTI, bool KV8>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     tc_decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap mk,
                      const __grid_constant__ CUtensorMap mv)
 {
-    static_assert(!(KV8 && MULTI), "E4M3 caches take single-token steps");
     using RG = Ring<QF32, KV8, MULTI>;
     static_assert(!(MULTI && QF32), "multi-token steps take a bfloat16 query");
     constexpr int kRW = MULTI ? 2 * kGMax : kGMax;   // query rows of a unit
@@ -568,16 +570,29 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     }
                 }
             } else if constexpr (KV8) {
-                // bf16 query as f16 (exact in the normal range)
+                // bf16 query as f16 (exact in the normal range); a multi-token
+                // unit's row g0 + 8 is a query row of its own
                 const uint8_t *qs = kring + 2 * kKVB + g0 * (kD * 2);
+                const int nrow = MULTI ? qrows : G;
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     qa[ks][0] = qa[ks][1] = 0u;
-                    if (g0 < G) {
+                    if (g0 < nrow) {
                         const uint32_t w0 = *reinterpret_cast<const uint32_t *>(qs + (16 * ks + 4 * q4) * 2);
                         const uint32_t w1 = *reinterpret_cast<const uint32_t *>(qs + (16 * ks + 4 * q4 + 2) * 2);
                         qa[ks][0] = pack_f16(bf16_lo(w0), bf16_hi(w0));
                         qa[ks][1] = pack_f16(bf16_lo(w1), bf16_hi(w1));
+                    }
+                    if constexpr (MULTI) {
+                        ql[ks][0] = ql[ks][1] = 0u;
+                        if (g0 + 8 < nrow) {
+                            const uint8_t *qs1 = qs + 8 * (kD * 2);
+                            const uint32_t w0 = *reinterpret_cast<const uint32_t *>(qs1 + (16 * ks + 4 * q4) * 2);
+                            const uint32_t w1 =
+                                *reinterpret_cast<const uint32_t *>(qs1 + (16 * ks + 4 * q4 + 2) * 2);
+                            ql[ks][0] = pack_f16(bf16_lo(w0), bf16_hi(w0));
+                            ql[ks][1] = pack_f16(bf16_lo(w1), bf16_hi(w1));
+                        }
                     }
                 }
             } else {
@@ -609,7 +624,30 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 // new-token rows: substituted from k_new / v_new (and appended
                 // by the unit owning the token); rows no query row attends:
                 // zero V
-                if constexpr (KV8) {
+                if constexpr (KV8 && MULTI) {
+                    // this warp's rows holding new tokens, quantised into the
+                    // ring; the unit that owns a token appends it (lanes 0-7:
+                    // K, 8-15: V, sixteen elements each)
+                    const int first_new = max(cur.Lb, slot0 + row0);
+                    const int last_new = min(L, slot0 + row0 + 15);
+                    const int c16 = lane & 7;
+                    const bool is_k = lane < 8;
+                    const float qsc = lane < 16 ? __ldg((is_k ? p.k_scale : p.v_scale) + kvh) : 1.f;
+                    for (int sn = first_new; sn <= last_new && lane < 16; ++sn) {
+                        const int lr = sn - slot0;
+                        const long long tok = cur.tokL - (L - sn);
+                        const long long nidx = (tok * p.Hkv + kvh) * kD;
+                        const uint4 *src = reinterpret_cast<const uint4 *>((is_k ? knew : vnew) + nidx) + 2 * c16;
+                        const uint4 q8 = quant_e4m3x16(__ldg(src), __ldg(src + 1), qsc);
+                        *reinterpret_cast<uint4 *>((is_k ? kring : vring) + swz(lr, c16)) = q8;
+                        if (sn > L - cur.nq) {
+                            const long long off = slot_offset(p, b, kvh, sn);
+                            if (off >= 0)
+                                reinterpret_cast<uint4 *>(static_cast<uint8_t *>(is_k ? p.k_cache : p.v_cache) +
+                                                          off)[c16] = q8;
+                        }
+                    }
+                } else if constexpr (KV8) {
                     // row L of the last tile: the new token, quantised into the
                     // ring and appended to the cache (lanes 0-7: K, 8-15: V,
                     // sixteen elements each)
@@ -707,8 +745,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                             uint32_t b0, b1;
                             e4m3x4_to_f16(kb[mm], b0, b1);
                             float(&acc)[2][4] = (ks & 1) ? s_odd : s_acc;
-                            mma_f16(acc[nt], qa[ks][0], QF32 ? ql[ks][0] : 0u, qa[ks][1], QF32 ? ql[ks][1] : 0u,
-                                    b0, b1);
+                            mma_f16(acc[nt], qa[ks][0], (QF32 || MULTI) ? ql[ks][0] : 0u, qa[ks][1],
+                                    (QF32 || MULTI) ? ql[ks][1] : 0u, b0, b1);
                         }
                     }
                 }
@@ -736,6 +774,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             if constexpr (MULTI) {
                 // two query rows per lane, g0 (c0, c1) and g0 + 8 (c2, c3), each
                 // with its own causal bound, window and softmax state; P in bf16
+                // (f16 over an E4M3 cache)
+                const float ssl = KV8 ? ssc : p.scale_log2;
                 float x0[2][2], x1[2][2];
                 float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
@@ -745,8 +785,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                         const int j = slot0 + row0 + 8 * nt + 2 * q4 + e;
                         const bool on0 = WIN ? attended(lim, lo_r, cur.P, j) : j <= lim;
                         const bool on1 = WIN ? attended(lim1, lo_r1, cur.P, j) : j <= lim1;
-                        x0[nt][e] = (!partial || on0) ? s_acc[nt][e] * p.scale_log2 : -INFINITY;
-                        x1[nt][e] = (!partial || on1) ? s_acc[nt][e + 2] * p.scale_log2 : -INFINITY;
+                        x0[nt][e] = (!partial || on0) ? s_acc[nt][e] * ssl : -INFINITY;
+                        x1[nt][e] = (!partial || on1) ? s_acc[nt][e + 2] * ssl : -INFINITY;
                         mx0 = fmaxf(mx0, x0[nt][e]);
                         mx1 = fmaxf(mx1, x1[nt][e]);
                     }
@@ -784,8 +824,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                         l_run += p0[e];
                         l_run1 += p1[e];
                     }
-                    pa[2 * nt] = pack_bf16(p0[0], p0[1]);       // row g0:     slots 8nt + 2q4, +1
-                    pa[2 * nt + 1] = pack_bf16(p1[0], p1[1]);   // row g0 + 8
+                    // row g0: slots 8nt + 2q4, +1; then row g0 + 8
+                    pa[2 * nt] = KV8 ? pack_f16(p0[0], p0[1]) : pack_bf16(p0[0], p0[1]);
+                    pa[2 * nt + 1] = KV8 ? pack_f16(p1[0], p1[1]) : pack_bf16(p1[0], p1[1]);
                 }
             } else {
                 // ---- masked online softmax (base 2), rows g0; only the partial
@@ -909,9 +950,18 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 }
 #pragma unroll
                 for (int n = 0; n < 16; ++n) {
-                    *reinterpret_cast<float2 *>(&sh.o[warp][g0][8 * n + 2 * q4]) = make_float2(acc_o[n][0], acc_o[n][1]);
-                    *reinterpret_cast<float2 *>(&sh.o[warp][g0 + 8][8 * n + 2 * q4]) =
-                        make_float2(acc_o[n][2], acc_o[n][3]);
+                    if constexpr (KV8) {   // interleaved dims (as below), times the V scale
+                        const int d = 16 * (n >> 1) + 4 * q4 + (n & 1);
+                        sh.o[warp][g0][d] = acc_o[n][0] * vsc;
+                        sh.o[warp][g0][d + 2] = acc_o[n][1] * vsc;
+                        sh.o[warp][g0 + 8][d] = acc_o[n][2] * vsc;
+                        sh.o[warp][g0 + 8][d + 2] = acc_o[n][3] * vsc;
+                    } else {
+                        *reinterpret_cast<float2 *>(&sh.o[warp][g0][8 * n + 2 * q4]) =
+                            make_float2(acc_o[n][0], acc_o[n][1]);
+                        *reinterpret_cast<float2 *>(&sh.o[warp][g0 + 8][8 * n + 2 * q4]) =
+                            make_float2(acc_o[n][2], acc_o[n][3]);
+                    }
                 }
             } else if (g0 < G) {
                 if (q4 == 0) {

@@ -1,5 +1,5 @@
-// Tensor-core decode kernel, multi-token instantiations (bfloat16 query); the
-// kernel is in gqa_tc_kernel.cuh.
+// Tensor-core decode kernel, multi-token instantiations (bfloat16 query over a
+// bfloat16 or E4M3 cache); the kernel is in gqa_tc_kernel.cuh.
 #include "gqa_tc_kernel.cuh"
 
 namespace gqa {
@@ -8,6 +8,9 @@ cudaError_t tc_launch_multi(const DecodeParams &p, const TcMaps &maps, cudaStrea
 {
     if (!p.q_bf16)
         return cudaErrorInvalidValue;
+    if (p.kv8)
+        return p.window > 0 ? launch_q<false, true, true, true>(p, maps, st)
+                            : launch_q<false, false, true, true>(p, maps, st);
     return p.window > 0 ? launch_q<false, true, true>(p, maps, st) : launch_q<false, false, true>(p, maps, st);
 }
 

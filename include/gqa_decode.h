@@ -321,8 +321,9 @@ gqa_status gqa_validate_attend(const int32_t *lengths, const int32_t *slot_ids,
  *  cannot be addressed. Rows with q_len = 0 are left alone.
  * Kernels: up to 16 / G tokens of a row (G = Hq / Hkv <= 8; 8 / G on the
  * CUDA-core kernel) share one pass over the cache; longer runs are cut into
- * chunks, each streaming the cache again. An E4M3 cache takes single-token
- * steps only (GQA_ERR_UNSUPPORTED here).
+ * chunks, each streaming the cache again. Over an E4M3 cache (tensor-core
+ * kernel only) q, k_new and v_new are bfloat16, opt carries k_scale / v_scale
+ * and each appended token is quantised as in gqa_decode_step.
  */
 size_t gqa_workspace_bytes_multi(int B, int Hq, int Hkv, int D, gqa_dtype dt, int max_q_len,
                                  const gqa_options *opt);

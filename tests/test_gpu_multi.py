@@ -5,9 +5,10 @@ lengths[b] + i and token i attends slots 0 .. lengths[b] + i
 the causal bound). Against the CPU oracle on the same seeded inputs, both
 kernels, dense / slot_ids / paged, group sizes 1..8 (tokens per chunk: 16 / G
 on the tensor cores, 8 / G on the CUDA cores),
-rows with q_len 0, chunks crossing tiles, the softmax modifiers; the whole
-cache is compared with the oracle's appended host copy bit for bit. Bars:
-float32 1e-5; bfloat16 2e-2 max|V|."""
+rows with q_len 0, chunks crossing tiles, the softmax modifiers, E4M3 caches
+(each appended token quantised); the whole cache is compared with the
+oracle's appended host copy bit for bit. Bars: float32 1e-5; bfloat16 and
+E4M3 2e-2 max|V|."""
 import numpy as np
 import pytest
 import torch
@@ -28,6 +29,8 @@ def _tc_ok(w):
 def _run_gpu(w, t, max_q, kernel="auto", grid=0, status=None, **mods):
     import gqa_kv_cache_gb300 as gqa
     kw = dict(max_q_len=max_q, kernel=kernel, grid_ctas=grid, status=status, **mods)
+    if "k_scale" in t:                        # an E4M3 cache
+        kw.update(k_scale=t["k_scale"], v_scale=t["v_scale"])
     if w.paged:
         return gqa.decode_multi_paged(t["q"], t["k_new"], t["v_new"], t["k_blocks"], t["v_blocks"],
                                       t["block_table"], t["lengths"], t["cu_q"], **kw)
@@ -41,6 +44,8 @@ def _run_oracle(w, a, **mods):
         om["sink"] = mods["sink"].cpu().numpy()
     om["window"] = mods.get("window", 0)
     om["kept_prefix"] = mods.get("kept_prefix", 0)
+    if "k_scale" in a:
+        om.update(k_scale=a["k_scale"], v_scale=a["v_scale"])
     if w.paged:
         r = oracle.decode_multi_paged(a["q"], a["k_new"], a["v_new"], a["k_blocks"], a["v_blocks"],
                                       a["block_table"], a["lengths"], a["cu_q"], **om)
@@ -54,11 +59,15 @@ def _run_oracle(w, a, **mods):
 def _vmax(a):
     v = a["v_blocks"] if "v_blocks" in a else a["v_cache"]
     f = lambda x: (x.astype(np.uint32) << 16).view(np.float32) if x.dtype == np.uint16 else x
+    if v.dtype == np.uint8:                   # E4M3 bytes times the per-head scale
+        vf = torch.from_numpy(v).view(torch.float8_e4m3fn).float().numpy()
+        vc = np.abs(vf).max(axis=(0, 2, 3)) * a["v_scale"]
+        return float(max(vc.max(), np.abs(f(a["v_new"])).max()))
     return float(max(np.abs(f(v)).max(), np.abs(f(a["v_new"])).max()))
 
 
-def check_multi(w, q_lens, kernel="auto", grid=0, **mods):
-    t = {k: v.cuda() for k, v in W.generate(w, q_lens=q_lens).items()}
+def check_multi(w, q_lens, kernel="auto", grid=0, fp8=False, **mods):
+    t = {k: v.cuda() for k, v in W.generate(w, q_lens=q_lens, kv_e4m3=fp8).items()}
     a = {k: to_np(v) for k, v in t.items()}
     max_q = max(max(q_lens), 1)
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -103,6 +112,24 @@ def test_multi_small_cases(name, base, kw, q_lens, kernel, grid):
     if kernel == "tc" and not _tc_ok(w):
         pytest.skip("kernel does not take these sizes")
     check_multi(w, q_lens, kernel, grid)
+
+
+FP8_CASES = [c for c in CASES if c[0] not in ("f32_d64",)]
+
+
+@pytest.mark.parametrize("name,base,kw,q_lens", FP8_CASES, ids=[c[0] for c in FP8_CASES])
+@pytest.mark.parametrize("grid", [0, 7])
+def test_multi_fp8_small_cases(name, base, kw, q_lens, grid):
+    """E4M3 caches (tensor-core kernel): the quantised tokens appended bit for
+    bit, outputs within 2e-2 max|V| of the oracle over the same bytes."""
+    check_multi(W.small(base, **kw), q_lens, "tc", grid, fp8=True)
+
+
+def test_multi_fp8_window_sink():
+    w = W.small("llama3_8b", B=4, Smax=500, len_lo=100, len_hi=490, seed=416)
+    g = torch.Generator().manual_seed(4)
+    check_multi(w, [3, 4, 1, 2], "tc", 0, fp8=True, window=70, kept_prefix=9,
+                sink=(torch.randn(w.Hq, generator=g)).cuda())
 
 
 @pytest.mark.parametrize("kernel", ["simt", "tc"])
@@ -174,20 +201,23 @@ def test_validate_multi_matches_oracle_rules():
         assert got == want, (trial, cu, L, bt)
 
 
-@pytest.mark.parametrize("name,q_len", [("llama3_8b", 2), ("llama3_8b", 4), ("paged", 3)])
-def test_multi_full_size(name, q_len):
+@pytest.mark.parametrize("name,q_len,fp8", [("llama3_8b", 2, False), ("llama3_8b", 4, False), ("paged", 3, False),
+                                            ("llama3_8b", 4, True), ("paged", 3, True)])
+def test_multi_full_size(name, q_len, fp8):
     """Full-size caches with q_len new tokens per row: the tokens of 3
     sampled rows against the oracle (the sampled rows' caches copied to the
     host), the appended slots bit for bit."""
     import gqa_kv_cache_gb300 as gqa
     w = W.WORKLOADS[name]
-    t = W.generate(w, "cuda", q_lens=[q_len] * w.B)
+    t = W.generate(w, "cuda", q_lens=[q_len] * w.B, kv_e4m3=fp8)
     rows = [0, w.B // 2, w.B - 1]
     sel = torch.tensor(rows, device="cuda")
     tok = torch.cat([torch.arange(int(t["cu_q"][b]), int(t["cu_q"][b + 1]), device="cuda") for b in rows])
     a = {"q": to_np(t["q"][tok]), "k_new": to_np(t["k_new"][tok]), "v_new": to_np(t["v_new"][tok]),
          "lengths": to_np(t["lengths"][sel]),
          "cu_q": np.arange(0, q_len * (len(rows) + 1), q_len, dtype=np.int32)}
+    if fp8:
+        a["k_scale"], a["v_scale"] = to_np(t["k_scale"]), to_np(t["v_scale"])
     if w.paged:
         bt = t["block_table"][sel].cpu().numpy()
         used = sorted(set(int(x) for x in bt[bt >= 0].tolist()))

@@ -1093,3 +1093,60 @@ def test_e4m3_library_sdpa_on_dequantised_cache():
         v = torch.from_numpy(dec(v8[b, :, :L + 1]) * vs[:, None, None].astype(np.float64)).repeat_interleave(3, 0)
         o = torch.nn.functional.scaled_dot_product_attention(torch.from_numpy(q[b]).double()[:, None], k, v)[:, 0]
         np.testing.assert_allclose(r.out[b], o.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def _e4m3_multi_case(seed, q_lens, Smax=24, Hq=4, Hkv=2, D=8):
+    rng = np.random.default_rng(seed)
+    finite = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8)
+    B = len(q_lens)
+    cu = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    T = int(cu[-1])
+    lens = np.array([rng.integers(0, Smax - n + 1) for n in q_lens], np.int32)
+    to_bf16 = lambda a: to_np(torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16))
+    q, kn, vn = (to_bf16(rng.normal(size=sh)) for sh in ((T, Hq, D), (T, Hkv, D), (T, Hkv, D)))
+    kc = rng.choice(finite, size=(B, Hkv, Smax, D)).astype(np.uint8)
+    vc = rng.choice(finite, size=(B, Hkv, Smax, D)).astype(np.uint8)
+    return dict(q=q, k_new=kn, v_new=vn, k_cache=kc, v_cache=vc, lengths=lens, cu_q=cu,
+                k_scale=np.array([0.013, 0.011], np.float32), v_scale=np.array([0.0113, 0.021], np.float32))
+
+
+def test_e4m3_multi_equals_successive_decode_steps():
+    """Over an E4M3 cache too, n tokens appended at once under the causal
+    bound equal n single-token steps (quantised appends and outputs, bit for
+    bit): each token is quantised on its own, and later tokens of the run
+    attend to the stored (quantised) earlier ones."""
+    q_lens = [3, 1, 4, 2]
+    c = _e4m3_multi_case(64, q_lens)
+    sc = dict(k_scale=c["k_scale"], v_scale=c["v_scale"])
+    kcm, vcm = c["k_cache"].copy(), c["v_cache"].copy()
+    rm = oracle.decode_multi_dense(c["q"], c["k_new"], c["v_new"], kcm, vcm, c["lengths"], c["cu_q"], **sc)
+    assert rm.status == oracle.OK
+    kcs, vcs = c["k_cache"].copy(), c["v_cache"].copy()
+    for b, n in enumerate(q_lens):
+        for i in range(n):
+            t = int(c["cu_q"][b]) + i
+            kb, vb = np.ascontiguousarray(kcs[b:b + 1]), np.ascontiguousarray(vcs[b:b + 1])
+            r = oracle.decode_dense(c["q"][t:t + 1], c["k_new"][t:t + 1], c["v_new"][t:t + 1], kb, vb,
+                                    np.array([c["lengths"][b] + i], np.int32), **sc)
+            kcs[b:b + 1], vcs[b:b + 1] = kb, vb
+            assert r.out.tobytes() == rm.out[t:t + 1].tobytes(), (b, i)
+    assert kcs.tobytes() == kcm.tobytes() and vcs.tobytes() == vcm.tobytes()
+
+
+def test_e4m3_multi_appends_the_library_cast():
+    """Each appended token's bytes are the library's E4M3 cast of
+    float32(k_new) / k_scale (in-range values), at slot lengths[b] + i."""
+    q_lens = [2, 3]
+    c = _e4m3_multi_case(65, q_lens)
+    kc, vc = c["k_cache"].copy(), c["v_cache"].copy()
+    r = oracle.decode_multi_dense(c["q"], c["k_new"], c["v_new"], kc, vc, c["lengths"], c["cu_q"],
+                                  k_scale=c["k_scale"], v_scale=c["v_scale"])
+    assert r.status == oracle.OK
+    bf = lambda a: (a.astype(np.uint32) << 16).view(np.float32)
+    for b, n in enumerate(q_lens):
+        for i in range(n):
+            t = int(c["cu_q"][b]) + i
+            s = int(c["lengths"][b]) + i
+            want_k = _e4m3_lib(bf(c["k_new"][t]) / c["k_scale"][:, None])
+            want_v = _e4m3_lib(bf(c["v_new"][t]) / c["v_scale"][:, None])
+            assert kc[b, :, s].tobytes() == want_k.tobytes() and vc[b, :, s].tobytes() == want_v.tobytes()
