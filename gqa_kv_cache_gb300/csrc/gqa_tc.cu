@@ -20,11 +20,7 @@ bool tc_supports(bool bf16, int D, int G, bool paged, int block_size)
 }
 
 int tc_tile() { return kTile; }
-int tc_ctas_per_sm() { return kCtasPerSm; }
-size_t tc_smem_bytes(bool q_bf16)
-{
-    return (q_bf16 ? Ring<false>::kDynSmem : Ring<true>::kDynSmem) + sizeof(Shared<kStages>);
-}
+int tc_ctas_per_sm(bool kv8, bool multi) { return (kv8 && !multi) ? kCtasPerSmKV8 : kCtasPerSm; }
 
 cudaError_t tc_launch(const DecodeParams &p, const TcMaps &maps, cudaStream_t st)
 {

@@ -11,21 +11,23 @@
 //    consumer ever waits on a global load. Table and row lookups for a tile
 //    are issued one tile ahead, before the wait for a free stage.
 //  * four consumer warps each take 16 slots of every tile and compute, on the
-//    tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate):
-//      S  = Q K^T   M = 16 query rows: rows 0..7 hold the G heads (rows >= G
-//                   are zero); a float32 query is split into bf16(q) in rows
-//                   0..7 and the remainder bf16(q - bf16(q)) in rows 8..15,
-//                   and the two halves of S are added (so q enters with ~16
-//                   significant bits at no extra MMA: rows 8..15 would be
-//                   padding); N = 8 slots, K = 16 dims, 8 steps over D = 128
-//                   (two accumulator chains per tile, even and odd steps);
-//      O += P V     M = 16 rows: rows 0..7 carry bf16(p) and rows 8..15 the
-//                   remainder bf16(p - bf16(p)), so p enters the product with
-//                   ~16 significant bits and the sum stays float32-accurate;
-//                   N = 8 dims (16 tiles over D), K = 16 slots.
-//    The S accumulator fragment is reused directly as the A fragment of the
-//    P V product. K fragments come from ldmatrix, V fragments from
-//    ldmatrix.trans; the swizzle makes both conflict-free.
+//    tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate), with the
+//    operands swapped so that the G <= 8 query rows are the N = 8 side:
+//      S^T = K Q^T    M = the warp's 16 slots, N = 8 query rows (rows >= G
+//                     are zero), K = 16 dims, 8 steps over D = 128 (two
+//                     accumulator chains, even and odd steps); a float32
+//                     query adds a second product with its bf16 remainders
+//                     bf16(q - bf16(q)), so q enters with ~16 significant bits;
+//      O^T += V^T P^T M = 16 dims (8 tiles over D), N = 8 query rows, K = 16
+//                     slots; P^T is bf16(p) plus a second product with the
+//                     remainders bf16(p - bf16(p)), so the weights keep ~16
+//                     significant bits and the sum stays float32-accurate.
+//    The K fragments come from ldmatrix, the V^T fragments from
+//    ldmatrix.trans (the swizzle makes both conflict-free), and the score
+//    fragment (slot, row pairs) becomes the P^T fragment (row, slot pairs)
+//    with one movmatrix transpose per 8 slots. Compared with putting the
+//    heads on the M = 16 side, no MMA row is padding: half the products and
+//    half the accumulator registers.
 //  * online softmax in float32 with base-2 scores (scale log2(e)/sqrt(D)
 //    folded in), a lazy rescale (the running max is only raised when a score
 //    exceeds it by more than 8, i.e. p <= 256), masking by selection so stale
@@ -34,24 +36,26 @@
 //    before the product (0 * NaN would not be 0). A window skips whole tiles
 //    (the schedule lists only tiles holding attended slots) and, for paged
 //    caches, whole blocks.
-//  * E4M3 caches (KV8): tiles arrive as bytes (half the traffic) through a
-//    4-stage ring, and the products run in f16 (every E4M3 value is an f16):
-//    K fragments come from a b16 ldmatrix over the byte rows -- each lane gets
-//    four consecutive E4M3 values, two conversions make its B fragment, and
+//  * E4M3 caches (KV8): tiles arrive as bytes (half the traffic), and the
+//    products run in f16 (every E4M3 value is an f16): K fragments come from a
+//    b16 ldmatrix over the byte rows -- each lane gets four consecutive E4M3
+//    values of a slot, two conversions make its part of the A fragment, and
 //    the query fragments are gathered in the same permuted order of the 16
-//    dims of a k-step (a dot product does not depend on the order); V
+//    dims of a k-step (a dot product does not depend on the order); V^T
 //    fragments come from ldmatrix.trans, whose byte pairs one byte permute
-//    splits into (slot, slot + 1) pairs of an even and of an odd dim, so each
-//    transposed matrix feeds two products and the accumulator columns are
-//    interleaved (undone in the epilogue). The query and P are f16 (a float32
-//    query and P split into hi + remainder as below); the K scale joins the
-//    score scale, the V scale multiplies the accumulator before the epilogue,
-//    and the appended token is quantised (float32 division by the scale,
-//    round to nearest even, saturating).
+//    splits into (slot, slot + 1) pairs of an even and of an odd dim, the two
+//    halves of one M = 16 tile (the dims are interleaved, undone in the
+//    epilogue). The query is f16 (a float32 one split into hi + remainder), P
+//    is f16; the K scale joins the score scale, the V scale multiplies the
+//    accumulator before the epilogue, and the appended token is quantised
+//    (float32 division by the scale, round to nearest even, saturating). With
+//    its smaller stages the single-token E4M3 kernel runs three CTAs per SM
+//    (2-stage rings, at most 128 registers a thread).
 //  * multi-token steps (MULTI): a unit is a chunk of up to 16 / G tokens of a
-//    row; its query rows are (token, head) pairs, up to 16 distinct rows in
-//    the 16 MMA rows (so P enters in plain bf16, f16 over an E4M3 cache; no
-//    remainder rows), gathered by one bulk copy per token; each row is masked
+//    row; its query rows are (token, head) pairs, up to 16 distinct rows, so
+//    these units keep the heads on the M = 16 side (S = Q K^T, O += P V, the
+//    score fragment reused as the A fragment of P; P in plain bf16, f16 over
+//    an E4M3 cache), gathered by one bulk copy per token; each row is masked
 //    beyond its own token's position and keeps its own softmax state, every
 //    slot holding a new token is substituted from k_new / v_new as below
 //    (quantised over an E4M3 cache), and the chunk appends its own tokens.
@@ -65,8 +69,8 @@
 //  * at the end of each unit segment the four warp states are merged in
 //    shared memory (finish_segment): a whole unit writes its output, a cut
 //    unit its partial state, and the last CTA of a cut unit merges them.
-// Two CTAs share each SM, so one CTA's segment epilogue overlaps the other's
-// streaming.
+// Two CTAs (three for the single-token E4M3 kernel) share each SM, so one
+// CTA's segment epilogue overlaps the others' streaming.
 // Every mbarrier wait is bounded. A wait that gives up sets GQA_STATUS_TIMEOUT
 // and a CTA-wide abort flag: the producer stops issuing and waits (bounded)
 // for its copies in flight; the consumer warps stop waiting and computing but
@@ -87,11 +91,15 @@ namespace {
 #ifndef GQA_TC_CTAS_PER_SM
 #define GQA_TC_CTAS_PER_SM 2
 #endif
+#ifndef GQA_TC_KV8_CTAS_PER_SM
+#define GQA_TC_KV8_CTAS_PER_SM 3
+#endif
 
 constexpr int kD = 128;
 constexpr int kTile = 64;                             // slots per tile
 constexpr int kStages = GQA_TC_STAGES;                // depth of one CTA's TMA ring (bf16)
 constexpr int kCtasPerSm = GQA_TC_CTAS_PER_SM;        // resident CTAs per SM
+constexpr int kCtasPerSmKV8 = GQA_TC_KV8_CTAS_PER_SM; // the same, single-token steps over an E4M3 cache
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kGMax = 8;
@@ -107,9 +115,10 @@ struct Ring {
     static constexpr int kQBytes = kQRows * kD * kQElem;             // the unit's query rows
     static constexpr int kKVBytes = KV8 ? kTile * kD : 2 * kHalfBytes; // K (or V) of one tile
     static constexpr int kStageBytes = 2 * kKVBytes + kQBytes;       // K (lo, hi), V (lo, hi), Q
-    // E4M3: 4 stages; 3 with the 16 query rows of a multi-token unit, so two
-    // CTAs still share an SM
-    static constexpr int kNumStages = KV8 ? (MULTI ? 3 : 4) : kStages;
+    // E4M3: 4 stages at two CTAs per SM, 2 at three; 3 with the 16 query
+    // rows of a multi-token unit, so two CTAs still share an SM
+    static constexpr int kNumStages = KV8 ? (MULTI ? 3 : (kCtasPerSmKV8 >= 3 ? 2 : 4)) : kStages;
+    static constexpr int kCtas = (KV8 && !MULTI) ? kCtasPerSmKV8 : kCtasPerSm;   // resident CTAs per SM
     static constexpr int kDynSmem = kNumStages * kStageBytes + 1024;
     static_assert(kStageBytes % 1024 == 0, "stages must stay 1024-byte aligned for the swizzle");
 };
@@ -258,6 +267,15 @@ __device__ __forceinline__ uint4 quant_e4m3x16(uint4 a, uint4 b, float scale)
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// The 8x8 matrix of 16-bit values held in fragment layout (lane 4 r + c holds
+// row r, columns 2 c and 2 c + 1) transposed in registers.
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t a)
+{
+    uint32_t d;
+    asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
+}
+
 // A float32 pair as bf16 hi parts and bf16 remainders: v = hi + lo to ~16 bits.
 __device__ __forceinline__ void split_bf16(float2 v, uint32_t &hi, uint32_t &lo)
 {
@@ -273,7 +291,7 @@ __device__ __forceinline__ uint32_t swz(int r, int c8) { return (uint32_t)(r * 1
 // whose o rows take less padding to fit two CTAs per SM).
 template <int NS, int RW = kGMax>
 struct Shared {
-    static constexpr int kOPad = RW == kGMax ? 8 : 4;
+    static constexpr int kOPad = 4;   // rows 132 floats apart: the epilogue's stores are conflict-free
     uint64_t full[NS];
     uint64_t empty[NS];
     int stage_bad[NS];
@@ -297,7 +315,7 @@ __device__ __forceinline__ void consumer_sync()
 // multi-token step (the chunk fields of the cursor are read only then). KV8:
 // an E4M3 cache.
 template <bool QF32, bool WIN, bool MULTI, bool KV8>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+__global__ void __launch_bounds__(kThreads, (Ring<QF32, KV8, MULTI>::kCtas))
     tc_decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap mk,
                      const __grid_constant__ CUtensorMap mv)
 {
@@ -479,9 +497,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     bool more = walk_first(p, cur, walk, in_b);
     int stage = 0;
     uint32_t phase = 0;
-    uint32_t qa[8][2];                   // Q fragments (rows g0 < G), 8 k-steps
-    uint32_t ql[8][2];                   // float32 query: the remainders (rows g0 + 8)
-    float acc_o[16][4];                  // O: 16 n-tiles of 8 dims, rows g0 (hi) and g0+8 (lo)
+    // Q fragments of query row g0 (< G), 8 k-steps: the B operand of S^T = K Q^T
+    // (single-token units) or rows 0-7 of the A operand of S = Q K^T
+    // (multi-token units)
+    uint32_t qa[8][2];
+    // float32 query: the remainders of row g0 (a second B operand);
+    // multi-token units: query row g0 + 8 (A rows 8-15)
+    uint32_t ql[8][2];
+    // O: multi-token units, 16 n-tiles of 8 dims for rows g0 and g0 + 8;
+    // single-token units, O^T in 8 m-tiles of 16 dims for rows 2 q4, 2 q4 + 1
+    constexpr int kOT = MULTI ? 16 : 8;
+    float acc_o[kOT][4];
     float m_run = -INFINITY, l_run = 0.f;
     int seg_first_t = 0;
     bool seg_start = true, row_good = true, aborted = false;
@@ -502,18 +528,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             if (!row_good && tid == 0 && cur.t == 0 && kvh == 0)
                 report(p, row_error_bits(p, b, L));
 #pragma unroll
-            for (int n = 0; n < 16; ++n)
+            for (int n = 0; n < kOT; ++n)
                 acc_o[n][0] = acc_o[n][1] = acc_o[n][2] = acc_o[n][3] = 0.f;
-            m_run = -INFINITY;
-            l_run = 0.f;
+            m_run = m_run1 = -INFINITY;
+            l_run = l_run1 = 0.f;
             seg_bad = 0;
             seg_start = false;
             if constexpr (MULTI) {
                 lim = L - (cur.nq - 1 - g0 / p.Gh);          // row g0 is token g0 / Gh of the chunk
                 lim1 = L - (cur.nq - 1 - (g0 + 8) / p.Gh);   // row g0 + 8
                 qrows = p.Gh * cur.nq;
-                m_run1 = -INFINITY;
-                l_run1 = 0.f;
                 if constexpr (WIN) {
                     lo_r = max(0, lim - p.window + 1);
                     lo_r1 = max(0, lim1 - p.window + 1);
@@ -724,57 +748,52 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             }
 
 
-            // ---- S = Q K^T for this warp's 16 slots (two n-tiles of 8);
-            // even and odd k-steps accumulate separately (shorter chains)
-            float s_acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            {
-                float s_odd[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                const int mi = lane >> 3, ri = lane & 7;
-                const int r = row0 + 8 * (mi >> 1) + ri;
-                if constexpr (KV8) {
-                    // matrix mi: slots 8 (mi >> 1) .. +7 of the warp, k-step
-                    // 2 kp + (mi & 1) (16 bytes of each row)
-                    const int rk = row0 + 8 * (mi >> 1) + ri;
+            if constexpr (MULTI) {
+                // ---- S = Q K^T for this warp's 16 slots (two n-tiles of 8);
+                // rows g0 and g0 + 8 are query rows of their own; even and odd
+                // k-steps accumulate separately (shorter chains)
+                float s_acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                {
+                    float s_odd[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                    const int mi = lane >> 3, ri = lane & 7;
+                    const int r = row0 + 8 * (mi >> 1) + ri;
+                    if constexpr (KV8) {
+                        // matrix mi: slots 8 (mi >> 1) .. +7, k-step 2 kp + (mi & 1)
+                        // (16 bytes of each row)
 #pragma unroll
-                    for (int kp = 0; kp < 4; ++kp) {
-                        uint32_t kb[4];
-                        ldsm_x4(kbase + swz(rk, 2 * kp + (mi & 1)), kb);
+                        for (int kp = 0; kp < 4; ++kp) {
+                            uint32_t kb[4];
+                            ldsm_x4(kbase + swz(r, 2 * kp + (mi & 1)), kb);
 #pragma unroll
-                        for (int mm = 0; mm < 4; ++mm) {
-                            const int ks = 2 * kp + (mm & 1), nt = mm >> 1;
-                            uint32_t b0, b1;
-                            e4m3x4_to_f16(kb[mm], b0, b1);
+                            for (int mm = 0; mm < 4; ++mm) {
+                                const int ks = 2 * kp + (mm & 1), nt = mm >> 1;
+                                uint32_t b0, b1;
+                                e4m3x4_to_f16(kb[mm], b0, b1);
+                                float(&acc)[2][4] = (ks & 1) ? s_odd : s_acc;
+                                mma_f16(acc[nt], qa[ks][0], ql[ks][0], qa[ks][1], ql[ks][1], b0, b1);
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks) {
+                            const int c = 2 * ks + (mi & 1);
+                            uint32_t kb[4];
                             float(&acc)[2][4] = (ks & 1) ? s_odd : s_acc;
-                            mma_f16(acc[nt], qa[ks][0], (QF32 || MULTI) ? ql[ks][0] : 0u, qa[ks][1],
-                                    (QF32 || MULTI) ? ql[ks][1] : 0u, b0, b1);
+                            ldsm_x4(kbase + (c >> 3) * kHalfBytes + swz(r, c & 7), kb);
+                            mma_bf16(acc[0], qa[ks][0], ql[ks][0], qa[ks][1], ql[ks][1], kb[0], kb[1]);
+                            mma_bf16(acc[1], qa[ks][0], ql[ks][0], qa[ks][1], ql[ks][1], kb[2], kb[3]);
                         }
                     }
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            s_acc[nt][e] += s_odd[nt][e];
                 }
-#pragma unroll
-                for (int ks = 0; ks < (KV8 ? 0 : 8); ++ks) {
-                    const int c = 2 * ks + (mi & 1);
-                    uint32_t kb[4];
-                    float(&acc)[2][4] = (ks & 1) ? s_odd : s_acc;
-                    ldsm_x4(kbase + (c >> 3) * kHalfBytes + swz(r, c & 7), kb);
-                    if constexpr (QF32 || MULTI) {   // rows g0 + 8: the remainder / a second query row
-                        mma_bf16(acc[0], qa[ks][0], ql[ks][0], qa[ks][1], ql[ks][1], kb[0], kb[1]);
-                        mma_bf16(acc[1], qa[ks][0], ql[ks][0], qa[ks][1], ql[ks][1], kb[2], kb[3]);
-                    } else {
-                        mma_bf16(acc[0], qa[ks][0], 0u, qa[ks][1], 0u, kb[0], kb[1]);
-                        mma_bf16(acc[1], qa[ks][0], 0u, qa[ks][1], 0u, kb[2], kb[3]);
-                    }
-                }
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        s_acc[nt][e] += s_odd[nt][e];
-            }
-            uint32_t pa[4];
-            if constexpr (MULTI) {
                 // two query rows per lane, g0 (c0, c1) and g0 + 8 (c2, c3), each
                 // with its own causal bound, window and softmax state; P in bf16
                 // (f16 over an E4M3 cache)
+                uint32_t pa[4];
                 const float ssl = KV8 ? ssc : p.scale_log2;
                 float x0[2][2], x1[2][2];
                 float mx0 = -INFINITY, mx1 = -INFINITY;
@@ -798,7 +817,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     const float alpha = (m_run == -INFINITY) ? 0.f : fast_ex2(m_run - mx0);
                     l_run *= alpha;
 #pragma unroll
-                    for (int n = 0; n < 16; ++n) {
+                    for (int n = 0; n < kOT; ++n) {
                         acc_o[n][0] *= alpha;
                         acc_o[n][1] *= alpha;
                     }
@@ -808,7 +827,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     const float alpha = (m_run1 == -INFINITY) ? 0.f : fast_ex2(m_run1 - mx1);
                     l_run1 *= alpha;
 #pragma unroll
-                    for (int n = 0; n < 16; ++n) {
+                    for (int n = 0; n < kOT; ++n) {
                         acc_o[n][2] *= alpha;
                         acc_o[n][3] *= alpha;
                     }
@@ -828,96 +847,192 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     pa[2 * nt] = KV8 ? pack_f16(p0[0], p0[1]) : pack_bf16(p0[0], p0[1]);
                     pa[2 * nt + 1] = KV8 ? pack_f16(p1[0], p1[1]) : pack_bf16(p1[0], p1[1]);
                 }
-            } else {
-                // ---- masked online softmax (base 2), rows g0; only the partial
-                // tiles (the last one, those below a window's start) test slots
-                float x[2][2];
-                float mx = -INFINITY;
-    #pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-    #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int j = slot0 + row0 + 8 * nt + 2 * q4 + e;
-                        float sc = s_acc[nt][e];
-                        if constexpr (QF32)
-                            sc += s_acc[nt][e + 2];   // row g0 + 8: the query remainder
-                        const bool on = MULTI ? (WIN ? attended(lim, lo_r, cur.P, j) : j <= lim)
-                                              : (WIN ? attended(L, cur.lo, cur.P, j) : j <= L);
-                        x[nt][e] = (!partial || on) ? sc * (KV8 ? ssc : p.scale_log2) : -INFINITY;
-                        mx = fmaxf(mx, x[nt][e]);
-                    }
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-                if (mx > m_run + 8.f) {          // raise the running max (also from -inf)
-                    const float alpha = (m_run == -INFINITY) ? 0.f : fast_ex2(m_run - mx);
-                    l_run *= alpha;
-    #pragma unroll
-                    for (int n = 0; n < 16; ++n) {
-                        acc_o[n][0] *= alpha;
-                        acc_o[n][1] *= alpha;
-                        acc_o[n][2] *= alpha;
-                        acc_o[n][3] *= alpha;
-                    }
-                    m_run = mx;
-                }
+                // ---- O += P V (16 n-tiles of 8 dims)
                 {
-                    float pr[2][2];
-    #pragma unroll
-                    for (int nt = 0; nt < 2; ++nt)
-    #pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            pr[nt][e] = (x[nt][e] == -INFINITY) ? 0.f : fast_ex2(x[nt][e] - m_run);
-                            l_run += pr[nt][e];
+                    const int mi = lane >> 3, ri = lane & 7;
+                    const int r = row0 + 8 * (mi & 1) + ri;
+                    if constexpr (KV8) {
+                        // matrix mi: slots 8 (mi & 1) .. +7, 16-dim block
+                        // 2 bp + (mi >> 1); each lane gets bytes (s, d), (s, d+1),
+                        // (s+1, d), (s+1, d+1) and splits them into the (s, s+1)
+                        // pairs of dim d (even) and d + 1 (odd)
+#pragma unroll
+                        for (int bp = 0; bp < 4; ++bp) {
+                            uint32_t vb[4];
+                            ldsm_x4_t(vbase + swz(r, 2 * bp + (mi >> 1)), vb);
+                            uint32_t ev[4], od[4];
+#pragma unroll
+                            for (int mm = 0; mm < 4; ++mm)
+                                e4m3x4_to_f16(__byte_perm(vb[mm], 0u, 0x3120u), ev[mm], od[mm]);
+#pragma unroll
+                            for (int hb = 0; hb < 2; ++hb) {   // block 2 bp + hb: matrices 2 hb (slots 0-7), 2 hb + 1
+                                const int blk = 2 * bp + hb;
+                                mma_f16(acc_o[2 * blk], pa[0], pa[1], pa[2], pa[3], ev[2 * hb], ev[2 * hb + 1]);
+                                mma_f16(acc_o[2 * blk + 1], pa[0], pa[1], pa[2], pa[3], od[2 * hb], od[2 * hb + 1]);
+                            }
                         }
-    #pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) {
-                        if constexpr (KV8) {
-                            uint32_t hi, lo;
-                            split_f16(make_float2(pr[nt][0], pr[nt][1]), hi, lo);
-                            pa[2 * nt] = hi;
-                            pa[2 * nt + 1] = lo;
-                            continue;
+                    } else {
+#pragma unroll
+                        for (int np = 0; np < 8; ++np) {
+                            const int c = 2 * np + (mi >> 1);
+                            uint32_t vb[4];
+                            ldsm_x4_t(vbase + (c >> 3) * kHalfBytes + swz(r, c & 7), vb);
+                            mma_bf16(acc_o[2 * np], pa[0], pa[1], pa[2], pa[3], vb[0], vb[1]);
+                            mma_bf16(acc_o[2 * np + 1], pa[0], pa[1], pa[2], pa[3], vb[2], vb[3]);
                         }
-                        const uint32_t hi = pack_bf16(pr[nt][0], pr[nt][1]);
-                        const float h0 = __uint_as_float(hi << 16), h1 = __uint_as_float(hi & 0xffff0000u);
-                        const uint32_t lo = pack_bf16(pr[nt][0] - h0, pr[nt][1] - h1);
-                        pa[2 * nt] = hi;      // rows g0:   slots 8nt + 2q4, +1
-                        pa[2 * nt + 1] = lo;  // rows g0+8
                     }
                 }
-            }
-            // ---- O += P V (16 n-tiles of 8 dims)
-            {
-                const int mi = lane >> 3, ri = lane & 7;
-                const int r = row0 + 8 * (mi & 1) + ri;
+            } else {
+                // ---- S^T = K Q^T: M = this warp's 16 slots, N = the 8 query
+                // rows, K = 16 dims per step. Lane (g0, q4) holds the scores of
+                // slots g0 (c0, c1) and g0 + 8 (c2, c3) for query rows 2 q4
+                // (c0, c2) and 2 q4 + 1 (c1, c3). Even and odd k-steps
+                // accumulate separately (shorter chains).
+                float st[4] = {0.f, 0.f, 0.f, 0.f};
+                {
+                    float st2[4] = {0.f, 0.f, 0.f, 0.f};
+                    const int mi = lane >> 3, ri = lane & 7;
+                    if constexpr (KV8) {
+                        // matrix mi: slots 8 (mi >> 1) .. +7, byte chunk
+                        // 2 kp + (mi & 1); each lane gets bytes 4 q4 .. +3 of its
+                        // slot, i.e. the k-step's dims in the permuted order the
+                        // query fragments use
+                        const int r = row0 + 8 * (mi >> 1) + ri;
+#pragma unroll
+                        for (int kp = 0; kp < 4; ++kp) {
+                            uint32_t kb[4];
+                            ldsm_x4(kbase + swz(r, 2 * kp + (mi & 1)), kb);
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                const int ks = 2 * kp + h;
+                                uint32_t lo0, hi0, lo1, hi1;
+                                e4m3x4_to_f16(kb[h], lo0, hi0);       // slots 0-7
+                                e4m3x4_to_f16(kb[2 + h], lo1, hi1);   // slots 8-15
+                                float(&acc)[4] = h ? st2 : st;
+                                mma_f16(acc, lo0, lo1, hi0, hi1, qa[ks][0], qa[ks][1]);
+                                if constexpr (QF32)   // the query remainders
+                                    mma_f16(acc, lo0, lo1, hi0, hi1, ql[ks][0], ql[ks][1]);
+                            }
+                        }
+                    } else {
+                        // matrix mi: slots 8 (mi & 1) .. +7, dims 16 ks + 8 (mi >> 1) .. +7
+                        const int r = row0 + 8 * (mi & 1) + ri;
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks) {
+                            const int c = 2 * ks + (mi >> 1);
+                            uint32_t kb[4];
+                            ldsm_x4(kbase + (c >> 3) * kHalfBytes + swz(r, c & 7), kb);
+                            float(&acc)[4] = (ks & 1) ? st2 : st;
+                            mma_bf16(acc, kb[0], kb[1], kb[2], kb[3], qa[ks][0], qa[ks][1]);
+                            if constexpr (QF32)   // the query remainders
+                                mma_bf16(acc, kb[0], kb[1], kb[2], kb[3], ql[ks][0], ql[ks][1]);
+                        }
+                    }
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        st[e] += st2[e];
+                }
+                // ---- masked online softmax (base 2) of rows 2 q4 (m_run) and
+                // 2 q4 + 1 (m_run1); only the partial tiles (the last one, those
+                // below a window's start) test slots. The row maxima need a
+                // reduction over the eight lanes sharing q4, which the lazy
+                // rescale makes rare: it runs only when some lane sees a score
+                // above its row's running max + 8 (a warp vote).
+                const float sl = KV8 ? ssc : p.scale_log2;
+                const int j0 = slot0 + row0 + g0;
+                const bool on0 = !partial || (WIN ? attended(L, cur.lo, cur.P, j0) : j0 <= L);
+                const bool on1 = !partial || (WIN ? attended(L, cur.lo, cur.P, j0 + 8) : j0 + 8 <= L);
+                const float x00 = on0 ? st[0] * sl : -INFINITY;   // row 2 q4,     slot g0
+                const float x10 = on0 ? st[1] * sl : -INFINITY;   // row 2 q4 + 1, slot g0
+                const float x01 = on1 ? st[2] * sl : -INFINITY;   // row 2 q4,     slot g0 + 8
+                const float x11 = on1 ? st[3] * sl : -INFINITY;   // row 2 q4 + 1, slot g0 + 8
+                float mx0 = fmaxf(x00, x01), mx1 = fmaxf(x10, x11);
+                if (__any_sync(0xffffffffu, mx0 > m_run + 8.f || mx1 > m_run1 + 8.f)) {
+#pragma unroll
+                    for (int off = 4; off < 32; off <<= 1) {
+                        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                    }
+                    if (mx0 > m_run + 8.f) {   // raise the running max (also from -inf)
+                        const float alpha = (m_run == -INFINITY) ? 0.f : fast_ex2(m_run - mx0);
+                        l_run *= alpha;
+#pragma unroll
+                        for (int n = 0; n < kOT; ++n) {
+                            acc_o[n][0] *= alpha;
+                            acc_o[n][2] *= alpha;
+                        }
+                        m_run = mx0;
+                    }
+                    if (mx1 > m_run1 + 8.f) {
+                        const float alpha = (m_run1 == -INFINITY) ? 0.f : fast_ex2(m_run1 - mx1);
+                        l_run1 *= alpha;
+#pragma unroll
+                        for (int n = 0; n < kOT; ++n) {
+                            acc_o[n][1] *= alpha;
+                            acc_o[n][3] *= alpha;
+                        }
+                        m_run1 = mx1;
+                    }
+                }
+                const float p00 = (x00 == -INFINITY) ? 0.f : fast_ex2(x00 - m_run);
+                const float p01 = (x01 == -INFINITY) ? 0.f : fast_ex2(x01 - m_run);
+                const float p10 = (x10 == -INFINITY) ? 0.f : fast_ex2(x10 - m_run1);
+                const float p11 = (x11 == -INFINITY) ? 0.f : fast_ex2(x11 - m_run1);
+                l_run += p00 + p01;
+                l_run1 += p10 + p11;
+                // P^T as the B operand of the next product: the lane's pairs
+                // (slot g0; rows 2 q4, 2 q4 + 1) transposed in registers into
+                // (row g0; slots 2 q4, 2 q4 + 1), per half of the 16 slots. Over
+                // a bf16 cache P enters as bf16 + a bf16 remainder (a second
+                // product), so the weights keep ~16 significant bits and the
+                // result does not depend on the split of a unit beyond float32
+                // rounding; over an E4M3 cache as f16 (11 bits).
+                uint32_t ph0, ph1, pl0 = 0u, pl1 = 0u;
                 if constexpr (KV8) {
-                    // matrix mi: slots 8 (mi & 1) .. +7, 16-dim block
-                    // 2 bp + (mi >> 1); each lane gets bytes (s, d), (s, d+1),
-                    // (s+1, d), (s+1, d+1) and splits them into the (s, s+1)
-                    // pairs of dim d (even) and d + 1 (odd)
+                    ph0 = pack_f16(p00, p10);
+                    ph1 = pack_f16(p01, p11);
+                } else {
+                    split_bf16(make_float2(p00, p10), ph0, pl0);
+                    split_bf16(make_float2(p01, p11), ph1, pl1);
+                    pl0 = movmatrix_t(pl0);
+                    pl1 = movmatrix_t(pl1);
+                }
+                const uint32_t pb0 = movmatrix_t(ph0), pb1 = movmatrix_t(ph1);
+                // ---- O^T += V^T P^T: M = 16 dims per tile, N = the 8 query
+                // rows, K = the 16 slots. Lane (g0, q4) accumulates rows 2 q4
+                // (c0, c2) and 2 q4 + 1 (c1, c3).
+                {
+                    const int mi = lane >> 3, ri = lane & 7;
+                    const int r = row0 + 8 * (mi & 1) + ri;
+                    if constexpr (KV8) {
+                        // matrix mi: slots 8 (mi & 1) .. +7, byte chunk
+                        // 2 bp + (mi >> 1); each lane gets bytes (s, d), (s, d+1),
+                        // (s+1, d), (s+1, d+1), d = 16 chunk + 2 g0, s = 2 q4, and
+                        // one byte permute splits them into the (s, s+1) pairs of
+                        // dim d (A rows 0-7) and dim d + 1 (A rows 8-15)
 #pragma unroll
-                    for (int bp = 0; bp < 4; ++bp) {
-                        uint32_t vb[4];
-                        ldsm_x4_t(vbase + swz(r, 2 * bp + (mi >> 1)), vb);
-                        uint32_t ev[4], od[4];
+                        for (int bp = 0; bp < 4; ++bp) {
+                            uint32_t vb[4];
+                            ldsm_x4_t(vbase + swz(r, 2 * bp + (mi >> 1)), vb);
 #pragma unroll
-                        for (int mm = 0; mm < 4; ++mm)
-                            e4m3x4_to_f16(__byte_perm(vb[mm], 0u, 0x3120u), ev[mm], od[mm]);
+                            for (int hb = 0; hb < 2; ++hb) {   // chunk 2 bp + hb
+                                uint32_t e0, o0, e1, o1;
+                                e4m3x4_to_f16(__byte_perm(vb[2 * hb], 0u, 0x3120u), e0, o0);       // slots 0-7
+                                e4m3x4_to_f16(__byte_perm(vb[2 * hb + 1], 0u, 0x3120u), e1, o1);   // slots 8-15
+                                mma_f16(acc_o[2 * bp + hb], e0, o0, e1, o1, pb0, pb1);
+                            }
+                        }
+                    } else {
+                        // matrix mi: slots 8 (mi & 1) .. +7, dims 16 mt + 8 (mi >> 1) .. +7
 #pragma unroll
-                        for (int hb = 0; hb < 2; ++hb) {   // block 2 bp + hb: matrices 2 hb (slots 0-7), 2 hb + 1
-                            const int blk = 2 * bp + hb;
-                            mma_f16(acc_o[2 * blk], pa[0], pa[1], pa[2], pa[3], ev[2 * hb], ev[2 * hb + 1]);
-                            mma_f16(acc_o[2 * blk + 1], pa[0], pa[1], pa[2], pa[3], od[2 * hb], od[2 * hb + 1]);
+                        for (int mt = 0; mt < 8; ++mt) {
+                            const int c = 2 * mt + (mi >> 1);
+                            uint32_t vb[4];
+                            ldsm_x4_t(vbase + (c >> 3) * kHalfBytes + swz(r, c & 7), vb);
+                            mma_bf16(acc_o[mt], vb[0], vb[2], vb[1], vb[3], pb0, pb1);
+                            mma_bf16(acc_o[mt], vb[0], vb[2], vb[1], vb[3], pl0, pl1);   // the remainders
                         }
                     }
-                }
-#pragma unroll
-                for (int np = 0; np < (KV8 ? 0 : 8); ++np) {
-                    const int c = 2 * np + (mi >> 1);
-                    uint32_t vb[4];
-                    ldsm_x4_t(vbase + (c >> 3) * kHalfBytes + swz(r, c & 7), vb);
-                    mma_bf16(acc_o[2 * np], pa[0], pa[1], pa[2], pa[3], vb[0], vb[1]);
-                    mma_bf16(acc_o[2 * np + 1], pa[0], pa[1], pa[2], pa[3], vb[2], vb[3]);
                 }
             }
             if (partial)
@@ -935,13 +1050,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const bool range_done = (cur.g + 1 == cur.end);
         if (unit_done || range_done) {
             // ---- merge the four warps' states and emit
-            float l_tot = l_run;
-            l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 1);
-            l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 2);
-            float l_tot1 = l_run1;
-            l_tot1 += __shfl_xor_sync(0xffffffffu, l_tot1, 1);
-            l_tot1 += __shfl_xor_sync(0xffffffffu, l_tot1, 2);
             if constexpr (MULTI) {   // rows g0 and g0 + 8, each its own query row
+                float l_tot = l_run;
+                l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 1);
+                l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 2);
+                float l_tot1 = l_run1;
+                l_tot1 += __shfl_xor_sync(0xffffffffu, l_tot1, 1);
+                l_tot1 += __shfl_xor_sync(0xffffffffu, l_tot1, 2);
                 if (q4 == 0) {
                     sh.m[warp][g0] = m_run;
                     sh.l[warp][g0] = l_tot;
@@ -949,8 +1064,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     sh.l[warp][g0 + 8] = l_tot1;
                 }
 #pragma unroll
-                for (int n = 0; n < 16; ++n) {
-                    if constexpr (KV8) {   // interleaved dims (as below), times the V scale
+                for (int n = 0; n < kOT; ++n) {
+                    if constexpr (KV8) {
+                        // n-tile n = 2 blk + parity holds dims 16 blk + 4 q4 +
+                        // parity (+2); times the V scale
                         const int d = 16 * (n >> 1) + 4 * q4 + (n & 1);
                         sh.o[warp][g0][d] = acc_o[n][0] * vsc;
                         sh.o[warp][g0][d + 2] = acc_o[n][1] * vsc;
@@ -963,22 +1080,49 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                             make_float2(acc_o[n][2], acc_o[n][3]);
                     }
                 }
-            } else if (g0 < G) {
-                if (q4 == 0) {
-                    sh.m[warp][g0] = m_run;
-                    sh.l[warp][g0] = l_tot;
+            } else {
+                // rows 2 q4 and 2 q4 + 1; the eight lanes sharing q4 hold
+                // different slots of them
+                float l_tot = l_run, l_tot1 = l_run1;
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    l_tot += __shfl_xor_sync(0xffffffffu, l_tot, off);
+                    l_tot1 += __shfl_xor_sync(0xffffffffu, l_tot1, off);
+                }
+                const int r0 = 2 * q4, r1 = r0 + 1;
+                if (g0 == 0) {
+                    if (r0 < G) {
+                        sh.m[warp][r0] = m_run;
+                        sh.l[warp][r0] = l_tot;
+                    }
+                    if (r1 < G) {
+                        sh.m[warp][r1] = m_run1;
+                        sh.l[warp][r1] = l_tot1;
+                    }
                 }
 #pragma unroll
-                for (int n = 0; n < 16; ++n) {
-                    const float2 o = make_float2(acc_o[n][0] + acc_o[n][2], acc_o[n][1] + acc_o[n][3]);
+                for (int n = 0; n < kOT; ++n) {
                     if constexpr (KV8) {
-                        // n-tile n = 2 blk + parity holds dims 16 blk + 2 c +
-                        // parity for its columns c; times the V scale
-                        const int d = 16 * (n >> 1) + 4 * q4 + (n & 1);
-                        sh.o[warp][g0][d] = o.x * vsc;
-                        sh.o[warp][g0][d + 2] = o.y * vsc;
+                        // m-tile n: dims 16 n + 2 g0 (c0, c1) and + 1 (c2, c3);
+                        // times the V scale
+                        const int d = 16 * n + 2 * g0;
+                        if (r0 < G)
+                            *reinterpret_cast<float2 *>(&sh.o[warp][r0][d]) =
+                                make_float2(acc_o[n][0] * vsc, acc_o[n][2] * vsc);
+                        if (r1 < G)
+                            *reinterpret_cast<float2 *>(&sh.o[warp][r1][d]) =
+                                make_float2(acc_o[n][1] * vsc, acc_o[n][3] * vsc);
                     } else {
-                        *reinterpret_cast<float2 *>(&sh.o[warp][g0][8 * n + 2 * q4]) = o;
+                        // m-tile n: dims 16 n + g0 (c0, c1) and + 8 (c2, c3)
+                        const int d = 16 * n + g0;
+                        if (r0 < G) {
+                            sh.o[warp][r0][d] = acc_o[n][0];
+                            sh.o[warp][r0][d + 8] = acc_o[n][2];
+                        }
+                        if (r1 < G) {
+                            sh.o[warp][r1][d] = acc_o[n][1];
+                            sh.o[warp][r1][d + 8] = acc_o[n][3];
+                        }
                     }
                 }
             }
@@ -1005,6 +1149,12 @@ cudaError_t launch_q(const DecodeParams &p, const TcMaps &maps, cudaStream_t st)
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(tc_decode_kernel<QF32, WIN, MULTI, KV8>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem);
+        if (e != cudaSuccess)
+            return e;
+        // all of the unified L1 / shared memory as shared memory, so the
+        // intended CTAs per SM fit
+        e = cudaFuncSetAttribute(tc_decode_kernel<QF32, WIN, MULTI, KV8>,
+                                 cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess)
             return e;
         attr_set = true;
