@@ -49,7 +49,7 @@ int pick_kernel(const gqa_options *opt, gqa_dtype dt, int D, int G, bool paged, 
 
 // Persistent grid: every SM holds as many CTAs as fit at once (cached per
 // device and kernel instantiation).
-int grid_for(int kernel, const gqa_options *opt, gqa_dtype dt, int D, int G, bool multi = false)
+int grid_for(int kernel, const gqa_options *opt, gqa_dtype dt, int D, int G)
 {
     if (opt && opt->grid_ctas > 0)
         return opt->grid_ctas;
@@ -58,7 +58,7 @@ int grid_for(int kernel, const gqa_options *opt, gqa_dtype dt, int D, int G, boo
         return 0;
     const int sms = sm_count(dev);
     if (kernel == GQA_KERNEL_TC)
-        return sms * tc_ctas_per_sm(dt == GQA_DTYPE_E4M3, multi);
+        return sms * tc_ctas_per_sm(dt == GQA_DTYPE_E4M3, G);   // G: query rows of a unit
     static std::mutex mu;
     static int cache[kMaxDevices][2][9][9] = {};
     int dlog = 0;
@@ -263,7 +263,7 @@ gqa_status run_step(const Shape &s, const void *q, const void *k_new, const void
     const MultiCut cut = s.multi ? multi_cut(Gh, s.max_q, kernel == GQA_KERNEL_TC ? 16 : 8) : MultiCut{1, 1};
     const int G = Gh * cut.tpc;             // query rows of a unit
     const int Bv = s.B * cut.chunks;        // (virtual) rows of the schedule
-    const int grid = grid_for(kernel, opt, s.dt, s.D, G, s.multi);
+    const int grid = grid_for(kernel, opt, s.dt, s.D, G);
     if (grid <= 0)
         return GQA_ERR_CUDA;
     const WorkspaceLayout lay = workspace_layout(Bv, s.Hkv, G, s.D, grid);
@@ -518,7 +518,7 @@ size_t gqa_workspace_bytes_multi(int B, int Hq, int Hkv, int D, gqa_dtype dt, in
             continue;
         const MultiCut cut = multi_cut(Gh, max_q_len, k == GQA_KERNEL_TC ? 16 : 8);
         const int G = Gh * cut.tpc;
-        const int grid = grid_for(k, &o, dt, D, G, true);
+        const int grid = grid_for(k, &o, dt, D, G);
         if (grid <= 0)
             continue;
         const size_t b = workspace_layout(B * cut.chunks, Hkv, G, D, grid).bytes;

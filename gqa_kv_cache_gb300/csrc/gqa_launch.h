@@ -20,7 +20,7 @@ struct TcMaps {
 };
 bool tc_supports(bool bf16, int D, int G, bool paged, int block_size);  // bf16: the cache
 int tc_tile();
-int tc_ctas_per_sm(bool kv8, bool multi);   // resident CTAs per SM of the instantiation
+int tc_ctas_per_sm(bool kv8, int unit_rows);   // resident CTAs per SM of the instantiation
 cudaError_t tc_launch(const DecodeParams &p, const TcMaps &maps, cudaStream_t st);
 
 // Content validation (gqa_validate.cu). *d_result must be zero on entry; the

@@ -20,7 +20,7 @@ bool tc_supports(bool bf16, int D, int G, bool paged, int block_size)
 }
 
 int tc_tile() { return kTile; }
-int tc_ctas_per_sm(bool kv8, bool multi) { return (kv8 && !multi) ? kCtasPerSmKV8 : kCtasPerSm; }
+int tc_ctas_per_sm(bool kv8, int unit_rows) { return (kv8 && unit_rows <= kGMax) ? kCtasPerSmKV8 : kCtasPerSm; }
 
 cudaError_t tc_launch(const DecodeParams &p, const TcMaps &maps, cudaStream_t st)
 {

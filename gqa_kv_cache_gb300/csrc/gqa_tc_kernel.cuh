@@ -52,14 +52,16 @@
 //    its smaller stages the single-token E4M3 kernel runs three CTAs per SM
 //    (2-stage rings, at most 128 registers a thread).
 //  * multi-token steps (MULTI): a unit is a chunk of up to 16 / G tokens of a
-//    row; its query rows are (token, head) pairs, up to 16 distinct rows, so
-//    these units keep the heads on the M = 16 side (S = Q K^T, O += P V, the
-//    score fragment reused as the A fragment of P; P in plain bf16, f16 over
-//    an E4M3 cache), gathered by one bulk copy per token; each row is masked
+//    row; its query rows are (token, head) pairs, gathered by one bulk copy
+//    per token. Units of up to 8 rows take the products above (rows on the
+//    N = 8 side); units of 9 to 16 rows (M16) keep the rows on the M = 16 side
+//    (S = Q K^T, O += P V, the score fragment reused as the A fragment of P;
+//    P in plain bf16, f16 over an E4M3 cache). Each row is masked
 //    beyond its own token's position and keeps its own softmax state, every
 //    slot holding a new token is substituted from k_new / v_new as below
 //    (quantised over an E4M3 cache), and the chunk appends its own tokens.
-//    With 16 query rows the E4M3 ring takes 3 stages (two CTAs per SM).
+//    With 16 query rows the E4M3 ring takes 3 stages (two CTAs per SM); with
+//    up to 8, the E4M3 kernel runs three CTAs per SM as for single tokens.
 //  * the new token (decode step only; the read-only attend reads slot L from
 //    the cache like any other): in the tile that holds slot L the owning warp writes
 //    k_new / v_new into the ring slot of row L (the TMA copy of the stale
@@ -108,17 +110,18 @@ constexpr long long kWaitCycles = 4LL << 30;          // ~2 s at 2 GHz
 
 // Ring geometry for a bfloat16 (QF32 = false) or float32 query over a
 // bfloat16 or E4M3 (KV8) cache.
-template <bool QF32, bool KV8 = false, bool MULTI = false>
+template <bool QF32, bool KV8 = false, bool MULTI = false, bool M16 = false>
 struct Ring {
+    static constexpr bool kMside = MULTI && M16;   // units of up to 16 query rows
     static constexpr int kQElem = QF32 ? 4 : 2;
-    static constexpr int kQRows = MULTI ? 2 * kGMax : kGMax;         // query rows of a unit
+    static constexpr int kQRows = kMside ? 2 * kGMax : kGMax;        // query rows of a unit
     static constexpr int kQBytes = kQRows * kD * kQElem;             // the unit's query rows
     static constexpr int kKVBytes = KV8 ? kTile * kD : 2 * kHalfBytes; // K (or V) of one tile
     static constexpr int kStageBytes = 2 * kKVBytes + kQBytes;       // K (lo, hi), V (lo, hi), Q
     // E4M3: 4 stages at two CTAs per SM, 2 at three; 3 with the 16 query
-    // rows of a multi-token unit, so two CTAs still share an SM
-    static constexpr int kNumStages = KV8 ? (MULTI ? 3 : (kCtasPerSmKV8 >= 3 ? 2 : 4)) : kStages;
-    static constexpr int kCtas = (KV8 && !MULTI) ? kCtasPerSmKV8 : kCtasPerSm;   // resident CTAs per SM
+    // rows of a 16-row multi-token unit, so two CTAs still share an SM
+    static constexpr int kNumStages = KV8 ? (kMside ? 3 : (kCtasPerSmKV8 >= 3 ? 2 : 4)) : kStages;
+    static constexpr int kCtas = (KV8 && !kMside) ? kCtasPerSmKV8 : kCtasPerSm;   // resident CTAs per SM
     static constexpr int kDynSmem = kNumStages * kStageBytes + 1024;
     static_assert(kStageBytes % 1024 == 0, "stages must stay 1024-byte aligned for the swizzle");
 };
@@ -313,15 +316,19 @@ __device__ __forceinline__ void consumer_sync()
 // WIN: a sliding window is in force. Without one the window fields of the
 // cursor are never read, so they take no registers and no code. MULTI: a
 // multi-token step (the chunk fields of the cursor are read only then). KV8:
-// an E4M3 cache.
-template <bool QF32, bool WIN, bool MULTI, bool KV8>
-__global__ void __launch_bounds__(kThreads, (Ring<QF32, KV8, MULTI>::kCtas))
+// an E4M3 cache. M16: multi-token units of 9 to 16 query rows, which keep the
+// rows on the M = 16 side of the products; units of up to 8 rows (and every
+// single-token unit) put them on the N = 8 side.
+template <bool QF32, bool WIN, bool MULTI, bool KV8, bool M16>
+__global__ void __launch_bounds__(kThreads, (Ring<QF32, KV8, MULTI, M16>::kCtas))
     tc_decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap mk,
                      const __grid_constant__ CUtensorMap mv)
 {
-    using RG = Ring<QF32, KV8, MULTI>;
+    using RG = Ring<QF32, KV8, MULTI, M16>;
     static_assert(!(MULTI && QF32), "multi-token steps take a bfloat16 query");
-    constexpr int kRW = MULTI ? 2 * kGMax : kGMax;   // query rows of a unit
+    static_assert(MULTI || !M16, "16-row units are multi-token units");
+    constexpr bool kMside = RG::kMside;              // query rows on the M = 16 side
+    constexpr int kRW = kMside ? 2 * kGMax : kGMax;  // query rows of a unit
     constexpr int kStageBytes = RG::kStageBytes;
     constexpr int kNS = RG::kNumStages;   // ring depth
     constexpr int kKVB = RG::kKVBytes;    // K (or V) bytes of one tile
@@ -506,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, (Ring<QF32, KV8, MULTI>::kCtas))
     uint32_t ql[8][2];
     // O: multi-token units, 16 n-tiles of 8 dims for rows g0 and g0 + 8;
     // single-token units, O^T in 8 m-tiles of 16 dims for rows 2 q4, 2 q4 + 1
-    constexpr int kOT = MULTI ? 16 : 8;
+    constexpr int kOT = kMside ? 16 : 8;
     float acc_o[kOT][4];
     float m_run = -INFINITY, l_run = 0.f;
     int seg_first_t = 0;
@@ -535,9 +542,13 @@ __global__ void __launch_bounds__(kThreads, (Ring<QF32, KV8, MULTI>::kCtas))
             seg_bad = 0;
             seg_start = false;
             if constexpr (MULTI) {
-                lim = L - (cur.nq - 1 - g0 / p.Gh);          // row g0 is token g0 / Gh of the chunk
-                lim1 = L - (cur.nq - 1 - (g0 + 8) / p.Gh);   // row g0 + 8
+                // this lane's two query rows (g0 and g0 + 8 on the M side, else
+                // 2 q4 and 2 q4 + 1); row r is token r / Gh of the chunk and
+                // attends up to its own position; rows without a token none
+                const int ra = kMside ? g0 : 2 * q4, rb = kMside ? g0 + 8 : 2 * q4 + 1;
                 qrows = p.Gh * cur.nq;
+                lim = ra < qrows ? L - (cur.nq - 1 - ra / p.Gh) : -1;
+                lim1 = rb < qrows ? L - (cur.nq - 1 - rb / p.Gh) : -1;
                 if constexpr (WIN) {
                     lo_r = max(0, lim - p.window + 1);
                     lo_r1 = max(0, lim1 - p.window + 1);
@@ -607,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, (Ring<QF32, KV8, MULTI>::kCtas))
                         qa[ks][0] = pack_f16(bf16_lo(w0), bf16_hi(w0));
                         qa[ks][1] = pack_f16(bf16_lo(w1), bf16_hi(w1));
                     }
-                    if constexpr (MULTI) {
+                    if constexpr (kMside) {
                         ql[ks][0] = ql[ks][1] = 0u;
                         if (g0 + 8 < nrow) {
                             const uint8_t *qs1 = qs + 8 * (kD * 2);
@@ -626,7 +637,7 @@ __global__ void __launch_bounds__(kThreads, (Ring<QF32, KV8, MULTI>::kCtas))
                     const bool on = g0 < (MULTI ? qrows : G);
                     qa[ks][0] = on ? *reinterpret_cast<const uint32_t *>(qs + (16 * ks + 2 * q4) * 2) : 0u;
                     qa[ks][1] = on ? *reinterpret_cast<const uint32_t *>(qs + (16 * ks + 8 + 2 * q4) * 2) : 0u;
-                    if constexpr (MULTI) {   // row g0 + 8: a query row of its own
+                    if constexpr (kMside) {   // row g0 + 8: a query row of its own
                         const bool on1 = g0 + 8 < qrows;
                         const uint8_t *qs1 = qs + 8 * (kD * 2);
                         ql[ks][0] = on1 ? *reinterpret_cast<const uint32_t *>(qs1 + (16 * ks + 2 * q4) * 2) : 0u;
@@ -748,7 +759,7 @@ __global__ void __launch_bounds__(kThreads, (Ring<QF32, KV8, MULTI>::kCtas))
             }
 
 
-            if constexpr (MULTI) {
+            if constexpr (kMside) {
                 // ---- S = Q K^T for this warp's 16 slots (two n-tiles of 8);
                 // rows g0 and g0 + 8 are query rows of their own; even and odd
                 // k-steps accumulate separately (shorter chains)
@@ -940,12 +951,20 @@ __global__ void __launch_bounds__(kThreads, (Ring<QF32, KV8, MULTI>::kCtas))
                 // above its row's running max + 8 (a warp vote).
                 const float sl = KV8 ? ssc : p.scale_log2;
                 const int j0 = slot0 + row0 + g0;
-                const bool on0 = !partial || (WIN ? attended(L, cur.lo, cur.P, j0) : j0 <= L);
-                const bool on1 = !partial || (WIN ? attended(L, cur.lo, cur.P, j0 + 8) : j0 + 8 <= L);
-                const float x00 = on0 ? st[0] * sl : -INFINITY;   // row 2 q4,     slot g0
-                const float x10 = on0 ? st[1] * sl : -INFINITY;   // row 2 q4 + 1, slot g0
-                const float x01 = on1 ? st[2] * sl : -INFINITY;   // row 2 q4,     slot g0 + 8
-                const float x11 = on1 ? st[3] * sl : -INFINITY;   // row 2 q4 + 1, slot g0 + 8
+                bool on00, on01, on10, on11;   // (row 2 q4 + i, slot j0 + 8 k)
+                if constexpr (MULTI) {         // each row its own causal bound and window
+                    on00 = !partial || (WIN ? attended(lim, lo_r, cur.P, j0) : j0 <= lim);
+                    on01 = !partial || (WIN ? attended(lim, lo_r, cur.P, j0 + 8) : j0 + 8 <= lim);
+                    on10 = !partial || (WIN ? attended(lim1, lo_r1, cur.P, j0) : j0 <= lim1);
+                    on11 = !partial || (WIN ? attended(lim1, lo_r1, cur.P, j0 + 8) : j0 + 8 <= lim1);
+                } else {
+                    on00 = on10 = !partial || (WIN ? attended(L, cur.lo, cur.P, j0) : j0 <= L);
+                    on01 = on11 = !partial || (WIN ? attended(L, cur.lo, cur.P, j0 + 8) : j0 + 8 <= L);
+                }
+                const float x00 = on00 ? st[0] * sl : -INFINITY;   // row 2 q4,     slot g0
+                const float x10 = on10 ? st[1] * sl : -INFINITY;   // row 2 q4 + 1, slot g0
+                const float x01 = on01 ? st[2] * sl : -INFINITY;   // row 2 q4,     slot g0 + 8
+                const float x11 = on11 ? st[3] * sl : -INFINITY;   // row 2 q4 + 1, slot g0 + 8
                 float mx0 = fmaxf(x00, x01), mx1 = fmaxf(x10, x11);
                 if (__any_sync(0xffffffffu, mx0 > m_run + 8.f || mx1 > m_run1 + 8.f)) {
 #pragma unroll
@@ -1050,7 +1069,7 @@ __global__ void __launch_bounds__(kThreads, (Ring<QF32, KV8, MULTI>::kCtas))
         const bool range_done = (cur.g + 1 == cur.end);
         if (unit_done || range_done) {
             // ---- merge the four warps' states and emit
-            if constexpr (MULTI) {   // rows g0 and g0 + 8, each its own query row
+            if constexpr (kMside) {   // rows g0 and g0 + 8, each its own query row
                 float l_tot = l_run;
                 l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 1);
                 l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 2);
@@ -1141,19 +1160,19 @@ __global__ void __launch_bounds__(kThreads, (Ring<QF32, KV8, MULTI>::kCtas))
 }
 
 
-template <bool QF32, bool WIN, bool MULTI, bool KV8 = false>
+template <bool QF32, bool WIN, bool MULTI, bool KV8 = false, bool M16 = false>
 cudaError_t launch_q(const DecodeParams &p, const TcMaps &maps, cudaStream_t st)
 {
-    constexpr int kDynSmem = Ring<QF32, KV8, MULTI>::kDynSmem;
+    constexpr int kDynSmem = Ring<QF32, KV8, MULTI, M16>::kDynSmem;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(tc_decode_kernel<QF32, WIN, MULTI, KV8>,
+        cudaError_t e = cudaFuncSetAttribute(tc_decode_kernel<QF32, WIN, MULTI, KV8, M16>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem);
         if (e != cudaSuccess)
             return e;
         // all of the unified L1 / shared memory as shared memory, so the
         // intended CTAs per SM fit
-        e = cudaFuncSetAttribute(tc_decode_kernel<QF32, WIN, MULTI, KV8>,
+        e = cudaFuncSetAttribute(tc_decode_kernel<QF32, WIN, MULTI, KV8, M16>,
                                  cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess)
             return e;
@@ -1169,7 +1188,7 @@ cudaError_t launch_q(const DecodeParams &p, const TcMaps &maps, cudaStream_t st)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tc_decode_kernel<QF32, WIN, MULTI, KV8>, p, maps.k, maps.v);
+    return cudaLaunchKernelEx(&cfg, tc_decode_kernel<QF32, WIN, MULTI, KV8, M16>, p, maps.k, maps.v);
 }
 
 }  // namespace

@@ -8,10 +8,20 @@ cudaError_t tc_launch_multi(const DecodeParams &p, const TcMaps &maps, cudaStrea
 {
     if (!p.q_bf16)
         return cudaErrorInvalidValue;
+    const bool win = p.window > 0;
+    // units of more than 8 query rows keep the rows on the M = 16 side
+    if (p.G > 8) {
+        if (p.kv8)
+            return win ? launch_q<false, true, true, true, true>(p, maps, st)
+                       : launch_q<false, false, true, true, true>(p, maps, st);
+        return win ? launch_q<false, true, true, false, true>(p, maps, st)
+                   : launch_q<false, false, true, false, true>(p, maps, st);
+    }
     if (p.kv8)
-        return p.window > 0 ? launch_q<false, true, true, true>(p, maps, st)
-                            : launch_q<false, false, true, true>(p, maps, st);
-    return p.window > 0 ? launch_q<false, true, true>(p, maps, st) : launch_q<false, false, true>(p, maps, st);
+        return win ? launch_q<false, true, true, true, false>(p, maps, st)
+                   : launch_q<false, false, true, true, false>(p, maps, st);
+    return win ? launch_q<false, true, true, false, false>(p, maps, st)
+               : launch_q<false, false, true, false, false>(p, maps, st);
 }
 
 }  // namespace gqa

@@ -101,6 +101,16 @@ CASES = [
     ("g4_rows16", "llama3_8b", dict(B=3, Smax=400, len_lo=0, len_hi=390, seed=413), [4, 8, 3]),
     ("g2_rows16", "llama3_8b", dict(Hq=4, Hkv=2, B=2, Smax=300, len_lo=0, len_hi=290, seed=414), [8, 16]),
     ("g1_rows16", "llama3_8b", dict(Hq=2, Hkv=2, B=2, Smax=300, len_lo=0, len_hi=280, seed=415), [16, 5]),
+    # units of at most 8 query rows (one chunk): on the tensor cores the rows
+    # sit on the N = 8 side of the products
+    ("g4_rows8", "llama3_8b", dict(B=5, Smax=400, len_lo=0, len_hi=390, seed=417), [2, 1, 0, 2, 2]),
+    ("g2_rows8", "llama3_8b", dict(Hq=4, Hkv=2, B=3, Smax=300, len_lo=0, len_hi=290, seed=418), [4, 3, 1]),
+    ("g1_rows8", "llama3_8b", dict(Hq=2, Hkv=2, B=3, Smax=300, len_lo=0, len_hi=290, seed=419), [8, 5, 3]),
+    ("g8_rows8", "long_context", dict(B=4, Smax=400, len_lo=50, len_hi=390, seed=420), [1, 1, 0, 1]),
+    ("g6_rows6_paged16", "paged", dict(B=4, num_blocks=4 * 30, max_blocks=30, len_lo=0, len_hi=470, seed=421),
+     [1, 1, 1, 0]),
+    ("g4_rows8_paged8", "paged", dict(Hq=8, Hkv=2, B=3, block_size=8, num_blocks=3 * 40, max_blocks=40,
+                                      len_lo=0, len_hi=310, seed=422), [2, 2, 1]),
 ]
 
 
@@ -125,26 +135,27 @@ def test_multi_fp8_small_cases(name, base, kw, q_lens, grid):
     check_multi(W.small(base, **kw), q_lens, "tc", grid, fp8=True)
 
 
-def test_multi_fp8_window_sink():
+@pytest.mark.parametrize("q_lens", [[3, 4, 1, 2], [2, 2, 1, 2]], ids=["rows16", "rows8"])
+def test_multi_fp8_window_sink(q_lens):
     w = W.small("llama3_8b", B=4, Smax=500, len_lo=100, len_hi=490, seed=416)
     g = torch.Generator().manual_seed(4)
-    check_multi(w, [3, 4, 1, 2], "tc", 0, fp8=True, window=70, kept_prefix=9,
+    check_multi(w, q_lens, "tc", 0, fp8=True, window=70, kept_prefix=9,
                 sink=(torch.randn(w.Hq, generator=g)).cuda())
 
 
+@pytest.mark.parametrize("q_lens", [[3, 4, 1, 2], [2, 2, 1, 2]], ids=["rows16", "rows8"])
 @pytest.mark.parametrize("kernel", ["simt", "tc"])
-def test_multi_with_window_and_sink(kernel):
+def test_multi_with_window_and_sink(kernel, q_lens):
     w = W.small("llama3_8b", B=4, Smax=500, len_lo=100, len_hi=490, seed=410)
     g = torch.Generator().manual_seed(3)
-    check_multi(w, [3, 4, 1, 2], kernel, 0, window=70, kept_prefix=9,
+    check_multi(w, q_lens, kernel, 0, window=70, kept_prefix=9,
                 sink=(torch.randn(w.Hq, generator=g)).cuda())
 
 
 @pytest.mark.parametrize("kernel", ["simt", "tc"])
 def test_multi_q_len_one_matches_decode_step(kernel):
     """q_len = 1 everywhere is the decode step: the same appended bytes and
-    outputs within the bf16 bar (a multi-token tensor-core unit takes P in
-    plain bf16, the decode step splits it into bf16 + remainder)."""
+    outputs within the bf16 bar."""
     import gqa_kv_cache_gb300 as gqa
     w = W.small("llama3_8b", B=5, Smax=600, len_lo=0, len_hi=590, seed=411)
     t = {k: v.cuda() for k, v in W.generate(w, q_lens=[1] * w.B).items()}
