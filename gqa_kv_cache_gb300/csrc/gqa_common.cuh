@@ -275,10 +275,20 @@ __device__ __forceinline__ long long working_ctas(long long N, int grid)
     return N < grid ? N : (long long)grid;
 }
 
+// floor(a / c) for 0 <= a, 0 < c: a 32-bit division when both fit (the
+// usual case; a 64-bit one is a long software sequence on the start and end
+// paths of the kernels).
+__device__ __forceinline__ long long div_floor(long long a, long long c)
+{
+    if (((unsigned long long)a | (unsigned long long)c) < (1ull << 32))
+        return (long long)((unsigned)a / (unsigned)c);
+    return a / c;
+}
+
 // CTA that owns global tile x: the largest i with floor(i N / C) <= x.
 __device__ __forceinline__ int cta_of_tile(long long x, long long N, long long C)
 {
-    return (int)(((x + 1) * C - 1) / N);
+    return (int)div_floor((x + 1) * C - 1, N);
 }
 
 __device__ __forceinline__ void report(const DecodeParams &p, int bits)
@@ -335,8 +345,8 @@ __device__ __forceinline__ TileCursor cursor_at(const DecodeParams &p, int b, lo
     set_row(p, c);
     const int nt = c.nr + p.pad_tiles;   // cursor_at is only used on rows with tiles
     const long long within = g - run;
-    c.kvh = (int)(within / nt);
-    c.t = (int)(within % nt);
+    c.kvh = (int)div_floor(within, nt);
+    c.t = (int)(within - (long long)c.kvh * nt);
     return c;
 }
 
@@ -356,16 +366,22 @@ struct TileWalk {
 // `scratch`, >= blockDim.x / 32 + 8 long longs of shared memory; blockDim.x a
 // multiple of 32). The row prefix is a block-wide scan of the per-row tile
 // counts, recomputed by every CTA from `lengths` (no host round trip). The
-// walk is written to `out` (shared memory), visible to all threads on return.
+// threads whose rows hold the CTA's first and last tiles build those two
+// cursors (in `out`), and thread 0 then orders them into the walk: the start
+// of the kernel is a chain of dependent steps, kept short. The walk is
+// visible to all threads on return.
 __device__ inline void schedule_walk(const DecodeParams &p, long long *scratch, TileWalk *out)
 {
     const int nthr = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nwarps = nthr >> 5;
     const int chunk = (p.B + nthr - 1) / nthr;
     const int r0 = min(p.B, tid * chunk), r1 = min(p.B, r0 + chunk);
-    long long local = 0;
-    for (int b = r0; b < r1; ++b)
-        local += (long long)p.Hkv * row_tiles(p, b);
+    long long local = 0, n0 = 0;        // tiles of this thread's rows, of its first row
+    for (int b = r0; b < r1; ++b) {
+        const long long n = (long long)p.Hkv * row_tiles(p, b);
+        n0 = (b == r0) ? n : n0;
+        local += n;
+    }
     // inclusive scan: within the warp by shuffles, then over the warp totals
     long long incl = local;
 #pragma unroll
@@ -375,11 +391,8 @@ __device__ inline void schedule_walk(const DecodeParams &p, long long *scratch, 
             incl += v;
     }
     long long *wsum = scratch;              // [nwarps]
-    long long *found = scratch + nwarps;    // row of begin, its run; row of end-1, its run
     if (lane == 31)
         wsum[warp] = incl;
-    if (tid == 0)
-        found[0] = found[1] = found[2] = found[3] = 0;
     __syncthreads();
     long long before = 0, N = 0;
     for (int w = 0; w < nwarps; ++w) {
@@ -390,21 +403,19 @@ __device__ inline void schedule_walk(const DecodeParams &p, long long *scratch, 
     incl += before;
     const long long excl = incl - local;
     const long long C = working_ctas(N, p.grid);
-    const long long begin = blockIdx.x < C ? (long long)blockIdx.x * N / C : N;
-    const long long end = blockIdx.x < C ? ((long long)blockIdx.x + 1) * N / C : N;
+    const long long begin = blockIdx.x < C ? div_floor((long long)blockIdx.x * N, C) : N;
+    const long long end = blockIdx.x < C ? div_floor(((long long)blockIdx.x + 1) * N, C) : N;
     const long long last = end - 1;
     if (begin < end && ((begin >= excl && begin < incl) || (last >= excl && last < incl))) {
+        // this thread's rows hold the first tile (cursor -> out->b) and/or the
+        // last one (-> out->a)
         long long run = excl;
         for (int b = r0; b < r1; ++b) {
-            const long long n = (long long)p.Hkv * row_tiles(p, b);
-            if (begin >= run && begin < run + n) {
-                found[0] = b;
-                found[1] = run;
-            }
-            if (last >= run && last < run + n) {
-                found[2] = b;
-                found[3] = run;
-            }
+            const long long n = (b == r0) ? n0 : (long long)p.Hkv * row_tiles(p, b);
+            if (begin >= run && begin < run + n)
+                out->b = cursor_at(p, b, run, begin, end);
+            if (last >= run && last < run + n)
+                out->a = cursor_at(p, b, run, last, end);
             run += n;
         }
     }
@@ -418,12 +429,12 @@ __device__ inline void schedule_walk(const DecodeParams &p, long long *scratch, 
             none.g = none.end = N;
             none.b = none.kvh = none.t = none.L = 0;
             none.lo = none.P = none.tp = none.gap = 0;
-        none.nq = none.tokL = none.Lb = 0;
+            none.nq = none.tokL = none.Lb = 0;
             none.nr = 1;
             w.a = w.b = none;
         } else {
-            const TileCursor first = cursor_at(p, (int)found[0], found[1], begin, end);
-            const TileCursor tail = cursor_at(p, (int)found[2], found[3], last, end);
+            const TileCursor first = w.b;
+            const TileCursor tail = w.a;
             const long long unit_start = last - tail.t;
             if (unit_start <= begin) {        // a single segment: walk it in order
                 w.a = first;
@@ -614,12 +625,16 @@ __device__ __forceinline__ float *out_row(const DecodeParams &p, const TileCurso
 }
 
 // MULTI: the unit may be a chunk of a multi-token step (any form then works).
+// pre_cnt (thread 0 only): the unit's arrival count read with acquire
+// semantics shortly before the segment's end, or -1. When it already shows
+// every other piece of the unit arrived, this CTA is the last arriver: it
+// skips the ticket's round trip and merges at once.
 template <int NW, int GP, int DD, int DP, bool MULTI, class Sync, int GR, int KM>
 __device__ inline void finish_segment(const DecodeParams &p, const TileCursor &cur, const TileWalk &walk,
                                       int seg_first_t,
                                       bool bad, const float (&sm_m)[NW][GP], const float (&sm_l)[NW][GP],
                                       const float (&sm_o)[NW][GP][DP], int *sm_flag, MergeBufT<GR, KM> &mb,
-                                      int tid, int nthr, Sync sync)
+                                      int tid, int nthr, Sync sync, int pre_cnt = -1)
 {
     static_assert(NW <= kMergeW && GP <= GR && DP >= DD, "merge buffer too small");
     const int G = p.G, b = cur.b, kvh = cur.kvh;
@@ -709,8 +724,9 @@ __device__ inline void finish_segment(const DecodeParams &p, const TileCursor &c
     const int first = cta_of_tile(first_tile, walk.N, walk.C);
     const int last = cta_of_tile(first_tile + cur.nr - 1, walk.N, walk.C);
     if (tid == 0) {
-        int old;
-        asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(p.ws_cnt + u) : "memory");
+        int old = pre_cnt;
+        if (old != last - first)
+            asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(p.ws_cnt + u) : "memory");
         *sm_flag = (old == last - first);
     }
     sync();

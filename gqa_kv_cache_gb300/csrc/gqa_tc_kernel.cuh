@@ -517,6 +517,7 @@ __global__ void __launch_bounds__(kThreads, (Ring<QF32, KV8, MULTI, M16>::kCtas)
     float acc_o[kOT][4];
     float m_run = -INFINITY, l_run = 0.f;
     int seg_first_t = 0;
+    int pre_cnt = -1;                    // thread 0: the unit's arrival count near the segment's end
     bool seg_start = true, row_good = true, aborted = false;
     int seg_bad = 0;
     // multi-token units only: this lane's rows g0 and g0 + 8 (last slot,
@@ -558,7 +559,17 @@ __global__ void __launch_bounds__(kThreads, (Ring<QF32, KV8, MULTI, M16>::kCtas)
                 ssc = p.scale_log2 * __ldg(p.k_scale + kvh);
                 vsc = __ldg(p.v_scale + kvh);
             }
+            pre_cnt = -1;
         }
+        // One tile before the segment ends, thread 0 reads the unit's arrival
+        // count (acquire): if every other piece has arrived by then, the
+        // segment's end needs no ticket (finish_segment). The load's latency
+        // hides behind the last tile.
+        if (tid == 0 && (cur.t == cur.nr - 2 || cur.g + 2 == cur.end))
+            asm volatile("ld.acquire.gpu.global.s32 %0, [%1];"
+                         : "=r"(pre_cnt)
+                         : "l"(p.ws_cnt + (long long)b * p.Hkv + kvh)
+                         : "memory");
 
         // After an abort every warp keeps walking its tiles and taking part in
         // every barrier, but waits for and computes nothing (outputs NaN).
@@ -1152,7 +1163,7 @@ __global__ void __launch_bounds__(kThreads, (Ring<QF32, KV8, MULTI, M16>::kCtas)
             finish_segment<kConsumerWarps, kRW, kD, kD + Shared<kNS, kRW>::kOPad, MULTI>(p, cur, walk, seg_first_t,
                                                                                    bad, sh.m, sh.l, sh.o,
                                                       &sh.last_flag, sh.merge, tid, kConsumerWarps * 32,
-                                                      [] { consumer_sync(); });
+                                                      [] { consumer_sync(); }, pre_cnt);
             seg_start = true;
         }
         more = walk_next(p, cur, walk, in_b);
