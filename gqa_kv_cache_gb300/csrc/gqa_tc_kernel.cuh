@@ -1181,12 +1181,6 @@ cudaError_t launch_q(const DecodeParams &p, const TcMaps &maps, cudaStream_t st)
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem);
         if (e != cudaSuccess)
             return e;
-        // all of the unified L1 / shared memory as shared memory, so the
-        // intended CTAs per SM fit
-        e = cudaFuncSetAttribute(tc_decode_kernel<QF32, WIN, MULTI, KV8, M16>,
-                                 cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
-        if (e != cudaSuccess)
-            return e;
         attr_set = true;
     }
     cudaLaunchConfig_t cfg = {};
