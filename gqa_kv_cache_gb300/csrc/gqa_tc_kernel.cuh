@@ -505,11 +505,11 @@ __global__ void __launch_bounds__(kThreads, (Ring<QF32, KV8, MULTI, M16>::kCtas)
     int stage = 0;
     uint32_t phase = 0;
     // Q fragments of query row g0 (< G), 8 k-steps: the B operand of S^T = K Q^T
-    // (single-token units) or rows 0-7 of the A operand of S = Q K^T
-    // (multi-token units)
+    // (single-token units, multi-token units of up to 8 rows) or rows 0-7 of
+    // the A operand of S = Q K^T (16-row units)
     uint32_t qa[8][2];
     // float32 query: the remainders of row g0 (a second B operand);
-    // multi-token units: query row g0 + 8 (A rows 8-15)
+    // 16-row units: query row g0 + 8 (A rows 8-15)
     uint32_t ql[8][2];
     // O: multi-token units, 16 n-tiles of 8 dims for rows g0 and g0 + 8;
     // single-token units, O^T in 8 m-tiles of 16 dims for rows 2 q4, 2 q4 + 1
