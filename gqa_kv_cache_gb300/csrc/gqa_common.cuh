@@ -362,15 +362,49 @@ struct TileWalk {
     long long N, C;   // tiles in the list, CTAs sharing them
 };
 
+// L2 prefetch of the cached K and V rows of the first n tiles from cursor c
+// (dense and slot-id caches of kv_es bytes per element; paged caches and
+// kv_es = 0: nothing). Rows are clamped to the attended slots and the row's
+// capacity; rows with a bad length or slot id are skipped. A hint only: the
+// kernel's own copies read the same bytes.
+__device__ __forceinline__ void prefetch_tiles(const DecodeParams &p, const TileCursor &c, int n, int kv_es)
+{
+    if (p.paged || kv_es == 0 || c.L < 0)
+        return;
+    int row = real_row(p, c.b);
+    if (p.slot_ids) {
+        row = __ldg(p.slot_ids + row);
+        if (row < 0 || row >= p.R)
+            return;
+    }
+    const int s0 = tile_slot0(c, p.tile);
+    const int s1 = min(min(p.Smax, c.L + 1), s0 + n * p.tile);
+    if (s1 <= s0)
+        return;
+    const size_t rowbytes = (size_t)p.D * kv_es;
+    const size_t off = (((size_t)row * p.Hkv + c.kvh) * p.Smax + s0) * rowbytes;
+    const size_t bytes = (size_t)(s1 - s0) * rowbytes;
+    if ((bytes & 15) || (off & 15) || bytes >= (1u << 31))
+        return;
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(static_cast<const char *>(p.k_cache) + off),
+                 "r"((unsigned)bytes)
+                 : "memory");
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(static_cast<const char *>(p.v_cache) + off),
+                 "r"((unsigned)bytes)
+                 : "memory");
+}
+
 // Every thread of the block must call it (it uses __syncthreads and
 // `scratch`, >= blockDim.x / 32 + 8 long longs of shared memory; blockDim.x a
-// multiple of 32). The row prefix is a block-wide scan of the per-row tile
+// multiple of 32). kv_es > 0: the threads that find the CTA's first tiles
+// also prefetch them into L2 (prefetch_tiles), so HBM starts working before
+// the walk is assembled and the first copies are issued. The row prefix is a block-wide scan of the per-row tile
 // counts, recomputed by every CTA from `lengths` (no host round trip). The
 // threads whose rows hold the CTA's first and last tiles build those two
 // cursors (in `out`), and thread 0 then orders them into the walk: the start
 // of the kernel is a chain of dependent steps, kept short. The walk is
 // visible to all threads on return.
-__device__ inline void schedule_walk(const DecodeParams &p, long long *scratch, TileWalk *out)
+__device__ inline void schedule_walk(const DecodeParams &p, long long *scratch, TileWalk *out, int kv_es = 0)
 {
     const int nthr = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nwarps = nthr >> 5;
@@ -412,10 +446,19 @@ __device__ inline void schedule_walk(const DecodeParams &p, long long *scratch, 
         long long run = excl;
         for (int b = r0; b < r1; ++b) {
             const long long n = (b == r0) ? n0 : (long long)p.Hkv * row_tiles(p, b);
-            if (begin >= run && begin < run + n)
-                out->b = cursor_at(p, b, run, begin, end);
-            if (last >= run && last < run + n)
-                out->a = cursor_at(p, b, run, last, end);
+            if (begin >= run && begin < run + n) {
+                const TileCursor c = cursor_at(p, b, run, begin, end);
+                out->b = c;
+                prefetch_tiles(p, c, 2, kv_es);
+            }
+            if (last >= run && last < run + n) {
+                TileCursor c = cursor_at(p, b, run, last, end);
+                out->a = c;
+                if (last - c.t > begin) {   // range a, walked first, starts at the unit's tile 0
+                    c.t = 0;
+                    prefetch_tiles(p, c, 2, kv_es);
+                }
+            }
             run += n;
         }
     }

@@ -355,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, (Ring<QF32, KV8, MULTI, M16>::kCtas)
     // stream: everything above overlaps its tail; no input is read before it
     // has completed and its memory is visible.
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    schedule_walk(p, sh.sched, &sh.walk);   // contains __syncthreads
+    schedule_walk(p, sh.sched, &sh.walk, KV8 ? 1 : 2);   // contains __syncthreads
     const TileWalk &walk = sh.walk;
 
     const int G = p.G;
