@@ -442,21 +442,23 @@ __device__ inline void schedule_walk(const DecodeParams &p, long long *scratch, 
     const long long last = end - 1;
     if (begin < end && ((begin >= excl && begin < incl) || (last >= excl && last < incl))) {
         // this thread's rows hold the first tile (cursor -> out->b) and/or the
-        // last one (-> out->a)
+        // last one (-> out->a); each range's first 32 KB or so of K and V go
+        // to L2 ahead of the copies (measured: deeper prefetches were slower)
+        const int pf_tiles = kv_es == 1 ? 2 : 1;
         long long run = excl;
         for (int b = r0; b < r1; ++b) {
             const long long n = (b == r0) ? n0 : (long long)p.Hkv * row_tiles(p, b);
             if (begin >= run && begin < run + n) {
                 const TileCursor c = cursor_at(p, b, run, begin, end);
                 out->b = c;
-                prefetch_tiles(p, c, 2, kv_es);
+                prefetch_tiles(p, c, pf_tiles, kv_es);
             }
             if (last >= run && last < run + n) {
                 TileCursor c = cursor_at(p, b, run, last, end);
                 out->a = c;
                 if (last - c.t > begin) {   // range a, walked first, starts at the unit's tile 0
                     c.t = 0;
-                    prefetch_tiles(p, c, 2, kv_es);
+                    prefetch_tiles(p, c, pf_tiles, kv_es);
                 }
             }
             run += n;
