@@ -444,7 +444,7 @@ __device__ inline void schedule_walk(const DecodeParams &p, long long *scratch, 
         // this thread's rows hold the first tile (cursor -> out->b) and/or the
         // last one (-> out->a); each range's first 32 KB or so of K and V go
         // to L2 ahead of the copies (measured: deeper prefetches were slower)
-        const int pf_tiles = kv_es == 1 ? 2 : 1;
+        const int pf_tiles = kv_es == 1 ? 2 : 1;   // E4M3 tiles are half the bytes
         long long run = excl;
         for (int b = r0; b < r1; ++b) {
             const long long n = (b == r0) ? n0 : (long long)p.Hkv * row_tiles(p, b);

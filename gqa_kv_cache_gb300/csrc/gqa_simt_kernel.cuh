@@ -150,7 +150,7 @@ __global__ void __launch_bounds__(kThreads) simt_decode_kernel(const DecodeParam
 
     // programmatic dependent of the previous kernel: read no input before it is done
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    schedule_walk(p, sched, &walk);
+    schedule_walk(p, sched, &walk, (int)sizeof(T));   // also prefetches the first tiles into L2
     TileCursor cur;
     bool in_b = false;
     bool more = walk_first(p, cur, walk, in_b);
