@@ -74,6 +74,8 @@ def parse():
     ap.add_argument("--kv", default="native", choices=["native", "e4m3"],
                     help="cache element type: the workload's own or E4M3 bytes with per-head scales")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clocks-dir", default=None,
+                    help="folder for the raw nvidia-smi samples of the timed region (default: the temp dir)")
     ap.add_argument("--sched-pad", type=int, default=None,
                     help="schedule-only tiles per (row, head); default: the library's")
     ap.add_argument("--l2-flush", default="write_read", choices=["write_read", "write", "none"],
@@ -231,10 +233,12 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, device_index):
+    def __init__(self, device_index, log_dir=None):
         self.dev = device_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{device_index}.csv")
+        # the raw samples stay on disk for inspection (--clocks-dir)
+        import tempfile
+        self.path = os.path.join(log_dir or tempfile.gettempdir(), f"clocks_rank{device_index}.csv")
 
     def start(self):
         try:
@@ -469,7 +473,7 @@ def run_ours(args, ranks):
     # ---- timed region: K steps, L2 flushed between them (outside the events)
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    clocks = ClockSampler(ranks.local)
+    clocks = ClockSampler(ranks.local, args.clocks_dir)
     clocks.start()
     ranks.barrier()
     torch.cuda.synchronize()
