@@ -202,10 +202,12 @@ __device__ __forceinline__ bool geom_ok(const DecodeParams &p, int L, int P)
     return L >= 0 && (long long)L < row_capacity(p) && P >= 0;
 }
 
-// Not inlined: it is reached from half a dozen places (schedule scan, cursor
-// set-up, row changes) and inlining its window arithmetic into each of them
-// measurably slowed the streaming loop (instruction fetch).
-static __device__ __noinline__ RowGeom row_geom(const DecodeParams &p, int b)
+// Two forms of one body: the schedule (once per kernel, on the critical path
+// to the first copy) inlines it; the streaming loops' row changes call the
+// out-of-line form, since inlining its window arithmetic there measurably
+// slowed the loops (instruction fetch), while a call from the schedule costs
+// a cold instruction fetch before the first byte moves.
+__device__ __forceinline__ RowGeom row_geom_inl(const DecodeParams &p, int b)
 {
     RowGeom r;
     r.P = kept_prefix(p, b);
@@ -248,6 +250,8 @@ static __device__ __noinline__ RowGeom row_geom(const DecodeParams &p, int b)
     return r;
 }
 
+static __device__ __noinline__ RowGeom row_geom(const DecodeParams &p, int b) { return row_geom_inl(p, b); }
+
 // Whether slot j of a row with this geometry takes part in the softmax.
 __device__ __forceinline__ bool attended(int L, int lo, int P, int j)
 {
@@ -261,7 +265,7 @@ __device__ __forceinline__ bool attended(int L, int lo, int P, int j)
 // tiles, so all CTAs finish together.
 __device__ __forceinline__ int row_tiles(const DecodeParams &p, int b)
 {
-    const int nr = row_geom(p, b).nr;
+    const int nr = row_geom_inl(p, b).nr;   // schedule only
 #if GQA_MULTI_TOKEN
     return nr ? nr + p.pad_tiles : 0;
 #else
@@ -342,7 +346,16 @@ __device__ __forceinline__ TileCursor cursor_at(const DecodeParams &p, int b, lo
     c.g = g;
     c.end = end;
     c.b = b;
-    set_row(p, c);
+    const RowGeom r = row_geom_inl(p, b);   // schedule only: inlined (see row_geom)
+    c.L = r.L;
+    c.lo = r.lo;
+    c.P = r.P;
+    c.nr = r.nr;
+    c.tp = r.tp;
+    c.gap = r.gap;
+    c.nq = r.nq;
+    c.tokL = r.tokL;
+    c.Lb = r.Lb;
     const int nt = c.nr + p.pad_tiles;   // cursor_at is only used on rows with tiles
     const long long within = g - run;
     c.kvh = (int)div_floor(within, nt);
