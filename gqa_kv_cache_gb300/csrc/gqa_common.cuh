@@ -687,7 +687,7 @@ __device__ __forceinline__ float *out_row(const DecodeParams &p, const TileCurso
 // semantics shortly before the segment's end, or -1. When it already shows
 // every other piece of the unit arrived, this CTA is the last arriver: it
 // skips the ticket's round trip and merges at once.
-template <int NW, int GP, int DD, int DP, bool MULTI, class Sync, int GR, int KM>
+template <int NW, int GP, int DD, int DP, bool MULTI, bool PRE2 = false, class Sync, int GR, int KM>
 __device__ inline void finish_segment(const DecodeParams &p, const TileCursor &cur, const TileWalk &walk,
                                       int seg_first_t,
                                       bool bad, const float (&sm_m)[NW][GP], const float (&sm_l)[NW][GP],
@@ -793,7 +793,18 @@ __device__ inline void finish_segment(const DecodeParams &p, const TileCursor &c
         const long long P0 = (long long)u + first;
         if (K <= KM) {
             // one parallel load of every partial's (m, l), weights per head,
-            // then independent (vector) loads of the partial outputs
+            // then independent (vector) loads of the partial outputs. PRE2: a
+            // unit cut once (K = 2, the usual case) has this thread's first
+            // two partial outputs loaded together with the (m, l) pairs, one
+            // round trip to L2 instead of two on the kernel's last step (it
+            // costs registers: kernels at their register cap leave it off).
+            constexpr int V = (DD % 4 == 0) ? 4 : 1;
+            const bool pre2 = PRE2 && (V == 4) && K == 2 && tid * V < G * DD;
+            float4 pv0 = make_float4(0.f, 0.f, 0.f, 0.f), pv1 = pv0;
+            if (pre2) {
+                pv0 = __ldcg(reinterpret_cast<const float4 *>(p.ws_o + P0 * G * DD + tid * V));
+                pv1 = __ldcg(reinterpret_cast<const float4 *>(p.ws_o + (P0 + 1) * G * DD + tid * V));
+            }
             for (int k = tid; k < K * G; k += nthr) {
                 mb.w[k] = __ldcg(p.ws_ml + (P0 * G + k) * 2);
                 mb.l[k] = __ldcg(p.ws_ml + (P0 * G + k) * 2 + 1);
@@ -814,13 +825,31 @@ __device__ inline void finish_segment(const DecodeParams &p, const TileCursor &c
                 mb.inv_den[tid] = 1.f / den;
             }
             sync();
-            constexpr int V = (DD % 4 == 0) ? 4 : 1;
             for (int idx = tid * V; idx < G * DD; idx += nthr * V) {
                 const int g = idx / DD;
                 float acc[V];
 #pragma unroll
                 for (int e = 0; e < V; ++e)
                     acc[e] = 0.f;
+                if constexpr (PRE2 && V == 4) {
+                    if (pre2 && idx == tid * V) {   // the preloaded pair
+                        const float a0 = mb.w[g], a1 = mb.w[G + g];
+                        acc[0] = fmaf(a1, pv1.x, a0 * pv0.x);
+                        acc[1] = fmaf(a1, pv1.y, a0 * pv0.y);
+                        acc[2] = fmaf(a1, pv1.z, a0 * pv0.z);
+                        acc[3] = fmaf(a1, pv1.w, a0 * pv0.w);
+                        *reinterpret_cast<float4 *>(p.ws_o + P0 * G * DD + idx) = make_float4(0.f, 0.f, 0.f, 0.f);
+                        *reinterpret_cast<float4 *>(p.ws_o + (P0 + 1) * G * DD + idx) =
+                            make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (g < nrow) {
+                            float *o = out_row<MULTI>(p, cur, g, DD) + (idx - g * DD);
+#pragma unroll
+                            for (int e = 0; e < V; ++e)
+                                o[e] = acc[e] * mb.inv_den[g];
+                        }
+                        continue;
+                    }
+                }
 #pragma unroll 4
                 for (int i = 0; i < K; ++i) {
                     const float a = mb.w[i * G + g];

@@ -1160,7 +1160,9 @@ __global__ void __launch_bounds__(kThreads, (Ring<QF32, KV8, MULTI, M16>::kCtas)
             const bool bad = !row_good || seg_bad;
             if (bad && row_good && tid == 0)
                 report(p, aborted ? kTimeout : kBadBlock);
-            finish_segment<kConsumerWarps, kRW, kD, kD + Shared<kNS, kRW>::kOPad, MULTI>(p, cur, walk, seg_first_t,
+            // the merge's preload of partial outputs costs registers: off for
+            // the E4M3 kernels (at their 128-register cap)
+            finish_segment<kConsumerWarps, kRW, kD, kD + Shared<kNS, kRW>::kOPad, MULTI, !KV8>(p, cur, walk, seg_first_t,
                                                                                    bad, sh.m, sh.l, sh.o,
                                                       &sh.last_flag, sh.merge, tid, kConsumerWarps * 32,
                                                       [] { consumer_sync(); }, pre_cnt);
