@@ -4,13 +4,13 @@
 
 namespace gqa {
 
-cudaError_t simt_launch_f32_large(int D, int G, const DecodeParams *p, cudaStream_t st, int *per_sm)
+cudaError_t GQA_SIMT_FN(simt_launch_f32_large)(int D, int G, const DecodeParams *p, cudaStream_t st, int *per_sm)
 {
     switch (D) {
-    case 32: return launch_g<float, 32>(G, p, st, per_sm);
-    case 64: return launch_g<float, 64>(G, p, st, per_sm);
-    case 128: return launch_g<float, 128>(G, p, st, per_sm);
-    case 256: return launch_g<float, 256>(G, p, st, per_sm);
+    case 32: return launch_g<float, 32, kSimtGen>(G, p, st, per_sm);
+    case 64: return launch_g<float, 64, kSimtGen>(G, p, st, per_sm);
+    case 128: return launch_g<float, 128, kSimtGen>(G, p, st, per_sm);
+    case 256: return launch_g<float, 256, kSimtGen>(G, p, st, per_sm);
     default: return cudaErrorInvalidValue;
     }
 }

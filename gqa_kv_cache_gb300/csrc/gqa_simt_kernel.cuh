@@ -19,13 +19,30 @@
 // In a multi-token step every slot from the row's write offset on is a new
 // token, read from k_new / v_new (and appended by the chunk that owns it), and
 // each query row (token, head) is masked beyond its own token's position.
+//
+// GEN: the general form (multi-token steps, sliding windows). The plain
+// single-token forms (decode step and attend without a window) are compiled
+// without the per-row bounds and, in their own translation units, without the
+// multi-token schedule branches (GQA_SIMT_GEN 0, GQA_MULTI_TOKEN 0): measured,
+// the general code cost the plain step about 20 %.
 #pragma once
+
+#ifndef GQA_SIMT_GEN
+#define GQA_SIMT_GEN 1
+#endif
+#if GQA_SIMT_GEN
+#define GQA_SIMT_FN(name) name
+#else
+#define GQA_SIMT_FN(name) name##_plain
+#endif
 
 #include "gqa_common.cuh"
 #include "gqa_launch.h"
 
 namespace gqa {
 namespace {
+
+constexpr bool kSimtGen = GQA_SIMT_GEN;
 
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
@@ -129,7 +146,7 @@ __device__ __forceinline__ void merge_state(float (&m1)[GP], float (&l1)[GP], fl
     }
 }
 
-template <typename T, int D, int GP>
+template <typename T, int D, int GP, bool GEN>
 __global__ void __launch_bounds__(kThreads) simt_decode_kernel(const DecodeParams p)
 {
     using S = SimtShape<T, D>;
@@ -170,19 +187,21 @@ __global__ void __launch_bounds__(kThreads) simt_decode_kernel(const DecodeParam
             row_good = row_ok(p, b, L);
             if (!row_good && tid == 0 && cur.t == 0 && kvh == 0)
                 report(p, row_error_bits(p, b, L));
-            const int qrows = p.cu_q ? p.Gh * cur.nq : G;   // query rows with data
+            const bool multi = GEN && p.cu_q;
+            const int qrows = multi ? p.Gh * cur.nq : G;   // query rows with data
 #pragma unroll
             for (int g = 0; g < GP; ++g) {
                 m[g] = -INFINITY;
                 l[g] = 0.f;
-                lim[g] = p.cu_q ? L - (cur.nq - 1 - g / p.Gh) : L;
+                if constexpr (GEN)
+                    lim[g] = multi ? L - (cur.nq - 1 - g / p.Gh) : L;
 #pragma unroll
                 for (int e = 0; e < VEC; ++e)
                     o[g][e] = 0.f;
                 if (g < qrows) {
                     float tmp[VEC];
                     // row g: token tok, head kvh * Gh + g % Gh
-                    const long long tok = p.cu_q ? cur.tokL - (cur.nq - 1 - g / p.Gh) : b;
+                    const long long tok = multi ? cur.tokL - (cur.nq - 1 - g / p.Gh) : b;
                     load_q<VEC>(p, (tok * p.Hq + (long long)kvh * p.Gh + g % p.Gh) * D + li * VEC, tmp);
 #pragma unroll
                     for (int e = 0; e < VEC; ++e)
@@ -200,7 +219,8 @@ __global__ void __launch_bounds__(kThreads) simt_decode_kernel(const DecodeParam
             const int s0 = tile_slot0(cur, p.tile);
             const int s1 = min(s0 + p.tile, L + 1);
             // slots from here on are new tokens (none in the read-only attend)
-            const int first_new = p.attend ? INT_MAX : (p.cu_q ? cur.Lb : L);
+            const bool multi = GEN && p.cu_q;
+            const int first_new = p.attend ? INT_MAX : (multi ? cur.Lb : L);
             // warp-uniform trip count: every lane takes part in the shuffles
             for (int jb = s0 + warp * SPW; jb < s1; jb += STREAMS) {
                 const int j = jb + lg;
@@ -210,7 +230,9 @@ __global__ void __launch_bounds__(kThreads) simt_decode_kernel(const DecodeParam
                     kv[e] = vv[e] = 0.f;
                 bool use = false;
                 if (j < first_new) {
-                    if (attended(L, cur.lo, cur.P, j)) {
+                    // without a window every slot up to L is attended (j may
+                    // pass s1 in the tile's last lane groups)
+                    if (GEN ? attended(L, cur.lo, cur.P, j) : j <= L) {
                         long long off = slot_offset(p, b, kvh, j);
                         if (off < 0) {
                             bad_local = 1;
@@ -221,13 +243,13 @@ __global__ void __launch_bounds__(kThreads) simt_decode_kernel(const DecodeParam
                         }
                     }
                 } else if (j <= L) {  // a new token, and its in-place append
-                    const long long tok = p.cu_q ? cur.tokL - (L - j) : b;
+                    const long long tok = multi ? cur.tokL - (L - j) : b;
                     const long long new_off = (tok * p.Hkv + kvh) * D + li * VEC;
                     load_vec<T, VEC>(static_cast<const T *>(p.k_new) + new_off, kv);
                     load_vec<T, VEC>(static_cast<const T *>(p.v_new) + new_off, vv);
                     use = true;
                     // appended by the unit that owns the token
-                    long long off = (!p.cu_q || j > L - cur.nq) ? slot_offset(p, b, kvh, j) : -2;
+                    long long off = (!multi || j > L - cur.nq) ? slot_offset(p, b, kvh, j) : -2;
                     if (off >= 0) {
                         copy_vec<T, VEC>(static_cast<T *>(p.k_cache) + off + li * VEC,
                                          static_cast<const T *>(p.k_new) + new_off);
@@ -253,7 +275,7 @@ __global__ void __launch_bounds__(kThreads) simt_decode_kernel(const DecodeParam
 #pragma unroll
                     for (int g = 0; g < GP; ++g) {
                         // row g's own causal bound and window
-                        if (j > lim[g] || (p.window > 0 && j <= lim[g] - p.window && j >= cur.P))
+                        if (GEN && (j > lim[g] || (p.window > 0 && j <= lim[g] - p.window && j >= cur.P)))
                             continue;
                         float mn = fmaxf(m[g], s[g]);
                         float alpha = ex2(m[g] - mn);  // m = -inf gives 0
@@ -302,7 +324,8 @@ __global__ void __launch_bounds__(kThreads) simt_decode_kernel(const DecodeParam
             const bool bad = !row_good || seg_bad;
             if (bad && row_good && tid == 0)
                 report(p, kBadBlock);
-            finish_segment<kWarps, GP, D, D, true>(p, cur, walk, seg_first_t, bad, sm_m, sm_l, sm_o, &sm_flag, sm_merge, tid,
+            // the plain form's cursor carries no chunk fields (output row b)
+            finish_segment<kWarps, GP, D, D, GEN>(p, cur, walk, seg_first_t, bad, sm_m, sm_l, sm_o, &sm_flag, sm_merge, tid,
                                           kThreads, [] { __syncthreads(); });
             seg_start = true;
         }
@@ -312,11 +335,11 @@ __global__ void __launch_bounds__(kThreads) simt_decode_kernel(const DecodeParam
 
 // Either launches the instantiation for (T, D, GP) or, with p == nullptr,
 // reports how many of its CTAs fit on one SM.
-template <typename T, int D, int GP>
+template <typename T, int D, int GP, bool GEN>
 cudaError_t launch_one(const DecodeParams *p, cudaStream_t st, int *per_sm)
 {
     if (!p) {
-        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, simt_decode_kernel<T, D, GP>,
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, simt_decode_kernel<T, D, GP, GEN>,
                                                              kThreads, 0);
     }
     cudaLaunchConfig_t cfg = {};
@@ -328,26 +351,31 @@ cudaError_t launch_one(const DecodeParams *p, cudaStream_t st, int *per_sm)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, simt_decode_kernel<T, D, GP>, *p);
+    return cudaLaunchKernelEx(&cfg, simt_decode_kernel<T, D, GP, GEN>, *p);
 }
 
-template <typename T, int D>
+template <typename T, int D, bool GEN>
 cudaError_t launch_g(int G, const DecodeParams *p, cudaStream_t st, int *per_sm)
 {
-    if (G == 1) return launch_one<T, D, 1>(p, st, per_sm);
-    if (G == 2) return launch_one<T, D, 2>(p, st, per_sm);
-    if (G <= 4) return launch_one<T, D, 4>(p, st, per_sm);
-    if (G <= 6) return launch_one<T, D, 6>(p, st, per_sm);
-    return launch_one<T, D, 8>(p, st, per_sm);
+    if (G == 1) return launch_one<T, D, 1, GEN>(p, st, per_sm);
+    if (G == 2) return launch_one<T, D, 2, GEN>(p, st, per_sm);
+    if (G <= 4) return launch_one<T, D, 4, GEN>(p, st, per_sm);
+    if (G <= 6) return launch_one<T, D, 6, GEN>(p, st, per_sm);
+    return launch_one<T, D, 8, GEN>(p, st, per_sm);
 }
 
 }  // namespace
 
-// The instantiations are spread over several translation units (by dtype and
-// head width) so that they compile in parallel; each defines one of these.
+// The instantiations are spread over several translation units (by dtype,
+// head width and form) so that they compile in parallel; each defines one of
+// these (the _plain ones: GEN = false).
 cudaError_t simt_launch_f32_small(int D, int G, const DecodeParams *p, cudaStream_t st, int *per_sm);
 cudaError_t simt_launch_f32_large(int D, int G, const DecodeParams *p, cudaStream_t st, int *per_sm);
 cudaError_t simt_launch_bf16_small(int D, int G, const DecodeParams *p, cudaStream_t st, int *per_sm);
 cudaError_t simt_launch_bf16_large(int D, int G, const DecodeParams *p, cudaStream_t st, int *per_sm);
+cudaError_t simt_launch_f32_small_plain(int D, int G, const DecodeParams *p, cudaStream_t st, int *per_sm);
+cudaError_t simt_launch_f32_large_plain(int D, int G, const DecodeParams *p, cudaStream_t st, int *per_sm);
+cudaError_t simt_launch_bf16_small_plain(int D, int G, const DecodeParams *p, cudaStream_t st, int *per_sm);
+cudaError_t simt_launch_bf16_large_plain(int D, int G, const DecodeParams *p, cudaStream_t st, int *per_sm);
 
 }  // namespace gqa
