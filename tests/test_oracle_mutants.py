@@ -61,6 +61,8 @@ MUTANTS = {
                                "return orc_e4m3_decode(((const uint8_t *)cache)[i]);"),
     "e4m3_append_not_divided": ("const float y = (float)elem(news, src + d, J->new_dtype) / scale[kvh];",
                                 "const float y = (float)elem(news, src + d, J->new_dtype);"),
+    "e4m3_new_unquantised": ("    if (J->kv_dtype != ORC_E4M3)\n        return x;\n    const float y = (float)x / scale[kvh];",
+                             "    if (1)\n        return x;\n    const float y = (float)x / scale[kvh];"),
     "query_head_offset": ("const size_t q_i = ((size_t)tok * J->Hq + h) * D;", "const size_t q_i = ((size_t)tok * J->Hq + g) * D;"),
 }
 

@@ -1150,3 +1150,28 @@ def test_e4m3_multi_appends_the_library_cast():
             want_k = _e4m3_lib(bf(c["k_new"][t]) / c["k_scale"][:, None])
             want_v = _e4m3_lib(bf(c["v_new"][t]) / c["v_scale"][:, None])
             assert kc[b, :, s].tobytes() == want_k.tobytes() and vc[b, :, s].tobytes() == want_v.tobytes()
+
+
+def test_e4m3_without_append_reads_the_stored_new_values():
+    """Without the append, the new token is read from k_new / v_new as the
+    cache would store it (quantised): the outputs equal the appending step's
+    bit for bit and the cache is untouched (single and multi-token)."""
+    c = _e4m3_multi_case(66, [1, 1, 1])
+    sc = dict(k_scale=c["k_scale"], v_scale=c["v_scale"])
+    q, kn, vn = c["q"], c["k_new"], c["v_new"]
+    kc, vc = c["k_cache"].copy(), c["v_cache"].copy()
+    r1 = oracle.decode_dense(q, kn, vn, kc, vc, c["lengths"], **sc)
+    kc2, vc2 = c["k_cache"].copy(), c["v_cache"].copy()
+    r2 = oracle.decode_dense(q, kn, vn, kc2, vc2, c["lengths"], append=False, **sc)
+    assert r1.status == r2.status == oracle.OK
+    assert r1.out.tobytes() == r2.out.tobytes()
+    assert kc2.tobytes() == c["k_cache"].tobytes() and vc2.tobytes() == c["v_cache"].tobytes()
+    m = _e4m3_multi_case(67, [3, 2, 4])
+    sc = dict(k_scale=m["k_scale"], v_scale=m["v_scale"])
+    kc, vc = m["k_cache"].copy(), m["v_cache"].copy()
+    r3 = oracle.decode_multi_dense(m["q"], m["k_new"], m["v_new"], kc, vc, m["lengths"], m["cu_q"], **sc)
+    kc2, vc2 = m["k_cache"].copy(), m["v_cache"].copy()
+    r4 = oracle.decode_multi_dense(m["q"], m["k_new"], m["v_new"], kc2, vc2, m["lengths"], m["cu_q"],
+                                   append=False, **sc)
+    assert r3.out.tobytes() == r4.out.tobytes()
+    assert kc2.tobytes() == m["k_cache"].tobytes()
