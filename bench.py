@@ -2,11 +2,22 @@
 """Benchmark of the GQA decode step over a KV cache on one GB300.
 
 A step is one call of the library's decode step (in-place append, split-S
-attention, log-sum-exp combine) over the whole synthetic batch of the chosen
-workload (default: the Llama-3-8B-shaped decode, bf16, B=32, Hq=32, Hkv=8,
-D=128, Smax=4096, lengths ~ U{1024..4095}).
+attention, log-sum-exp combine) over the whole synthetic batch of a workload.
 
-Prints ONE JSON line (rank 0):
+By default every one of the five decode workloads is measured in turn (each
+generated, timed and freed before the next):
+
+  pr1_fp32      fp32, B=2, Hq=8, Hkv=2, D=64, Smax=256
+  llama3_8b     bf16, B=32, Hq=32, Hkv=8, D=128, Smax=4096
+  long_context  bf16, B=4, Hq=64, Hkv=8, D=128, Smax=131072
+  ragged_slots  bf16, B=256 of 512 rows, Hq=32, Hkv=4, D=128, Smax=8192
+  paged         bf16, B=64, Hq=48, Hkv=8, D=128, 65536 blocks of 16 slots
+
+and ONE JSON line is printed (rank 0) whose headline is `paged`, the largest
+workload by KV bytes read per step (2.2 GB), with every workload's own
+figures under `per_config`. `--workload NAME` measures that one alone.
+
+Per workload:
   value     KV-cache bytes the step must read (sum_b lengths[b]*Hkv*D*2*es)
             divided by the device time of the step, in GB/s, inputs resident
             in HBM, L2 flushed between timed steps (a 256 MB write and then a
@@ -16,8 +27,10 @@ Prints ONE JSON line (rank 0):
             copied from pinned host memory (one staging buffer, one copy) and
             the output read back, every step;
   roofline  the decode kernel alone (CUDA events around its launches) against
-            the measured HBM copy bandwidth;
-  cpu_baseline  the float64 CPU oracle on this machine's host cores.
+            the measured HBM copy bandwidth, with the per-launch DRAM traffic
+            of the committed ncu capture of that kernel and workload;
+  cpu_baseline  the float64 CPU oracle on this machine's host cores over a
+            bounded sample of the workload's batch rows.
 With --impl reference the oracle itself is timed as the reference arm.
 
 --op attend times the read-only attend instead (no append; lengths count the
@@ -27,8 +40,8 @@ then count only the slots inside the window or the prefix.
 --kv e4m3 stores the cache as E4M3 (FP8) bytes with per-head scales (the KV
 bytes are then one per element; q, k_new, v_new stay bfloat16).
 --q-len N times the multi-token step (N new tokens per row, causal); its KV
-bytes count the cached slots once (a row whose tokens span several chunks of
-8 / G tokens streams them once per chunk, which shows in the roofline).
+bytes count the cached slots once (a row whose tokens span several chunks
+streams them once per chunk, which shows in the roofline).
 
 Multi-GPU (torchrun): every rank runs an independent replica with its own
 batch (weak scaling, no data-path collective); times are max over ranks.
@@ -53,15 +66,20 @@ UNIT = "GB/s"
 NOMINAL_HBM_GBPS = 8000.0
 FALLBACK_HBM_GBPS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
+SUITE = ["pr1_fp32", "llama3_8b", "long_context", "ragged_slots", "paged"]
+HEADLINE = "paged"          # the largest workload by KV bytes read per step
+CPU_SAMPLE_KV_BYTES = 192 << 20   # KV bytes of one CPU-baseline pass (bounded sample)
+REF_SAMPLE_KV_BYTES = 64 << 20    # KV bytes of one reference-arm step
 
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="llama3_8b")
+    ap.add_argument("--workload", default="all",
+                    help="one workload, or 'all' (default): the five, headline " + HEADLINE)
     ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "tc"])
     ap.add_argument("--op", default="decode", choices=["decode", "attend"],
                     help="decode step (default) or the read-only attend")
@@ -74,6 +92,9 @@ def parse():
     ap.add_argument("--kv", default="native", choices=["native", "e4m3"],
                     help="cache element type: the workload's own or E4M3 bytes with per-head scales")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--shrink", type=int, default=1,
+                    help="divide the batch (and the cache rows / paged blocks) by this factor: a "
+                         "smaller instance of the same shapes and length law, for ncu captures")
     ap.add_argument("--clocks-dir", default=None,
                     help="folder for the raw nvidia-smi samples of the timed region (default: the temp dir)")
     ap.add_argument("--sched-pad", type=int, default=None,
@@ -128,12 +149,20 @@ class Ranks:
 
 # ------------------------------------------------------------- workload ----
 
-def workload(name, rank):
+def workload(name, rank, shrink=1):
+    """The named workload; rank r > 0 draws its own batch (seed + 1000 r).
+    shrink > 1: B, the dense rows and the paged block pool divided by it (the
+    same G, D, block size and length law; a paged table still gets distinct
+    blocks)."""
     import workloads as W
+    from dataclasses import replace
     w = W.WORKLOADS[name]
     if rank:
-        from dataclasses import replace
         w = replace(w, seed=w.seed + 1000 * rank)
+    if shrink > 1:
+        w = replace(w, B=max(1, w.B // shrink), R=max(1, w.R // shrink) if w.R else 0,
+                    num_blocks=max(1, w.num_blocks // shrink) if w.paged else 0,
+                    name=f"{w.name}/shrink{shrink}")
     return w
 
 
@@ -233,12 +262,12 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, device_index, log_dir=None):
+    def __init__(self, device_index, log_dir=None, tag=""):
         self.dev = device_index
         self.proc = None
         # the raw samples stay on disk for inspection (--clocks-dir)
         import tempfile
-        self.path = os.path.join(log_dir or tempfile.gettempdir(), f"clocks_rank{device_index}.csv")
+        self.path = os.path.join(log_dir or tempfile.gettempdir(), f"clocks_rank{device_index}{tag}.csv")
 
     def start(self):
         try:
@@ -288,42 +317,96 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- oracle ---
 
-def oracle_rate(w, t, rows, repeats=3, mods=None):
-    """CPU oracle over batch rows `rows` (host copies), timed: returns
-    (GB/s of KV processed, seconds per pass, threads)."""
+def sample_rows(w, t, budget_bytes, kv_es, attend, multi, offset=0):
+    """A bounded sample of batch rows for the CPU oracle: rows taken in order
+    (starting at `offset`, wrapping) until their cached KV bytes reach
+    `budget_bytes` (at least one row)."""
+    L = t["lengths"].to("cpu").tolist()
+    rows, total = [], 0
+    for k in range(w.B):
+        b = (offset + k) % w.B
+        rows.append(b)
+        total += max(int(L[b]), 0) * w.Hkv * w.D * 2 * kv_es
+        if total >= budget_bytes:
+            break
+    return sorted(rows)
+
+
+def oracle_problem(w, t, rows, mods=None):
+    """Host copies of what the oracle needs for batch rows `rows`: the rows'
+    cache rows (dense / slot-id caches) or the blocks their tables name (paged,
+    renumbered), their queries and new tokens (packed tokens of a multi-token
+    step, with new offsets). Returns (callable running the oracle without
+    append, cached KV bytes it reads)."""
     import numpy as np
     import torch
     import oracle
-    sel = torch.tensor(rows, dtype=torch.long, device=t["q"].device)
+    dev = t["q"].device
+    sel = torch.tensor(rows, dtype=torch.long, device=dev)
 
     def host(x):
         x = x.detach().cpu().contiguous()
-        return x.view(torch.int16).numpy().view(np.uint16).copy() if x.dtype == torch.bfloat16 \
-            else x.numpy().copy()
+        if x.dtype == torch.bfloat16:
+            return x.view(torch.int16).numpy().view(np.uint16).copy()
+        if x.dtype == torch.uint8:
+            return x.numpy().copy()
+        return x.numpy().copy()
 
     attend = "k_new" not in t
+    multi = "cu_q" in t
     om = {}
     if mods:
         om = {"window": mods.get("window", 0), "kept_prefix": mods.get("kept_prefix", 0)}
         if mods.get("sink") is not None:
             om["sink"] = mods["sink"].cpu().numpy()
-    q, L = host(t["q"][sel]), host(t["lengths"][sel])
-    if not attend:
-        kn, vn = host(t["k_new"][sel]), host(t["v_new"][sel])
+    if "k_scale" in t:
+        om["k_scale"] = t["k_scale"].cpu().numpy()
+        om["v_scale"] = t["v_scale"].cpu().numpy()
+    L = host(t["lengths"][sel])
+    if multi:
+        cu = t["cu_q"].cpu().tolist()
+        tok = [i for b in rows for i in range(cu[b], cu[b + 1])]
+        tsel = torch.tensor(tok, dtype=torch.long, device=dev)
+        qlen = [cu[b + 1] - cu[b] for b in rows]
+        cu_s = np.concatenate([[0], np.cumsum(qlen)]).astype(np.int32)
+        q, kn, vn = host(t["q"][tsel]), host(t["k_new"][tsel]), host(t["v_new"][tsel])
+    else:
+        q = host(t["q"][sel])
+        if not attend:
+            kn, vn = host(t["k_new"][sel]), host(t["v_new"][sel])
     if w.paged:
         bt = t["block_table"][sel].cpu().numpy()
         used = sorted(set(int(x) for x in bt[bt >= 0].tolist()))
         remap = {b: i for i, b in enumerate(used)}
-        idx = torch.tensor(used, dtype=torch.long, device=t["q"].device)
+        idx = torch.tensor(used, dtype=torch.long, device=dev)
         kb, vb = host(t["k_blocks"][idx]), host(t["v_blocks"][idx])
         btr = np.vectorize(lambda x: remap.get(int(x), -1))(bt).astype(np.int32)
-        run = (lambda: oracle.attend_paged(q, kb, vb, btr, L, **om)) if attend else \
-            (lambda: oracle.decode_paged(q, kn, vn, kb, vb, btr, L, append=False, **om))
+        if multi:
+            run = lambda: oracle.decode_multi_paged(q, kn, vn, kb, vb, btr, L, cu_s, append=False, **om)
+        elif attend:
+            run = lambda: oracle.attend_paged(q, kb, vb, btr, L, **om)
+        else:
+            run = lambda: oracle.decode_paged(q, kn, vn, kb, vb, btr, L, append=False, **om)
     else:
         cr = t["slot_ids"][sel].long() if "slot_ids" in t else sel
         kc, vc = host(t["k_cache"][cr]), host(t["v_cache"][cr])
-        run = (lambda: oracle.attend_dense(q, kc, vc, L, **om)) if attend else \
-            (lambda: oracle.decode_dense(q, kn, vn, kc, vc, L, append=False, **om))
+        if multi:
+            run = lambda: oracle.decode_multi_dense(q, kn, vn, kc, vc, L, cu_s, append=False, **om)
+        elif attend:
+            run = lambda: oracle.attend_dense(q, kc, vc, L, **om)
+        else:
+            run = lambda: oracle.decode_dense(q, kn, vn, kc, vc, L, append=False, **om)
+    win, kp = (mods or {}).get("window", 0), (mods or {}).get("kept_prefix", 0)
+    n = cached_slots_read(torch.from_numpy(np.asarray(L, dtype=np.int64)), attend, win, kp)
+    kv_es = 1 if "k_scale" in t else w.elem_bytes
+    kv = int(n.sum().item()) * w.Hkv * w.D * 2 * kv_es
+    return run, kv
+
+
+def oracle_rate(w, t, rows, repeats=3, mods=None):
+    """CPU oracle over batch rows `rows` (host copies), timed: returns
+    (GB/s of KV processed, seconds per pass, threads)."""
+    run, kv = oracle_problem(w, t, rows, mods)
     r = run()                                   # warm-up
     times = []
     for _ in range(repeats):
@@ -331,9 +414,6 @@ def oracle_rate(w, t, rows, repeats=3, mods=None):
         r = run()
         times.append(time.perf_counter() - t0)
     sec = statistics.median(times)
-    win, kp = (mods or {}).get("window", 0), (mods or {}).get("kept_prefix", 0)
-    n = cached_slots_read(torch.from_numpy(np.asarray(L, dtype=np.int64)), attend, win, kp)
-    kv = int(n.sum().item()) * w.Hkv * w.D * 2 * w.elem_bytes
     return kv / sec / 1e9, sec, r.threads
 
 
@@ -372,18 +452,36 @@ def sources_sha(names):
     return h.hexdigest()[:16]
 
 
-def traffic_for(kernel_name, workload):
-    """Per-launch DRAM bytes (read + write) of the kernel on this workload from
-    the committed ncu summary, if it was taken on the current sources of that
-    kernel; else None."""
+def traffic_for(kernel_name, key):
+    """Per-launch DRAM bytes (read + write) of the kernel on this workload and
+    operation from the committed ncu summary, if it was taken on the current
+    sources of that kernel; else None. Captures of a scaled-down instance
+    carry the scale factor to a full launch (`scale`)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
-        d = json.load(open(p))[kernel_name][workload]
+        d = json.load(open(p))[kernel_name][key]
         if sources_sha(d["sources"]) != d["sources_sha"]:
             return None
         return d["bytes_per_launch"]
     except Exception:
         return None
+
+
+def traffic_key(wname, attend, fp8, q_len, mods):
+    key = wname + ("/attend" if attend else "") + ("/e4m3" if fp8 else "") + (f"/q{q_len}" if q_len else "")
+    if mods:
+        key += "/mods"
+    return key
+
+
+def supported(wname, args):
+    """Whether the workload takes the options asked for (an E4M3 cache needs
+    the tensor-core kernel's D = 128)."""
+    import workloads as W
+    w = W.WORKLOADS[wname]
+    if args.kv == "e4m3" and (w.D != 128 or w.dtype != "bf16" or args.kernel == "simt"):
+        return False
+    return True
 
 
 # ------------------------------------------------------------------ arms ---
@@ -394,60 +492,70 @@ def run_reference(args, ranks):
     if ranks.rank != 0:
         return
     import torch
-    w = workload(args.workload, 0)
+    wname = HEADLINE if args.workload == "all" else args.workload
+    w = workload(wname, 0, args.shrink)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     import workloads as W
     attend = args.op == "attend"
-    t = W.generate(w, dev, attend=attend, q_f32=attend and args.q_dtype != "cache")
+    multi = args.q_len > 0
+    fp8 = args.kv == "e4m3"
+    t = W.generate(w, dev, attend=attend, q_f32=attend and args.q_dtype != "cache",
+                   q_lens=[args.q_len] * w.B if multi else None, kv_e4m3=fp8)
     mods = make_mods(args, w, dev)
-    n = min(w.B, 4)
+    kv_es = 1 if fp8 else w.elem_bytes
+    rows0 = sample_rows(w, t, REF_SAMPLE_KV_BYTES, kv_es, attend, multi)
+    n = len(rows0)
     for i in range(args.warmup):
-        oracle_rate(w, t, [(i * n + k) % w.B for k in range(n)], repeats=1, mods=mods)
-    rates, secs, threads = [], [], 1
+        oracle_rate(w, t, sample_rows(w, t, REF_SAMPLE_KV_BYTES, kv_es, attend, multi, i * n), repeats=1,
+                    mods=mods)
+    threads = 1
     kv_total, t_total = 0, 0.0
     for i in range(args.steps):
-        rows = [((i + args.warmup) * n + k) % w.B for k in range(n)]
+        rows = sample_rows(w, t, REF_SAMPLE_KV_BYTES, kv_es, attend, multi, (i + args.warmup) * n)
         gbs, sec, threads = oracle_rate(w, t, rows, repeats=1, mods=mods)
         kv_total += gbs * sec * 1e9
         t_total += sec
     value = kv_total / t_total / 1e9
+    metric = METRIC_MULTI if multi else (METRIC_ATTEND if attend else METRIC)
     line = {
-        "impl": "reference", "metric": METRIC_ATTEND if attend else METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "impl": "reference", "metric": metric, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_total / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": w.name, "op": args.op, "B": w.B, "Hq": w.Hq,
                                         "Hkv": w.Hkv, "D": w.D, "sample_rows_per_step": n,
                                         **mods_config(args)},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                         "sample": f"{n} of {w.B} batch rows per step, rotating, float64 loops"},
+                         "sample": f"about {REF_SAMPLE_KV_BYTES >> 20} MB of cached KV per step "
+                                   f"({n} of {w.B} batch rows, rotating), float64 loops"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
-def run_ours(args, ranks):
+def measure(args, ranks, wname, dev):
+    """Times one workload: the step (device time, L2 flushed between steps),
+    the decode kernel alone, the end-to-end step through the public API and
+    the CPU oracle on a bounded sample. Returns the workload's record."""
     import torch
     import workloads as W
     import gqa_kv_cache_gb300 as gqa
 
-    torch.cuda.set_device(ranks.local)
-    dev = torch.device("cuda", ranks.local)
-    w = workload(args.workload, ranks.rank)
+    w = workload(wname, ranks.rank, args.shrink)
     attend = args.op == "attend"
     multi = args.q_len > 0
-    if multi and (attend or args.window or args.kept_prefix):
-        raise SystemExit("--q-len times the plain multi-token step (no --op attend / window)")
     fp8 = args.kv == "e4m3"
     t = W.generate(w, dev, attend=attend, q_f32=attend and args.q_dtype != "cache",
                    q_lens=[args.q_len] * w.B if multi else None, kv_e4m3=fp8)
     torch.cuda.synchronize()
     out = torch.empty(t["q"].shape[0], w.Hq, w.D, dtype=torch.float32, device=dev)
     mods = make_mods(args, w, dev)
+    call_mods = dict(mods or {})
     if fp8:
-        mods = dict(mods or {}, k_scale=t["k_scale"], v_scale=t["v_scale"])
-    step = step_fn(w, t, args.kernel, out, args.sched_pad, attend, mods, args.q_len)
-    alg = algorithmic_bytes_multi(w, t, 1 if fp8 else None) if multi else algorithmic_bytes(w, t, attend, args.window,
-                                                                         args.kept_prefix, 1 if fp8 else None)
+        call_mods.update(k_scale=t["k_scale"], v_scale=t["v_scale"])
+    step = step_fn(w, t, args.kernel, out, args.sched_pad, attend, call_mods, args.q_len)
+    kv_es = 1 if fp8 else None
+    alg = algorithmic_bytes_multi(w, t, kv_es) if multi else algorithmic_bytes(w, t, attend, args.window,
+                                                                               args.kept_prefix, kv_es)
     flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush_r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     flush_sink = torch.empty((), dtype=torch.float32, device=dev)
@@ -473,7 +581,7 @@ def run_ours(args, ranks):
     # ---- timed region: K steps, L2 flushed between them (outside the events)
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    clocks = ClockSampler(ranks.local, args.clocks_dir)
+    clocks = ClockSampler(ranks.local, args.clocks_dir, "_" + wname)
     clocks.start()
     ranks.barrier()
     torch.cuda.synchronize()
@@ -508,8 +616,8 @@ def run_ours(args, ranks):
     avg_main_s = ms_main / max(n_main, 1) * 1e-3
     hbm_peak, peak_kind = peaks()
     achieved = alg["total"] / avg_main_s / 1e9
-    traffic = None if (mods or multi) else traffic_for(
-        main, w.name + ("/attend" if attend else "") + ("/e4m3" if fp8 else ""))
+    tkey = traffic_key(w.name, attend, fp8, args.q_len, mods)
+    traffic = traffic_for(main, tkey) if args.kernel == "auto" else None
 
     # ---- end to end through the public API, host buffers, copies inside
     Ke = min(K, 500)
@@ -532,7 +640,7 @@ def run_ours(args, ranks):
         dev_in[k] = dev_buf[offs[k]:offs[k] + nb].view(t[k].dtype).view(t[k].shape)
     tt = dict(t)
     tt.update(dev_in)
-    step_e2e = step_fn(w, tt, args.kernel, out, args.sched_pad, attend, mods, args.q_len)
+    step_e2e = step_fn(w, tt, args.kernel, out, args.sched_pad, attend, call_mods, args.q_len)
     out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
     h2d = total
     d2h = out.numel() * out.element_size()
@@ -551,22 +659,20 @@ def run_ours(args, ranks):
     e2e_ms = ranks.max(e2e_ms)
     e2e_value = kv_all * Ke / (e2e_ms * 1e-3) / 1e9
 
-    # ---- CPU baseline: the oracle on host cores, rank 0 at N = 1 only
+    # ---- CPU baseline: the oracle on host cores (bounded sample), rank 0 at N = 1 only
     cpu = None
-    if ranks.world == 1 and not args.no_cpu_baseline and not multi and not fp8:
-        rows = list(range(w.B))
+    if ranks.world == 1 and not args.no_cpu_baseline:
+        rows = sample_rows(w, t, CPU_SAMPLE_KV_BYTES, 1 if fp8 else w.elem_bytes, attend, multi)
         gbs, sec, threads = oracle_rate(w, t, rows, repeats=3, mods=mods)
         cpu = {"value": gbs, "unit": UNIT, "cores": threads, "kind": "oracle",
-               "sample": f"all {w.B} batch rows of one step (no append), float64 loops, "
-                         f"median of 3 after 1 warm-up, {sec:.2f} s per pass"}
+               "sample": f"{len(rows)} of {w.B} batch rows of one step (about "
+                         f"{CPU_SAMPLE_KV_BYTES >> 20} MB of cached KV or all rows; no append), "
+                         f"float64 loops, median of 3 after 1 warm-up, {sec:.3f} s per pass"}
 
-    line = {
-        "metric": METRIC_MULTI if multi else (METRIC_ATTEND if attend else METRIC), "value": value,
-        "unit": UNIT,
-        "n_gpus": ranks.world, "steps": K,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "us_per_step": ms_per_step * 1e3,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
-        "data": "synthetic",
+    rec = {
+        "metric": METRIC_MULTI if multi else (METRIC_ATTEND if attend else METRIC),
+        "value": value, "unit": UNIT, "ms_per_step": ms_per_step, "us_per_step": ms_per_step * 1e3,
+        "dtype": w.dtype,
         "frac_of_8TBps": value / ranks.world / NOMINAL_HBM_GBPS,
         "frac_of_measured_hbm": value / ranks.world / hbm_peak,
         "config": {"workload": w.name, "op": args.op, "q_dtype": str(t["q"].dtype).replace("torch.", ""),
@@ -582,6 +688,7 @@ def run_ours(args, ranks):
                    "wall_s_timed_region": wall},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": traffic,
+                     "traffic_key": tkey,
                      "peak_kind": peak_kind + " (STREAM-style copy)",
                      "kernel": main, "avg_launch_us": avg_main_s * 1e6,
                      "algorithmic_bytes_per_launch": alg["total"]},
@@ -591,6 +698,51 @@ def run_ours(args, ranks):
         "gpu_launches": K,   # one decode kernel per step (the split merge is fused)
         "clocks": clk,
     }
+    del t, out, flush_w, flush_r, host_buf, dev_buf, dev_in, tt
+    torch.cuda.empty_cache()
+    return rec
+
+
+def run_ours(args, ranks):
+    import torch
+
+    torch.cuda.set_device(ranks.local)
+    dev = torch.device("cuda", ranks.local)
+    if args.q_len > 0 and (args.op == "attend" or args.window or args.kept_prefix):
+        raise SystemExit("--q-len times the plain multi-token step (no --op attend / window)")
+    names = SUITE if args.workload == "all" else [args.workload]
+    head = HEADLINE if args.workload == "all" else args.workload
+    if not supported(head, args):
+        raise SystemExit(f"{head} does not take these options")
+    per = {}
+    for name in names:
+        if not supported(name, args):
+            per[name] = {"skipped": "an E4M3 cache needs the tensor-core kernel (bfloat16 data, D = 128)"}
+            continue
+        per[name] = measure(args, ranks, name, dev)
+    h = per[head]
+    line = {
+        "metric": h["metric"], "value": h["value"], "unit": UNIT,
+        "n_gpus": ranks.world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": h["ms_per_step"], "us_per_step": h["us_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": h["dtype"],
+        "data": "synthetic",
+        "frac_of_8TBps": h["frac_of_8TBps"], "frac_of_measured_hbm": h["frac_of_measured_hbm"],
+        "config": dict(h["config"], headline=("largest workload by KV bytes per step"
+                                              if args.workload == "all" else "the workload asked for")),
+        "roofline": h["roofline"],
+        "cpu_baseline": h["cpu_baseline"],
+        "e2e": h["e2e"],
+        "gpu_launches": h["gpu_launches"],
+        "clocks": h["clocks"],
+    }
+    if len(names) > 1:
+        keys = ("value", "us_per_step", "frac_of_8TBps", "frac_of_measured_hbm", "roofline",
+                "cpu_baseline", "e2e", "gpu_launches", "clocks", "dtype")
+        line["per_config"] = {n: (r if "skipped" in r else
+                                  dict({k: r[k] for k in keys}, kernel=r["config"]["kernel"],
+                                       kv_bytes_per_step=r["config"]["kv_bytes_per_step_per_gpu"]))
+                              for n, r in per.items()}
     if ranks.rank == 0:
         print(json.dumps(line), flush=True)
 
