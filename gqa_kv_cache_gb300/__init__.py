@@ -34,7 +34,7 @@ __all__ = ["decode_step", "decode_step_paged", "attend", "attend_paged", "decode
            "GqaError", "trace_enable", "trace_collect", "KERNELS", "library_path"]
 
 OK, INVALID_ARGUMENT, UNSUPPORTED, CUDA_ERROR, WORKSPACE = 0, 1, 2, 3, 4
-KERNELS = {"auto": 0, "simt": 1, "tc": 2}
+KERNELS = {"auto": 0, "simt": 1, "tc": 2, "unit": 3}
 STATUS_BITS = {1: "bad length", 2: "bad slot id", 4: "bad block", 8: "timeout", 16: "bad kept prefix",
                32: "bad token offsets"}
 _DTYPES = {torch.float32: 0, torch.bfloat16: 1}
@@ -70,11 +70,16 @@ def _ptr(t):
 
 
 def _opts(kernel, grid_ctas, sched_pad=None, sink=None, window=0, kept_prefix=0, device=None, B=None,
-          Hq=None, k_scale=None, v_scale=None, Hkv=None):
+          Hq=None, k_scale=None, v_scale=None, Hkv=None, wait_limit_cycles=0, test_stall=False):
     """The gqa_options struct. Softmax modifiers: ``sink`` a float32 (Hq,)
     device tensor, ``window`` an int >= 0, ``kept_prefix`` an int >= 0 or an
-    int32 (B,) device tensor."""
+    int32 (B,) device tensor. ``wait_limit_cycles`` > 0 shortens the
+    tensor-core consumers' wait for a tile to that many SM clock cycles and
+    ``test_stall`` makes each consumer's first wait one that runs out (both
+    for tests of the timeout path)."""
     o = _lib.GqaOptions()
+    o.wait_limit_cycles = int(wait_limit_cycles or 0)
+    o.test_stall = 1 if test_stall else 0
     o.kernel = KERNELS[kernel] if isinstance(kernel, str) else int(kernel)
     o.grid_ctas = int(grid_ctas)
     o.sched_pad = 0 if sched_pad is None else int(sched_pad) + 1   # 0 = library default
@@ -170,7 +175,8 @@ def _common_checks(q, k_new, v_new, caches, lengths, out, q_any_dtype=False):
 
 def decode_step(q, k_new, v_new, k_cache, v_cache, lengths, slot_ids=None, *, out=None,
                 status=None, kernel="auto", grid_ctas=0, workspace=None, stream=None, sched_pad=None,
-                sink=None, window=0, kept_prefix=0, k_scale=None, v_scale=None):
+                sink=None, window=0, kept_prefix=0, k_scale=None, v_scale=None,
+                wait_limit_cycles=0, test_stall=False):
     """One decode step on a dense (R, Hkv, Smax, D) cache (continuous batch
     when ``slot_ids`` is given). Appends in place; returns ``out``. A
     ``workspace`` passed in must be zero-filled before its first use (the
@@ -184,7 +190,8 @@ def decode_step(q, k_new, v_new, k_cache, v_cache, lengths, slot_ids=None, *, ou
         raise ValueError("shape mismatch between q, k_new, v_new and the caches")
     if slot_ids is not None and (slot_ids.dtype != torch.int32 or slot_ids.shape != (B,)):
         raise TypeError("slot_ids must be int32 of shape (B,)")
-    o = _opts(kernel, grid_ctas, sched_pad, sink, window, kept_prefix, q.device, B, Hq, k_scale, v_scale, Hkv)
+    o = _opts(kernel, grid_ctas, sched_pad, sink, window, kept_prefix, q.device, B, Hq, k_scale, v_scale, Hkv,
+              wait_limit_cycles, test_stall)
     lib = _lib.load()
     need = lib.gqa_workspace_bytes(B, Hq, Hkv, D, dt, ctypes.byref(o))
     ws = _workspace(q.device, need) if workspace is None else workspace
@@ -198,7 +205,8 @@ def decode_step(q, k_new, v_new, k_cache, v_cache, lengths, slot_ids=None, *, ou
 
 def decode_step_paged(q, k_new, v_new, k_blocks, v_blocks, block_table, lengths, *, out=None,
                       status=None, kernel="auto", grid_ctas=0, workspace=None, stream=None,
-                      sched_pad=None, sink=None, window=0, kept_prefix=0, k_scale=None, v_scale=None):
+                      sched_pad=None, sink=None, window=0, kept_prefix=0, k_scale=None, v_scale=None,
+                      wait_limit_cycles=0, test_stall=False):
     """One decode step on a paged cache (num_blocks, Hkv, block_size, D) with
     a (B, max_blocks) int32 block table (-1 = unused). Appends in place."""
     dt, out = _common_checks(q, k_new, v_new, (("k_blocks", k_blocks), ("v_blocks", v_blocks)),
@@ -211,7 +219,8 @@ def decode_step_paged(q, k_new, v_new, k_blocks, v_blocks, block_table, lengths,
             or not block_table.is_contiguous():
         raise TypeError("block_table must be a contiguous int32 (B, max_blocks) tensor")
     MB = block_table.shape[1]
-    o = _opts(kernel, grid_ctas, sched_pad, sink, window, kept_prefix, q.device, B, Hq, k_scale, v_scale, Hkv)
+    o = _opts(kernel, grid_ctas, sched_pad, sink, window, kept_prefix, q.device, B, Hq, k_scale, v_scale, Hkv,
+              wait_limit_cycles, test_stall)
     lib = _lib.load()
     need = lib.gqa_workspace_bytes(B, Hq, Hkv, D, dt, ctypes.byref(o))
     ws = _workspace(q.device, need) if workspace is None else workspace
@@ -226,7 +235,7 @@ def decode_step_paged(q, k_new, v_new, k_blocks, v_blocks, block_table, lengths,
 
 def attend(q, k_cache, v_cache, lengths, slot_ids=None, *, out=None, status=None, kernel="auto",
            grid_ctas=0, workspace=None, stream=None, sched_pad=None, sink=None, window=0,
-           kept_prefix=0, k_scale=None, v_scale=None):
+           kept_prefix=0, k_scale=None, v_scale=None, wait_limit_cycles=0, test_stall=False):
     """Read-only attend on a dense (R, Hkv, Smax, D) cache: slots
     ``0..lengths[b]-1`` (1 <= lengths[b] <= Smax), nothing written but ``out``.
     ``q`` (B, Hq, D) is float32 or bfloat16 whatever the cache dtype."""
@@ -238,7 +247,8 @@ def attend(q, k_cache, v_cache, lengths, slot_ids=None, *, out=None, status=None
         raise ValueError("shape mismatch between q and the caches")
     if slot_ids is not None and (slot_ids.dtype != torch.int32 or slot_ids.shape != (B,)):
         raise TypeError("slot_ids must be int32 of shape (B,)")
-    o = _opts(kernel, grid_ctas, sched_pad, sink, window, kept_prefix, q.device, B, Hq, k_scale, v_scale, Hkv)
+    o = _opts(kernel, grid_ctas, sched_pad, sink, window, kept_prefix, q.device, B, Hq, k_scale, v_scale, Hkv,
+              wait_limit_cycles, test_stall)
     lib = _lib.load()
     need = lib.gqa_workspace_bytes(B, Hq, Hkv, D, dt, ctypes.byref(o))
     ws = _workspace(q.device, need) if workspace is None else workspace
@@ -252,7 +262,8 @@ def attend(q, k_cache, v_cache, lengths, slot_ids=None, *, out=None, status=None
 
 def attend_paged(q, k_blocks, v_blocks, block_table, lengths, *, out=None, status=None,
                  kernel="auto", grid_ctas=0, workspace=None, stream=None, sched_pad=None,
-                 sink=None, window=0, kept_prefix=0, k_scale=None, v_scale=None):
+                 sink=None, window=0, kept_prefix=0, k_scale=None, v_scale=None,
+                wait_limit_cycles=0, test_stall=False):
     """Read-only attend on a paged cache (num_blocks, Hkv, block_size, D)."""
     dt, out = _common_checks(q, None, None, (("k_blocks", k_blocks), ("v_blocks", v_blocks)),
                              lengths, out, q_any_dtype=True)
@@ -263,7 +274,8 @@ def attend_paged(q, k_blocks, v_blocks, block_table, lengths, *, out=None, statu
     if block_table.dtype != torch.int32 or block_table.dim() != 2 or block_table.shape[0] != B \
             or not block_table.is_contiguous():
         raise TypeError("block_table must be a contiguous int32 (B, max_blocks) tensor")
-    o = _opts(kernel, grid_ctas, sched_pad, sink, window, kept_prefix, q.device, B, Hq, k_scale, v_scale, Hkv)
+    o = _opts(kernel, grid_ctas, sched_pad, sink, window, kept_prefix, q.device, B, Hq, k_scale, v_scale, Hkv,
+              wait_limit_cycles, test_stall)
     lib = _lib.load()
     need = lib.gqa_workspace_bytes(B, Hq, Hkv, D, dt, ctypes.byref(o))
     ws = _workspace(q.device, need) if workspace is None else workspace
@@ -287,7 +299,7 @@ def _multi_checks(q, k_new, v_new, caches, lengths, cu_q, out):
 def decode_multi(q, k_new, v_new, k_cache, v_cache, lengths, cu_q, slot_ids=None, *, max_q_len,
                  out=None, status=None, kernel="auto", grid_ctas=0, workspace=None, stream=None,
                  sched_pad=None, sink=None, window=0, kept_prefix=0, k_scale=None,
-                 v_scale=None):
+                 v_scale=None, wait_limit_cycles=0, test_stall=False):
     """Multi-token step on a dense (R, Hkv, Smax, D) cache: the packed tokens
     cu_q[b] .. cu_q[b+1]-1 of row b (q (T, Hq, D), k_new / v_new (T, Hkv, D))
     are appended at slots lengths[b] + i and token i attends slots
@@ -303,7 +315,8 @@ def decode_multi(q, k_new, v_new, k_cache, v_cache, lengths, cu_q, slot_ids=None
         raise ValueError("shape mismatch between q, k_new, v_new and the caches")
     if slot_ids is not None and (slot_ids.dtype != torch.int32 or slot_ids.shape != (B,)):
         raise TypeError("slot_ids must be int32 of shape (B,)")
-    o = _opts(kernel, grid_ctas, sched_pad, sink, window, kept_prefix, q.device, B, Hq, k_scale, v_scale, Hkv)
+    o = _opts(kernel, grid_ctas, sched_pad, sink, window, kept_prefix, q.device, B, Hq, k_scale, v_scale, Hkv,
+              wait_limit_cycles, test_stall)
     lib = _lib.load()
     need = lib.gqa_workspace_bytes_multi(B, Hq, Hkv, D, dt, int(max_q_len), ctypes.byref(o))
     ws = _workspace(q.device, need) if workspace is None else workspace
@@ -318,7 +331,7 @@ def decode_multi(q, k_new, v_new, k_cache, v_cache, lengths, cu_q, slot_ids=None
 def decode_multi_paged(q, k_new, v_new, k_blocks, v_blocks, block_table, lengths, cu_q, *, max_q_len,
                        out=None, status=None, kernel="auto", grid_ctas=0, workspace=None, stream=None,
                        sched_pad=None, sink=None, window=0, kept_prefix=0, k_scale=None,
-                       v_scale=None):
+                       v_scale=None, wait_limit_cycles=0, test_stall=False):
     """Multi-token step on a paged cache (num_blocks, Hkv, block_size, D)."""
     dt, out = _multi_checks(q, k_new, v_new, (("k_blocks", k_blocks), ("v_blocks", v_blocks)), lengths,
                             cu_q, out)
@@ -330,7 +343,8 @@ def decode_multi_paged(q, k_new, v_new, k_blocks, v_blocks, block_table, lengths
     if block_table.dtype != torch.int32 or block_table.dim() != 2 or block_table.shape[0] != B \
             or not block_table.is_contiguous():
         raise TypeError("block_table must be a contiguous int32 (B, max_blocks) tensor")
-    o = _opts(kernel, grid_ctas, sched_pad, sink, window, kept_prefix, q.device, B, Hq, k_scale, v_scale, Hkv)
+    o = _opts(kernel, grid_ctas, sched_pad, sink, window, kept_prefix, q.device, B, Hq, k_scale, v_scale, Hkv,
+              wait_limit_cycles, test_stall)
     lib = _lib.load()
     need = lib.gqa_workspace_bytes_multi(B, Hq, Hkv, D, dt, int(max_q_len), ctypes.byref(o))
     ws = _workspace(q.device, need) if workspace is None else workspace
@@ -398,7 +412,7 @@ def trace_enable(on: bool = True) -> bool:
 def trace_collect() -> dict:
     """{kernel name: (launches, total ms)} since the previous collect."""
     lib = _lib.load()
-    n = 2
+    n = 3
     launches = (ctypes.c_int64 * n)()
     ms = (ctypes.c_double * n)()
     _check(lib.gqa_trace_collect(n, launches, ms), "gqa_trace_collect")

@@ -40,7 +40,8 @@ SIGNATURES = {
 class GqaOptions(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int), ("grid_ctas", ctypes.c_int),
                 ("sched_pad", ctypes.c_int), ("window", ctypes.c_int),
-                ("kept_prefix", ctypes.c_int), ("reserved", ctypes.c_int * 3),
+                ("kept_prefix", ctypes.c_int), ("wait_limit_cycles", ctypes.c_int),
+                ("test_stall", ctypes.c_int), ("reserved", ctypes.c_int * 1),
                 ("head_sink", ctypes.c_void_p), ("kept_prefix_rows", ctypes.c_void_p),
                 ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p)]
 

@@ -20,7 +20,7 @@ BUILD = os.path.join(HERE, "_build")
 SOURCES = ["gqa_api.cu", "gqa_simt.cu", "gqa_simt_f32_small.cu", "gqa_simt_f32_large.cu",
            "gqa_simt_bf16_small.cu", "gqa_simt_bf16_large.cu", "gqa_simt_f32_small_plain.cu",
            "gqa_simt_f32_large_plain.cu", "gqa_simt_bf16_small_plain.cu", "gqa_simt_bf16_large_plain.cu",
-           "gqa_tc.cu", "gqa_tc_multi.cu",
+           "gqa_tc.cu", "gqa_tc_multi.cu", "gqa_unit.cu",
            "gqa_validate.cu",
            "gqa_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

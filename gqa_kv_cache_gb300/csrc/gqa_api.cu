@@ -1,5 +1,6 @@
 // The C ABI (include/gqa_decode.h): host-side argument checks, kernel
 // choice, workspace sizing, TMA descriptor encoding, launches and tracing.
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -14,34 +15,60 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int kDefaultSchedPad = 3;
+constexpr long long kDefaultWaitCycles = 4LL << 30;   // about 2 s at 2 GHz
 
 int sm_count(int dev)
 {
-    static int cache[kMaxDevices] = {0};
+    static std::atomic<int> cache[kMaxDevices];   // zero-initialised (static storage)
     if (dev < 0 || dev >= kMaxDevices)
         return 0;
-    if (!cache[dev]) {
-        int n = 0;
+    int n = cache[dev].load(std::memory_order_relaxed);
+    if (!n) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return 0;
-        cache[dev] = n;
+        cache[dev].store(n, std::memory_order_relaxed);
     }
-    return cache[dev];
+    return n;
 }
 
-// Kernel the call will use (GQA_KERNEL_SIMT / GQA_KERNEL_TC) or -1.
-int pick_kernel(const gqa_options *opt, gqa_dtype dt, int D, int G, bool paged, int block_size)
+// Whether the small-cache kernel takes the step: single-token, a float32 or
+// bfloat16 cache, and a row capacity whose K and V fit in shared memory
+// (cap_rows < 0: capacity unknown, no).
+bool unit_ok(gqa_dtype dt, int D, int G, long long cap_rows, bool multi)
+{
+    return !multi && cap_rows > 0 && (dt == GQA_DTYPE_F32 || dt == GQA_DTYPE_BF16) &&
+           unit_supports(dt == GQA_DTYPE_BF16, D, G, cap_rows);
+}
+
+// Kernel the call will use (GQA_KERNEL_SIMT / _TC / _UNIT) or -1. AUTO takes
+// the small-cache kernel when it applies and the units (B * Hkv, known > 0)
+// fit in one wave of it; else the tensor-core kernel where it applies, else
+// the CUDA-core one.
+int pick_kernel(const gqa_options *opt, gqa_dtype dt, int D, int G, bool paged, int block_size,
+                long long cap_rows = -1, bool multi = false, long long units = 0)
 {
     const int want = opt ? opt->kernel : GQA_KERNEL_AUTO;
     const bool bf16 = dt == GQA_DTYPE_BF16 || dt == GQA_DTYPE_E4M3;   // the tensor-core kernel's caches
     const bool tc_ok = tc_supports(bf16, D, G, paged, block_size);
     const bool simt_ok = dt != GQA_DTYPE_E4M3 && simt_supports(D, G);
+    const bool small_ok = unit_ok(dt, D, G, cap_rows, multi);
     if (want == GQA_KERNEL_TC)
         return tc_ok ? GQA_KERNEL_TC : -1;
     if (want == GQA_KERNEL_SIMT)
         return simt_ok ? GQA_KERNEL_SIMT : -1;
+    if (want == GQA_KERNEL_UNIT)
+        return small_ok ? GQA_KERNEL_UNIT : -1;
     if (want != GQA_KERNEL_AUTO)
         return -1;
+    if (small_ok && units > 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess) {
+            const long long wave =
+                (long long)sm_count(dev) * unit_ctas_per_sm(dt == GQA_DTYPE_BF16, D, G, cap_rows);
+            if (units <= wave)
+                return GQA_KERNEL_UNIT;
+        }
+    }
     if (tc_ok)
         return GQA_KERNEL_TC;
     return simt_ok ? GQA_KERNEL_SIMT : -1;
@@ -248,7 +275,7 @@ gqa_status run_step(const Shape &s, const void *q, const void *k_new, const void
         return GQA_ERR_INVALID_ARGUMENT;
     if (!aligned16(q) || !aligned16(kc) || !aligned16(vc) || !aligned16(out))
         return GQA_ERR_INVALID_ARGUMENT;
-    if (opt && (opt->window < 0 || opt->kept_prefix < 0 ||
+    if (opt && (opt->window < 0 || opt->kept_prefix < 0 || opt->wait_limit_cycles < 0 ||
                 (reinterpret_cast<uintptr_t>(opt->head_sink) & 3u) ||
                 (reinterpret_cast<uintptr_t>(opt->kept_prefix_rows) & 3u)))
         return GQA_ERR_INVALID_ARGUMENT;
@@ -257,17 +284,20 @@ gqa_status run_step(const Shape &s, const void *q, const void *k_new, const void
     const int Gh = s.Hq / s.Hkv;
     if (s.multi && Gh > 8)
         return GQA_ERR_UNSUPPORTED;
-    const int kernel = pick_kernel(opt, s.dt, s.D, Gh, s.paged, s.block_size);
+    const long long cap_rows = s.paged ? (long long)s.max_blocks * s.block_size : (long long)s.Smax;
+    const int kernel = pick_kernel(opt, s.dt, s.D, Gh, s.paged, s.block_size, cap_rows, s.multi,
+                                   (long long)s.B * s.Hkv);
     if (kernel < 0)
         return GQA_ERR_UNSUPPORTED;
     const MultiCut cut = s.multi ? multi_cut(Gh, s.max_q, kernel == GQA_KERNEL_TC ? 16 : 8) : MultiCut{1, 1};
     const int G = Gh * cut.tpc;             // query rows of a unit
     const int Bv = s.B * cut.chunks;        // (virtual) rows of the schedule
-    const int grid = grid_for(kernel, opt, s.dt, s.D, G);
+    const bool unit = kernel == GQA_KERNEL_UNIT;   // no schedule, no workspace
+    const int grid = unit ? s.B * s.Hkv : grid_for(kernel, opt, s.dt, s.D, G);
     if (grid <= 0)
         return GQA_ERR_CUDA;
     const WorkspaceLayout lay = workspace_layout(Bv, s.Hkv, G, s.D, grid);
-    if (!ws || ws_bytes < lay.bytes || (reinterpret_cast<uintptr_t>(ws) & 255u))
+    if (!unit && (!ws || ws_bytes < lay.bytes || (reinterpret_cast<uintptr_t>(ws) & 255u)))
         return GQA_ERR_WORKSPACE;
 
     DecodeParams p;
@@ -316,11 +346,15 @@ gqa_status run_step(const Shape &s, const void *q, const void *k_new, const void
     // about the time a CTA spends finishing a sequence, in tiles of streaming
     p.pad_tiles = (opt && opt->sched_pad > 0) ? opt->sched_pad - 1 : kDefaultSchedPad;
     p.grid = grid;
-    char *w = static_cast<char *>(ws);
-    p.ws_cnt = reinterpret_cast<int *>(w + lay.off_cnt);
-    p.ws_ml = reinterpret_cast<float *>(w + lay.off_ml);
-    p.ws_o = reinterpret_cast<float *>(w + lay.off_o);
+    if (!unit) {
+        char *w = static_cast<char *>(ws);
+        p.ws_cnt = reinterpret_cast<int *>(w + lay.off_cnt);
+        p.ws_ml = reinterpret_cast<float *>(w + lay.off_ml);
+        p.ws_o = reinterpret_cast<float *>(w + lay.off_o);
+    }
     p.status = d_status;
+    p.wait_cycles = (opt && opt->wait_limit_cycles > 0) ? (long long)opt->wait_limit_cycles : kDefaultWaitCycles;
+    p.test_stall = (opt && opt->test_stall) ? 1 : 0;
 
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     cudaError_t e;
@@ -341,6 +375,9 @@ gqa_status run_step(const Shape &s, const void *q, const void *k_new, const void
             return GQA_ERR_CUDA;
         TraceScope ts(1, cs);
         e = tc_launch(p, maps, cs);
+    } else if (unit) {
+        TraceScope ts(2, cs);
+        e = unit_launch(p, s.dt == GQA_DTYPE_BF16, cap_rows, cs);
     } else {
         TraceScope ts(0, cs);
         e = simt_launch(p, s.dt == GQA_DTYPE_BF16, cs);
@@ -373,6 +410,8 @@ size_t gqa_workspace_bytes(int B, int Hq, int Hkv, int D, gqa_dtype dt, const gq
     // the block size only matters for the paged form; 16 is the common case and
     // the workspace does not depend on it
     int kernel = pick_kernel(opt, dt, D, G, false, 16);
+    if (opt && opt->kernel == GQA_KERNEL_UNIT)
+        return 0;   // the small-cache kernel takes no workspace
     if (kernel < 0)
         return 0;
     int grid = grid_for(kernel, opt, dt, D, G);
@@ -620,6 +659,7 @@ const char *gqa_kernel_name(int kind)
     switch (kind) {
     case 0: return "simt_decode_kernel";
     case 1: return "tc_decode_kernel";
+    case 2: return "unit_decode_kernel";
     }
     return "unknown";
 }

@@ -96,6 +96,8 @@ struct DecodeParams {
     float *ws_ml;      // [P][G][2] partial (m, l), base-2 max
     float *ws_o;       // [P][G][D] partial unnormalised output
     int32_t *status;   // sticky content-error bits, may be null
+    long long wait_cycles;  // consumer warps: SM clock cycles before a wait for a tile gives up
+    int test_stall;         // 1: the consumers' first wait also waits on a barrier nothing completes
 };
 
 // Workspace layout (bytes from the workspace base), shared by host and device.

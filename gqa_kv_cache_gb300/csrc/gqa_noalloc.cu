@@ -13,7 +13,9 @@
 // its name is only a stand-in, not a device address, so the address is looked
 // up with cudaGetSymbolAddress once per device, with that device current, on
 // the first call made on that device; that first call should therefore come
-// before any stream capture. All calls share the one array and it keeps the
+// before any stream capture. The address is kept for the life of the process,
+// so the entry point must not be used on a device after cudaDeviceReset (or
+// anything else that destroys its primary context and reloads the module). All calls share the one array and it keeps the
 // last call's contents: calls whose kernels overlap on the GPU (two streams,
 // or two threads) race on it and must be serialised by the caller. Of the
 // scratch only the per-(row, head) arrival counters must start at zero (a

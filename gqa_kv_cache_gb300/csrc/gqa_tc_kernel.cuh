@@ -77,9 +77,16 @@
 // and a CTA-wide abort flag: the producer stops issuing and waits (bounded)
 // for its copies in flight; the consumer warps stop waiting and computing but
 // keep walking their tiles and taking part in every barrier, writing NaN.
+// The consumers' limit on a wait for a tile is a launch parameter (about 2 s
+// by default), the producer's waits always keep the full limit. For tests of
+// this path a launch can also make each consumer warp's first wait include a
+// barrier that nothing completes, so that wait runs out after the (shortened)
+// limit whatever the timing of the copies.
 #pragma once
 
 #include <cuda_fp16.h>
+
+#include <atomic>
 
 #include "gqa_common.cuh"
 #include "gqa_launch.h"
@@ -158,14 +165,43 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
-// Bounded wait; false when it gave up.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
+// The same test with a suspend-time hint of `ns` nanoseconds: the thread
+// sleeps at most about that long before the test answers.
+__device__ __forceinline__ bool mbar_try_ns(uint32_t bar, uint32_t parity, uint32_t ns)
 {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(bar), "r"(parity), "r"(ns)
+                 : "memory");
+    return ok != 0;
+}
+
+// Limits below this are honoured to the cycle: the wait then polls with a
+// one-nanosecond suspend hint instead of letting a test sleep for the
+// hardware's own time limit first.
+constexpr long long kShortWait = 1LL << 20;
+
+// Bounded wait: false when it gave up after `limit` SM clock cycles or, with
+// `abort` given, as soon as *abort is set.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long long limit = kWaitCycles,
+                                          const int *abort = nullptr)
+{
+    if (limit < kShortWait) {
+        const long long t0 = clock64();
+        while (!mbar_try_ns(bar, parity, 1u)) {
+            if (clock64() - t0 > limit || (abort && *((const volatile int *)abort)))
+                return false;
+        }
+        return true;
+    }
     if (mbar_try(bar, parity))
         return true;
     const long long t0 = clock64();
     while (!mbar_try(bar, parity)) {
-        if (clock64() - t0 > kWaitCycles)
+        if (clock64() - t0 > limit || (abort && *((const volatile int *)abort)))
             return false;
     }
     return true;
@@ -297,6 +333,7 @@ struct Shared {
     static constexpr int kOPad = 4;   // rows 132 floats apart: the epilogue's stores are conflict-free
     uint64_t full[NS];
     uint64_t empty[NS];
+    uint64_t stall;      // a barrier nothing completes (tests of the timeout path)
     int stage_bad[NS];
     int abort_flag;
     int last_flag;
@@ -345,6 +382,7 @@ __global__ void __launch_bounds__(kThreads, (Ring<QF32, KV8, MULTI, M16>::kCtas)
             sh.stage_bad[s] = 0;
         }
         sh.abort_flag = 0;
+        mbar_init(smem_u32(&sh.stall), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == kConsumerWarps && lane == 0) {
@@ -413,10 +451,13 @@ __global__ void __launch_bounds__(kThreads, (Ring<QF32, KV8, MULTI, M16>::kCtas)
         int issued = 0;
         Plan pl = more ? plan(cur) : Plan{-1, 0, false, false};
         while (more) {
-            if (*((volatile int *)&sh.abort_flag))
+            // every decision below is warp-uniform (the loop uses warp votes)
+            if (__any_sync(0xffffffffu, *((volatile int *)&sh.abort_flag) != 0))
                 break;
-            if (!mbar_wait(smem_u32(&sh.empty[stage]), phase ^ 1)) {
-                if (lane == 0) {
+            // (a wait for a free stage also ends when the consumers have aborted)
+            if (!__all_sync(0xffffffffu,
+                            mbar_wait(smem_u32(&sh.empty[stage]), phase ^ 1, kWaitCycles, &sh.abort_flag))) {
+                if (lane == 0 && !*((volatile int *)&sh.abort_flag)) {
                     report(p, kTimeout);
                     atomicExch(&sh.abort_flag, 1);
                 }
@@ -482,8 +523,16 @@ __global__ void __launch_bounds__(kThreads, (Ring<QF32, KV8, MULTI, M16>::kCtas)
         }
         // every tile is issued: the next kernel on the stream may start launching
         asm volatile("griddepcontrol.launch_dependents;");
-        // Abort path only: let every copy still in flight land before exit.
-        if (*((volatile int *)&sh.abort_flag)) {
+        // Let every copy still in flight land before the producer exits, so
+        // that no CTA can end while one of its copies is still writing into
+        // its shared memory (consumers that gave up on a wait no longer hold
+        // the CTA open until their tiles land). At most kNS stages are in
+        // flight (a stage is refilled only after the consumers released it,
+        // i.e. after its copies landed), and the last min(kNS, issued) issued
+        // stages are exactly those; each wait keeps the full limit, whatever
+        // the consumers' limit. Without an abort these waits end as the
+        // tiles land, which the consumers wait for anyway.
+        {
             int s = stage, ph = phase;
             for (int k = 0; k < kNS && k < issued; ++k) {
                 if (--s < 0) {
@@ -519,6 +568,7 @@ __global__ void __launch_bounds__(kThreads, (Ring<QF32, KV8, MULTI, M16>::kCtas)
     int seg_first_t = 0;
     int pre_cnt = -1;                    // thread 0: the unit's arrival count near the segment's end
     bool seg_start = true, row_good = true, aborted = false;
+    bool stall = p.test_stall != 0;      // the first wait also waits on sh.stall (runs out)
     int seg_bad = 0;
     // multi-token units only: this lane's rows g0 and g0 + 8 (last slot,
     // window start, softmax state of the second), rows with data
@@ -573,9 +623,16 @@ __global__ void __launch_bounds__(kThreads, (Ring<QF32, KV8, MULTI, M16>::kCtas)
 
         // After an abort every warp keeps walking its tiles and taking part in
         // every barrier, but waits for and computes nothing (outputs NaN).
+        // The outcome is made warp-uniform: a lane that gave up makes the
+        // whole warp give up (the products below are warp-wide).
         bool have = false;
-        if (!aborted && !*((volatile int *)&sh.abort_flag)) {
-            have = mbar_wait(smem_u32(&sh.full[stage]), phase);
+        if (!aborted && !__any_sync(0xffffffffu, *((volatile int *)&sh.abort_flag) != 0)) {
+            bool ok = mbar_wait(smem_u32(&sh.full[stage]), phase, p.wait_cycles);
+            if (stall) {   // tests of the timeout path: a wait that nothing ends
+                ok = ok && mbar_wait(smem_u32(&sh.stall), 0, p.wait_cycles);
+                stall = false;
+            }
+            have = __all_sync(0xffffffffu, ok);
             if (!have && lane == 0) {
                 report(p, kTimeout);
                 atomicExch(&sh.abort_flag, 1);
@@ -1177,13 +1234,21 @@ template <bool QF32, bool WIN, bool MULTI, bool KV8 = false, bool M16 = false>
 cudaError_t launch_q(const DecodeParams &p, const TcMaps &maps, cudaStream_t st)
 {
     constexpr int kDynSmem = Ring<QF32, KV8, MULTI, M16>::kDynSmem;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(tc_decode_kernel<QF32, WIN, MULTI, KV8, M16>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem);
+    // The shared-memory limit is a per-device attribute of the kernel: set it
+    // once on every device this instantiation is launched on (a bit per
+    // device; devices beyond 64 set it on every launch).
+    static std::atomic<unsigned long long> attr_set{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+    if (!bit || !(attr_set.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(tc_decode_kernel<QF32, WIN, MULTI, KV8, M16>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem);
         if (e != cudaSuccess)
             return e;
-        attr_set = true;
+        attr_set.fetch_or(bit, std::memory_order_acq_rel);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.grid);

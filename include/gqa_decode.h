@@ -101,8 +101,15 @@ typedef enum gqa_kernel {
     GQA_KERNEL_AUTO = 0, /* the fastest kernel that supports the shapes                  */
     GQA_KERNEL_SIMT = 1, /* CUDA-core FMA kernel: any D in {1,2,4,...,256}, G <= 8,
                             float32 or bfloat16, any block size                          */
-    GQA_KERNEL_TC = 2    /* TMA ring + tensor-core kernel: bfloat16, D = 128, G <= 8,
+    GQA_KERNEL_TC = 2,   /* TMA ring + tensor-core kernel: bfloat16, D = 128, G <= 8,
                             block size a power of two >= 8                               */
+    GQA_KERNEL_UNIT = 3  /* small caches: one CTA per (row, cache head), the row's attended
+                            slots staged in shared memory by bulk copies, no workspace
+                            used: float32 or bfloat16, D in {32, 64, 128, 256}, G <= 8,
+                            2 * capacity * D * element size <= 200 KB (capacity = Smax,
+                            or max_blocks * block_size); single-token steps (decode and
+                            attend). AUTO takes it when those hold and the (row, head)
+                            pairs fit in one wave of the GPU                             */
 } gqa_kernel;
 
 /* Launch options (all zero = defaults). */
@@ -127,7 +134,19 @@ typedef struct gqa_options {
      * scores: w_j = e^{s_j} / (e^{sink_h} + sum_{i attended} e^{s_i}).        */
     int window;       /* >= 0 (0: no window); < 0 is GQA_ERR_INVALID_ARGUMENT          */
     int kept_prefix;  /* P >= 0 for every row, used when kept_prefix_rows is NULL       */
-    int reserved[3];
+    int wait_limit_cycles; /* 0: the default (about 2 s). c > 0: a tensor-core consumer
+                       warp's wait for a tile to land gives up after c SM clock cycles;
+                       its CTA then aborts (the units it touches get NaN, their appends
+                       may be skipped, GQA_STATUS_TIMEOUT is set), every copy it issued
+                       still lands before it exits, and the workspace is left
+                       zero-filled. For tests of the timeout path; < 0 is
+                       GQA_ERR_INVALID_ARGUMENT                                        */
+    int test_stall;   /* 0: off. 1 (tests of the timeout path): every tensor-core
+                       consumer warp's first wait for a tile also waits on an on-chip
+                       barrier that nothing completes, so that wait runs out after
+                       wait_limit_cycles (keep it short) and every CTA aborts as
+                       described above                                                 */
+    int reserved[1];
     const float *head_sink;          /* (device) (Hq,) float32 logits, or NULL          */
     const int32_t *kept_prefix_rows; /* (device) (B,) int32 P per batch row, or NULL;
                                         a negative entry makes that row bad
@@ -144,7 +163,9 @@ const char *gqa_status_string(gqa_status s);
  * Workspace bytes a decode step needs on the current device for these sizes
  * (one arrival counter per (row, cache head) and the float32 partial softmax
  * states of the sequences that several CTAs share). opt may be NULL. Returns
- * 0 for invalid sizes.
+ * 0 for invalid sizes, and 0 when opt asks for GQA_KERNEL_UNIT (that kernel
+ * takes no workspace: NULL may then be passed). Under GQA_KERNEL_AUTO the
+ * size covers whichever kernel the call may take.
  *
  * The workspace must be zero-filled (gqa_workspace_reset or any memset)
  * before its first use; every call leaves it zero-filled again, whatever the
@@ -377,8 +398,11 @@ const char *gqa_kernel_name(int kind);
  * (gqa_workspace_bytes) exceeds it return GQA_ERR_TOO_LARGE before any launch.
  * The call allocates nothing. The first call on a device looks up the array's
  * device address (cudaGetSymbolAddress) with that device current; make that
- * first call before any stream capture. All calls share the array: calls whose
- * kernels overlap on the GPU race and must be serialised by the caller.
+ * first call before any stream capture. The address is kept for the life of
+ * the process: do not use this entry point on a device after cudaDeviceReset
+ * (or anything else that destroys its primary context) in the same process.
+ * All calls share the array: calls whose kernels overlap on the GPU race and
+ * must be serialised by the caller.
  */
 size_t gqa_noalloc_scratch_bytes(void);
 gqa_status gqa_decode_step_noalloc(const void *q, const void *k_new, const void *v_new,

@@ -115,3 +115,30 @@ def test_binding_raises_without_gpu_tensors():
     q = torch.zeros(1, 2, 8)
     with pytest.raises(ValueError):
         gqa.decode_step(q, q[:, :1], q[:, :1], q[None], q[None], torch.zeros(1, dtype=torch.int32))
+
+
+def test_options_struct_layout_matches_the_header(tmp_path):
+    """The binding's gqa_options has the header's size and field offsets."""
+    from gqa_kv_cache_gb300 import _lib
+    fields = [f[0] for f in _lib.GqaOptions._fields_ if f[0] != "reserved"]
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "gqa_decode.h"\nint main(void) {\n'
+                   '  printf("%zu\\n", sizeof(gqa_options));\n'
+                   + "".join(f'  printf("%zu\\n", offsetof(gqa_options, {f}));\n' for f in fields)
+                   + "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.check_call(["gcc", "-I", os.path.join(ROOT, "include"), "-o", str(exe), str(src)])
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    assert got[0] == ctypes.sizeof(_lib.GqaOptions)
+    assert got[1:] == [getattr(_lib.GqaOptions, f).offset for f in fields]
+
+
+def test_negative_wait_limit_is_refused(lib):
+    """A negative consumer wait limit is an argument error, found before any launch."""
+    from gqa_kv_cache_gb300 import _lib
+    P = lambda x: ctypes.c_void_p(x * 256)
+    o = _lib.GqaOptions()
+    o.wait_limit_cycles = -1
+    code = lib.gqa_decode_step_ex(P(1), P(1), P(1), P(1), P(1), P(1), None, P(1), 2, 8, 2, 128, 2, 16, 1,
+                                  None, 0, None, None, ctypes.byref(o))
+    assert code == 1

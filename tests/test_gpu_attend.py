@@ -18,18 +18,13 @@ import torch
 
 import oracle
 import workloads as W
-from gpu_cases import BF16_REL_TOL, F32_TOL, attended_vmax, host_problem
+from gpu_cases import BF16_REL_TOL, F32_TOL, attended_vmax, guard, host_problem, path_of, supports
 from helpers import to_np
 
 pytestmark = pytest.mark.gpu
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 F32Q_REL_TOL = 2e-4
-
-
-def _supports_tc(w):
-    return w.dtype == "bf16" and w.D == 128 and w.G <= 8 and (
-        not w.paged or (w.block_size >= 8 and (w.block_size & (w.block_size - 1)) == 0))
 
 
 def inputs(w, q_f32, gpu_gen=False):
@@ -85,7 +80,9 @@ def check_attend(w, q_f32, kernel="auto", grid_ctas=0, rows=None, gpu_gen=False)
     want = run_oracle(w, prob)
     got = out[torch.tensor(prob["rows"], device="cuda")].double().cpu().numpy()
     assert np.isfinite(got).all()
-    return float(np.abs(got - want).max()), tolerance(w, q_f32, attended_vmax(prob)), out
+    err, vmax = float(np.abs(got - want).max()), attended_vmax(prob)
+    guard(path_of(w, kernel, q_f32=q_f32), err, vmax)
+    return err, tolerance(w, q_f32, vmax), out
 
 
 # ------------------------------------------------------------ page examples
@@ -126,19 +123,19 @@ SMALL = [
 ]
 
 
-@pytest.mark.parametrize("kernel", ["simt", "tc"])
+@pytest.mark.parametrize("kernel", ["simt", "tc", "unit"])
 @pytest.mark.parametrize("q_f32", [True, False], ids=["q_f32", "q_cache_dtype"])
 @pytest.mark.parametrize("name,base,kw", SMALL, ids=[s[0] for s in SMALL])
 @pytest.mark.parametrize("grid_ctas", [0, 7])
 def test_attend_small_cases(name, base, kw, q_f32, kernel, grid_ctas):
     w = W.small(base, **kw)
-    if kernel == "tc" and not _supports_tc(w):
+    if not supports(kernel, w):
         pytest.skip("kernel does not take these sizes")
     err, tol, _ = check_attend(w, q_f32, kernel, grid_ctas)
     assert err <= tol, f"max abs error {err} > {tol}"
 
 
-@pytest.mark.parametrize("kernel", ["simt", "tc"])
+@pytest.mark.parametrize("kernel", ["simt", "tc", "unit"])
 def test_bf16_query_over_f32_cache_and_mixed(kernel):
     """A bfloat16 query over a float32 cache (CUDA-core kernel only) matches
     the oracle at the float32 bar."""
@@ -154,7 +151,7 @@ def test_bf16_query_over_f32_cache_and_mixed(kernel):
     assert np.abs(out.double().cpu().numpy() - want).max() <= F32_TOL
 
 
-@pytest.mark.parametrize("kernel", ["simt", "tc"])
+@pytest.mark.parametrize("kernel", ["simt", "tc", "unit"])
 def test_attend_one_slot_and_full(kernel):
     """lengths 1 (every head returns slot 0's value exactly) and lengths Smax."""
     import gqa_kv_cache_gb300 as gqa
@@ -169,7 +166,7 @@ def test_attend_one_slot_and_full(kernel):
         assert torch.equal(out[b], t["v_cache"][b, :, 0].float().repeat_interleave(w.G, 0))
 
 
-@pytest.mark.parametrize("kernel", ["simt", "tc"])
+@pytest.mark.parametrize("kernel", ["simt", "tc", "unit"])
 def test_attend_stale_nan(kernel):
     """NaN / Inf at and beyond lengths[b] cannot change a single output bit."""
     w = W.small("llama3_8b", B=4, Smax=400, len_lo=0, len_hi=398, seed=221)
@@ -184,13 +181,15 @@ def test_attend_stale_nan(kernel):
         assert torch.equal(run_gpu(w, t2, kernel), ref)
 
 
-@pytest.mark.parametrize("kernel", ["simt", "tc"])
+@pytest.mark.parametrize("kernel", ["simt", "tc", "unit"])
 def test_attend_after_decode_step_is_bit_identical(kernel):
     """A decode step appends slot L and attends 0..L; the read-only attend of
     the resulting cache with lengths L + 1 attends the same slots and must
     return the same bits (bfloat16 query for both)."""
     import gqa_kv_cache_gb300 as gqa
     w = W.small("llama3_8b", B=5, Smax=700, len_lo=0, len_hi=698, seed=222)
+    if not supports(kernel, w):
+        w = W.small("llama3_8b", B=5, Smax=400, len_lo=0, len_hi=398, seed=222)
     t = {k: v.cuda() for k, v in W.generate(w).items()}
     dec = gqa.decode_step(t["q"], t["k_new"], t["v_new"], t["k_cache"], t["v_cache"], t["lengths"],
                           kernel=kernel).clone()
@@ -198,7 +197,7 @@ def test_attend_after_decode_step_is_bit_identical(kernel):
     assert torch.equal(dec, att)
 
 
-@pytest.mark.parametrize("kernel", ["simt", "tc"])
+@pytest.mark.parametrize("kernel", ["simt", "tc", "unit"])
 def test_attend_bad_lengths(kernel):
     """lengths 0 and Smax + 1 are bad rows: NaN outputs and the length bit;
     the other rows are unaffected; gqa_validate_attend rejects the content."""

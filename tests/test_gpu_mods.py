@@ -14,15 +14,10 @@ import torch
 
 import oracle
 import workloads as W
-from gpu_cases import attended_vmax, host_problem, make_inputs, tolerance
+from gpu_cases import attended_vmax, host_problem, make_inputs, supports, tolerance
 from helpers import to_np
 
 pytestmark = pytest.mark.gpu
-
-
-def _tc_ok(w):
-    return w.dtype == "bf16" and w.D == 128 and w.G <= 8 and (
-        not w.paged or (w.block_size >= 8 and (w.block_size & (w.block_size - 1)) == 0))
 
 
 def _gpu(w, t, attend, kernel, grid, mods, status=None):
@@ -90,19 +85,23 @@ CASES = [
     ("bf16_slots", "ragged_slots", dict(B=6, R=11, Smax=600, len_lo=1, len_hi=599, seed=302)),
     ("bf16_paged16", "paged", dict(B=5, num_blocks=5 * 40, max_blocks=40, len_lo=0, len_hi=639, seed=303)),
     ("f32_d64", "pr1_fp32", dict(B=3, Smax=300, len_lo=0, len_hi=299, seed=304)),
+    # capacities the small-cache kernel stages whole
+    ("bf16_dense_cap380", "llama3_8b", dict(B=5, Smax=380, len_lo=0, len_hi=379, seed=305)),
+    ("bf16_paged16_cap384", "paged", dict(B=5, num_blocks=5 * 24, max_blocks=24, len_lo=0, len_hi=383,
+                                          seed=306)),
 ]
 MODS = ["sink", "window1", "window64", "window100_prefix10", "window70_prefix200",
         "window37_prefix_rows_sink"]
 
 
-@pytest.mark.parametrize("kernel", ["simt", "tc"])
+@pytest.mark.parametrize("kernel", ["simt", "tc", "unit"])
 @pytest.mark.parametrize("attend", [False, True], ids=["decode", "attend"])
 @pytest.mark.parametrize("mod", MODS)
 @pytest.mark.parametrize("name,base,kw", CASES, ids=[c[0] for c in CASES])
 @pytest.mark.parametrize("grid", [0, 7])
 def test_mods_against_oracle(name, base, kw, mod, attend, kernel, grid):
     w = W.small(base, **kw)
-    if kernel == "tc" and not _tc_ok(w):
+    if not supports(kernel, w):
         pytest.skip("kernel does not take these sizes")
     t = _inputs(w, attend)
     mods = _mods(mod, w, kw["seed"])
@@ -128,12 +127,14 @@ def test_mods_against_oracle(name, base, kw, mod, attend, kernel, grid):
         assert to_np(t[n][idx]).tobytes() == prob[n].tobytes()
 
 
-@pytest.mark.parametrize("kernel", ["simt", "tc"])
+@pytest.mark.parametrize("kernel", ["simt", "tc", "unit"])
 def test_masked_region_never_matters(kernel):
     """NaN in every slot outside the window and the kept prefix (below the
     query position) changes no output bit: those tiles are not read, and the
     masked rows of partly covered tiles are masked by selection and zeroed."""
     w = W.small("llama3_8b", B=4, Smax=900, len_lo=300, len_hi=899, seed=310)
+    if not supports(kernel, w):
+        w = W.small("llama3_8b", B=4, Smax=400, len_lo=250, len_hi=399, seed=310)
     t = make_inputs(w)
     mods = dict(window=150, kept_prefix=20)
     ref = _gpu(w, {k: v.clone() for k, v in t.items()}, False, kernel, 0, mods).clone()
@@ -147,12 +148,14 @@ def test_masked_region_never_matters(kernel):
     assert torch.equal(out, ref)
 
 
-@pytest.mark.parametrize("kernel", ["simt", "tc"])
+@pytest.mark.parametrize("kernel", ["simt", "tc", "unit"])
 def test_paged_blocks_outside_window_may_be_unmapped(kernel):
     """Table entries whose blocks hold no attended slot (between the kept
     prefix and the window) may be -1: the result is the same bits and no
     status bit is set."""
     w = W.small("paged", B=4, num_blocks=4 * 60, max_blocks=60, len_lo=500, len_hi=959, seed=311)
+    if not supports(kernel, w):
+        w = W.small("paged", B=4, num_blocks=4 * 25, max_blocks=25, len_lo=300, len_hi=399, seed=311)
     t = make_inputs(w)
     mods = dict(window=100, kept_prefix=16)
     ref = _gpu(w, {k: v.clone() for k, v in t.items()}, False, kernel, 0, mods).clone()
@@ -171,7 +174,7 @@ def test_paged_blocks_outside_window_may_be_unmapped(kernel):
     assert torch.equal(out, ref)
 
 
-@pytest.mark.parametrize("kernel", ["simt", "tc"])
+@pytest.mark.parametrize("kernel", ["simt", "tc", "unit"])
 def test_negative_prefix_row_is_bad(kernel):
     w = W.small("llama3_8b", B=3, Smax=300, len_lo=100, len_hi=299, seed=312)
     t = make_inputs(w)

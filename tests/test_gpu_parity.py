@@ -12,19 +12,12 @@ import torch
 
 import oracle
 import workloads as W
-from gpu_cases import check_step, make_inputs, run_gpu, host_problem, run_oracle, tolerance, attended_vmax
+from gpu_cases import check_step, make_inputs, run_gpu, host_problem, run_oracle, supports, tolerance, attended_vmax
 from helpers import to_np
 
 pytestmark = pytest.mark.gpu
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
-
-
-def _supports(kernel, w):
-    if kernel == "simt":
-        return True
-    return w.dtype == "bf16" and w.D == 128 and w.G <= 8 and (
-        not w.paged or (w.block_size >= 8 and (w.block_size & (w.block_size - 1)) == 0))
 
 
 # ------------------------------------------------------------ page examples
@@ -89,18 +82,18 @@ SMALL = [
 ]
 
 
-@pytest.mark.parametrize("kernel", ["simt", "tc"])
+@pytest.mark.parametrize("kernel", ["simt", "tc", "unit"])
 @pytest.mark.parametrize("name,base,kw", SMALL, ids=[s[0] for s in SMALL])
 @pytest.mark.parametrize("grid_ctas", [0, 1, 7])
 def test_small_cases(name, base, kw, kernel, grid_ctas):
     w = W.small(base, **kw)
-    if not _supports(kernel, w):
+    if not supports(kernel, w):
         pytest.skip("kernel does not take these sizes")
     err, tol, _ = check_step(w, kernel=kernel, grid_ctas=grid_ctas)
     assert err <= tol, f"max abs error {err} > {tol}"
 
 
-@pytest.mark.parametrize("kernel", ["simt", "tc"])
+@pytest.mark.parametrize("kernel", ["simt", "tc", "unit"])
 def test_lengths_zero_and_full(kernel):
     """Rows with an empty cache (output = v_new) and rows at capacity - 1."""
     w = W.small("llama3_8b", B=4, Smax=256, len_lo=0, len_hi=0, seed=120)
@@ -117,7 +110,7 @@ def test_lengths_zero_and_full(kernel):
         assert torch.equal(out[b], vn[b].repeat_interleave(w.G, 0))
 
 
-@pytest.mark.parametrize("kernel", ["simt", "tc"])
+@pytest.mark.parametrize("kernel", ["simt", "tc", "unit"])
 def test_stale_slots_nan(kernel):
     """NaN / Inf in every stale slot and in the (stale) append slot cannot
     change a single output bit."""
@@ -135,11 +128,13 @@ def test_stale_slots_nan(kernel):
         assert torch.equal(out, ref)
 
 
-@pytest.mark.parametrize("kernel", ["simt", "tc"])
+@pytest.mark.parametrize("kernel", ["simt", "tc", "unit"])
 def test_paged_unused_blocks_nan(kernel):
     """Blocks the table does not name, and the unused tail of the last block,
     hold NaN: the output must equal the clean run bit for bit."""
     w = W.small("paged", B=4, num_blocks=4 * 30 + 17, max_blocks=30, len_lo=0, len_hi=479, seed=122)
+    if not supports(kernel, w):
+        w = W.small("paged", B=4, num_blocks=4 * 20 + 17, max_blocks=20, len_lo=0, len_hi=319, seed=122)
     t = make_inputs(w)
     ref = run_gpu(w, {k: v.clone() for k, v in t.items()}, kernel).clone()
     used = set(t["block_table"][t["block_table"] >= 0].tolist())
@@ -193,7 +188,7 @@ def test_bad_content_reports_and_never_faults():
     assert not gqa.validate(t["lengths"], slot_ids=t["slot_ids"], R=w.R, Smax=w.Smax)
 
 
-@pytest.mark.parametrize("kernel", ["simt", "tc"])
+@pytest.mark.parametrize("kernel", ["simt", "tc", "unit"])
 def test_bad_block_reports(kernel):
     w = W.small("paged", B=3, num_blocks=3 * 20, max_blocks=20, len_lo=100, len_hi=300, seed=131)
     t = make_inputs(w)
@@ -238,8 +233,8 @@ def test_empty_batch_and_errors():
     q = torch.zeros(1, 8, 128, dtype=torch.bfloat16, device="cuda")
     kv = torch.zeros(1, 2, 128, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(gqa.GqaError):
-        gqa.decode_step(q, kv, kv, c, c, torch.zeros(1, dtype=torch.int32, device="cuda"),
-                        workspace=torch.zeros(16, dtype=torch.uint8, device="cuda"))
+        gqa.decode_step(q, kv, kv, c, c, torch.zeros(1, dtype=torch.int32, device="cuda"), kernel="tc",
+                        workspace=torch.zeros(16, dtype=torch.uint8, device="cuda"))   # too small a workspace
 
 
 # ----------------------------------------------------- full-size workloads

@@ -61,18 +61,26 @@ def test_noalloc_matches_regular_entry_point(w):
     torch.cuda.synchronize()
     vmax = float(t["v_cache"].float().abs().max().item())
     tol = F32_TOL if w.dtype == "f32" else BF16_REL_TOL * vmax
-    kc0 = t["k_cache"].clone()
+    kc0, vc0 = t["k_cache"].clone(), t["v_cache"].clone()
     for call in range(2):
         out = torch.full_like(ref, float("nan"))
         assert _noalloc(lib, t, w, out, stream) == 0
         torch.cuda.synchronize()
         err = (out - ref).abs().max().item()
         assert err <= tol, f"call {call}: max abs error {err} > {tol}"
-    # the append happened in place (one slot per row and head), as with the regular call
+        if call == 0:
+            # a regular call on its own workspace in between leaves the shared scratch alone
+            mid = torch.empty_like(ref)
+            assert _regular(lib, {k: v.clone() for k, v in t.items()}, w, mid, stream) == 0
+            torch.cuda.synchronize()
+            assert (mid - ref).abs().max().item() <= tol
+    # the append happened in place (one slot per row and head, K and V), as with the regular call
     L = t["lengths"].long()
     rows = t["slot_ids"].long() if "slot_ids" in t else torch.arange(w.B, device="cuda")
     kc0[rows, :, L] = t["k_new"]
+    vc0[rows, :, L] = t["v_new"]
     assert torch.equal(kc0, t["k_cache"])
+    assert torch.equal(vc0, t["v_cache"])
 
 
 def test_noalloc_refuses_sizes_beyond_its_scratch():
