@@ -25,3 +25,18 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+def pytest_sessionfinish(session, exitstatus):
+    """With GQA_ERR_LOG set, the parity cases' observed errors (relative to
+    max|V|, per arithmetic path) are written there as JSON lines."""
+    path = os.environ.get("GQA_ERR_LOG")
+    if not path:
+        return
+    mod = sys.modules.get("gpu_cases")
+    if mod is None:
+        return
+    import json
+    with open(path, "w") as f:
+        for test, p, rel in mod.OBSERVED:
+            f.write(json.dumps({"test": test, "path": p, "rel": rel}) + "\n")

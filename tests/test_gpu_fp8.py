@@ -12,7 +12,7 @@ import torch
 
 import oracle
 import workloads as W
-from gpu_cases import BF16_REL_TOL, host_problem
+from gpu_cases import BF16_REL_TOL, guard, host_problem, path_of
 from helpers import to_np
 
 pytestmark = pytest.mark.gpu
@@ -52,12 +52,26 @@ def _oracle(w, prob, attend, ks, vs, **mods):
     return r.out
 
 
-def _vmax(t, w):
-    v = t["v_blocks"] if w.paged else t["v_cache"]
-    vmax = (v.view(torch.float8_e4m3fn).float() * t["v_scale"].view(1, -1, 1, 1)).abs().max().item()
-    if "v_new" in t:
-        vmax = max(vmax, t["v_new"].float().abs().max().item())
-    return vmax
+def _vmax(t, w, prob):
+    """max |V| over the values the call attends (the valid slots of the
+    compared rows, dequantised, and the new values)."""
+    v = prob["v_blocks"] if w.paged else prob["v_cache"]
+    vs = t["v_scale"].cpu().numpy()
+    vf = torch.from_numpy(v).view(torch.float8_e4m3fn).double().numpy() * vs.reshape(1, -1, 1, 1)
+    L = prob["lengths"]
+    vals = [float(t["v_new"].float().abs().max().item())] if "v_new" in t else [0.0]
+    # cached valid slots of row i: lengths[i] (decode: 0..L-1 and the new
+    # value; attend: its L valid slots)
+    if w.paged:
+        bs = vf.shape[2]
+        for i in range(len(L)):
+            for s in range(int(L[i])):
+                vals.append(float(np.abs(vf[prob["block_table"][i, s // bs], :, s % bs]).max()))
+    else:
+        for i in range(len(L)):
+            if int(L[i]) > 0:
+                vals.append(float(np.abs(vf[i, :, :int(L[i])]).max()))
+    return max(vals)
 
 
 def check_fp8(w, attend=False, q_f32=False, kernel="auto", grid=0, rows=None, gpu_gen=False, **mods):
@@ -80,8 +94,10 @@ def check_fp8(w, attend=False, q_f32=False, kernel="auto", grid=0, rows=None, gp
     got = out[sel].double().cpu().numpy()
     assert np.isfinite(got).all()
     err = float(np.abs(got - want).max())
-    tol = BF16_REL_TOL * _vmax(t, w)
+    vmax = _vmax(t, w, prob)
+    tol = BF16_REL_TOL * vmax
     assert err <= tol, f"max abs error {err} > {tol}"
+    guard(path_of(w, kernel, fp8=True), err, vmax)
     if attend:
         for n in names:
             assert torch.equal(before[n], t[n]), f"{n} written by a read-only attend"

@@ -15,7 +15,7 @@ import torch
 
 import oracle
 import workloads as W
-from gpu_cases import BF16_REL_TOL, F32_TOL
+from gpu_cases import BF16_REL_TOL, F32_TOL, guard, path_of
 from helpers import to_np
 
 pytestmark = pytest.mark.gpu
@@ -56,14 +56,29 @@ def _run_oracle(w, a, **mods):
     return r.out
 
 
-def _vmax(a):
-    v = a["v_blocks"] if "v_blocks" in a else a["v_cache"]
+def _vmax(w, a):
+    """max |V| over the values the step attends: each row's cached slots
+    0 .. lengths[b]-1 (E4M3 bytes times the per-head scale) and the new values."""
     f = lambda x: (x.astype(np.uint32) << 16).view(np.float32) if x.dtype == np.uint16 else x
-    if v.dtype == np.uint8:                   # E4M3 bytes times the per-head scale
-        vf = torch.from_numpy(v).view(torch.float8_e4m3fn).float().numpy()
-        vc = np.abs(vf).max(axis=(0, 2, 3)) * a["v_scale"]
-        return float(max(vc.max(), np.abs(f(a["v_new"])).max()))
-    return float(max(np.abs(f(v)).max(), np.abs(f(a["v_new"])).max()))
+    v = a["v_blocks"] if "v_blocks" in a else a["v_cache"]
+    if v.dtype == np.uint8:
+        v = torch.from_numpy(v).view(torch.float8_e4m3fn).double().numpy() * a["v_scale"].reshape(1, -1, 1, 1)
+    else:
+        v = f(v)
+    vals = [float(np.abs(f(a["v_new"])).max())] if a["v_new"].size else [0.0]
+    cu, L = a["cu_q"], a["lengths"]
+    for b in range(len(L)):
+        n = int(L[b])
+        if cu[b + 1] == cu[b] or n <= 0:
+            continue
+        if "v_blocks" in a:
+            bs = v.shape[2]
+            blk = a["block_table"][b, np.arange(n) // bs]
+            vals.append(float(np.abs(v[blk, :, np.arange(n) % bs]).max()))
+        else:
+            r = int(a["slot_ids"][b]) if "slot_ids" in a else b
+            vals.append(float(np.abs(v[r, :, :n]).max()))
+    return max(vals)
 
 
 def check_multi(w, q_lens, kernel="auto", grid=0, fp8=False, **mods):
@@ -74,12 +89,16 @@ def check_multi(w, q_lens, kernel="auto", grid=0, fp8=False, **mods):
     out = _run_gpu(w, t, max_q, kernel, grid, st, **mods)
     torch.cuda.synchronize()
     assert int(st.item()) == 0, f"device status {int(st.item())}"
-    want = _run_oracle(w, a, **mods)          # appends into the host copies
+    vmax = _vmax(w, a)                        # before the oracle appends into the host copies
+    want = _run_oracle(w, a, **mods)
     got = out.double().cpu().numpy()
     assert np.isfinite(got).all()
-    tol = F32_TOL if w.dtype == "f32" else BF16_REL_TOL * _vmax(a)
+    tol = F32_TOL if w.dtype == "f32" else BF16_REL_TOL * vmax
     err = float(np.abs(got - want).max()) if got.size else 0.0
     assert err <= tol, f"max abs error {err} > {tol}"
+    G = w.Hq // w.Hkv
+    tpc = max(1, min(16 // G if kernel != "simt" else 8 // G, max_q))
+    guard(path_of(w, kernel, fp8=fp8, unit_rows=G * tpc), err, vmax)
     for n in (("k_blocks", "v_blocks") if w.paged else ("k_cache", "v_cache")):
         assert to_np(t[n]).tobytes() == a[n].tobytes(), f"{n} differs from the oracle's appended copy"
     return err
@@ -242,9 +261,13 @@ def test_multi_full_size(name, q_len, fp8):
     out = _run_gpu(w, t, q_len, status=st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
+    vmax = _vmax(w, a)
     want = _run_oracle(w, a)
     got = out[tok].double().cpu().numpy()
-    assert np.abs(got - want).max() <= BF16_REL_TOL * _vmax(a)
+    err = float(np.abs(got - want).max())
+    assert err <= BF16_REL_TOL * vmax
+    G = w.Hq // w.Hkv
+    guard(path_of(w, "tc", fp8=fp8, unit_rows=G * max(1, min(16 // G, q_len))), err, vmax)
     if w.paged:
         assert to_np(t["k_blocks"][idx]).tobytes() == a["k_blocks"].tobytes()
     else:

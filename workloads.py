@@ -243,11 +243,12 @@ def _to_e4m3(x, scale):
     return out
 
 
-def quantise_cache(w: Workload, t: dict) -> dict:
+def quantise_cache(w: Workload, t: dict, key_range: float = 4.0) -> dict:
     """The cache of ``t`` as E4M3 bytes with per-head scales (see the module
-    docstring); the other inputs unchanged."""
+    docstring; ``key_range`` * key_scale is the largest key the scale
+    represents, 4 sigma by default); the other inputs unchanged."""
     dev = t["q"].device
-    ks = torch.full((w.Hkv,), 4.0 * w.key_scale / 448.0, dtype=torch.float32, device=dev)
+    ks = torch.full((w.Hkv,), key_range * w.key_scale / 448.0, dtype=torch.float32, device=dev)
     vs = torch.full((w.Hkv,), 4.0 / 448.0, dtype=torch.float32, device=dev)
     names = ("k_blocks", "v_blocks") if w.paged else ("k_cache", "v_cache")
     t[names[0]] = _to_e4m3(t[names[0]], ks)
