@@ -684,17 +684,15 @@ __device__ __forceinline__ float *out_row(const DecodeParams &p, const TileCurso
     }
 }
 
-// MULTI: the unit may be a chunk of a multi-token step (any form then works).
-// pre_cnt (thread 0 only): the unit's arrival count read with acquire
-// semantics shortly before the segment's end, or -1. When it already shows
-// every other piece of the unit arrived, this CTA is the last arriver: it
-// skips the ticket's round trip and merges at once.
-template <int NW, int GP, int DD, int DP, bool MULTI, bool PRE2 = false, class Sync, int GR, int KM>
-__device__ inline void finish_segment(const DecodeParams &p, const TileCursor &cur, const TileWalk &walk,
-                                      int seg_first_t,
-                                      bool bad, const float (&sm_m)[NW][GP], const float (&sm_l)[NW][GP],
-                                      const float (&sm_o)[NW][GP][DP], int *sm_flag, MergeBufT<GR, KM> &mb,
-                                      int tid, int nthr, Sync sync, int pre_cnt = -1)
+// First part of the end of a unit segment: the weights of the warp states,
+// then the normalised output (the segment is the whole unit) or this CTA's
+// partial state (a cut unit). Returns whether the unit was whole. Every
+// calling thread takes part; ends with a sync().
+template <int NW, int GP, int DD, int DP, bool MULTI, class Sync, int GR, int KM>
+__device__ inline bool segment_out(const DecodeParams &p, const TileCursor &cur, int seg_first_t, bool bad,
+                                   const float (&sm_m)[NW][GP], const float (&sm_l)[NW][GP],
+                                   const float (&sm_o)[NW][GP][DP], MergeBufT<GR, KM> &mb, int tid, int nthr,
+                                   Sync sync)
 {
     static_assert(NW <= kMergeW && GP <= GR && DP >= DD, "merge buffer too small");
     const int G = p.G, b = cur.b, kvh = cur.kvh;
@@ -771,18 +769,27 @@ __device__ inline void finish_segment(const DecodeParams &p, const TileCursor &c
             }
         }
     }
-    if (whole) {
-        sync();
-        return;
-    }
-    // The barrier orders every thread's partial stores before thread 0's
-    // acquire-release ticket at GPU scope (release is cumulative); the last
-    // arriver's acquire plus the barrier order its reads after the stores of
-    // every other CTA of the unit.
     sync();
-    const long long first_tile = cur.g - cur.t;
-    const int first = cta_of_tile(first_tile, walk.N, walk.C);
-    const int last = cta_of_tile(first_tile + cur.nr - 1, walk.N, walk.C);
+    return whole;
+}
+
+// Second part for a cut unit: the arrival ticket and, in the last CTA of the
+// unit to arrive, the merge of every partial (log-sum-exp rule), the output,
+// and the partials and counter back to zero. `cur` names the unit (b, kvh,
+// and nq / tokL of a multi-token chunk); first..last are the CTAs whose
+// ranges hold its tiles. The threads calling it must be ordered after the
+// partial stores of this CTA (a barrier): thread 0's acquire-release ticket
+// at GPU scope then publishes them (release is cumulative), and the last
+// arriver's acquire plus the barrier order its reads after the stores of
+// every other CTA of the unit.
+template <int DD, bool MULTI, bool PRE2, class Sync, int GR, int KM>
+__device__ inline void unit_ticket_merge(const DecodeParams &p, const TileCursor &cur, int first, int last,
+                                         int *sm_flag, MergeBufT<GR, KM> &mb, int tid, int nthr, Sync sync,
+                                         int pre_cnt)
+{
+    const int G = p.G, kvh = cur.kvh;
+    const int u = cur.b * p.Hkv + kvh;
+    const int nrow = MULTI ? p.Gh * cur.nq : G;   // query rows with an output
     if (tid == 0) {
         int old = pre_cnt;
         if (old != last - first)
@@ -905,6 +912,26 @@ __device__ inline void finish_segment(const DecodeParams &p, const TileCursor &c
             p.ws_cnt[u] = 0;
     }
     sync();
+}
+
+// MULTI: the unit may be a chunk of a multi-token step (any form then works).
+// pre_cnt (thread 0 only): the unit's arrival count read with acquire
+// semantics shortly before the segment's end, or -1. When it already shows
+// every other piece of the unit arrived, this CTA is the last arriver: it
+// skips the ticket's round trip and merges at once.
+template <int NW, int GP, int DD, int DP, bool MULTI, bool PRE2 = false, class Sync, int GR, int KM>
+__device__ inline void finish_segment(const DecodeParams &p, const TileCursor &cur, const TileWalk &walk,
+                                      int seg_first_t,
+                                      bool bad, const float (&sm_m)[NW][GP], const float (&sm_l)[NW][GP],
+                                      const float (&sm_o)[NW][GP][DP], int *sm_flag, MergeBufT<GR, KM> &mb,
+                                      int tid, int nthr, Sync sync, int pre_cnt = -1)
+{
+    if (segment_out<NW, GP, DD, DP, MULTI>(p, cur, seg_first_t, bad, sm_m, sm_l, sm_o, mb, tid, nthr, sync))
+        return;
+    const long long first_tile = cur.g - cur.t;
+    const int first = cta_of_tile(first_tile, walk.N, walk.C);
+    const int last = cta_of_tile(first_tile + cur.nr - 1, walk.N, walk.C);
+    unit_ticket_merge<DD, MULTI, PRE2>(p, cur, first, last, sm_flag, mb, tid, nthr, sync, pre_cnt);
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }

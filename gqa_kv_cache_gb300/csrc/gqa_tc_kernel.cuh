@@ -87,6 +87,7 @@
 #include <cuda_fp16.h>
 
 #include <atomic>
+#include <type_traits>
 
 #include "gqa_common.cuh"
 #include "gqa_launch.h"
@@ -110,7 +111,7 @@ constexpr int kStages = GQA_TC_STAGES;                // depth of one CTA's TMA 
 constexpr int kCtasPerSm = GQA_TC_CTAS_PER_SM;        // resident CTAs per SM
 constexpr int kCtasPerSmKV8 = GQA_TC_KV8_CTAS_PER_SM; // the same, single-token steps over an E4M3 cache
 constexpr int kConsumerWarps = 4;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kMaxWarps = kConsumerWarps + 2;          // consumers, producer, finisher
 constexpr int kGMax = 8;
 constexpr int kHalfBytes = kTile * 128;               // one 64-element half of a tile
 constexpr long long kWaitCycles = 4LL << 30;          // ~2 s at 2 GHz
@@ -124,12 +125,27 @@ struct Ring {
     static constexpr int kQRows = kMside ? 2 * kGMax : kGMax;        // query rows of a unit
     static constexpr int kQBytes = kQRows * kD * kQElem;             // the unit's query rows
     static constexpr int kKVBytes = KV8 ? kTile * kD : 2 * kHalfBytes; // K (or V) of one tile
-    static constexpr int kStageBytes = 2 * kKVBytes + kQBytes;       // K (lo, hi), V (lo, hi), Q
+    // single-token steps over an E4M3 cache: the new token's bf16 K and V rows
+    // (2 x 256 bytes), copied by the producer into the stage of the tile that
+    // holds slot L (measured: about 0.5 us off llama3_8b's step; over a bf16
+    // cache it made no difference or cost time, so there the owning warp
+    // loads them from global memory)
+    static constexpr int kNewBytes = (!MULTI && KV8) ? 1024 : 0;
+    static constexpr int kStageBytes = 2 * kKVBytes + kQBytes + kNewBytes;   // K (lo, hi), V (lo, hi), Q, new
     // E4M3: 4 stages at two CTAs per SM, 2 at three; 3 with the 16 query
     // rows of a 16-row multi-token unit, so two CTAs still share an SM
     static constexpr int kNumStages = KV8 ? (kMside ? 3 : (kCtasPerSmKV8 >= 3 ? 2 : 4)) : kStages;
     static constexpr int kCtas = (KV8 && !kMside) ? kCtasPerSmKV8 : kCtasPerSm;   // resident CTAs per SM
     static constexpr int kDynSmem = kNumStages * kStageBytes + 1024;
+    // Multi-token steps over a bfloat16 cache: a finisher warp takes the
+    // arrival ticket (and the merge, when last) of every cut unit but the
+    // CTA's last off the consumers' path (measured: llama3_8b q_len 4 91.5 ->
+    // 84.0 us, paged q_len 3 811.8 -> 793.7 us). In the single-token kernels a
+    // sixth warp made every CTA stream about 5 % slower and the steps 1-2 us
+    // longer, and the E4M3 kernels at three CTAs per SM have no registers to
+    // spare, so those keep the ticket on the consumers.
+    static constexpr bool kFin = MULTI && !KV8;
+    static constexpr int kThreads = (kConsumerWarps + 1 + (kFin ? 1 : 0)) * 32;
     static_assert(kStageBytes % 1024 == 0, "stages must stay 1024-byte aligned for the swizzle");
 };
 
@@ -326,9 +342,131 @@ __device__ __forceinline__ void split_bf16(float2 v, uint32_t &hi, uint32_t &lo)
 // under the 128-byte swizzle (the half starts on a 1024-byte boundary).
 __device__ __forceinline__ uint32_t swz(int r, int c8) { return (uint32_t)(r * 128 + ((c8 ^ (r & 7)) << 4)); }
 
+// The consumers and the finisher warp hand over cut units through one job
+// slot and two named barriers: 2 (a job is posted: the consumers arrive, the
+// finisher waits) and 3 (the slot is free again: the finisher arrives, the
+// consumers wait). The barriers also order the consumers' partial stores
+// before the finisher's ticket.
+constexpr int kFinBarThreads = (kConsumerWarps + 1) * 32;
+
+struct FinJob {
+    int stop;          // 1: no more jobs
+    int first, last;   // CTAs whose ranges hold the unit's tiles
+    int b, kvh, nq, tokL;
+};
+
+__device__ __forceinline__ void job_wait_posted() { asm volatile("bar.sync 2, %0;" ::"n"(kFinBarThreads) : "memory"); }
+__device__ __forceinline__ void job_post() { asm volatile("bar.arrive 2, %0;" ::"n"(kFinBarThreads) : "memory"); }
+__device__ __forceinline__ void job_wait_free() { asm volatile("bar.sync 3, %0;" ::"n"(kFinBarThreads) : "memory"); }
+__device__ __forceinline__ void job_free() { asm volatile("bar.arrive 3, %0;" ::"n"(kFinBarThreads) : "memory"); }
+
+// The finisher warp's handling of a cut unit (RW query rows at most): the
+// arrival ticket and, in the last CTA of the unit to arrive, the merge of the
+// K partials (log-sum-exp rule), the output, and the partials and counter
+// back to zero. One warp: the partial outputs are read with all of a lane's
+// loads of one partial in flight at once, so a merge costs about one L2 round
+// trip per partial.
+template <int RW, bool MULTI, int GR, int KM>
+__device__ __noinline__ void fin_ticket_merge(const DecodeParams &p, const FinJob j, MergeBufT<GR, KM> &mb,
+                                              int *flag, int lane)
+{
+    constexpr int IT = RW * kD / (32 * 4);   // float4 per lane and partial
+    const int G = p.G;
+    const int u = j.b * p.Hkv + j.kvh;
+    const int K = j.last - j.first + 1;
+    int old = 0;
+    if (lane == 0)
+        asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(p.ws_cnt + u) : "memory");
+    old = __shfl_sync(0xffffffffu, old, 0);
+    if (old != K - 1)
+        return;                              // other pieces still to come
+    TileCursor c;
+    c.b = j.b;
+    c.kvh = j.kvh;
+    c.nq = j.nq;
+    c.tokL = j.tokL;
+    if (K > KM) {   // more partials than the merge buffer holds: the general merge
+        unit_ticket_merge<kD, MULTI, false>(p, c, j.first, j.last, flag, mb, lane, 32, [] { __syncwarp(); }, K - 1);
+        return;
+    }
+    const long long P0 = (long long)u + j.first;
+    float4 acc[IT];
+#pragma unroll
+    for (int it = 0; it < IT; ++it)
+        acc[it] = make_float4(0.f, 0.f, 0.f, 0.f);
+    // every partial's (m, l): weights and the denominator per query row
+    for (int k = lane; k < K * G; k += 32) {
+        mb.w[k] = __ldcg(p.ws_ml + (P0 * G + k) * 2);
+        mb.l[k] = __ldcg(p.ws_ml + (P0 * G + k) * 2 + 1);
+    }
+    __syncwarp();
+    if (lane < G) {
+        float M = -INFINITY;
+        for (int i = 0; i < K; ++i)
+            M = fmaxf(M, mb.w[i * G + lane]);
+        const float sk = p.sink ? sink_log2(p, j.kvh * p.Gh + lane % p.Gh) : -INFINITY;
+        M = fmaxf(M, sk);
+        float den = (sk == -INFINITY) ? 0.f : fast_ex2(sk - M);
+        for (int i = 0; i < K; ++i) {
+            const float a = fast_ex2(mb.w[i * G + lane] - M);
+            mb.w[i * G + lane] = a;
+            den = fmaf(a, mb.l[i * G + lane], den);
+        }
+        mb.inv_den[lane] = 1.f / den;
+    }
+    __syncwarp();
+    for (int i = 0; i < K; ++i) {
+        float4 *po = reinterpret_cast<float4 *>(p.ws_o + (P0 + i) * G * kD);
+        float4 v[IT];
+#pragma unroll
+        for (int it = 0; it < IT; ++it) {
+            const int idx = (it * 32 + lane) * 4;
+            v[it] = idx < G * kD ? __ldcg(po + idx / 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int it = 0; it < IT; ++it) {
+            const int idx = (it * 32 + lane) * 4;
+            if (idx < G * kD) {
+                const float a = mb.w[i * G + idx / kD];
+                acc[it].x = fmaf(a, v[it].x, acc[it].x);
+                acc[it].y = fmaf(a, v[it].y, acc[it].y);
+                acc[it].z = fmaf(a, v[it].z, acc[it].z);
+                acc[it].w = fmaf(a, v[it].w, acc[it].w);
+                po[idx / 4] = make_float4(0.f, 0.f, 0.f, 0.f);   // consumed: zero-filled again
+            }
+        }
+    }
+    const int nrow = MULTI ? p.Gh * j.nq : G;
+#pragma unroll
+    for (int it = 0; it < IT; ++it) {
+        const int idx = (it * 32 + lane) * 4;
+        const int g = idx / kD;
+        if (idx < G * kD && g < nrow) {
+            const float s = mb.inv_den[g];
+            *reinterpret_cast<float4 *>(out_row<MULTI>(p, c, g, kD) + (idx - g * kD)) =
+                make_float4(acc[it].x * s, acc[it].y * s, acc[it].z * s, acc[it].w * s);
+        }
+    }
+    float *ml = p.ws_ml + P0 * G * 2;
+    for (int k = lane; k < K * G * 2; k += 32)
+        ml[k] = 0.f;
+    if (lane == 0)
+        p.ws_cnt[u] = 0;
+    __syncwarp();
+}
+
+// The finisher warp's job slot, merge buffer and flag (kernels with one).
+template <int RW>
+struct FinShared {
+    FinJob job;
+    MergeBufT<RW, RW == kGMax ? kMergeMax : 16> merge;
+    int flag;
+};
+struct NoFinShared {};
+
 // NS ring stages; RW query rows per unit (8, or 16 for multi-token units,
-// whose o rows take less padding to fit two CTAs per SM).
-template <int NS, int RW = kGMax>
+// whose o rows take less padding to fit two CTAs per SM); FIN: a finisher warp.
+template <int NS, int RW = kGMax, bool FIN = false>
 struct Shared {
     static constexpr int kOPad = 4;   // rows 132 floats apart: the epilogue's stores are conflict-free
     uint64_t full[NS];
@@ -337,18 +475,20 @@ struct Shared {
     int stage_bad[NS];
     int abort_flag;
     int last_flag;
-    long long sched[kThreads / 32 + 8];
+    long long sched[kMaxWarps + 8];
     TileWalk walk;
     float m[kConsumerWarps][RW];
     float l[kConsumerWarps][RW];
     alignas(16) float o[kConsumerWarps][RW][kD + kOPad];  // rows padded: (near) conflict-free 8-byte stores
     MergeBufT<RW, RW == kGMax ? kMergeMax : 16> merge;
+    std::conditional_t<FIN, FinShared<RW>, NoFinShared> fin;
 };
 
 __device__ __forceinline__ void consumer_sync()
 {
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
 }
+
 
 // WIN: a sliding window is in force. Without one the window fields of the
 // cursor are never read, so they take no registers and no code. MULTI: a
@@ -357,7 +497,7 @@ __device__ __forceinline__ void consumer_sync()
 // rows on the M = 16 side of the products; units of up to 8 rows (and every
 // single-token unit) put them on the N = 8 side.
 template <bool QF32, bool WIN, bool MULTI, bool KV8, bool M16>
-__global__ void __launch_bounds__(kThreads, (Ring<QF32, KV8, MULTI, M16>::kCtas))
+__global__ void __launch_bounds__((Ring<QF32, KV8, MULTI, M16>::kThreads), (Ring<QF32, KV8, MULTI, M16>::kCtas))
     tc_decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap mk,
                      const __grid_constant__ CUtensorMap mv)
 {
@@ -370,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, (Ring<QF32, KV8, MULTI, M16>::kCtas)
     constexpr int kNS = RG::kNumStages;   // ring depth
     constexpr int kKVB = RG::kKVBytes;    // K (or V) bytes of one tile
     extern __shared__ uint8_t dyn_smem[];
-    __shared__ Shared<kNS, kRW> sh;
+    __shared__ Shared<kNS, kRW, RG::kFin> sh;
     uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
     const uint32_t ring_u32 = smem_u32(ring);
 
@@ -471,11 +611,25 @@ __global__ void __launch_bounds__(kThreads, (Ring<QF32, KV8, MULTI, M16>::kCtas)
             const bool seg_first = pl.good && (cur.t == 0 || cur.g == range_start);
             const int qrows = MULTI ? p.Gh * cur.nq : G;   // query rows with data
             const uint32_t qbytes = seg_first ? (uint32_t)(qrows * kD * RG::kQElem) : 0u;
-            const uint32_t bytes = (uint32_t)__popc(copying) * (KV8 ? 2u : 4u) * (uint32_t)box_rows * 128u + qbytes;
+            // single-token decode over an E4M3 cache: the tile holding slot L
+            // (the unit's last real tile) also brings the new token's K and V
+            // rows, so the consumers quantise and append them from shared memory
+            const bool newt = RG::kNewBytes > 0 && !p.attend && pl.good && cur.t == cur.nr - 1;
+            const uint32_t nbytes = newt ? 2u * kD * 2u : 0u;
+            const uint32_t bytes =
+                (uint32_t)__popc(copying) * (KV8 ? 2u : 4u) * (uint32_t)box_rows * 128u + qbytes + nbytes;
             const uint32_t fb = smem_u32(&sh.full[stage]);
             if (lane == 0) {
                 sh.stage_bad[stage] = any_bad ? 1 : 0;
                 mbar_arrive_tx(fb, bytes);
+                if constexpr (RG::kNewBytes > 0) {
+                    if (newt) {
+                        const uint32_t ndst = ring_u32 + stage * kStageBytes + 2 * kKVB + RG::kQBytes;
+                        const long long nidx = ((long long)b * p.Hkv + kvh) * kD;
+                        bulk_load(ndst, knew + nidx, kD * 2u, fb);
+                        bulk_load(ndst + kD * 2u, vnew + nidx, kD * 2u, fb);
+                    }
+                }
                 if (qbytes) {
                     const uint32_t qdst = ring_u32 + stage * kStageBytes + 2 * kKVB;
                     if constexpr (MULTI) {
@@ -543,6 +697,26 @@ __global__ void __launch_bounds__(kThreads, (Ring<QF32, KV8, MULTI, M16>::kCtas)
             }
         }
         return;
+    }
+
+    // --------------------------------------------------------- finisher --
+    // Takes each cut unit the consumers hand over: the arrival ticket (whose
+    // release must wait until this CTA's partial stores are visible at GPU
+    // scope, about 2 us under full HBM load) and, in the last CTA of the unit
+    // to arrive, the merge. The consumers meanwhile stream the next segment.
+    if constexpr (RG::kFin) {
+        if (warp == kConsumerWarps + 1) {
+            job_free();                  // the slot starts free
+            while (true) {
+                job_wait_posted();
+                const FinJob j = sh.fin.job;
+                if (j.stop)
+                    break;
+                job_free();
+                fin_ticket_merge<kRW, MULTI>(p, j, sh.fin.merge, &sh.fin.flag, lane);
+            }
+            return;
+        }
     }
 
     // -------------------------------------------------------- consumers --
@@ -756,12 +930,12 @@ __global__ void __launch_bounds__(kThreads, (Ring<QF32, KV8, MULTI, M16>::kCtas)
                     // sixteen elements each)
                     const int lr = L - slot0;
                     if (last_tile && !p.attend && lr >= row0 && lr < row0 + 16 && lane < 16) {
-                        const long long nidx = ((long long)b * p.Hkv + kvh) * kD;
                         const int c16 = lane & 7;
                         const bool is_k = lane < 8;
-                        const uint4 *src = reinterpret_cast<const uint4 *>((is_k ? knew : vnew) + nidx) + 2 * c16;
-                        const uint4 q8 = quant_e4m3x16(__ldg(src), __ldg(src + 1),
-                                                       __ldg((is_k ? p.k_scale : p.v_scale) + kvh));
+                        // the new token's rows, brought into the stage by the producer
+                        const uint4 *src = reinterpret_cast<const uint4 *>(kring + 2 * kKVB + RG::kQBytes +
+                                                                           (is_k ? 0 : kD * 2)) + 2 * c16;
+                        const uint4 q8 = quant_e4m3x16(src[0], src[1], __ldg((is_k ? p.k_scale : p.v_scale) + kvh));
                         *reinterpret_cast<uint4 *>((is_k ? kring : vring) + swz(lr, c16)) = q8;
                         const long long off = slot_offset(p, b, kvh, L);
                         if (off >= 0)
@@ -1217,15 +1391,50 @@ __global__ void __launch_bounds__(kThreads, (Ring<QF32, KV8, MULTI, M16>::kCtas)
             const bool bad = !row_good || seg_bad;
             if (bad && row_good && tid == 0)
                 report(p, aborted ? kTimeout : kBadBlock);
-            // the merge's preload of partial outputs costs registers: off for
-            // the E4M3 kernels (at their 128-register cap)
-            finish_segment<kConsumerWarps, kRW, kD, kD + Shared<kNS, kRW>::kOPad, MULTI, !KV8>(p, cur, walk, seg_first_t,
-                                                                                   bad, sh.m, sh.l, sh.o,
-                                                      &sh.last_flag, sh.merge, tid, kConsumerWarps * 32,
-                                                      [] { consumer_sync(); }, pre_cnt);
+            // With a finisher warp, a cut unit's ticket and merge go to it --
+            // but not in the CTA's last segment: nothing is left to overlap
+            // with there, and four warps merge faster than one.
+            bool handed = false;
+            if constexpr (RG::kFin) {
+                if (!(range_done && (in_b || walk.b.g >= walk.b.end))) {
+                    handed = true;
+                    // the output (a whole unit) or the partial state
+                    if (!segment_out<kConsumerWarps, kRW, kD, kD + Shared<kNS, kRW, RG::kFin>::kOPad, MULTI>(
+                            p, cur, seg_first_t, bad, sh.m, sh.l, sh.o, sh.merge, tid, kConsumerWarps * 32,
+                            [] { consumer_sync(); })) {
+                        const long long first_tile = cur.g - cur.t;
+                        job_wait_free();
+                        if (tid == 0) {
+                            FinJob j;
+                            j.stop = 0;
+                            j.first = cta_of_tile(first_tile, walk.N, walk.C);
+                            j.last = cta_of_tile(first_tile + cur.nr - 1, walk.N, walk.C);
+                            j.b = cur.b;
+                            j.kvh = cur.kvh;
+                            j.nq = MULTI ? cur.nq : 1;
+                            j.tokL = MULTI ? cur.tokL : cur.b;
+                            sh.fin.job = j;
+                        }
+                        job_post();
+                    }
+                }
+            }
+            if (!handed) {
+                // the merge's preload of partial outputs costs registers: off
+                // for the E4M3 kernels (at their 128-register cap)
+                finish_segment<kConsumerWarps, kRW, kD, kD + Shared<kNS, kRW, RG::kFin>::kOPad, MULTI, !KV8>(
+                    p, cur, walk, seg_first_t, bad, sh.m, sh.l, sh.o, &sh.last_flag, sh.merge, tid,
+                    kConsumerWarps * 32, [] { consumer_sync(); }, pre_cnt);
+            }
             seg_start = true;
         }
         more = walk_next(p, cur, walk, in_b);
+    }
+    if constexpr (RG::kFin) {   // no more jobs
+        job_wait_free();
+        if (tid == 0)
+            sh.fin.job.stop = 1;
+        job_post();
     }
 }
 
@@ -1252,7 +1461,7 @@ cudaError_t launch_q(const DecodeParams &p, const TcMaps &maps, cudaStream_t st)
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(Ring<QF32, KV8, MULTI, M16>::kThreads);
     cfg.dynamicSmemBytes = kDynSmem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];

@@ -297,3 +297,19 @@ def test_schedule_padding(kernel, sched_pad):
             assert np.abs(out.double().cpu().numpy() - want).max() <= tolerance(w, attended_vmax(prob)), (name, grid)
             idx = torch.tensor(prob["cache_rows"], dtype=torch.long, device="cuda")
             assert to_np(t["k_cache"][idx]).tobytes() == prob["k_cache"].tobytes()
+
+
+@pytest.mark.parametrize("kernel", ["simt", "tc"])
+@pytest.mark.parametrize("grid_ctas", [40, 150])
+def test_unit_cut_into_many_pieces(kernel, grid_ctas):
+    """One or two long sequences over many CTAs: every unit is cut into far
+    more pieces than the in-shared-memory merge takes (more than 32), so the
+    merge falls back to its general form; outputs against the oracle, the
+    cache bit-exact, the workspace left zero-filled."""
+    import gqa_kv_cache_gb300 as gqa
+    w = W.small("long_context", B=2, Hq=8, Hkv=1, Smax=9000, len_lo=7000, len_hi=8999, key_scale=1.0, seed=160)
+    err, tol, _ = check_step(w, kernel=kernel, grid_ctas=grid_ctas)
+    assert err <= tol, f"max abs error {err} > {tol}"
+    ws = gqa._ws_cache.get(torch.device("cuda", torch.cuda.current_device()))
+    if ws is not None:
+        assert int(torch.count_nonzero(ws).item()) == 0
