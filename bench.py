@@ -452,17 +452,21 @@ def sources_sha(names):
     return h.hexdigest()[:16]
 
 
-def traffic_for(kernel_name, key):
+def traffic_for(kernel_name, key, alg_total):
     """Per-launch DRAM bytes (read + write) of the kernel on this workload and
     operation from the committed ncu summary, if it was taken on the current
-    sources of that kernel; else None. Captures of a scaled-down instance
-    carry the scale factor to a full launch (`scale`)."""
+    sources of that kernel; else None. A capture of the full launch gives its
+    bytes; a capture of a scaled-down instance (fewer rows, the same length
+    law) gives its bytes over its own algorithmic bytes, which scales to this
+    launch by the slots it processes (`alg_total`)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         d = json.load(open(p))[kernel_name][key]
         if sources_sha(d["sources"]) != d["sources_sha"]:
             return None
-        return d["bytes_per_launch"]
+        if "bytes_per_launch" in d:
+            return d["bytes_per_launch"]
+        return int(round(d["bytes_over_algorithmic"] * alg_total))
     except Exception:
         return None
 
@@ -617,7 +621,7 @@ def measure(args, ranks, wname, dev):
     hbm_peak, peak_kind = peaks()
     achieved = alg["total"] / avg_main_s / 1e9
     tkey = traffic_key(w.name, attend, fp8, args.q_len, mods)
-    traffic = traffic_for(main, tkey) if args.kernel == "auto" else None
+    traffic = traffic_for(main, tkey, alg["total"]) if args.kernel == "auto" else None
 
     # ---- end to end through the public API, host buffers, copies inside
     Ke = min(K, 500)
