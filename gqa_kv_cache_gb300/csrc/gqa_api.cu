@@ -376,8 +376,12 @@ gqa_status run_step(const Shape &s, const void *q, const void *k_new, const void
         TraceScope ts(1, cs);
         e = tc_launch(p, maps, cs);
     } else if (unit) {
+        int dev = 0;
+        e = cudaGetDevice(&dev);
+        if (e != cudaSuccess)
+            return GQA_ERR_CUDA;
         TraceScope ts(2, cs);
-        e = unit_launch(p, s.dt == GQA_DTYPE_BF16, cap_rows, cs);
+        e = unit_launch(p, s.dt == GQA_DTYPE_BF16, cap_rows, sm_count(dev), cs);
     } else {
         TraceScope ts(0, cs);
         e = simt_launch(p, s.dt == GQA_DTYPE_BF16, cs);

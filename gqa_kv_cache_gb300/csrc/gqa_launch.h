@@ -23,12 +23,13 @@ int tc_tile();
 int tc_ctas_per_sm(bool kv8, int unit_rows);   // resident CTAs per SM of the instantiation
 cudaError_t tc_launch(const DecodeParams &p, const TcMaps &maps, cudaStream_t st);
 
-// Small-cache kernel: one CTA per unit, the unit staged in shared memory
-// (gqa_unit.cu). cap_rows: the row capacity in slots.
+// Small-cache kernel: one cluster of CTAs per unit, the unit staged in their
+// shared memory (gqa_unit.cu). cap_rows: the row capacity in slots.
 bool unit_supports(bool bf16, int D, int G, long long cap_rows);
-size_t unit_smem_bytes(bool bf16, int D, int G, long long cap_rows);
+size_t unit_smem_bytes(bool bf16, int D, int G, long long rows, int cl);
 int unit_ctas_per_sm(bool bf16, int D, int G, long long cap_rows);
-cudaError_t unit_launch(const DecodeParams &p, bool bf16, long long cap_rows, cudaStream_t st);
+int unit_cluster(long long cap_rows, long long units, int sms);   // CTAs a unit
+cudaError_t unit_launch(const DecodeParams &p, bool bf16, long long cap_rows, int sms, cudaStream_t st);
 
 // Content validation (gqa_validate.cu). *d_result must be zero on entry; the
 // kernel sets it to 1 on any violation. attend = 1 checks the read-only

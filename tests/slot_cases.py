@@ -182,9 +182,29 @@ def cut_slots(st, grid):
     return cuts
 
 
-def plant_dominant(st, seed, grid=0):
+def part_slots(st, b, k):
+    """Slots at the edges of the parts the small-cache kernel shares a unit of
+    row b out in, when a cluster of 2, 4 or 8 CTAs (by k) takes the unit:
+    either its staged rows (the attended slots, the new token last) cut into
+    equal contiguous parts, or (a dense cache staged before the lengths are
+    known) the row's capacity cut so. The first slot of each part after the
+    first, and the slot before it, for both cuts."""
+    cl = (2, 4, 8)[k % 3]
+    n = st.last[b] + 1
+    cap = st.w.max_blocks * st.w.block_size if st.w.paged else st.w.Smax
+    out = []
+    for chunk in (-(-n // cl), -(-cap // cl)):
+        for m in range(1, cl):
+            if m * chunk < n:
+                out += [m * chunk, m * chunk - 1]
+    return out
+
+
+def plant_dominant(st, seed, grid=0, unit_parts=False):
     """Gives every unit a shared query direction and one dominant slot j*;
-    returns {(b, kvh): j*}."""
+    returns {(b, kvh): j*}. j* sits at a CTA cut of a `grid`-CTA tensor-core
+    launch, or (`unit_parts`) at a part edge of the small-cache kernel, or
+    else at tile edges, the new token and the last slot."""
     w, t = st.w, st.t
     g = torch.Generator().manual_seed(seed)
     cuts = cut_slots(st, grid) if grid and not st.multi else {}
@@ -201,8 +221,8 @@ def plant_dominant(st, seed, grid=0):
             for tok, _ in st.rows(b):
                 for h in range(kvh * w.G, (kvh + 1) * w.G):
                     t["q"][tok, h] = (u + 0.3 * torch.randn(w.D, generator=g)).to(t["q"].dtype)
-            c = cuts.get((b, kvh))
-            j = c[k % len(c)] if c else cand[k % len(cand)]
+            c = part_slots(st, b, k) if unit_parts else cuts.get((b, kvh))
+            j = c[(k // 3 if unit_parts else k) % len(c)] if c else cand[k % len(cand)]
             j = min(max(j, 0), last)
             ten, idx = st.key_slot(b, kvh, j, "k")
             ten[idx] = (C_DOM * (128.0 / w.D) ** 0.5 * u).to(ten.dtype)
@@ -280,9 +300,14 @@ MULTI = [
                                       len_lo=0, len_hi=540, seed=615), [2, 2, 1, 2]),
 ]
 
-# capacities the small-cache kernel stages whole (K and V of a row within 200 KB)
+# capacities the small-cache kernel takes (K and V of a row within 200 KB of
+# one CTA's shared memory); few units are shared out over clusters of 2 to 8
+# CTAs, 128 units (the first case) take one CTA each; the dense float32 and
+# the two-row bfloat16 cases stage the capacity before the lengths are known
 UNIT = [
+    ("dense_g4_cap384_b16", "llama3_8b", dict(B=16, Smax=384, len_lo=0, len_hi=383, seed=625)),
     ("dense_g4_cap384", "llama3_8b", dict(B=8, Smax=384, len_lo=0, len_hi=383, seed=621)),
+    ("dense_g4_cap256_b2", "llama3_8b", dict(B=2, Smax=256, len_lo=0, len_hi=255, seed=626)),
     ("slots_g8_cap320", "ragged_slots", dict(B=6, R=11, Smax=320, len_lo=1, len_hi=319, seed=622)),
     ("paged16_g6_cap384", "paged", dict(B=6, num_blocks=6 * 24, max_blocks=24, len_lo=0, len_hi=380, seed=623)),
     ("f32_d64_g4_cap256", "pr1_fp32", dict(B=4, Smax=256, len_lo=0, len_hi=255, seed=624)),

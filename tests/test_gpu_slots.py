@@ -7,7 +7,8 @@ drops, duplicates or misplaces one slot, which the stated bar on random data
 
 Covered: the bfloat16 single-token tensor-core kernel (dense, slot ids,
 paged blocks of 16 and 8; the default grid, 7 and 33 CTAs so units are cut),
-the CUDA-core kernel, the small-cache kernel (decode and attend), the
+the CUDA-core kernel, the small-cache kernel (decode and attend; the
+dominant slot at the edges of the parts a cluster of CTAs shares out), the
 read-only attend (bfloat16 and float32 query, bfloat16 and E4M3 caches), the
 E4M3 decode kernels, and the multi-token units of up to 8 and of 16 query
 rows (and a step of two chunks)."""
@@ -51,8 +52,8 @@ def run_gpu(st, kernel="auto", grid=0):
     return out.double().cpu().numpy()
 
 
-def dominant(st, seed, kernel, grid, cut_grid=None):
-    dom = plant_dominant(st, seed, grid if cut_grid is None else cut_grid)
+def dominant(st, seed, kernel, grid, cut_grid=None, unit_parts=False):
+    dom = plant_dominant(st, seed, grid if cut_grid is None else cut_grid, unit_parts)
     st.finish()
     got = run_gpu(st, kernel, grid)
     check_dominant(st, dom, got, run_oracle(st))
@@ -125,7 +126,7 @@ def test_zero_query_multi(name, base, kw, q_lens, grid, fp8):
 @pytest.mark.parametrize("name,base,kw", UNIT, ids=[c[0] for c in UNIT])
 def test_dominant_small_cache_kernel(name, base, kw, kind):
     w = W.small(base, **(dict(kw, len_lo=1) if kind == "attend" else kw))
-    dominant(Step(w, kind), 15, "unit", 0)
+    dominant(Step(w, kind), 15, "unit", 0, unit_parts=True)
 
 
 @pytest.mark.parametrize("kind", ["decode", "attend"])

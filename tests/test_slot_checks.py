@@ -17,13 +17,13 @@ import numpy as np
 import pytest
 
 import workloads as W
-from slot_cases import MULTI, SINGLE, Step, check_dominant, check_uniform, plant_dominant, run_oracle
+from slot_cases import MULTI, SINGLE, UNIT, Step, check_dominant, check_uniform, part_slots, plant_dominant, run_oracle
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 TESTS = os.path.join(ROOT, "tests")
 SRC = os.path.join(ROOT, "oracle", "gqa_oracle.c")
 
-CASES = {c[0]: c for c in SINGLE}
+CASES = {c[0]: c for c in SINGLE + UNIT}
 MCASES = {c[0]: c for c in MULTI}
 
 
@@ -40,6 +40,8 @@ def build_step(kind, name, fp8, uniform):
     dom = None
     if uniform:
         st.t["q"].zero_()
+    elif name in dict((c[0], 0) for c in UNIT):
+        dom = plant_dominant(st, 15, unit_parts=True)
     else:
         dom = plant_dominant(st, 11, 33 if kind != "multi" else 0)
     st.finish()
@@ -48,7 +50,9 @@ def build_step(kind, name, fp8, uniform):
 
 @pytest.mark.parametrize("kind,name,fp8", [("decode", "dense_g4", False), ("decode", "paged16_g6", True),
                                            ("decode", "slots_g8", False), ("attend", "paged16_g6", False),
-                                           ("multi", "rows16_g4", False), ("multi", "rows18_g6_paged16", True)])
+                                           ("multi", "rows16_g4", False), ("multi", "rows18_g6_paged16", True),
+                                           ("decode", "f32_d64_g4_cap256", False),
+                                           ("attend", "slots_g8_cap320", False)])
 def test_constructions_hold_on_the_oracle(kind, name, fp8):
     st, dom = build_step(kind, name, fp8, uniform=False)
     out = run_oracle(st)
@@ -128,3 +132,20 @@ def test_zero_query_check_rejects_a_wrong_slot_count(tmp_path, mutant, kind, nam
     want = run_oracle(st)
     with pytest.raises(AssertionError):
         check_uniform(st, got, want)
+
+
+def test_unit_part_edges_are_planted():
+    """The small-cache construction puts j* on a part edge of a 2-, 4- or
+    8-CTA cluster in every unit whose row has such an edge."""
+    _, base, kw = CASES["f32_d64_g4_cap256"]
+    st = Step(W.small(base, **kw), "decode")
+    dom = plant_dominant(st, 15, unit_parts=True)
+    k = 0
+    for b in range(st.w.B):
+        if not st.live(b):
+            continue
+        for kvh in range(st.w.Hkv):
+            edges = part_slots(st, b, k)
+            if edges:
+                assert dom[(b, kvh)] in edges
+            k += 1
