@@ -210,7 +210,7 @@ struct Shape {
 };
 
 // How a multi-token step is cut into virtual rows: tokens per chunk (so that
-// chunk rows G * tpc fit the query rows of a unit: 16 for the tensor-core
+// chunk rows G * tpc fit the query rows of a unit: 32 for the tensor-core
 // kernel, 8 for the CUDA-core one) and chunks per batch row.
 struct MultiCut {
     int tpc, chunks;
@@ -289,7 +289,7 @@ gqa_status run_step(const Shape &s, const void *q, const void *k_new, const void
                                    (long long)s.B * s.Hkv);
     if (kernel < 0)
         return GQA_ERR_UNSUPPORTED;
-    const MultiCut cut = s.multi ? multi_cut(Gh, s.max_q, kernel == GQA_KERNEL_TC ? 16 : 8) : MultiCut{1, 1};
+    const MultiCut cut = s.multi ? multi_cut(Gh, s.max_q, kernel == GQA_KERNEL_TC ? 32 : 8) : MultiCut{1, 1};
     const int G = Gh * cut.tpc;             // query rows of a unit
     const int Bv = s.B * cut.chunks;        // (virtual) rows of the schedule
     const bool unit = kernel == GQA_KERNEL_UNIT;   // no schedule, no workspace
@@ -559,7 +559,7 @@ size_t gqa_workspace_bytes_multi(int B, int Hq, int Hkv, int D, gqa_dtype dt, in
         o.kernel = k;
         if (pick_kernel(&o, dt, D, Gh, false, 16) != k)
             continue;
-        const MultiCut cut = multi_cut(Gh, max_q_len, k == GQA_KERNEL_TC ? 16 : 8);
+        const MultiCut cut = multi_cut(Gh, max_q_len, k == GQA_KERNEL_TC ? 32 : 8);
         const int G = Gh * cut.tpc;
         const int grid = grid_for(k, &o, dt, D, G);
         if (grid <= 0)

@@ -51,17 +51,23 @@
 //    (float32 division by the scale, round to nearest even, saturating). With
 //    its smaller stages the single-token E4M3 kernel runs three CTAs per SM
 //    (2-stage rings, at most 128 registers a thread).
-//  * multi-token steps (MULTI): a unit is a chunk of up to 16 / G tokens of a
+//  * multi-token steps (MULTI): a unit is a chunk of up to 32 / G tokens of a
 //    row; its query rows are (token, head) pairs, gathered by one bulk copy
 //    per token. Units of up to 8 rows take the products above (rows on the
-//    N = 8 side); units of 9 to 16 rows (M16) keep the rows on the M = 16 side
+//    N = 8 side); units of 9 to 16 rows keep the rows on the M = 16 side
 //    (S = Q K^T, O += P V, the score fragment reused as the A fragment of P;
-//    P in plain bf16, f16 over an E4M3 cache). Each row is masked
+//    P in plain bf16, f16 over an E4M3 cache), each warp on its 16 slots of
+//    a tile; units of 17 to 32 rows do the same with two warps per 16 query
+//    rows, each on 32 slots of a tile (two passes of 16), so a row's KV is
+//    streamed once for up to 32 rows; at the segment's end the warps holding
+//    slots 32-63 hand their states to those holding slots 0-31, which merge
+//    them in registers and write the output or partial. Each row is masked
 //    beyond its own token's position and keeps its own softmax state, every
 //    slot holding a new token is substituted from k_new / v_new as below
 //    (quantised over an E4M3 cache), and the chunk appends its own tokens.
-//    With 16 query rows the E4M3 ring takes 3 stages (two CTAs per SM); with
-//    up to 8, the E4M3 kernel runs three CTAs per SM as for single tokens.
+//    With 16 or 32 query rows the E4M3 ring takes 3 stages (two CTAs per
+//    SM); with up to 8, the E4M3 kernel runs three CTAs per SM as for single
+//    tokens.
 //  * the new token (decode step only; the read-only attend reads slot L from
 //    the cache like any other): in the tile that holds slot L the owning warp writes
 //    k_new / v_new into the ring slot of row L (the TMA copy of the stale
@@ -118,11 +124,11 @@ constexpr long long kWaitCycles = 4LL << 30;          // ~2 s at 2 GHz
 
 // Ring geometry for a bfloat16 (QF32 = false) or float32 query over a
 // bfloat16 or E4M3 (KV8) cache.
-template <bool QF32, bool KV8 = false, bool MULTI = false, bool M16 = false>
+template <bool QF32, bool KV8 = false, bool MULTI = false, int MR = 0>
 struct Ring {
-    static constexpr bool kMside = MULTI && M16;   // units of up to 16 query rows
+    static constexpr bool kMside = MULTI && MR > 0;   // units of up to MR (16 or 32) query rows
     static constexpr int kQElem = QF32 ? 4 : 2;
-    static constexpr int kQRows = kMside ? 2 * kGMax : kGMax;        // query rows of a unit
+    static constexpr int kQRows = kMside ? MR : kGMax;               // query rows of a unit
     static constexpr int kQBytes = kQRows * kD * kQElem;             // the unit's query rows
     static constexpr int kKVBytes = KV8 ? kTile * kD : 2 * kHalfBytes; // K (or V) of one tile
     // single-token steps over an E4M3 cache: the new token's bf16 K and V rows
@@ -132,8 +138,8 @@ struct Ring {
     // loads them from global memory)
     static constexpr int kNewBytes = (!MULTI && KV8) ? 1024 : 0;
     static constexpr int kStageBytes = 2 * kKVBytes + kQBytes + kNewBytes;   // K (lo, hi), V (lo, hi), Q, new
-    // E4M3: 4 stages at two CTAs per SM, 2 at three; 3 with the 16 query
-    // rows of a 16-row multi-token unit, so two CTAs still share an SM
+    // E4M3: 4 stages at two CTAs per SM, 2 at three; 3 with the query rows
+    // of a 16- or 32-row multi-token unit, so two CTAs still share an SM
     static constexpr int kNumStages = KV8 ? (kMside ? 3 : (kCtasPerSmKV8 >= 3 ? 2 : 4)) : kStages;
     static constexpr int kCtas = (KV8 && !kMside) ? kCtasPerSmKV8 : kCtasPerSm;   // resident CTAs per SM
     static constexpr int kDynSmem = kNumStages * kStageBytes + 1024;
@@ -364,13 +370,14 @@ __device__ __forceinline__ void job_free() { asm volatile("bar.arrive 3, %0;" ::
 // arrival ticket and, in the last CTA of the unit to arrive, the merge of the
 // K partials (log-sum-exp rule), the output, and the partials and counter
 // back to zero. One warp: the partial outputs are read with all of a lane's
-// loads of one partial in flight at once, so a merge costs about one L2 round
-// trip per partial.
+// loads of one partial (of up to 16 rows at a time) in flight at once, so a
+// merge costs about one L2 round trip per partial and block of rows.
 template <int RW, bool MULTI, int GR, int KM>
 __device__ __noinline__ void fin_ticket_merge(const DecodeParams &p, const FinJob j, MergeBufT<GR, KM> &mb,
                                               int *flag, int lane)
 {
-    constexpr int IT = RW * kD / (32 * 4);   // float4 per lane and partial
+    constexpr int RB = RW > 16 ? 16 : RW;    // rows merged at a time (the registers of acc and v)
+    constexpr int IT = RB * kD / (32 * 4);   // float4 per lane and partial
     const int G = p.G;
     const int u = j.b * p.Hkv + j.kvh;
     const int K = j.last - j.first + 1;
@@ -390,10 +397,6 @@ __device__ __noinline__ void fin_ticket_merge(const DecodeParams &p, const FinJo
         return;
     }
     const long long P0 = (long long)u + j.first;
-    float4 acc[IT];
-#pragma unroll
-    for (int it = 0; it < IT; ++it)
-        acc[it] = make_float4(0.f, 0.f, 0.f, 0.f);
     // every partial's (m, l): weights and the denominator per query row
     for (int k = lane; k < K * G; k += 32) {
         mb.w[k] = __ldcg(p.ws_ml + (P0 * G + k) * 2);
@@ -415,36 +418,43 @@ __device__ __noinline__ void fin_ticket_merge(const DecodeParams &p, const FinJo
         mb.inv_den[lane] = 1.f / den;
     }
     __syncwarp();
-    for (int i = 0; i < K; ++i) {
-        float4 *po = reinterpret_cast<float4 *>(p.ws_o + (P0 + i) * G * kD);
-        float4 v[IT];
+    const int nrow = MULTI ? p.Gh * j.nq : G;
+    for (int r0 = 0; r0 < G; r0 += RB) {
+        const int base = r0 * kD;            // first element of this block of rows
+        float4 acc[IT];
 #pragma unroll
-        for (int it = 0; it < IT; ++it) {
-            const int idx = (it * 32 + lane) * 4;
-            v[it] = idx < G * kD ? __ldcg(po + idx / 4) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+        for (int it = 0; it < IT; ++it)
+            acc[it] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i = 0; i < K; ++i) {
+            float4 *po = reinterpret_cast<float4 *>(p.ws_o + (P0 + i) * G * kD + base);
+            float4 v[IT];
 #pragma unroll
-        for (int it = 0; it < IT; ++it) {
-            const int idx = (it * 32 + lane) * 4;
-            if (idx < G * kD) {
-                const float a = mb.w[i * G + idx / kD];
-                acc[it].x = fmaf(a, v[it].x, acc[it].x);
-                acc[it].y = fmaf(a, v[it].y, acc[it].y);
-                acc[it].z = fmaf(a, v[it].z, acc[it].z);
-                acc[it].w = fmaf(a, v[it].w, acc[it].w);
-                po[idx / 4] = make_float4(0.f, 0.f, 0.f, 0.f);   // consumed: zero-filled again
+            for (int it = 0; it < IT; ++it) {
+                const int idx = base + (it * 32 + lane) * 4;
+                v[it] = idx < G * kD ? __ldcg(po + it * 32 + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int it = 0; it < IT; ++it) {
+                const int idx = base + (it * 32 + lane) * 4;
+                if (idx < G * kD) {
+                    const float a = mb.w[i * G + idx / kD];
+                    acc[it].x = fmaf(a, v[it].x, acc[it].x);
+                    acc[it].y = fmaf(a, v[it].y, acc[it].y);
+                    acc[it].z = fmaf(a, v[it].z, acc[it].z);
+                    acc[it].w = fmaf(a, v[it].w, acc[it].w);
+                    po[it * 32 + lane] = make_float4(0.f, 0.f, 0.f, 0.f);   // consumed: zero-filled again
+                }
             }
         }
-    }
-    const int nrow = MULTI ? p.Gh * j.nq : G;
 #pragma unroll
-    for (int it = 0; it < IT; ++it) {
-        const int idx = (it * 32 + lane) * 4;
-        const int g = idx / kD;
-        if (idx < G * kD && g < nrow) {
-            const float s = mb.inv_den[g];
-            *reinterpret_cast<float4 *>(out_row<MULTI>(p, c, g, kD) + (idx - g * kD)) =
-                make_float4(acc[it].x * s, acc[it].y * s, acc[it].z * s, acc[it].w * s);
+        for (int it = 0; it < IT; ++it) {
+            const int idx = base + (it * 32 + lane) * 4;
+            const int g = idx / kD;
+            if (idx < G * kD && g < nrow) {
+                const float sc = mb.inv_den[g];
+                *reinterpret_cast<float4 *>(out_row<MULTI>(p, c, g, kD) + (idx - g * kD)) =
+                    make_float4(acc[it].x * sc, acc[it].y * sc, acc[it].z * sc, acc[it].w * sc);
+            }
         }
     }
     float *ml = p.ws_ml + P0 * G * 2;
@@ -455,18 +465,25 @@ __device__ __noinline__ void fin_ticket_merge(const DecodeParams &p, const FinJo
     __syncwarp();
 }
 
+// Partials of a cut unit merged through shared memory (more: direct loads),
+// by query rows of a unit.
+constexpr int merge_partials(int rw) { return rw == kGMax ? kMergeMax : (rw == 16 ? 16 : 8); }
+
 // The finisher warp's job slot, merge buffer and flag (kernels with one).
 template <int RW>
 struct FinShared {
     FinJob job;
-    MergeBufT<RW, RW == kGMax ? kMergeMax : 16> merge;
+    MergeBufT<RW, merge_partials(RW)> merge;
     int flag;
 };
 struct NoFinShared {};
 
-// NS ring stages; RW query rows per unit (8, or 16 for multi-token units,
-// whose o rows take less padding to fit two CTAs per SM); FIN: a finisher warp.
-template <int NS, int RW = kGMax, bool FIN = false>
+// NS ring stages; RW query rows per unit (8, or 16 or 32 for multi-token
+// units); FIN: a finisher warp; SW warp states of SR rows each kept for the
+// segment's end (the four warps' states of every row; 32-row units: the two
+// warps holding slots 32-63 of rows 0-15 and 16-31, handed to the two holding
+// slots 0-31).
+template <int NS, int RW = kGMax, bool FIN = false, int SW = kConsumerWarps, int SR = RW>
 struct Shared {
     static constexpr int kOPad = 4;   // rows 132 floats apart: the epilogue's stores are conflict-free
     uint64_t full[NS];
@@ -477,10 +494,10 @@ struct Shared {
     int last_flag;
     long long sched[kMaxWarps + 8];
     TileWalk walk;
-    float m[kConsumerWarps][RW];
-    float l[kConsumerWarps][RW];
-    alignas(16) float o[kConsumerWarps][RW][kD + kOPad];  // rows padded: (near) conflict-free 8-byte stores
-    MergeBufT<RW, RW == kGMax ? kMergeMax : 16> merge;
+    float m[SW][SR];
+    float l[SW][SR];
+    alignas(16) float o[SW][SR][kD + kOPad];  // rows padded: (near) conflict-free 8-byte stores
+    MergeBufT<RW, merge_partials(RW)> merge;
     std::conditional_t<FIN, FinShared<RW>, NoFinShared> fin;
 };
 
@@ -489,28 +506,52 @@ __device__ __forceinline__ void consumer_sync()
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
 }
 
+// consumer_sync that also returns whether v was true in any consumer thread.
+__device__ __forceinline__ bool consumer_sync_or(bool v)
+{
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+                 "bar.red.or.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+                 : "=r"(r)
+                 : "r"((uint32_t)v), "n"(kConsumerWarps * 32)
+                 : "memory");
+    return r != 0;
+}
+
+// The two consumer warps 2 pr and 2 pr + 1 (32-row units: the pair that
+// shares slots 32 pr .. 32 pr + 31 of every tile).
+__device__ __forceinline__ void pair_sync(int pr)
+{
+    asm volatile("bar.sync %0, 64;" ::"r"(4 + pr) : "memory");
+}
+
 
 // WIN: a sliding window is in force. Without one the window fields of the
 // cursor are never read, so they take no registers and no code. MULTI: a
 // multi-token step (the chunk fields of the cursor are read only then). KV8:
-// an E4M3 cache. M16: multi-token units of 9 to 16 query rows, which keep the
-// rows on the M = 16 side of the products; units of up to 8 rows (and every
-// single-token unit) put them on the N = 8 side.
-template <bool QF32, bool WIN, bool MULTI, bool KV8, bool M16>
-__global__ void __launch_bounds__((Ring<QF32, KV8, MULTI, M16>::kThreads), (Ring<QF32, KV8, MULTI, M16>::kCtas))
+// an E4M3 cache. MR: multi-token units of 9 to 16 (MR = 16) or of 17 to 32
+// (MR = 32) query rows, which keep the rows on the M = 16 side of the
+// products; units of up to 8 rows (and every single-token unit, MR = 0) put
+// them on the N = 8 side.
+template <bool QF32, bool WIN, bool MULTI, bool KV8, int MR>
+__global__ void __launch_bounds__((Ring<QF32, KV8, MULTI, MR>::kThreads), (Ring<QF32, KV8, MULTI, MR>::kCtas))
     tc_decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap mk,
                      const __grid_constant__ CUtensorMap mv)
 {
-    using RG = Ring<QF32, KV8, MULTI, M16>;
+    using RG = Ring<QF32, KV8, MULTI, MR>;
     static_assert(!(MULTI && QF32), "multi-token steps take a bfloat16 query");
-    static_assert(MULTI || !M16, "16-row units are multi-token units");
+    static_assert(MR == 0 || (MULTI && (MR == 16 || MR == 32)), "16- and 32-row units are multi-token units");
     constexpr bool kMside = RG::kMside;              // query rows on the M = 16 side
-    constexpr int kRW = kMside ? 2 * kGMax : kGMax;  // query rows of a unit
+    constexpr bool kM32 = kMside && MR == 32;        // two warps per 16 query rows, 32 slots each
+    constexpr int kRW = kMside ? MR : kGMax;         // query rows of a unit
+    constexpr int kSW = kM32 ? 2 : kConsumerWarps;   // warp states kept for the segment's end
+    constexpr int kSR = kM32 ? 16 : kRW;             // rows of each
+    using SharedT = Shared<RG::kNumStages, kRW, RG::kFin, kSW, kSR>;
     constexpr int kStageBytes = RG::kStageBytes;
     constexpr int kNS = RG::kNumStages;   // ring depth
     constexpr int kKVB = RG::kKVBytes;    // K (or V) bytes of one tile
     extern __shared__ uint8_t dyn_smem[];
-    __shared__ Shared<kNS, kRW, RG::kFin> sh;
+    __shared__ SharedT sh;
     uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
     const uint32_t ring_u32 = smem_u32(ring);
 
@@ -721,7 +762,11 @@ __global__ void __launch_bounds__((Ring<QF32, KV8, MULTI, M16>::kThreads), (Ring
 
     // -------------------------------------------------------- consumers --
     const int g0 = lane >> 2, q4 = lane & 3;
-    const int row0 = warp * 16;          // this warp's 16 rows of every tile
+    // this warp's 16 rows of every tile (the slots it substitutes and zeroes,
+    // and, but for 32-row units, the slots it computes on)
+    const int row0 = warp * 16;
+    // 32-row units: query rows rq0 .. rq0 + 15 over slots 32 (warp >> 1) .. +31
+    const int rq0 = kM32 ? 16 * (warp & 1) : 0;
     TileCursor cur;
     bool in_b = false;
     bool more = walk_first(p, cur, walk, in_b);
@@ -770,7 +815,7 @@ __global__ void __launch_bounds__((Ring<QF32, KV8, MULTI, M16>::kThreads), (Ring
                 // this lane's two query rows (g0 and g0 + 8 on the M side, else
                 // 2 q4 and 2 q4 + 1); row r is token r / Gh of the chunk and
                 // attends up to its own position; rows without a token none
-                const int ra = kMside ? g0 : 2 * q4, rb = kMside ? g0 + 8 : 2 * q4 + 1;
+                const int ra = kMside ? rq0 + g0 : 2 * q4, rb = kMside ? rq0 + g0 + 8 : 2 * q4 + 1;
                 qrows = p.Gh * cur.nq;
                 lim = ra < qrows ? L - (cur.nq - 1 - ra / p.Gh) : -1;
                 lim1 = rb < qrows ? L - (cur.nq - 1 - rb / p.Gh) : -1;
@@ -849,12 +894,12 @@ __global__ void __launch_bounds__((Ring<QF32, KV8, MULTI, M16>::kThreads), (Ring
             } else if constexpr (KV8) {
                 // bf16 query as f16 (exact in the normal range); a multi-token
                 // unit's row g0 + 8 is a query row of its own
-                const uint8_t *qs = kring + 2 * kKVB + g0 * (kD * 2);
+                const uint8_t *qs = kring + 2 * kKVB + (rq0 + g0) * (kD * 2);
                 const int nrow = MULTI ? qrows : G;
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     qa[ks][0] = qa[ks][1] = 0u;
-                    if (g0 < nrow) {
+                    if (rq0 + g0 < nrow) {
                         const uint32_t w0 = *reinterpret_cast<const uint32_t *>(qs + (16 * ks + 4 * q4) * 2);
                         const uint32_t w1 = *reinterpret_cast<const uint32_t *>(qs + (16 * ks + 4 * q4 + 2) * 2);
                         qa[ks][0] = pack_f16(bf16_lo(w0), bf16_hi(w0));
@@ -862,7 +907,7 @@ __global__ void __launch_bounds__((Ring<QF32, KV8, MULTI, M16>::kThreads), (Ring
                     }
                     if constexpr (kMside) {
                         ql[ks][0] = ql[ks][1] = 0u;
-                        if (g0 + 8 < nrow) {
+                        if (rq0 + g0 + 8 < nrow) {
                             const uint8_t *qs1 = qs + 8 * (kD * 2);
                             const uint32_t w0 = *reinterpret_cast<const uint32_t *>(qs1 + (16 * ks + 4 * q4) * 2);
                             const uint32_t w1 =
@@ -873,14 +918,14 @@ __global__ void __launch_bounds__((Ring<QF32, KV8, MULTI, M16>::kThreads), (Ring
                     }
                 }
             } else {
-                const uint8_t *qs = kring + 2 * kKVB + g0 * (kD * 2);
+                const uint8_t *qs = kring + 2 * kKVB + (rq0 + g0) * (kD * 2);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
-                    const bool on = g0 < (MULTI ? qrows : G);
+                    const bool on = rq0 + g0 < (MULTI ? qrows : G);
                     qa[ks][0] = on ? *reinterpret_cast<const uint32_t *>(qs + (16 * ks + 2 * q4) * 2) : 0u;
                     qa[ks][1] = on ? *reinterpret_cast<const uint32_t *>(qs + (16 * ks + 8 + 2 * q4) * 2) : 0u;
                     if constexpr (kMside) {   // row g0 + 8: a query row of its own
-                        const bool on1 = g0 + 8 < qrows;
+                        const bool on1 = rq0 + g0 + 8 < qrows;
                         const uint8_t *qs1 = qs + 8 * (kD * 2);
                         ql[ks][0] = on1 ? *reinterpret_cast<const uint32_t *>(qs1 + (16 * ks + 2 * q4) * 2) : 0u;
                         ql[ks][1] = on1 ? *reinterpret_cast<const uint32_t *>(qs1 + (16 * ks + 8 + 2 * q4) * 2) : 0u;
@@ -889,15 +934,16 @@ __global__ void __launch_bounds__((Ring<QF32, KV8, MULTI, M16>::kThreads), (Ring
             }
         }
 
-        if (have && row_good && !tile_bad) {
-            const bool last_tile = (cur.t == cur.nr - 1);
-            // tiles holding new tokens: the last one; in a multi-token step
-            // every tile reaching the row's write offset
-            const bool newt = MULTI ? (slot0 + kTile - 1 >= cur.Lb) : last_tile;
-            // tiles that hold slots outside some row's softmax: those, and,
-            // with a window, those below the last row's window start
-            const bool partial = newt || (WIN && slot0 < (MULTI ? max(0, L - p.window + 1) : cur.lo));
-            if (partial) {
+        const bool last_tile = (cur.t == cur.nr - 1);
+        // tiles holding new tokens: the last one; in a multi-token step
+        // every tile reaching the row's write offset
+        const bool newt = MULTI ? (slot0 + kTile - 1 >= cur.Lb) : last_tile;
+        // tiles that hold slots outside some row's softmax: those, and,
+        // with a window, those below the last row's window start
+        const bool partial = newt || (WIN && slot0 < (MULTI ? max(0, L - p.window + 1) : cur.lo));
+        const bool work = have && row_good && !tile_bad;
+        {
+            if (work && partial) {
                 // new-token rows: substituted from k_new / v_new (and appended
                 // by the unit owning the token); rows no query row attends:
                 // zero V
@@ -999,139 +1045,152 @@ __global__ void __launch_bounds__((Ring<QF32, KV8, MULTI, M16>::kThreads), (Ring
                 }
                 __syncwarp();
             }
-
-
+        }
+        // 32-row units: a warp computes on slots that its pair partner
+        // substituted or zeroed (whatever either warp's wait gave: both walk
+        // the same tiles)
+        if constexpr (kM32) {
+            if (partial && row_good)
+                pair_sync(warp >> 1);
+        }
+        if (work) {
             if constexpr (kMside) {
-                // ---- S = Q K^T for this warp's 16 slots (two n-tiles of 8);
-                // rows g0 and g0 + 8 are query rows of their own; even and odd
-                // k-steps accumulate separately (shorter chains)
-                float s_acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                {
-                    float s_odd[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                    const int mi = lane >> 3, ri = lane & 7;
-                    const int r = row0 + 8 * (mi >> 1) + ri;
-                    if constexpr (KV8) {
-                        // matrix mi: slots 8 (mi >> 1) .. +7, k-step 2 kp + (mi & 1)
-                        // (16 bytes of each row)
 #pragma unroll
-                        for (int kp = 0; kp < 4; ++kp) {
-                            uint32_t kb[4];
-                            ldsm_x4(kbase + swz(r, 2 * kp + (mi & 1)), kb);
+                for (int sb = 0; sb < (kM32 ? 2 : 1); ++sb) {
+                    // the 16 slots of this pass: the warp's own (16-row units), or
+                    // half sb of its 32 (32-row units)
+                    const int crow = kM32 ? 32 * (warp >> 1) + 16 * sb : row0;
+                    // ---- S = Q K^T for these 16 slots (two n-tiles of 8);
+                    // rows g0 and g0 + 8 are query rows of their own; even and odd
+                    // k-steps accumulate separately (shorter chains)
+                    float s_acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                    {
+                        float s_odd[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                        const int mi = lane >> 3, ri = lane & 7;
+                        const int r = crow + 8 * (mi >> 1) + ri;
+                        if constexpr (KV8) {
+                            // matrix mi: slots 8 (mi >> 1) .. +7, k-step 2 kp + (mi & 1)
+                            // (16 bytes of each row)
 #pragma unroll
-                            for (int mm = 0; mm < 4; ++mm) {
-                                const int ks = 2 * kp + (mm & 1), nt = mm >> 1;
-                                uint32_t b0, b1;
-                                e4m3x4_to_f16(kb[mm], b0, b1);
+                            for (int kp = 0; kp < 4; ++kp) {
+                                uint32_t kb[4];
+                                ldsm_x4(kbase + swz(r, 2 * kp + (mi & 1)), kb);
+#pragma unroll
+                                for (int mm = 0; mm < 4; ++mm) {
+                                    const int ks = 2 * kp + (mm & 1), nt = mm >> 1;
+                                    uint32_t b0, b1;
+                                    e4m3x4_to_f16(kb[mm], b0, b1);
+                                    float(&acc)[2][4] = (ks & 1) ? s_odd : s_acc;
+                                    mma_f16(acc[nt], qa[ks][0], ql[ks][0], qa[ks][1], ql[ks][1], b0, b1);
+                                }
+                            }
+                        } else {
+#pragma unroll
+                            for (int ks = 0; ks < 8; ++ks) {
+                                const int c = 2 * ks + (mi & 1);
+                                uint32_t kb[4];
                                 float(&acc)[2][4] = (ks & 1) ? s_odd : s_acc;
-                                mma_f16(acc[nt], qa[ks][0], ql[ks][0], qa[ks][1], ql[ks][1], b0, b1);
+                                ldsm_x4(kbase + (c >> 3) * kHalfBytes + swz(r, c & 7), kb);
+                                mma_bf16(acc[0], qa[ks][0], ql[ks][0], qa[ks][1], ql[ks][1], kb[0], kb[1]);
+                                mma_bf16(acc[1], qa[ks][0], ql[ks][0], qa[ks][1], ql[ks][1], kb[2], kb[3]);
                             }
                         }
-                    } else {
 #pragma unroll
-                        for (int ks = 0; ks < 8; ++ks) {
-                            const int c = 2 * ks + (mi & 1);
-                            uint32_t kb[4];
-                            float(&acc)[2][4] = (ks & 1) ? s_odd : s_acc;
-                            ldsm_x4(kbase + (c >> 3) * kHalfBytes + swz(r, c & 7), kb);
-                            mma_bf16(acc[0], qa[ks][0], ql[ks][0], qa[ks][1], ql[ks][1], kb[0], kb[1]);
-                            mma_bf16(acc[1], qa[ks][0], ql[ks][0], qa[ks][1], ql[ks][1], kb[2], kb[3]);
-                        }
+                        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                s_acc[nt][e] += s_odd[nt][e];
                     }
+                    // two query rows per lane, g0 (c0, c1) and g0 + 8 (c2, c3), each
+                    // with its own causal bound, window and softmax state; P in bf16
+                    // (f16 over an E4M3 cache)
+                    uint32_t pa[4];
+                    const float ssl = KV8 ? ssc : p.scale_log2;
+                    float x0[2][2], x1[2][2];
+                    float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
                     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            s_acc[nt][e] += s_odd[nt][e];
-                }
-                // two query rows per lane, g0 (c0, c1) and g0 + 8 (c2, c3), each
-                // with its own causal bound, window and softmax state; P in bf16
-                // (f16 over an E4M3 cache)
-                uint32_t pa[4];
-                const float ssl = KV8 ? ssc : p.scale_log2;
-                float x0[2][2], x1[2][2];
-                float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int j = slot0 + row0 + 8 * nt + 2 * q4 + e;
-                        const bool on0 = WIN ? attended(lim, lo_r, cur.P, j) : j <= lim;
-                        const bool on1 = WIN ? attended(lim1, lo_r1, cur.P, j) : j <= lim1;
-                        x0[nt][e] = (!partial || on0) ? s_acc[nt][e] * ssl : -INFINITY;
-                        x1[nt][e] = (!partial || on1) ? s_acc[nt][e + 2] * ssl : -INFINITY;
-                        mx0 = fmaxf(mx0, x0[nt][e]);
-                        mx1 = fmaxf(mx1, x1[nt][e]);
-                    }
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-                if (mx0 > m_run + 8.f) {
-                    const float alpha = (m_run == -INFINITY) ? 0.f : fast_ex2(m_run - mx0);
-                    l_run *= alpha;
-#pragma unroll
-                    for (int n = 0; n < kOT; ++n) {
-                        acc_o[n][0] *= alpha;
-                        acc_o[n][1] *= alpha;
-                    }
-                    m_run = mx0;
-                }
-                if (mx1 > m_run1 + 8.f) {
-                    const float alpha = (m_run1 == -INFINITY) ? 0.f : fast_ex2(m_run1 - mx1);
-                    l_run1 *= alpha;
-#pragma unroll
-                    for (int n = 0; n < kOT; ++n) {
-                        acc_o[n][2] *= alpha;
-                        acc_o[n][3] *= alpha;
-                    }
-                    m_run1 = mx1;
-                }
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    float p0[2], p1[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        p0[e] = (x0[nt][e] == -INFINITY) ? 0.f : fast_ex2(x0[nt][e] - m_run);
-                        p1[e] = (x1[nt][e] == -INFINITY) ? 0.f : fast_ex2(x1[nt][e] - m_run1);
-                        l_run += p0[e];
-                        l_run1 += p1[e];
-                    }
-                    // row g0: slots 8nt + 2q4, +1; then row g0 + 8
-                    pa[2 * nt] = KV8 ? pack_f16(p0[0], p0[1]) : pack_bf16(p0[0], p0[1]);
-                    pa[2 * nt + 1] = KV8 ? pack_f16(p1[0], p1[1]) : pack_bf16(p1[0], p1[1]);
-                }
-                // ---- O += P V (16 n-tiles of 8 dims)
-                {
-                    const int mi = lane >> 3, ri = lane & 7;
-                    const int r = row0 + 8 * (mi & 1) + ri;
-                    if constexpr (KV8) {
-                        // matrix mi: slots 8 (mi & 1) .. +7, 16-dim block
-                        // 2 bp + (mi >> 1); each lane gets bytes (s, d), (s, d+1),
-                        // (s+1, d), (s+1, d+1) and splits them into the (s, s+1)
-                        // pairs of dim d (even) and d + 1 (odd)
-#pragma unroll
-                        for (int bp = 0; bp < 4; ++bp) {
-                            uint32_t vb[4];
-                            ldsm_x4_t(vbase + swz(r, 2 * bp + (mi >> 1)), vb);
-                            uint32_t ev[4], od[4];
-#pragma unroll
-                            for (int mm = 0; mm < 4; ++mm)
-                                e4m3x4_to_f16(__byte_perm(vb[mm], 0u, 0x3120u), ev[mm], od[mm]);
-#pragma unroll
-                            for (int hb = 0; hb < 2; ++hb) {   // block 2 bp + hb: matrices 2 hb (slots 0-7), 2 hb + 1
-                                const int blk = 2 * bp + hb;
-                                mma_f16(acc_o[2 * blk], pa[0], pa[1], pa[2], pa[3], ev[2 * hb], ev[2 * hb + 1]);
-                                mma_f16(acc_o[2 * blk + 1], pa[0], pa[1], pa[2], pa[3], od[2 * hb], od[2 * hb + 1]);
-                            }
+                        for (int e = 0; e < 2; ++e) {
+                            const int j = slot0 + crow + 8 * nt + 2 * q4 + e;
+                            const bool on0 = WIN ? attended(lim, lo_r, cur.P, j) : j <= lim;
+                            const bool on1 = WIN ? attended(lim1, lo_r1, cur.P, j) : j <= lim1;
+                            x0[nt][e] = (!partial || on0) ? s_acc[nt][e] * ssl : -INFINITY;
+                            x1[nt][e] = (!partial || on1) ? s_acc[nt][e + 2] * ssl : -INFINITY;
+                            mx0 = fmaxf(mx0, x0[nt][e]);
+                            mx1 = fmaxf(mx1, x1[nt][e]);
                         }
-                    } else {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+                    if (mx0 > m_run + 8.f) {
+                        const float alpha = (m_run == -INFINITY) ? 0.f : fast_ex2(m_run - mx0);
+                        l_run *= alpha;
 #pragma unroll
-                        for (int np = 0; np < 8; ++np) {
-                            const int c = 2 * np + (mi >> 1);
-                            uint32_t vb[4];
-                            ldsm_x4_t(vbase + (c >> 3) * kHalfBytes + swz(r, c & 7), vb);
-                            mma_bf16(acc_o[2 * np], pa[0], pa[1], pa[2], pa[3], vb[0], vb[1]);
-                            mma_bf16(acc_o[2 * np + 1], pa[0], pa[1], pa[2], pa[3], vb[2], vb[3]);
+                        for (int n = 0; n < kOT; ++n) {
+                            acc_o[n][0] *= alpha;
+                            acc_o[n][1] *= alpha;
+                        }
+                        m_run = mx0;
+                    }
+                    if (mx1 > m_run1 + 8.f) {
+                        const float alpha = (m_run1 == -INFINITY) ? 0.f : fast_ex2(m_run1 - mx1);
+                        l_run1 *= alpha;
+#pragma unroll
+                        for (int n = 0; n < kOT; ++n) {
+                            acc_o[n][2] *= alpha;
+                            acc_o[n][3] *= alpha;
+                        }
+                        m_run1 = mx1;
+                    }
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        float p0[2], p1[2];
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            p0[e] = (x0[nt][e] == -INFINITY) ? 0.f : fast_ex2(x0[nt][e] - m_run);
+                            p1[e] = (x1[nt][e] == -INFINITY) ? 0.f : fast_ex2(x1[nt][e] - m_run1);
+                            l_run += p0[e];
+                            l_run1 += p1[e];
+                        }
+                        // row g0: slots 8nt + 2q4, +1; then row g0 + 8
+                        pa[2 * nt] = KV8 ? pack_f16(p0[0], p0[1]) : pack_bf16(p0[0], p0[1]);
+                        pa[2 * nt + 1] = KV8 ? pack_f16(p1[0], p1[1]) : pack_bf16(p1[0], p1[1]);
+                    }
+                    // ---- O += P V (16 n-tiles of 8 dims)
+                    {
+                        const int mi = lane >> 3, ri = lane & 7;
+                        const int r = crow + 8 * (mi & 1) + ri;
+                        if constexpr (KV8) {
+                            // matrix mi: slots 8 (mi & 1) .. +7, 16-dim block
+                            // 2 bp + (mi >> 1); each lane gets bytes (s, d), (s, d+1),
+                            // (s+1, d), (s+1, d+1) and splits them into the (s, s+1)
+                            // pairs of dim d (even) and d + 1 (odd)
+#pragma unroll
+                            for (int bp = 0; bp < 4; ++bp) {
+                                uint32_t vb[4];
+                                ldsm_x4_t(vbase + swz(r, 2 * bp + (mi >> 1)), vb);
+                                uint32_t ev[4], od[4];
+#pragma unroll
+                                for (int mm = 0; mm < 4; ++mm)
+                                    e4m3x4_to_f16(__byte_perm(vb[mm], 0u, 0x3120u), ev[mm], od[mm]);
+#pragma unroll
+                                for (int hb = 0; hb < 2; ++hb) {   // block 2 bp + hb: matrices 2 hb (slots 0-7), 2 hb + 1
+                                    const int blk = 2 * bp + hb;
+                                    mma_f16(acc_o[2 * blk], pa[0], pa[1], pa[2], pa[3], ev[2 * hb], ev[2 * hb + 1]);
+                                    mma_f16(acc_o[2 * blk + 1], pa[0], pa[1], pa[2], pa[3], od[2 * hb], od[2 * hb + 1]);
+                                }
+                            }
+                        } else {
+#pragma unroll
+                            for (int np = 0; np < 8; ++np) {
+                                const int c = 2 * np + (mi >> 1);
+                                uint32_t vb[4];
+                                ldsm_x4_t(vbase + (c >> 3) * kHalfBytes + swz(r, c & 7), vb);
+                                mma_bf16(acc_o[2 * np], pa[0], pa[1], pa[2], pa[3], vb[0], vb[1]);
+                                mma_bf16(acc_o[2 * np + 1], pa[0], pa[1], pa[2], pa[3], vb[2], vb[3]);
+                            }
                         }
                     }
                 }
@@ -1310,121 +1369,226 @@ __global__ void __launch_bounds__((Ring<QF32, KV8, MULTI, M16>::kThreads), (Ring
         const bool unit_done = (cur.t == cur.nr - 1);
         const bool range_done = (cur.g + 1 == cur.end);
         if (unit_done || range_done) {
-            // ---- merge the four warps' states and emit
-            if constexpr (kMside) {   // rows g0 and g0 + 8, each its own query row
-                float l_tot = l_run;
+            // a cut unit's arrival ticket (and the merge, when last) handed to the
+            // finisher warp: not in the CTA's last segment, where nothing is left
+            // to overlap with and four warps merge faster than one
+            const bool to_fin = RG::kFin && !(range_done && (in_b || walk.b.g >= walk.b.end));
+            auto post_job = [&] {
+                if constexpr (RG::kFin) {
+                    const long long first_tile = cur.g - cur.t;
+                    job_wait_free();
+                    if (tid == 0) {
+                        FinJob j;
+                        j.stop = 0;
+                        j.first = cta_of_tile(first_tile, walk.N, walk.C);
+                        j.last = cta_of_tile(first_tile + cur.nr - 1, walk.N, walk.C);
+                        j.b = cur.b;
+                        j.kvh = cur.kvh;
+                        j.nq = MULTI ? cur.nq : 1;
+                        j.tokL = MULTI ? cur.tokL : cur.b;
+                        sh.fin.job = j;
+                    }
+                    job_post();
+                }
+            };
+            if constexpr (kM32) {
+                // ---- 32-row units: warps 2 and 3 (slots 32-63 of every tile)
+                // hand their states of rows rq0 + g0 and rq0 + g0 + 8 to warps 0
+                // and 1 (slots 0-31, the same rows), which merge them in registers
+                // and write the output (a whole unit) or the partial state
+                float l_tot = l_run, l_tot1 = l_run1;
                 l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 1);
                 l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 2);
-                float l_tot1 = l_run1;
                 l_tot1 += __shfl_xor_sync(0xffffffffu, l_tot1, 1);
                 l_tot1 += __shfl_xor_sync(0xffffffffu, l_tot1, 2);
-                if (q4 == 0) {
-                    sh.m[warp][g0] = m_run;
-                    sh.l[warp][g0] = l_tot;
-                    sh.m[warp][g0 + 8] = m_run1;
-                    sh.l[warp][g0 + 8] = l_tot1;
+                const float osc = KV8 ? vsc : 1.f;   // the V scale of an E4M3 cache
+                // n-tile n holds dims dn(n) (c0, c2) and dn(n) + de (c1, c3)
+                constexpr int de = KV8 ? 2 : 1;
+                auto dn = [&](int n) { return KV8 ? 16 * (n >> 1) + 4 * q4 + (n & 1) : 8 * n + 2 * q4; };
+                if (warp >= 2) {
+                    const int sw = warp - 2;
+                    if (q4 == 0) {
+                        sh.m[sw][g0] = m_run;
+                        sh.l[sw][g0] = l_tot;
+                        sh.m[sw][g0 + 8] = m_run1;
+                        sh.l[sw][g0 + 8] = l_tot1;
+                    }
+    #pragma unroll
+                    for (int n = 0; n < kOT; ++n) {
+                        const int d = dn(n);
+                        sh.o[sw][g0][d] = acc_o[n][0] * osc;
+                        sh.o[sw][g0][d + de] = acc_o[n][1] * osc;
+                        sh.o[sw][g0 + 8][d] = acc_o[n][2] * osc;
+                        sh.o[sw][g0 + 8][d + de] = acc_o[n][3] * osc;
+                    }
                 }
-#pragma unroll
-                for (int n = 0; n < kOT; ++n) {
-                    if constexpr (KV8) {
-                        // n-tile n = 2 blk + parity holds dims 16 blk + 4 q4 +
-                        // parity (+2); times the V scale
-                        const int d = 16 * (n >> 1) + 4 * q4 + (n & 1);
-                        sh.o[warp][g0][d] = acc_o[n][0] * vsc;
-                        sh.o[warp][g0][d + 2] = acc_o[n][1] * vsc;
-                        sh.o[warp][g0 + 8][d] = acc_o[n][2] * vsc;
-                        sh.o[warp][g0 + 8][d + 2] = acc_o[n][3] * vsc;
+                const bool bad = consumer_sync_or(!row_good || seg_bad);
+                const bool any_abort = consumer_sync_or(aborted);
+                if (bad && row_good && tid == 0)
+                    report(p, any_abort ? kTimeout : kBadBlock);
+                const bool whole = (seg_first_t == 0) && unit_done;
+                if (warp < 2) {
+                    const int G = p.G;
+                    const int nrow = p.Gh * cur.nq;           // query rows with an output
+                    const long long P = (long long)cur.b * p.Hkv + cur.kvh + blockIdx.x;
+                    const float qnan = __int_as_float(0x7fc00000);
+                    float sc[2], wo[2], wl[2];                // per row: own weight, other's weight
+                    int rr[2];
+    #pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int gr = g0 + 8 * h;            // row within the warp's 16
+                        const float ms = h ? m_run1 : m_run, ls = h ? l_tot1 : l_tot;
+                        const float mo = sh.m[warp][gr], lo = sh.l[warp][gr];
+                        float M = fmaxf(ms, mo);
+                        const float as = (ms == -INFINITY) ? 0.f : fast_ex2(ms - M);
+                        const float ao = (mo == -INFINITY) ? 0.f : fast_ex2(mo - M);
+                        float den = as * ls + ao * lo;
+                        rr[h] = rq0 + gr;
+                        wl[h] = as * osc;
+                        wo[h] = ao;
+                        if (whole) {
+                            // the normalisation, with the sink logit when given
+                            const float sk = p.sink ? sink_log2(p, cur.kvh * p.Gh + rr[h] % p.Gh) : -INFINITY;
+                            const float Mx = fmaxf(M, sk);
+                            const float a = (M == -INFINITY) ? 0.f : fast_ex2(M - Mx);
+                            den = a * den + ((sk == -INFINITY) ? 0.f : fast_ex2(sk - Mx));
+                            sc[h] = a / den;
+                        } else {
+                            sc[h] = 1.f;
+                            if (q4 == 0 && rr[h] < G) {
+                                p.ws_ml[(P * G + rr[h]) * 2 + 0] = bad ? qnan : M;
+                                p.ws_ml[(P * G + rr[h]) * 2 + 1] = bad ? qnan : den;
+                            }
+                        }
+                    }
+    #pragma unroll
+                    for (int n = 0; n < kOT; ++n) {
+                        const int d = dn(n);
+    #pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int gr = g0 + 8 * h;
+                            const float v0 = fmaf(wl[h], acc_o[n][2 * h], wo[h] * sh.o[warp][gr][d]) * sc[h];
+                            const float v1 = fmaf(wl[h], acc_o[n][2 * h + 1], wo[h] * sh.o[warp][gr][d + de]) * sc[h];
+                            float *dst = nullptr;
+                            if (whole && rr[h] < nrow)
+                                dst = out_row<MULTI>(p, cur, rr[h], kD);
+                            else if (!whole && rr[h] < G)
+                                dst = p.ws_o + (P * G + rr[h]) * kD;
+                            if (dst) {
+                                dst[d] = bad ? qnan : v0;
+                                dst[d + de] = bad ? qnan : v1;
+                            }
+                        }
+                    }
+                }
+                consumer_sync();   // the output or partial stores before the ticket
+                if (!whole) {
+                    if (to_fin) {
+                        post_job();
                     } else {
-                        *reinterpret_cast<float2 *>(&sh.o[warp][g0][8 * n + 2 * q4]) =
-                            make_float2(acc_o[n][0], acc_o[n][1]);
-                        *reinterpret_cast<float2 *>(&sh.o[warp][g0 + 8][8 * n + 2 * q4]) =
-                            make_float2(acc_o[n][2], acc_o[n][3]);
+                        const long long first_tile = cur.g - cur.t;
+                        const int first = cta_of_tile(first_tile, walk.N, walk.C);
+                        const int last = cta_of_tile(first_tile + cur.nr - 1, walk.N, walk.C);
+                        unit_ticket_merge<kD, MULTI, !KV8>(p, cur, first, last, &sh.last_flag, sh.merge, tid,
+                                                           kConsumerWarps * 32, [] { consumer_sync(); }, pre_cnt);
                     }
                 }
             } else {
-                // rows 2 q4 and 2 q4 + 1; the eight lanes sharing q4 hold
-                // different slots of them
-                float l_tot = l_run, l_tot1 = l_run1;
-#pragma unroll
-                for (int off = 4; off < 32; off <<= 1) {
-                    l_tot += __shfl_xor_sync(0xffffffffu, l_tot, off);
-                    l_tot1 += __shfl_xor_sync(0xffffffffu, l_tot1, off);
-                }
-                const int r0 = 2 * q4, r1 = r0 + 1;
-                if (g0 == 0) {
-                    if (r0 < G) {
-                        sh.m[warp][r0] = m_run;
-                        sh.l[warp][r0] = l_tot;
+                // ---- merge the four warps' states and emit
+                if constexpr (kMside) {   // rows g0 and g0 + 8, each its own query row
+                    float l_tot = l_run;
+                    l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 1);
+                    l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 2);
+                    float l_tot1 = l_run1;
+                    l_tot1 += __shfl_xor_sync(0xffffffffu, l_tot1, 1);
+                    l_tot1 += __shfl_xor_sync(0xffffffffu, l_tot1, 2);
+                    if (q4 == 0) {
+                        sh.m[warp][g0] = m_run;
+                        sh.l[warp][g0] = l_tot;
+                        sh.m[warp][g0 + 8] = m_run1;
+                        sh.l[warp][g0 + 8] = l_tot1;
                     }
-                    if (r1 < G) {
-                        sh.m[warp][r1] = m_run1;
-                        sh.l[warp][r1] = l_tot1;
+    #pragma unroll
+                    for (int n = 0; n < kOT; ++n) {
+                        if constexpr (KV8) {
+                            // n-tile n = 2 blk + parity holds dims 16 blk + 4 q4 +
+                            // parity (+2); times the V scale
+                            const int d = 16 * (n >> 1) + 4 * q4 + (n & 1);
+                            sh.o[warp][g0][d] = acc_o[n][0] * vsc;
+                            sh.o[warp][g0][d + 2] = acc_o[n][1] * vsc;
+                            sh.o[warp][g0 + 8][d] = acc_o[n][2] * vsc;
+                            sh.o[warp][g0 + 8][d + 2] = acc_o[n][3] * vsc;
+                        } else {
+                            *reinterpret_cast<float2 *>(&sh.o[warp][g0][8 * n + 2 * q4]) =
+                                make_float2(acc_o[n][0], acc_o[n][1]);
+                            *reinterpret_cast<float2 *>(&sh.o[warp][g0 + 8][8 * n + 2 * q4]) =
+                                make_float2(acc_o[n][2], acc_o[n][3]);
+                        }
                     }
-                }
-#pragma unroll
-                for (int n = 0; n < kOT; ++n) {
-                    if constexpr (KV8) {
-                        // m-tile n: dims 16 n + 2 g0 (c0, c1) and + 1 (c2, c3);
-                        // times the V scale
-                        const int d = 16 * n + 2 * g0;
-                        if (r0 < G)
-                            *reinterpret_cast<float2 *>(&sh.o[warp][r0][d]) =
-                                make_float2(acc_o[n][0] * vsc, acc_o[n][2] * vsc);
-                        if (r1 < G)
-                            *reinterpret_cast<float2 *>(&sh.o[warp][r1][d]) =
-                                make_float2(acc_o[n][1] * vsc, acc_o[n][3] * vsc);
-                    } else {
-                        // m-tile n: dims 16 n + g0 (c0, c1) and + 8 (c2, c3)
-                        const int d = 16 * n + g0;
+                } else {
+                    // rows 2 q4 and 2 q4 + 1; the eight lanes sharing q4 hold
+                    // different slots of them
+                    float l_tot = l_run, l_tot1 = l_run1;
+    #pragma unroll
+                    for (int off = 4; off < 32; off <<= 1) {
+                        l_tot += __shfl_xor_sync(0xffffffffu, l_tot, off);
+                        l_tot1 += __shfl_xor_sync(0xffffffffu, l_tot1, off);
+                    }
+                    const int r0 = 2 * q4, r1 = r0 + 1;
+                    if (g0 == 0) {
                         if (r0 < G) {
-                            sh.o[warp][r0][d] = acc_o[n][0];
-                            sh.o[warp][r0][d + 8] = acc_o[n][2];
+                            sh.m[warp][r0] = m_run;
+                            sh.l[warp][r0] = l_tot;
                         }
                         if (r1 < G) {
-                            sh.o[warp][r1][d] = acc_o[n][1];
-                            sh.o[warp][r1][d + 8] = acc_o[n][3];
+                            sh.m[warp][r1] = m_run1;
+                            sh.l[warp][r1] = l_tot1;
+                        }
+                    }
+    #pragma unroll
+                    for (int n = 0; n < kOT; ++n) {
+                        if constexpr (KV8) {
+                            // m-tile n: dims 16 n + 2 g0 (c0, c1) and + 1 (c2, c3);
+                            // times the V scale
+                            const int d = 16 * n + 2 * g0;
+                            if (r0 < G)
+                                *reinterpret_cast<float2 *>(&sh.o[warp][r0][d]) =
+                                    make_float2(acc_o[n][0] * vsc, acc_o[n][2] * vsc);
+                            if (r1 < G)
+                                *reinterpret_cast<float2 *>(&sh.o[warp][r1][d]) =
+                                    make_float2(acc_o[n][1] * vsc, acc_o[n][3] * vsc);
+                        } else {
+                            // m-tile n: dims 16 n + g0 (c0, c1) and + 8 (c2, c3)
+                            const int d = 16 * n + g0;
+                            if (r0 < G) {
+                                sh.o[warp][r0][d] = acc_o[n][0];
+                                sh.o[warp][r0][d + 8] = acc_o[n][2];
+                            }
+                            if (r1 < G) {
+                                sh.o[warp][r1][d] = acc_o[n][1];
+                                sh.o[warp][r1][d + 8] = acc_o[n][3];
+                            }
                         }
                     }
                 }
-            }
-            consumer_sync();
-            const bool bad = !row_good || seg_bad;
-            if (bad && row_good && tid == 0)
-                report(p, aborted ? kTimeout : kBadBlock);
-            // With a finisher warp, a cut unit's ticket and merge go to it --
-            // but not in the CTA's last segment: nothing is left to overlap
-            // with there, and four warps merge faster than one.
-            bool handed = false;
-            if constexpr (RG::kFin) {
-                if (!(range_done && (in_b || walk.b.g >= walk.b.end))) {
-                    handed = true;
-                    // the output (a whole unit) or the partial state
-                    if (!segment_out<kConsumerWarps, kRW, kD, kD + Shared<kNS, kRW, RG::kFin>::kOPad, MULTI>(
+                consumer_sync();
+                const bool bad = !row_good || seg_bad;
+                if (bad && row_good && tid == 0)
+                    report(p, aborted ? kTimeout : kBadBlock);
+                if (to_fin) {
+                    // the output (a whole unit) or the partial state; a cut unit's
+                    // ticket and merge go to the finisher
+                    if (!segment_out<kSW, kSR, kD, kD + SharedT::kOPad, MULTI>(
                             p, cur, seg_first_t, bad, sh.m, sh.l, sh.o, sh.merge, tid, kConsumerWarps * 32,
-                            [] { consumer_sync(); })) {
-                        const long long first_tile = cur.g - cur.t;
-                        job_wait_free();
-                        if (tid == 0) {
-                            FinJob j;
-                            j.stop = 0;
-                            j.first = cta_of_tile(first_tile, walk.N, walk.C);
-                            j.last = cta_of_tile(first_tile + cur.nr - 1, walk.N, walk.C);
-                            j.b = cur.b;
-                            j.kvh = cur.kvh;
-                            j.nq = MULTI ? cur.nq : 1;
-                            j.tokL = MULTI ? cur.tokL : cur.b;
-                            sh.fin.job = j;
-                        }
-                        job_post();
-                    }
+                            [] { consumer_sync(); }))
+                        post_job();
+                } else {
+                    // the merge's preload of partial outputs costs registers: off
+                    // for the E4M3 kernels (at their 128-register cap)
+                    finish_segment<kSW, kSR, kD, kD + SharedT::kOPad, MULTI, !KV8>(
+                        p, cur, walk, seg_first_t, bad, sh.m, sh.l, sh.o, &sh.last_flag, sh.merge, tid,
+                        kConsumerWarps * 32, [] { consumer_sync(); }, pre_cnt);
                 }
-            }
-            if (!handed) {
-                // the merge's preload of partial outputs costs registers: off
-                // for the E4M3 kernels (at their 128-register cap)
-                finish_segment<kConsumerWarps, kRW, kD, kD + Shared<kNS, kRW, RG::kFin>::kOPad, MULTI, !KV8>(
-                    p, cur, walk, seg_first_t, bad, sh.m, sh.l, sh.o, &sh.last_flag, sh.merge, tid,
-                    kConsumerWarps * 32, [] { consumer_sync(); }, pre_cnt);
             }
             seg_start = true;
         }
@@ -1439,10 +1603,10 @@ __global__ void __launch_bounds__((Ring<QF32, KV8, MULTI, M16>::kThreads), (Ring
 }
 
 
-template <bool QF32, bool WIN, bool MULTI, bool KV8 = false, bool M16 = false>
+template <bool QF32, bool WIN, bool MULTI, bool KV8 = false, int MR = 0>
 cudaError_t launch_q(const DecodeParams &p, const TcMaps &maps, cudaStream_t st)
 {
-    constexpr int kDynSmem = Ring<QF32, KV8, MULTI, M16>::kDynSmem;
+    constexpr int kDynSmem = Ring<QF32, KV8, MULTI, MR>::kDynSmem;
     // The shared-memory limit is a per-device attribute of the kernel: set it
     // once on every device this instantiation is launched on (a bit per
     // device; devices beyond 64 set it on every launch).
@@ -1453,7 +1617,7 @@ cudaError_t launch_q(const DecodeParams &p, const TcMaps &maps, cudaStream_t st)
         return e;
     const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
     if (!bit || !(attr_set.load(std::memory_order_acquire) & bit)) {
-        e = cudaFuncSetAttribute(tc_decode_kernel<QF32, WIN, MULTI, KV8, M16>,
+        e = cudaFuncSetAttribute(tc_decode_kernel<QF32, WIN, MULTI, KV8, MR>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem);
         if (e != cudaSuccess)
             return e;
@@ -1461,7 +1625,7 @@ cudaError_t launch_q(const DecodeParams &p, const TcMaps &maps, cudaStream_t st)
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.grid);
-    cfg.blockDim = dim3(Ring<QF32, KV8, MULTI, M16>::kThreads);
+    cfg.blockDim = dim3(Ring<QF32, KV8, MULTI, MR>::kThreads);
     cfg.dynamicSmemBytes = kDynSmem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -1469,7 +1633,7 @@ cudaError_t launch_q(const DecodeParams &p, const TcMaps &maps, cudaStream_t st)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tc_decode_kernel<QF32, WIN, MULTI, KV8, M16>, p, maps.k, maps.v);
+    return cudaLaunchKernelEx(&cfg, tc_decode_kernel<QF32, WIN, MULTI, KV8, MR>, p, maps.k, maps.v);
 }
 
 }  // namespace

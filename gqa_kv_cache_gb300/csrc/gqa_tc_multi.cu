@@ -9,19 +9,27 @@ cudaError_t tc_launch_multi(const DecodeParams &p, const TcMaps &maps, cudaStrea
     if (!p.q_bf16)
         return cudaErrorInvalidValue;
     const bool win = p.window > 0;
-    // units of more than 8 query rows keep the rows on the M = 16 side
+    // units of more than 8 query rows keep the rows on the M = 16 side: up
+    // to 16 one M tile per warp, up to 32 two warps per M tile
+    if (p.G > 16) {
+        if (p.kv8)
+            return win ? launch_q<false, true, true, true, 32>(p, maps, st)
+                       : launch_q<false, false, true, true, 32>(p, maps, st);
+        return win ? launch_q<false, true, true, false, 32>(p, maps, st)
+                   : launch_q<false, false, true, false, 32>(p, maps, st);
+    }
     if (p.G > 8) {
         if (p.kv8)
-            return win ? launch_q<false, true, true, true, true>(p, maps, st)
-                       : launch_q<false, false, true, true, true>(p, maps, st);
-        return win ? launch_q<false, true, true, false, true>(p, maps, st)
-                   : launch_q<false, false, true, false, true>(p, maps, st);
+            return win ? launch_q<false, true, true, true, 16>(p, maps, st)
+                       : launch_q<false, false, true, true, 16>(p, maps, st);
+        return win ? launch_q<false, true, true, false, 16>(p, maps, st)
+                   : launch_q<false, false, true, false, 16>(p, maps, st);
     }
     if (p.kv8)
-        return win ? launch_q<false, true, true, true, false>(p, maps, st)
-                   : launch_q<false, false, true, true, false>(p, maps, st);
-    return win ? launch_q<false, true, true, false, false>(p, maps, st)
-               : launch_q<false, false, true, false, false>(p, maps, st);
+        return win ? launch_q<false, true, true, true, 0>(p, maps, st)
+                   : launch_q<false, false, true, true, 0>(p, maps, st);
+    return win ? launch_q<false, true, true, false, 0>(p, maps, st)
+               : launch_q<false, false, true, false, 0>(p, maps, st);
 }
 
 }  // namespace gqa

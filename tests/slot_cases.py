@@ -215,7 +215,7 @@ def plant_dominant(st, seed, grid=0, unit_parts=False):
             continue
         last = st.last[b]
         first_new = st.Lb[b] if not st.attend else last
-        cand = [0, 63, 64, 127, 128, last - 1, last, first_new, first_new - 1, 16, 15]
+        cand = [0, 63, 64, 127, 128, last - 1, last, first_new, first_new - 1, 16, 15, 31, 32, 47, 48]
         for kvh in range(w.Hkv):
             u = torch.randn(w.D, generator=g)
             for tok, _ in st.rows(b):
@@ -289,7 +289,8 @@ SINGLE = [
 
 MULTI = [
     # name, family, sizes, q_lens: query rows per unit G * q_len (up to 8: rows on
-    # the N side of the products; 9 to 16: the M side; 18: two chunks)
+    # the N side of the products; 9 to 16: the M side, one warp per 16 slots; 17
+    # to 32: the M side, two warps per 16 rows; 40: two chunks)
     ("rows8_g4", "llama3_8b", dict(B=6, Smax=520, len_lo=0, len_hi=500, seed=611), [2, 1, 2, 0, 2, 2]),
     ("rows16_g4", "llama3_8b", dict(B=5, Smax=520, len_lo=0, len_hi=500, seed=612), [4, 3, 4, 1, 4]),
     ("rows16_g8_paged16", "paged", dict(Hq=16, Hkv=2, B=4, num_blocks=4 * 40, max_blocks=40, len_lo=0,
@@ -298,6 +299,9 @@ MULTI = [
                                         seed=614), [3, 3, 2, 3]),
     ("rows8_g4_paged8", "paged", dict(Hq=8, Hkv=2, B=4, block_size=8, num_blocks=4 * 70, max_blocks=70,
                                       len_lo=0, len_hi=540, seed=615), [2, 2, 1, 2]),
+    ("rows32_g4", "llama3_8b", dict(B=5, Smax=520, len_lo=0, len_hi=500, seed=616), [8, 5, 8, 1, 7]),
+    ("rows40_g8", "long_context", dict(B=4, Smax=600, len_lo=60, len_hi=560, key_scale=1.0, seed=617),
+     [5, 4, 5, 2]),
 ]
 
 # capacities the small-cache kernel takes (K and V of a row within 200 KB of

@@ -3,8 +3,9 @@ packed tokens cu_q[b] .. cu_q[b+1]-1 of row b are appended in place at slots
 lengths[b] + i and token i attends slots 0 .. lengths[b] + i
 ("groupQueryAttention": packed q/k/v, write offset cu_seqlens_k[b] - q_len[b],
 the causal bound). Against the CPU oracle on the same seeded inputs, both
-kernels, dense / slot_ids / paged, group sizes 1..8 (tokens per chunk: 16 / G
-on the tensor cores, 8 / G on the CUDA cores),
+kernels, dense / slot_ids / paged, group sizes 1..8 (tokens per chunk: 32 / G
+on the tensor cores, 8 / G on the CUDA cores; units of up to 8, 16 and 32
+query rows on the tensor cores),
 rows with q_len 0, chunks crossing tiles, the softmax modifiers, E4M3 caches
 (each appended token quantised); the whole cache is compared with the
 oracle's appended host copy bit for bit. Bars: float32 1e-5; bfloat16 and
@@ -97,7 +98,7 @@ def check_multi(w, q_lens, kernel="auto", grid=0, fp8=False, **mods):
     err = float(np.abs(got - want).max()) if got.size else 0.0
     assert err <= tol, f"max abs error {err} > {tol}"
     G = w.Hq // w.Hkv
-    tpc = max(1, min(16 // G if kernel != "simt" else 8 // G, max_q))
+    tpc = max(1, min(32 // G if kernel != "simt" else 8 // G, max_q))
     guard(path_of(w, kernel, fp8=fp8, unit_rows=G * tpc), err, vmax)
     for n in (("k_blocks", "v_blocks") if w.paged else ("k_cache", "v_cache")):
         assert to_np(t[n]).tobytes() == a[n].tobytes(), f"{n} differs from the oracle's appended copy"
@@ -117,9 +118,20 @@ CASES = [
                                 len_lo=0, len_hi=310, seed=408), [3, 6, 2]),
     ("f32_d64", "pr1_fp32", dict(B=3, Smax=256, len_lo=0, len_hi=250, seed=409), [3, 1, 4]),
     # full 16-row units on the tensor cores (and two 8-row chunks on the CUDA cores)
-    ("g4_rows16", "llama3_8b", dict(B=3, Smax=400, len_lo=0, len_hi=390, seed=413), [4, 8, 3]),
+    ("g4_rows16", "llama3_8b", dict(B=3, Smax=400, len_lo=0, len_hi=390, seed=413), [4, 4, 3]),
     ("g2_rows16", "llama3_8b", dict(Hq=4, Hkv=2, B=2, Smax=300, len_lo=0, len_hi=290, seed=414), [8, 16]),
     ("g1_rows16", "llama3_8b", dict(Hq=2, Hkv=2, B=2, Smax=300, len_lo=0, len_hi=280, seed=415), [16, 5]),
+    # units of 17 to 32 query rows on the tensor cores (two warps per 16 rows),
+    # and rows of more tokens than one unit holds (several chunks)
+    ("g4_rows32", "llama3_8b", dict(B=3, Smax=400, len_lo=0, len_hi=390, seed=423), [8, 5, 7]),
+    ("g6_rows18_paged16", "paged", dict(B=4, num_blocks=4 * 30, max_blocks=30, len_lo=0, len_hi=460, seed=424),
+     [3, 3, 2, 3]),
+    ("g8_rows32", "long_context", dict(B=3, Smax=400, len_lo=50, len_hi=390, seed=425), [4, 3, 4]),
+    ("g8_rows40", "long_context", dict(B=3, Smax=400, len_lo=50, len_hi=390, seed=426), [5, 2, 6]),
+    ("g2_rows32_slots", "ragged_slots", dict(Hq=8, Hkv=4, B=3, R=7, Smax=300, len_lo=1, len_hi=280, seed=427),
+     [16, 11, 9]),
+    ("g4_rows32_paged8", "paged", dict(Hq=8, Hkv=2, B=3, block_size=8, num_blocks=3 * 40, max_blocks=40,
+                                       len_lo=0, len_hi=300, seed=428), [8, 6, 8]),
     # units of at most 8 query rows (one chunk): on the tensor cores the rows
     # sit on the N = 8 side of the products
     ("g4_rows8", "llama3_8b", dict(B=5, Smax=400, len_lo=0, len_hi=390, seed=417), [2, 1, 0, 2, 2]),
@@ -154,7 +166,7 @@ def test_multi_fp8_small_cases(name, base, kw, q_lens, grid):
     check_multi(W.small(base, **kw), q_lens, "tc", grid, fp8=True)
 
 
-@pytest.mark.parametrize("q_lens", [[3, 4, 1, 2], [2, 2, 1, 2]], ids=["rows16", "rows8"])
+@pytest.mark.parametrize("q_lens", [[7, 8, 1, 5], [3, 4, 1, 2], [2, 2, 1, 2]], ids=["rows32", "rows16", "rows8"])
 def test_multi_fp8_window_sink(q_lens):
     w = W.small("llama3_8b", B=4, Smax=500, len_lo=100, len_hi=490, seed=416)
     g = torch.Generator().manual_seed(4)
@@ -162,7 +174,7 @@ def test_multi_fp8_window_sink(q_lens):
                 sink=(torch.randn(w.Hq, generator=g)).cuda())
 
 
-@pytest.mark.parametrize("q_lens", [[3, 4, 1, 2], [2, 2, 1, 2]], ids=["rows16", "rows8"])
+@pytest.mark.parametrize("q_lens", [[7, 8, 1, 5], [3, 4, 1, 2], [2, 2, 1, 2]], ids=["rows32", "rows16", "rows8"])
 @pytest.mark.parametrize("kernel", ["simt", "tc"])
 def test_multi_with_window_and_sink(kernel, q_lens):
     w = W.small("llama3_8b", B=4, Smax=500, len_lo=100, len_hi=490, seed=410)
@@ -232,7 +244,7 @@ def test_validate_multi_matches_oracle_rules():
 
 
 @pytest.mark.parametrize("name,q_len,fp8", [("llama3_8b", 2, False), ("llama3_8b", 4, False), ("paged", 3, False),
-                                            ("llama3_8b", 4, True), ("paged", 3, True)])
+                                            ("llama3_8b", 8, False), ("llama3_8b", 4, True), ("paged", 3, True)])
 def test_multi_full_size(name, q_len, fp8):
     """Full-size caches with q_len new tokens per row: the tokens of 3
     sampled rows against the oracle (the sampled rows' caches copied to the
@@ -267,7 +279,7 @@ def test_multi_full_size(name, q_len, fp8):
     err = float(np.abs(got - want).max())
     assert err <= BF16_REL_TOL * vmax
     G = w.Hq // w.Hkv
-    guard(path_of(w, "tc", fp8=fp8, unit_rows=G * max(1, min(16 // G, q_len))), err, vmax)
+    guard(path_of(w, "tc", fp8=fp8, unit_rows=G * max(1, min(32 // G, q_len))), err, vmax)
     if w.paged:
         assert to_np(t["k_blocks"][idx]).tobytes() == a["k_blocks"].tobytes()
     else:

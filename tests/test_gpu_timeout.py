@@ -31,6 +31,8 @@ CASES = [
     ("decode_e4m3", "llama3_8b", dict(B=16, Smax=2048, len_lo=900, len_hi=2000, seed=703), "decode", None, True),
     ("multi_rows16", "llama3_8b", dict(B=8, Smax=2048, len_lo=900, len_hi=2000, seed=704), "multi", [4] * 8,
      False),
+    ("multi_rows32", "llama3_8b", dict(B=8, Smax=2048, len_lo=900, len_hi=2000, seed=705), "multi", [8] * 8,
+     False),
 ]
 
 

@@ -51,6 +51,7 @@ def build_step(kind, name, fp8, uniform):
 @pytest.mark.parametrize("kind,name,fp8", [("decode", "dense_g4", False), ("decode", "paged16_g6", True),
                                            ("decode", "slots_g8", False), ("attend", "paged16_g6", False),
                                            ("multi", "rows16_g4", False), ("multi", "rows18_g6_paged16", True),
+                                           ("multi", "rows32_g4", False), ("multi", "rows40_g8", True),
                                            ("decode", "f32_d64_g4_cap256", False),
                                            ("attend", "slots_g8_cap320", False)])
 def test_constructions_hold_on_the_oracle(kind, name, fp8):
