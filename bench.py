@@ -80,7 +80,7 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="all",
                     help="one workload, or 'all' (default): the five, headline " + HEADLINE)
-    ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "tc"])
+    ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "tc", "tc5"])
     ap.add_argument("--op", default="decode", choices=["decode", "attend"],
                     help="decode step (default) or the read-only attend")
     ap.add_argument("--q-dtype", default=None, choices=["cache", "f32"],

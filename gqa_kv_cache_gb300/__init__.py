@@ -34,7 +34,7 @@ __all__ = ["decode_step", "decode_step_paged", "attend", "attend_paged", "decode
            "GqaError", "trace_enable", "trace_collect", "KERNELS", "library_path"]
 
 OK, INVALID_ARGUMENT, UNSUPPORTED, CUDA_ERROR, WORKSPACE = 0, 1, 2, 3, 4
-KERNELS = {"auto": 0, "simt": 1, "tc": 2, "unit": 3}
+KERNELS = {"auto": 0, "simt": 1, "tc": 2, "unit": 3, "tc5": 4}
 STATUS_BITS = {1: "bad length", 2: "bad slot id", 4: "bad block", 8: "timeout", 16: "bad kept prefix",
                32: "bad token offsets"}
 _DTYPES = {torch.float32: 0, torch.bfloat16: 1}
@@ -412,7 +412,7 @@ def trace_enable(on: bool = True) -> bool:
 def trace_collect() -> dict:
     """{kernel name: (launches, total ms)} since the previous collect."""
     lib = _lib.load()
-    n = 3
+    n = 4
     launches = (ctypes.c_int64 * n)()
     ms = (ctypes.c_double * n)()
     _check(lib.gqa_trace_collect(n, launches, ms), "gqa_trace_collect")

@@ -47,7 +47,9 @@ bool unit_ok(gqa_dtype dt, int D, int G, long long cap_rows, bool multi)
 int pick_kernel(const gqa_options *opt, gqa_dtype dt, int D, int G, bool paged, int block_size,
                 long long cap_rows = -1, bool multi = false, long long units = 0)
 {
-    const int want = opt ? opt->kernel : GQA_KERNEL_AUTO;
+    // GQA_KERNEL_TC5 is the tensor-core kernel with one of its unit forms on
+    // tcgen05 (chosen at the launch)
+    const int want = opt ? (opt->kernel == GQA_KERNEL_TC5 ? GQA_KERNEL_TC : opt->kernel) : GQA_KERNEL_AUTO;
     const bool bf16 = dt == GQA_DTYPE_BF16 || dt == GQA_DTYPE_E4M3;   // the tensor-core kernel's caches
     const bool tc_ok = tc_supports(bf16, D, G, paged, block_size);
     const bool simt_ok = dt != GQA_DTYPE_E4M3 && simt_supports(D, G);
@@ -373,8 +375,10 @@ gqa_status run_step(const Shape &s, const void *q, const void *k_new, const void
         }
         if (!ok)
             return GQA_ERR_CUDA;
-        TraceScope ts(1, cs);
-        e = tc_launch(p, maps, cs);
+        // the opt-in tcgen05 form of 17- to 32-row multi-token units
+        const bool t5 = opt && opt->kernel == GQA_KERNEL_TC5 && s.multi && tc5_takes(p);
+        TraceScope ts(t5 ? 3 : 1, cs);
+        e = t5 ? tc5_launch_multi(p, maps, cs) : tc_launch(p, maps, cs);
     } else if (unit) {
         int dev = 0;
         e = cudaGetDevice(&dev);
@@ -552,7 +556,7 @@ size_t gqa_workspace_bytes_multi(int B, int Hq, int Hkv, int D, gqa_dtype dt, in
     // paged block size): the larger of the two cuts' workspaces
     size_t bytes = 0;
     for (int k = GQA_KERNEL_SIMT; k <= GQA_KERNEL_TC; ++k) {
-        const int want = opt ? opt->kernel : GQA_KERNEL_AUTO;
+        const int want = opt ? (opt->kernel == GQA_KERNEL_TC5 ? GQA_KERNEL_TC : opt->kernel) : GQA_KERNEL_AUTO;
         if (want != GQA_KERNEL_AUTO && want != k)
             continue;
         gqa_options o = opt ? *opt : gqa_options{};
@@ -664,6 +668,7 @@ const char *gqa_kernel_name(int kind)
     case 0: return "simt_decode_kernel";
     case 1: return "tc_decode_kernel";
     case 2: return "unit_decode_kernel";
+    case 3: return "tc5_multi_kernel";
     }
     return "unknown";
 }

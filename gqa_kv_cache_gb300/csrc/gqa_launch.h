@@ -22,6 +22,10 @@ bool tc_supports(bool bf16, int D, int G, bool paged, int block_size);  // bf16:
 int tc_tile();
 int tc_ctas_per_sm(bool kv8, int unit_rows);   // resident CTAs per SM of the instantiation
 cudaError_t tc_launch(const DecodeParams &p, const TcMaps &maps, cudaStream_t st);
+// The tcgen05 form of multi-token units of 17 to 32 query rows over a bf16
+// cache (gqa_tc_multi.cu): whether it takes the step, and its launch.
+bool tc5_takes(const DecodeParams &p);
+cudaError_t tc5_launch_multi(const DecodeParams &p, const TcMaps &maps, cudaStream_t st);
 
 // Small-cache kernel: one cluster of CTAs per unit, the unit staged in their
 // shared memory (gqa_unit.cu). cap_rows: the row capacity in slots.

@@ -1,6 +1,7 @@
 // Tensor-core decode kernel, multi-token instantiations (bfloat16 query over a
-// bfloat16 or E4M3 cache); the kernel is in gqa_tc_kernel.cuh.
-#include "gqa_tc_kernel.cuh"
+// bfloat16 or E4M3 cache); the kernels are in gqa_tc_kernel.cuh (mma.sync)
+// and gqa_tc5_kernel.cuh (tcgen05, units of 17 to 32 rows over bf16).
+#include "gqa_tc5_kernel.cuh"
 
 namespace gqa {
 
@@ -30,6 +31,15 @@ cudaError_t tc_launch_multi(const DecodeParams &p, const TcMaps &maps, cudaStrea
                    : launch_q<false, false, true, true, 0>(p, maps, st);
     return win ? launch_q<false, true, true, false, 0>(p, maps, st)
                : launch_q<false, false, true, false, 0>(p, maps, st);
+}
+
+bool tc5_takes(const DecodeParams &p) { return p.q_bf16 && !p.kv8 && p.G > 16 && p.G <= kT5Rows; }
+
+cudaError_t tc5_launch_multi(const DecodeParams &p, const TcMaps &maps, cudaStream_t st)
+{
+    if (!tc5_takes(p))
+        return tc_launch_multi(p, maps, st);
+    return p.window > 0 ? launch_t5<true>(p, maps, st) : launch_t5<false>(p, maps, st);
 }
 
 }  // namespace gqa

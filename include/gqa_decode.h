@@ -109,7 +109,11 @@ typedef enum gqa_kernel {
                             2 * capacity * D * element size <= 200 KB (capacity = Smax,
                             or max_blocks * block_size); single-token steps (decode and
                             attend). AUTO takes it when those hold and the (row, head)
-                            pairs fit in one wave of the GPU                             */
+                            pairs fit in one wave of the GPU                             */,
+    GQA_KERNEL_TC5 = 4   /* as GQA_KERNEL_TC, but multi-token units of 17 to 32 query rows
+                            over a bfloat16 cache run on the tcgen05 tensor cores
+                            (accumulators in tensor memory); never chosen by AUTO:
+                            measured slower than GQA_KERNEL_TC for those units       */
 } gqa_kernel;
 
 /* Launch options (all zero = defaults). */
@@ -378,8 +382,10 @@ gqa_status gqa_validate_multi(const int32_t *lengths, const int32_t *cu_q, const
  * Kernel timing trace. When enabled, every decode call records CUDA events
  * around the kernel it launches; gqa_trace_collect waits for them and
  * returns, per kernel kind, the launches and total milliseconds since the
- * previous collect. Kinds: 0 = SIMT decode, 1 = tensor-core decode (each
- * decode step is exactly one kernel launch). Meant for benchmarks.
+ * previous collect. Kinds: 0 = SIMT decode, 1 = tensor-core decode, 2 = the
+ * small-cache decode, 3 = the tcgen05 form of 17- to 32-row multi-token
+ * units (each decode step is exactly one kernel launch); gqa_kernel_name
+ * gives each kind's kernel name. Meant for benchmarks.
  */
 int gqa_trace_enable(int on);
 gqa_status gqa_trace_collect(int n_kinds, int64_t *launches, double *ms);

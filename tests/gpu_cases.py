@@ -30,7 +30,7 @@ BF16_REL_TOL = 2e-2
 # "simt_bf16" (CUDA-core FMA), "unit_bf16" (the small-cache kernel, FMA).
 # Float32 caches keep their absolute 1e-5 bar.
 GUARD = {"tc_bf16": 1.2e-5, "tc_bf16_q32": 2e-5, "tc_bf16_m16": 8e-3, "tc_e4m3": 1.2e-3,
-         "tc_e4m3_m16": 1.2e-3, "simt_bf16": 2e-6, "unit_bf16": 3e-7}
+         "tc_e4m3_m16": 1.2e-3, "simt_bf16": 2e-6, "unit_bf16": 3e-7, "tc5_bf16": 8e-3}
 OBSERVED = []   # (test id, path, error / max|V|), written out by conftest
 
 
@@ -63,7 +63,9 @@ def path_of(w: W.Workload, kernel="auto", fp8=False, q_f32=False, unit_rows=None
         return None
     if kernel == "unit":
         return "unit_bf16"
-    tc = kernel == "tc" or (kernel == "auto" and tc_ok) or fp8
+    if kernel == "tc5" and not fp8 and unit_rows is not None and unit_rows > 16:
+        return "tc5_bf16"
+    tc = kernel in ("tc", "tc5") or (kernel == "auto" and tc_ok) or fp8
     if not tc:
         return "simt_bf16"
     m16 = unit_rows is not None and unit_rows > 8

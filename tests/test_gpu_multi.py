@@ -98,7 +98,7 @@ def check_multi(w, q_lens, kernel="auto", grid=0, fp8=False, **mods):
     err = float(np.abs(got - want).max()) if got.size else 0.0
     assert err <= tol, f"max abs error {err} > {tol}"
     G = w.Hq // w.Hkv
-    tpc = max(1, min(32 // G if kernel != "simt" else 8 // G, max_q))
+    tpc = max(1, min(32 // G if kernel != "simt" else 8 // G, max_q))   # tokens of a full chunk
     guard(path_of(w, kernel, fp8=fp8, unit_rows=G * tpc), err, vmax)
     for n in (("k_blocks", "v_blocks") if w.paged else ("k_cache", "v_cache")):
         assert to_np(t[n]).tobytes() == a[n].tobytes(), f"{n} differs from the oracle's appended copy"
@@ -157,6 +157,19 @@ def test_multi_small_cases(name, base, kw, q_lens, kernel, grid):
 
 FP8_CASES = [c for c in CASES if c[0] not in ("f32_d64",)]
 
+# units of 17 to 32 query rows (and, after them, a second chunk)
+T5_CASES = [c for c in CASES if c[0] in ("g4", "g8", "g2", "g2_rows16", "g4_rows32", "g6_rows18_paged16",
+                                          "g8_rows32", "g8_rows40", "g2_rows32_slots", "g4_rows32_paged8")]
+
+
+@pytest.mark.parametrize("name,base,kw,q_lens", T5_CASES, ids=[c[0] for c in T5_CASES])
+@pytest.mark.parametrize("grid", [0, 7])
+def test_multi_tcgen05_units(name, base, kw, q_lens, grid):
+    """The opt-in tcgen05 form (kernel="tc5"): units of 17 to 32 query rows
+    with S and O in tensor memory; smaller units and other chunks of the same
+    call take the mma.sync forms. Same bars and cache check as above."""
+    check_multi(W.small(base, **kw), q_lens, "tc5", grid)
+
 
 @pytest.mark.parametrize("name,base,kw,q_lens", FP8_CASES, ids=[c[0] for c in FP8_CASES])
 @pytest.mark.parametrize("grid", [0, 7])
@@ -175,7 +188,7 @@ def test_multi_fp8_window_sink(q_lens):
 
 
 @pytest.mark.parametrize("q_lens", [[7, 8, 1, 5], [3, 4, 1, 2], [2, 2, 1, 2]], ids=["rows32", "rows16", "rows8"])
-@pytest.mark.parametrize("kernel", ["simt", "tc"])
+@pytest.mark.parametrize("kernel", ["simt", "tc", "tc5"])
 def test_multi_with_window_and_sink(kernel, q_lens):
     w = W.small("llama3_8b", B=4, Smax=500, len_lo=100, len_hi=490, seed=410)
     g = torch.Generator().manual_seed(3)

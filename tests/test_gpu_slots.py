@@ -10,8 +10,9 @@ paged blocks of 16 and 8; the default grid, 7 and 33 CTAs so units are cut),
 the CUDA-core kernel, the small-cache kernel (decode and attend; the
 dominant slot at the edges of the parts a cluster of CTAs shares out), the
 read-only attend (bfloat16 and float32 query, bfloat16 and E4M3 caches), the
-E4M3 decode kernels, and the multi-token units of up to 8 and of 16 query
-rows (and a step of two chunks)."""
+E4M3 decode kernels, the multi-token units of up to 8, 16 and 32 query
+rows (and a step of two chunks), and the opt-in tcgen05 form of the units
+of more than 16 rows."""
 import pytest
 import torch
 
@@ -94,6 +95,22 @@ def test_dominant_attend(name, base, kw, fp8, q_f32):
 @pytest.mark.parametrize("name,base,kw,q_lens", MULTI, ids=[c[0] for c in MULTI])
 def test_dominant_multi(name, base, kw, q_lens, grid, fp8):
     dominant(Step(W.small(base, **kw), "multi", q_lens=q_lens, fp8=fp8), 14, "tc", grid)
+
+
+# the multi-token cases with units of more than 16 query rows
+MULTI_T5 = [c for c in MULTI if c[0] in ("rows18_g6_paged16", "rows32_g4", "rows40_g8")]
+
+
+@pytest.mark.parametrize("grid", [0, 7])
+@pytest.mark.parametrize("name,base,kw,q_lens", MULTI_T5, ids=[c[0] for c in MULTI_T5])
+def test_dominant_multi_tcgen05(name, base, kw, q_lens, grid):
+    dominant(Step(W.small(base, **kw), "multi", q_lens=q_lens), 14, "tc5", grid)
+
+
+@pytest.mark.parametrize("grid", [0, 7])
+@pytest.mark.parametrize("name,base,kw,q_lens", MULTI_T5, ids=[c[0] for c in MULTI_T5])
+def test_zero_query_multi_tcgen05(name, base, kw, q_lens, grid):
+    uniform(Step(W.small(base, **kw), "multi", q_lens=q_lens), "tc5", grid)
 
 
 @pytest.mark.parametrize("grid", [0, 7, 33])

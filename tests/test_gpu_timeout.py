@@ -24,7 +24,7 @@ from slot_cases import BF16_REL_TOL, Step, run_oracle
 pytestmark = pytest.mark.gpu
 
 CASES = [
-    # name, family, sizes, kind, q_lens, fp8
+    # name, family, sizes, kind, q_lens, fp8 (kernel "tc"; the last case "tc5")
     ("decode_dense", "llama3_8b", dict(B=16, Smax=2048, len_lo=900, len_hi=2000, seed=701), "decode", None, False),
     ("decode_paged", "paged", dict(B=8, num_blocks=8 * 128, max_blocks=128, len_lo=900, len_hi=2000, seed=702),
      "decode", None, False),
@@ -33,6 +33,8 @@ CASES = [
      False),
     ("multi_rows32", "llama3_8b", dict(B=8, Smax=2048, len_lo=900, len_hi=2000, seed=705), "multi", [8] * 8,
      False),
+    ("multi_rows32_tcgen05", "llama3_8b", dict(B=8, Smax=2048, len_lo=900, len_hi=2000, seed=706), "multi",
+     [8] * 8, False),
 ]
 
 
@@ -66,7 +68,8 @@ def test_wait_runs_out_then_next_call_is_correct(name, base, kw, kind, q_lens, f
 
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     out = torch.full((t["q"].shape[0], w.Hq, w.D), 7.0, device="cuda")
-    _call(st, t, out=out, status=status, kernel="tc", wait_limit_cycles=2000, test_stall=True)
+    kernel = "tc5" if name.endswith("tcgen05") else "tc"
+    _call(st, t, out=out, status=status, kernel=kernel, wait_limit_cycles=2000, test_stall=True)
     torch.cuda.synchronize()
     s = int(status.item())
     assert s == 8, f"status {s}: expected exactly the timeout bit"
@@ -76,7 +79,7 @@ def test_wait_runs_out_then_next_call_is_correct(name, base, kw, kind, q_lens, f
 
     # the next call, default limit, same workspace: correct in full
     status.zero_()
-    out2 = _call(st, t, status=status, kernel="tc")
+    out2 = _call(st, t, status=status, kernel=kernel)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     got2 = out2.double().cpu().numpy()
