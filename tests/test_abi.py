@@ -59,6 +59,34 @@ def test_version(lib):
     assert lib.gqa_version() >= 100
 
 
+def test_kernel_names_and_choices(lib):
+    """Every trace kind has its kernel's name, and the binding's kernel
+    choices are the header's enum values."""
+    names = [lib.gqa_kernel_name(k).decode() for k in range(4)]
+    assert names == ["simt_decode_kernel", "tc_decode_kernel", "unit_decode_kernel", "tc5_multi_kernel"]
+    assert lib.gqa_kernel_name(4) == b"unknown"
+    import gqa_kv_cache_gb300 as gqa
+    text = open(os.path.join(ROOT, "include", "gqa_decode.h")).read()
+    enum = {m.group(1).lower(): int(m.group(2)) for m in re.finditer(r"GQA_KERNEL_(\w+) = (\d+)", text)}
+    assert gqa.KERNELS == enum
+
+
+def test_tcgen05_choice_sizes_the_workspace_like_tc(lib):
+    """The opt-in tcgen05 form is the tensor-core kernel for every size
+    question: the same workspace for the single- and multi-token steps."""
+    from gqa_kv_cache_gb300 import _lib
+    def opts(kernel):
+        o = _lib.GqaOptions()
+        o.kernel = kernel
+        o.grid_ctas = 304          # no device query (no GPU here)
+        return o
+    tc, t5 = opts(2), opts(4)
+    for B, Hq, Hkv in ((32, 32, 8), (4, 64, 8), (64, 48, 8)):
+        a = lib.gqa_workspace_bytes_multi(B, Hq, Hkv, 128, 1, 8, ctypes.byref(tc))
+        b = lib.gqa_workspace_bytes_multi(B, Hq, Hkv, 128, 1, 8, ctypes.byref(t5))
+        assert a == b and a > 0
+
+
 def _step(lib, **kw):
     a = dict(q=1, k_new=1, v_new=1, kc=1, vc=1, lengths=1, slot_ids=None, out=1,
              B=2, Hq=8, Hkv=2, D=64, R=2, Smax=16, dt=1, ws=None, ws_bytes=0, status=None)

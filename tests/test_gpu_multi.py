@@ -196,6 +196,22 @@ def test_multi_with_window_and_sink(kernel, q_lens):
                 sink=(torch.randn(w.Hq, generator=g)).cuda())
 
 
+def test_tcgen05_choice_leaves_other_steps_on_tc():
+    """kernel="tc5" changes only 17- to 32-row multi-token units over a bf16
+    cache: a single-token step and an 8-row multi-token step give the very
+    bits of kernel="tc"."""
+    import gqa_kv_cache_gb300 as gqa
+    w = W.small("llama3_8b", B=4, Smax=400, len_lo=0, len_hi=390, seed=429)
+    res = {}
+    for kernel in ("tc", "tc5"):
+        t = {k: v.cuda() for k, v in W.generate(w).items()}
+        a = gqa.decode_step(t["q"], t["k_new"], t["v_new"], t["k_cache"], t["v_cache"], t["lengths"], kernel=kernel)
+        t = {k: v.cuda() for k, v in W.generate(w, q_lens=[2, 1, 2, 2]).items()}
+        b = _run_gpu(w, t, 2, kernel)
+        res[kernel] = (a.clone(), b.clone())
+    assert torch.equal(res["tc"][0], res["tc5"][0]) and torch.equal(res["tc"][1], res["tc5"][1])
+
+
 @pytest.mark.parametrize("kernel", ["simt", "tc"])
 def test_multi_q_len_one_matches_decode_step(kernel):
     """q_len = 1 everywhere is the decode step: the same appended bytes and
