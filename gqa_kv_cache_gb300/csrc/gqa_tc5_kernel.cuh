@@ -12,10 +12,13 @@
 //    their accumulator lanes are never loaded); K comes straight from the TMA
 //    ring, whose 128-byte-swizzled 64-dim halves are the K-major SW128 layout
 //    of the B operand. Two S buffers in TMEM (64 columns each) alternate.
-//  * the softmax warp owns TMEM lanes 0-31, i.e. lane r holds query row r's
-//    64 scores of the tile: the row maximum, the lazy rescale and the
-//    weights are per-thread work, no shuffles. It writes row r's weights
-//    (bf16) into one of two P buffers in the K-major SW128 layout.
+//  * two softmax warps (0 and 4, both on TMEM lanes 0-31): lane r holds
+//    query row r, warp 0 its scores of slots 0-31 of the tile, warp 4 of
+//    slots 32-63; the partial row maxima are exchanged through shared
+//    memory, the rest (the lazy rescale, the weights) is per-thread work, no
+//    shuffles. Each writes its half of row r's weights (bf16) into one of two
+//    P buffers in the K-major SW128 layout, and rescales and reads back its
+//    64 dims of O.
 //  * O += P V (M = 128, N = 128 dims, K = 64 slots, four steps of 16): A = P,
 //    B = the V tile of the ring as an MN-major SW128 operand (dims
 //    contiguous: leading offset = the 64-dim half, stride = 8 slot rows).
@@ -51,15 +54,19 @@ constexpr int kT5Rows = 32;                                    // query rows of 
 constexpr int kT5Stages = 2;
 constexpr int kT5QBytes = kT5Rows * kD * 2;                    // the unit's query rows in a stage
 constexpr int kT5StageBytes = 4 * kHalfBytes + kT5QBytes;      // K lo, K hi, V lo, V hi, Q (40 KB)
-// Operands in front of the ring: Q dims 0-63, Q dims 64-127, P buffer 0, P
-// buffer 1, rows 0-31 of each (4 KB); each is read as 128 rows (16 KB), the
-// rest landing on what follows (never used).
-constexpr int kT5OpBytes = 4 * 4096;
+// Operands in front of the ring: Q dims 0-63 and Q dims 64-127, rows 0-63
+// of each (the unit's 32 query rows twice: 8 KB), then P buffers 0 and 1,
+// rows 0-31 of each (4 KB); each is read as 128 rows (16 KB), the rest
+// landing on what follows (never used).
+constexpr int kT5QOp = 8192, kT5POp = 2 * kT5QOp;
+constexpr int kT5OpBytes = kT5POp + 2 * 4096;
 constexpr int kT5DynSmem = kT5OpBytes + kT5Stages * kT5StageBytes + 1024;
-constexpr int kT5Threads = 3 * 32;                             // softmax, MMA, producer warps
+// softmax (warp 0: TMEM lanes 0-31, warp 1: lanes 32-63, the same query
+// rows), MMA (2), producer (3)
+constexpr int kT5Threads = 4 * 32;
 constexpr uint32_t kT5Cols = 256;                              // TMEM: S0, S1 (64 each), O (128)
 static_assert(kT5StageBytes % 1024 == 0, "stages must stay 1024-byte aligned for the swizzle");
-static_assert(kT5OpBytes + 12 * 1024 <= kT5OpBytes + kT5Stages * kT5StageBytes, "operand windows");
+static_assert(kT5POp + 4096 + 16384 <= kT5OpBytes + kT5Stages * kT5StageBytes, "operand windows");
 
 struct T5Shared {
     uint64_t full[kT5Stages];
@@ -71,6 +78,8 @@ struct T5Shared {
     int stage_bad[kT5Stages];
     int abort_flag;
     uint32_t tmem;
+    float xm[2][2][32];   // [tile parity][softmax warp][row]: partial row maxima of a tile
+    float xl[2][32];      // [softmax warp][row]: partial row sums at a segment's end
     long long sched[kMaxWarps + 8];
     TileWalk walk;
     MergeBufT<kT5Rows, merge_partials(kT5Rows)> merge;
@@ -155,8 +164,21 @@ __device__ __forceinline__ void t5_st32(uint32_t taddr, const float (&v)[32])
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// The softmax and MMA warps (0 and 1) only.
-__device__ __forceinline__ void t5_pair_sync() { asm volatile("bar.sync 1, 64;" ::: "memory"); }
+// The softmax and MMA warps (0, 1 and 2).
+__device__ __forceinline__ void t5_end_sync() { asm volatile("bar.sync 1, 96;" ::: "memory"); }
+
+// The two softmax warps (0 and 1): a barrier that also returns whether v
+// held in any of their threads.
+__device__ __forceinline__ bool t5_softmax_or(bool v)
+{
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+                 "bar.red.or.pred q, 2, 64, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+                 : "=r"(r)
+                 : "r"((uint32_t)v)
+                 : "memory");
+    return r != 0;
+}
 
 template <bool WIN>
 __global__ void __launch_bounds__(kT5Threads, 2)
@@ -177,7 +199,7 @@ __global__ void __launch_bounds__(kT5Threads, 2)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&sh.s_ready[b]), 1);
-            mbar_init(smem_u32(&sh.p_ready[b]), 1);
+            mbar_init(smem_u32(&sh.p_ready[b]), 2);   // both softmax warps
             mbar_init(smem_u32(&sh.pv_done[b]), 1);
         }
         mbar_init(smem_u32(&sh.q_ready), 1);
@@ -193,7 +215,7 @@ __global__ void __launch_bounds__(kT5Threads, 2)
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
         t5_fence_before();
     }
-    if (warp == 2 && lane == 0) {
+    if (warp == 3 && lane == 0) {
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mk)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mv)) : "memory");
     }
@@ -205,7 +227,7 @@ __global__ void __launch_bounds__(kT5Threads, 2)
     const __nv_bfloat16 *knew = static_cast<const __nv_bfloat16 *>(p.k_new);
     const __nv_bfloat16 *vnew = static_cast<const __nv_bfloat16 *>(p.v_new);
 
-    if (warp == 2) {
+    if (warp == 3) {
         // ------------------------------------------------------ producer --
         uint64_t policy;
         asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
@@ -328,13 +350,14 @@ __global__ void __launch_bounds__(kT5Threads, 2)
     bool stall = p.test_stall != 0;     // the first wait also waits on sh.stall (runs out)
     const uint32_t idesc_s = t5_idesc(128, kTile, 0), idesc_o = t5_idesc(128, kD, 1);
 
-    if (warp == 1) {
+    if (warp == 2) {
         // ----------------------------------------------------------- MMA --
         int i = 0;                           // tiles of this CTA so far
         bool pend = false, pend_acc = false; // a product O += P V still to issue
         int pend_i = 0, pend_stage = 0;
         uint32_t q_phase = 0;
         bool aborted = false;
+        bool row_good = true;                // of the current segment's row
         auto issue_pv = [&]() {
             // O += P(pend_i) V(pend_i): waits for the weights of that tile
             const int bufp = pend_i & 1;
@@ -347,7 +370,7 @@ __global__ void __launch_bounds__(kT5Threads, 2)
             aborted = aborted || !ok;
             if (ok && lane == 0) {
                 t5_fence_after();
-                const uint32_t pa = op_u32 + 2 * 4096 + bufp * 4096;
+                const uint32_t pa = op_u32 + kT5POp + bufp * 4096;
                 const uint32_t va = ring_u32 + pend_stage * kT5StageBytes + 2 * kHalfBytes;
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
@@ -392,7 +415,8 @@ __global__ void __launch_bounds__(kT5Threads, 2)
                 aborted = aborted || !ok;
                 have = have && ok;
             }
-            const bool row_good = row_ok(p, b, L);
+            if (seg_first)
+                row_good = row_ok(p, b, L);
             const bool tile_bad = have ? sh.stage_bad[stage] != 0 : true;
             const int slot0 = WIN ? tile_slot0(cur, kTile) : cur.t * kTile;
             uint8_t *kring = ring + stage * kT5StageBytes;
@@ -439,7 +463,7 @@ __global__ void __launch_bounds__(kT5Threads, 2)
                     const uint32_t ka = ring_u32 + stage * kT5StageBytes;
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
-                        const uint32_t qo = (ks >> 2) * 4096 + (ks & 3) * 32, ko = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
+                        const uint32_t qo = (ks >> 2) * kT5QOp + (ks & 3) * 32, ko = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
                         t5_mma(tmem + (i & 1) * kTile, t5_desc(op_u32 + qo, 16, 1024), t5_desc(ka + ko, 16, 1024),
                                idesc_s, ks > 0);
                     }
@@ -473,18 +497,25 @@ __global__ void __launch_bounds__(kT5Threads, 2)
         __syncwarp();
         mbar_wait(smem_u32(&sh.mma_done), 0);
         t5_fence_before();
-        t5_pair_sync();
+        t5_end_sync();
         return;
     }
 
-    // ----------------------------------------------------- softmax (warp 0) --
-    // lane r: query row r of the unit (TMEM lane r)
+    // ---------------------------------------------- softmax (warps 0 and 1) --
+    // lane r: query row r of the unit, in TMEM lane r (warp 0) and lane
+    // 32 + r (warp 1: the query rows are in A twice). Warp h takes slots
+    // 32 h .. 32 h + 31 of every tile; they exchange their partial row maxima
+    // every tile and their partial sums at a segment's end, so both keep the
+    // same running maximum. Warp 0 also copies the query rows, rescales and
+    // reads back O (rows 0-31), and takes a cut unit's ticket and merge.
+    const int h = warp;
+    const uint32_t tlane = (uint32_t)(32 * h) << 16;   // this warp's TMEM lanes
     const int r = lane;
     const float qnan = __int_as_float(0x7fc00000);
     int i = 0;
     int pv_seen[2] = {0, 0};             // products of each P buffer seen complete
     bool aborted = false;
-    float m_run = -INFINITY, l_run = 0.f;
+    float m_run = -INFINITY, l_run = 0.f; // l_run: this warp's slots
     int lim = -1, lo_r = 0, seg_first_i = 0, seg_first_t = 0;
     bool seg_bad = false, row_good = true;
     // waits until the product of tile j (P buffer j & 1) is complete
@@ -528,7 +559,7 @@ __global__ void __launch_bounds__(kT5Threads, 2)
             seg_first_i = i;
             seg_first_t = cur.t;
             row_good = row_ok(p, b, L);
-            if (!row_good && lane == 0 && cur.t == 0 && kvh == 0)
+            if (!row_good && h == 0 && lane == 0 && cur.t == 0 && kvh == 0)
                 report(p, row_error_bits(p, b, L));
             seg_bad = false;
             m_run = -INFINITY;
@@ -536,13 +567,15 @@ __global__ void __launch_bounds__(kT5Threads, 2)
             // row r is token r / Gh of the chunk and attends up to its own position
             lim = r < qrows ? L - (cur.nq - 1 - r / p.Gh) : -1;
             lo_r = WIN ? max(0, lim - p.window + 1) : 0;
-            if (have) {
-                // the query rows into the A operand (K-major, 128-byte swizzle)
+            if (have && h == 0) {
+                // the query rows into the A operand (K-major, 128-byte swizzle),
+                // as rows r and 32 + r
                 const uint8_t *qs = ring + stage * kT5StageBytes + 4 * kHalfBytes + r * (kD * 2);
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
                     const uint4 v = r < qrows ? *reinterpret_cast<const uint4 *>(qs + c * 16) : make_uint4(0u, 0u, 0u, 0u);
-                    *reinterpret_cast<uint4 *>(opnd + (c >> 3) * 4096 + swz(r, c & 7)) = v;
+                    *reinterpret_cast<uint4 *>(opnd + (c >> 3) * kT5QOp + swz(r, c & 7)) = v;
+                    *reinterpret_cast<uint4 *>(opnd + (c >> 3) * kT5QOp + swz(32 + r, c & 7)) = v;
                 }
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
@@ -567,40 +600,46 @@ __global__ void __launch_bounds__(kT5Threads, 2)
             aborted = aborted || !s_ok;
             seg_bad = seg_bad || !s_ok;
         }
+        // this warp's 32 raw scores of row r; masked (-inf) only on the tiles
+        // that hold slots outside some row's softmax (a warp-uniform branch)
+        float x[32];
+        float pm = -INFINITY;
         if (s_ok) {
             t5_fence_after();
-            // the raw scores of row r; masked (-inf) only on the tiles that
-            // hold slots outside some row's softmax (a warp-uniform branch)
-            float x[64];
-            t5_ld32(tmem + sb * kTile, *reinterpret_cast<float(*)[32]>(x));
-            t5_ld32(tmem + sb * kTile + 32, *reinterpret_cast<float(*)[32]>(x + 32));
+            t5_ld32(tmem + tlane + sb * kTile + 32 * h, x);
             if (partial || lim < 0) {
 #pragma unroll
-                for (int j = 0; j < 64; ++j) {
-                    const int sl = slot0 + j;
+                for (int j = 0; j < 32; ++j) {
+                    const int sl = slot0 + 32 * h + j;
                     const bool on = lim >= 0 && (WIN ? attended(lim, lo_r, cur.P, sl) : sl <= lim);
                     x[j] = on ? x[j] : -INFINITY;
                 }
             }
-            // the row maximum (a tree), in base-2 units
-            float mt[16];
+            float mt[8];
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
+            for (int j = 0; j < 8; ++j)
                 mt[j] = fmaxf(fmaxf(x[4 * j], x[4 * j + 1]), fmaxf(x[4 * j + 2], x[4 * j + 3]));
 #pragma unroll
-            for (int w = 8; w > 0; w >>= 1)
+            for (int w = 4; w > 0; w >>= 1)
 #pragma unroll
                 for (int j = 0; j < w; ++j)
                     mt[j] = fmaxf(mt[j], mt[j + w]);
-            const float mx = mt[0] * p.scale_log2;   // the scale is positive
-            // lazy rescale: a row's running maximum moves only by more than 8.
-            // The decision is per row (lane), the TMEM accesses and the wait
-            // are warp-wide: the warp rescales when any row must, each lane
-            // by its own factor (1 for rows that keep their maximum).
+            pm = mt[0];
+        }
+        // the row maximum over both warps' slots (every tile, both warps)
+        sh.xm[sb][h][lane] = pm;
+        t5_softmax_or(false);
+        const float mx = fmaxf(pm, sh.xm[sb][1 - h][lane]) * p.scale_log2;   // the scale is positive
+        if (s_ok) {
+            // lazy rescale: a row's running maximum moves only by more than
+            // 8. The decision is per row (lane) and the same in both warps;
+            // warp 0 rescales O, warp-wide (TMEM accesses and the wait): when
+            // any row must, each lane by its own factor (1 for rows that keep
+            // their maximum).
             const bool raise = mx > m_run + 8.f;
             const bool scale_o = raise && m_run != -INFINITY && i > seg_first_i;   // O holds tiles up to i - 1
             const float alpha = scale_o ? fast_ex2(m_run - mx) : 1.f;
-            if (__any_sync(0xffffffffu, scale_o) && wait_pv(i - 1)) {
+            if (h == 0 && __any_sync(0xffffffffu, scale_o) && wait_pv(i - 1)) {
 #pragma unroll 1
                 for (int c = 0; c < 4; ++c) {
                     float o[32];
@@ -615,13 +654,14 @@ __global__ void __launch_bounds__(kT5Threads, 2)
                 l_run = scale_o ? l_run * alpha : 0.f;
                 m_run = mx;
             }
-            // the weights 2^(s scale - m) in bf16, into P buffer sb once the
-            // product of tile i - 2 has read it; their sum in float32
-            uint32_t pk[32];
+            // the weights 2^(s scale - m) in bf16, into this warp's half of
+            // P buffer sb once the product of tile i - 2 has read it; their
+            // sum in float32
+            uint32_t pk[16];
             float ps[4] = {0.f, 0.f, 0.f, 0.f};
             const float nm = m_run == -INFINITY ? 0.f : -m_run;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
+            for (int j = 0; j < 16; ++j) {
                 const float a = x[2 * j] == -INFINITY ? 0.f : fast_ex2(fmaf(x[2 * j], p.scale_log2, nm));
                 const float c = x[2 * j + 1] == -INFINITY ? 0.f : fast_ex2(fmaf(x[2 * j + 1], p.scale_log2, nm));
                 pk[j] = pack_bf16(a, c);
@@ -630,10 +670,10 @@ __global__ void __launch_bounds__(kT5Threads, 2)
             l_run += (ps[0] + ps[1]) + (ps[2] + ps[3]);
             if (i >= 2)
                 wait_pv(i - 2);
-            uint8_t *pb = opnd + 2 * 4096 + sb * 4096;
+            uint8_t *pb = opnd + kT5POp + sb * 4096;
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
-                *reinterpret_cast<uint4 *>(pb + swz(r, c)) =
+            for (int c = 0; c < 4; ++c)
+                *reinterpret_cast<uint4 *>(pb + swz(r, 4 * h + c)) =
                     make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             t5_fence_before();
@@ -645,32 +685,33 @@ __global__ void __launch_bounds__(kT5Threads, 2)
         const bool unit_done = (cur.t == cur.nr - 1);
         const bool range_done = (cur.g + 1 == cur.end);
         if (unit_done || range_done) {
-            // ---- the segment's end: O of row r from TMEM, then the output
-            // (a whole unit) or the partial state
-            const bool o_ok = s_ok && wait_pv(i);
-            const bool bad = __any_sync(0xffffffffu, !row_good || seg_bad || !o_ok);
+            // ---- the segment's end: O of row r from TMEM (warp 0), then the
+            // output (a whole unit) or the partial state
+            const bool o_ok = s_ok && (h == 1 || wait_pv(i));
+            sh.xl[h][lane] = l_run;
+            const bool bad = t5_softmax_or(!row_good || seg_bad || !o_ok);   // both warps
             const bool whole = (seg_first_t == 0) && unit_done;
             const int G = p.G;
             const long long P = (long long)b * p.Hkv + kvh + blockIdx.x;
             float sc = 1.f;
-            float M = m_run, den = l_run;
+            float M = m_run, den = l_run + sh.xl[1 - h][lane];
             if (whole) {
                 const float sk = p.sink ? sink_log2(p, kvh * p.Gh + r % p.Gh) : -INFINITY;
                 const float Mx = fmaxf(M, sk);
                 const float a = (M == -INFINITY) ? 0.f : fast_ex2(M - Mx);
                 den = a * den + ((sk == -INFINITY) ? 0.f : fast_ex2(sk - Mx));
                 sc = a / den;
-            } else if (r < G) {
+            } else if (r < G && h == 0) {
                 p.ws_ml[(P * G + r) * 2 + 0] = bad ? qnan : M;
                 p.ws_ml[(P * G + r) * 2 + 1] = bad ? qnan : den;
             }
             float *dst = nullptr;
-            if (whole && r < qrows)
+            if (h == 0 && whole && r < qrows)
                 dst = out_row<true>(p, cur, r, kD);
-            else if (!whole && r < G)
+            else if (h == 0 && !whole && r < G)
                 dst = p.ws_o + (P * G + r) * kD;
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < (h == 0 ? 4 : 0); ++c) {
                 float o[32];
                 if (o_ok)
                     t5_ld32(tmem + 128 + c * 32, o);
@@ -682,11 +723,13 @@ __global__ void __launch_bounds__(kT5Threads, 2)
                                 : make_float4(o[j] * sc, o[j + 1] * sc, o[j + 2] * sc, o[j + 3] * sc);
                 }
             }
-            if (bad && row_good && lane == 0)
+            if (bad && row_good && h == 0 && lane == 0)
                 report(p, aborted ? kTimeout : kBadBlock);
             t5_fence_before();
-            __syncwarp();
-            if (!whole) {
+            // both warps' stores before the ticket (and the sums read before
+            // the next segment's end rewrites them)
+            t5_softmax_or(false);
+            if (!whole && h == 0) {
                 // the arrival ticket and, in the last CTA of the unit, the merge
                 const long long first_tile = cur.g - cur.t;
                 FinJob j;
@@ -710,10 +753,14 @@ __global__ void __launch_bounds__(kT5Threads, 2)
             phase ^= 1;
         }
     }
-    // the MMA warp has seen its last product complete: free TMEM
-    t5_pair_sync();
-    t5_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kT5Cols) : "memory");
+    // the MMA warp has seen its last product complete, the other softmax warp
+    // is done with TMEM: free it
+    t5_fence_before();
+    t5_end_sync();
+    if (warp == 0) {
+        t5_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kT5Cols) : "memory");
+    }
 }
 
 template <bool WIN>
