@@ -121,6 +121,18 @@ __device__ __forceinline__ void t5_commit(uint32_t bar)
                  : "memory");
 }
 
+// Whether the phase of `bar` with this parity has completed (never blocks).
+__device__ __forceinline__ bool t5_test(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(bar), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ void t5_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void t5_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -358,11 +370,13 @@ __global__ void __launch_bounds__(kT5Threads, 2)
         uint32_t q_phase = 0;
         bool aborted = false;
         bool row_good = true;                // of the current segment's row
-        auto issue_pv = [&]() {
+        auto issue_pv = [&](bool ready) {
             // O += P(pend_i) V(pend_i): waits for the weights of that tile
+            // (unless already seen ready)
             const int bufp = pend_i & 1;
-            bool ok = !aborted && __all_sync(0xffffffffu, mbar_wait(smem_u32(&sh.p_ready[bufp]), (pend_i >> 1) & 1,
-                                                                      p.wait_cycles, &sh.abort_flag));
+            bool ok = ready || (!aborted && __all_sync(0xffffffffu, mbar_wait(smem_u32(&sh.p_ready[bufp]),
+                                                                                (pend_i >> 1) & 1, p.wait_cycles,
+                                                                                &sh.abort_flag)));
             if (!ok && !aborted && lane == 0 && !*((volatile int *)&sh.abort_flag)) {
                 report(p, kTimeout);
                 atomicExch(&sh.abort_flag, 1);
@@ -387,7 +401,20 @@ __global__ void __launch_bounds__(kT5Threads, 2)
             const bool seg_first = cur.t == 0 || cur.g == range_start;
             bool have = false;
             if (!aborted && !__any_sync(0xffffffffu, *((volatile int *)&sh.abort_flag) != 0)) {
-                bool ok = mbar_wait(smem_u32(&sh.full[stage]), phase, p.wait_cycles, &sh.abort_flag);
+                // while tile i has not landed, the pending product is issued
+                // as soon as its weights are ready (it frees its ring stage)
+                // (bounded: past the limit the wait below gives up in turn)
+                const uint32_t fb = smem_u32(&sh.full[stage]);
+                const long long t0 = clock64();
+                while (pend && !stall && !__all_sync(0xffffffffu, t5_test(fb, phase))) {
+                    if (__all_sync(0xffffffffu, t5_test(smem_u32(&sh.p_ready[pend_i & 1]), (pend_i >> 1) & 1))) {
+                        issue_pv(true);
+                        break;
+                    }
+                    if (__any_sync(0xffffffffu, *((volatile int *)&sh.abort_flag) != 0 || clock64() - t0 > p.wait_cycles))
+                        break;
+                }
+                bool ok = mbar_wait(fb, phase, p.wait_cycles, &sh.abort_flag);
                 if (stall) {   // tests of the timeout path: a wait that nothing ends
                     ok = ok && mbar_wait(smem_u32(&sh.stall), 0, p.wait_cycles);
                     stall = false;
@@ -403,7 +430,7 @@ __global__ void __launch_bounds__(kT5Threads, 2)
             // last product goes first (the softmax warp reads O after it and
             // only then copies the next query)
             if (seg_first && pend)
-                issue_pv();
+                issue_pv(false);
             if (have && seg_first) {
                 const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sh.q_ready), q_phase, p.wait_cycles,
                                                                   &sh.abort_flag));
@@ -472,7 +499,7 @@ __global__ void __launch_bounds__(kT5Threads, 2)
                 __syncwarp();
             }
             if (pend)
-                issue_pv();
+                issue_pv(false);
             if (have) {
                 pend = true;
                 pend_i = i;
@@ -490,7 +517,7 @@ __global__ void __launch_bounds__(kT5Threads, 2)
             }
         }
         if (pend)
-            issue_pv();
+            issue_pv(false);
         // every product issued has completed before TMEM is freed
         if (lane == 0)
             t5_commit(smem_u32(&sh.mma_done));
