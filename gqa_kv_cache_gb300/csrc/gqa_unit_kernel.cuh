@@ -38,7 +38,7 @@ namespace {
 
 constexpr int kUnitWarps = 8;
 constexpr int kUnitThreads = kUnitWarps * 32;
-constexpr long long kUnitWaitCycles = 4LL << 30;   // about 2 s at 2 GHz
+constexpr long long kUnitWaitCycles = 4LL << 30;   // about 2 s at 2 GHz: the limit of the drain after a timeout
 constexpr int kUnitMaxCluster = 8;                  // CTAs a unit at most (the portable cluster size)
 
 template <typename T, int D>
@@ -166,6 +166,33 @@ __host__ __device__ constexpr size_t unit_stage_bytes(int rows)
     return ((stage > warps ? stage : warps) + 15) / 16 * 16;
 }
 
+// Bounded wait for phase 0 of `bar`: false when it gave up after `limit`
+// SM clock cycles (below 2^20 cycles with a one-nanosecond suspend hint, so
+// a short limit is honoured to the cycle).
+__device__ __forceinline__ bool unit_wait(uint32_t bar, long long limit)
+{
+    const long long t0 = clock64();
+    while (true) {
+        uint32_t ok;
+        if (limit < (1LL << 20))
+            asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0, 1;\n\t"
+                         "selp.u32 %0, 1, 0, p;\n\t}"
+                         : "=r"(ok)
+                         : "r"(bar)
+                         : "memory");
+        else
+            asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n\t"
+                         "selp.u32 %0, 1, 0, p;\n\t}"
+                         : "=r"(ok)
+                         : "r"(bar)
+                         : "memory");
+        if (ok)
+            return true;
+        if (clock64() - t0 > limit)
+            return false;
+    }
+}
+
 __device__ __forceinline__ void bulk_copy(const void *dst_smem, const void *src, uint32_t bytes, uint32_t bar)
 {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
@@ -190,6 +217,7 @@ __global__ void __launch_bounds__(kUnitThreads) unit_decode_kernel(const DecodeP
     // by every CTA
     extern __shared__ __align__(128) uint8_t dyn[];
     __shared__ uint64_t bar;
+    __shared__ uint64_t stall_bar;   // a barrier nothing completes (tests of the timeout path)
     __shared__ UnitInfo info;
     __shared__ int blk_bad;
     __shared__ float sm_m[kUnitWarps][GP], sm_l[kUnitWarps][GP];
@@ -226,6 +254,7 @@ __global__ void __launch_bounds__(kUnitThreads) unit_decode_kernel(const DecodeP
     cluster_arrive_relaxed();
     if (tid == 0) {
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar_u));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(unit_smem(&stall_bar)));
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         blk_bad = 0;
     }
@@ -341,7 +370,11 @@ __global__ void __launch_bounds__(kUnitThreads) unit_decode_kernel(const DecodeP
                 q[g][e] = tmp[e] * p.scale_log2;
         }
     }
-    // the new token: the CTA holding the unit's last row keeps it and appends it
+    // the new token: the CTA holding the unit's last row scores it from
+    // k_new / v_new and appends it now, so the stores overlap the wait
+    // (appending it at the end, after every CTA of the unit is known good,
+    // cost pr1_fp32 0.2 us: a step that times out may therefore have
+    // appended it); an unusable slot makes the unit bad
     const bool has_new = f.append && !f.bad && f.r1 > f.n_cached;
     const long long new_off = ((long long)b * p.Hkv + kvh) * D;
     if (has_new && tid < 2 * (RB / 16)) {
@@ -357,21 +390,20 @@ __global__ void __launch_bounds__(kUnitThreads) unit_decode_kernel(const DecodeP
         }
     }
 
-    // ---- wait for the staged rows (bounded; the copies land whatever happens)
+    // ---- wait for the staged rows, bounded by the launch's limit (tests of
+    // the timeout path also wait on a barrier nothing completes, so the wait
+    // runs out). A wait that ran out is followed by a drain with the full
+    // limit, so that no copy still writes into shared memory when the CTA
+    // exits.
     int timed_out = 0;
     if (staged) {
-        uint32_t ok = 0;
-        const long long t0 = clock64();
-        while (true) {
-            asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n\t"
-                         "selp.u32 %0, 1, 0, p;\n\t}"
-                         : "=r"(ok)
-                         : "r"(bar_u)
-                         : "memory");
-            if (ok || clock64() - t0 > kUnitWaitCycles)
-                break;
+        bool ok = unit_wait(bar_u, p.wait_cycles);
+        if (p.test_stall)
+            ok = ok && unit_wait(unit_smem(&stall_bar), p.wait_cycles);
+        if (!ok) {
+            timed_out = 1;
+            unit_wait(bar_u, kUnitWaitCycles);
         }
-        timed_out = ok ? 0 : 1;
     }
 
     // ---- online softmax over this CTA's rows (cached rows from shared
