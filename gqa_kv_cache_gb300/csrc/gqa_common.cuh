@@ -637,7 +637,7 @@ __device__ __forceinline__ float fast_ex2(float x)
 
 // Shared-memory scratch of a segment's epilogue and of the in-kernel merge of
 // a cut unit's partials.
-constexpr int kMergeMax = 32;   // partials merged through shared memory (more: direct loads)
+constexpr int kMergeMax = 32;   // partials weighted in one pass through shared memory (more: in chunks)
 constexpr int kMergeG = 8;      // query rows per unit (G <= 8)
 constexpr int kMergeW = 4;      // warps whose states a segment merges
 // For GR query rows per unit, up to KM partials merged through shared memory.
@@ -883,24 +883,61 @@ __device__ inline void unit_ticket_merge(const DecodeParams &p, const TileCursor
                 }
             }
         } else {
-            for (int idx = tid; idx < G * DD; idx += nthr) {
-                const int g = idx / DD, d = idx % DD;
+            // more partials than the buffer holds: the maximum and the
+            // denominator of each row first (every partial's (m, l) loaded
+            // directly), then the outputs KM partials at a time, their weights
+            // through shared memory and the sums in the output rows
+            constexpr int V = (DD % 4 == 0) ? 4 : 1;
+            for (int g = tid; g < G; g += nthr) {
                 float M = -INFINITY;
                 for (int i = 0; i < K; ++i)
                     M = fmaxf(M, __ldcg(p.ws_ml + ((P0 + i) * G + g) * 2));
                 const float sk = p.sink ? sink_log2(p, kvh * p.Gh + g % p.Gh) : -INFINITY;
                 M = fmaxf(M, sk);
-                float num = 0.f, den = (sk == -INFINITY) ? 0.f : fast_ex2(sk - M);
+                float den = (sk == -INFINITY) ? 0.f : fast_ex2(sk - M);
                 for (int i = 0; i < K; ++i) {
-                    const long long Q = P0 + i;
-                    const float a = fast_ex2(__ldcg(p.ws_ml + (Q * G + g) * 2) - M);
-                    float *po = p.ws_o + (Q * G + g) * DD + d;
-                    num = fmaf(a, __ldcg(po), num);
-                    den = fmaf(a, __ldcg(p.ws_ml + (Q * G + g) * 2 + 1), den);
-                    *po = 0.f;       // consumed: leave the workspace zero-filled
+                    const float *ml = p.ws_ml + ((P0 + i) * G + g) * 2;
+                    den = fmaf(fast_ex2(__ldcg(ml) - M), __ldcg(ml + 1), den);
                 }
-                if (g < nrow)
-                    out_row<MULTI>(p, cur, g, DD)[d] = num / den;
+                mb.M[g] = M;
+                mb.inv_den[g] = 1.f / den;
+            }
+            for (int c0 = 0; c0 < K; c0 += KM) {
+                const int kc = min(KM, K - c0);
+                sync();   // the rows' maxima (first chunk); the previous chunk's weights read
+                for (int k = tid; k < kc * G; k += nthr)   // partial c0 + k / G, row k % G
+                    mb.w[k] = fast_ex2(__ldcg(p.ws_ml + ((P0 + c0) * G + k) * 2) - mb.M[k % G]);
+                sync();
+                for (int idx = tid * V; idx < G * DD; idx += nthr * V) {
+                    const int g = idx / DD;
+                    float acc[V];
+#pragma unroll
+                    for (int e = 0; e < V; ++e)
+                        acc[e] = 0.f;
+#pragma unroll 4
+                    for (int i = 0; i < kc; ++i) {
+                        const float a = mb.w[i * G + g];
+                        float *po = p.ws_o + (P0 + c0 + i) * G * DD + idx;
+                        if constexpr (V == 4) {
+                            const float4 v = __ldcg(reinterpret_cast<const float4 *>(po));
+                            acc[0] = fmaf(a, v.x, acc[0]);
+                            acc[1] = fmaf(a, v.y, acc[1]);
+                            acc[2] = fmaf(a, v.z, acc[2]);
+                            acc[3] = fmaf(a, v.w, acc[3]);
+                            *reinterpret_cast<float4 *>(po) = make_float4(0.f, 0.f, 0.f, 0.f);
+                        } else {
+                            acc[0] = fmaf(a, __ldcg(po), acc[0]);
+                            *po = 0.f;   // consumed: leave the workspace zero-filled
+                        }
+                    }
+                    if (g < nrow) {
+                        // this thread's own elements: the earlier chunks' sums
+                        float *o = out_row<MULTI>(p, cur, g, DD) + (idx - g * DD);
+#pragma unroll
+                        for (int e = 0; e < V; ++e)
+                            o[e] = fmaf(acc[e], mb.inv_den[g], c0 == 0 ? 0.f : o[e]);
+                    }
+                }
             }
         }
         sync();

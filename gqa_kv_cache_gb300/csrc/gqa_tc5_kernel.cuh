@@ -83,7 +83,6 @@ struct T5Shared {
     long long sched[kMaxWarps + 8];
     TileWalk walk;
     MergeBufT<kT5Rows, merge_partials(kT5Rows)> merge;
-    int flag;
 };
 
 // Shared-memory matrix descriptor of a 128-byte-swizzled operand: start
@@ -767,7 +766,7 @@ __global__ void __launch_bounds__(kT5Threads, 2)
                 j.kvh = cur.kvh;
                 j.nq = cur.nq;
                 j.tokL = cur.tokL;
-                fin_ticket_merge<kT5Rows, true>(p, j, sh.merge, &sh.flag, lane);
+                fin_ticket_merge<kT5Rows, true>(p, j, sh.merge, lane);
             }
         }
         ++i;

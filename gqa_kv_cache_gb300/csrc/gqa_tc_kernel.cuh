@@ -373,8 +373,7 @@ __device__ __forceinline__ void job_free() { asm volatile("bar.arrive 3, %0;" ::
 // loads of one partial (of up to 16 rows at a time) in flight at once, so a
 // merge costs about one L2 round trip per partial and block of rows.
 template <int RW, bool MULTI, int GR, int KM>
-__device__ __noinline__ void fin_ticket_merge(const DecodeParams &p, const FinJob j, MergeBufT<GR, KM> &mb,
-                                              int *flag, int lane)
+__device__ __noinline__ void fin_ticket_merge(const DecodeParams &p, const FinJob j, MergeBufT<GR, KM> &mb, int lane)
 {
     constexpr int RB = RW > 16 ? 16 : RW;    // rows merged at a time (the registers of acc and v)
     constexpr int IT = RB * kD / (32 * 4);   // float4 per lane and partial
@@ -392,29 +391,43 @@ __device__ __noinline__ void fin_ticket_merge(const DecodeParams &p, const FinJo
     c.kvh = j.kvh;
     c.nq = j.nq;
     c.tokL = j.tokL;
-    if (K > KM) {   // more partials than the merge buffer holds: the general merge
-        unit_ticket_merge<kD, MULTI, false>(p, c, j.first, j.last, flag, mb, lane, 32, [] { __syncwarp(); }, K - 1);
-        return;
-    }
     const long long P0 = (long long)u + j.first;
-    // every partial's (m, l): weights and the denominator per query row
-    for (int k = lane; k < K * G; k += 32) {
-        mb.w[k] = __ldcg(p.ws_ml + (P0 * G + k) * 2);
-        mb.l[k] = __ldcg(p.ws_ml + (P0 * G + k) * 2 + 1);
-    }
-    __syncwarp();
-    if (lane < G) {
+    if (K <= KM) {
+        // every partial's (m, l): weights and the denominator per query row
+        for (int k = lane; k < K * G; k += 32) {
+            mb.w[k] = __ldcg(p.ws_ml + (P0 * G + k) * 2);
+            mb.l[k] = __ldcg(p.ws_ml + (P0 * G + k) * 2 + 1);
+        }
+        __syncwarp();
+        if (lane < G) {
+            float M = -INFINITY;
+            for (int i = 0; i < K; ++i)
+                M = fmaxf(M, mb.w[i * G + lane]);
+            const float sk = p.sink ? sink_log2(p, j.kvh * p.Gh + lane % p.Gh) : -INFINITY;
+            M = fmaxf(M, sk);
+            float den = (sk == -INFINITY) ? 0.f : fast_ex2(sk - M);
+            for (int i = 0; i < K; ++i) {
+                const float a = fast_ex2(mb.w[i * G + lane] - M);
+                mb.w[i * G + lane] = a;
+                den = fmaf(a, mb.l[i * G + lane], den);
+            }
+            mb.inv_den[lane] = 1.f / den;
+        }
+    } else if (lane < G) {
+        // more partials than the buffer holds: the maximum and the denominator
+        // per row from every partial's (m, l) directly; the weights follow KM
+        // partials at a time
         float M = -INFINITY;
         for (int i = 0; i < K; ++i)
-            M = fmaxf(M, mb.w[i * G + lane]);
+            M = fmaxf(M, __ldcg(p.ws_ml + ((P0 + i) * G + lane) * 2));
         const float sk = p.sink ? sink_log2(p, j.kvh * p.Gh + lane % p.Gh) : -INFINITY;
         M = fmaxf(M, sk);
         float den = (sk == -INFINITY) ? 0.f : fast_ex2(sk - M);
         for (int i = 0; i < K; ++i) {
-            const float a = fast_ex2(mb.w[i * G + lane] - M);
-            mb.w[i * G + lane] = a;
-            den = fmaf(a, mb.l[i * G + lane], den);
+            const float *ml = p.ws_ml + ((P0 + i) * G + lane) * 2;
+            den = fmaf(fast_ex2(__ldcg(ml) - M), __ldcg(ml + 1), den);
         }
+        mb.M[lane] = M;
         mb.inv_den[lane] = 1.f / den;
     }
     __syncwarp();
@@ -425,24 +438,33 @@ __device__ __noinline__ void fin_ticket_merge(const DecodeParams &p, const FinJo
 #pragma unroll
         for (int it = 0; it < IT; ++it)
             acc[it] = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int i = 0; i < K; ++i) {
-            float4 *po = reinterpret_cast<float4 *>(p.ws_o + (P0 + i) * G * kD + base);
-            float4 v[IT];
-#pragma unroll
-            for (int it = 0; it < IT; ++it) {
-                const int idx = base + (it * 32 + lane) * 4;
-                v[it] = idx < G * kD ? __ldcg(po + it * 32 + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int c0 = 0; c0 < K; c0 += KM) {
+            const int kc = min(KM, K - c0);
+            if (K > KM) {   // this chunk's weights (partial c0 + k / G, row k % G)
+                __syncwarp();
+                for (int k = lane; k < kc * G; k += 32)
+                    mb.w[k] = fast_ex2(__ldcg(p.ws_ml + ((P0 + c0) * G + k) * 2) - mb.M[k % G]);
+                __syncwarp();
             }
+            for (int i = 0; i < kc; ++i) {
+                float4 *po = reinterpret_cast<float4 *>(p.ws_o + (P0 + c0 + i) * G * kD + base);
+                float4 v[IT];
 #pragma unroll
-            for (int it = 0; it < IT; ++it) {
-                const int idx = base + (it * 32 + lane) * 4;
-                if (idx < G * kD) {
-                    const float a = mb.w[i * G + idx / kD];
-                    acc[it].x = fmaf(a, v[it].x, acc[it].x);
-                    acc[it].y = fmaf(a, v[it].y, acc[it].y);
-                    acc[it].z = fmaf(a, v[it].z, acc[it].z);
-                    acc[it].w = fmaf(a, v[it].w, acc[it].w);
-                    po[it * 32 + lane] = make_float4(0.f, 0.f, 0.f, 0.f);   // consumed: zero-filled again
+                for (int it = 0; it < IT; ++it) {
+                    const int idx = base + (it * 32 + lane) * 4;
+                    v[it] = idx < G * kD ? __ldcg(po + it * 32 + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int it = 0; it < IT; ++it) {
+                    const int idx = base + (it * 32 + lane) * 4;
+                    if (idx < G * kD) {
+                        const float a = mb.w[i * G + idx / kD];
+                        acc[it].x = fmaf(a, v[it].x, acc[it].x);
+                        acc[it].y = fmaf(a, v[it].y, acc[it].y);
+                        acc[it].z = fmaf(a, v[it].z, acc[it].z);
+                        acc[it].w = fmaf(a, v[it].w, acc[it].w);
+                        po[it * 32 + lane] = make_float4(0.f, 0.f, 0.f, 0.f);   // consumed: zero-filled again
+                    }
                 }
             }
         }
@@ -465,16 +487,15 @@ __device__ __noinline__ void fin_ticket_merge(const DecodeParams &p, const FinJo
     __syncwarp();
 }
 
-// Partials of a cut unit merged through shared memory (more: direct loads),
-// by query rows of a unit.
+// Partials of a cut unit whose weights one pass through shared memory holds
+// (more: that many at a time), by query rows of a unit.
 constexpr int merge_partials(int rw) { return rw == kGMax ? kMergeMax : (rw == 16 ? 16 : 8); }
 
-// The finisher warp's job slot, merge buffer and flag (kernels with one).
+// The finisher warp's job slot and merge buffer (kernels with one).
 template <int RW>
 struct FinShared {
     FinJob job;
     MergeBufT<RW, merge_partials(RW)> merge;
-    int flag;
 };
 struct NoFinShared {};
 
@@ -754,7 +775,7 @@ __global__ void __launch_bounds__((Ring<QF32, KV8, MULTI, MR>::kThreads), (Ring<
                 if (j.stop)
                     break;
                 job_free();
-                fin_ticket_merge<kRW, MULTI>(p, j, sh.fin.merge, &sh.fin.flag, lane);
+                fin_ticket_merge<kRW, MULTI>(p, j, sh.fin.merge, lane);
             }
             return;
         }

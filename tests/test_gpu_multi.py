@@ -196,6 +196,37 @@ def test_multi_with_window_and_sink(kernel, q_lens):
                 sink=(torch.randn(w.Hq, generator=g)).cuda())
 
 
+# One or two long rows over many CTAs: each unit is cut into more pieces than
+# one pass of the merge's shared-memory weights takes (8 partials for 32-row
+# units, 16 for 16-row units, 32 for 8-row units), so the merge goes through
+# them in chunks (in the CTA's own last segment end, and in the finisher
+# warp's when a CTA ends a cut unit in the middle of its walk).
+MANY_PIECES = [
+    ("rows32_g8", "long_context", dict(B=1, Hq=8, Hkv=1, Smax=2400, len_lo=2300, len_hi=2390, seed=431), [4]),
+    ("rows16_g4", "llama3_8b", dict(B=2, Hq=4, Hkv=1, Smax=2400, len_lo=2200, len_hi=2390, seed=432), [4, 3]),
+    ("rows8_g4", "llama3_8b", dict(B=1, Hq=4, Hkv=1, Smax=4200, len_lo=4000, len_hi=4190, seed=433), [2]),
+]
+
+
+@pytest.mark.parametrize("sink", [False, True], ids=["plain", "sink"])
+@pytest.mark.parametrize("grid", [0, 40])
+@pytest.mark.parametrize("kernel", ["tc", "tc5"])
+@pytest.mark.parametrize("name,base,kw,q_lens", MANY_PIECES, ids=[c[0] for c in MANY_PIECES])
+def test_multi_unit_cut_into_many_pieces(name, base, kw, q_lens, kernel, grid, sink):
+    import gqa_kv_cache_gb300 as gqa
+    if kernel == "tc5" and not name.startswith("rows32"):
+        pytest.skip("the tcgen05 form takes units of more than 16 rows only")
+    w = W.small(base, **kw)
+    mods = {}
+    if sink:
+        g = torch.Generator().manual_seed(5)
+        mods["sink"] = torch.randn(w.Hq, generator=g).cuda()
+    check_multi(w, q_lens, kernel, grid, **mods)
+    ws = gqa._ws_cache.get(torch.device("cuda", torch.cuda.current_device()))
+    if ws is not None:
+        assert int(torch.count_nonzero(ws).item()) == 0
+
+
 def test_tcgen05_choice_leaves_other_steps_on_tc():
     """kernel="tc5" changes only 17- to 32-row multi-token units over a bf16
     cache: a single-token step and an 8-row multi-token step give the very
