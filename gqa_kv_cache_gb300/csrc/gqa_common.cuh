@@ -882,11 +882,14 @@ __device__ inline void unit_ticket_merge(const DecodeParams &p, const TileCursor
                         o[e] = acc[e] * mb.inv_den[g];
                 }
             }
-        } else {
-            // more partials than the buffer holds: the maximum and the
-            // denominator of each row first (every partial's (m, l) loaded
-            // directly), then the outputs KM partials at a time, their weights
-            // through shared memory and the sums in the output rows
+        } else if constexpr (MULTI && PRE2) {
+            // more partials than the buffer holds (multi-token units over a
+            // bfloat16 cache: up to 32 rows): the maximum and the denominator
+            // of each row first (every partial's (m, l) loaded directly), then
+            // the outputs KM partials at a time, their weights through shared
+            // memory and the sums in the output rows. long_context, 4 tokens a
+            // row (each unit cut about 10 times): 246 us against 564 with the
+            // element form below
             constexpr int V = (DD % 4 == 0) ? 4 : 1;
             for (int g = tid; g < G; g += nthr) {
                 float M = -INFINITY;
@@ -938,6 +941,32 @@ __device__ inline void unit_ticket_merge(const DecodeParams &p, const TileCursor
                             o[e] = fmaf(acc[e], mb.inv_den[g], c0 == 0 ? 0.f : o[e]);
                     }
                 }
+            }
+        } else {
+            // element by element, every partial's (m, l) read again per
+            // element: few registers. Single-token units (at most 8 rows, and
+            // only past 32 pieces), and the E4M3 kernels at their register cap
+            // (their four-warp merge in this form: long_context 4 tokens a row
+            // 300 us against 238 chunked, but the chunked form's spills cost
+            // their common steps 3-5 %)
+            for (int idx = tid; idx < G * DD; idx += nthr) {
+                const int g = idx / DD, d = idx % DD;
+                float M = -INFINITY;
+                for (int i = 0; i < K; ++i)
+                    M = fmaxf(M, __ldcg(p.ws_ml + ((P0 + i) * G + g) * 2));
+                const float sk = p.sink ? sink_log2(p, kvh * p.Gh + g % p.Gh) : -INFINITY;
+                M = fmaxf(M, sk);
+                float num = 0.f, den = (sk == -INFINITY) ? 0.f : fast_ex2(sk - M);
+                for (int i = 0; i < K; ++i) {
+                    const long long Q = P0 + i;
+                    const float a = fast_ex2(__ldcg(p.ws_ml + (Q * G + g) * 2) - M);
+                    float *po = p.ws_o + (Q * G + g) * DD + d;
+                    num = fmaf(a, __ldcg(po), num);
+                    den = fmaf(a, __ldcg(p.ws_ml + (Q * G + g) * 2 + 1), den);
+                    *po = 0.f;       // consumed: leave the workspace zero-filled
+                }
+                if (g < nrow)
+                    out_row<MULTI>(p, cur, g, DD)[d] = num / den;
             }
         }
         sync();

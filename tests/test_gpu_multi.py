@@ -199,8 +199,9 @@ def test_multi_with_window_and_sink(kernel, q_lens):
 # One or two long rows over many CTAs: each unit is cut into more pieces than
 # one pass of the merge's shared-memory weights takes (8 partials for 32-row
 # units, 16 for 16-row units, 32 for 8-row units), so the merge goes through
-# them in chunks (in the CTA's own last segment end, and in the finisher
-# warp's when a CTA ends a cut unit in the middle of its walk).
+# them in chunks (bfloat16 cache: in the CTA's own last segment end, and in
+# the finisher warp's when a CTA ends a cut unit in the middle of its walk)
+# or element by element (E4M3 cache, CUDA-core kernel).
 MANY_PIECES = [
     ("rows32_g8", "long_context", dict(B=1, Hq=8, Hkv=1, Smax=2400, len_lo=2300, len_hi=2390, seed=431), [4]),
     ("rows16_g4", "llama3_8b", dict(B=2, Hq=4, Hkv=1, Smax=2400, len_lo=2200, len_hi=2390, seed=432), [4, 3]),
@@ -210,7 +211,7 @@ MANY_PIECES = [
 
 @pytest.mark.parametrize("sink", [False, True], ids=["plain", "sink"])
 @pytest.mark.parametrize("grid", [0, 40])
-@pytest.mark.parametrize("kernel", ["tc", "tc5"])
+@pytest.mark.parametrize("kernel", ["tc", "tc_e4m3", "tc5", "simt"])
 @pytest.mark.parametrize("name,base,kw,q_lens", MANY_PIECES, ids=[c[0] for c in MANY_PIECES])
 def test_multi_unit_cut_into_many_pieces(name, base, kw, q_lens, kernel, grid, sink):
     import gqa_kv_cache_gb300 as gqa
@@ -221,7 +222,7 @@ def test_multi_unit_cut_into_many_pieces(name, base, kw, q_lens, kernel, grid, s
     if sink:
         g = torch.Generator().manual_seed(5)
         mods["sink"] = torch.randn(w.Hq, generator=g).cuda()
-    check_multi(w, q_lens, kernel, grid, **mods)
+    check_multi(w, q_lens, "tc" if kernel == "tc_e4m3" else kernel, grid, fp8=kernel == "tc_e4m3", **mods)
     ws = gqa._ws_cache.get(torch.device("cuda", torch.cuda.current_device()))
     if ws is not None:
         assert int(torch.count_nonzero(ws).item()) == 0
