@@ -369,9 +369,13 @@ gqa_status run_step(const Shape &s, const void *q, const void *k_new, const void
             const int box = s.block_size < T ? s.block_size : T;
             ok = encode_cache_map(&maps.k, kc, s.D, s.block_size, (long long)s.num_blocks * s.Hkv, box, es) &&
                  encode_cache_map(&maps.v, vc, s.D, s.block_size, (long long)s.num_blocks * s.Hkv, box, es);
+            maps.k16 = maps.k;   // not used with a paged cache
+            maps.v16 = maps.v;
         } else {
             ok = encode_cache_map(&maps.k, kc, s.D, s.Smax, (long long)s.R * s.Hkv, T, es) &&
-                 encode_cache_map(&maps.v, vc, s.D, s.Smax, (long long)s.R * s.Hkv, T, es);
+                 encode_cache_map(&maps.v, vc, s.D, s.Smax, (long long)s.R * s.Hkv, T, es) &&
+                 encode_cache_map(&maps.k16, kc, s.D, s.Smax, (long long)s.R * s.Hkv, kDenseBoxRows, es) &&
+                 encode_cache_map(&maps.v16, vc, s.D, s.Smax, (long long)s.R * s.Hkv, kDenseBoxRows, es);
         }
         if (!ok)
             return GQA_ERR_CUDA;

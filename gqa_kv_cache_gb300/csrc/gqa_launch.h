@@ -16,8 +16,14 @@ cudaError_t simt_launch(const DecodeParams &p, bool bf16, cudaStream_t st);
 
 // TMA-ring + tensor-core decode kernel (gqa_tc.cu).
 struct TcMaps {
-    CUtensorMap k, v;  // tiled maps over the key / value cache, 128-byte swizzle
+    CUtensorMap k, v;      // tiled maps over the key / value cache, 128-byte swizzle
+    CUtensorMap k16, v16;  // dense caches: the same with a box of kDenseBoxRows slots
 };
+// A dense cache's tile is one 64-slot box when every part of it is read; a
+// tile that is only partly read (a unit's last tile, a window's first) is
+// copied in boxes of kDenseBoxRows slots, those that hold a slot the step
+// reads. A paged cache's box is its block (at most the tile).
+constexpr int kDenseBoxRows = 16;
 bool tc_supports(bool bf16, int D, int G, bool paged, int block_size);  // bf16: the cache
 int tc_tile();
 int tc_ctas_per_sm(bool kv8, int unit_rows);   // resident CTAs per SM of the instantiation

@@ -193,7 +193,8 @@ __device__ __forceinline__ bool t5_softmax_or(bool v)
 
 template <bool WIN>
 __global__ void __launch_bounds__(kT5Threads, 2)
-    tc5_multi_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv)
+    tc5_multi_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
+                     const __grid_constant__ CUtensorMap mk16, const __grid_constant__ CUtensorMap mv16)
 {
     extern __shared__ uint8_t dyn_smem[];
     __shared__ T5Shared sh;
@@ -229,6 +230,10 @@ __global__ void __launch_bounds__(kT5Threads, 2)
     if (warp == 3 && lane == 0) {
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mk)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mv)) : "memory");
+        if (!p.paged) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mk16)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mv16)) : "memory");
+        }
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
     schedule_walk(p, sh.sched, &sh.walk, 2);   // contains __syncthreads (publishes the TMEM address too)
@@ -254,18 +259,27 @@ __global__ void __launch_bounds__(kT5Threads, 2)
         struct Plan {
             int z, y;
             bool bad_entry, good;
+            int rows;   // the tile's box height (warp-uniform)
         };
         auto plan = [&](const TileCursor &c) {
-            Plan r{-1, 0, false, row_ok(p, c.b, c.L)};
+            Plan r{-1, 0, false, row_ok(p, c.b, c.L), box_rows};
             if (!r.good)
                 return r;
             const int slot0 = WIN ? tile_slot0(c, kTile) : c.t * kTile;
             const int rb = real_row(p, c.b);
             if (!p.paged) {
-                if (lane == 0) {
+                // a dense cache: one box for a tile read whole, else a small
+                // box per part that holds a slot the step reads
+                const int s = slot0 + lane * kDenseBoxRows;
+                const bool need = lane < kTile / kDenseBoxRows && s <= c.L &&
+                                  (!WIN || s + kDenseBoxRows - 1 >= c.lo || s < c.P);
+                const unsigned parts = __ballot_sync(0xffffffffu, need);
+                const bool whole = parts == (1u << (kTile / kDenseBoxRows)) - 1u;
+                r.rows = whole ? kTile : kDenseBoxRows;
+                if (whole ? lane == 0 : need) {
                     const int row = p.slot_ids ? __ldg(p.slot_ids + rb) : rb;
                     r.z = row * p.Hkv + c.kvh;
-                    r.y = slot0;
+                    r.y = s;
                 }
             } else if (lane < nblk) {
                 const int s = slot0 + lane * box_rows;
@@ -298,7 +312,7 @@ __global__ void __launch_bounds__(kT5Threads, 2)
             const bool any_bad = __any_sync(0xffffffffu, pl.bad_entry);
             const bool seg_first = pl.good && (cur.t == 0 || cur.g == range_start);
             const uint32_t qbytes = seg_first ? (uint32_t)(p.Gh * cur.nq * kD * 2) : 0u;
-            const uint32_t bytes = (uint32_t)__popc(copying) * 4u * (uint32_t)box_rows * 128u + qbytes;
+            const uint32_t bytes = (uint32_t)__popc(copying) * 4u * (uint32_t)pl.rows * 128u + qbytes;
             const uint32_t fb = smem_u32(&sh.full[stage]);
             if (lane == 0) {
                 sh.stage_bad[stage] = any_bad ? 1 : 0;
@@ -317,11 +331,19 @@ __global__ void __launch_bounds__(kT5Threads, 2)
             }
             __syncwarp();
             if (pl.z >= 0) {
-                const uint32_t dst = ring_u32 + stage * kT5StageBytes + lane * box_rows * 128;
-                tma_load_3d(dst, &mk, 0, pl.y, pl.z, fb, policy);
-                tma_load_3d(dst + kHalfBytes, &mk, 64, pl.y, pl.z, fb, policy);
-                tma_load_3d(dst + 2 * kHalfBytes, &mv, 0, pl.y, pl.z, fb, policy);
-                tma_load_3d(dst + 3 * kHalfBytes, &mv, 64, pl.y, pl.z, fb, policy);
+                if (pl.rows == box_rows) {   // a whole box (a paged block, a dense tile)
+                    const uint32_t dst = ring_u32 + stage * kT5StageBytes + lane * box_rows * 128;
+                    tma_load_3d(dst, &mk, 0, pl.y, pl.z, fb, policy);
+                    tma_load_3d(dst + kHalfBytes, &mk, 64, pl.y, pl.z, fb, policy);
+                    tma_load_3d(dst + 2 * kHalfBytes, &mv, 0, pl.y, pl.z, fb, policy);
+                    tma_load_3d(dst + 3 * kHalfBytes, &mv, 64, pl.y, pl.z, fb, policy);
+                } else {   // a part of a dense tile (the small-box maps)
+                    const uint32_t dst = ring_u32 + stage * kT5StageBytes + lane * kDenseBoxRows * 128;
+                    tma_load_3d(dst, &mk16, 0, pl.y, pl.z, fb, policy);
+                    tma_load_3d(dst + kHalfBytes, &mk16, 64, pl.y, pl.z, fb, policy);
+                    tma_load_3d(dst + 2 * kHalfBytes, &mv16, 0, pl.y, pl.z, fb, policy);
+                    tma_load_3d(dst + 3 * kHalfBytes, &mv16, 64, pl.y, pl.z, fb, policy);
+                }
             }
             ++issued;
             const bool was_b = in_b;
@@ -814,7 +836,7 @@ cudaError_t launch_t5(const DecodeParams &p, const TcMaps &maps, cudaStream_t st
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tc5_multi_kernel<WIN>, p, maps.k, maps.v);
+    return cudaLaunchKernelEx(&cfg, tc5_multi_kernel<WIN>, p, maps.k, maps.v, maps.k16, maps.v16);
 }
 
 }  // namespace

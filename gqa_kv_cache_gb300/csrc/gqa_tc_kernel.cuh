@@ -557,7 +557,8 @@ __device__ __forceinline__ void pair_sync(int pr)
 template <bool QF32, bool WIN, bool MULTI, bool KV8, int MR>
 __global__ void __launch_bounds__((Ring<QF32, KV8, MULTI, MR>::kThreads), (Ring<QF32, KV8, MULTI, MR>::kCtas))
     tc_decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap mk,
-                     const __grid_constant__ CUtensorMap mv)
+                     const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mk16,
+                     const __grid_constant__ CUtensorMap mv16)
 {
     using RG = Ring<QF32, KV8, MULTI, MR>;
     static_assert(!(MULTI && QF32), "multi-token steps take a bfloat16 query");
@@ -590,6 +591,10 @@ __global__ void __launch_bounds__((Ring<QF32, KV8, MULTI, MR>::kThreads), (Ring<
     if (warp == kConsumerWarps && lane == 0) {
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mk)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mv)) : "memory");
+        if (!KV8 && !p.paged) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mk16)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mv16)) : "memory");
+        }
     }
     // Launched as a programmatic dependent of the previous kernel on the
     // stream: everything above overlaps its tail; no input is read before it
@@ -616,24 +621,46 @@ __global__ void __launch_bounds__((Ring<QF32, KV8, MULTI, MR>::kThreads), (Ring<
         const int nblk = p.paged ? (bs < kTile ? kTile / bs : 1) : 1;  // copies per half per tile
         const int box_rows = p.paged ? (bs < kTile ? bs : kTile) : kTile;
         // Where this lane copies tile `c` from: z (cache head row of the
-        // tensor map) and y (first slot in it); z < 0: nothing. Computed one
-        // tile ahead, before the wait for a free stage, so the table reads
-        // overlap the wait.
+        // tensor map) and y (first slot in it); z < 0: nothing; `rows`: the
+        // tile's box height (warp-uniform). Computed one tile ahead, before
+        // the wait for a free stage, so the table reads overlap the wait.
         struct Plan {
             int z, y;
             bool bad_entry, good;
+            int rows;
         };
         auto plan = [&](const TileCursor &c) {
-            Plan r{-1, 0, false, row_ok(p, c.b, c.L)};
+            Plan r{-1, 0, false, row_ok(p, c.b, c.L), box_rows};
             if (!r.good)
                 return r;
             const int slot0 = WIN ? tile_slot0(c, kTile) : c.t * kTile;
             const int rb = MULTI ? real_row(p, c.b) : c.b;   // the batch row
-            if (!p.paged) {
+            if (KV8 && !p.paged) {
+                // an E4M3 dense cache: the whole tile (half the bytes of a
+                // bf16 one; small boxes for partly read tiles measured slower
+                // here: llama3_8b 44.5 against 43.4 us)
                 if (lane == 0) {
                     const int row = p.slot_ids ? __ldg(p.slot_ids + rb) : rb;
                     r.z = row * p.Hkv + c.kvh;
                     r.y = slot0;
+                }
+            } else if (!p.paged) {
+                // a dense cache: one box when every part of the tile holds a
+                // slot the step reads, else a small box per part that does (a
+                // unit's last tile, a window's first; the consumers mask and
+                // zero the rest as in any such tile). ragged_slots 118.3 ->
+                // 117.0 us, llama3_8b 63.7 -> 63.0 us; a small box for every
+                // part of every tile was slower (ragged_slots 120.9 us)
+                const int s = slot0 + lane * kDenseBoxRows;
+                const bool need = lane < kTile / kDenseBoxRows && s <= c.L &&
+                                  (!WIN || s + kDenseBoxRows - 1 >= c.lo || s < c.P);
+                const unsigned parts = __ballot_sync(0xffffffffu, need);
+                const bool whole = parts == (1u << (kTile / kDenseBoxRows)) - 1u;
+                r.rows = whole ? kTile : kDenseBoxRows;
+                if (whole ? lane == 0 : need) {
+                    const int row = p.slot_ids ? __ldg(p.slot_ids + rb) : rb;
+                    r.z = row * p.Hkv + c.kvh;
+                    r.y = s;
                 }
             } else if (lane < nblk) {
                 const int s = slot0 + lane * box_rows;  // first slot this lane copies
@@ -678,8 +705,8 @@ __global__ void __launch_bounds__((Ring<QF32, KV8, MULTI, MR>::kThreads), (Ring<
             // rows, so the consumers quantise and append them from shared memory
             const bool newt = RG::kNewBytes > 0 && !p.attend && pl.good && cur.t == cur.nr - 1;
             const uint32_t nbytes = newt ? 2u * kD * 2u : 0u;
-            const uint32_t bytes =
-                (uint32_t)__popc(copying) * (KV8 ? 2u : 4u) * (uint32_t)box_rows * 128u + qbytes + nbytes;
+            const uint32_t bytes = (uint32_t)__popc(copying) * (KV8 ? 2u : 4u) *
+                                       (uint32_t)(KV8 ? box_rows : pl.rows) * 128u + qbytes + nbytes;
             const uint32_t fb = smem_u32(&sh.full[stage]);
             if (lane == 0) {
                 sh.stage_bad[stage] = any_bad ? 1 : 0;
@@ -714,15 +741,22 @@ __global__ void __launch_bounds__((Ring<QF32, KV8, MULTI, MR>::kThreads), (Ring<
             }
             __syncwarp();
             if (pl.z >= 0) {
-                const uint32_t dst = ring_u32 + stage * kStageBytes + lane * box_rows * 128;
                 if constexpr (KV8) {   // rows of 128 one-byte elements: one box each
+                    const uint32_t dst = ring_u32 + stage * kStageBytes + lane * box_rows * 128;
                     tma_load_3d(dst, &mk, 0, pl.y, pl.z, fb, policy);
                     tma_load_3d(dst + kKVB, &mv, 0, pl.y, pl.z, fb, policy);
-                } else {
+                } else if (pl.rows == box_rows) {   // a whole box (a paged block, a dense tile)
+                    const uint32_t dst = ring_u32 + stage * kStageBytes + lane * box_rows * 128;
                     tma_load_3d(dst, &mk, 0, pl.y, pl.z, fb, policy);
                     tma_load_3d(dst + kHalfBytes, &mk, 64, pl.y, pl.z, fb, policy);
                     tma_load_3d(dst + 2 * kHalfBytes, &mv, 0, pl.y, pl.z, fb, policy);
                     tma_load_3d(dst + 3 * kHalfBytes, &mv, 64, pl.y, pl.z, fb, policy);
+                } else {   // a part of a dense tile (the small-box maps)
+                    const uint32_t dst = ring_u32 + stage * kStageBytes + lane * kDenseBoxRows * 128;
+                    tma_load_3d(dst, &mk16, 0, pl.y, pl.z, fb, policy);
+                    tma_load_3d(dst + kHalfBytes, &mk16, 64, pl.y, pl.z, fb, policy);
+                    tma_load_3d(dst + 2 * kHalfBytes, &mv16, 0, pl.y, pl.z, fb, policy);
+                    tma_load_3d(dst + 3 * kHalfBytes, &mv16, 64, pl.y, pl.z, fb, policy);
                 }
             }
             ++issued;
@@ -1657,7 +1691,8 @@ cudaError_t launch_q(const DecodeParams &p, const TcMaps &maps, cudaStream_t st)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tc_decode_kernel<QF32, WIN, MULTI, KV8, MR>, p, maps.k, maps.v);
+    return cudaLaunchKernelEx(&cfg, tc_decode_kernel<QF32, WIN, MULTI, KV8, MR>, p, maps.k, maps.v, maps.k16,
+                              maps.v16);
 }
 
 }  // namespace

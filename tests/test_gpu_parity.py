@@ -128,6 +128,45 @@ def test_stale_slots_nan(kernel):
         assert torch.equal(out, ref)
 
 
+@pytest.mark.parametrize("slots", [False, True], ids=["rows", "slot_ids"])
+@pytest.mark.parametrize("window", [0, 40], ids=["full", "window40"])
+@pytest.mark.parametrize("grid_ctas", [0, 7])
+def test_stale_slots_nan_in_partly_copied_tiles(grid_ctas, window, slots):
+    """A dense cache's partly read tiles (a unit's last, a window's first) are
+    copied in 16-slot parts; the parts not copied keep whatever the ring
+    stage held before. With few CTAs each walking many short units, those
+    are often NaN / Inf rows of an earlier unit's stale slots: not a single
+    output bit may change against the clean cache."""
+    import gqa_kv_cache_gb300 as gqa
+    base = "ragged_slots" if slots else "llama3_8b"
+    kw = dict(R=40) if slots else {}
+    w = W.small(base, B=24, Hq=8, Hkv=2, Smax=256, len_lo=1, len_hi=250, seed=131 + window + slots, **kw)
+    t = make_inputs(w)
+    mods = dict(window=window, kept_prefix=5) if window else {}
+
+    def run(tt):
+        return gqa.decode_step(tt["q"], tt["k_new"], tt["v_new"], tt["k_cache"], tt["v_cache"], tt["lengths"],
+                               tt.get("slot_ids"), kernel="tc", grid_ctas=grid_ctas, **mods)
+
+    ref = run({k: v.clone() for k, v in t.items()}).clone()
+    L = t["lengths"].long()
+    rows = t["slot_ids"].long() if slots else torch.arange(w.B, device="cuda")
+    j = torch.arange(w.Smax, device="cuda")
+    for fill in (float("nan"), float("inf")):
+        t2 = {k: v.clone() for k, v in t.items()}
+        stale = torch.ones(t["k_cache"].shape[0], w.Smax, dtype=torch.bool, device="cuda")
+        stale[rows] = j[None, :] >= L[:, None]
+        if window:   # slots outside every query's window and the kept prefix are not read either
+            lo = (L - window + 1).clamp(min=0)
+            stale[rows] |= (j[None, :] < lo[:, None]) & (j[None, :] >= 5)
+        stale = stale[:, None, :, None]
+        t2["k_cache"] = torch.where(stale, torch.full_like(t["k_cache"], fill), t["k_cache"])
+        t2["v_cache"] = torch.where(stale, torch.full_like(t["v_cache"], -fill), t["v_cache"])
+        out = run(t2)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref), (fill, grid_ctas, window, slots)
+
+
 @pytest.mark.parametrize("kernel", ["simt", "tc", "unit"])
 def test_paged_unused_blocks_nan(kernel):
     """Blocks the table does not name, and the unused tail of the last block,
